@@ -1,0 +1,80 @@
+"""The pins are strong enough: each plausible mistake, planted in a temporary copy
+of the oracle's C source (on the CPU, never on the GPU), makes at least one pin
+fail.  The real oracle source is never modified."""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text in oracle.c, replacement, which occurrence: index or "all")
+MUTANTS = [
+    ("sigma_convention_2sigma2",
+     "return exp(-sq_dist(xi, yj, D) / (sigma * sigma));",
+     "return exp(-sq_dist(xi, yj, D) / (2.0 * sigma * sigma));", 0),
+    ("exponent_sign",
+     "return exp(-sq_dist(xi, yj, D) / (sigma * sigma));",
+     "return exp(sq_dist(xi, yj, D) / (sigma * sigma));", 0),
+    ("abs_instead_of_square", "s += diff * diff;", "s += fabs(diff);", 0),
+    ("dropped_last_coordinate",
+     "for (int d = 0; d < D; ++d) {\n        double diff = xi[d] - yj[d];",
+     "for (int d = 0; d < D - 1; ++d) {\n        double diff = xi[d] - yj[d];", 0),
+    ("sum_drops_signal", "double term = k * b[j * E + e];", "double term = k;", 0),
+    ("sum_ignores_column", "double term = k * b[j * E + e];", "double term = k * b[j * E];", 0),
+    ("sum_drops_last_point",
+     "for (int64_t j = 0; j < N; ++j) {\n                double k = gauss(x + i * D, y + j * D, D, sigma);\n                double term",
+     "for (int64_t j = 0; j < N - 1; ++j) {\n                double k = gauss(x + i * D, y + j * D, D, sigma);\n                double term", 0),
+    ("compensation_sign", "*comp += (*sum - t) + v;", "*comp += (*sum - t) - v;", 0),
+    ("lse_weight_sign_second_pass",
+     "/ (sigma * sigma) + w[j * E + e];", "/ (sigma * sigma) - w[j * E + e];", 1),
+    ("lse_drops_max", "L[i * E + e] = m + log(s + c);", "L[i * E + e] = log(s + c);", 0),
+    ("lse_sigma_not_squared",
+     "-sq_dist(x + i * D, y + j * D, D) / (sigma * sigma) + w",
+     "-sq_dist(x + i * D, y + j * D, D) / (sigma) + w", "all"),
+    ("grad_factor", "-(2.0 / (sigma * sigma)) * k", "-(1.0 / (sigma * sigma)) * k", 0),
+    ("grad_direction", "double diff = x[i * D + d] - y[j * D + d];",
+     "double diff = y[j * D + d] - x[i * D + d];", 0),
+    ("grad_drops_signal", "beta += g[i * E + e] * b[j * E + e];", "beta += g[i * E + e];", 0),
+    ("grad_wrong_row_of_g", "beta += g[i * E + e] * b[j * E + e];", "beta += g[e] * b[j * E + e];", 0),
+    ("knn_tie_highest_index", "(d1 == d2 && j1 < j2)", "(d1 == d2 && j1 > j2)", 0),
+    ("knn_largest_first", "return d1 < d2 ||", "return d1 > d2 ||", 0),
+    ("knn_next_is_kth", "next[i] = (K < n) ? bd[K] : INFINITY;",
+     "next[i] = (K < n) ? bd[K - 1] : INFINITY;", 0),
+    ("knn_fill_zero", "idx[i * K + k] = (k < n) ? bj[k] : -1;",
+     "idx[i * K + k] = (k < n) ? bj[k] : 0;", 0),
+]
+
+
+def _mutate(src, old, new, which):
+    n = src.count(old)
+    assert n >= 1, f"mutation anchor not found in oracle.c: {old!r}"
+    if which == "all":
+        return src.replace(old, new)
+    assert which < n, f"anchor {old!r} occurs {n} times"
+    pos = -1
+    for _ in range(which + 1):
+        pos = src.index(old, pos + 1)
+    return src[:pos] + new + src[pos + len(old):]
+
+
+@pytest.mark.parametrize("name,old,new,which", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new, which):
+    with open(SRC) as f:
+        src = f.read()
+    mutated = _mutate(src, old, new, which)
+    assert mutated != src
+    c = tmp_path / f"{name}.c"
+    c.write_text(mutated)
+    so = oracle.build(str(c), str(tmp_path / f"lib{name}.so"))
+    orc = oracle.Oracle(so)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            caught.append(pin.__name__)
+            break
+    assert caught, f"mutant {name} passes every pin"
