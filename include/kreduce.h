@@ -1,0 +1,169 @@
+/*
+ * kreduce.h -- C ABI of the symbolic kernel-reduction library for one sm_103a GPU.
+ *
+ * The library reduces an M x N matrix whose entries are a formula of two point
+ * clouds, x_i in R^D (i < M) and y_j in R^D (j < N), without ever storing the
+ * matrix: the entries are evaluated in registers, tile by tile, and reduced over j.
+ *
+ *   Sum       a_ie = sum_j exp(-|x_i - y_j|^2 / sigma^2) b_je
+ *   LogSumExp L_ie = log sum_j exp(-|x_i - y_j|^2 / sigma^2 + w_je)
+ *   grad-x    gx_id = d/dx_id sum_{i,e} g_ie a_ie
+ *                   = -(2/sigma^2) sum_j k_ij (sum_e g_ie b_je)(x_id - y_jd)
+ *   K-min     the K pairs (|x_i - y_j|^2, j) that are smallest in lexicographic
+ *             order, sorted ascending; K = 1 is ArgMin.
+ *
+ * Sources: "Kernel Operations on the GPU, with Autodiff, without Memory Overflows",
+ * §1 Introduction (target operation: a_i = sum_j k(x_i, y_j) b_j with a Gaussian
+ * k of width sigma) and §2 (generic reductions: sum, logsumexp, argmin, argKmin;
+ * autodiff); KeOps README, PyTorch usage example (squared distances, exp(-D),
+ * .sum / .logsumexp / .argmin, gradient of sum_i a_i^2 wrt x) and feature list
+ * (Sum, LogSumExp, ArgMin, K-min); GitHub issue "Transparent interface for
+ * billion-scale matrices" (caller-allocated output, calls that do not hold the
+ * caller's interpreter lock).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.   All arrays are float32 (int32 for indices), row-major, contiguous:
+ *           x: M x D, y: N x D, b and w: N x E, g: M x E, out: M x E,
+ *           gx: M x D, idx and dist: M x K.  Each pointer may address device
+ *           memory or host memory (pageable or pinned); host arrays are staged
+ *           through device memory allocated for the call, and the call then
+ *           blocks until its host outputs are written.  With device pointers
+ *           only, the call is asynchronous on `stream`.
+ * Ownership. The caller owns every array, outputs included; the library never
+ *           frees or keeps caller memory.  Workspace (split-j partials, staging)
+ *           is taken stream-ordered (cudaMallocAsync / cudaFreeAsync on
+ *           `stream`) and released before the work it serves is complete.
+ * Aliasing. Outputs must not overlap inputs or each other.
+ * Stream.   `stream` is a cudaStream_t (NULL = the legacy default stream).  The
+ *           device is the current device of the calling thread.
+ * Errors.   Arguments are validated before any CUDA call; an invalid call
+ *           returns a status and launches nothing.  The return value reports
+ *           validation, allocation and launch errors; with device pointers,
+ *           errors during execution surface at the caller's next synchronisation.
+ * Threads.  Calls from several host threads on different streams are safe; the
+ *           library's only global state is per-device cached attributes.
+ * Limits.   1 <= D <= 128, 1 <= E <= 16, 1 <= K <= 32; M, N >= 0; M*D, N*D,
+ *           M*E, N*E and M*K below 2^31 elements.  sigma finite and > 0.
+ *           M = 0 is a no-op; N = 0 gives Sum 0, LogSumExp -inf, grad 0,
+ *           K-min indices -1 and distances +inf.
+ * Numerics. fp32 inputs and outputs; exp is computed as ex2.approx on arguments
+ *           prescaled by sqrt(log2 e)/sigma; sums over j use per-tile partials
+ *           with a compensated running sum; split-j partials are combined in a
+ *           fixed order, so results are deterministic run to run.
+ */
+#ifndef KREDUCE_H
+#define KREDUCE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA header. */
+typedef struct CUstream_st *kr_stream_t;
+
+typedef enum {
+    KR_SUM = 0, /* a_ie = sum_j k_ij b_je */
+    KR_LSE = 1  /* L_ie = log sum_j exp(-|x_i - y_j|^2/sigma^2 + w_je); b holds w */
+} kr_reduction;
+
+typedef enum {
+    KR_OK = 0,
+    KR_ERR_INVALID = 1,     /* null pointer with a nonzero size, negative size, bad sigma,
+                               unknown reduction, overlapping outputs */
+    KR_ERR_UNSUPPORTED = 2, /* valid request outside the limits above */
+    KR_ERR_ALLOC = 3,       /* workspace or staging allocation failed; outputs untouched */
+    KR_ERR_CUDA = 4         /* a CUDA runtime call failed; see kr_last_cuda_error() */
+} kr_status;
+
+/* Optional knobs; pass NULL for the defaults. */
+typedef struct {
+    int split;       /* S >= 1 forces S disjoint j-ranges (split-j); 0 = automatic */
+    int reserved[7]; /* must be zero */
+} kr_options;
+
+/*
+ * Sum or LogSumExp of the Gaussian kernel over j ("Kernel Operations on the GPU...",
+ * §1 target operation; KeOps README .sum(dim=1) and .logsumexp()).
+ *   x [M x D], y [N x D]: point clouds.
+ *   b [N x E]: the signal b_je for KR_SUM, the additive log-weight w_je for KR_LSE
+ *              (pass log b for positive weights; -inf is allowed and means weight 0).
+ *   out [M x E]: written with a (KR_SUM) or L (KR_LSE).
+ *   sigma: kernel width, k = exp(-|x - y|^2 / sigma^2).
+ * Returns a kr_status.
+ */
+int kernel_reduce(const float *x, const float *y, const float *b, float *out,
+                  int64_t M, int64_t N, int D, int E, float sigma, int reduction,
+                  kr_stream_t stream);
+int kernel_reduce_ex(const float *x, const float *y, const float *b, float *out,
+                     int64_t M, int64_t N, int D, int E, float sigma, int reduction,
+                     kr_stream_t stream, const kr_options *opt);
+
+/*
+ * Gradient wrt x of sum_{i,e} g_ie a_ie, a the Sum reduction (KeOps README usage
+ * example: torch.autograd.grad((a_i ** 2).sum(), [x]), i.e. g = 2a).
+ *   x [M x D], y [N x D], b [N x E], g [M x E] (upstream gradient), gx [M x D] output.
+ */
+int kernel_reduce_grad_x(const float *x, const float *y, const float *b, const float *g,
+                         float *gx, int64_t M, int64_t N, int D, int E, float sigma,
+                         kr_stream_t stream);
+int kernel_reduce_grad_x_ex(const float *x, const float *y, const float *b, const float *g,
+                            float *gx, int64_t M, int64_t N, int D, int E, float sigma,
+                            kr_stream_t stream, const kr_options *opt);
+
+/*
+ * K-min / ArgMin over squared Euclidean distance (KeOps README feature list:
+ * ArgMin and K-min reductions; "Kernel Operations on the GPU...", §2 argKmin).
+ *   idx [M x K] (int32): the K indices j with the smallest (|x_i - y_j|^2, j),
+ *                        ascending; ties keep the lowest j; -1 past N.
+ *   dist [M x K] (nullable): the matching fp32 squared distances, +inf past N.
+ */
+int kernel_knn(const float *x, const float *y, int32_t *idx, float *dist,
+               int64_t M, int64_t N, int D, int K, kr_stream_t stream);
+int kernel_knn_ex(const float *x, const float *y, int32_t *idx, float *dist,
+                  int64_t M, int64_t N, int D, int K, kr_stream_t stream,
+                  const kr_options *opt);
+
+/* Static text for a kr_status value. */
+const char *kr_status_string(int status);
+
+/* The cudaError_t of the last KR_ERR_CUDA returned on the calling thread (0 if none). */
+int kr_last_cuda_error(void);
+
+/*
+ * Launch plan, exposed so that the host logic can be inspected without a GPU.
+ * op: 0 = Sum, 1 = LogSumExp, 2 = grad-x, 3 = K-min; EK = E (ops 0-2) or K (op 3).
+ * num_sms and blocks_per_sm describe the device (blocks_per_sm <= 0: use the
+ * plan's own estimate).  Fills *plan and returns a kr_status; no CUDA call.
+ */
+typedef struct {
+    int d_pad;         /* compile-time coordinate count of the kernel instance (>= D) */
+    int ek_pad;        /* compile-time E (or K) of the instance (>= E or K) */
+    int rows_per_thread;
+    int threads;       /* per block */
+    int tile_points;   /* points of y per shared-memory tile */
+    int64_t row_blocks;
+    int split;         /* S */
+    int64_t chunk;     /* columns per split; the last split may be shorter */
+    int64_t workspace_bytes;
+} kr_plan_t;
+
+int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm,
+            const kr_options *opt, kr_plan_t *plan);
+
+/*
+ * The plan a call with these arguments makes on the calling thread's current device:
+ * kr_plan with that device's SM count and the kernel instance's resident blocks per
+ * SM.  Queries device attributes; launches nothing and allocates nothing.  Useful to
+ * size workspace in advance and to count launches (1 + (split > 1) per call).
+ */
+int kr_plan_device(int op, int64_t M, int64_t N, int D, int EK, const kr_options *opt,
+                   kr_plan_t *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KREDUCE_H */

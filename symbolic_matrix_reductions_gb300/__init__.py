@@ -1,0 +1,283 @@
+"""kreduce for one GB300: reductions over symbolic Gaussian / squared-distance matrices.
+
+The compute lives in ``libkreduce.so`` (CUDA for sm_103a, built from ``csrc/`` by
+``build.py``); this package only marshals arguments to its C ABI through
+``ctypes`` (which releases the interpreter lock around each call, so several
+Python threads can run reductions at once).  There is no CPU fallback: if the
+library is missing, every call raises.
+
+Functions, named after the C entry points (see ``include/kreduce.h``):
+
+* ``kernel_reduce(x, y, b, sigma, reduction="sum"|"lse", out=None, split=0)``
+* ``kernel_reduce_grad_x(x, y, b, g, sigma, out=None, split=0)``
+* ``kernel_knn(x, y, K, idx=None, dist=None, split=0)``
+
+Arguments are float32 torch tensors, contiguous, row-major: x (M, D), y (N, D),
+b (N, E) or (N,), g (M, E) or (M,).  CUDA tensors run asynchronously on the
+current stream; CPU tensors are staged through device memory by the library and
+the call blocks until the result is back.  ``GaussianSum`` wraps the Sum with its
+x-gradient as a ``torch.autograd.Function``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import workloads  # noqa: F401  (seeded inputs; no compute)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkreduce.so")
+
+KR_SUM, KR_LSE = 0, 1
+KR_OK, KR_ERR_INVALID, KR_ERR_UNSUPPORTED, KR_ERR_ALLOC, KR_ERR_CUDA = 0, 1, 2, 3, 4
+OP_SUM, OP_LSE, OP_GRAD, OP_KNN = 0, 1, 2, 3
+
+# Names exported by libkreduce.so, in the order include/kreduce.h declares them.
+EXPORTS = ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_grad_x", "kernel_reduce_grad_x_ex",
+           "kernel_knn", "kernel_knn_ex", "kr_status_string", "kr_last_cuda_error", "kr_plan",
+           "kr_plan_device")
+
+
+class KrError(RuntimeError):
+    """A kreduce call returned a status other than KR_OK."""
+
+    def __init__(self, status: int, what: str, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        msg = f"{what}: {_status_text(status)} (status {status})"
+        if status == KR_ERR_CUDA:
+            msg += f", cudaError {cuda_error}"
+        super().__init__(msg)
+
+
+class KrOptions(ctypes.Structure):
+    _fields_ = [("split", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+
+
+class KrPlan(ctypes.Structure):
+    _fields_ = [("d_pad", ctypes.c_int), ("ek_pad", ctypes.c_int), ("rows_per_thread", ctypes.c_int),
+                ("threads", ctypes.c_int), ("tile_points", ctypes.c_int), ("row_blocks", ctypes.c_int64),
+                ("split", ctypes.c_int), ("chunk", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libkreduce.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libkreduce.so not found at {path}; build it with "
+                "`python -m symbolic_matrix_reductions_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        opt = ctypes.POINTER(KrOptions)
+        lib.kernel_reduce.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
+        lib.kernel_reduce_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp, opt]
+        lib.kernel_reduce_grad_x.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
+        lib.kernel_reduce_grad_x_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
+        lib.kernel_knn.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp]
+        lib.kernel_knn_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp, opt]
+        lib.kr_status_string.argtypes = [i32]
+        lib.kr_status_string.restype = ctypes.c_char_p
+        lib.kr_last_cuda_error.argtypes = []
+        lib.kr_plan.argtypes = [i32, i64, i64, i32, i32, i32, i32, opt, ctypes.POINTER(KrPlan)]
+        lib.kr_plan_device.argtypes = [i32, i64, i64, i32, i32, opt, ctypes.POINTER(KrPlan)]
+        for name in ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_grad_x", "kernel_reduce_grad_x_ex",
+                     "kernel_knn", "kernel_knn_ex", "kr_last_cuda_error", "kr_plan", "kr_plan_device"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _status_text(status: int) -> str:
+    try:
+        return load_library().kr_status_string(int(status)).decode()
+    except Exception:  # library missing: keep the error readable
+        return "status"
+
+
+def _check(status: int, what: str) -> None:
+    if status != KR_OK:
+        cuda_err = load_library().kr_last_cuda_error() if status == KR_ERR_CUDA else 0
+        raise KrError(status, what, cuda_err)
+
+
+def _options(split: int):
+    if not split:
+        return None
+    o = KrOptions()
+    o.split = int(split)
+    return ctypes.byref(o)
+
+
+def plan(op: int, M: int, N: int, D: int, EK: int, num_sms: int = 152, blocks_per_sm: int = 0,
+         split: int = 0) -> KrPlan:
+    """The launch plan the library would use (host logic only, no GPU needed)."""
+    p = KrPlan()
+    _check(load_library().kr_plan(op, M, N, D, EK, num_sms, blocks_per_sm, _options(split), ctypes.byref(p)),
+           "kr_plan")
+    return p
+
+
+def plan_device(op: int, M: int, N: int, D: int, EK: int, split: int = 0) -> KrPlan:
+    """The launch plan a call makes on the current CUDA device (queries the device)."""
+    p = KrPlan()
+    _check(load_library().kr_plan_device(op, M, N, D, EK, _options(split), ctypes.byref(p)), "kr_plan_device")
+    return p
+
+
+# ---------------------------------------------------------------------------
+# tensor marshalling
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _mat(t, rows, name, cols=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if t.dim() == 1:
+        t = t.view(-1, 1)
+    if t.dim() != 2 or (rows is not None and t.shape[0] != rows) or (cols is not None and t.shape[1] != cols):
+        raise ValueError(f"{name}: bad shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _same_device(*ts):
+    devs = {t.device for t in ts if t is not None}
+    if len(devs) > 1:
+        raise ValueError(f"tensors on different devices: {devs}")
+    return devs.pop()
+
+
+def _stream(device):
+    torch = _torch()
+    if device.type == "cuda":
+        return torch.cuda.current_stream(device).cuda_stream
+    return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else None
+
+
+def kernel_reduce(x, y, b, sigma: float, reduction: str = "sum", out=None, split: int = 0):
+    """Sum (``reduction="sum"``) or LogSumExp (``"lse"``; b holds log-weights) over j.
+
+    Returns ``out`` (M, E): a_ie = sum_j exp(-|x_i-y_j|^2/sigma^2) b_je, or
+    L_ie = log sum_j exp(-|x_i-y_j|^2/sigma^2 + b_je)."""
+    torch = _torch()
+    red = {"sum": KR_SUM, "lse": KR_LSE}.get(reduction)
+    if red is None:
+        raise ValueError(f"reduction must be 'sum' or 'lse', got {reduction!r}")
+    x = _mat(x, None, "x")
+    M, D = x.shape
+    y = _mat(y, None, "y", D)
+    N = y.shape[0]
+    b = _mat(b, N, "b")
+    E = b.shape[1]
+    dev = _same_device(x, y, b)
+    if out is None:
+        out = torch.empty((M, E), dtype=torch.float32, device=dev)
+    out2 = _mat(out, M, "out", E)
+    _same_device(x, out2)
+    st = load_library().kernel_reduce_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(out2), M, N, D, E, float(sigma), red,
+                                         _stream(dev), _options(split))
+    _check(st, "kernel_reduce")
+    return out
+
+
+def kernel_reduce_grad_x(x, y, b, g, sigma: float, out=None, split: int = 0):
+    """Gradient wrt x of sum_ie g_ie a_ie (a the Sum reduction); returns (M, D)."""
+    torch = _torch()
+    x = _mat(x, None, "x")
+    M, D = x.shape
+    y = _mat(y, None, "y", D)
+    N = y.shape[0]
+    b = _mat(b, N, "b")
+    E = b.shape[1]
+    g = _mat(g, M, "g", E)
+    dev = _same_device(x, y, b, g)
+    if out is None:
+        out = torch.empty((M, D), dtype=torch.float32, device=dev)
+    out = _mat(out, M, "out", D)
+    _same_device(x, out)
+    st = load_library().kernel_reduce_grad_x_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(g), _ptr(out), M, N, D, E,
+                                                float(sigma), _stream(dev), _options(split))
+    _check(st, "kernel_reduce_grad_x")
+    return out
+
+
+def kernel_knn(x, y, K: int, idx=None, dist=None, want_dist: bool = True, split: int = 0):
+    """K smallest (|x_i-y_j|^2, j) per row, ascending, lowest index on ties.
+
+    Returns (idx int32 (M, K), dist float32 (M, K) or None)."""
+    torch = _torch()
+    x = _mat(x, None, "x")
+    M, D = x.shape
+    y = _mat(y, None, "y", D)
+    N = y.shape[0]
+    dev = _same_device(x, y)
+    K = int(K)
+    if idx is None:
+        idx = torch.empty((M, K), dtype=torch.int32, device=dev)
+    if dist is None and want_dist:
+        dist = torch.empty((M, K), dtype=torch.float32, device=dev)
+    if idx.dtype != torch.int32 or tuple(idx.shape) != (M, K) or not idx.is_contiguous():
+        raise ValueError("idx must be a contiguous int32 tensor of shape (M, K)")
+    if dist is not None:
+        dist = _mat(dist, M, "dist", K)
+    _same_device(x, idx, dist)
+    st = load_library().kernel_knn_ex(_ptr(x), _ptr(y), _ptr(idx), _ptr(dist), M, N, D, K, _stream(dev),
+                                      _options(split))
+    _check(st, "kernel_knn")
+    return idx, dist
+
+
+def _make_gaussian_sum():
+    torch = _torch()
+
+    class GaussianSum(torch.autograd.Function):
+        """a = sum_j exp(-|x_i-y_j|^2/sigma^2) b_j, differentiable wrt x.
+
+        Gradients wrt y and b are not provided (they raise if requested)."""
+
+        @staticmethod
+        def forward(ctx, x, y, b, sigma):
+            ctx.save_for_backward(x, y, b)
+            ctx.sigma = float(sigma)
+            return kernel_reduce(x.detach(), y.detach(), b.detach(), sigma, "sum")
+
+        @staticmethod
+        def backward(ctx, grad_out):
+            x, y, b = ctx.saved_tensors
+            if ctx.needs_input_grad[1] or ctx.needs_input_grad[2]:
+                raise NotImplementedError("GaussianSum differentiates wrt x only")
+            gx = None
+            if ctx.needs_input_grad[0]:
+                gx = kernel_reduce_grad_x(x.detach(), y.detach(), b.detach(),
+                                          grad_out.contiguous().view(x.shape[0], -1), ctx.sigma)
+            return gx, None, None, None
+
+    return GaussianSum
+
+
+def __getattr__(name):
+    if name == "GaussianSum":
+        cls = _make_gaussian_sum()
+        globals()["GaussianSum"] = cls
+        return cls
+    raise AttributeError(name)

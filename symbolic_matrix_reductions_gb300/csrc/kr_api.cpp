@@ -1,0 +1,442 @@
+// kr_api.cpp -- the C ABI: argument validation, launch planning, host-buffer
+// staging, stream-ordered workspace, launches.  No device code here.
+//
+// Planning: a launch is a grid of (row blocks, S) blocks.  A row block owns
+// kThreads * R rows; S splits the j axis into S disjoint ranges whose partial
+// results a second kernel combines in a fixed order (split-j).  S is chosen to
+// minimise the modelled time  waves(S) * (chunk(S) + tile overhead) where
+// waves = ceil(row_blocks * S / (SMs * resident blocks)), so that small-M /
+// huge-N problems (the tall products of the GitHub issue "Transparent interface
+// for billion-scale matrices") still fill every SM, and the last wave of a large
+// problem is not left mostly empty.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "kr_config.h"
+#include "kr_internal.h"
+
+namespace kr {
+
+static thread_local int g_last_cuda_error = 0;
+
+static int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return KR_ERR_CUDA;
+}
+
+Instance choose_instance(int op, int D, int EK) {
+    Instance in{};
+    in.d_pad = pad_d(D);
+    if (op == OP_KNN) {
+        in.ek_pad = pad_k(EK);
+        in.rows = rows_knn(in.d_pad, in.ek_pad);
+        in.tile = tile_points(pack_stride(in.d_pad, 0));
+    } else {
+        in.ek_pad = pad_e(EK);
+        in.rows = (op == OP_GRAD) ? rows_grad(in.d_pad, in.ek_pad) : rows_fwd(in.d_pad, in.ek_pad);
+        in.tile = tile_points(pack_stride(in.d_pad, in.ek_pad));
+    }
+    return in;
+}
+
+// Bytes of split-j workspace for S splits.
+static int64_t workspace_bytes(int op, const Instance &in, int64_t M, int D, int EK, int S) {
+    if (S <= 1) return 0;
+    switch (op) {
+        case OP_SUM:
+        case OP_LSE: return 2 * (int64_t)S * M * EK * (int64_t)sizeof(float);
+        case OP_GRAD: return 2 * (int64_t)S * M * D * (int64_t)sizeof(float);
+        case OP_KNN: return (int64_t)S * M * in.ek_pad * (int64_t)(sizeof(float) + sizeof(int32_t));
+    }
+    return 0;
+}
+
+static const int64_t kMaxWorkspace = (int64_t)1 << 30;  // 1 GiB of partials at most
+
+// Pure planner (no CUDA call).  blocks_per_sm <= 0: assume 4 resident blocks.
+static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm,
+                int forced_split, kr_plan_t *p) {
+    const Instance in = choose_instance(op, D, EK);
+    p->d_pad = in.d_pad;
+    p->ek_pad = in.ek_pad;
+    p->rows_per_thread = in.rows;
+    p->threads = kThreads;
+    p->tile_points = in.tile;
+    const int64_t bm = (int64_t)kThreads * in.rows;
+    p->row_blocks = (M + bm - 1) / bm;
+    if (num_sms < 1) num_sms = 1;
+    if (blocks_per_sm < 1) blocks_per_sm = 4;
+    const int64_t slots = (int64_t)num_sms * blocks_per_sm;
+
+    int S = 1;
+    if (forced_split >= 1) {
+        S = (int)std::min<int64_t>(forced_split, std::max<int64_t>(N, 1));
+        S = std::min(S, kMaxSplit);
+    } else if (N > 0 && p->row_blocks > 0) {
+        // At least 64 points per split, at most kMaxSplit splits.
+        const int64_t s_max = std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, N / 64));
+        double best = 0.0;
+        for (int64_t s = 1; s <= s_max; ++s) {
+            if (workspace_bytes(op, in, M, D, EK, (int)s) > kMaxWorkspace) break;
+            const int64_t chunk = (N + s - 1) / s;
+            const int64_t waves = (p->row_blocks * s + slots - 1) / slots;
+            const int64_t tiles = (chunk + in.tile - 1) / in.tile;
+            // per-tile fixed cost ~ 32 points; each split adds a small combine cost
+            const double cost = (double)waves * (double)(chunk + 32 * tiles) * (1.0 + 0.002 * (double)s);
+            if (s == 1 || cost < best * 0.999) {
+                best = cost;
+                S = (int)s;
+            }
+        }
+    }
+    p->split = S;
+    p->chunk = (N + S - 1) / S;
+    if (p->chunk < 1) p->chunk = 1;
+    // Every split must own a nonempty range, except when N == 0.
+    if (N > 0 && (int64_t)(S - 1) * p->chunk >= N) {
+        S = (int)((N + p->chunk - 1) / p->chunk);
+        p->split = S;
+    }
+    p->workspace_bytes = workspace_bytes(op, in, M, D, EK, S);
+    return KR_OK;
+}
+
+// ---- per-device cached attributes -----------------------------------------------
+namespace {
+struct DeviceCache {
+    int num_sms = 0;
+    int occ[4][10][33] = {};  // resident blocks per (op, d_pad index, ek_pad); 0 = not queried
+};
+std::mutex g_cache_mutex;
+DeviceCache g_cache[64];
+
+int d_index(int d_pad) {
+    switch (d_pad) {
+        case 1: case 2: case 3: case 4: return d_pad - 1;
+        case 8: return 4;
+        case 16: return 5;
+        case 32: return 6;
+        case 50: return 7;
+        case 64: return 8;
+        default: return 9;
+    }
+}
+
+int query_occupancy(int op, const Instance &in) {
+    switch (op) {
+        case OP_SUM: return occupancy_sum(in);
+        case OP_LSE: return occupancy_lse(in);
+        case OP_GRAD: return occupancy_grad(in);
+        case OP_KNN: return occupancy_knn(in);
+    }
+    return 0;
+}
+
+int device_info(int dev, int op, const Instance &in, int *num_sms, int *occ) {
+    if (dev < 0 || dev >= 64) return -1;
+    std::lock_guard<std::mutex> lock(g_cache_mutex);
+    DeviceCache &c = g_cache[dev];
+    if (c.num_sms == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        c.num_sms = n;
+    }
+    *num_sms = c.num_sms;
+    int &slot = c.occ[op][d_index(in.d_pad)][in.ek_pad];
+    if (slot == 0) slot = query_occupancy(op, in);
+    *occ = slot;
+    return 0;
+}
+}  // namespace
+
+// ---- validation ---------------------------------------------------------------------
+static bool overlaps(const void *a, int64_t abytes, const void *b, int64_t bbytes) {
+    if (!a || !b || abytes <= 0 || bbytes <= 0) return false;
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
+}
+
+static bool fits_int31(int64_t rows, int64_t cols) {
+    return rows >= 0 && cols >= 0 && (cols == 0 || rows <= (((int64_t)1 << 31) - 1) / cols);
+}
+
+struct Buf {
+    const void *ptr;
+    int64_t bytes;
+    bool output;
+};
+
+static int validate(int op, const Buf *bufs, int nbuf, int64_t M, int64_t N, int D, int EK, float sigma,
+                    const kr_options *opt) {
+    if (M < 0 || N < 0) return KR_ERR_INVALID;
+    if (D < 1 || EK < 1) return KR_ERR_INVALID;
+    if (op != OP_KNN && !(std::isfinite(sigma) && sigma > 0.f)) return KR_ERR_INVALID;
+    if (opt) {
+        if (opt->split < 0) return KR_ERR_INVALID;
+        for (int k = 0; k < 7; ++k)
+            if (opt->reserved[k] != 0) return KR_ERR_INVALID;
+    }
+    if (D > kMaxD) return KR_ERR_UNSUPPORTED;
+    if (op == OP_KNN ? EK > kMaxK : EK > kMaxE) return KR_ERR_UNSUPPORTED;
+    const int64_t Mx = std::max<int64_t>(M, 1), Nx = std::max<int64_t>(N, 1);
+    if (!fits_int31(Mx, D) || !fits_int31(Nx, D) || !fits_int31(Mx, EK) || !fits_int31(Nx, EK))
+        return KR_ERR_UNSUPPORTED;
+    if (N > INT32_MAX - 1) return KR_ERR_UNSUPPORTED;
+    for (int k = 0; k < nbuf; ++k)
+        if (bufs[k].bytes > 0 && bufs[k].ptr == nullptr) return KR_ERR_INVALID;
+    for (int k = 0; k < nbuf; ++k) {
+        if (!bufs[k].output) continue;
+        for (int l = 0; l < nbuf; ++l) {
+            if (l == k) continue;
+            if (overlaps(bufs[k].ptr, bufs[k].bytes, bufs[l].ptr, bufs[l].bytes)) return KR_ERR_INVALID;
+        }
+    }
+    return KR_OK;
+}
+
+// ---- allocation (with an opt-in failure injection for tests) -----------------------
+static cudaError_t ws_alloc(void **p, size_t bytes, cudaStream_t s) {
+    // KREDUCE_FAIL_ALLOC=1 makes every workspace/staging allocation fail, so that
+    // the KR_ERR_ALLOC path can be tested without exhausting device memory.
+    const char *inj = std::getenv("KREDUCE_FAIL_ALLOC");
+    if (inj && inj[0] == '1') {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMallocAsync(p, bytes, s);
+}
+
+// Is `p` directly usable by kernels?  Host memory (pageable or pinned) is staged.
+static int is_device_ptr(const void *p, bool *dev) {
+    cudaPointerAttributes at;
+    const cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return (int)e;
+    }
+    *dev = (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged);
+    return 0;
+}
+
+// ---- the common driver --------------------------------------------------------------
+static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStream_t stream,
+               const kr_options *opt) {
+    int st = validate(op, bufs, nbuf, a.M, a.N, a.D, EK, sigma, opt);
+    if (st != KR_OK) return st;
+    if (a.M == 0) return KR_OK;
+
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+
+    const Instance in = choose_instance(op, a.D, EK);
+    int num_sms = 0, occ = 0;
+    if (device_info(dev, op, in, &num_sms, &occ) != 0) return cuda_fail(cudaGetLastError());
+    kr_plan_t p;
+    plan(op, a.M, a.N, a.D, EK, num_sms, occ, opt ? opt->split : 0, &p);
+
+    // Host arrays: stage through one device allocation.
+    bool host[8] = {};
+    int64_t stage_bytes = 0;
+    for (int k = 0; k < nbuf; ++k) {
+        if (!bufs[k].ptr || bufs[k].bytes <= 0) continue;
+        bool d = true;
+        const int e = is_device_ptr(bufs[k].ptr, &d);
+        if (e) return cuda_fail((cudaError_t)e);
+        host[k] = !d;
+        if (host[k]) stage_bytes += (bufs[k].bytes + 255) / 256 * 256;
+    }
+    const int64_t ws_bytes = (p.workspace_bytes + 255) / 256 * 256;
+    char *mem = nullptr;
+    if (stage_bytes + ws_bytes > 0) {
+        ce = ws_alloc((void **)&mem, (size_t)(stage_bytes + ws_bytes), stream);
+        if (ce != cudaSuccess) {
+            cudaGetLastError();
+            return KR_ERR_ALLOC;
+        }
+    }
+    void *dptr[8] = {};
+    int64_t off = 0;
+    int status = KR_OK;
+    for (int k = 0; k < nbuf && status == KR_OK; ++k) {
+        dptr[k] = const_cast<void *>(bufs[k].ptr);
+        if (!host[k]) continue;
+        dptr[k] = mem + off;
+        off += (bufs[k].bytes + 255) / 256 * 256;
+        if (!bufs[k].output) {
+            ce = cudaMemcpyAsync(dptr[k], bufs[k].ptr, (size_t)bufs[k].bytes, cudaMemcpyHostToDevice, stream);
+            if (ce != cudaSuccess) status = cuda_fail(ce);
+        }
+    }
+    char *ws = mem ? mem + stage_bytes : nullptr;
+
+    if (status == KR_OK) {
+        // Buffer order: x, y, b, [g,] out | x, y, idx, dist
+        a.x = (const float *)dptr[0];
+        a.y = (const float *)dptr[1];
+        if (op == OP_KNN) {
+            a.idx = (int32_t *)dptr[2];
+            a.out = (float *)dptr[3];
+        } else {
+            a.b = (const float *)dptr[2];
+            if (op == OP_GRAD) {
+                a.g = (const float *)dptr[3];
+                a.out = (float *)dptr[4];
+            } else {
+                a.out = (float *)dptr[3];
+            }
+        }
+        a.S = p.split;
+        a.chunk = p.chunk;
+        if (p.split > 1) {
+            a.ws0 = (float *)ws;
+            if (op == OP_KNN) {
+                a.wsi = (int32_t *)(ws + (int64_t)p.split * a.M * p.ek_pad * (int64_t)sizeof(float));
+            } else {
+                a.ws1 = (float *)(ws + p.workspace_bytes / 2);
+            }
+        }
+        const dim3 grid((unsigned)p.row_blocks, (unsigned)p.split);
+        switch (op) {
+            case OP_SUM: ce = launch_sum(in, a, grid, stream); break;
+            case OP_LSE: ce = launch_lse(in, a, grid, stream); break;
+            case OP_GRAD: ce = launch_grad(in, a, grid, stream); break;
+            default: ce = launch_knn(in, a, grid, stream); break;
+        }
+        if (ce == cudaSuccess && p.split > 1) ce = launch_combine(op, in, a, stream);
+        if (ce != cudaSuccess) status = cuda_fail(ce);
+    }
+    if (status == KR_OK) {
+        for (int k = 0; k < nbuf; ++k) {
+            if (!host[k] || !bufs[k].output) continue;
+            ce = cudaMemcpyAsync(const_cast<void *>(bufs[k].ptr), dptr[k], (size_t)bufs[k].bytes,
+                                 cudaMemcpyDeviceToHost, stream);
+            if (ce != cudaSuccess) {
+                status = cuda_fail(ce);
+                break;
+            }
+        }
+    }
+    if (mem) {
+        ce = cudaFreeAsync(mem, stream);
+        if (ce != cudaSuccess && status == KR_OK) status = cuda_fail(ce);
+    }
+    if (stage_bytes > 0) {
+        ce = cudaStreamSynchronize(stream);
+        if (ce != cudaSuccess && status == KR_OK) status = cuda_fail(ce);
+    }
+    return status;
+}
+
+}  // namespace kr
+
+using namespace kr;
+
+extern "C" {
+
+int kernel_reduce_ex(const float *x, const float *y, const float *b, float *out, int64_t M, int64_t N,
+                     int D, int E, float sigma, int reduction, kr_stream_t stream, const kr_options *opt) {
+    if (reduction != KR_SUM && reduction != KR_LSE) return KR_ERR_INVALID;
+    const int op = reduction == KR_SUM ? OP_SUM : OP_LSE;
+    if (M < 0 || N < 0 || D < 1 || E < 1) return KR_ERR_INVALID;
+    const int64_t f = (int64_t)sizeof(float);
+    Buf bufs[4] = {{x, M * D * f, false}, {y, N * D * f, false}, {b, N * E * f, false}, {out, M * E * f, true}};
+    Args a{};
+    a.M = M;
+    a.N = N;
+    a.D = D;
+    a.E = E;
+    a.K = 0;
+    a.c = (float)(std::sqrt(1.4426950408889634) / (double)sigma);
+    return run(op, bufs, 4, a, E, sigma, (cudaStream_t)stream, opt);
+}
+
+int kernel_reduce(const float *x, const float *y, const float *b, float *out, int64_t M, int64_t N, int D,
+                  int E, float sigma, int reduction, kr_stream_t stream) {
+    return kernel_reduce_ex(x, y, b, out, M, N, D, E, sigma, reduction, stream, nullptr);
+}
+
+int kernel_reduce_grad_x_ex(const float *x, const float *y, const float *b, const float *g, float *gx,
+                            int64_t M, int64_t N, int D, int E, float sigma, kr_stream_t stream,
+                            const kr_options *opt) {
+    if (M < 0 || N < 0 || D < 1 || E < 1) return KR_ERR_INVALID;
+    const int64_t f = (int64_t)sizeof(float);
+    Buf bufs[5] = {{x, M * D * f, false}, {y, N * D * f, false}, {b, N * E * f, false},
+                   {g, M * E * f, false}, {gx, M * D * f, true}};
+    Args a{};
+    a.M = M;
+    a.N = N;
+    a.D = D;
+    a.E = E;
+    const double c = std::sqrt(1.4426950408889634) / (double)sigma;
+    a.c = (float)c;
+    a.gscale = (float)(-2.0 / ((double)sigma * (double)sigma * c));
+    return run(OP_GRAD, bufs, 5, a, E, sigma, (cudaStream_t)stream, opt);
+}
+
+int kernel_reduce_grad_x(const float *x, const float *y, const float *b, const float *g, float *gx, int64_t M,
+                         int64_t N, int D, int E, float sigma, kr_stream_t stream) {
+    return kernel_reduce_grad_x_ex(x, y, b, g, gx, M, N, D, E, sigma, stream, nullptr);
+}
+
+int kernel_knn_ex(const float *x, const float *y, int32_t *idx, float *dist, int64_t M, int64_t N, int D,
+                  int K, kr_stream_t stream, const kr_options *opt) {
+    if (M < 0 || N < 0 || D < 1 || K < 1) return KR_ERR_INVALID;
+    const int64_t f = (int64_t)sizeof(float);
+    Buf bufs[4] = {{x, M * D * f, false}, {y, N * D * f, false}, {idx, M * K * (int64_t)sizeof(int32_t), true},
+                   {dist, dist ? M * K * f : 0, true}};
+    Args a{};
+    a.M = M;
+    a.N = N;
+    a.D = D;
+    a.E = 1;
+    a.K = K;
+    a.c = 1.f;
+    return run(OP_KNN, bufs, 4, a, K, 1.f, (cudaStream_t)stream, opt);
+}
+
+int kernel_knn(const float *x, const float *y, int32_t *idx, float *dist, int64_t M, int64_t N, int D, int K,
+               kr_stream_t stream) {
+    return kernel_knn_ex(x, y, idx, dist, M, N, D, K, stream, nullptr);
+}
+
+const char *kr_status_string(int status) {
+    switch (status) {
+        case KR_OK: return "ok";
+        case KR_ERR_INVALID: return "invalid argument";
+        case KR_ERR_UNSUPPORTED: return "unsupported size or shape";
+        case KR_ERR_ALLOC: return "workspace allocation failed";
+        case KR_ERR_CUDA: return "CUDA runtime error";
+        default: return "unknown status";
+    }
+}
+
+int kr_last_cuda_error(void) { return g_last_cuda_error; }
+
+int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm, const kr_options *opt,
+            kr_plan_t *out) {
+    if (!out || op < 0 || op > 3) return KR_ERR_INVALID;
+    const int st = validate(op, nullptr, 0, M, N, D, EK, 1.f, opt);
+    if (st != KR_OK) return st;
+    return plan(op, M, N, D, EK, num_sms, blocks_per_sm, opt ? opt->split : 0, out);
+}
+
+int kr_plan_device(int op, int64_t M, int64_t N, int D, int EK, const kr_options *opt, kr_plan_t *out) {
+    if (!out || op < 0 || op > 3) return KR_ERR_INVALID;
+    const int st = validate(op, nullptr, 0, M, N, D, EK, 1.f, opt);
+    if (st != KR_OK) return st;
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    int num_sms = 0, occ = 0;
+    if (device_info(dev, op, choose_instance(op, D, EK), &num_sms, &occ) != 0) return cuda_fail(cudaGetLastError());
+    return plan(op, M, N, D, EK, num_sms, occ, opt ? opt->split : 0, out);
+}
+
+}  // extern "C"

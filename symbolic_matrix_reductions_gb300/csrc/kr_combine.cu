@@ -1,0 +1,91 @@
+// Split-j combine kernels: deterministic, fixed split order.
+#include "kr_kernels.cuh"
+
+namespace kr {
+
+__global__ void combine_sum_kernel(const Args a, int W) {
+    const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t total = a.M * W;
+    if (o >= total) return;
+    double acc = 0.0;
+    for (int s = 0; s < a.S; ++s) acc += (double)a.ws0[s * total + o] + (double)a.ws1[s * total + o];
+    a.out[o] = (float)acc;
+}
+
+__global__ void combine_lse_kernel(const Args a) {
+    const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t total = a.M * a.E;
+    if (o >= total) return;
+    float mmax = -f_inf();
+    for (int s = 0; s < a.S; ++s) mmax = fmaxf(mmax, a.ws0[s * total + o]);
+    if (mmax == -f_inf()) {
+        a.out[o] = -f_inf();
+        return;
+    }
+    double acc = 0.0;
+    for (int s = 0; s < a.S; ++s) {
+        const float acc_s = a.ws1[s * total + o];
+        if (acc_s > 0.f) acc += (double)acc_s * exp2((double)a.ws0[s * total + o] - (double)mmax);
+    }
+    a.out[o] = (float)(0.6931471805599453 * ((double)mmax + log2(acc)));
+}
+
+__global__ void combine_knn_kernel(const Args a, int KP) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= a.M) return;
+    int head[kMaxSplit];
+    for (int s = 0; s < a.S; ++s) head[s] = 0;
+    for (int k = 0; k < a.K; ++k) {
+        int best = -1;
+        float bd = 0.f;
+        int bj = 0;
+        for (int s = 0; s < a.S; ++s) {
+            if (head[s] >= KP) continue;
+            const int64_t w = ((int64_t)s * a.M + i) * KP + head[s];
+            const int j = a.wsi[w];
+            if (j < 0) continue;  // empty slot: ranks after every real pair
+            const float d = a.ws0[w];
+            if (best < 0 || d < bd || (d == bd && j < bj)) {
+                best = s;
+                bd = d;
+                bj = j;
+            }
+        }
+        if (best < 0) {
+            a.idx[i * a.K + k] = -1;
+            if (a.out) a.out[i * a.K + k] = f_inf();
+        } else {
+            a.idx[i * a.K + k] = bj;
+            if (a.out) a.out[i * a.K + k] = bd;
+            ++head[best];
+        }
+    }
+}
+
+cudaError_t launch_combine(int op, const Instance &inst, const Args &a, cudaStream_t s) {
+    const int threads = 256;
+    int64_t n = 0;
+    switch (op) {
+        case OP_SUM:
+            n = a.M * a.E;
+            combine_sum_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(a, a.E);
+            break;
+        case OP_GRAD:
+            n = a.M * a.D;
+            combine_sum_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(a, a.D);
+            break;
+        case OP_LSE:
+            n = a.M * a.E;
+            combine_lse_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(a);
+            break;
+        case OP_KNN:
+            n = a.M;
+            combine_knn_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(a, inst.ek_pad);
+            break;
+        default:
+            return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kr

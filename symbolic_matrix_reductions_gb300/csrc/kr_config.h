@@ -1,0 +1,52 @@
+// kr_config.h -- compile-time shapes of the kernel instances, shared by the host
+// planner and the device code (constexpr, no CUDA dependency).
+#pragma once
+
+#ifdef __CUDACC__
+#define KR_HD __host__ __device__
+#else
+#define KR_HD
+#endif
+
+namespace kr {
+
+// Coordinate count the instance is compiled for: exact for D <= 4, else the next
+// of 8, 16, 32, 50, 64, 128 (padded coordinates are zero on both sides, so they
+// add nothing to a distance).
+KR_HD constexpr int pad_d(int D) {
+    return D <= 4 ? D : D <= 8 ? 8 : D <= 16 ? 16 : D <= 32 ? 32 : D <= 50 ? 50 : D <= 64 ? 64 : 128;
+}
+// Signal columns the instance is compiled for (zero-padded signal columns).
+KR_HD constexpr int pad_e(int E) { return E <= 1 ? 1 : E <= 4 ? 4 : 16; }
+// K-min list length the instance keeps (the first K of a longer sorted list are
+// the K smallest).
+KR_HD constexpr int pad_k(int K) { return K <= 1 ? 1 : K <= 4 ? 4 : K <= 10 ? 10 : K <= 16 ? 16 : 32; }
+
+// Floats per point in the shared-memory tile: coordinates then values, rounded
+// up to whole float4s so every point is read with 16-byte loads.
+KR_HD constexpr int pack_stride(int DP, int VP) { return (DP + VP + 3) / 4 * 4; }
+
+// Points of y per tile: the largest power of two whose tile fits in 32 KB,
+// between 32 and 512.
+KR_HD constexpr int tile_points(int PS) {
+    return (8192 / PS) >= 512 ? 512 : (8192 / PS) >= 256 ? 256 : (8192 / PS) >= 128 ? 128
+         : (8192 / PS) >= 64 ? 64 : 32;
+}
+
+// Rows of x each thread keeps in registers (each shared-memory read of y_j then
+// feeds R pairs).  Chosen so that coordinates, accumulators and the K-min list
+// stay in registers.
+KR_HD constexpr int rows_fwd(int DP, int EP) {
+    return EP >= 16 ? 1 : EP >= 4 ? (DP <= 8 ? 2 : 1) : (DP <= 8 ? 4 : DP <= 16 ? 2 : 1);
+}
+KR_HD constexpr int rows_grad(int DP, int EP) {
+    return DP <= 4 ? (EP == 1 ? 4 : EP == 4 ? 2 : 1) : DP <= 8 ? (EP == 1 ? 2 : 1) : 1;
+}
+KR_HD constexpr int rows_knn(int DP, int KP) {
+    return DP <= 4 ? (KP <= 10 ? 4 : KP == 16 ? 2 : 1) : DP <= 16 ? (KP <= 10 ? 2 : 1) : 1;
+}
+
+// Inner-loop unroll over tile points (tiles are padded to a multiple of it).
+KR_HD constexpr int unroll_points(int DP) { return DP <= 8 ? 4 : DP <= 32 ? 2 : 1; }
+
+}  // namespace kr

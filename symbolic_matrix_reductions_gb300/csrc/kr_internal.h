@@ -1,0 +1,61 @@
+// kr_internal.h -- declarations shared by the host planner and the kernel instance files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kreduce.h"
+
+namespace kr {
+
+enum Op { OP_SUM = 0, OP_LSE = 1, OP_GRAD = 2, OP_KNN = 3 };
+
+constexpr int kThreads = 128;   // threads per block for every main kernel
+constexpr int kMaxD = 128;
+constexpr int kMaxE = 16;
+constexpr int kMaxK = 32;
+constexpr int kMaxSplit = 64;   // most j-ranges a call is split into
+
+// Everything a main kernel needs; passed by value as the kernel parameter.
+struct Args {
+    const float *x;      // M x D
+    const float *y;      // N x D
+    const float *b;      // N x E: signal (Sum, grad) or log-weight (LSE)
+    const float *g;      // M x E upstream gradient (grad only)
+    float *out;          // S == 1: final output (M x E, M x D or M x K distances)
+    int32_t *idx;        // K-min indices, S == 1
+    float *ws0;          // S > 1: first partial array  (S x M x W)
+    float *ws1;          // S > 1: second partial array (S x M x W)
+    int32_t *wsi;        // S > 1: K-min partial indices (S x M x K_pad)
+    int64_t M, N;
+    int D, E, K;
+    float c;             // coordinate prescale sqrt(log2 e) / sigma (1 for K-min)
+    float gscale;        // grad: -2 / (sigma^2 c)
+    int64_t chunk;       // columns per split
+    int S;
+};
+
+// Compile-time shape of one kernel instance, chosen by the planner.
+struct Instance {
+    int d_pad, ek_pad, rows, tile;
+};
+
+// Instance selection (pure host logic).
+Instance choose_instance(int op, int D, int EK);
+
+// Launchers, one per kernel family; they dispatch on the instance and return the
+// launch's cudaError_t.  grid = (row_blocks, S).
+cudaError_t launch_sum(const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
+cudaError_t launch_lse(const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
+cudaError_t launch_grad(const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
+cudaError_t launch_knn(const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
+cudaError_t launch_combine(int op, const Instance &inst, const Args &a, cudaStream_t s);
+
+// Resident blocks per SM of an instance (cudaOccupancyMaxActiveBlocksPerMultiprocessor);
+// 0 if unknown.
+int occupancy_sum(const Instance &inst);
+int occupancy_lse(const Instance &inst);
+int occupancy_grad(const Instance &inst);
+int occupancy_knn(const Instance &inst);
+
+}  // namespace kr

@@ -1,0 +1,165 @@
+"""The C ABI without a GPU: the library loads, exports every function the header
+declares, rejects bad arguments before any CUDA call, and plans launches with
+pure host logic."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import symbolic_matrix_reductions_gb300 as kr
+from symbolic_matrix_reductions_gb300 import build as kbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kreduce.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kr.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("kernel_reduce", "kernel_reduce_grad_x", "kernel_knn", "kr_status_string"):
+        assert n in names
+    assert tuple(names) == kr.EXPORTS
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    texts = {lib.kr_status_string(s).decode() for s in range(5)}
+    assert len(texts) == 5
+    assert lib.kr_status_string(99).decode() == "unknown status"
+
+
+P = ctypes.c_void_p
+FAKE = [P(0x10000 * (k + 1)) for k in range(8)]  # never dereferenced: validation fails first
+
+
+def _reduce(lib, x=FAKE[0], y=FAKE[1], b=FAKE[2], out=FAKE[3], M=10, N=10, D=3, E=1, sigma=1.0, red=0,
+            opt=None):
+    return lib.kernel_reduce_ex(x, y, b, out, M, N, D, E, sigma, red, None, opt)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1), kr.KR_ERR_INVALID),
+    (dict(N=-5), kr.KR_ERR_INVALID),
+    (dict(D=0), kr.KR_ERR_INVALID),
+    (dict(E=0), kr.KR_ERR_INVALID),
+    (dict(sigma=0.0), kr.KR_ERR_INVALID),
+    (dict(sigma=-1.0), kr.KR_ERR_INVALID),
+    (dict(sigma=float("nan")), kr.KR_ERR_INVALID),
+    (dict(sigma=float("inf")), kr.KR_ERR_INVALID),
+    (dict(red=2), kr.KR_ERR_INVALID),
+    (dict(x=None), kr.KR_ERR_INVALID),
+    (dict(y=None), kr.KR_ERR_INVALID),
+    (dict(b=None), kr.KR_ERR_INVALID),
+    (dict(out=None), kr.KR_ERR_INVALID),
+    (dict(D=129), kr.KR_ERR_UNSUPPORTED),
+    (dict(E=17), kr.KR_ERR_UNSUPPORTED),
+    (dict(M=1 << 30, D=3), kr.KR_ERR_UNSUPPORTED),      # M*D >= 2^31
+    (dict(out=P(0x10000 + 8)), kr.KR_ERR_INVALID),      # output overlaps x
+    (dict(M=0, out=None, x=None), kr.KR_OK),            # M = 0 is a no-op, no device needed
+])
+def test_reduce_validation(lib, kw, status):
+    assert _reduce(lib, **kw) == status
+
+
+def test_options_validation(lib):
+    o = kr.KrOptions()
+    o.split = -1
+    assert _reduce(lib, opt=ctypes.byref(o)) == kr.KR_ERR_INVALID
+    o.split = 0
+    o.reserved[3] = 1
+    assert _reduce(lib, opt=ctypes.byref(o)) == kr.KR_ERR_INVALID
+
+
+def test_grad_and_knn_validation(lib):
+    g = lib.kernel_reduce_grad_x_ex
+    assert g(FAKE[0], FAKE[1], FAKE[2], None, FAKE[4], 10, 10, 3, 1, 1.0, None, None) == kr.KR_ERR_INVALID
+    assert g(FAKE[0], FAKE[1], FAKE[2], FAKE[3], FAKE[4], 10, 10, 3, 1, 0.0, None, None) == kr.KR_ERR_INVALID
+    assert g(FAKE[0], FAKE[1], FAKE[2], FAKE[3], FAKE[4], 10, 10, 200, 1, 1.0, None, None) == kr.KR_ERR_UNSUPPORTED
+    k = lib.kernel_knn_ex
+    assert k(FAKE[0], FAKE[1], FAKE[2], None, 10, 10, 3, 0, None, None) == kr.KR_ERR_INVALID
+    assert k(FAKE[0], FAKE[1], FAKE[2], None, 10, 10, 3, 33, None, None) == kr.KR_ERR_UNSUPPORTED
+    assert k(FAKE[0], FAKE[1], None, None, 10, 10, 3, 4, None, None) == kr.KR_ERR_INVALID
+    # idx and dist may not overlap
+    assert k(FAKE[0], FAKE[1], FAKE[2], P(0x30000 + 4), 10, 10, 3, 4, None, None) == kr.KR_ERR_INVALID
+    assert k(None, None, None, None, 0, 0, 3, 4, None, None) == kr.KR_OK
+
+
+# ---------------------------------------------------------------------------
+# planner (pure host logic)
+# ---------------------------------------------------------------------------
+def test_instance_choice(lib):
+    p = kr.plan(kr.OP_SUM, 1000, 1000, 3, 1)
+    assert (p.d_pad, p.ek_pad, p.threads) == (3, 1, 128)
+    assert kr.plan(kr.OP_SUM, 10, 10, 5, 2).d_pad == 8 and kr.plan(kr.OP_SUM, 10, 10, 5, 2).ek_pad == 4
+    assert kr.plan(kr.OP_SUM, 10, 10, 50, 1).d_pad == 50
+    assert kr.plan(kr.OP_SUM, 10, 10, 51, 16).d_pad == 64
+    assert kr.plan(kr.OP_KNN, 10, 10, 16, 10).ek_pad == 10
+    assert kr.plan(kr.OP_KNN, 10, 10, 16, 11).ek_pad == 16
+    assert kr.plan(kr.OP_KNN, 10, 10, 16, 1).ek_pad == 1
+
+
+@pytest.mark.parametrize("op,M,N,D,EK", [
+    (kr.OP_SUM, 100_000, 100_000, 3, 1),
+    (kr.OP_LSE, 1_000_000, 1_000_000, 3, 1),
+    (kr.OP_SUM, 100_000, 10_000_000, 50, 1),
+    (kr.OP_KNN, 1_000_000, 1_000_000, 16, 10),
+    (kr.OP_GRAD, 1000, 1000, 3, 1),
+    (kr.OP_SUM, 7, 3, 3, 1),
+    (kr.OP_SUM, 5, 0, 3, 1),
+])
+def test_split_covers_all_columns(lib, op, M, N, D, EK):
+    p = kr.plan(op, M, N, D, EK, num_sms=152, blocks_per_sm=8)
+    assert 1 <= p.split <= 64
+    assert p.split * p.chunk >= N
+    assert N == 0 or (p.split - 1) * p.chunk < N      # no empty split
+    bm = p.threads * p.rows_per_thread
+    assert p.row_blocks == (M + bm - 1) // bm
+    if p.split == 1:
+        assert p.workspace_bytes == 0
+
+
+def test_split_fills_the_gpu_for_tall_products(lib):
+    # M = 1e5 rows at D = 50 are only a few hundred blocks: the j axis must be split.
+    p = kr.plan(kr.OP_SUM, 100_000, 10_000_000, 50, 1, num_sms=152, blocks_per_sm=4)
+    assert p.split > 1
+    waves = (p.row_blocks * p.split) / (152 * 4)
+    assert waves >= 2
+    assert p.workspace_bytes == 2 * p.split * 100_000 * 4
+    # never split below 64 points per split
+    assert kr.plan(kr.OP_SUM, 10, 100, 3, 1).split == 1
+    assert kr.plan(kr.OP_SUM, 1000, 1000, 3, 1, blocks_per_sm=8).chunk >= 64
+
+
+def test_forced_split(lib):
+    p = kr.plan(kr.OP_KNN, 1000, 5000, 16, 10, split=7)
+    assert p.split == 7 and p.chunk == 715
+    assert p.workspace_bytes == 7 * 1000 * 10 * 8
+    assert kr.plan(kr.OP_SUM, 10, 3, 3, 1, split=9).split == 3   # never more splits than columns
+
+
+def test_python_marshalling_errors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(4, 3)
+    with pytest.raises(TypeError):
+        kr.kernel_reduce(x.double(), x, torch.zeros(4), 1.0)
+    with pytest.raises(ValueError):
+        kr.kernel_reduce(x, torch.zeros(4, 2), torch.zeros(4), 1.0)
+    with pytest.raises(ValueError):
+        kr.kernel_reduce(x, x, torch.zeros(4), 1.0, reduction="max")
+    with pytest.raises(ValueError):
+        kr.kernel_reduce(x.t(), x, torch.zeros(3), 1.0)
