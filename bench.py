@@ -1,0 +1,473 @@
+"""Benchmark of the symbolic kernel reductions on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch of synthetic input: on
+the gauss_d3 batch (M = N = 100000 points in dimension 3, sigma = 0.5, x, y, b
+~ N(0,1)) it runs the Gaussian Sum, the LogSumExp (with b as log-weights), the
+x-gradient (upstream g ~ N(0,1)) and the K-min (K = 10), each through the C ABI;
+split-j runs whenever the planner picks it.  The metric is pair-evaluations per
+second, M*N per reduction, over the whole step.
+
+Prints ONE JSON line (rank 0).  Timing: W warm-up steps, then K steps, each
+bracketed by CUDA events on the launching stream; L2 is flushed (a 256 MB write)
+before every timed step, outside the events.  Also reported:
+  * roofline of the dominant kernel against the FP32 / MUFU pipe peak derived
+    from the SM count, the FP32 lanes per SM, the ex2 lanes per SM (measured by
+    the pipe probe in this run) and the maximum SM clock;
+  * e2e: the same step with HOST buffers through the same C ABI calls (the
+    library stages inputs and results), timed on the host clock;
+  * secondary lines for the other workloads (D=3 at 1M points, the D=50 tall
+    product, the D=16 K-min), one timed run set each, each with its roofline;
+  * cpu_baseline: the fp64 oracle on this host's cores on a bounded row sample.
+``--impl reference`` times the oracle as the reference arm instead.
+Under torchrun (N > 1) every rank runs its own replica (no data exchange); the
+job value is N times the per-step pairs over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Gaussian kernel pair-evals/s (M·N/t) at D=3 and D=50; % of FP32/MUFU roofline"
+UNIT = "pair-evals/s"
+PRIMARY = "gauss_d3"
+K_NN = 10
+
+# Per-pair pipe operations of each kernel (the counts the hot loop must issue, with
+# x and y prescaled once per point):  FP32 = FADD/FMUL/FFMA lanes, XU = MUFU ex2,
+# ALU = compare.  Sum: D sub + D mul/fma + 1 fma;  LSE: the same (the per-tile
+# offset W - w'_j starts the distance's fma chain, so no per-pair max is needed);
+# grad: D sub + D fma
+# (distance) + 1 mul (k*b) + D fma;  K-min: D sub + D fma + 1 compare.
+def ops_per_pair(op: str, D: int, E: int = 1):
+    if op == "sum":
+        return {"fp32": 2 * D + E, "xu": 1, "alu": 0}
+    if op == "lse":
+        return {"fp32": 2 * D + E, "xu": E, "alu": 0}
+    if op == "grad":
+        return {"fp32": 3 * D + 1 + (E if E > 1 else 0), "xu": 1, "alu": 0}
+    if op == "knn":
+        return {"fp32": 2 * D, "xu": 0, "alu": 1}
+    raise ValueError(op)
+
+
+FP32_LANES_PER_SM = 128   # Blackwell SM: 4 partitions x 32 FP32 lanes
+ALU_LANES_PER_SM = 64     # integer/compare pipe: 4 partitions x 16 lanes
+
+# DRAM traffic per launch from ncu captures (profiles/), keyed by kernel and the
+# hash of the kernel source it was taken on; stale entries report null.
+TRAFFIC = {}
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("kr_kernels.cuh", "kr_config.h"):
+        with open(os.path.join(ROOT, "symbolic_matrix_reductions_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in getattr(self, "lines", []):
+            p = [s.strip() for s in l.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                rows.append((float(p[1]), float(p[2]), p[5], p[6], p[7], p[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = np.array([r[0] for r in rows])
+        smax = max(r[1] for r in rows)
+        load = sm[sm >= 0.5 * smax] if (sm >= 0.5 * smax).any() else sm
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[2 + k].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(load)), "sm_max_mhz": float(smax), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# pipe probe (ex2 lanes per clock per SM), measured in this run
+# ---------------------------------------------------------------------------
+def probe_pipes(torch, nsm):
+    lib = ctypes.CDLL(os.path.join(ROOT, "symbolic_matrix_reductions_gb300", "libkrprobe.so"))
+    lib.kr_probe_pipe.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 3
+    bps, iters = 4, 8192
+    blocks = nsm * bps
+    sink = torch.zeros(1, device="cuda")
+    cyc = torch.zeros(blocks, dtype=torch.int64, device="cuda")
+    res = {}
+    for kind, name, lpo in ((0, "fp32", 1), (2, "xu", 1)):
+        for _ in range(2):
+            rc = lib.kr_probe_pipe(kind, blocks, iters, ctypes.c_void_p(sink.data_ptr()),
+                                   ctypes.c_void_p(cyc.data_ptr()), None)
+            if rc != 0:
+                raise RuntimeError(f"probe launch failed: {rc}")
+            torch.cuda.synchronize()
+        c = cyc.double().mean().item()
+        res[name] = bps * 256 * iters * 8 * lpo / c
+    return res  # lanes per clock per SM
+
+
+def roofline(op, D, E, seconds_per_launch, pairs, nsm, clk_mhz, xu_lanes, kernel, live_mhz=None):
+    n = ops_per_pair(op, D, E)
+
+    def peak_at(mhz):
+        f = mhz * 1e6
+        t = max(n["fp32"] / (nsm * FP32_LANES_PER_SM * f),
+                n["xu"] / (nsm * xu_lanes * f) if n["xu"] else 0.0,
+                n["alu"] / (nsm * ALU_LANES_PER_SM * f) if n["alu"] else 0.0)
+        return 1.0 / t
+
+    peak = peak_at(clk_mhz)
+    achieved = pairs / seconds_per_launch
+    pipe = "xu" if n["xu"] / xu_lanes > n["fp32"] / FP32_LANES_PER_SM else "fp32"
+    tr = TRAFFIC.get(kernel)
+    traffic = tr["bytes_per_launch"] if tr and tr.get("source_hash") == _kernel_source_hash() else None
+    out = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+           "traffic": traffic, "kernel": kernel, "limiting_pipe": pipe, "ops_per_pair": n,
+           "peak_basis": f"{nsm} SMs x (128 FP32, {xu_lanes:.1f} ex2 measured, 64 ALU) lanes/clk x {clk_mhz:.0f} MHz max SM clock"}
+    if live_mhz:
+        out["frac_at_live_clock"] = achieved / peak_at(live_mhz)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import symbolic_matrix_reductions_gb300 as kr
+    from symbolic_matrix_reductions_gb300 import build, workloads as W
+
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    kr.load_library()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    max_mhz = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("sm_max_mhz", 2070.0)) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 2070.0
+
+    inp = W.generate(args.workload)
+    x, y, b, g = (torch.from_numpy(inp[k]).to(dev) for k in ("x", "y", "b", "g"))
+    M, D = x.shape
+    N, E = y.shape[0], b.shape[1]
+    s = inp["sigma"]
+    a = torch.empty((M, E), device=dev)
+    L = torch.empty((M, E), device=dev)
+    gx = torch.empty((M, D), device=dev)
+    idx = torch.empty((M, K_NN), dtype=torch.int32, device=dev)
+    dist_ = torch.empty((M, K_NN), device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ops = [("sum", lambda: kr.kernel_reduce(x, y, b, s, "sum", out=a)),
+           ("lse", lambda: kr.kernel_reduce(x, y, b, s, "lse", out=L)),
+           ("grad", lambda: kr.kernel_reduce_grad_x(x, y, b, g, s, out=gx)),
+           ("knn", lambda: kr.kernel_knn(x, y, K_NN, idx=idx, dist=dist_))]
+    op_code = {"sum": kr.OP_SUM, "lse": kr.OP_LSE, "grad": kr.OP_GRAD, "knn": kr.OP_KNN}
+    plans = {name: kr.plan_device(op_code[name], M, N, D, K_NN if name == "knn" else E) for name, _ in ops}
+    launches_per_step = sum(1 + (plans[n].split > 1) for n, _ in ops)
+    pairs_per_step = len(ops) * M * N
+
+    for _ in range(args.warmup):
+        for _, fn in ops:
+            fn()
+    torch.cuda.synchronize(dev)
+    xu_lanes = probe_pipes(torch, nsm)["xu"] if rank == 0 else 16.0
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clk:
+        t_wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            for o, (_, fn) in enumerate(ops):
+                fn()
+                ev[k][o + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(args.steps)]
+    op_ms = {name: float(np.mean([ev[k][o].elapsed_time(ev[k][o + 1]) for k in range(args.steps)]))
+             for o, (name, _) in enumerate(ops)}
+    total_ms = float(np.sum(step_ms))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * pairs_per_step / (ms_per_step / 1e3)
+    clocks = clk.summary()
+
+    e2e_line = e2e(torch, kr, inp, s, args, world)
+    if rank != 0:
+        return None
+
+    dominant = max(op_ms, key=op_ms.get)
+    kname = {"sum": "fwd_kernel<Sum>", "lse": "fwd_kernel<LSE>", "grad": "grad_kernel",
+             "knn": "knn_kernel"}[dominant]
+    kname += f"[D={D},E={E if dominant != 'knn' else K_NN}]"
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {W.WORKLOADS[args.workload].note}; step = Sum + LogSumExp "
+                               f"(b as log-weight) + grad-x (g~N(0,1)) + K-min (K={K_NN})",
+                   "M": M, "N": N, "D": D, "E": E, "K": K_NN, "sigma": s,
+                   "pairs_per_step": pairs_per_step, "l2": "flushed before every timed step (256 MB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "splits": {n: plans[n].split for n, _ in ops}},
+        "per_op_ms": op_ms,
+        "roofline": roofline(dominant, D, E, op_ms[dominant] / 1e3, M * N, nsm, max_mhz, xu_lanes, kname,
+                             clocks.get("sm_mhz")),
+        "per_op_frac": {n: roofline(n, D, E, op_ms[n] / 1e3, M * N, nsm, max_mhz, xu_lanes, n)["frac"]
+                        for n, _ in ops},
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+        "pipe_probe_lanes_per_clk_per_sm": {"xu_ex2": xu_lanes},
+        "wall_s_timed": t_wall,
+    }
+    line["e2e"] = e2e_line
+    if world == 1:
+        line["secondary"] = secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev)
+        line["cpu_baseline"] = cpu_baseline(inp, s, target_s=args.cpu_seconds)
+    return line
+
+
+def e2e(torch, kr, inp, s, args, world):
+    """The same step through the C ABI with pinned host buffers (every rank)."""
+    xc, yc, bc, gc = (torch.from_numpy(inp[k]).pin_memory() for k in ("x", "y", "b", "g"))
+    M, D = xc.shape
+    N, E = yc.shape[0], bc.shape[1]
+    a = torch.empty((M, E)).pin_memory()
+    L = torch.empty((M, E)).pin_memory()
+    gx = torch.empty((M, D)).pin_memory()
+    idx = torch.empty((M, K_NN), dtype=torch.int32).pin_memory()
+    dist_ = torch.empty((M, K_NN)).pin_memory()
+
+    def step():
+        kr.kernel_reduce(xc, yc, bc, s, "sum", out=a)
+        kr.kernel_reduce(xc, yc, bc, s, "lse", out=L)
+        kr.kernel_reduce_grad_x(xc, yc, bc, gc, s, out=gx)
+        kr.kernel_knn(xc, yc, K_NN, idx=idx, dist=dist_)
+
+    nb = lambda t: t.numel() * t.element_size()
+    h2d = 4 * (nb(xc) + nb(yc)) + 3 * nb(bc) + nb(gc)
+    d2h = nb(a) + nb(L) + nb(gx) + nb(idx) + nb(dist_)
+    for _ in range(max(1, args.warmup)):
+        step()
+    steps = max(1, args.steps)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    t = (time.perf_counter() - t0) / steps
+    if world > 1:
+        tt = torch.tensor([t], dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t = float(tt.item())
+    return {"value": world * 4 * M * N / t, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": t * 1e3, "steps": steps, "timer": "host perf_counter; each call blocks on host outputs"}
+
+
+def _time_op(torch, fn, reps):
+    fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return float(np.mean(ts))
+
+
+def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
+    """One timed set (1 warm-up + 2 runs) per other workload, with its roofline."""
+    out = []
+    plan = [("gauss_d3_unit", [("sum", "b"), ("lse", "w_log")]), ("falkon_d50", [("sum", "b")]),
+            ("knn_d16", [("knn", None)])]
+    for wname, ops in plan:
+        inp = W.generate(wname)
+        x, y = (torch.from_numpy(inp[k]).to(dev) for k in ("x", "y"))
+        M, D = x.shape
+        N = y.shape[0]
+        s = inp["sigma"]
+        for op, key in ops:
+            if op == "knn":
+                K = inp["K"]
+                fn = (lambda: kr.kernel_knn(x, y, K))
+                p = kr.plan_device(kr.OP_KNN, M, N, D, K)
+                kname = f"knn_kernel[D={D},K={K}]"
+                E = 1
+            else:
+                bb = torch.from_numpy(inp[key]).to(dev)
+                E = bb.shape[1]
+                fn = (lambda bb=bb, op=op: kr.kernel_reduce(x, y, bb, s, op))
+                p = kr.plan_device(kr.OP_SUM if op == "sum" else kr.OP_LSE, M, N, D, E)
+                kname = f"fwd_kernel<{'Sum' if op == 'sum' else 'LSE'}>[D={D},E={E}]"
+            ms = _time_op(torch, fn, 2)
+            out.append({"workload": f"{wname}: {W.WORKLOADS[wname].note}", "op": op, "ms": ms,
+                        "value": M * N / (ms / 1e3), "unit": UNIT, "split": p.split,
+                        "roofline": roofline(op, D, E, ms / 1e3, M * N, nsm, max_mhz, xu_lanes, kname)})
+        del x, y
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline / reference arm: the fp64 oracle, as it stands
+# ---------------------------------------------------------------------------
+def _oracle_step(orc, inp, s, rows):
+    x = inp["x"][rows]
+    orc.gauss_sum(x, inp["y"], inp["b"], s)
+    orc.gauss_lse(x, inp["y"], inp["b"], s)
+    orc.gauss_grad_x(x, inp["y"], inp["b"], inp["g"][rows], s)
+    orc.knn(x, inp["y"], K_NN)
+
+
+def _oracle_rows_for(orc, inp, s, target_s):
+    M = inp["x"].shape[0]
+    r0 = 16
+    t0 = time.perf_counter()
+    _oracle_step(orc, inp, s, np.arange(r0))
+    dt = time.perf_counter() - t0
+    return int(min(M, max(r0, r0 * target_s / max(dt, 1e-6))))
+
+
+def cpu_baseline(inp, s, target_s=15.0):
+    import oracle
+    orc = oracle.load()
+    r = _oracle_rows_for(orc, inp, s, target_s)
+    rows = np.arange(r)
+    t0 = time.perf_counter()
+    _oracle_step(orc, inp, s, rows)
+    t = time.perf_counter() - t0
+    N = inp["y"].shape[0]
+    return {"value": 4 * r * N / t, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"first {r} rows of the step's batch, full N={N}: Sum + LSE + grad-x + K-min "
+                      f"(K={K_NN}) in fp64, {t:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    from symbolic_matrix_reductions_gb300 import workloads as W
+    orc = oracle.load()
+    inp = W.generate(args.workload)
+    s = inp["sigma"]
+    N = inp["y"].shape[0]
+    per_step = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    r = _oracle_rows_for(orc, inp, s, per_step)
+    rows = np.arange(r)
+    for _ in range(args.warmup):
+        _oracle_step(orc, inp, s, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(orc, inp, s, rows)
+    t = (time.perf_counter() - t0) / max(1, args.steps)
+    value = 4 * r * N / t
+    sample = f"first {r} rows of the {args.workload} batch per step, full N={N}: Sum + LSE + grad-x + K-min in fp64"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {W.WORKLOADS[args.workload].note}", "rows_per_step": r},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=PRIMARY, help="workload of the step (default: gauss_d3)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the CPU baseline sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3   # at least three warm-up steps
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+
+    line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,267 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Small cases span several tiles and row blocks with ragged tails, every kernel
+family and the split-j combine; the workload cases run the full configuration
+on the GPU (the launch the benchmark times) and check a seeded row subset with
+the full N against the oracle.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import symbolic_matrix_reductions_gb300 as kr
+from symbolic_matrix_reductions_gb300 import workloads as W
+
+from parity import check_grad, check_knn, check_lse, check_sum
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from symbolic_matrix_reductions_gb300 import build
+    build.build()
+    kr.load_library()
+
+
+def _rng(seed):
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def _dev(*arrs):
+    return [torch.from_numpy(np.ascontiguousarray(a)).to(DEV) for a in arrs]
+
+
+def _np(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def _case(seed, M, N, D, E, scale=1.0):
+    r = _rng(seed)
+    x = (r.standard_normal((M, D)) * scale).astype(np.float32)
+    y = (r.standard_normal((N, D)) * scale).astype(np.float32)
+    b = r.standard_normal((N, E)).astype(np.float32)
+    g = r.standard_normal((M, E)).astype(np.float32)
+    return x, y, b, g
+
+
+# (M, N, D, E, sigma, split): tails around the 512-row block and the tile sizes,
+# padded coordinate counts (5 -> 8, 20 -> 32, 70 -> 128), padded signal columns.
+SMALL = [
+    (1, 1, 3, 1, 1.0, 0), (33, 7, 3, 1, 0.7, 0), (513, 1537, 3, 1, 0.5, 0), (1100, 2049, 3, 1, 0.9, 1),
+    (1100, 2049, 3, 1, 0.9, 5), (700, 3000, 1, 1, 0.3, 0), (257, 1000, 2, 2, 1.5, 0), (300, 777, 4, 3, 1.0, 3),
+    (300, 1001, 5, 1, 1.2, 0), (129, 600, 16, 1, 2.0, 0), (200, 513, 16, 4, 3.0, 2), (150, 300, 20, 5, 2.5, 0),
+    (100, 257, 50, 1, 3.0, 0), (100, 300, 50, 1, 3.0, 4), (64, 200, 64, 2, 4.0, 0), (40, 100, 70, 1, 5.0, 0),
+    (40, 65, 128, 16, 6.0, 2), (90, 130, 8, 16, 1.5, 0),
+]
+
+
+@pytest.mark.parametrize("M,N,D,E,sigma,split", SMALL)
+def test_sum_small(orc, M, N, D, E, sigma, split):
+    x, y, b, _ = _case(M * 7 + N + D, M, N, D, E)
+    a = kr.kernel_reduce(*_dev(x, y, b), sigma, "sum", split=split)
+    a_ref, S_ref = orc.gauss_sum(x, y, b, sigma)
+    check_sum(_np(a), a_ref, S_ref, f"{M}x{N} D{D} E{E} S{split}")
+
+
+@pytest.mark.parametrize("M,N,D,E,sigma,split", SMALL)
+def test_lse_small(orc, M, N, D, E, sigma, split):
+    x, y, w, _ = _case(M * 5 + N + D, M, N, D, E)
+    L = kr.kernel_reduce(*_dev(x, y, w), sigma, "lse", split=split)
+    check_lse(_np(L), orc.gauss_lse(x, y, w, sigma), f"{M}x{N} D{D} E{E} S{split}")
+
+
+@pytest.mark.parametrize("M,N,D,E,sigma,split", SMALL)
+def test_grad_small(orc, M, N, D, E, sigma, split):
+    x, y, b, g = _case(M * 3 + N + D, M, N, D, E)
+    gx = kr.kernel_reduce_grad_x(*_dev(x, y, b, g), sigma, split=split)
+    gx_ref, G_ref = orc.gauss_grad_x(x, y, b, g, sigma)
+    check_grad(_np(gx), gx_ref, G_ref, f"{M}x{N} D{D} E{E} S{split}")
+
+
+KNN_SMALL = [
+    (1, 1, 3, 1, 0), (33, 7, 3, 10, 0), (513, 1537, 3, 10, 0), (513, 1537, 3, 10, 6), (300, 2000, 16, 10, 0),
+    (300, 2000, 16, 10, 3), (200, 900, 1, 4, 0), (100, 700, 5, 3, 0), (90, 1000, 50, 16, 2), (70, 300, 128, 32, 0),
+    (64, 100, 8, 1, 0), (64, 100, 8, 1, 4), (50, 20, 2, 32, 0),   # last: K > N
+]
+
+
+@pytest.mark.parametrize("M,N,D,K,split", KNN_SMALL)
+def test_knn_small(orc, M, N, D, K, split):
+    x, y, _, _ = _case(M + 11 * N + D, M, N, D, 1)
+    idx, dist = kr.kernel_knn(*_dev(x, y), K, split=split)
+    i_ref, d_ref, n_ref = orc.knn(x, y, K)
+    check_knn(_np(idx), _np(dist), x, y, i_ref, d_ref, n_ref, f"{M}x{N} D{D} K{K} S{split}")
+
+
+def test_knn_ties_lowest_index(orc):
+    """Integer grid points with many exact duplicates: ties must keep the lowest index."""
+    r = _rng(5)
+    y = r.integers(-3, 4, size=(3000, 3)).astype(np.float32)
+    x = r.integers(-3, 4, size=(400, 3)).astype(np.float32)
+    for split in (0, 1, 7):
+        idx, dist = kr.kernel_knn(*_dev(x, y), 10, split=split)
+        i_ref, d_ref, _ = orc.knn(x, y, 10)
+        assert np.array_equal(_np(idx), i_ref), f"split {split}"   # integer distances are exact
+        assert np.array_equal(_np(dist), d_ref.astype(np.float32))
+
+
+def test_lse_far_rows_and_extreme_weights(orc):
+    """Rows far from every point (all kernel values underflow in the tile frame),
+    weights shifted by +-1000, and zero weights (log-weight -inf)."""
+    r = _rng(6)
+    y = r.standard_normal((2000, 3)).astype(np.float32)
+    x = np.concatenate([r.standard_normal((200, 3)), 40 + r.standard_normal((100, 3))]).astype(np.float32)
+    w = r.standard_normal((2000, 2)).astype(np.float32)
+    for shift in (0.0, 1000.0, -1000.0):
+        ws = (w + shift).astype(np.float32)
+        L = kr.kernel_reduce(*_dev(x, y, ws), 0.5, "lse")
+        check_lse(_np(L), orc.gauss_lse(x, y, ws, 0.5), f"shift {shift}")
+    w2 = w.copy()
+    w2[::3, 0] = -np.inf
+    w2[:, 1] = -np.inf
+    w2[1500:1600, 1] = 0.0
+    L = kr.kernel_reduce(*_dev(x, y, w2), 0.8, "lse", split=3)
+    check_lse(_np(L), orc.gauss_lse(x, y, w2, 0.8), "zero weights")
+
+
+def test_empty_and_degenerate(orc):
+    x, y, b, g = _case(9, 50, 0, 3, 2)
+    xt, yt, bt, gt = _dev(x, y, b, g)
+    assert (_np(kr.kernel_reduce(xt, yt, bt, 1.0, "sum")) == 0).all()
+    assert np.isneginf(_np(kr.kernel_reduce(xt, yt, bt, 1.0, "lse"))).all()
+    assert (_np(kr.kernel_reduce_grad_x(xt, yt, bt, gt, 1.0)) == 0).all()
+    idx, dist = kr.kernel_knn(xt, yt, 4)
+    assert (_np(idx) == -1).all() and np.isinf(_np(dist)).all()
+    e = torch.empty((0, 3), device=DEV)
+    assert kr.kernel_reduce(e, yt, bt, 1.0).shape == (0, 2)
+    # x_i = y_j, N = 1: a = b exactly (k = 2^0 = 1)
+    p = _rng(1).standard_normal((1, 3)).astype(np.float32)
+    bb = np.array([[1.25, -3.5]], dtype=np.float32)
+    a = _np(kr.kernel_reduce(*_dev(p, p, bb), 0.7, "sum"))
+    assert np.array_equal(a, bb)
+
+
+def test_split_and_determinism(orc):
+    x, y, b, g = _case(12, 3000, 20000, 3, 1)
+    xt, yt, bt, gt = _dev(x, y, b, g)
+
+    def run(split):
+        return [_np(kr.kernel_reduce(xt, yt, bt, 0.6, "sum", split=split)),
+                _np(kr.kernel_reduce(xt, yt, bt, 0.6, "lse", split=split)),
+                _np(kr.kernel_reduce_grad_x(xt, yt, bt, gt, 0.6, split=split)),
+                _np(kr.kernel_knn(xt, yt, 10, split=split)[0])]
+
+    outs = {}
+    for split in (1, 9):
+        outs[split] = run(split)
+        for u, v in zip(outs[split], run(split)):
+            assert np.array_equal(u, v), "run-to-run results differ"
+    # K-min selection is unique under the (d, j) order, so the split does not change it
+    assert np.array_equal(outs[1][3], outs[9][3])
+    a_ref, S_ref = orc.gauss_sum(x[:300], y, b, 0.6)
+    for split in (1, 9):
+        check_sum(outs[split][0][:300], a_ref, S_ref, f"split {split}")
+
+
+def test_host_buffers_match_device(orc):
+    """CPU tensors go through the library's staging path and give the same bits."""
+    x, y, b, g = _case(13, 1000, 5000, 3, 1)
+    xt, yt, bt, gt = _dev(x, y, b, g)
+    xc, yc, bc, gc = (torch.from_numpy(a) for a in (x, y, b, g))
+    assert np.array_equal(kr.kernel_reduce(xc, yc, bc, 0.8, "sum").numpy(),
+                          _np(kr.kernel_reduce(xt, yt, bt, 0.8, "sum")))
+    assert np.array_equal(kr.kernel_reduce_grad_x(xc, yc, bc, gc, 0.8).numpy(),
+                          _np(kr.kernel_reduce_grad_x(xt, yt, bt, gt, 0.8)))
+    pinned = [t.pin_memory() for t in (xc, yc)]
+    i_host, d_host = kr.kernel_knn(*pinned, 5)
+    i_dev, d_dev = kr.kernel_knn(xt, yt, 5)
+    assert np.array_equal(i_host.numpy(), _np(i_dev)) and np.array_equal(d_host.numpy(), _np(d_dev))
+
+
+def test_workspace_allocation_failure_leaves_output_untouched():
+    x, y, b, _ = _case(14, 500, 4000, 3, 1)
+    xt, yt, bt = _dev(x, y, b)
+    out = torch.full((500, 1), 7.0, device=DEV)
+    os.environ["KREDUCE_FAIL_ALLOC"] = "1"
+    try:
+        with pytest.raises(kr.KrError) as ei:
+            kr.kernel_reduce(xt, yt, bt, 1.0, "sum", out=out, split=4)
+        assert ei.value.status == kr.KR_ERR_ALLOC
+    finally:
+        del os.environ["KREDUCE_FAIL_ALLOC"]
+    assert (_np(out) == 7.0).all()
+    kr.kernel_reduce(xt, yt, bt, 1.0, "sum", out=out, split=4)   # works again
+    assert not (_np(out) == 7.0).all()
+
+
+def test_autograd_readme_example(orc):
+    """KeOps README usage example: a = K.sum(dim=1), grad of sum(a^2) wrt x."""
+    inp = W.generate("gauss_small")
+    x = torch.from_numpy(inp["x"]).to(DEV).requires_grad_(True)
+    y, b = _dev(inp["y"], inp["b"])
+    a = kr.GaussianSum.apply(x, y, b, inp["sigma"])
+    (gx,) = torch.autograd.grad((a ** 2).sum(), [x])
+    a_ref, S_ref = orc.gauss_sum(inp["x"], inp["y"], inp["b"], inp["sigma"])
+    check_sum(_np(a.detach()), a_ref, S_ref, "gauss_small")
+    gx_ref, G_ref = orc.gauss_grad_x(inp["x"], inp["y"], inp["b"], 2 * _np(a.detach()), inp["sigma"])
+    check_grad(_np(gx), gx_ref, G_ref, "gauss_small grad of sum(a^2)")
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: the GPU runs every row, the oracle a seeded subset
+# ---------------------------------------------------------------------------
+def test_workload_gauss_d3(orc):
+    inp = W.generate("gauss_d3")
+    s = inp["sigma"]
+    xt, yt, bt, gt = _dev(inp["x"], inp["y"], inp["b"], inp["g"])
+    a = _np(kr.kernel_reduce(xt, yt, bt, s, "sum"))
+    gx = _np(kr.kernel_reduce_grad_x(xt, yt, bt, gt, s))
+    rows = W.row_subset(inp["x"].shape[0], 2048, 7)
+    a_ref, S_ref = orc.gauss_sum(inp["x"][rows], inp["y"], inp["b"], s)
+    check_sum(a[rows], a_ref, S_ref, "gauss_d3")
+    gx_ref, G_ref = orc.gauss_grad_x(inp["x"][rows], inp["y"], inp["b"], inp["g"][rows], s)
+    check_grad(gx[rows], gx_ref, G_ref, "gauss_d3")
+
+
+def test_workload_gauss_d3_unit(orc):
+    inp = W.generate("gauss_d3_unit")
+    s = inp["sigma"]
+    xt, yt, bt, wt = _dev(inp["x"], inp["y"], inp["b"], inp["w_log"])
+    a = _np(kr.kernel_reduce(xt, yt, bt, s, "sum"))
+    L = _np(kr.kernel_reduce(xt, yt, wt, s, "lse"))
+    rows = W.row_subset(inp["x"].shape[0], 512, 8)
+    a_ref, S_ref = orc.gauss_sum(inp["x"][rows], inp["y"], inp["b"], s)
+    check_sum(a[rows], a_ref, S_ref, "gauss_d3_unit")
+    check_lse(L[rows], orc.gauss_lse(inp["x"][rows], inp["y"], inp["w_log"], s), "gauss_d3_unit")
+    # LogSumExp of log b equals log of the Sum of b (b > 0)
+    assert np.max(np.abs(L[rows] - np.log(a_ref))) < 1e-4
+
+
+def test_workload_falkon_d50(orc):
+    inp = W.generate("falkon_d50")
+    s = inp["sigma"]
+    xt, yt, bt = _dev(inp["x"], inp["y"], inp["b"])
+    a = _np(kr.kernel_reduce(xt, yt, bt, s, "sum"))
+    p = kr.plan_device(kr.OP_SUM, inp["x"].shape[0], inp["y"].shape[0], 50, 1)
+    assert p.split > 1, "the tall product must run in split-j mode"
+    rows = W.row_subset(inp["x"].shape[0], 1000, 9)
+    a_ref, S_ref = orc.gauss_sum(inp["x"][rows], inp["y"], inp["b"], s)
+    check_sum(a[rows], a_ref, S_ref, "falkon_d50")
+
+
+def test_workload_knn_d16(orc):
+    inp = W.generate("knn_d16")
+    xt, yt = _dev(inp["x"], inp["y"])
+    idx, dist = kr.kernel_knn(xt, yt, inp["K"])
+    rows = W.row_subset(inp["x"].shape[0], 1024, 10)
+    i_ref, d_ref, n_ref = orc.knn(inp["x"][rows], inp["y"], inp["K"])
+    ties = check_knn(_np(idx)[rows], _np(dist)[rows], inp["x"][rows], inp["y"], i_ref, d_ref, n_ref, "knn_d16")
+    print(f"knn_d16: {ties} near-tie positions of {i_ref.size}")
