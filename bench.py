@@ -136,23 +136,32 @@ class ClockSampler:
 # pipe probe (ex2 lanes per clock per SM), measured in this run
 # ---------------------------------------------------------------------------
 def probe_pipes(torch, nsm):
+    """ex2 lanes per clock per SM, from the ex2 : FFMA throughput ratio of the pipe
+    probe (both timed with CUDA events back to back, so the SM clock cancels) times
+    the 128 FP32 lanes of an SM; reported raw and rounded to the power of two the
+    hardware has."""
     lib = ctypes.CDLL(os.path.join(ROOT, "symbolic_matrix_reductions_gb300", "libkrprobe.so"))
     lib.kr_probe_pipe.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 3
     bps, iters = 4, 8192
     blocks = nsm * bps
     sink = torch.zeros(1, device="cuda")
     cyc = torch.zeros(blocks, dtype=torch.int64, device="cuda")
-    res = {}
-    for kind, name, lpo in ((0, "fp32", 1), (2, "xu", 1)):
-        for _ in range(2):
-            rc = lib.kr_probe_pipe(kind, blocks, iters, ctypes.c_void_p(sink.data_ptr()),
-                                   ctypes.c_void_p(cyc.data_ptr()), None)
-            if rc != 0:
-                raise RuntimeError(f"probe launch failed: {rc}")
-            torch.cuda.synchronize()
-        c = cyc.double().mean().item()
-        res[name] = bps * 256 * iters * 8 * lpo / c
-    return res  # lanes per clock per SM
+    ms = {}
+    for kind in (0, 2, 0, 2):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        rc = lib.kr_probe_pipe(kind, blocks, iters, ctypes.c_void_p(sink.data_ptr()),
+                               ctypes.c_void_p(cyc.data_ptr()), None)
+        e1.record()
+        if rc != 0:
+            raise RuntimeError(f"probe launch failed: {rc}")
+        torch.cuda.synchronize()
+        ms[kind] = e0.elapsed_time(e1)          # the second run of each kind is kept
+    ratio = ms[0] / ms[2]                       # same lane count in both probes
+    measured = FP32_LANES_PER_SM * ratio
+    return {"xu": float(2 ** round(np.log2(measured))), "xu_measured": measured, "ex2_to_ffma": ratio,
+            "ffma_lanes_per_s": nsm * bps * 256 * iters * 8 / (ms[0] / 1e3)}
 
 
 def roofline(op, D, E, seconds_per_launch, pairs, nsm, clk_mhz, xu_lanes, kernel, live_mhz=None):
@@ -172,7 +181,7 @@ def roofline(op, D, E, seconds_per_launch, pairs, nsm, clk_mhz, xu_lanes, kernel
     traffic = tr["bytes_per_launch"] if tr and tr.get("source_hash") == _kernel_source_hash() else None
     out = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
            "traffic": traffic, "kernel": kernel, "limiting_pipe": pipe, "ops_per_pair": n,
-           "peak_basis": f"{nsm} SMs x (128 FP32, {xu_lanes:.1f} ex2 measured, 64 ALU) lanes/clk x {clk_mhz:.0f} MHz max SM clock"}
+           "peak_basis": f"{nsm} SMs x (128 FP32, {xu_lanes:.0f} ex2, 64 ALU) lanes/clk x {clk_mhz:.0f} MHz max SM clock"}
     if live_mhz:
         out["frac_at_live_clock"] = achieved / peak_at(live_mhz)
     return out
@@ -226,7 +235,8 @@ def run_ours(args, rank, world, local_rank):
         for _, fn in ops:
             fn()
     torch.cuda.synchronize(dev)
-    xu_lanes = probe_pipes(torch, nsm)["xu"] if rank == 0 else 16.0
+    probe = probe_pipes(torch, nsm) if rank == 0 else {"xu": 32.0}
+    xu_lanes = probe["xu"]
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
     if world > 1:
@@ -264,7 +274,7 @@ def run_ours(args, rank, world, local_rank):
     dominant = max(op_ms, key=op_ms.get)
     kname = {"sum": "fwd_kernel<Sum>", "lse": "fwd_kernel<LSE>", "grad": "grad_kernel",
              "knn": "knn_kernel"}[dominant]
-    kname += f"[D={D},E={E if dominant != 'knn' else K_NN}]"
+    kname += f"[D={D},K={K_NN}]" if dominant == "knn" else f"[D={D},E={E}]"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -282,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
                         for n, _ in ops},
         "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
-        "pipe_probe_lanes_per_clk_per_sm": {"xu_ex2": xu_lanes},
+        "pipe_probe": probe,
         "wall_s_timed": t_wall,
     }
     line["e2e"] = e2e_line
