@@ -102,6 +102,31 @@ int kernel_reduce_ex(const float *x, const float *y, const float *b, float *out,
                      kr_stream_t stream, const kr_options *opt);
 
 /*
+ * kernel_reduce without any device allocation.  The pages have no counterpart to
+ * this entry point; it exists for callers that cannot allocate device memory when
+ * they call -- a process whose own memory arena already holds (almost) all of the
+ * GPU, so cudaMalloc / cudaMallocAsync would fail, or a latency-critical loop that
+ * must not wait on the driver's allocator.  Same arguments and result as
+ * kernel_reduce, always in split-j mode, with the split partials kept in a 16 MiB
+ * static device array that every GPU loading this library reserves until exit.
+ *   - All four arrays must be device (or managed) memory; host arrays, which would
+ *     need staging memory, give KR_ERR_INVALID.
+ *   - Limit: M * E <= 1048576 (two splits of partials must fit the 16 MiB array);
+ *     larger requests give KR_ERR_UNSUPPORTED.  Use kernel_reduce for them.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream
+ *     capture.  A failed lookup gives KR_ERR_CUDA (kr_last_cuda_error is not set
+ *     by this entry point).
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents; each call overwrites every partial it reads, so nothing needs
+ *     clearing, but calls whose work overlaps on the GPU (different streams, or
+ *     threads without ordering between them) race on it and must be serialised.
+ */
+int kernel_reduce_noalloc(const float *x, const float *y, const float *b, float *out,
+                          int64_t M, int64_t N, int D, int E, float sigma, int reduction,
+                          kr_stream_t stream);
+
+/*
  * Gradient wrt x of sum_{i,e} g_ie a_ie, a the Sum reduction (KeOps README usage
  * example: torch.autograd.grad((a_i ** 2).sum(), [x]), i.e. g = 2a).
  *   x [M x D], y [N x D], b [N x E], g [M x E] (upstream gradient), gx [M x D] output.

@@ -34,7 +34,8 @@ KR_OK, KR_ERR_INVALID, KR_ERR_UNSUPPORTED, KR_ERR_ALLOC, KR_ERR_CUDA = 0, 1, 2, 
 OP_SUM, OP_LSE, OP_GRAD, OP_KNN = 0, 1, 2, 3
 
 # Names exported by libkreduce.so, in the order include/kreduce.h declares them.
-EXPORTS = ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_grad_x", "kernel_reduce_grad_x_ex",
+EXPORTS = ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_noalloc", "kernel_reduce_grad_x",
+           "kernel_reduce_grad_x_ex",
            "kernel_knn", "kernel_knn_ex", "kr_status_string", "kr_last_cuda_error", "kr_plan",
            "kr_plan_device")
 
@@ -80,6 +81,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         opt = ctypes.POINTER(KrOptions)
         lib.kernel_reduce.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
         lib.kernel_reduce_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp, opt]
+        lib.kernel_reduce_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
         lib.kernel_reduce_grad_x.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
         lib.kernel_reduce_grad_x_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
         lib.kernel_knn.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp]
@@ -89,7 +91,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kr_last_cuda_error.argtypes = []
         lib.kr_plan.argtypes = [i32, i64, i64, i32, i32, i32, i32, opt, ctypes.POINTER(KrPlan)]
         lib.kr_plan_device.argtypes = [i32, i64, i64, i32, i32, opt, ctypes.POINTER(KrPlan)]
-        for name in ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_grad_x", "kernel_reduce_grad_x_ex",
+        for name in ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_noalloc", "kernel_reduce_grad_x",
+                     "kernel_reduce_grad_x_ex",
                      "kernel_knn", "kernel_knn_ex", "kr_last_cuda_error", "kr_plan", "kr_plan_device"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -197,6 +200,30 @@ def kernel_reduce(x, y, b, sigma: float, reduction: str = "sum", out=None, split
     st = load_library().kernel_reduce_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(out2), M, N, D, E, float(sigma), red,
                                          _stream(dev), _options(split))
     _check(st, "kernel_reduce")
+    return out
+
+
+def kernel_reduce_noalloc(x, y, b, sigma: float, reduction: str, out):
+    """kernel_reduce for callers that cannot allocate device memory at call time.
+
+    The library allocates nothing: the split partials live in its 16 MiB static
+    device array.  x, y, b and the caller's ``out`` (M, E) must be CUDA tensors;
+    M * E may not exceed 1048576.  Calls that overlap on the GPU race on the shared
+    array.  Returns ``out``."""
+    red = {"sum": KR_SUM, "lse": KR_LSE}.get(reduction)
+    if red is None:
+        raise ValueError(f"reduction must be 'sum' or 'lse', got {reduction!r}")
+    x = _mat(x, None, "x")
+    M, D = x.shape
+    y = _mat(y, None, "y", D)
+    N = y.shape[0]
+    b = _mat(b, N, "b")
+    E = b.shape[1]
+    out2 = _mat(out, M, "out", E)
+    dev = _same_device(x, y, b, out2)
+    st = load_library().kernel_reduce_noalloc(_ptr(x), _ptr(y), _ptr(b), _ptr(out2), M, N, D, E, float(sigma),
+                                              red, _stream(dev))
+    _check(st, "kernel_reduce_noalloc")
     return out
 
 
