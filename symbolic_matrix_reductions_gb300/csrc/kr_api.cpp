@@ -4,11 +4,14 @@
 // Planning: a launch is a grid of (row blocks, S) blocks.  A row block owns
 // kThreads * R rows; S splits the j axis into S disjoint ranges whose partial
 // results a second kernel combines in a fixed order (split-j).  S is chosen to
-// minimise the modelled time  waves(S) * (chunk(S) + tile overhead) where
-// waves = ceil(row_blocks * S / (SMs * resident blocks)), so that small-M /
-// huge-N problems (the tall products of the GitHub issue "Transparent interface
-// for billion-scale matrices") still fill every SM, and the last wave of a large
-// problem is not left mostly empty.
+// minimise a model of the busiest SM's time: it runs ceil(blocks / SMs) blocks of
+// (chunk + per-tile overhead [+ K-min insertions]) work each, at full rate when it
+// holds at least 16 resident warps and proportionally slower below that.  So
+// small-M / huge-N problems (the tall products of the GitHub issue "Transparent
+// interface for billion-scale matrices") still fill every SM, the last wave of a
+// large problem is not left mostly empty, and K-min, whose register list restarts
+// in every split (early in a scan almost every point enters it), is split only
+// when the extra parallelism pays for the extra insertions.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -36,11 +39,12 @@ Instance choose_instance(int op, int D, int EK) {
     if (op == OP_KNN) {
         in.ek_pad = pad_k(EK);
         in.rows = rows_knn(in.d_pad, in.ek_pad);
-        in.tile = tile_points(pack_stride(in.d_pad, 0));
+        in.tile = instance_tile(in.d_pad, 0);
     } else {
         in.ek_pad = pad_e(EK);
         in.rows = (op == OP_GRAD) ? rows_grad(in.d_pad, in.ek_pad) : rows_fwd(in.d_pad, in.ek_pad);
-        in.tile = tile_points(pack_stride(in.d_pad, in.ek_pad));
+        in.tile = (op == OP_GRAD && !packed_grad(in.d_pad)) ? tile_points(pack_stride(in.d_pad, in.ek_pad))
+                                                            : instance_tile(in.d_pad, in.ek_pad);
     }
     return in;
 }
@@ -72,7 +76,6 @@ static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int bl
     p->row_blocks = (M + bm - 1) / bm;
     if (num_sms < 1) num_sms = 1;
     if (blocks_per_sm < 1) blocks_per_sm = 4;
-    const int64_t slots = (int64_t)num_sms * blocks_per_sm;
 
     int S = 1;
     if (forced_split >= 1) {
@@ -81,14 +84,30 @@ static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int bl
     } else if (N > 0 && p->row_blocks > 0) {
         // At least 64 points per split, at most kMaxSplit splits.
         const int64_t s_max = std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, N / 64));
+        // K-min: warp-level insertion events per row slot and split, each worth
+        // `ins_points` points of distance work (about 75 instructions against
+        // D + 1.25 per point and row for the packed kernel, 2D + 1 for the scalar).
+        const bool pk = packed(in.d_pad);
+        const double pt_cost = pk ? in.d_pad + 1.25 : 2.0 * in.d_pad + 1.0;
+        const double ins_points = 75.0 / pt_cost;
+        const double group = pk ? 2.0 * unroll_pairs(in.d_pad) : (double)unroll_points(in.d_pad);
+        const double lanes_k = 32.0 * in.ek_pad;
         double best = 0.0;
         for (int64_t s = 1; s <= s_max; ++s) {
             if (workspace_bytes(op, in, M, D, EK, (int)s) > kMaxWorkspace) break;
             const int64_t chunk = (N + s - 1) / s;
-            const int64_t waves = (p->row_blocks * s + slots - 1) / slots;
             const int64_t tiles = (chunk + in.tile - 1) / in.tile;
-            // per-tile fixed cost ~ 32 points; each split adds a small combine cost
-            const double cost = (double)waves * (double)(chunk + 32 * tiles) * (1.0 + 0.002 * (double)s);
+            double work = (double)chunk + 32.0 * (double)tiles;   // per block, in points
+            if (op == OP_KNN) {
+                const double groups = (double)chunk / group;
+                const double events = groups <= lanes_k ? groups : lanes_k * (1.0 + std::log(groups / lanes_k));
+                work += events * ins_points;
+            }
+            const int64_t per_sm = (p->row_blocks * s + num_sms - 1) / num_sms;
+            const int64_t conc = std::min<int64_t>(per_sm, blocks_per_sm);
+            const double eff = std::min(1.0, (double)(conc * (kThreads / 32)) / 16.0);
+            // each split also costs a little in partial traffic and the combine
+            const double cost = (double)per_sm * work / eff * (1.0 + 0.002 * (double)s);
             if (s == 1 || cost < best * 0.999) {
                 best = cost;
                 S = (int)s;

@@ -49,4 +49,26 @@ KR_HD constexpr int rows_knn(int DP, int KP) {
 // Inner-loop unroll over tile points (tiles are padded to a multiple of it).
 KR_HD constexpr int unroll_points(int DP) { return DP <= 8 ? 4 : DP <= 32 ? 2 : 1; }
 
+// Packed (f32x2) instances evaluate two points per instruction; they keep x'
+// duplicated in register pairs, so they are used up to D = 64.
+KR_HD constexpr bool packed(int DP) { return DP <= 64; }
+// The packed gradient also keeps 2 R D partial sums in registers: up to D = 16.
+KR_HD constexpr bool packed_grad(int DP) { return DP <= 16; }
+// Pair record: points 2m and 2m+1 of a tile interleaved field by field, so one
+// 16-byte load yields two float2 operands; rounded up to whole float4s.
+KR_HD constexpr int pair_stride(int DP, int VP) { return (2 * (DP + VP) + 3) / 4 * 4; }
+// Points per tile for pair records: a power of two, at most 512, tile <= 32 KB.
+KR_HD constexpr int tile_points_packed(int PS2) {
+    return (16384 / PS2) >= 512 ? 512 : (16384 / PS2) >= 256 ? 256 : (16384 / PS2) >= 128 ? 128
+         : (16384 / PS2) >= 64 ? 64 : 32;
+}
+// Candidate buffer of the packed K-min, entries per row (0: insert at once).
+KR_HD constexpr int knn_buffer(int DP, int KP) { return 0; }
+// Pair records per unrolled step of the packed inner loop.
+KR_HD constexpr int unroll_pairs(int DP) { return DP <= 8 ? 2 : 1; }
+// Tile points of an instance (value columns VP = E, K-min: 0).
+KR_HD constexpr int instance_tile(int DP, int VP) {
+    return packed(DP) ? tile_points_packed(pair_stride(DP, VP)) : tile_points(pack_stride(DP, VP));
+}
+
 }  // namespace kr

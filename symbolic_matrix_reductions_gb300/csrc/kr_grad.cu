@@ -1,5 +1,5 @@
 // x-gradient instances and launcher.
-#include "kr_kernels.cuh"
+#include "kr_kernels_packed.cuh"
 
 namespace kr {
 
@@ -8,7 +8,10 @@ typedef void (*KernelFn)(const Args);
 
 template <int DP, int EP>
 KernelFn grad_instance() {
-    return grad_kernel<DP, EP, rows_grad(DP, EP), tile_points(pack_stride(DP, EP))>;
+    if constexpr (packed_grad(DP))
+        return grad2_kernel<DP, EP, rows_grad(DP, EP), tile_points_packed(pair_stride(DP, EP))>;
+    else
+        return grad_kernel<DP, EP, rows_grad(DP, EP), tile_points(pack_stride(DP, EP))>;
 }
 
 template <int EP>

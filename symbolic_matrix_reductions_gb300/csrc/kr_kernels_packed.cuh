@@ -1,0 +1,571 @@
+// kr_kernels_packed.cuh -- the reduction kernels with packed fp32x2 arithmetic.
+//
+// Same scheme and same per-pair arithmetic as kr_kernels.cuh, but every FP32
+// instruction works on two points at once (FADD2 / FMUL2 / FFMA2 on register
+// pairs): the SM's FP32 lanes are the same, but a pair of points now costs half
+// the issue slots, so the FP32 pipe rather than instruction issue bounds the loop.
+//   * the tile holds pair records: points 2m and 2m+1 interleaved field by field
+//     (the coordinates are stored negated, -y', so x' - y' is one FADD2);
+//   * each thread keeps its rows as (x'_d, x'_d) register pairs;
+//   * the per-point partial sums of even and odd points are kept in the two
+//     halves of a float2 and added once per tile.
+// Used for D <= 64 (register pairs of x' cost 2 R D registers).
+#pragma once
+
+#include "kr_kernels.cuh"
+
+namespace kr {
+
+// Reads one pair record (PS2 floats, 16-byte aligned) as PS2/2 float2 fields.
+template <int PS2>
+__device__ __forceinline__ void load_pair_record(const float *rec, float2 (&pv)[PS2 / 2]) {
+    const float4 *p4 = reinterpret_cast<const float4 *>(rec);
+#pragma unroll
+    for (int k = 0; k < PS2 / 4; ++k) {
+        const float4 v = p4[k];
+        pv[2 * k + 0] = make_float2(v.x, v.y);
+        pv[2 * k + 1] = make_float2(v.z, v.w);
+    }
+}
+
+// Rows of x owned by this thread, times `scale`, as duplicated register pairs.
+template <int DP, int R>
+__device__ __forceinline__ void load_rows_pairs(const Args &a, int64_t row0, float2 (&x2)[R][DP], float scale) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t i = row0 + (int64_t)r * kThreads + threadIdx.x;
+#pragma unroll
+        for (int d = 0; d < DP; ++d) {
+            const float v = (i < a.M && d < a.D) ? scale * __ldg(a.x + i * a.D + d) : 0.f;
+            x2[r][d] = make_float2(v, v);
+        }
+    }
+}
+
+// Field slot of point p: record p/2, half p%2.
+template <int PS2>
+__device__ __forceinline__ float *pair_slot(float *tile, int p, int field) {
+    return tile + (p >> 1) * PS2 + 2 * field + (p & 1);
+}
+
+// Coordinates of points [jt, jt + nv) into pair records, times `scale`; padding
+// points [nv, nvp) get coordinate 0 = `pad0` and zeros.
+template <int DP, int PS2>
+__device__ __forceinline__ void stage_coords_pairs(const Args &a, float *tile, int64_t jt, int nv, int nvp,
+                                                   float scale, float pad0) {
+    for (int p = threadIdx.x; p < nvp; p += kThreads) {
+        if (p < nv) {
+            const float *src = a.y + (jt + p) * a.D;
+#pragma unroll
+            for (int d = 0; d < DP; ++d)
+                if (d < a.D) *pair_slot<PS2>(tile, p, d) = scale * __ldg(src + d);
+        } else {
+#pragma unroll
+            for (int d = 0; d < DP; ++d)
+                if (d < a.D) *pair_slot<PS2>(tile, p, d) = (d == 0) ? pad0 : 0.f;
+        }
+    }
+}
+
+template <int DP, int PS2, int BN>
+__device__ __forceinline__ void zero_pad_coords_pairs(const Args &a, float *tile) {
+    if (a.D < DP) {
+        for (int f = threadIdx.x; f < BN * DP; f += kThreads) {
+            const int p = f / DP, d = f % DP;
+            if (d >= a.D) *pair_slot<PS2>(tile, p, d) = 0.f;
+        }
+    }
+}
+
+// q = |x' - y'|^2 for the two points of a record (coordinates stored negated).
+template <int DP, int PS2>
+__device__ __forceinline__ float2 sq_dist_pair(const float2 (&x2)[DP], const float2 (&pv)[PS2 / 2], float2 q0,
+                                               bool start_from_q0) {
+    float2 q = q0;
+#pragma unroll
+    for (int d = 0; d < DP; ++d) {
+        const float2 df = __fadd2_rn(x2[d], pv[d]);
+        q = (d == 0 && !start_from_q0) ? __fmul2_rn(df, df) : __ffma2_rn(df, df, q);
+    }
+    return q;
+}
+
+// ---------------------------------------------------------------------------
+// Sum / LogSumExp (packed).  Value fields: b_je (Sum) or W_e - w'_je (LSE), as in
+// fwd_kernel; the LSE tile frame and careful path are the same.
+// ---------------------------------------------------------------------------
+template <int DP, int EP, int R, int BN, bool LSE>
+__global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a) {
+    constexpr int PS2 = pair_stride(DP, EP);
+    constexpr int UP = unroll_pairs(DP);
+    constexpr int UPT = 2 * UP;
+    constexpr float kLog2e = 1.4426950408889634f;
+    static_assert(BN % UPT == 0, "tile must be a multiple of the unroll");
+    __shared__ __align__(16) float tile[(BN / 2) * PS2];
+    __shared__ float wmax[kThreads / 32][EP];
+
+    const int t = threadIdx.x;
+    const int64_t row0 = (int64_t)blockIdx.x * (kThreads * R);
+    const int64_t j_begin = (int64_t)blockIdx.y * a.chunk;
+    const int64_t j_end = min(a.N, j_begin + a.chunk);
+
+    zero_pad_coords_pairs<DP, PS2, BN>(a, tile);
+    float2 x2[R][DP];
+    load_rows_pairs<DP, R>(a, row0, x2, a.c);
+
+    float2 part2[R][EP];
+    float hi[R][EP], lo[R][EP], m[R][EP], est[R][EP];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+            part2[r][e] = make_float2(0.f, 0.f);
+            hi[r][e] = lo[r][e] = 0.f;
+            m[r][e] = est[r][e] = -f_inf();
+        }
+
+    for (int64_t jt = j_begin; jt < j_end; jt += BN) {
+        const int nv = (int)min((int64_t)BN, j_end - jt);
+        const int nvp = (nv + UPT - 1) / UPT * UPT;
+        __syncthreads();
+        stage_coords_pairs<DP, PS2>(a, tile, jt, nv, nvp, -a.c, 0.f);
+
+        float W[EP];
+        if (!LSE) {
+            for (int p = t; p < nvp; p += kThreads) {
+#pragma unroll
+                for (int e = 0; e < EP; ++e)
+                    *pair_slot<PS2>(tile, p, DP + e) = (p < nv && e < a.E) ? __ldg(a.b + (jt + p) * a.E + e) : 0.f;
+            }
+        } else {
+            float lmax[EP];
+#pragma unroll
+            for (int e = 0; e < EP; ++e) lmax[e] = -f_inf();
+            for (int p = t; p < nvp; p += kThreads) {
+#pragma unroll
+                for (int e = 0; e < EP; ++e) {
+                    const float v = (p < nv && e < a.E) ? kLog2e * __ldg(a.b + (jt + p) * a.E + e) : -f_inf();
+                    *pair_slot<PS2>(tile, p, DP + e) = v;
+                    lmax[e] = fmaxf(lmax[e], v);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) lmax[e] = fmaxf(lmax[e], __shfl_xor_sync(0xffffffffu, lmax[e], o));
+                if ((t & 31) == 0) wmax[t >> 5][e] = lmax[e];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+                W[e] = wmax[0][e];
+#pragma unroll
+                for (int w = 1; w < kThreads / 32; ++w) W[e] = fmaxf(W[e], wmax[w][e]);
+            }
+            for (int p = t; p < nvp; p += kThreads) {
+#pragma unroll
+                for (int e = 0; e < EP; ++e) {
+                    float *slot = pair_slot<PS2>(tile, p, DP + e);
+                    const float v = *slot;
+                    *slot = (v == -f_inf()) ? f_inf() : W[e] - v;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- fast pass ------------------------------------------------------------
+        for (int jj = 0; jj < nvp; jj += UPT) {
+#pragma unroll
+            for (int u = 0; u < UP; ++u) {
+                float2 pv[PS2 / 2];
+                load_pair_record<PS2>(tile + ((jj >> 1) + u) * PS2, pv);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const bool fold = LSE && EP == 1;
+                    const float2 q = sq_dist_pair<DP, PS2>(x2[r], pv, fold ? pv[DP] : make_float2(0.f, 0.f), fold);
+                    if (!LSE) {
+                        const float2 k2 = make_float2(ex2_approx(-q.x), ex2_approx(-q.y));
+#pragma unroll
+                        for (int e = 0; e < EP; ++e) part2[r][e] = __ffma2_rn(k2, pv[DP + e], part2[r][e]);
+                    } else if (EP == 1) {
+                        part2[r][0] = __fadd2_rn(part2[r][0], make_float2(ex2_approx(-q.x), ex2_approx(-q.y)));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < EP; ++e) {
+                            const float2 tq = __fadd2_rn(q, pv[DP + e]);
+                            part2[r][e] = __fadd2_rn(part2[r][e], make_float2(ex2_approx(-tq.x), ex2_approx(-tq.y)));
+                        }
+                    }
+                }
+            }
+        }
+
+        float part[R][EP];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+                part[r][e] = part2[r][e].x + part2[r][e].y;
+                part2[r][e] = make_float2(0.f, 0.f);
+            }
+        if (!LSE) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int e = 0; e < EP; ++e) two_sum_add(hi[r][e], lo[r][e], part[r][e]);
+            continue;
+        }
+
+        // ---- LSE: frames, careful recomputation when needed ---------------------
+        bool careful = false;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < EP; ++e)
+                careful |= !(W[e] <= est[r][e] + 64.f || part[r][e] >= 0x1p-60f);
+        float F[R][EP];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < EP; ++e) F[r][e] = W[e];
+        if (careful) {
+            float umin[R][EP];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int e = 0; e < EP; ++e) umin[r][e] = f_inf();
+            for (int jj = 0; jj < nvp; jj += 2) {
+                float2 pv[PS2 / 2];
+                load_pair_record<PS2>(tile + (jj >> 1) * PS2, pv);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float2 q = sq_dist_pair<DP, PS2>(x2[r], pv, make_float2(0.f, 0.f), false);
+#pragma unroll
+                    for (int e = 0; e < EP; ++e) {
+                        const float2 tq = __fadd2_rn(q, pv[DP + e]);
+                        umin[r][e] = fminf(umin[r][e], fminf(tq.x, tq.y));
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int e = 0; e < EP; ++e) {
+                    part[r][e] = 0.f;
+                    if (umin[r][e] == f_inf()) umin[r][e] = 0.f;  // column empty in this tile
+                    F[r][e] = W[e] - umin[r][e];
+                }
+            for (int jj = 0; jj < nvp; jj += 2) {
+                float2 pv[PS2 / 2];
+                load_pair_record<PS2>(tile + (jj >> 1) * PS2, pv);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float2 q = sq_dist_pair<DP, PS2>(x2[r], pv, make_float2(0.f, 0.f), false);
+#pragma unroll
+                    for (int e = 0; e < EP; ++e) {
+                        const float2 tq = __fadd2_rn(q, pv[DP + e]);
+                        part[r][e] += ex2_approx(umin[r][e] - tq.x) + ex2_approx(umin[r][e] - tq.y);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+                const float p = part[r][e];
+                if (p > 0.f) {
+                    const float mn = fmaxf(m[r][e], F[r][e]);
+                    const float so = ex2_approx(m[r][e] - mn);
+                    const float sn = ex2_approx(F[r][e] - mn);
+                    hi[r][e] *= so;
+                    lo[r][e] *= so;
+                    two_sum_add(hi[r][e], lo[r][e], p * sn);
+                    m[r][e] = mn;
+                    est[r][e] = mn + lg2_approx(hi[r][e] + lo[r][e]);
+                }
+            }
+    }
+
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t i = row0 + (int64_t)r * kThreads + t;
+        if (i >= a.M) continue;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+            if (e >= a.E) continue;
+            const int64_t o = i * a.E + e;
+            if (!LSE) {
+                if (a.S == 1) {
+                    a.out[o] = hi[r][e] + lo[r][e];
+                } else {
+                    const int64_t w = (int64_t)blockIdx.y * a.M * a.E + o;
+                    a.ws0[w] = hi[r][e];
+                    a.ws1[w] = lo[r][e];
+                }
+            } else {
+                const float tot = hi[r][e] + lo[r][e];
+                if (a.S == 1) {
+                    a.out[o] = tot > 0.f ? (float)(0.6931471805599453 * ((double)m[r][e] + log2((double)tot)))
+                                         : -f_inf();
+                } else {
+                    const int64_t w = (int64_t)blockIdx.y * a.M * a.E + o;
+                    a.ws0[w] = tot > 0.f ? m[r][e] : -f_inf();
+                    a.ws1[w] = tot;
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// x-gradient (packed): the same sum as grad_kernel, two points per instruction.
+// ---------------------------------------------------------------------------
+template <int DP, int EP, int R, int BN>
+__global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a) {
+    constexpr int PS2 = pair_stride(DP, EP);
+    constexpr int UP = unroll_pairs(DP);
+    constexpr int UPT = 2 * UP;
+    static_assert(BN % UPT == 0, "tile must be a multiple of the unroll");
+    __shared__ __align__(16) float tile[(BN / 2) * PS2];
+
+    const int t = threadIdx.x;
+    const int64_t row0 = (int64_t)blockIdx.x * (kThreads * R);
+    const int64_t j_begin = (int64_t)blockIdx.y * a.chunk;
+    const int64_t j_end = min(a.N, j_begin + a.chunk);
+
+    zero_pad_coords_pairs<DP, PS2, BN>(a, tile);
+    float2 x2[R][DP];
+    load_rows_pairs<DP, R>(a, row0, x2, a.c);
+    float gr[R][EP];
+    float2 g2[R][EP];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t i = row0 + (int64_t)r * kThreads + t;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+            gr[r][e] = (i < a.M && e < a.E) ? __ldg(a.g + i * a.E + e) : 0.f;
+            g2[r][e] = make_float2(gr[r][e], gr[r][e]);
+        }
+    }
+    float2 part2[R][DP];
+    float hi[R][DP], lo[R][DP];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int d = 0; d < DP; ++d) {
+            part2[r][d] = make_float2(0.f, 0.f);
+            hi[r][d] = lo[r][d] = 0.f;
+        }
+
+    for (int64_t jt = j_begin; jt < j_end; jt += BN) {
+        const int nv = (int)min((int64_t)BN, j_end - jt);
+        const int nvp = (nv + UPT - 1) / UPT * UPT;
+        __syncthreads();
+        stage_coords_pairs<DP, PS2>(a, tile, jt, nv, nvp, -a.c, 0.f);
+        for (int p = t; p < nvp; p += kThreads) {
+#pragma unroll
+            for (int e = 0; e < EP; ++e)
+                *pair_slot<PS2>(tile, p, DP + e) = (p < nv && e < a.E) ? __ldg(a.b + (jt + p) * a.E + e) : 0.f;
+        }
+        __syncthreads();
+
+        for (int jj = 0; jj < nvp; jj += UPT) {
+#pragma unroll
+            for (int u = 0; u < UP; ++u) {
+                float2 pv[PS2 / 2];
+                load_pair_record<PS2>(tile + ((jj >> 1) + u) * PS2, pv);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float2 df[DP];
+                    float2 q = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int d = 0; d < DP; ++d) {
+                        df[d] = __fadd2_rn(x2[r][d], pv[d]);
+                        q = d == 0 ? __fmul2_rn(df[d], df[d]) : __ffma2_rn(df[d], df[d], q);
+                    }
+                    float2 beta;
+                    if (EP == 1) {
+                        beta = pv[DP];
+                    } else {
+                        beta = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int e = 0; e < EP; ++e) beta = __ffma2_rn(g2[r][e], pv[DP + e], beta);
+                    }
+                    const float2 kb = __fmul2_rn(make_float2(ex2_approx(-q.x), ex2_approx(-q.y)), beta);
+#pragma unroll
+                    for (int d = 0; d < DP; ++d) part2[r][d] = __ffma2_rn(kb, df[d], part2[r][d]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int d = 0; d < DP; ++d) {
+                two_sum_add(hi[r][d], lo[r][d], part2[r][d].x + part2[r][d].y);
+                part2[r][d] = make_float2(0.f, 0.f);
+            }
+    }
+
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t i = row0 + (int64_t)r * kThreads + t;
+        if (i >= a.M) continue;
+        const float sc = (EP == 1) ? a.gscale * gr[r][0] : a.gscale;
+#pragma unroll
+        for (int d = 0; d < DP; ++d) {
+            if (d >= a.D) continue;
+            const int64_t o = i * a.D + d;
+            if (a.S == 1) {
+                a.out[o] = (hi[r][d] + lo[r][d]) * sc;
+            } else {
+                const int64_t w = (int64_t)blockIdx.y * a.M * a.D + o;
+                a.ws0[w] = hi[r][d] * sc;
+                a.ws1[w] = lo[r][d] * sc;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K-min (packed distances).  The threshold test is taken once per row for a
+// group of UPT points (the minimum of their distances against the list's last
+// entry); the group's passing points are then walked in increasing j from a bit
+// mask, so each row has a single insertion site in the code.  Insertion is
+// strictly-smaller and in increasing j, so equal distances keep the lower index.
+// With CB > 0, passing points are appended to a per-row buffer of CB register
+// entries (a shift register, newest in slot 0) and inserted when it is full or
+// when the warp drains all buffers together at the end of a tile; the order of
+// insertion is still increasing j.  A buffered point may be stale against the
+// list (it passed an older threshold); knn_insert then leaves the list as is.
+// ---------------------------------------------------------------------------
+template <int KP, int CB>
+__device__ __forceinline__ void knn_drain(float (&dk)[KP], int (&ik)[KP], float (&cd)[CB], int (&cj)[CB], int &nc) {
+#pragma unroll
+    for (int b = CB - 1; b >= 0; --b)
+        if (b < nc) knn_insert<KP>(dk, ik, cd[b], cj[b]);
+    nc = 0;
+}
+
+template <int DP, int KP, int R, int BN>
+__global__ void __launch_bounds__(kThreads) knn2_kernel(const Args a) {
+    constexpr int PS2 = pair_stride(DP, 0);
+    constexpr int UP = unroll_pairs(DP);
+    constexpr int UPT = 2 * UP;
+    constexpr int CB = knn_buffer(DP, KP);
+    constexpr int CBA = CB > 0 ? CB : 1;
+    static_assert(BN % UPT == 0, "tile must be a multiple of the unroll");
+    __shared__ __align__(16) float tile[(BN / 2) * PS2];
+
+    const int t = threadIdx.x;
+    const int64_t row0 = (int64_t)blockIdx.x * (kThreads * R);
+    const int64_t j_begin = (int64_t)blockIdx.y * a.chunk;
+    const int64_t j_end = min(a.N, j_begin + a.chunk);
+
+    zero_pad_coords_pairs<DP, PS2, BN>(a, tile);
+    float2 x2[R][DP];
+    load_rows_pairs<DP, R>(a, row0, x2, 1.f);
+    float dk[R][KP];
+    int ik[R][KP];
+    float cd[R][CBA];
+    int cj[R][CBA];
+    int nc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int k = 0; k < KP; ++k) {
+            dk[r][k] = f_inf();
+            ik[r][k] = -1;
+        }
+#pragma unroll
+        for (int b = 0; b < CBA; ++b) {
+            cd[r][b] = f_inf();
+            cj[r][b] = -1;
+        }
+        nc[r] = 0;
+    }
+
+    for (int64_t jt = j_begin; jt < j_end; jt += BN) {
+        const int nv = (int)min((int64_t)BN, j_end - jt);
+        const int nvp = (nv + UPT - 1) / UPT * UPT;
+        __syncthreads();
+        stage_coords_pairs<DP, PS2>(a, tile, jt, nv, nvp, -1.f, -f_inf());
+        __syncthreads();
+
+        for (int jj = 0; jj < nvp; jj += UPT) {
+            float2 q[UP][R];
+#pragma unroll
+            for (int u = 0; u < UP; ++u) {
+                float2 pv[PS2 / 2];
+                load_pair_record<PS2>(tile + ((jj >> 1) + u) * PS2, pv);
+#pragma unroll
+                for (int r = 0; r < R; ++r) q[u][r] = sq_dist_pair<DP, PS2>(x2[r], pv, make_float2(0.f, 0.f), false);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float mn = fminf(q[0][r].x, q[0][r].y);
+#pragma unroll
+                for (int u = 1; u < UP; ++u) mn = fminf(mn, fminf(q[u][r].x, q[u][r].y));
+                if (mn < dk[r][KP - 1]) {
+                    const float thr = dk[r][KP - 1];
+                    unsigned mask = 0;
+#pragma unroll
+                    for (int u = 0; u < UP; ++u) {
+                        mask |= (q[u][r].x < thr ? 1u : 0u) << (2 * u);
+                        mask |= (q[u][r].y < thr ? 1u : 0u) << (2 * u + 1);
+                    }
+                    const int j0 = (int)(jt + jj);
+                    while (mask) {
+                        const int c = __ffs(mask) - 1;
+                        mask &= mask - 1;
+                        float2 qq = q[0][r];
+#pragma unroll
+                        for (int u = 1; u < UP; ++u) qq = ((c >> 1) == u) ? q[u][r] : qq;
+                        const float v = (c & 1) ? qq.y : qq.x;
+                        if (CB == 0) {
+                            knn_insert<KP>(dk[r], ik[r], v, j0 + c);
+                        } else {
+                            if (nc[r] == CB) knn_drain<KP, CBA>(dk[r], ik[r], cd[r], cj[r], nc[r]);
+#pragma unroll
+                            for (int b = CBA - 1; b > 0; --b) {
+                                cd[r][b] = cd[r][b - 1];
+                                cj[r][b] = cj[r][b - 1];
+                            }
+                            cd[r][0] = v;
+                            cj[r][0] = j0 + c;
+                            ++nc[r];
+                        }
+                    }
+                }
+            }
+        }
+        if (CB > 0) {  // the warp drains every buffer together
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                if (__any_sync(0xffffffffu, nc[r] > 0)) knn_drain<KP, CBA>(dk[r], ik[r], cd[r], cj[r], nc[r]);
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t i = row0 + (int64_t)r * kThreads + t;
+        if (i >= a.M) continue;
+        if (a.S == 1) {
+#pragma unroll
+            for (int k = 0; k < KP; ++k) {
+                if (k >= a.K) continue;
+                a.idx[i * a.K + k] = ik[r][k];
+                if (a.out) a.out[i * a.K + k] = dk[r][k];
+            }
+        } else {
+            const int64_t w = ((int64_t)blockIdx.y * a.M + i) * KP;
+#pragma unroll
+            for (int k = 0; k < KP; ++k) {
+                a.ws0[w + k] = dk[r][k];
+                a.wsi[w + k] = ik[r][k];
+            }
+        }
+    }
+}
+
+}  // namespace kr

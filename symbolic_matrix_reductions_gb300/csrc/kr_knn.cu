@@ -1,5 +1,5 @@
 // K-min / ArgMin instances and launcher.
-#include "kr_kernels.cuh"
+#include "kr_kernels_packed.cuh"
 
 namespace kr {
 
@@ -8,7 +8,10 @@ typedef void (*KernelFn)(const Args);
 
 template <int DP, int KP>
 KernelFn knn_instance() {
-    return knn_kernel<DP, KP, rows_knn(DP, KP), tile_points(pack_stride(DP, 0))>;
+    if constexpr (packed(DP))
+        return knn2_kernel<DP, KP, rows_knn(DP, KP), instance_tile(DP, 0)>;
+    else
+        return knn_kernel<DP, KP, rows_knn(DP, KP), instance_tile(DP, 0)>;
 }
 
 template <int KP>
