@@ -164,6 +164,31 @@ def probe_pipes(torch, nsm):
             "ffma_lanes_per_s": nsm * bps * 256 * iters * 8 / (ms[0] / 1e3)}
 
 
+# Tensor-core Sum (E = 1, 32 <= D <= 62): per pair, three fp16 products (hi.hi, hi.lo,
+# lo.hi) of the K = 64 augmented vectors, 2 FLOP per multiply-add.
+TC_FLOP_PER_PAIR = 3 * 2 * 64
+
+
+def tensor_peak_tflops():
+    """Dense fp16 tensor peak: the measured bf16 cuBLAS burst peak (fp16 and bf16 have
+    the same nominal dense rate on this part), else the fallback figure."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        v = json.load(open(path)).get("bf16_tflops")
+        if v:
+            return float(v), "measured bf16 burst (fp16 nominal ratio 1)"
+    return 1900.0, "fallback 1.9 PFLOP/s bf16 (fp16 nominal ratio 1)"
+
+
+def roofline_tensor(seconds_per_launch, pairs, kernel, fp32_line):
+    peak, basis = tensor_peak_tflops()
+    achieved = pairs * TC_FLOP_PER_PAIR / seconds_per_launch / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": None, "kernel": kernel, "flop_per_pair": TC_FLOP_PER_PAIR, "peak_basis": basis,
+            "pairs_per_s": pairs / seconds_per_launch,
+            "vs_fp32_direct_roofline": {"peak_pairs_per_s": fp32_line["peak"], "frac": fp32_line["frac"]}}
+
+
 def roofline(op, D, E, seconds_per_launch, pairs, nsm, clk_mhz, xu_lanes, kernel, live_mhz=None):
     n = ops_per_pair(op, D, E)
 
@@ -209,7 +234,7 @@ def run_ours(args, rank, world, local_rank):
     max_mhz = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("sm_max_mhz", 2070.0)) \
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 2070.0
 
-    inp = W.generate(args.workload)
+    inp = W.generate(args.workload, M=args.size[0], N=args.size[1]) if args.size else W.generate(args.workload)
     x, y, b, g = (torch.from_numpy(inp[k]).to(dev) for k in ("x", "y", "b", "g"))
     M, D = x.shape
     N, E = y.shape[0], b.shape[1]
@@ -279,7 +304,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {W.WORKLOADS[args.workload].note}; step = Sum + LogSumExp "
+        "config": {"workload": f"{args.workload}{' resized' if args.size else ''}: {W.WORKLOADS[args.workload].note}; step = Sum + LogSumExp "
                                f"(b as log-weight) + grad-x (g~N(0,1)) + K-min (K={K_NN})",
                    "M": M, "N": N, "D": D, "E": E, "K": K_NN, "sigma": s,
                    "pairs_per_step": pairs_per_step, "l2": "flushed before every timed step (256 MB write)",
@@ -379,9 +404,13 @@ def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
                 p = kr.plan_device(kr.OP_SUM if op == "sum" else kr.OP_LSE, M, N, D, E)
                 kname = f"fwd_kernel<{'Sum' if op == 'sum' else 'LSE'}>[D={D},E={E}]"
             ms = _time_op(torch, fn, 2)
+            rl = roofline(op, D, E, ms / 1e3, M * N, nsm, max_mhz, xu_lanes, kname)
+            if getattr(p, "path", 1) == kr.KR_PATH_TENSOR_CORES:
+                rl = roofline_tensor(ms / 1e3, M * N, "tc_sum_kernel (tcgen05)", rl)
             out.append({"workload": f"{wname}: {W.WORKLOADS[wname].note}", "op": op, "ms": ms,
                         "value": M * N / (ms / 1e3), "unit": UNIT, "split": p.split,
-                        "roofline": roofline(op, D, E, ms / 1e3, M * N, nsm, max_mhz, xu_lanes, kname)})
+                        "path": "tensor cores" if getattr(p, "path", 1) == kr.KR_PATH_TENSOR_CORES else "cuda cores",
+                        "roofline": rl})
         del x, y
         torch.cuda.empty_cache()
     return out
@@ -427,7 +456,7 @@ def run_reference(args, rank, world):
     import oracle
     from symbolic_matrix_reductions_gb300 import workloads as W
     orc = oracle.load()
-    inp = W.generate(args.workload)
+    inp = W.generate(args.workload, M=args.size[0], N=args.size[1]) if args.size else W.generate(args.workload)
     s = inp["sigma"]
     N = inp["y"].shape[0]
     per_step = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -458,6 +487,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=PRIMARY, help="workload of the step (default: gauss_d3)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the CPU baseline sample")
+    ap.add_argument("--size", type=lambda v: tuple(int(t) for t in v.split(",")), default=None,
+                    help="M,N: the workload's distributions at another size (e.g. a smaller case to profile)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3   # at least three warm-up steps

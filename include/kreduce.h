@@ -81,8 +81,19 @@ typedef enum {
 /* Optional knobs; pass NULL for the defaults. */
 typedef struct {
     int split;       /* S >= 1 forces S disjoint j-ranges (split-j); 0 = automatic */
-    int reserved[7]; /* must be zero */
+    int path;        /* KR_PATH_*: which units evaluate the Sum (0 = automatic) */
+    int reserved[6]; /* must be zero */
 } kr_options;
+
+typedef enum {
+    KR_PATH_AUTO = 0,         /* tensor cores where eligible, else CUDA cores */
+    KR_PATH_CUDA_CORES = 1,   /* FP32 pipe: direct differences, every shape */
+    KR_PATH_TENSOR_CORES = 2  /* tcgen05 split-fp16 expansion: Sum with E = 1, 32 <= D <= 62;
+                                 ignored elsewhere.  At run time it stands down to the CUDA
+                                 cores when max |x'|^2 + max |y'|^2 exceeds 16 (x' = x
+                                 sqrt(log2 e)/sigma), where the expansion's rounding would
+                                 exceed the Sum tolerance. */
+} kr_path;
 
 /*
  * Sum or LogSumExp of the Gaussian kernel over j ("Kernel Operations on the GPU...",
@@ -166,13 +177,14 @@ int kr_last_cuda_error(void);
 typedef struct {
     int d_pad;         /* compile-time coordinate count of the kernel instance (>= D) */
     int ek_pad;        /* compile-time E (or K) of the instance (>= E or K) */
-    int rows_per_thread;
+    int rows_per_thread; /* CUDA-core kernels; the tensor-core kernel has 128 rows per block */
     int threads;       /* per block */
     int tile_points;   /* points of y per shared-memory tile */
     int64_t row_blocks;
     int split;         /* S */
     int64_t chunk;     /* columns per split; the last split may be shorter */
     int64_t workspace_bytes;
+    int path;          /* KR_PATH_CUDA_CORES or KR_PATH_TENSOR_CORES */
 } kr_plan_t;
 
 int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm,

@@ -53,13 +53,17 @@ class KrError(RuntimeError):
 
 
 class KrOptions(ctypes.Structure):
-    _fields_ = [("split", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+    _fields_ = [("split", ctypes.c_int), ("path", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+
+
+KR_PATH_AUTO, KR_PATH_CUDA_CORES, KR_PATH_TENSOR_CORES = 0, 1, 2
 
 
 class KrPlan(ctypes.Structure):
     _fields_ = [("d_pad", ctypes.c_int), ("ek_pad", ctypes.c_int), ("rows_per_thread", ctypes.c_int),
                 ("threads", ctypes.c_int), ("tile_points", ctypes.c_int), ("row_blocks", ctypes.c_int64),
-                ("split", ctypes.c_int), ("chunk", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+                ("split", ctypes.c_int), ("chunk", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+                ("path", ctypes.c_int)]
 
 
 _lib = None
@@ -112,27 +116,29 @@ def _check(status: int, what: str) -> None:
         raise KrError(status, what, cuda_err)
 
 
-def _options(split: int):
-    if not split:
+def _options(split: int, path: int = 0):
+    if not split and not path:
         return None
     o = KrOptions()
     o.split = int(split)
+    o.path = int(path)
     return ctypes.byref(o)
 
 
 def plan(op: int, M: int, N: int, D: int, EK: int, num_sms: int = 152, blocks_per_sm: int = 0,
-         split: int = 0) -> KrPlan:
+         split: int = 0, path: int = 0) -> KrPlan:
     """The launch plan the library would use (host logic only, no GPU needed)."""
     p = KrPlan()
-    _check(load_library().kr_plan(op, M, N, D, EK, num_sms, blocks_per_sm, _options(split), ctypes.byref(p)),
-           "kr_plan")
+    _check(load_library().kr_plan(op, M, N, D, EK, num_sms, blocks_per_sm, _options(split, path),
+                                  ctypes.byref(p)), "kr_plan")
     return p
 
 
-def plan_device(op: int, M: int, N: int, D: int, EK: int, split: int = 0) -> KrPlan:
+def plan_device(op: int, M: int, N: int, D: int, EK: int, split: int = 0, path: int = 0) -> KrPlan:
     """The launch plan a call makes on the current CUDA device (queries the device)."""
     p = KrPlan()
-    _check(load_library().kr_plan_device(op, M, N, D, EK, _options(split), ctypes.byref(p)), "kr_plan_device")
+    _check(load_library().kr_plan_device(op, M, N, D, EK, _options(split, path), ctypes.byref(p)),
+           "kr_plan_device")
     return p
 
 
@@ -177,7 +183,7 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else None
 
 
-def kernel_reduce(x, y, b, sigma: float, reduction: str = "sum", out=None, split: int = 0):
+def kernel_reduce(x, y, b, sigma: float, reduction: str = "sum", out=None, split: int = 0, path: int = 0):
     """Sum (``reduction="sum"``) or LogSumExp (``"lse"``; b holds log-weights) over j.
 
     Returns ``out`` (M, E): a_ie = sum_j exp(-|x_i-y_j|^2/sigma^2) b_je, or
@@ -198,7 +204,7 @@ def kernel_reduce(x, y, b, sigma: float, reduction: str = "sum", out=None, split
     out2 = _mat(out, M, "out", E)
     _same_device(x, out2)
     st = load_library().kernel_reduce_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(out2), M, N, D, E, float(sigma), red,
-                                         _stream(dev), _options(split))
+                                         _stream(dev), _options(split, path))
     _check(st, "kernel_reduce")
     return out
 

@@ -23,6 +23,7 @@
 
 #include "kr_config.h"
 #include "kr_internal.h"
+#include "kr_tc.h"
 
 namespace kr {
 
@@ -63,10 +64,58 @@ static int64_t workspace_bytes(int op, const Instance &in, int64_t M, int D, int
 
 static const int64_t kMaxWorkspace = (int64_t)1 << 30;  // 1 GiB of partials at most
 
+static const int64_t kMaxTcOperands = (int64_t)8 << 30;  // split fp16 operands of the tensor path
+
+static int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+// Tensor-core Sum plan: 128 rows per block (one TMEM lane each), tiles of 128
+// points, splits on 128-point boundaries, one block per SM.
+static void plan_tc(int64_t M, int64_t N, int num_sms, int blocks_per_sm, int forced_split, kr_plan_t *p) {
+    p->d_pad = 64;
+    p->ek_pad = 1;
+    p->rows_per_thread = 1;
+    p->threads = 192;
+    p->tile_points = 128;
+    p->row_blocks = (M + 127) / 128;
+    p->path = KR_PATH_TENSOR_CORES;
+    if (num_sms < 1) num_sms = 1;
+    if (blocks_per_sm < 1) blocks_per_sm = 1;
+    const int64_t tiles_total = std::max<int64_t>(1, (N + 127) / 128);
+    int S = 1;
+    if (forced_split >= 1) {
+        S = (int)std::min<int64_t>(std::min<int64_t>(forced_split, tiles_total), kMaxSplit);
+    } else if (N > 0) {
+        double best = 0.0;
+        for (int64_t s = 1; s <= std::min<int64_t>(kMaxSplit, tiles_total); ++s) {
+            if (2 * s * M * (int64_t)sizeof(float) > kMaxWorkspace) break;
+            const int64_t chunk = round_up((N + s - 1) / s, 128);
+            const double work = (double)(chunk / 128) * (128.0 + 16.0);
+            const int64_t per_sm = (p->row_blocks * s + num_sms - 1) / num_sms;
+            const double cost = (double)per_sm * work * (1.0 + 0.002 * (double)s);
+            if (s == 1 || cost < best * 0.999) {
+                best = cost;
+                S = (int)s;
+            }
+        }
+    }
+    p->chunk = round_up((std::max<int64_t>(N, 1) + S - 1) / S, 128);
+    S = (int)std::max<int64_t>(1, (N + p->chunk - 1) / p->chunk);  // every split nonempty
+    p->split = S;
+    const int64_t n_pad = round_up(std::max<int64_t>(N, 1), 128);
+    const int64_t operands = (round_up(std::max<int64_t>(M, 1), 128) + n_pad) * 256 + n_pad * 4;
+    p->workspace_bytes = 256 + operands + (S > 1 ? 2 * (int64_t)S * M * (int64_t)sizeof(float) : 0);
+}
+
+static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, int path) {
+    if (op != OP_SUM || path == KR_PATH_CUDA_CORES || !tc_dims(D, EK)) return false;
+    return (round_up(std::max<int64_t>(M, 1), 128) + round_up(std::max<int64_t>(N, 1), 128)) * 256 <= kMaxTcOperands;
+}
+
 // Pure planner (no CUDA call).  blocks_per_sm <= 0: assume 4 resident blocks.
 static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm,
                 int forced_split, kr_plan_t *p) {
     const Instance in = choose_instance(op, D, EK);
+    p->path = KR_PATH_CUDA_CORES;
     p->d_pad = in.d_pad;
     p->ek_pad = in.ek_pad;
     p->rows_per_thread = in.rows;
@@ -131,6 +180,7 @@ namespace {
 struct DeviceCache {
     int num_sms = 0;
     int occ[4][10][33] = {};  // resident blocks per (op, d_pad index, ek_pad); 0 = not queried
+    int tc_occ = 0;           // resident tensor-core Sum blocks; 0 = not queried
 };
 std::mutex g_cache_mutex;
 DeviceCache g_cache[64];
@@ -172,6 +222,13 @@ int device_info(int dev, int op, const Instance &in, int *num_sms, int *occ) {
     *occ = slot;
     return 0;
 }
+
+int device_tc_occupancy(int dev) {
+    if (dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(g_cache_mutex);
+    if (g_cache[dev].tc_occ == 0) g_cache[dev].tc_occ = tc_occupancy();
+    return g_cache[dev].tc_occ;
+}
 }  // namespace
 
 // ---- validation ---------------------------------------------------------------------
@@ -198,7 +255,8 @@ static int validate(int op, const Buf *bufs, int nbuf, int64_t M, int64_t N, int
     if (op != OP_KNN && !(std::isfinite(sigma) && sigma > 0.f)) return KR_ERR_INVALID;
     if (opt) {
         if (opt->split < 0) return KR_ERR_INVALID;
-        for (int k = 0; k < 7; ++k)
+        if (opt->path < KR_PATH_AUTO || opt->path > KR_PATH_TENSOR_CORES) return KR_ERR_INVALID;
+        for (int k = 0; k < 6; ++k)
             if (opt->reserved[k] != 0) return KR_ERR_INVALID;
     }
     if (D > kMaxD) return KR_ERR_UNSUPPORTED;
@@ -243,6 +301,57 @@ static int is_device_ptr(const void *p, bool *dev) {
     return 0;
 }
 
+// ---- tensor-core Sum: operand prepass, tensor kernel, CUDA-core stand-in, combine -------
+// Workspace: [guard (2 x u32) + status | A_hi | A_lo | B_hi | B_lo | padded b | partials].  The
+// CUDA-core kernel is always launched after the tensor kernel with the same splits;
+// it returns at once unless the prepass found norms the expansion cannot serve.
+static cudaError_t run_tc(Args a, const kr_plan_t &p, const Instance &in, char *ws, cudaStream_t stream) {
+    const int64_t m_pad = round_up(a.M, 128), n_pad = round_up(std::max<int64_t>(a.N, 1), 128);
+    unsigned *guard = (unsigned *)ws;
+    __half *a_hi = (__half *)(ws + 256);
+    __half *a_lo = a_hi + m_pad * 64;
+    __half *b_hi = a_lo + m_pad * 64;
+    __half *b_lo = b_hi + n_pad * 64;
+    float *bpad = (float *)(b_lo + n_pad * 64);
+    float *part = bpad + n_pad;
+    cudaError_t ce = cudaMemsetAsync(guard, 0, 256, stream);
+    if (ce == cudaSuccess)
+        ce = tc_launch_prep(a.x, a.M, m_pad, a.D, a.c, true, a_hi, a_lo, guard, nullptr, nullptr, stream);
+    if (ce == cudaSuccess)
+        ce = tc_launch_prep(a.y, a.N, n_pad, a.D, a.c, false, b_hi, b_lo, guard + 1, a.b, bpad, stream);
+    if (p.split > 1) {
+        a.ws0 = part;
+        a.ws1 = part + (int64_t)p.split * a.M;
+    }
+    if (ce == cudaSuccess) {
+        TcArgs t{};
+        t.a_hi = a_hi;
+        t.a_lo = a_lo;
+        t.b_hi = b_hi;
+        t.b_lo = b_lo;
+        t.bpad = bpad;
+        t.m_pad = m_pad;
+        t.n_pad = n_pad;
+        t.out = a.out;
+        t.ws0 = a.ws0;
+        t.ws1 = a.ws1;
+        t.guard = guard;
+        t.status = (int *)(guard + 2);
+        t.M = a.M;
+        t.N = a.N;
+        t.chunk = p.chunk;
+        t.S = p.split;
+        ce = tc_launch_sum(t, dim3((unsigned)p.row_blocks, (unsigned)p.split), stream);
+    }
+    if (ce == cudaSuccess) {
+        a.tc_guard = guard;
+        const int64_t bm = (int64_t)kThreads * in.rows;
+        ce = launch_sum(in, a, dim3((unsigned)((a.M + bm - 1) / bm), (unsigned)p.split), stream);
+    }
+    if (ce == cudaSuccess && p.split > 1) ce = launch_combine(OP_SUM, in, a, stream);
+    return ce;
+}
+
 // ---- the common driver --------------------------------------------------------------
 static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStream_t stream,
                const kr_options *opt) {
@@ -258,7 +367,11 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
     int num_sms = 0, occ = 0;
     if (device_info(dev, op, in, &num_sms, &occ) != 0) return cuda_fail(cudaGetLastError());
     kr_plan_t p;
-    plan(op, a.M, a.N, a.D, EK, num_sms, occ, opt ? opt->split : 0, &p);
+    const bool tc = tc_eligible(op, a.M, a.N, a.D, EK, opt ? opt->path : 0) && tc_available();
+    if (tc)
+        plan_tc(a.M, a.N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, &p);
+    else
+        plan(op, a.M, a.N, a.D, EK, num_sms, occ, opt ? opt->split : 0, &p);
 
     // Host arrays: stage through one device allocation.
     bool host[8] = {};
@@ -313,22 +426,26 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
         }
         a.S = p.split;
         a.chunk = p.chunk;
-        if (p.split > 1) {
-            a.ws0 = (float *)ws;
-            if (op == OP_KNN) {
-                a.wsi = (int32_t *)(ws + (int64_t)p.split * a.M * p.ek_pad * (int64_t)sizeof(float));
-            } else {
-                a.ws1 = (float *)(ws + p.workspace_bytes / 2);
+        if (tc) {
+            ce = run_tc(a, p, in, ws, stream);
+        } else {
+            if (p.split > 1) {
+                a.ws0 = (float *)ws;
+                if (op == OP_KNN) {
+                    a.wsi = (int32_t *)(ws + (int64_t)p.split * a.M * p.ek_pad * (int64_t)sizeof(float));
+                } else {
+                    a.ws1 = (float *)(ws + p.workspace_bytes / 2);
+                }
             }
+            const dim3 grid((unsigned)p.row_blocks, (unsigned)p.split);
+            switch (op) {
+                case OP_SUM: ce = launch_sum(in, a, grid, stream); break;
+                case OP_LSE: ce = launch_lse(in, a, grid, stream); break;
+                case OP_GRAD: ce = launch_grad(in, a, grid, stream); break;
+                default: ce = launch_knn(in, a, grid, stream); break;
+            }
+            if (ce == cudaSuccess && p.split > 1) ce = launch_combine(op, in, a, stream);
         }
-        const dim3 grid((unsigned)p.row_blocks, (unsigned)p.split);
-        switch (op) {
-            case OP_SUM: ce = launch_sum(in, a, grid, stream); break;
-            case OP_LSE: ce = launch_lse(in, a, grid, stream); break;
-            case OP_GRAD: ce = launch_grad(in, a, grid, stream); break;
-            default: ce = launch_knn(in, a, grid, stream); break;
-        }
-        if (ce == cudaSuccess && p.split > 1) ce = launch_combine(op, in, a, stream);
         if (ce != cudaSuccess) status = cuda_fail(ce);
     }
     if (status == KR_OK) {
@@ -443,6 +560,10 @@ int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks
     if (!out || op < 0 || op > 3) return KR_ERR_INVALID;
     const int st = validate(op, nullptr, 0, M, N, D, EK, 1.f, opt);
     if (st != KR_OK) return st;
+    if (tc_eligible(op, M, N, D, EK, opt ? opt->path : 0)) {
+        plan_tc(M, N, num_sms, blocks_per_sm, opt ? opt->split : 0, out);
+        return KR_OK;
+    }
     return plan(op, M, N, D, EK, num_sms, blocks_per_sm, opt ? opt->split : 0, out);
 }
 
@@ -455,6 +576,10 @@ int kr_plan_device(int op, int64_t M, int64_t N, int D, int EK, const kr_options
     if (ce != cudaSuccess) return cuda_fail(ce);
     int num_sms = 0, occ = 0;
     if (device_info(dev, op, choose_instance(op, D, EK), &num_sms, &occ) != 0) return cuda_fail(cudaGetLastError());
+    if (tc_eligible(op, M, N, D, EK, opt ? opt->path : 0) && tc_available()) {
+        plan_tc(M, N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, out);
+        return KR_OK;
+    }
     return plan(op, M, N, D, EK, num_sms, occ, opt ? opt->split : 0, out);
 }
 

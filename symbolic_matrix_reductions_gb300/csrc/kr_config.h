@@ -46,6 +46,14 @@ KR_HD constexpr int rows_knn(int DP, int KP) {
     return DP <= 4 ? (KP <= 10 ? 4 : KP == 16 ? 2 : 1) : DP <= 16 ? (KP <= 10 ? 2 : 1) : 1;
 }
 
+// Tensor-core Sum: largest |x'|^2 + |y'|^2 (prescaled, base-2 exponent units) for
+// which the expanded exponent 2x'.y' - |x'|^2 - |y'|^2, accumulated in fp32 from
+// split fp16 operands, keeps the kernel values within the Sum tolerance (its
+// absolute error is a few 1e-6 times this sum).
+constexpr float kTcNormLimit = 16.0f;
+// Coordinate range of the tensor-core Sum (the augmented vector must fit K = 64).
+KR_HD constexpr bool tc_dims(int D, int E) { return E == 1 && D >= 32 && D <= 62; }
+
 // Inner-loop unroll over tile points (tiles are padded to a multiple of it).
 KR_HD constexpr int unroll_points(int DP) { return DP <= 8 ? 4 : DP <= 32 ? 2 : 1; }
 

@@ -33,6 +33,8 @@ struct Args {
     float gscale;        // grad: -2 / (sigma^2 c)
     int64_t chunk;       // columns per split
     int S;
+    const unsigned *tc_guard;  // Sum only: non-null when the tensor-core kernel ran first;
+                               // the CUDA-core kernel then works only if the norms failed it
 };
 
 // Compile-time shape of one kernel instance, chosen by the planner.

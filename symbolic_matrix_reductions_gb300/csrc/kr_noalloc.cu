@@ -94,14 +94,16 @@ extern "C" int kernel_reduce_noalloc(const float *x, const float *y, const float
     const Instance in = choose_instance(op, D, E);
     const int occ = op == OP_SUM ? occupancy_sum(in) : occupancy_lse(in);
 
-    // The planner's split, at least 2, at most what the scratch holds.
+    // The planner's split for the CUDA-core kernel, at least 2, at most what the
+    // scratch holds.
+    kr_options opt = {};
+    opt.path = KR_PATH_CUDA_CORES;
     kr_plan_t p;
-    int st = kr_plan(op, M, N, D, E, num_sms, occ, nullptr, &p);
+    int st = kr_plan(op, M, N, D, E, num_sms, occ, &opt, &p);
     if (st != KR_OK) return st;
     const int64_t fit = kScratchFloats / (2 * M * (int64_t)E);
     int S = p.split < 2 ? 2 : p.split;
     if (S > fit) S = (int)fit;
-    kr_options opt = {};
     opt.split = S;
     st = kr_plan(op, M, N, D, E, num_sms, occ, &opt, &p);
     if (st != KR_OK) return st;

@@ -1,0 +1,410 @@
+// kr_tc.cu -- tensor-core (tcgen05) path of the Gaussian Sum for 32 <= D <= 62, E = 1.
+//
+// The exponent of the prescaled Gaussian is a dot product of augmented vectors:
+//   -|x' - y'|^2 = 2 x'.y' - |x'|^2 - |y'|^2 = A_i . B_j,
+//   A_i = [2 x'_i, -|x'_i|^2, -1, 0...],  B_j = [y'_j, 1, |y'_j|^2, 0...]   (K = 64),
+// so a 128-row block of A against a 128-point tile of B is one M=128, N=128, K=64
+// matrix product on the 5th-generation tensor cores, accumulated in fp32 in tensor
+// memory (TMEM).  fp16 operands alone would carry 11 bits; each value v is split
+// as v = hi + lo (both fp16, lo = fp16(v - hi)) and the product is taken as
+// hi.hi + hi.lo + lo.hi (12 MMAs of K = 16): the dropped lo.lo term and the
+// split residual are below 2^-21 |v|.  The expansion cancels |x'|^2 + |y'|^2 down to
+// -|x'-y'|^2, so its absolute error grows with the norms: a prepass records the
+// largest |x'|^2 and |y'|^2 and, when their sum exceeds kTcNormLimit, the tensor
+// kernel leaves the work to the CUDA-core kernel launched after it (which runs only
+// in that case), without a host round trip.
+//
+// Block = 6 warps, one block per SM, warp-specialised around mbarriers:
+//   warp 0, one thread: TMA producer.  Loads the block's A tiles once, then streams
+//     B tiles (hi, lo: 2 x 16 KB, landing in the 128-byte-swizzled K-major layout
+//     the MMA reads) and their 128 signal values into a ring of kStages stages.
+//   warp 1: allocates TMEM; one thread issues the 12 MMAs of each tile into one of
+//     two TMEM accumulators and commits them to the stage's `empty` barrier and the
+//     accumulator's `full` barrier.
+//   warps 2-5: evaluation.  Warp w reads TMEM lanes 32 (w mod 4)..+31 (its rows),
+//     computes 2^t and accumulates b_j 2^t, then releases the accumulator and (with
+//     the MMA's commit) the stage.
+// Every mbarrier wait is bounded; a role that gives up raises a block-wide abort
+// flag, records an error, and every role then leaves its loop.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "kr_kernels.cuh"
+#include "kr_tc.h"
+
+namespace kr {
+
+namespace {
+
+constexpr int kRows = 128;              // rows per block = TMEM lanes = MMA M
+constexpr int kCols = 128;              // points per tile = MMA N
+constexpr int kStages = 4;              // B tiles in flight
+constexpr int kThreadsTc = 192;         // 6 warps
+constexpr int kTileBytes = 128 * 128;   // 128 rows x 64 fp16
+constexpr int kTmemCols = 256;          // two fp32 accumulators of 128 columns
+constexpr long kWaitLimit = 1L << 26;   // mbarrier polls before giving up
+
+// Dynamic shared memory: A hi/lo, kStages x (B hi, B lo), kStages x 128 signal
+// values, plus 1 KB of alignment slack.
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kSmemBytes = 2 * kTileBytes + kStages * kStageBytes + kStages * kCols * 4 + 1024;
+constexpr uint32_t kStageTx = 2 * kTileBytes + kCols * 4;   // bytes a stage's copies deliver
+
+// tcgen05 instruction descriptor: D = f32, A = B = f16, both K-major, M = 128, N = 128.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kCols >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 bytes,
+// 8-row (1024-byte) swizzle atoms, so the stride between 8-row groups is 1024 B.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
+        "l"(ad), "l"(bd), "r"(kIdesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void commit(uint32_t mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+                 : "memory");
+}
+
+// Bounded wait for the completion of the phase with the given parity.  Gives up
+// after kWaitLimit polls, or early when another role raised `abort`.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volatile int *abort) {
+    for (long it = 0; it < kWaitLimit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(mbar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((it & 255) == 255 && *abort) return false;
+    }
+    *abort = 1;
+    return false;
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(mbar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_1d(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ bool norms_ok(const unsigned *guard) {
+    return __uint_as_float(guard[0]) + __uint_as_float(guard[1]) <= kTcNormLimit;
+}
+
+// ---------------------------------------------------------------------------
+// Operand prepass: row r of src (D floats) -> augmented, split fp16 row of 64.
+// is_x: A = [2x', -|x'|^2, -1]; else B = [y', 1, |y'|^2].  Rows past `rows` are
+// zero.  guard receives the largest |.'|^2 (as float bits; non-negative floats
+// order like unsigned integers).  With b non-null, bpad[r] = b[r] (0 past `rows`).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t rows, int64_t rows_pad, int D,
+                                                      float c, int is_x, __half *hi, __half *lo, unsigned *guard,
+                                                      const float *b, float *bpad) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows_pad) return;
+    const bool live = r < rows;
+    const float *row = src + (live ? r : 0) * D;
+    float n = 0.f;
+    if (live) {
+        for (int d = 0; d < D; ++d) {
+            const float s = c * __ldg(row + d);
+            n = fmaf(s, s, n);
+        }
+        atomicMax(guard, __float_as_uint(n));
+    }
+    if (bpad) bpad[r] = live ? __ldg(b + r) : 0.f;
+    const float scale = is_x ? 2.f * c : c;
+    const float v_d = is_x ? -n : 1.f, v_d1 = is_x ? -1.f : n;
+    uint4 *ph = reinterpret_cast<uint4 *>(hi + r * 64);
+    uint4 *pl = reinterpret_cast<uint4 *>(lo + r * 64);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        __align__(16) __half h[8];
+        __align__(16) __half l[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int k = 8 * q + e;
+            float v = 0.f;
+            if (live) v = k < D ? scale * __ldg(row + k) : (k == D ? v_d : (k == D + 1 ? v_d1 : 0.f));
+            h[e] = __float2half_rn(v);
+            l[e] = __float2half_rn(v - __half2float(h[e]));
+        }
+        ph[q] = *reinterpret_cast<const uint4 *>(h);
+        pl[q] = *reinterpret_cast<const uint4 *>(l);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Main kernel: grid (ceil(M/128), S); block (row block, split) reduces its 128 rows
+// over the split's tiles of 128 points.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreadsTc, 1) tc_sum_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    // barriers: a_full, full[kStages], empty[kStages], acc_full[2], acc_empty[2]
+    __shared__ __align__(8) uint64_t bars[1 + 2 * kStages + 4];
+    if (!norms_ok(p.guard)) return;  // the CUDA-core kernel does this call's work
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t s_a_hi = smem_addr(smem), s_a_lo = s_a_hi + kTileBytes;
+    const uint32_t s_stage0 = s_a_hi + 2 * kTileBytes;  // stage s: B hi at +s*kStageBytes, B lo after it
+    const float *bval = reinterpret_cast<const float *>(smem + 2 * kTileBytes + kStages * kStageBytes);
+    const uint32_t s_bval0 = smem_addr(bval);
+    const uint32_t b_a_full = smem_addr(&bars[0]);
+    const uint32_t b_full0 = b_a_full + 8, b_empty0 = b_full0 + 8 * kStages;
+    const uint32_t b_accf0 = b_empty0 + 8 * kStages, b_acce0 = b_accf0 + 16;
+    volatile int *abort = &abort_flag;
+
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    const int64_t row0 = (int64_t)blockIdx.x * kRows;
+    const int64_t j_begin = (int64_t)blockIdx.y * p.chunk;
+    const int64_t j_end = min(p.N, j_begin + p.chunk);
+    const int T = j_end > j_begin ? (int)((j_end - j_begin + kCols - 1) / kCols) : 0;
+
+    if (w == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (t == 0) {
+        abort_flag = 0;
+        mbar_init(b_a_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(b_full0 + 8 * s, 1);       // the producer's expect_tx arrival
+            mbar_init(b_empty0 + 8 * s, 1 + 4);  // the MMAs' commit + the 4 evaluation warps
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(b_accf0 + 8 * k, 1);  // the MMAs' commit
+            mbar_init(b_acce0 + 8 * k, 4);  // the 4 evaluation warps
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const uint32_t tmem = tmem_slot;
+
+    float hi = 0.f, lo = 0.f;
+    if (w == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0 && T > 0) {
+            mbar_expect_tx(b_a_full, 2 * kTileBytes);
+            tma_2d(s_a_hi, &p.tm_a_hi, 0, (int)row0, b_a_full);
+            tma_2d(s_a_lo, &p.tm_a_lo, 0, (int)row0, b_a_full);
+            for (int i = 0; i < T; ++i) {
+                const int s = i % kStages;
+                if (i >= kStages && !mbar_wait(b_empty0 + 8 * s, ((i / kStages) - 1) & 1, abort)) break;
+                const int j0 = (int)(j_begin + (int64_t)i * kCols);
+                const uint32_t st = s_stage0 + s * kStageBytes, full = b_full0 + 8 * s;
+                mbar_expect_tx(full, kStageTx);
+                tma_2d(st, &p.tm_b_hi, 0, j0, full);
+                tma_2d(st + kTileBytes, &p.tm_b_lo, 0, j0, full);
+                bulk_1d(s_bval0 + s * kCols * 4, p.bpad + j0, kCols * 4, full);
+            }
+        }
+    } else if (w == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0 && T > 0 && mbar_wait(b_a_full, 0, abort)) {
+            for (int i = 0; i < T; ++i) {
+                const int s = i % kStages, k = i & 1;
+                if (!mbar_wait(b_full0 + 8 * s, (i / kStages) & 1, abort)) break;
+                if (i >= 2 && !mbar_wait(b_acce0 + 8 * k, ((i >> 1) - 1) & 1, abort)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;");
+                const uint32_t acc = tmem + (uint32_t)(k * kCols);
+                const uint32_t bh = s_stage0 + s * kStageBytes, bl = bh + kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(acc, desc_sw128(s_a_hi + 32 * kk), desc_sw128(bh + 32 * kk), kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) mma_f16(acc, desc_sw128(s_a_hi + 32 * kk), desc_sw128(bl + 32 * kk), 1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) mma_f16(acc, desc_sw128(s_a_lo + 32 * kk), desc_sw128(bh + 32 * kk), 1);
+                commit(b_empty0 + 8 * s);
+                commit(b_accf0 + 8 * k);
+            }
+        }
+    } else {
+        // ---------------- evaluation warps 2..5 ----------------
+        const int quarter = w & 3;
+        for (int i = 0; i < T; ++i) {
+            const int s = i % kStages, k = i & 1;
+            if (!mbar_wait(b_accf0 + 8 * k, (i >> 1) & 1, abort)) break;
+            // the stage's signal values were written by the copy engine: observe its barrier too
+            // (it cannot move on before this warp releases the stage)
+            if (!mbar_wait(b_full0 + 8 * s, (i / kStages) & 1, abort)) break;
+            asm volatile("tcgen05.fence::after_thread_sync;");
+            const uint32_t acc = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(k * kCols);
+            const float *bv = bval + s * kCols;
+            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t r[32];
+                tmem_ld32(acc + 32 * ch, r);
+                asm volatile("tcgen05.wait::ld.sync.aligned;");
+#pragma unroll
+                for (int q = 0; q < 32; q += 4) {
+                    const float4 b4 = *reinterpret_cast<const float4 *>(bv + 32 * ch + q);
+                    p0 = fmaf(ex2_approx(__uint_as_float(r[q + 0])), b4.x, p0);
+                    p1 = fmaf(ex2_approx(__uint_as_float(r[q + 1])), b4.y, p1);
+                    p2 = fmaf(ex2_approx(__uint_as_float(r[q + 2])), b4.z, p2);
+                    p3 = fmaf(ex2_approx(__uint_as_float(r[q + 3])), b4.w, p3);
+                }
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;");
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(b_acce0 + 8 * k);
+                mbar_arrive(b_empty0 + 8 * s);
+            }
+            two_sum_add(hi, lo, (p0 + p1) + (p2 + p3));
+        }
+    }
+
+    __syncthreads();
+    const bool ok = !*abort;
+    if (!ok && t == 0) atomicExch(p.status, 1);
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    if (w == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+
+    if (w >= 2) {
+        const int64_t i = row0 + 32 * (w & 3) + lane;
+        if (i < p.M) {
+            const float nan = __int_as_float(0x7fc00000);
+            if (p.S == 1) {
+                p.out[i] = ok ? hi + lo : nan;
+            } else {
+                const int64_t o = (int64_t)blockIdx.y * p.M + i;
+                p.ws0[o] = ok ? hi : nan;
+                p.ws1[o] = ok ? lo : 0.f;
+            }
+        }
+    }
+}
+
+// Host: cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)f;
+    });
+    return fn;
+}
+
+// Tensor map over rows x 64 fp16 (128-byte rows), boxes of 64 x 128 rows, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const __half *base, int64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {64, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void *)base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int tc_smem_bytes() { return kSmemBytes; }
+
+cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x, __half *hi,
+                           __half *lo, unsigned *guard, const float *b, float *bpad, cudaStream_t s) {
+    const unsigned blocks = (unsigned)((rows_pad + 255) / 256);
+    tc_prep_kernel<<<blocks, 256, 0, s>>>(src, rows, rows_pad, D, c, is_x ? 1 : 0, hi, lo, guard, b, bpad);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_launch_sum(const TcArgs &a, dim3 grid, cudaStream_t s) {
+    TcParams p;
+    if (!make_map(&p.tm_a_hi, a.a_hi, a.m_pad) || !make_map(&p.tm_a_lo, a.a_lo, a.m_pad) ||
+        !make_map(&p.tm_b_hi, a.b_hi, a.n_pad) || !make_map(&p.tm_b_lo, a.b_lo, a.n_pad))
+        return cudaErrorInvalidValue;
+    p.bpad = a.bpad;
+    p.out = a.out;
+    p.ws0 = a.ws0;
+    p.ws1 = a.ws1;
+    p.guard = a.guard;
+    p.status = a.status;
+    p.M = a.M;
+    p.N = a.N;
+    p.chunk = a.chunk;
+    p.S = a.S;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    tc_sum_kernel<<<grid, kThreadsTc, kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+int tc_occupancy() {
+    int n = 0;
+    if (cudaFuncSetAttribute(tc_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+        return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_sum_kernel, kThreadsTc, kSmemBytes) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+bool tc_available() { return encode_fn() != nullptr; }
+
+}  // namespace kr

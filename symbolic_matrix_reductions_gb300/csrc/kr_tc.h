@@ -1,0 +1,45 @@
+// kr_tc.h -- the tensor-core path of the Gaussian Sum (see kr_tc.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kr_internal.h"
+
+namespace kr {
+
+// Host-side description of one tensor-core Sum launch.
+struct TcArgs {
+    const __half *a_hi, *a_lo;  // m_pad x 64 augmented x operands (split fp16)
+    const __half *b_hi, *b_lo;  // n_pad x 64 augmented y operands
+    const float *bpad;          // n_pad signal values (zero past N)
+    float *out;                 // S == 1: M outputs
+    float *ws0, *ws1;           // S > 1: S x M (hi, lo) partials, as the CUDA-core Sum writes them
+    const unsigned *guard;      // [0] max |x'|^2, [1] max |y'|^2 (float bits), written by the prepass
+    int *status;                // set to 1 when a bounded wait gave up
+    int64_t M, N, m_pad, n_pad;
+    int64_t chunk;              // points per split, a multiple of 128
+    int S;
+};
+
+// Kernel parameters: TMA descriptors of the four operand arrays plus the rest.
+struct TcParams {
+    CUtensorMap tm_a_hi, tm_a_lo, tm_b_hi, tm_b_lo;
+    const float *bpad;
+    float *out, *ws0, *ws1;
+    const unsigned *guard;
+    int *status;
+    int64_t M, N, chunk;
+    int S;
+};
+
+int tc_smem_bytes();
+int tc_occupancy();
+bool tc_available();  // the driver offers cuTensorMapEncodeTiled
+cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x,
+                           __half *hi, __half *lo, unsigned *guard, const float *b, float *bpad, cudaStream_t s);
+cudaError_t tc_launch_sum(const TcArgs &a, dim3 grid, cudaStream_t s);
+
+}  // namespace kr

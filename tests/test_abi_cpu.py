@@ -81,6 +81,10 @@ def test_options_validation(lib):
     o.split = -1
     assert _reduce(lib, opt=ctypes.byref(o)) == kr.KR_ERR_INVALID
     o.split = 0
+    o.path = 3
+    assert _reduce(lib, opt=ctypes.byref(o)) == kr.KR_ERR_INVALID
+    o.path = 0
+    o.split = 0
     o.reserved[3] = 1
     assert _reduce(lib, opt=ctypes.byref(o)) == kr.KR_ERR_INVALID
 
@@ -106,7 +110,8 @@ def test_instance_choice(lib):
     p = kr.plan(kr.OP_SUM, 1000, 1000, 3, 1)
     assert (p.d_pad, p.ek_pad, p.threads) == (3, 1, 128)
     assert kr.plan(kr.OP_SUM, 10, 10, 5, 2).d_pad == 8 and kr.plan(kr.OP_SUM, 10, 10, 5, 2).ek_pad == 4
-    assert kr.plan(kr.OP_SUM, 10, 10, 50, 1).d_pad == 50
+    assert kr.plan(kr.OP_SUM, 10, 10, 50, 1, path=kr.KR_PATH_CUDA_CORES).d_pad == 50
+    assert kr.plan(kr.OP_LSE, 10, 10, 50, 1).d_pad == 50
     assert kr.plan(kr.OP_SUM, 10, 10, 51, 16).d_pad == 64
     assert kr.plan(kr.OP_KNN, 10, 10, 16, 10).ek_pad == 10
     assert kr.plan(kr.OP_KNN, 10, 10, 16, 11).ek_pad == 16
@@ -127,7 +132,8 @@ def test_split_covers_all_columns(lib, op, M, N, D, EK):
     assert 1 <= p.split <= 64
     assert p.split * p.chunk >= N
     assert N == 0 or (p.split - 1) * p.chunk < N      # no empty split
-    bm = p.threads * p.rows_per_thread
+    # tensor-core blocks: 256 threads over 128 rows (two column halves per row)
+    bm = 128 if p.path == kr.KR_PATH_TENSOR_CORES else p.threads * p.rows_per_thread
     assert p.row_blocks == (M + bm - 1) // bm
     if p.split == 1:
         assert p.workspace_bytes == 0
@@ -135,7 +141,8 @@ def test_split_covers_all_columns(lib, op, M, N, D, EK):
 
 def test_split_fills_the_gpu_for_tall_products(lib):
     # M = 1e5 rows at D = 50 are only a few hundred blocks: the j axis must be split.
-    p = kr.plan(kr.OP_SUM, 100_000, 10_000_000, 50, 1, num_sms=152, blocks_per_sm=4)
+    p = kr.plan(kr.OP_SUM, 100_000, 10_000_000, 50, 1, num_sms=152, blocks_per_sm=4, path=kr.KR_PATH_CUDA_CORES)
+    assert p.path == kr.KR_PATH_CUDA_CORES
     assert p.split > 1
     waves = (p.row_blocks * p.split) / (152 * 4)
     assert waves >= 2
@@ -143,6 +150,28 @@ def test_split_fills_the_gpu_for_tall_products(lib):
     # never split below 64 points per split
     assert kr.plan(kr.OP_SUM, 10, 100, 3, 1).split == 1
     assert kr.plan(kr.OP_SUM, 1000, 1000, 3, 1, blocks_per_sm=8).chunk >= 64
+
+
+def test_tensor_core_plan(lib):
+    """Sum with E = 1 and 32 <= D <= 62 plans the tcgen05 path: 128 rows per block, tiles
+    and splits of 128 points, split fp16 operands (256 B per point) and a padded copy of
+    the signal in the workspace."""
+    M, N = 100_000, 10_000_000
+    p = kr.plan(kr.OP_SUM, M, N, 50, 1, num_sms=152, blocks_per_sm=2)
+    assert p.path == kr.KR_PATH_TENSOR_CORES
+    assert (p.threads, p.rows_per_thread, p.tile_points, p.d_pad) == (192, 1, 128, 64)
+    assert p.row_blocks == (M + 127) // 128
+    assert p.chunk % 128 == 0 and p.split * p.chunk >= N and (p.split - 1) * p.chunk < N
+    n_pad = (N + 127) // 128 * 128
+    ops = ((M + 127) // 128 * 128 + n_pad) * 256 + 4 * n_pad
+    assert p.workspace_bytes == 256 + ops + (2 * p.split * M * 4 if p.split > 1 else 0)
+    for shape in [(kr.OP_SUM, 10, 10, 31, 1), (kr.OP_SUM, 10, 10, 63, 1), (kr.OP_SUM, 10, 10, 50, 2),
+                  (kr.OP_LSE, 10, 10, 50, 1), (kr.OP_GRAD, 10, 10, 50, 1)]:
+        assert kr.plan(*shape).path == kr.KR_PATH_CUDA_CORES, shape
+    assert kr.plan(kr.OP_SUM, 10, 10, 50, 1, path=kr.KR_PATH_CUDA_CORES).path == kr.KR_PATH_CUDA_CORES
+    assert kr.plan(kr.OP_SUM, 10, 1280, 50, 1, split=5).split == 5
+    assert kr.plan(kr.OP_SUM, 10, 1000, 50, 1, split=5).split == 4   # 256-point chunks
+    assert kr.plan(kr.OP_SUM, 10, 300, 50, 1, split=9).split == 3   # at most one split per 128-point tile
 
 
 def test_forced_split(lib):

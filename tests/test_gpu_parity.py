@@ -265,3 +265,46 @@ def test_workload_knn_d16(orc):
     i_ref, d_ref, n_ref = orc.knn(inp["x"][rows], inp["y"], inp["K"])
     ties = check_knn(_np(idx)[rows], _np(dist)[rows], inp["x"][rows], inp["y"], i_ref, d_ref, n_ref, "knn_d16")
     print(f"knn_d16: {ties} near-tie positions of {i_ref.size}")
+
+
+# ---------------------------------------------------------------------------
+# tensor-core Sum (tcgen05, split fp16 expansion): 32 <= D <= 62, E = 1
+# ---------------------------------------------------------------------------
+TC_CASES = [
+    (1, 1, 32, 0.9, 0), (127, 129, 50, 1.0, 0), (300, 1000, 50, 1.0, 0), (300, 1000, 50, 1.0, 3),
+    (513, 2000, 62, 1.3, 0), (256, 4096, 32, 0.8, 5), (1000, 300, 40, 1.1, 0),
+]
+
+
+@pytest.mark.parametrize("M,N,D,sigma,split", TC_CASES)
+def test_tensor_core_sum(orc, M, N, D, sigma, split):
+    r = _rng(M + N + D)
+    x = (r.standard_normal((M, D)) / np.sqrt(D)).astype(np.float32)
+    y = (r.standard_normal((N, D)) / np.sqrt(D)).astype(np.float32)
+    b = r.standard_normal((N, 1)).astype(np.float32)
+    assert kr.plan_device(kr.OP_SUM, M, N, D, 1).path == kr.KR_PATH_TENSOR_CORES
+    a = kr.kernel_reduce(*_dev(x, y, b), sigma, "sum", split=split, path=kr.KR_PATH_TENSOR_CORES)
+    a_ref, S_ref = orc.gauss_sum(x, y, b, sigma)
+    check_sum(_np(a), a_ref, S_ref, f"tc {M}x{N} D{D} S{split}")
+
+
+def test_tensor_core_norm_guard_falls_back(orc):
+    """Points far from the origin in units of sigma: the expansion would lose the
+    tolerance, so the tensor kernel stands down and the CUDA-core kernel answers."""
+    r = _rng(77)
+    x = (3.0 * r.standard_normal((200, 50))).astype(np.float32)
+    y = (x[r.integers(0, 200, 700)] + 0.3 * r.standard_normal((700, 50))).astype(np.float32)
+    b = r.standard_normal((700, 1)).astype(np.float32)
+    a = kr.kernel_reduce(*_dev(x, y, b), 2.0, "sum", path=kr.KR_PATH_TENSOR_CORES)
+    a_ref, S_ref = orc.gauss_sum(x, y, b, 2.0)
+    check_sum(_np(a), a_ref, S_ref, "norm guard")
+
+
+def test_tensor_and_cuda_core_paths_agree():
+    inp = W.generate("falkon_d50", M=2000, N=50_000)
+    xt, yt, bt = _dev(inp["x"], inp["y"], inp["b"])
+    a_tc = _np(kr.kernel_reduce(xt, yt, bt, 1.0, "sum", path=kr.KR_PATH_TENSOR_CORES))
+    a_cc = _np(kr.kernel_reduce(xt, yt, bt, 1.0, "sum", path=kr.KR_PATH_CUDA_CORES))
+    S = _np(kr.kernel_reduce(xt, yt, bt.abs(), 1.0, "sum", path=kr.KR_PATH_CUDA_CORES))
+    assert (np.abs(a_tc - a_cc) <= 1e-4 * S).all()
+    assert np.array_equal(a_tc, _np(kr.kernel_reduce(xt, yt, bt, 1.0, "sum", path=kr.KR_PATH_TENSOR_CORES)))
