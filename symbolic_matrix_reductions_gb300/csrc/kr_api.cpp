@@ -65,50 +65,58 @@ static int64_t workspace_bytes(int op, const Instance &in, int64_t M, int D, int
 static const int64_t kMaxWorkspace = (int64_t)1 << 30;  // 1 GiB of partials at most
 
 static const int64_t kMaxTcOperands = (int64_t)8 << 30;  // split fp16 operands of the tensor path
+static const int64_t kTcChunkMax = (int64_t)3 << 16;     // points per tensor-path split: 48 MB of B operands
 
 static int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
-// Tensor-core Sum plan: 128 rows per block (one TMEM lane each), tiles of 128
-// points, splits on 128-point boundaries, one block per SM.
+// Tensor-core Sum plan: kTcRows rows per block (one TMEM lane each), tiles of
+// kTcCols points, splits on tile boundaries, one block per SM.
 static void plan_tc(int64_t M, int64_t N, int num_sms, int blocks_per_sm, int forced_split, kr_plan_t *p) {
     p->d_pad = 64;
     p->ek_pad = 1;
     p->rows_per_thread = 1;
-    p->threads = 192;
-    p->tile_points = 128;
-    p->row_blocks = (M + 127) / 128;
+    p->threads = kTcThreads;
+    p->tile_points = kTcCols;
+    p->row_blocks = (M + kTcRows - 1) / kTcRows;
     p->path = KR_PATH_TENSOR_CORES;
     if (num_sms < 1) num_sms = 1;
     if (blocks_per_sm < 1) blocks_per_sm = 1;
-    const int64_t tiles_total = std::max<int64_t>(1, (N + 127) / 128);
+    const int64_t tiles_total = std::max<int64_t>(1, (N + kTcCols - 1) / kTcCols);
     int S = 1;
     if (forced_split >= 1) {
         S = (int)std::min<int64_t>(std::min<int64_t>(forced_split, tiles_total), kMaxSplit);
     } else if (N > 0) {
+        // The blocks resident at one time mostly share a split and stream its B tiles
+        // at slightly different paces; while a split's operands (256 B per point) fit
+        // in L2 every block after the first reads them from there.  Longer splits
+        // fall out of L2 and the copy latency of the misses stalls the MMAs.
+        const int64_t min_split = std::min<int64_t>((N + kTcChunkMax - 1) / kTcChunkMax, kMaxSplit);
+        // per block: its tiles plus a fixed start-up cost of about 1/8 tile
         double best = 0.0;
-        for (int64_t s = 1; s <= std::min<int64_t>(kMaxSplit, tiles_total); ++s) {
+        for (int64_t s = std::max<int64_t>(1, min_split); s <= std::min<int64_t>(kMaxSplit, tiles_total); ++s) {
             if (2 * s * M * (int64_t)sizeof(float) > kMaxWorkspace) break;
-            const int64_t chunk = round_up((N + s - 1) / s, 128);
-            const double work = (double)(chunk / 128) * (128.0 + 16.0);
+            const int64_t chunk = round_up((N + s - 1) / s, kTcCols);
+            const double work = (double)(chunk / kTcCols) + 0.125;
             const int64_t per_sm = (p->row_blocks * s + num_sms - 1) / num_sms;
             const double cost = (double)per_sm * work * (1.0 + 0.002 * (double)s);
-            if (s == 1 || cost < best * 0.999) {
+            if (best == 0.0 || cost < best * 0.999) {
                 best = cost;
                 S = (int)s;
             }
         }
     }
-    p->chunk = round_up((std::max<int64_t>(N, 1) + S - 1) / S, 128);
+    p->chunk = round_up((std::max<int64_t>(N, 1) + S - 1) / S, kTcCols);
     S = (int)std::max<int64_t>(1, (N + p->chunk - 1) / p->chunk);  // every split nonempty
     p->split = S;
-    const int64_t n_pad = round_up(std::max<int64_t>(N, 1), 128);
-    const int64_t operands = (round_up(std::max<int64_t>(M, 1), 128) + n_pad) * 256 + n_pad * 4;
+    const int64_t n_pad = round_up(std::max<int64_t>(N, 1), kTcCols);
+    const int64_t operands = (round_up(std::max<int64_t>(M, 1), kTcRows) + n_pad) * 256 + n_pad * 4;
     p->workspace_bytes = 256 + operands + (S > 1 ? 2 * (int64_t)S * M * (int64_t)sizeof(float) : 0);
 }
 
 static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, int path) {
     if (op != OP_SUM || path == KR_PATH_CUDA_CORES || !tc_dims(D, EK)) return false;
-    return (round_up(std::max<int64_t>(M, 1), 128) + round_up(std::max<int64_t>(N, 1), 128)) * 256 <= kMaxTcOperands;
+    return (round_up(std::max<int64_t>(M, 1), kTcRows) + round_up(std::max<int64_t>(N, 1), kTcCols)) * 256 <=
+           kMaxTcOperands;
 }
 
 // Pure planner (no CUDA call).  blocks_per_sm <= 0: assume 4 resident blocks.
@@ -306,7 +314,7 @@ static int is_device_ptr(const void *p, bool *dev) {
 // CUDA-core kernel is always launched after the tensor kernel with the same splits;
 // it returns at once unless the prepass found norms the expansion cannot serve.
 static cudaError_t run_tc(Args a, const kr_plan_t &p, const Instance &in, char *ws, cudaStream_t stream) {
-    const int64_t m_pad = round_up(a.M, 128), n_pad = round_up(std::max<int64_t>(a.N, 1), 128);
+    const int64_t m_pad = round_up(a.M, kTcRows), n_pad = round_up(std::max<int64_t>(a.N, 1), kTcCols);
     unsigned *guard = (unsigned *)ws;
     __half *a_hi = (__half *)(ws + 256);
     __half *a_lo = a_hi + m_pad * 64;

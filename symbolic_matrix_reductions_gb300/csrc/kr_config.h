@@ -51,6 +51,11 @@ KR_HD constexpr int rows_knn(int DP, int KP) {
 // split fp16 operands, keeps the kernel values within the Sum tolerance (its
 // absolute error is a few 1e-6 times this sum).
 constexpr float kTcNormLimit = 16.0f;
+// Tensor-core Sum geometry: rows per block (TMEM lanes, MMA M), points per tile
+// (MMA N), threads per block (a TMA warp, an MMA warp, 8 evaluation warps).
+constexpr int kTcRows = 128;
+constexpr int kTcCols = 256;
+constexpr int kTcThreads = 320;
 // Coordinate range of the tensor-core Sum (the augmented vector must fit K = 64).
 KR_HD constexpr bool tc_dims(int D, int E) { return E == 1 && D >= 32 && D <= 62; }
 

@@ -3,7 +3,7 @@
 // The exponent of the prescaled Gaussian is a dot product of augmented vectors:
 //   -|x' - y'|^2 = 2 x'.y' - |x'|^2 - |y'|^2 = A_i . B_j,
 //   A_i = [2 x'_i, -|x'_i|^2, -1, 0...],  B_j = [y'_j, 1, |y'_j|^2, 0...]   (K = 64),
-// so a 128-row block of A against a 128-point tile of B is one M=128, N=128, K=64
+// so a 128-row block of A against a 256-point tile of B is one M=128, N=256, K=64
 // matrix product on the 5th-generation tensor cores, accumulated in fp32 in tensor
 // memory (TMEM).  fp16 operands alone would carry 11 bits; each value v is split
 // as v = hi + lo (both fp16, lo = fp16(v - hi)) and the product is taken as
@@ -14,19 +14,25 @@
 // kernel leaves the work to the CUDA-core kernel launched after it (which runs only
 // in that case), without a host round trip.
 //
-// Block = 6 warps, one block per SM, warp-specialised around mbarriers:
-//   warp 0, one thread: TMA producer.  Loads the block's A tiles once, then streams
-//     B tiles (hi, lo: 2 x 16 KB, landing in the 128-byte-swizzled K-major layout
-//     the MMA reads) and their 128 signal values into a ring of kStages stages.
-//   warp 1: allocates TMEM; one thread issues the 12 MMAs of each tile into one of
-//     two TMEM accumulators and commits them to the stage's `empty` barrier and the
-//     accumulator's `full` barrier.
-//   warps 2-5: evaluation.  Warp w reads TMEM lanes 32 (w mod 4)..+31 (its rows),
-//     all 128 columns of the tile in one load, releases the accumulator at once (so
-//     the MMAs of tile i+2 can start while it computes), then computes 2^t,
-//     accumulates b_j 2^t and releases (with the MMA's commit) the stage.
+// Block = 10 warps, one block per SM, warp-specialised around mbarriers:
+//   warp 0, one thread: TMA producer.  Loads the block's A tiles (hi, lo) once, then
+//     streams B tiles of 256 points (hi, lo: 2 x 32 KB, landing in the
+//     128-byte-swizzled K-major layout the MMA reads) into a ring of kStages stages.
+//   warp 1: allocates TMEM; one thread issues the 12 MMAs (M=128, N=256, K=16) of
+//     each tile into one of two TMEM accumulators of 256 columns and commits them to
+//     the stage's `empty` barrier and the accumulator's `full` barrier.  A tcgen05
+//     MMA runs 128 x 256 x 16 in 128 cycles, but every barrier poll or commit
+//     between MMAs lets the MMA queue run dry for about 100 cycles, so the tiles are
+//     as wide as TMEM allows: 12 MMAs per handshake.
+//   warps 2-9: evaluation.  Warp w reads TMEM lanes 32 (w mod 4)..+31 (its rows);
+//     warps w and w+4 take the two 128-column halves of the tile.  Each loads its
+//     half in one TMEM load, releases the accumulator (the MMAs of tile i+2 may then
+//     overwrite it), computes 2^t and accumulates b_j 2^t, with b_j read through
+//     the L1 cache.
 // Every mbarrier wait is bounded; a role that gives up raises a block-wide abort
-// flag, records an error, and every role then leaves its loop.
+// flag, records an error, and every role then leaves its loop; the producer and the
+// MMA issuer then wait (bounded) for their copies and MMAs in flight, and the
+// block's rows come out as NaN.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -41,19 +47,24 @@ namespace kr {
 
 namespace {
 
-constexpr int kRows = 128;              // rows per block = TMEM lanes = MMA M
-constexpr int kCols = 128;              // points per tile = MMA N
-constexpr int kStages = 4;              // B tiles in flight
-constexpr int kThreadsTc = 192;         // 6 warps
-constexpr int kTileBytes = 128 * 128;   // 128 rows x 64 fp16
-constexpr int kTmemCols = 256;          // two fp32 accumulators of 128 columns
-constexpr long kWaitLimit = 1L << 26;   // mbarrier polls before giving up
+constexpr int kRows = kTcRows;          // rows per block = TMEM lanes = MMA M
+constexpr int kCols = kTcCols;          // points per tile = MMA N
+constexpr int kStages = 3;              // B tiles in flight
+constexpr int kEvalWarps = 8;           // two per TMEM lane quarter
+constexpr int kEvalCols = kCols / 2;    // tile columns per evaluation warp
+constexpr int kThreadsTc = kTcThreads;
+constexpr int kATileBytes = kRows * 128;  // 128 rows x 64 fp16
+constexpr int kBTileBytes = kCols * 128;  // 256 rows x 64 fp16
+constexpr int kTmemCols = 2 * kCols;      // two fp32 accumulators
+constexpr long kWaitLimit = 1L << 26;     // mbarrier polls before giving up
+static_assert(kThreadsTc == 64 + 32 * kEvalWarps, "warp roles");
+static_assert(kTmemCols <= 512, "TMEM has 512 columns");
 
-// Dynamic shared memory: A hi/lo, kStages x (B hi, B lo), kStages x 128 signal
-// values, plus 1 KB of alignment slack.
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kSmemBytes = 2 * kTileBytes + kStages * kStageBytes + kStages * kCols * 4 + 1024;
-constexpr uint32_t kStageTx = 2 * kTileBytes + kCols * 4;   // bytes a stage's copies deliver
+// Dynamic shared memory: A hi, A lo, kStages x (B hi, B lo), plus 1 KB of alignment
+// slack (the 128-byte swizzle wants 1024-byte aligned tiles).
+constexpr int kStageBytes = 2 * kBTileBytes;
+constexpr int kSmemBytes = 2 * kATileBytes + kStages * kStageBytes + 1024;
+static_assert(kSmemBytes + 256 <= 227 * 1024, "shared memory per block");
 
 // tcgen05 instruction descriptor: D = f32, A = B = f16, both K-major, M = 128, N = 128.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kCols >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
@@ -67,6 +78,7 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// D[tmem] (+)= A[smem] . B[smem]^T, fp16 operands, fp32 accumulation.
 __device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -106,17 +118,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volati
     return false;
 }
 
+// Bounded wait that ignores `abort`: used after an abort, to let this block's own
+// copies and MMAs in flight land before the block releases its memory.
+__device__ __forceinline__ bool mbar_drain(uint32_t mbar, uint32_t parity) {
+    for (long it = 0; it < kWaitLimit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(mbar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t mbar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
             "r"(dst),
         "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(mbar)
         : "memory");
-}
-__device__ __forceinline__ void bulk_1d(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(mbar)
-                 : "memory");
 }
 
 // One warp reads 128 consecutive fp32 columns of its 32 TMEM lanes (one row per lane).
@@ -175,24 +198,22 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t 
 
 // ---------------------------------------------------------------------------
 // Main kernel: grid (ceil(M/128), S); block (row block, split) reduces its 128 rows
-// over the split's tiles of 128 points.
+// over the split's tiles of 256 points.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreadsTc, 1) tc_sum_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
-    // barriers: a_full, full[kStages], empty[kStages], acc_full[2], acc_empty[2]
-    __shared__ __align__(8) uint64_t bars[1 + 2 * kStages + 4];
+    // barriers: a_full, full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain
+    __shared__ __align__(8) uint64_t bars[1 + 2 * kStages + 4 + 1];
     if (!norms_ok(p.guard)) return;  // the CUDA-core kernel does this call's work
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const uint32_t s_a_hi = smem_addr(smem), s_a_lo = s_a_hi + kTileBytes;
-    const uint32_t s_stage0 = s_a_hi + 2 * kTileBytes;  // stage s: B hi at +s*kStageBytes, B lo after it
-    const float *bval = reinterpret_cast<const float *>(smem + 2 * kTileBytes + kStages * kStageBytes);
-    const uint32_t s_bval0 = smem_addr(bval);
+    const uint32_t s_a_hi = smem_addr(smem), s_a_lo = s_a_hi + kATileBytes;
+    const uint32_t s_stage0 = s_a_hi + 2 * kATileBytes;  // stage s: B hi at +s*kStageBytes, B lo after it
     const uint32_t b_a_full = smem_addr(&bars[0]);
     const uint32_t b_full0 = b_a_full + 8, b_empty0 = b_full0 + 8 * kStages;
-    const uint32_t b_accf0 = b_empty0 + 8 * kStages, b_acce0 = b_accf0 + 16;
+    const uint32_t b_accf0 = b_empty0 + 8 * kStages, b_acce0 = b_accf0 + 16, b_drain = b_acce0 + 16;
     volatile int *abort = &abort_flag;
 
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
@@ -210,13 +231,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_sum_kernel(const __grid_cons
         abort_flag = 0;
         mbar_init(b_a_full, 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(b_full0 + 8 * s, 1);       // the producer's expect_tx arrival
-            mbar_init(b_empty0 + 8 * s, 1 + 4);  // the MMAs' commit + the 4 evaluation warps
+            mbar_init(b_full0 + 8 * s, 1);   // the producer's expect_tx arrival
+            mbar_init(b_empty0 + 8 * s, 1);  // the MMAs' commit
         }
         for (int k = 0; k < 2; ++k) {
-            mbar_init(b_accf0 + 8 * k, 1);  // the MMAs' commit
-            mbar_init(b_acce0 + 8 * k, 4);  // the 4 evaluation warps
+            mbar_init(b_accf0 + 8 * k, 1);           // the MMAs' commit
+            mbar_init(b_acce0 + 8 * k, kEvalWarps);  // the evaluation warps
         }
+        mbar_init(b_drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;");
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
@@ -228,30 +250,38 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_sum_kernel(const __grid_cons
     if (w == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0 && T > 0) {
-            mbar_expect_tx(b_a_full, 2 * kTileBytes);
+            mbar_expect_tx(b_a_full, 2 * kATileBytes);
             tma_2d(s_a_hi, &p.tm_a_hi, 0, (int)row0, b_a_full);
             tma_2d(s_a_lo, &p.tm_a_lo, 0, (int)row0, b_a_full);
+            int issued = 0;
             for (int i = 0; i < T; ++i) {
                 const int s = i % kStages;
                 if (i >= kStages && !mbar_wait(b_empty0 + 8 * s, ((i / kStages) - 1) & 1, abort)) break;
                 const int j0 = (int)(j_begin + (int64_t)i * kCols);
                 const uint32_t st = s_stage0 + s * kStageBytes, full = b_full0 + 8 * s;
-                mbar_expect_tx(full, kStageTx);
+                mbar_expect_tx(full, kStageBytes);
                 tma_2d(st, &p.tm_b_hi, 0, j0, full);
-                tma_2d(st + kTileBytes, &p.tm_b_lo, 0, j0, full);
-                bulk_1d(s_bval0 + s * kCols * 4, p.bpad + j0, kCols * 4, full);
+                tma_2d(st + kBTileBytes, &p.tm_b_lo, 0, j0, full);
+                issued = i + 1;
+            }
+            if (*abort) {  // let the copies in flight land before shared memory is released
+                mbar_drain(b_a_full, 0);
+                for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+                    mbar_drain(b_full0 + 8 * (i % kStages), (i / kStages) & 1);
             }
         }
     } else if (w == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0 && T > 0 && mbar_wait(b_a_full, 0, abort)) {
+            bool issued = false;
             for (int i = 0; i < T; ++i) {
                 const int s = i % kStages, k = i & 1;
                 if (!mbar_wait(b_full0 + 8 * s, (i / kStages) & 1, abort)) break;
                 if (i >= 2 && !mbar_wait(b_acce0 + 8 * k, ((i >> 1) - 1) & 1, abort)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;");
                 const uint32_t acc = tmem + (uint32_t)(k * kCols);
-                const uint32_t bh = s_stage0 + s * kStageBytes, bl = bh + kTileBytes;
+                const uint32_t bh = s_stage0 + s * kStageBytes, bl = bh + kBTileBytes;
+                // K = 16 per MMA: 32 bytes of each swizzled operand row
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_f16(acc, desc_sw128(s_a_hi + 32 * kk), desc_sw128(bh + 32 * kk), kk > 0);
@@ -261,37 +291,38 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_sum_kernel(const __grid_cons
                 for (int kk = 0; kk < 4; ++kk) mma_f16(acc, desc_sw128(s_a_lo + 32 * kk), desc_sw128(bh + 32 * kk), 1);
                 commit(b_empty0 + 8 * s);
                 commit(b_accf0 + 8 * k);
+                issued = true;
+            }
+            if (*abort && issued) {  // let the MMAs in flight finish before TMEM is released
+                commit(b_drain);
+                mbar_drain(b_drain, 0);
             }
         }
     } else {
-        // ---------------- evaluation warps 2..5 ----------------
-        const int quarter = w & 3;
+        // ---------------- evaluation warps 2..9 ----------------
+        const int quarter = w & 3, c0 = kEvalCols * ((w - 2) >> 2);
+        const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
         for (int i = 0; i < T; ++i) {
-            const int s = i % kStages, k = i & 1;
+            const int k = i & 1;
             if (!mbar_wait(b_accf0 + 8 * k, (i >> 1) & 1, abort)) break;
-            // the stage's signal values were written by the copy engine: observe its barrier too
-            // (it cannot move on before this warp releases the stage)
-            if (!mbar_wait(b_full0 + 8 * s, (i / kStages) & 1, abort)) break;
             asm volatile("tcgen05.fence::after_thread_sync;");
-            const uint32_t acc = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(k * kCols);
-            const float *bv = bval + s * kCols;
-            uint32_t r[128];
-            tmem_ld128(acc, r);  // the whole tile row in one load, one wait
+            uint32_t r[kEvalCols];
+            tmem_ld128(tmem + lanes + (uint32_t)(k * kCols + c0), r);  // one load, one wait
             asm volatile("tcgen05.wait::ld.sync.aligned;");
             asm volatile("tcgen05.fence::before_thread_sync;");
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_acce0 + 8 * k);  // the accumulator is free for the MMAs of tile i+2
+            if (lane == 0) mbar_arrive(b_acce0 + 8 * k);  // the MMAs of tile i+2 may overwrite it
+            // b of the tile's points (zero past N), the same for all lanes: L1 broadcasts
+            const float4 *bv = reinterpret_cast<const float4 *>(p.bpad + j_begin + (int64_t)i * kCols + c0);
             float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
-            for (int q = 0; q < 128; q += 4) {
-                const float4 b4 = *reinterpret_cast<const float4 *>(bv + q);
+            for (int q = 0; q < kEvalCols; q += 4) {
+                const float4 b4 = __ldg(bv + q / 4);
                 p0 = fmaf(ex2_approx(__uint_as_float(r[q + 0])), b4.x, p0);
                 p1 = fmaf(ex2_approx(__uint_as_float(r[q + 1])), b4.y, p1);
                 p2 = fmaf(ex2_approx(__uint_as_float(r[q + 2])), b4.z, p2);
                 p3 = fmaf(ex2_approx(__uint_as_float(r[q + 3])), b4.w, p3);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_empty0 + 8 * s);  // done with the stage's signal values
             two_sum_add(hi, lo, (p0 + p1) + (p2 + p3));
         }
     }
@@ -299,12 +330,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_sum_kernel(const __grid_cons
     __syncthreads();
     const bool ok = !*abort;
     if (!ok && t == 0) atomicExch(p.status, 1);
+    // warps 6..9 hand their row sums to warps 2..5 through the (now idle) A tile
+    float *red = reinterpret_cast<float *>(smem);
+    if (w >= 6) {
+        red[32 * (w & 3) + lane] = hi;
+        red[kRows + 32 * (w & 3) + lane] = lo;
+    }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
     if (w == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 
-    if (w >= 2) {
-        const int64_t i = row0 + 32 * (w & 3) + lane;
+    if (w >= 2 && w < 6) {
+        const int rl = 32 * (w & 3) + lane;
+        two_sum_add(hi, lo, red[rl]);
+        lo += red[kRows + rl];
+        const int64_t i = row0 + rl;
         if (i < p.M) {
             const float nan = __int_as_float(0x7fc00000);
             if (p.S == 1) {
@@ -338,13 +378,13 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tensor map over rows x 64 fp16 (128-byte rows), boxes of 64 x 128 rows, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const __half *base, int64_t rows) {
+// Tensor map over rows x 64 fp16 (128-byte rows), boxes of 64 x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const __half *base, int64_t rows, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {64, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void *)base, dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -364,8 +404,9 @@ cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int
 
 cudaError_t tc_launch_sum(const TcArgs &a, dim3 grid, cudaStream_t s) {
     TcParams p;
-    if (!make_map(&p.tm_a_hi, a.a_hi, a.m_pad) || !make_map(&p.tm_a_lo, a.a_lo, a.m_pad) ||
-        !make_map(&p.tm_b_hi, a.b_hi, a.n_pad) || !make_map(&p.tm_b_lo, a.b_lo, a.n_pad))
+    if (a.m_pad % kRows || a.n_pad % kCols || a.chunk % kCols) return cudaErrorInvalidValue;
+    if (!make_map(&p.tm_a_hi, a.a_hi, a.m_pad, kRows) || !make_map(&p.tm_a_lo, a.a_lo, a.m_pad, kRows) ||
+        !make_map(&p.tm_b_hi, a.b_hi, a.n_pad, kCols) || !make_map(&p.tm_b_lo, a.b_lo, a.n_pad, kCols))
         return cudaErrorInvalidValue;
     p.bpad = a.bpad;
     p.out = a.out;

@@ -12,15 +12,15 @@ namespace kr {
 
 // Host-side description of one tensor-core Sum launch.
 struct TcArgs {
-    const __half *a_hi, *a_lo;  // m_pad x 64 augmented x operands (split fp16)
-    const __half *b_hi, *b_lo;  // n_pad x 64 augmented y operands
-    const float *bpad;          // n_pad signal values (zero past N)
+    const __half *a_hi, *a_lo;  // m_pad x 64 augmented x operands (split fp16), m_pad % kTcRows == 0
+    const __half *b_hi, *b_lo;  // n_pad x 64 augmented y operands, n_pad % kTcCols == 0
+    const float *bpad;          // n_pad signal values (zero past N), 16-byte aligned
     float *out;                 // S == 1: M outputs
     float *ws0, *ws1;           // S > 1: S x M (hi, lo) partials, as the CUDA-core Sum writes them
     const unsigned *guard;      // [0] max |x'|^2, [1] max |y'|^2 (float bits), written by the prepass
     int *status;                // set to 1 when a bounded wait gave up
     int64_t M, N, m_pad, n_pad;
-    int64_t chunk;              // points per split, a multiple of 128
+    int64_t chunk;              // points per split, a multiple of kTcCols
     int S;
 };
 

@@ -154,24 +154,29 @@ def test_split_fills_the_gpu_for_tall_products(lib):
 
 def test_tensor_core_plan(lib):
     """Sum with E = 1 and 32 <= D <= 62 plans the tcgen05 path: 128 rows per block, tiles
-    and splits of 128 points, split fp16 operands (256 B per point) and a padded copy of
+    and splits of 256 points, split fp16 operands (256 B per point) and a padded copy of
     the signal in the workspace."""
     M, N = 100_000, 10_000_000
-    p = kr.plan(kr.OP_SUM, M, N, 50, 1, num_sms=152, blocks_per_sm=2)
+    p = kr.plan(kr.OP_SUM, M, N, 50, 1, num_sms=152, blocks_per_sm=1)
     assert p.path == kr.KR_PATH_TENSOR_CORES
-    assert (p.threads, p.rows_per_thread, p.tile_points, p.d_pad) == (192, 1, 128, 64)
+    assert (p.threads, p.rows_per_thread, p.tile_points, p.d_pad) == (320, 1, 256, 64)
     assert p.row_blocks == (M + 127) // 128
-    assert p.chunk % 128 == 0 and p.split * p.chunk >= N and (p.split - 1) * p.chunk < N
-    n_pad = (N + 127) // 128 * 128
+    assert p.chunk % 256 == 0 and p.split * p.chunk >= N and (p.split - 1) * p.chunk < N
+    # whole waves of 152 blocks: 782 row blocks x split fill them to within 1 %
+    assert (p.row_blocks * p.split) / (-(-p.row_blocks * p.split // 152) * 152) > 0.99
+    # a split's B operands (256 B per point) stay within 48 MB, so the blocks sharing it read L2
+    assert p.chunk * 256 <= 48 << 20
+    assert kr.plan(kr.OP_SUM, M, 1_000_000, 50, 1, num_sms=152, blocks_per_sm=1).chunk * 256 <= 48 << 20
+    n_pad = (N + 255) // 256 * 256
     ops = ((M + 127) // 128 * 128 + n_pad) * 256 + 4 * n_pad
     assert p.workspace_bytes == 256 + ops + (2 * p.split * M * 4 if p.split > 1 else 0)
     for shape in [(kr.OP_SUM, 10, 10, 31, 1), (kr.OP_SUM, 10, 10, 63, 1), (kr.OP_SUM, 10, 10, 50, 2),
                   (kr.OP_LSE, 10, 10, 50, 1), (kr.OP_GRAD, 10, 10, 50, 1)]:
         assert kr.plan(*shape).path == kr.KR_PATH_CUDA_CORES, shape
     assert kr.plan(kr.OP_SUM, 10, 10, 50, 1, path=kr.KR_PATH_CUDA_CORES).path == kr.KR_PATH_CUDA_CORES
-    assert kr.plan(kr.OP_SUM, 10, 1280, 50, 1, split=5).split == 5
-    assert kr.plan(kr.OP_SUM, 10, 1000, 50, 1, split=5).split == 4   # 256-point chunks
-    assert kr.plan(kr.OP_SUM, 10, 300, 50, 1, split=9).split == 3   # at most one split per 128-point tile
+    assert kr.plan(kr.OP_SUM, 10, 2560, 50, 1, split=5).split == 5
+    assert kr.plan(kr.OP_SUM, 10, 2000, 50, 1, split=5).split == 4   # 512-point chunks
+    assert kr.plan(kr.OP_SUM, 10, 600, 50, 1, split=9).split == 3   # at most one split per 256-point tile
 
 
 def test_forced_split(lib):

@@ -273,6 +273,7 @@ def test_workload_knn_d16(orc):
 TC_CASES = [
     (1, 1, 32, 0.9, 0), (127, 129, 50, 1.0, 0), (300, 1000, 50, 1.0, 0), (300, 1000, 50, 1.0, 3),
     (513, 2000, 62, 1.3, 0), (256, 4096, 32, 0.8, 5), (1000, 300, 40, 1.1, 0),
+    (130, 20001, 50, 1.0, 1),   # one split: 79 tiles per block, the stage and accumulator rings wrap many times
 ]
 
 
