@@ -434,31 +434,49 @@ __global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a) {
 // K-min (packed distances).  The threshold test is taken once per row for a
 // group of UPT points (the minimum of their distances against the list's last
 // entry); the group's passing points are then walked in increasing j from a bit
-// mask, so each row has a single insertion site in the code.  Insertion is
-// strictly-smaller and in increasing j, so equal distances keep the lower index.
-// With CB > 0, passing points are appended to a per-row buffer of CB register
-// entries (a shift register, newest in slot 0) and inserted when it is full or
-// when the warp drains all buffers together at the end of a tile; the order of
-// insertion is still increasing j.  A buffered point may be stale against the
-// list (it passed an older threshold); knn_insert then leaves the list as is.
+// mask.  Insertion is strictly-smaller and in increasing j, so equal distances
+// keep the lower index.
+//
+// CB == 0: a passing point is inserted into the sorted register list at once.
+// Late in a scan passing points are rare and land in one lane at a time, so the
+// warp runs the whole insertion for a single row while 31 lanes wait.
+// CB > 0: a passing point is appended instead to its row's buffer of CB (d, j)
+// slots in shared memory (a few instructions).  Every G groups the warp checks
+// whether any lane could overflow a buffer in the next G groups; if so, all 32
+// lanes drain all their buffers together, one slot per step, so each insertion
+// step serves up to 32 rows.  Slots are drained in the order they were filled
+// (increasing j), and a slot that passed an older, looser threshold simply
+// leaves the list unchanged, so the result is the same list as with CB == 0.
 // ---------------------------------------------------------------------------
-template <int KP, int CB>
-__device__ __forceinline__ void knn_drain(float (&dk)[KP], int (&ik)[KP], float (&cd)[CB], int (&cj)[CB], int &nc) {
+template <int KP, int CB, int R>
+__device__ __forceinline__ void knn_drain_warp(float (&dk)[R][KP], int (&ik)[R][KP], int (&nc)[R],
+                                               const float2 *cbuf) {
 #pragma unroll
-    for (int b = CB - 1; b >= 0; --b)
-        if (b < nc) knn_insert<KP>(dk, ik, cd[b], cj[b]);
-    nc = 0;
+    for (int r = 0; r < R; ++r) {
+        const int steps = __reduce_max_sync(0xffffffffu, nc[r]);
+        const float2 *slot = cbuf + r * CB * kThreads + threadIdx.x;
+        for (int s = 0; s < steps; ++s) {
+            const float2 e = slot[s * kThreads];
+            knn_insert<KP>(dk[r], ik[r], s < nc[r] ? e.x : f_inf(), __float_as_int(e.y));
+        }
+        nc[r] = 0;
+    }
 }
 
 template <int DP, int KP, int R, int BN>
-__global__ void __launch_bounds__(kThreads) knn2_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads, knn_buffer(DP, KP) > 0 ? 4 : 1) knn2_kernel(const Args a) {
     constexpr int PS2 = pair_stride(DP, 0);
     constexpr int UP = unroll_pairs(DP);
     constexpr int UPT = 2 * UP;
     constexpr int CB = knn_buffer(DP, KP);
     constexpr int CBA = CB > 0 ? CB : 1;
-    static_assert(BN % UPT == 0, "tile must be a multiple of the unroll");
+    constexpr int G = CB > 0 ? knn_check_groups(DP, KP) : 1;  // groups between buffer checks
+    constexpr int DRAIN_AT = CB - G * UPT;  // a lane above this many entries may overflow
+    static_assert(CB == 0 || DRAIN_AT >= 0, "buffer smaller than the points between checks");
+    static_assert(BN % (G * UPT) == 0, "tile must be a multiple of the unroll");
     __shared__ __align__(16) float tile[(BN / 2) * PS2];
+    // per row r, slot s, thread t: cbuf[(r CB + s) kThreads + t] = (d, j bits)
+    __shared__ __align__(16) float2 cbuf[CB > 0 ? R * CB * kThreads : 2];
 
     const int t = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.x * (kThreads * R);
@@ -470,9 +488,8 @@ __global__ void __launch_bounds__(kThreads) knn2_kernel(const Args a) {
     load_rows_pairs<DP, R>(a, row0, x2, 1.f);
     float dk[R][KP];
     int ik[R][KP];
-    float cd[R][CBA];
-    int cj[R][CBA];
     int nc[R];
+    int ntot = 0;  // entries over all of this thread's buffers (bounds each nc[r])
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
@@ -480,74 +497,68 @@ __global__ void __launch_bounds__(kThreads) knn2_kernel(const Args a) {
             dk[r][k] = f_inf();
             ik[r][k] = -1;
         }
-#pragma unroll
-        for (int b = 0; b < CBA; ++b) {
-            cd[r][b] = f_inf();
-            cj[r][b] = -1;
-        }
         nc[r] = 0;
     }
 
     for (int64_t jt = j_begin; jt < j_end; jt += BN) {
         const int nv = (int)min((int64_t)BN, j_end - jt);
-        const int nvp = (nv + UPT - 1) / UPT * UPT;
+        const int nvp = (nv + G * UPT - 1) / (G * UPT) * (G * UPT);
         __syncthreads();
         stage_coords_pairs<DP, PS2>(a, tile, jt, nv, nvp, -1.f, -f_inf());
         __syncthreads();
 
-        for (int jj = 0; jj < nvp; jj += UPT) {
-            float2 q[UP][R];
+        for (int jg = 0; jg < nvp; jg += G * UPT) {
 #pragma unroll
-            for (int u = 0; u < UP; ++u) {
-                float2 pv[PS2 / 2];
-                load_pair_record<PS2>(tile + ((jj >> 1) + u) * PS2, pv);
+            for (int g = 0; g < G; ++g) {
+                const int jj = jg + g * UPT;
+                float2 q[UP][R];
 #pragma unroll
-                for (int r = 0; r < R; ++r) q[u][r] = sq_dist_pair<DP, PS2>(x2[r], pv, make_float2(0.f, 0.f), false);
-            }
+                for (int u = 0; u < UP; ++u) {
+                    float2 pv[PS2 / 2];
+                    load_pair_record<PS2>(tile + ((jj >> 1) + u) * PS2, pv);
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                float mn = fminf(q[0][r].x, q[0][r].y);
+                    for (int r = 0; r < R; ++r)
+                        q[u][r] = sq_dist_pair<DP, PS2>(x2[r], pv, make_float2(0.f, 0.f), false);
+                }
 #pragma unroll
-                for (int u = 1; u < UP; ++u) mn = fminf(mn, fminf(q[u][r].x, q[u][r].y));
-                if (mn < dk[r][KP - 1]) {
-                    const float thr = dk[r][KP - 1];
-                    unsigned mask = 0;
+                for (int r = 0; r < R; ++r) {
+                    float mn = fminf(q[0][r].x, q[0][r].y);
 #pragma unroll
-                    for (int u = 0; u < UP; ++u) {
-                        mask |= (q[u][r].x < thr ? 1u : 0u) << (2 * u);
-                        mask |= (q[u][r].y < thr ? 1u : 0u) << (2 * u + 1);
-                    }
-                    const int j0 = (int)(jt + jj);
-                    while (mask) {
-                        const int c = __ffs(mask) - 1;
-                        mask &= mask - 1;
-                        float2 qq = q[0][r];
+                    for (int u = 1; u < UP; ++u) mn = fminf(mn, fminf(q[u][r].x, q[u][r].y));
+                    if (mn < dk[r][KP - 1]) {
+                        const float thr = dk[r][KP - 1];
+                        unsigned mask = 0;
 #pragma unroll
-                        for (int u = 1; u < UP; ++u) qq = ((c >> 1) == u) ? q[u][r] : qq;
-                        const float v = (c & 1) ? qq.y : qq.x;
-                        if (CB == 0) {
-                            knn_insert<KP>(dk[r], ik[r], v, j0 + c);
-                        } else {
-                            if (nc[r] == CB) knn_drain<KP, CBA>(dk[r], ik[r], cd[r], cj[r], nc[r]);
+                        for (int u = 0; u < UP; ++u) {
+                            mask |= (q[u][r].x < thr ? 1u : 0u) << (2 * u);
+                            mask |= (q[u][r].y < thr ? 1u : 0u) << (2 * u + 1);
+                        }
+                        const int j0 = (int)(jt + jj);
+                        while (mask) {
+                            const int c = __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            float2 qq = q[0][r];
 #pragma unroll
-                            for (int b = CBA - 1; b > 0; --b) {
-                                cd[r][b] = cd[r][b - 1];
-                                cj[r][b] = cj[r][b - 1];
+                            for (int u = 1; u < UP; ++u) qq = ((c >> 1) == u) ? q[u][r] : qq;
+                            const float v = (c & 1) ? qq.y : qq.x;
+                            if (CB == 0) {
+                                knn_insert<KP>(dk[r], ik[r], v, j0 + c);
+                            } else {
+                                cbuf[(r * CB + nc[r]) * kThreads + t] = make_float2(v, __int_as_float(j0 + c));
+                                ++nc[r];
+                                ++ntot;
                             }
-                            cd[r][0] = v;
-                            cj[r][0] = j0 + c;
-                            ++nc[r];
                         }
                     }
                 }
             }
-        }
-        if (CB > 0) {  // the warp drains every buffer together
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-                if (__any_sync(0xffffffffu, nc[r] > 0)) knn_drain<KP, CBA>(dk[r], ik[r], cd[r], cj[r], nc[r]);
+            if (CB > 0 && __any_sync(0xffffffffu, ntot > DRAIN_AT)) {
+                knn_drain_warp<KP, CBA, R>(dk, ik, nc, cbuf);
+                ntot = 0;
+            }
         }
     }
+    if (CB > 0) knn_drain_warp<KP, CBA, R>(dk, ik, nc, cbuf);
 
 #pragma unroll
     for (int r = 0; r < R; ++r) {
