@@ -10,6 +10,8 @@ Functions (each follows the passage cited in ``oracle.c``):
 * ``gauss_sum(x, y, b, sigma)``   -> (a, S)   Sum reduction and its tolerance scale
 * ``gauss_lse(x, y, w, sigma)``   -> L        LogSumExp with additive log-weights
 * ``gauss_grad_x(x, y, b, g, sigma)`` -> (gx, G)  x-gradient of sum(g * a) and its scale
+* ``gauss_grad_y(x, y, b, g, sigma)`` -> (gy, G)  y-gradient of sum(g * a) and its scale
+* ``gauss_grad_b(x, y, g, sigma)``    -> (gb, S)  b-gradient (transposed product) and its scale
 * ``knn(x, y, K)``                -> (idx, dist, next)  K-min by (distance, index)
 
 Inputs may be float32 or float64 arrays; they are converted to float64 (exact for
@@ -67,6 +69,10 @@ class Oracle:
         lib.oracle_gauss_lse.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_double, _dp]
         lib.oracle_gauss_grad_x.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_double, _dp, _dp]
+        lib.oracle_gauss_grad_y.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_double, _dp, _dp]
+        lib.oracle_gauss_grad_b.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int, ctypes.c_int, ctypes.c_double, _dp, _dp]
         lib.oracle_knn.argtypes = [_dp, _dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                    ctypes.c_int, _i64p, _dp, _dp]
@@ -128,6 +134,33 @@ class Oracle:
         self._lib.oracle_gauss_grad_x(_ptr(x), _ptr(y), _ptr(b), _ptr(g), M, N, D, E,
                                       float(sigma), _ptr(gx), _ptr(G))
         return gx, G
+
+    def gauss_grad_y(self, x, y, b, g, sigma):
+        x, y = self._points(x, y)
+        M, D = x.shape
+        N = y.shape[0]
+        b = _as2d(b, N, "b")
+        E = b.shape[1]
+        g = _as2d(g, M, "g")
+        if g.shape[1] != E:
+            raise ValueError(f"g must have E={E} columns, got {g.shape}")
+        gy = np.empty((N, D))
+        G = np.empty((N, D))
+        self._lib.oracle_gauss_grad_y(_ptr(x), _ptr(y), _ptr(b), _ptr(g), M, N, D, E,
+                                      float(sigma), _ptr(gy), _ptr(G))
+        return gy, G
+
+    def gauss_grad_b(self, x, y, g, sigma):
+        x, y = self._points(x, y)
+        M, D = x.shape
+        N = y.shape[0]
+        g = _as2d(g, M, "g")
+        E = g.shape[1]
+        gb = np.empty((N, E))
+        S = np.empty((N, E))
+        self._lib.oracle_gauss_grad_b(_ptr(x), _ptr(y), _ptr(g), M, N, D, E, float(sigma),
+                                      _ptr(gb), _ptr(S))
+        return gb, S
 
     def knn(self, x, y, K):
         x, y = self._points(x, y)

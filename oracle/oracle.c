@@ -173,6 +173,67 @@ void oracle_gauss_grad_x(const double *x, const double *y, const double *b,
     }
 }
 
+/*
+ * Gradient wrt y of the same scalar sum_{i,e} g_ie a_ie.  The kernel depends on
+ * y_j through |x_i - y_j|^2, and d/dy_jd exp(-|x_i - y_j|^2 / sigma^2)
+ *   = (2 / sigma^2) (x_id - y_jd) k(x_i, y_j), so
+ *   gy_jd = (2 / sigma^2) sum_i k(x_i, y_j) (sum_e g_ie b_je) (x_id - y_jd),
+ * summed in increasing i.  Rows j are independent: pass any subset of the rows
+ * of y (with the matching rows of b) to get those rows of gy.
+ * Also writes the tolerance scale
+ *   G_jd = (2 / sigma^2) sum_i k(x_i, y_j) |sum_e g_ie b_je| |x_id - y_jd|.
+ * ("Kernel Operations on the GPU...", §2 "Performance and differentiation":
+ * gradients through torch.autograd with respect to every input.)
+ */
+void oracle_gauss_grad_y(const double *x, const double *y, const double *b,
+                         const double *g, int64_t M, int64_t N, int D, int E,
+                         double sigma, double *gy, double *G)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < N; ++j) {
+        for (int d = 0; d < D; ++d) {
+            double s = 0.0, c = 0.0, sa = 0.0, ca = 0.0;
+            for (int64_t i = 0; i < M; ++i) {
+                double k = gauss(x + i * D, y + j * D, D, sigma);
+                double beta = 0.0;
+                for (int e = 0; e < E; ++e) beta += g[i * E + e] * b[j * E + e];
+                double diff = x[i * D + d] - y[j * D + d];
+                double term = (2.0 / (sigma * sigma)) * k * beta * diff;
+                neumaier_add(&s, &c, term);
+                neumaier_add(&sa, &ca, fabs(term));
+            }
+            gy[j * D + d] = s + c;
+            if (G) G[j * D + d] = sa + ca;
+        }
+    }
+}
+
+/*
+ * Gradient wrt b of sum_{i,e} g_ie a_ie.  a is linear in b, so
+ *   gb_je = sum_i k(x_i, y_j) g_ie,
+ * the transposed kernel product, summed in increasing i.  Rows j are independent.
+ * Also writes the tolerance scale S_je = sum_i |k(x_i, y_j) g_ie|.
+ * ("Kernel Operations on the GPU...", §2 "Performance and differentiation".)
+ */
+void oracle_gauss_grad_b(const double *x, const double *y, const double *g,
+                         int64_t M, int64_t N, int D, int E, double sigma,
+                         double *gb, double *scale)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < N; ++j) {
+        for (int e = 0; e < E; ++e) {
+            double s = 0.0, c = 0.0, sa = 0.0, ca = 0.0;
+            for (int64_t i = 0; i < M; ++i) {
+                double term = gauss(x + i * D, y + j * D, D, sigma) * g[i * E + e];
+                neumaier_add(&s, &c, term);
+                neumaier_add(&sa, &ca, fabs(term));
+            }
+            gb[j * E + e] = s + c;
+            if (scale) scale[j * E + e] = sa + ca;
+        }
+    }
+}
+
 /* (d1, j1) < (d2, j2) in lexicographic order: smaller distance first, then the
  * lower index. */
 static int lex_less(double d1, int64_t j1, double d2, int64_t j2)

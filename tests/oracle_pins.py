@@ -304,6 +304,104 @@ def pin_grad_stationary_and_translation(orc):
 
 
 # ---------------------------------------------------------------------------
+# y-gradient and b-gradient (transposed product)
+# ---------------------------------------------------------------------------
+def pin_grad_y_golden(orc):
+    for case in _golden()["grad_y"]:
+        gy, G = orc.gauss_grad_y(case["x"], case["y"], case["b"], case["g"], case["sigma"])
+        want = np.array([[_val(e) for e in row] for row in case["expect"]])
+        _close(gy, want, 1e-14, 1e-15, case["name"])
+
+
+def pin_grad_y_finite_differences(orc):
+    """gy = d/dy of L(y) = sum_ie g_ie a_ie(y), by central differences of the pinned Sum."""
+    r = _rng(18)
+    M, N, D, E, sigma = 9, 5, 3, 2, 0.7
+    x = r.standard_normal((M, D))
+    y = r.standard_normal((N, D))
+    b = r.standard_normal((N, E))
+    g = r.standard_normal((M, E))
+    gy, G = orc.gauss_grad_y(x, y, b, g, sigma)
+    h = 1e-5
+    fd = np.zeros_like(y)
+    for j in range(N):
+        for d in range(D):
+            yp = y.copy(); yp[j, d] += h
+            ym = y.copy(); ym[j, d] -= h
+            ap, _ = orc.gauss_sum(x, yp, b, sigma)
+            am, _ = orc.gauss_sum(x, ym, b, sigma)
+            fd[j, d] = np.sum(g * (ap - am)) / (2 * h)
+    assert (np.abs(gy - fd) <= 1e-7 * G + 1e-10).all(), np.max(np.abs(gy - fd))
+    assert (G >= np.abs(gy) - 1e-15).all()
+
+
+def pin_grad_xy_balance(orc):
+    """Moving both clouds by the same vector leaves a unchanged, so the x- and
+    y-gradients of any sum g.a add up to zero over the points, coordinate by coordinate."""
+    r = _rng(19)
+    x = r.standard_normal((11, 4))
+    y = r.standard_normal((7, 4))
+    b = r.standard_normal((7, 3))
+    g = r.standard_normal((11, 3))
+    gx, Gx = orc.gauss_grad_x(x, y, b, g, 1.1)
+    gy, Gy = orc.gauss_grad_y(x, y, b, g, 1.1)
+    tot = gx.sum(0) + gy.sum(0)
+    assert (np.abs(tot) <= 1e-13 * (Gx.sum(0) + Gy.sum(0))).all(), tot
+
+
+def pin_grad_y_rows_independent(orc):
+    """Rows j of gy depend on row j of y and b only (a subset gives the same rows)."""
+    r = _rng(20)
+    x = r.standard_normal((6, 2))
+    y = r.standard_normal((10, 2))
+    b = r.standard_normal((10, 1))
+    g = r.standard_normal((6, 1))
+    gy, _ = orc.gauss_grad_y(x, y, b, g, 0.9)
+    sub = [7, 2, 3]
+    gs, _ = orc.gauss_grad_y(x, y[sub], b[sub], g, 0.9)
+    assert np.array_equal(gs, gy[sub])
+
+
+def pin_grad_b_golden(orc):
+    for case in _golden()["grad_b"]:
+        gb, S = orc.gauss_grad_b(case["x"], case["y"], case["g"], case["sigma"])
+        want = np.array([[_val(e) for e in row] for row in case["expect"]])
+        _close(gb, want, 1e-14, 1e-15, case["name"])
+
+
+def pin_grad_b_linearity(orc):
+    """a is linear in b, so L(b + t e_je) - L(b) = t gb_je exactly (up to rounding) for the
+    pinned Sum; checked for every (j, e)."""
+    r = _rng(21)
+    M, N, D, E, sigma = 7, 6, 3, 2, 0.8
+    x = r.standard_normal((M, D))
+    y = r.standard_normal((N, D))
+    b = r.standard_normal((N, E))
+    g = r.standard_normal((M, E))
+    gb, S = orc.gauss_grad_b(x, y, g, sigma)
+    a0, _ = orc.gauss_sum(x, y, b, sigma)
+    for j in range(N):
+        for e in range(E):
+            bp = b.copy(); bp[j, e] += 1.0
+            a1, _ = orc.gauss_sum(x, y, bp, sigma)
+            assert abs(np.sum(g * (a1 - a0)) - gb[j, e]) <= 1e-12 * (S[j, e] + 1), (j, e)
+
+
+def pin_grad_b_bruteforce_scipy(orc):
+    """Tiny inputs against SciPy's distance matrix: gb = K^T g."""
+    from scipy.spatial.distance import cdist
+    r = _rng(22)
+    for (M, N, D, E, sigma) in [(8, 5, 3, 2, 0.6), (3, 12, 1, 1, 2.0)]:
+        x = r.standard_normal((M, D))
+        y = r.standard_normal((N, D))
+        g = r.standard_normal((M, E))
+        gb, S = orc.gauss_grad_b(x, y, g, sigma)
+        Kd = np.exp(-cdist(x, y, "sqeuclidean") / sigma ** 2)
+        _close(gb, Kd.T @ g, 1e-12, 1e-14, "transposed product")
+        _close(S, Kd.T @ np.abs(g), 1e-12, 1e-14, "transposed scale")
+
+
+# ---------------------------------------------------------------------------
 # K-min / ArgMin
 # ---------------------------------------------------------------------------
 def pin_knn_golden(orc):

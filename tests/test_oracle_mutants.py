@@ -39,6 +39,19 @@ MUTANTS = [
      "double diff = y[j * D + d] - x[i * D + d];", 0),
     ("grad_drops_signal", "beta += g[i * E + e] * b[j * E + e];", "beta += g[i * E + e];", 0),
     ("grad_wrong_row_of_g", "beta += g[i * E + e] * b[j * E + e];", "beta += g[e] * b[j * E + e];", 0),
+    ("grad_y_sign", "double term = (2.0 / (sigma * sigma)) * k * beta * diff;",
+     "double term = -(2.0 / (sigma * sigma)) * k * beta * diff;", 0),
+    ("grad_y_drops_signal", "beta += g[i * E + e] * b[j * E + e];", "beta += g[i * E + e];", 1),
+    ("grad_y_wrong_row_of_b", "beta += g[i * E + e] * b[j * E + e];", "beta += g[i * E + e] * b[e];", 1),
+    ("grad_y_drops_last_row",
+     "for (int64_t i = 0; i < M; ++i) {\n                double k = gauss(x + i * D, y + j * D, D, sigma);\n                double beta",
+     "for (int64_t i = 0; i < M - 1; ++i) {\n                double k = gauss(x + i * D, y + j * D, D, sigma);\n                double beta", 0),
+    ("grad_b_drops_kernel", "double term = gauss(x + i * D, y + j * D, D, sigma) * g[i * E + e];",
+     "double term = g[i * E + e];", 0),
+    ("grad_b_wrong_column", "double term = gauss(x + i * D, y + j * D, D, sigma) * g[i * E + e];",
+     "double term = gauss(x + i * D, y + j * D, D, sigma) * g[i * E];", 0),
+    ("grad_b_uses_j_row_of_g", "double term = gauss(x + i * D, y + j * D, D, sigma) * g[i * E + e];",
+     "double term = gauss(x + i * D, y + j * D, D, sigma) * g[(j % M) * E + e];", 0),
     ("knn_tie_highest_index", "(d1 == d2 && j1 < j2)", "(d1 == d2 && j1 > j2)", 0),
     ("knn_largest_first", "return d1 < d2 ||", "return d1 > d2 ||", 0),
     ("knn_next_is_kth", "next[i] = (K < n) ? bd[K] : INFINITY;",
