@@ -382,7 +382,8 @@ def _time_op(torch, fn, reps):
 def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
     """One timed set (1 warm-up + 2 runs) per other workload, with its roofline."""
     out = []
-    plan = [("gauss_d3_unit", [("sum", "b"), ("lse", "w_log")]), ("falkon_d50", [("sum", "b")]),
+    plan = [("gauss_d3", [("grad_y", None), ("grad_b", None)]),
+            ("gauss_d3_unit", [("sum", "b"), ("lse", "w_log")]), ("falkon_d50", [("sum", "b")]),
             ("knn_d16", [("knn", None)])]
     for wname, ops in plan:
         inp = W.generate(wname)
@@ -391,6 +392,25 @@ def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
         N = y.shape[0]
         s = inp["sigma"]
         for op, key in ops:
+            if op in ("grad_y", "grad_b"):
+                # the transposed problem: N output rows, reduction over the M points of x
+                bb, gg = (torch.from_numpy(inp[k]).to(dev) for k in ("b", "g"))
+                E = bb.shape[1]
+                if op == "grad_y":
+                    fn = (lambda bb=bb, gg=gg: kr.kernel_reduce_grad_y(x, y, bb, gg, s))
+                    p = kr.plan_device(kr.OP_GRAD, N, M, D, E)
+                    kname = f"grad_kernel[D={D},E={E}] on (y, x)"
+                else:
+                    fn = (lambda gg=gg: kr.kernel_reduce_grad_b(x, y, gg, s))
+                    p = kr.plan_device(kr.OP_SUM, N, M, D, E)
+                    kname = f"fwd_kernel<Sum>[D={D},E={E}] on (y, x)"
+                ms = _time_op(torch, fn, 5)
+                rl = roofline("grad" if op == "grad_y" else "sum", D, E, ms / 1e3, M * N, nsm, max_mhz, xu_lanes,
+                              kname)
+                out.append({"workload": f"{wname}: {W.WORKLOADS[wname].note}", "op": op, "ms": ms,
+                            "value": M * N / (ms / 1e3), "unit": UNIT, "split": p.split, "path": "cuda cores",
+                            "roofline": rl})
+                continue
             if op == "knn":
                 K = inp["K"]
                 fn = (lambda: kr.kernel_knn(x, y, K))

@@ -9,6 +9,9 @@
  *   LogSumExp L_ie = log sum_j exp(-|x_i - y_j|^2 / sigma^2 + w_je)
  *   grad-x    gx_id = d/dx_id sum_{i,e} g_ie a_ie
  *                   = -(2/sigma^2) sum_j k_ij (sum_e g_ie b_je)(x_id - y_jd)
+ *   grad-y    gy_jd = d/dy_jd sum_{i,e} g_ie a_ie
+ *                   = (2/sigma^2) sum_i k_ij (sum_e g_ie b_je)(x_id - y_jd)
+ *   grad-b    gb_je = d/db_je sum_{i,e} g_ie a_ie = sum_i k_ij g_ie
  *   K-min     the K pairs (|x_i - y_j|^2, j) that are smallest in lexicographic
  *             order, sorted ascending; K = 1 is ArgMin.
  *
@@ -25,8 +28,9 @@
  * ---------------------------------------
  * Memory.   All arrays are float32 (int32 for indices), row-major, contiguous:
  *           x: M x D, y: N x D, b and w: N x E, g: M x E, out: M x E,
- *           gx: M x D, idx and dist: M x K.  Each pointer may address device
- *           memory or host memory (pageable or pinned); host arrays are staged
+ *           gx: M x D, gy: N x D, gb: N x E, idx and dist: M x K.  Each
+ *           pointer may address device memory or host memory (pageable or
+ *           pinned); host arrays are staged
  *           through device memory allocated for the call, and the call then
  *           blocks until its host outputs are written.  With device pointers
  *           only, the call is asynchronous on `stream`.
@@ -148,6 +152,34 @@ int kernel_reduce_grad_x(const float *x, const float *y, const float *b, const f
 int kernel_reduce_grad_x_ex(const float *x, const float *y, const float *b, const float *g,
                             float *gx, int64_t M, int64_t N, int D, int E, float sigma,
                             kr_stream_t stream, const kr_options *opt);
+
+/*
+ * Gradient wrt y of sum_{i,e} g_ie a_ie ("Kernel Operations on the GPU...", §2
+ * "Performance and differentiation": gradients wrt every input through autodiff):
+ *   gy_jd = (2/sigma^2) sum_i k_ij (sum_e g_ie b_je) (x_id - y_jd).
+ *   x [M x D], y [N x D], b [N x E], g [M x E] (upstream gradient), gy [N x D] output.
+ * Computed by the x-gradient kernels with the two clouds exchanged, so it plans,
+ * splits and performs exactly like kernel_reduce_grad_x on (y, x).
+ */
+int kernel_reduce_grad_y(const float *x, const float *y, const float *b, const float *g,
+                         float *gy, int64_t M, int64_t N, int D, int E, float sigma,
+                         kr_stream_t stream);
+int kernel_reduce_grad_y_ex(const float *x, const float *y, const float *b, const float *g,
+                            float *gy, int64_t M, int64_t N, int D, int E, float sigma,
+                            kr_stream_t stream, const kr_options *opt);
+
+/*
+ * Gradient wrt b of sum_{i,e} g_ie a_ie, the transposed product
+ *   gb_je = sum_i k_ij g_ie
+ * (same section; a is linear in b).  x [M x D], y [N x D], g [M x E], gb [N x E]
+ * output.  Computed as kernel_reduce(y, x, g) (the Gaussian is symmetric), so it
+ * takes the tensor-core path under the same conditions as that call.
+ */
+int kernel_reduce_grad_b(const float *x, const float *y, const float *g, float *gb,
+                         int64_t M, int64_t N, int D, int E, float sigma, kr_stream_t stream);
+int kernel_reduce_grad_b_ex(const float *x, const float *y, const float *g, float *gb,
+                            int64_t M, int64_t N, int D, int E, float sigma, kr_stream_t stream,
+                            const kr_options *opt);
 
 /*
  * K-min / ArgMin over squared Euclidean distance (KeOps README feature list:

@@ -10,13 +10,15 @@ Functions, named after the C entry points (see ``include/kreduce.h``):
 
 * ``kernel_reduce(x, y, b, sigma, reduction="sum"|"lse", out=None, split=0)``
 * ``kernel_reduce_grad_x(x, y, b, g, sigma, out=None, split=0)``
+* ``kernel_reduce_grad_y(x, y, b, g, sigma, out=None, split=0)``
+* ``kernel_reduce_grad_b(x, y, g, sigma, out=None, split=0)``
 * ``kernel_knn(x, y, K, idx=None, dist=None, split=0)``
 
 Arguments are float32 torch tensors, contiguous, row-major: x (M, D), y (N, D),
 b (N, E) or (N,), g (M, E) or (M,).  CUDA tensors run asynchronously on the
 current stream; CPU tensors are staged through device memory by the library and
 the call blocks until the result is back.  ``GaussianSum`` wraps the Sum with its
-x-gradient as a ``torch.autograd.Function``.
+x-, y- and b-gradients as a ``torch.autograd.Function``.
 """
 from __future__ import annotations
 
@@ -35,7 +37,8 @@ OP_SUM, OP_LSE, OP_GRAD, OP_KNN = 0, 1, 2, 3
 
 # Names exported by libkreduce.so, in the order include/kreduce.h declares them.
 EXPORTS = ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_noalloc", "kernel_reduce_grad_x",
-           "kernel_reduce_grad_x_ex",
+           "kernel_reduce_grad_x_ex", "kernel_reduce_grad_y", "kernel_reduce_grad_y_ex",
+           "kernel_reduce_grad_b", "kernel_reduce_grad_b_ex",
            "kernel_knn", "kernel_knn_ex", "kr_status_string", "kr_last_cuda_error", "kr_plan",
            "kr_plan_device")
 
@@ -88,6 +91,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kernel_reduce_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
         lib.kernel_reduce_grad_x.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
         lib.kernel_reduce_grad_x_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
+        lib.kernel_reduce_grad_y.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
+        lib.kernel_reduce_grad_y_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
+        lib.kernel_reduce_grad_b.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
+        lib.kernel_reduce_grad_b_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
         lib.kernel_knn.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp]
         lib.kernel_knn_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp, opt]
         lib.kr_status_string.argtypes = [i32]
@@ -95,10 +102,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kr_last_cuda_error.argtypes = []
         lib.kr_plan.argtypes = [i32, i64, i64, i32, i32, i32, i32, opt, ctypes.POINTER(KrPlan)]
         lib.kr_plan_device.argtypes = [i32, i64, i64, i32, i32, opt, ctypes.POINTER(KrPlan)]
-        for name in ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_noalloc", "kernel_reduce_grad_x",
-                     "kernel_reduce_grad_x_ex",
-                     "kernel_knn", "kernel_knn_ex", "kr_last_cuda_error", "kr_plan", "kr_plan_device"):
-            getattr(lib, name).restype = ctypes.c_int
+        for name in EXPORTS:
+            if name != "kr_status_string":
+                getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -254,6 +260,47 @@ def kernel_reduce_grad_x(x, y, b, g, sigma: float, out=None, split: int = 0):
     return out
 
 
+def kernel_reduce_grad_y(x, y, b, g, sigma: float, out=None, split: int = 0):
+    """Gradient wrt y of sum_ie g_ie a_ie (a the Sum reduction); returns (N, D)."""
+    torch = _torch()
+    x = _mat(x, None, "x")
+    M, D = x.shape
+    y = _mat(y, None, "y", D)
+    N = y.shape[0]
+    b = _mat(b, N, "b")
+    E = b.shape[1]
+    g = _mat(g, M, "g", E)
+    dev = _same_device(x, y, b, g)
+    if out is None:
+        out = torch.empty((N, D), dtype=torch.float32, device=dev)
+    out = _mat(out, N, "out", D)
+    _same_device(x, out)
+    st = load_library().kernel_reduce_grad_y_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(g), _ptr(out), M, N, D, E,
+                                                float(sigma), _stream(dev), _options(split))
+    _check(st, "kernel_reduce_grad_y")
+    return out
+
+
+def kernel_reduce_grad_b(x, y, g, sigma: float, out=None, split: int = 0, path: int = 0):
+    """Gradient wrt b of sum_ie g_ie a_ie: gb_je = sum_i k_ij g_ie; returns (N, E)."""
+    torch = _torch()
+    x = _mat(x, None, "x")
+    M, D = x.shape
+    y = _mat(y, None, "y", D)
+    N = y.shape[0]
+    g = _mat(g, M, "g")
+    E = g.shape[1]
+    dev = _same_device(x, y, g)
+    if out is None:
+        out = torch.empty((N, E), dtype=torch.float32, device=dev)
+    out2 = _mat(out, N, "out", E)
+    _same_device(x, out2)
+    st = load_library().kernel_reduce_grad_b_ex(_ptr(x), _ptr(y), _ptr(g), _ptr(out2), M, N, D, E, float(sigma),
+                                                _stream(dev), _options(split, path))
+    _check(st, "kernel_reduce_grad_b")
+    return out
+
+
 def kernel_knn(x, y, K: int, idx=None, dist=None, want_dist: bool = True, split: int = 0):
     """K smallest (|x_i-y_j|^2, j) per row, ascending, lowest index on ties.
 
@@ -284,26 +331,31 @@ def _make_gaussian_sum():
     torch = _torch()
 
     class GaussianSum(torch.autograd.Function):
-        """a = sum_j exp(-|x_i-y_j|^2/sigma^2) b_j, differentiable wrt x.
+        """a = sum_j exp(-|x_i-y_j|^2/sigma^2) b_j, differentiable wrt x, y and b.
 
-        Gradients wrt y and b are not provided (they raise if requested)."""
+        The backward pass runs the library's x-gradient, y-gradient and transposed
+        product (b-gradient) kernels for the inputs that need a gradient."""
 
         @staticmethod
         def forward(ctx, x, y, b, sigma):
             ctx.save_for_backward(x, y, b)
             ctx.sigma = float(sigma)
+            ctx.b_shape = b.shape
             return kernel_reduce(x.detach(), y.detach(), b.detach(), sigma, "sum")
 
         @staticmethod
         def backward(ctx, grad_out):
             x, y, b = ctx.saved_tensors
-            if ctx.needs_input_grad[1] or ctx.needs_input_grad[2]:
-                raise NotImplementedError("GaussianSum differentiates wrt x only")
-            gx = None
+            xd, yd, bd = x.detach(), y.detach(), b.detach().contiguous().view(y.shape[0], -1)
+            g = grad_out.contiguous().view(x.shape[0], -1)
+            gx = gy = gb = None
             if ctx.needs_input_grad[0]:
-                gx = kernel_reduce_grad_x(x.detach(), y.detach(), b.detach(),
-                                          grad_out.contiguous().view(x.shape[0], -1), ctx.sigma)
-            return gx, None, None, None
+                gx = kernel_reduce_grad_x(xd, yd, bd, g, ctx.sigma)
+            if ctx.needs_input_grad[1]:
+                gy = kernel_reduce_grad_y(xd, yd, bd, g, ctx.sigma)
+            if ctx.needs_input_grad[2]:
+                gb = kernel_reduce_grad_b(xd, yd, g, ctx.sigma).view(ctx.b_shape)
+            return gx, gy, gb, None
 
     return GaussianSum
 

@@ -529,6 +529,44 @@ int kernel_reduce_grad_x(const float *x, const float *y, const float *b, const f
     return kernel_reduce_grad_x_ex(x, y, b, g, gx, M, N, D, E, sigma, stream, nullptr);
 }
 
+// The y-gradient is the x-gradient kernel with the clouds' roles exchanged: with
+// X = y, Y = x, B = g, G = b it computes -(2/sigma^2) sum_i k_ij (sum_e b_je g_ie)
+// (y_jd - x_id), which is d/dy_jd of sum_ie g_ie a_ie.
+int kernel_reduce_grad_y_ex(const float *x, const float *y, const float *b, const float *g, float *gy,
+                            int64_t M, int64_t N, int D, int E, float sigma, kr_stream_t stream,
+                            const kr_options *opt) {
+    if (M < 0 || N < 0 || D < 1 || E < 1) return KR_ERR_INVALID;
+    const int64_t f = (int64_t)sizeof(float);
+    Buf bufs[5] = {{y, N * D * f, false}, {x, M * D * f, false}, {g, M * E * f, false},
+                   {b, N * E * f, false}, {gy, N * D * f, true}};
+    Args a{};
+    a.M = N;
+    a.N = M;
+    a.D = D;
+    a.E = E;
+    const double c = std::sqrt(1.4426950408889634) / (double)sigma;
+    a.c = (float)c;
+    a.gscale = (float)(-2.0 / ((double)sigma * (double)sigma * c));
+    return run(OP_GRAD, bufs, 5, a, E, sigma, (cudaStream_t)stream, opt);
+}
+
+int kernel_reduce_grad_y(const float *x, const float *y, const float *b, const float *g, float *gy, int64_t M,
+                         int64_t N, int D, int E, float sigma, kr_stream_t stream) {
+    return kernel_reduce_grad_y_ex(x, y, b, g, gy, M, N, D, E, sigma, stream, nullptr);
+}
+
+// The b-gradient sum_i k_ij g_ie is the Sum reduction over i of the exchanged clouds
+// (the Gaussian is symmetric in its two points).
+int kernel_reduce_grad_b_ex(const float *x, const float *y, const float *g, float *gb, int64_t M, int64_t N,
+                            int D, int E, float sigma, kr_stream_t stream, const kr_options *opt) {
+    return kernel_reduce_ex(y, x, g, gb, N, M, D, E, sigma, KR_SUM, stream, opt);
+}
+
+int kernel_reduce_grad_b(const float *x, const float *y, const float *g, float *gb, int64_t M, int64_t N, int D,
+                         int E, float sigma, kr_stream_t stream) {
+    return kernel_reduce_grad_b_ex(x, y, g, gb, M, N, D, E, sigma, stream, nullptr);
+}
+
 int kernel_knn_ex(const float *x, const float *y, int32_t *idx, float *dist, int64_t M, int64_t N, int D,
                   int K, kr_stream_t stream, const kr_options *opt) {
     if (M < 0 || N < 0 || D < 1 || K < 1) return KR_ERR_INVALID;

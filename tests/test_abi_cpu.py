@@ -103,6 +103,30 @@ def test_grad_and_knn_validation(lib):
     assert k(None, None, None, None, 0, 0, 3, 4, None, None) == kr.KR_OK
 
 
+def test_grad_y_and_grad_b_validation(lib):
+    gy = lib.kernel_reduce_grad_y_ex
+    # argument order: x, y, b, g, gy -- each pointer checked
+    for k in range(5):
+        ptrs = list(FAKE[:5])
+        ptrs[k] = None
+        assert gy(*ptrs, 10, 20, 3, 1, 1.0, None, None) == kr.KR_ERR_INVALID, k
+    assert gy(*FAKE[:5], 10, 20, 3, 1, -2.0, None, None) == kr.KR_ERR_INVALID
+    assert gy(*FAKE[:5], 10, 20, 3, 17, 1.0, None, None) == kr.KR_ERR_UNSUPPORTED
+    # gy (N x D) overlapping y
+    assert gy(FAKE[0], FAKE[1], FAKE[2], FAKE[3], P(0x20000 + 4), 10, 20, 3, 1, 1.0, None, None) == kr.KR_ERR_INVALID
+    assert gy(None, None, None, None, None, 5, 0, 3, 1, 1.0, None, None) == kr.KR_ERR_INVALID  # x missing, M > 0
+    assert gy(None, None, None, None, None, 0, 0, 3, 1, 1.0, None, None) == kr.KR_OK
+    gb = lib.kernel_reduce_grad_b_ex
+    for k in range(4):
+        ptrs = list(FAKE[:4])
+        ptrs[k] = None
+        assert gb(*ptrs, 10, 20, 3, 2, 1.0, None, None) == kr.KR_ERR_INVALID, k
+    assert gb(*FAKE[:4], 10, 20, 3, 2, float("nan"), None, None) == kr.KR_ERR_INVALID
+    assert gb(*FAKE[:4], 10, 20, 129, 2, 1.0, None, None) == kr.KR_ERR_UNSUPPORTED
+    # N = 0: nothing to write (the transposed product has no rows)
+    assert gb(FAKE[0], None, FAKE[2], None, 10, 0, 3, 2, 1.0, None, None) == kr.KR_OK
+
+
 # ---------------------------------------------------------------------------
 # planner (pure host logic)
 # ---------------------------------------------------------------------------
