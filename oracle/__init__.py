@@ -12,6 +12,10 @@ Functions (each follows the passage cited in ``oracle.c``):
 * ``gauss_grad_x(x, y, b, g, sigma)`` -> (gx, G)  x-gradient of sum(g * a) and its scale
 * ``gauss_grad_y(x, y, b, g, sigma)`` -> (gy, G)  y-gradient of sum(g * a) and its scale
 * ``gauss_grad_b(x, y, g, sigma)``    -> (gb, S)  b-gradient (transposed product) and its scale
+* ``kernel_sum(x, y, b, sigma, kernel)`` -> (a, S)  Sum with a Gaussian, Laplace, Cauchy or
+  inverse-multiquadric kernel
+* ``kernel_maxmin(x, y, b, sigma, kernel, "max"|"min")`` -> (val, idx, second)  Max / Min of
+  k b over j with the lowest attaining index and the runner-up value
 * ``knn(x, y, K)``                -> (idx, dist, next)  K-min by (distance, index)
 
 Inputs may be float32 or float64 arrays; they are converted to float64 (exact for
@@ -74,6 +78,11 @@ class Oracle:
                                             ctypes.c_int, ctypes.c_int, ctypes.c_double, _dp, _dp]
         lib.oracle_gauss_grad_b.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int, ctypes.c_int, ctypes.c_double, _dp, _dp]
+        lib.oracle_kernel_sum.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_double, ctypes.c_int, _dp, _dp]
+        lib.oracle_kernel_maxmin.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, _dp,
+                                             _i64p, _dp]
         lib.oracle_knn.argtypes = [_dp, _dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                    ctypes.c_int, _i64p, _dp, _dp]
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -162,6 +171,32 @@ class Oracle:
                                       _ptr(gb), _ptr(S))
         return gb, S
 
+    def kernel_sum(self, x, y, b, sigma, kernel):
+        x, y = self._points(x, y)
+        M, D = x.shape
+        N = y.shape[0]
+        b = _as2d(b, N, "b")
+        E = b.shape[1]
+        a = np.empty((M, E))
+        S = np.empty((M, E))
+        self._lib.oracle_kernel_sum(_ptr(x), _ptr(y), _ptr(b), M, N, D, E, float(sigma), KERNELS[kernel],
+                                    _ptr(a), _ptr(S))
+        return a, S
+
+    def kernel_maxmin(self, x, y, b, sigma, kernel, reduction):
+        x, y = self._points(x, y)
+        M, D = x.shape
+        N = y.shape[0]
+        b = _as2d(b, N, "b")
+        E = b.shape[1]
+        sense = {"max": 1, "min": -1}[reduction]
+        val = np.empty((M, E))
+        idx = np.empty((M, E), dtype=np.int64)
+        second = np.empty((M, E))
+        self._lib.oracle_kernel_maxmin(_ptr(x), _ptr(y), _ptr(b), M, N, D, E, float(sigma), KERNELS[kernel],
+                                       sense, _ptr(val), idx.ctypes.data_as(_i64p), _ptr(second))
+        return val, idx, second
+
     def knn(self, x, y, K):
         x, y = self._points(x, y)
         M, D = x.shape
@@ -176,6 +211,9 @@ class Oracle:
                              idx.ctypes.data_as(_i64p), _ptr(dist), _ptr(nxt))
         return idx, dist, nxt
 
+
+# Radial kernels of oracle_kernel_sum / oracle_kernel_maxmin, by name.
+KERNELS = {"gaussian": 0, "laplace": 1, "cauchy": 2, "imq": 3}
 
 _default = None
 

@@ -234,6 +234,91 @@ void oracle_gauss_grad_b(const double *x, const double *y, const double *g,
     }
 }
 
+/*
+ * Other radial kernels of the squared distance q = |x - y|^2 and width sigma
+ * ("Kernel Operations on the GPU...", §2: reductions of generic formulas F(x_i, y_j);
+ * KeOps README: "support for a wide range of mathematical formulas").  kind:
+ *   0 Gaussian               exp(-q / sigma^2)
+ *   1 Laplace (exponential)  exp(-sqrt(q) / sigma)
+ *   2 Cauchy                 1 / (1 + q / sigma^2)
+ *   3 inverse multiquadric   1 / sqrt(1 + q / sigma^2)
+ * Each is 1 at q = 0 and decreases to 0 as q grows.
+ */
+static double radial_kernel(int kind, double q, double sigma)
+{
+    switch (kind) {
+    case 0: return exp(-q / (sigma * sigma));
+    case 1: return exp(-sqrt(q) / sigma);
+    case 2: return 1.0 / (1.0 + q / (sigma * sigma));
+    case 3: return 1.0 / sqrt(1.0 + q / (sigma * sigma));
+    default: return NAN;
+    }
+}
+
+/*
+ * Sum reduction with any of the radial kernels above:
+ *   a_ie = sum_j k(x_i, y_j) b_je, summed in increasing j, with the scale
+ *   S_ie = sum_j |k(x_i, y_j) b_je|.
+ */
+void oracle_kernel_sum(const double *x, const double *y, const double *b,
+                       int64_t M, int64_t N, int D, int E, double sigma, int kind,
+                       double *a, double *scale)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int e = 0; e < E; ++e) {
+            double s = 0.0, c = 0.0, sa = 0.0, ca = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                double k = radial_kernel(kind, sq_dist(x + i * D, y + j * D, D), sigma);
+                double term = k * b[j * E + e];
+                neumaier_add(&s, &c, term);
+                neumaier_add(&sa, &ca, fabs(term));
+            }
+            a[i * E + e] = s + c;
+            if (scale) scale[i * E + e] = sa + ca;
+        }
+    }
+}
+
+/*
+ * Max (sense = +1) or Min (sense = -1) reduction of the formula F_ije = k(x_i, y_j) b_je
+ * over j, with its Arg: val[i*E+e] = the extreme value, idx[i*E+e] = the lowest j
+ * that attains it ("Kernel Operations on the GPU...", §2: max, min and argmin
+ * reductions; KeOps README feature list: Min, Max, ArgMin, ArgMax).  N = 0 gives
+ * -inf (Max) / +inf (Min) and index -1.
+ * second[i*E+e] (if not NULL) is the best value over the other j (the runner-up,
+ * equal to val when the extreme is attained twice); the parity tests use it to
+ * find near-ties.  A plain scan in increasing j that replaces the best only on a
+ * strictly better value.
+ */
+void oracle_kernel_maxmin(const double *x, const double *y, const double *b,
+                          int64_t M, int64_t N, int D, int E, double sigma, int kind,
+                          int sense, double *val, int64_t *idx, double *second)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int e = 0; e < E; ++e) {
+            double best = sense > 0 ? -INFINITY : INFINITY, runner = best;
+            int64_t bj = -1;
+            for (int64_t j = 0; j < N; ++j) {
+                double f = radial_kernel(kind, sq_dist(x + i * D, y + j * D, D), sigma) * b[j * E + e];
+                int better = sense > 0 ? f > best : f < best;
+                if (better) {
+                    runner = best;
+                    best = f;
+                    bj = j;
+                } else {
+                    int beats_runner = sense > 0 ? f > runner : f < runner;
+                    if (beats_runner || f == best) runner = f;
+                }
+            }
+            val[i * E + e] = best;
+            idx[i * E + e] = bj;
+            if (second) second[i * E + e] = runner;
+        }
+    }
+}
+
 /* (d1, j1) < (d2, j2) in lexicographic order: smaller distance first, then the
  * lower index. */
 static int lex_less(double d1, int64_t j1, double d2, int64_t j2)

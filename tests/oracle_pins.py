@@ -402,6 +402,157 @@ def pin_grad_b_bruteforce_scipy(orc):
 
 
 # ---------------------------------------------------------------------------
+# other radial kernels (Sum) and the Max / Min reductions
+# ---------------------------------------------------------------------------
+KERNEL_FNS = {   # written from each kernel's definition, for the brute-force pins
+    "gaussian": lambda q, s: np.exp(-q / s ** 2),
+    "laplace": lambda q, s: np.exp(-np.sqrt(q) / s),
+    "cauchy": lambda q, s: 1.0 / (1.0 + q / s ** 2),
+    "imq": lambda q, s: 1.0 / np.sqrt(1.0 + q / s ** 2),
+}
+
+
+def pin_kernel_sum_golden(orc):
+    for case in _golden()["kernel_sum"]:
+        for sigma, expect in zip(case["sigmas"], case["expect"]):
+            a, _ = orc.kernel_sum(case["x"], case["y"], case["b"], sigma, case["kernel"])
+            want = np.array([[_val(e) for e in row] for row in expect])
+            _close(a, want, 1e-14, 0, f"{case['name']} sigma {sigma}")
+
+
+def pin_kernel_sum_bruteforce_scipy(orc):
+    """Every kernel against SciPy's distance matrix and a dense product."""
+    from scipy.spatial.distance import cdist
+    r = _rng(23)
+    for kern, fn in KERNEL_FNS.items():
+        for (M, N, D, E, sigma) in [(6, 13, 3, 2, 0.7), (9, 4, 5, 1, 2.0)]:
+            x = r.standard_normal((M, D))
+            y = r.standard_normal((N, D))
+            b = r.standard_normal((N, E))
+            a, S = orc.kernel_sum(x, y, b, sigma, kern)
+            Kd = fn(cdist(x, y, "sqeuclidean"), sigma)
+            _close(a, Kd @ b, 1e-12, 1e-14, f"{kern} dense product")
+            _close(S, Kd @ np.abs(b), 1e-12, 1e-14, f"{kern} dense scale")
+
+
+def pin_kernel_sum_gaussian_matches(orc):
+    """kind 0 is the Gaussian of the pinned Sum."""
+    r = _rng(24)
+    x, y, b = r.standard_normal((5, 3)), r.standard_normal((17, 3)), r.standard_normal((17, 2))
+    a0, S0 = orc.gauss_sum(x, y, b, 0.9)
+    a1, S1 = orc.kernel_sum(x, y, b, 0.9, "gaussian")
+    _close(a1, a0, 1e-15, 0, "gaussian kind")
+
+
+def pin_laplace_lattice_sum(orc):
+    """On a uniform 1-D lattice of spacing h through x, sum_k h exp(-|k| h / sigma)
+    = h coth(h / (2 sigma)) (a geometric series); the lattice runs to 45 sigma, so the
+    truncated tails are below 1e-19.  Fixes the square root and the sigma convention."""
+    for sigma, h in ((0.8, 0.1), (2.0, 0.37)):
+        n = int(45 * sigma / h)
+        y = (h * np.arange(-n, n + 1))[:, None] + 0.25
+        a, _ = orc.kernel_sum(np.array([[0.25]]), y, np.full((2 * n + 1, 1), h), sigma, "laplace")
+        _close(a[0, 0], h / math.tanh(h / (2 * sigma)), 1e-12, 0, f"laplace lattice sigma {sigma}")
+
+
+def pin_cauchy_lattice_sum(orc):
+    """sum_{|k| <= n} h / (1 + (k h / sigma)^2) = h a^2 [ (pi / a) coth(pi a) - 2 Im psi(n + 1 + i a) / a ]
+    with a = sigma / h: the Mittag-Leffler series of coth minus its tail, the tail
+    written with the digamma function (SciPy, complex argument)."""
+    from scipy.special import psi
+    for sigma, h, n in ((0.5, 0.1, 400), (1.5, 0.25, 1000)):
+        y = (h * np.arange(-n, n + 1))[:, None] - 1.0
+        a, _ = orc.kernel_sum(np.array([[-1.0]]), y, np.full((2 * n + 1, 1), h), sigma, "cauchy")
+        al = sigma / h
+        full = (math.pi / al) / math.tanh(math.pi * al)
+        tail = psi(complex(n + 1, al)).imag / al
+        _close(a[0, 0], h * al * al * (full - 2 * tail), 1e-11, 0, f"cauchy lattice sigma {sigma}")
+
+
+def pin_imq_squared_is_cauchy(orc):
+    """One point: the inverse multiquadric squared is the Cauchy kernel; both are 1 at x = y
+    and lie in (0, 1], so with b = 1 the sums lie in (0, N]."""
+    r = _rng(25)
+    x = r.standard_normal((7, 4))
+    y = r.standard_normal((1, 4))
+    ai, _ = orc.kernel_sum(x, y, np.ones((1, 1)), 1.3, "imq")
+    ac, _ = orc.kernel_sum(x, y, np.ones((1, 1)), 1.3, "cauchy")
+    _close(ai ** 2, ac, 1e-14, 0, "imq^2 = cauchy")
+    yy = r.standard_normal((30, 4))
+    for kern in KERNEL_FNS:
+        a, _ = orc.kernel_sum(yy[:3], yy, np.ones((30, 1)), 0.6, kern)
+        assert (a >= 1.0).all() and (a <= 30).all(), kern
+        a1, _ = orc.kernel_sum(yy[:1], yy[:1], np.full((1, 1), 2.5), 0.6, kern)
+        assert a1[0, 0] == 2.5, kern
+
+
+def pin_kernel_sum_scale_law(orc):
+    """a(x, y; sigma) = a(x / sigma, y / sigma; 1) for every kernel (all are functions of |x - y| / sigma)."""
+    r = _rng(26)
+    x, y, b = r.standard_normal((4, 3)), r.standard_normal((21, 3)), r.standard_normal((21, 1))
+    for kern in KERNEL_FNS:
+        a0, _ = orc.kernel_sum(x, y, b, 0.45, kern)
+        a1, _ = orc.kernel_sum(x / 0.45, y / 0.45, b, 1.0, kern)
+        _close(a1, a0, 1e-12, 1e-14, f"{kern} scale law")
+
+
+def pin_maxmin_golden(orc):
+    for case in _golden()["maxmin"]:
+        for red in ("max", "min"):
+            val, idx, second = orc.kernel_maxmin(case["x"], case["y"], case["b"], case["sigma"], case["kernel"], red)
+            want = case[red]
+            _close(val[:, 0], [_val(v) for v in want["val"]], 1e-15, 0, f"{case['name']} {red}")
+            assert idx[:, 0].tolist() == want["idx"], (case["name"], red, idx)
+            _close(second[:, 0], [_val(v) for v in want["second"]], 1e-15, 0, f"{case['name']} {red} second")
+
+
+def pin_maxmin_bruteforce_numpy(orc):
+    """Against NumPy's max/argmax (first occurrence) on the dense formula, including
+    exact ties from points on an integer grid."""
+    from scipy.spatial.distance import cdist
+    r = _rng(27)
+    for kern, fn in KERNEL_FNS.items():
+        x = r.integers(-2, 3, size=(12, 2)).astype(float)
+        y = r.integers(-2, 3, size=(40, 2)).astype(float)
+        b = r.integers(-2, 3, size=(40, 3)).astype(float)
+        F = fn(cdist(x, y, "sqeuclidean"), 1.1)[:, :, None] * b[None, :, :]
+        for red, pick, arg in (("max", np.max, np.argmax), ("min", np.min, np.argmin)):
+            val, idx, second = orc.kernel_maxmin(x, y, b, 1.1, kern, red)
+            _close(val, pick(F, axis=1), 1e-14, 1e-300, f"{kern} {red}")
+            assert np.array_equal(idx, arg(F, axis=1)), (kern, red)
+            for i in range(12):
+                for e in range(3):
+                    rest = np.delete(F[i, :, e], idx[i, e])
+                    _close(second[i, e], pick(rest), 1e-14, 1e-300, f"{kern} {red} runner-up")
+
+
+def pin_max_unit_weights_is_nearest(orc):
+    """b = 1: every kernel decreases with distance, so ArgMax is the nearest point (the
+    pinned K-min with K = 1, same lowest-index rule) and the Max is k at that distance."""
+    r = _rng(28)
+    x = np.round(r.standard_normal((15, 3)) * 2) / 2
+    y = np.round(r.standard_normal((50, 3)) * 2) / 2
+    i1, d1, _ = orc.knn(x, y, 1)
+    for kern, fn in KERNEL_FNS.items():
+        val, idx, _ = orc.kernel_maxmin(x, y, np.ones((50, 1)), 0.8, kern, "max")
+        assert np.array_equal(idx[:, 0], i1[:, 0]), kern
+        _close(val[:, 0], fn(d1[:, 0], 0.8), 1e-14, 0, kern)
+
+
+def pin_min_is_negated_max(orc):
+    """Min(k b) = -Max(k (-b)) with the same index; N = 0 gives -inf / +inf and -1."""
+    r = _rng(29)
+    x, y, b = r.standard_normal((6, 3)), r.standard_normal((25, 3)), r.standard_normal((25, 2))
+    vmin, imin, smin = orc.kernel_maxmin(x, y, b, 0.7, "cauchy", "min")
+    vmax, imax, smax = orc.kernel_maxmin(x, y, -b, 0.7, "cauchy", "max")
+    assert np.array_equal(vmin, -vmax) and np.array_equal(imin, imax) and np.array_equal(smin, -smax)
+    v, i, _ = orc.kernel_maxmin(x, np.zeros((0, 3)), np.zeros((0, 2)), 1.0, "gaussian", "max")
+    assert np.isneginf(v).all() and (i == -1).all()
+    v, i, _ = orc.kernel_maxmin(x, np.zeros((0, 3)), np.zeros((0, 2)), 1.0, "gaussian", "min")
+    assert np.isposinf(v).all() and (i == -1).all()
+
+
+# ---------------------------------------------------------------------------
 # K-min / ArgMin
 # ---------------------------------------------------------------------------
 def pin_knn_golden(orc):

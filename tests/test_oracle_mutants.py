@@ -52,6 +52,22 @@ MUTANTS = [
      "double term = gauss(x + i * D, y + j * D, D, sigma) * g[i * E];", 0),
     ("grad_b_uses_j_row_of_g", "double term = gauss(x + i * D, y + j * D, D, sigma) * g[i * E + e];",
      "double term = gauss(x + i * D, y + j * D, D, sigma) * g[(j % M) * E + e];", 0),
+    ("laplace_without_sqrt", "case 1: return exp(-sqrt(q) / sigma);", "case 1: return exp(-q / sigma);", 0),
+    ("laplace_sigma_squared", "case 1: return exp(-sqrt(q) / sigma);",
+     "case 1: return exp(-sqrt(q) / (sigma * sigma));", 0),
+    ("cauchy_drops_one", "case 2: return 1.0 / (1.0 + q / (sigma * sigma));",
+     "case 2: return 1.0 / (q / (sigma * sigma) + 1e-300);", 0),
+    ("cauchy_sigma_not_squared", "case 2: return 1.0 / (1.0 + q / (sigma * sigma));",
+     "case 2: return 1.0 / (1.0 + q / sigma);", 0),
+    ("imq_without_sqrt", "case 3: return 1.0 / sqrt(1.0 + q / (sigma * sigma));",
+     "case 3: return 1.0 / (1.0 + q / (sigma * sigma));", 0),
+    ("maxmin_ties_keep_last", "int better = sense > 0 ? f > best : f < best;",
+     "int better = sense > 0 ? f >= best : f <= best;", 0),
+    ("maxmin_min_is_max", "int better = sense > 0 ? f > best : f < best;", "int better = f > best;", 0),
+    ("maxmin_runner_not_shifted", "                    runner = best;\n", "", 0),
+    ("maxmin_drops_signal",
+     "double f = radial_kernel(kind, sq_dist(x + i * D, y + j * D, D), sigma) * b[j * E + e];",
+     "double f = radial_kernel(kind, sq_dist(x + i * D, y + j * D, D), sigma);", 0),
     ("knn_tie_highest_index", "(d1 == d2 && j1 < j2)", "(d1 == d2 && j1 > j2)", 0),
     ("knn_largest_first", "return d1 < d2 ||", "return d1 > d2 ||", 0),
     ("knn_next_is_kth", "next[i] = (K < n) ? bd[K] : INFINITY;",
