@@ -70,8 +70,18 @@ typedef struct CUstream_st *kr_stream_t;
 
 typedef enum {
     KR_SUM = 0, /* a_ie = sum_j k_ij b_je */
-    KR_LSE = 1  /* L_ie = log sum_j exp(-|x_i - y_j|^2/sigma^2 + w_je); b holds w */
+    KR_LSE = 1, /* L_ie = log sum_j exp(-|x_i - y_j|^2/sigma^2 + w_je); b holds w */
+    KR_MAX = 2, /* m_ie = max_j k_ij b_je (ArgMax: the lowest j attaining it) */
+    KR_MIN = 3  /* m_ie = min_j k_ij b_je (ArgMin: the lowest j attaining it) */
 } kr_reduction;
+
+/* Radial kernel k_ij = k(|x_i - y_j|) of width sigma, chosen with kr_options.kernel. */
+typedef enum {
+    KR_KERNEL_GAUSSIAN = 0,             /* exp(-|x - y|^2 / sigma^2) */
+    KR_KERNEL_LAPLACE = 1,              /* exp(-|x - y| / sigma) */
+    KR_KERNEL_CAUCHY = 2,               /* 1 / (1 + |x - y|^2 / sigma^2) */
+    KR_KERNEL_INVERSE_MULTIQUADRIC = 3  /* 1 / sqrt(1 + |x - y|^2 / sigma^2) */
+} kr_kernel;
 
 typedef enum {
     KR_OK = 0,
@@ -82,11 +92,14 @@ typedef enum {
     KR_ERR_CUDA = 4         /* a CUDA runtime call failed; see kr_last_cuda_error() */
 } kr_status;
 
-/* Optional knobs; pass NULL for the defaults. */
+/* Optional knobs; pass NULL for the defaults (a zeroed struct is the defaults). */
 typedef struct {
     int split;       /* S >= 1 forces S disjoint j-ranges (split-j); 0 = automatic */
     int path;        /* KR_PATH_*: which units evaluate the Sum (0 = automatic) */
-    int reserved[6]; /* must be zero */
+    int kernel;      /* KR_KERNEL_*: the radial kernel (0 = Gaussian).  Other kernels serve
+                        the Sum, Max and Min (and the b-gradient); the LogSumExp, the x- and
+                        y-gradients and the K-min give KR_ERR_UNSUPPORTED for them. */
+    int reserved[5]; /* must be zero */
 } kr_options;
 
 typedef enum {
@@ -100,13 +113,17 @@ typedef enum {
 } kr_path;
 
 /*
- * Sum or LogSumExp of the Gaussian kernel over j ("Kernel Operations on the GPU...",
- * §1 target operation; KeOps README .sum(dim=1) and .logsumexp()).
+ * Sum, LogSumExp, Max or Min over j ("Kernel Operations on the GPU...", §1 target
+ * operation, §2 generic reductions; KeOps README .sum(dim=1), .logsumexp() and the
+ * Min / Max reductions of its feature list).
  *   x [M x D], y [N x D]: point clouds.
- *   b [N x E]: the signal b_je for KR_SUM, the additive log-weight w_je for KR_LSE
- *              (pass log b for positive weights; -inf is allowed and means weight 0).
- *   out [M x E]: written with a (KR_SUM) or L (KR_LSE).
- *   sigma: kernel width, k = exp(-|x - y|^2 / sigma^2).
+ *   b [N x E]: the signal b_je for KR_SUM, KR_MAX, KR_MIN; the additive log-weight
+ *              w_je for KR_LSE (pass log b for positive weights; -inf is allowed and
+ *              means weight 0).
+ *   out [M x E]: written with a (KR_SUM), L (KR_LSE) or the extreme value of
+ *              k_ij b_je over j (KR_MAX, KR_MIN; -inf / +inf when N = 0).
+ *   sigma: kernel width; the kernel is the Gaussian exp(-|x - y|^2 / sigma^2)
+ *          unless kr_options.kernel picks another (Sum, Max, Min only).
  * Returns a kr_status.
  */
 int kernel_reduce(const float *x, const float *y, const float *b, float *out,
@@ -115,6 +132,25 @@ int kernel_reduce(const float *x, const float *y, const float *b, float *out,
 int kernel_reduce_ex(const float *x, const float *y, const float *b, float *out,
                      int64_t M, int64_t N, int D, int E, float sigma, int reduction,
                      kr_stream_t stream, const kr_options *opt);
+
+/*
+ * Max or Min of k_ij b_je over j together with its Arg ("Kernel Operations on the
+ * GPU...", §2: max, min and argmin reductions; KeOps README feature list: Min, Max,
+ * ArgMin, ArgMax).
+ *   reduction: KR_MAX or KR_MIN.
+ *   idx [M x E] (int32): the lowest j attaining the extreme value (-1 when N = 0).
+ *   out [M x E] (nullable): the extreme value, as kernel_reduce writes it.
+ * The values k_ij b_je are computed in fp32 (the kernel with ex2 / rcp / rsqrt /
+ * sqrt approximations), and the comparison that picks the index is taken on those
+ * values, so where two candidates agree to within fp32 rounding either index may
+ * be returned.
+ */
+int kernel_reduce_arg(const float *x, const float *y, const float *b, float *out, int32_t *idx,
+                      int64_t M, int64_t N, int D, int E, float sigma, int reduction,
+                      kr_stream_t stream);
+int kernel_reduce_arg_ex(const float *x, const float *y, const float *b, float *out, int32_t *idx,
+                         int64_t M, int64_t N, int D, int E, float sigma, int reduction,
+                         kr_stream_t stream, const kr_options *opt);
 
 /*
  * kernel_reduce without any device allocation.  The pages have no counterpart to
@@ -172,8 +208,9 @@ int kernel_reduce_grad_y_ex(const float *x, const float *y, const float *b, cons
  * Gradient wrt b of sum_{i,e} g_ie a_ie, the transposed product
  *   gb_je = sum_i k_ij g_ie
  * (same section; a is linear in b).  x [M x D], y [N x D], g [M x E], gb [N x E]
- * output.  Computed as kernel_reduce(y, x, g) (the Gaussian is symmetric), so it
- * takes the tensor-core path under the same conditions as that call.
+ * output.  Computed as kernel_reduce(y, x, g) (every kernel here is symmetric), so
+ * it takes the tensor-core path under the same conditions as that call, and
+ * kr_options.kernel picks the kernel as for the Sum.
  */
 int kernel_reduce_grad_b(const float *x, const float *y, const float *g, float *gb,
                          int64_t M, int64_t N, int D, int E, float sigma, kr_stream_t stream);
@@ -202,7 +239,8 @@ int kr_last_cuda_error(void);
 
 /*
  * Launch plan, exposed so that the host logic can be inspected without a GPU.
- * op: 0 = Sum, 1 = LogSumExp, 2 = grad-x, 3 = K-min; EK = E (ops 0-2) or K (op 3).
+ * op: 0 = Sum, 1 = LogSumExp, 2 = grad-x, 3 = K-min, 4 = Max / Min; EK = E (ops 0-2, 4)
+ * or K (op 3).  opt->kernel selects the radial kernel of ops 0 and 4.
  * num_sms and blocks_per_sm describe the device (blocks_per_sm <= 0: use the
  * plan's own estimate).  Fills *plan and returns a kr_status; no CUDA call.
  */

@@ -8,7 +8,9 @@ library is missing, every call raises.
 
 Functions, named after the C entry points (see ``include/kreduce.h``):
 
-* ``kernel_reduce(x, y, b, sigma, reduction="sum"|"lse", out=None, split=0)``
+* ``kernel_reduce(x, y, b, sigma, reduction="sum"|"lse"|"max"|"min", out=None, split=0,
+  kernel="gaussian"|"laplace"|"cauchy"|"imq")``
+* ``kernel_reduce_arg(x, y, b, sigma, reduction="max"|"min", idx=None, out=None, split=0, kernel=...)``
 * ``kernel_reduce_grad_x(x, y, b, g, sigma, out=None, split=0)``
 * ``kernel_reduce_grad_y(x, y, b, g, sigma, out=None, split=0)``
 * ``kernel_reduce_grad_b(x, y, g, sigma, out=None, split=0)``
@@ -31,12 +33,14 @@ from . import workloads  # noqa: F401  (seeded inputs; no compute)
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkreduce.so")
 
-KR_SUM, KR_LSE = 0, 1
+KR_SUM, KR_LSE, KR_MAX, KR_MIN = 0, 1, 2, 3
+KERNELS = {"gaussian": 0, "laplace": 1, "cauchy": 2, "imq": 3}  # kr_options.kernel
 KR_OK, KR_ERR_INVALID, KR_ERR_UNSUPPORTED, KR_ERR_ALLOC, KR_ERR_CUDA = 0, 1, 2, 3, 4
-OP_SUM, OP_LSE, OP_GRAD, OP_KNN = 0, 1, 2, 3
+OP_SUM, OP_LSE, OP_GRAD, OP_KNN, OP_MAX = 0, 1, 2, 3, 4
 
 # Names exported by libkreduce.so, in the order include/kreduce.h declares them.
-EXPORTS = ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_noalloc", "kernel_reduce_grad_x",
+EXPORTS = ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_arg", "kernel_reduce_arg_ex",
+           "kernel_reduce_noalloc", "kernel_reduce_grad_x",
            "kernel_reduce_grad_x_ex", "kernel_reduce_grad_y", "kernel_reduce_grad_y_ex",
            "kernel_reduce_grad_b", "kernel_reduce_grad_b_ex",
            "kernel_knn", "kernel_knn_ex", "kr_status_string", "kr_last_cuda_error", "kr_plan",
@@ -56,7 +60,8 @@ class KrError(RuntimeError):
 
 
 class KrOptions(ctypes.Structure):
-    _fields_ = [("split", ctypes.c_int), ("path", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+    _fields_ = [("split", ctypes.c_int), ("path", ctypes.c_int), ("kernel", ctypes.c_int),
+                ("reserved", ctypes.c_int * 5)]
 
 
 KR_PATH_AUTO, KR_PATH_CUDA_CORES, KR_PATH_TENSOR_CORES = 0, 1, 2
@@ -88,6 +93,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         opt = ctypes.POINTER(KrOptions)
         lib.kernel_reduce.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
         lib.kernel_reduce_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp, opt]
+        lib.kernel_reduce_arg.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
+        lib.kernel_reduce_arg_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp, opt]
         lib.kernel_reduce_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
         lib.kernel_reduce_grad_x.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
         lib.kernel_reduce_grad_x_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
@@ -122,28 +129,38 @@ def _check(status: int, what: str) -> None:
         raise KrError(status, what, cuda_err)
 
 
-def _options(split: int, path: int = 0):
-    if not split and not path:
+def _kernel_code(kernel) -> int:
+    if isinstance(kernel, str):
+        if kernel not in KERNELS:
+            raise ValueError(f"kernel must be one of {sorted(KERNELS)}, got {kernel!r}")
+        return KERNELS[kernel]
+    return int(kernel)
+
+
+def _options(split: int, path: int = 0, kernel=0):
+    kernel = _kernel_code(kernel)
+    if not split and not path and not kernel:
         return None
     o = KrOptions()
     o.split = int(split)
     o.path = int(path)
+    o.kernel = kernel
     return ctypes.byref(o)
 
 
 def plan(op: int, M: int, N: int, D: int, EK: int, num_sms: int = 152, blocks_per_sm: int = 0,
-         split: int = 0, path: int = 0) -> KrPlan:
+         split: int = 0, path: int = 0, kernel=0) -> KrPlan:
     """The launch plan the library would use (host logic only, no GPU needed)."""
     p = KrPlan()
-    _check(load_library().kr_plan(op, M, N, D, EK, num_sms, blocks_per_sm, _options(split, path),
+    _check(load_library().kr_plan(op, M, N, D, EK, num_sms, blocks_per_sm, _options(split, path, kernel),
                                   ctypes.byref(p)), "kr_plan")
     return p
 
 
-def plan_device(op: int, M: int, N: int, D: int, EK: int, split: int = 0, path: int = 0) -> KrPlan:
+def plan_device(op: int, M: int, N: int, D: int, EK: int, split: int = 0, path: int = 0, kernel=0) -> KrPlan:
     """The launch plan a call makes on the current CUDA device (queries the device)."""
     p = KrPlan()
-    _check(load_library().kr_plan_device(op, M, N, D, EK, _options(split, path), ctypes.byref(p)),
+    _check(load_library().kr_plan_device(op, M, N, D, EK, _options(split, path, kernel), ctypes.byref(p)),
            "kr_plan_device")
     return p
 
@@ -189,15 +206,17 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else None
 
 
-def kernel_reduce(x, y, b, sigma: float, reduction: str = "sum", out=None, split: int = 0, path: int = 0):
-    """Sum (``reduction="sum"``) or LogSumExp (``"lse"``; b holds log-weights) over j.
+def kernel_reduce(x, y, b, sigma: float, reduction: str = "sum", out=None, split: int = 0, path: int = 0,
+                  kernel="gaussian"):
+    """Sum (``"sum"``), LogSumExp (``"lse"``; b holds log-weights), Max or Min over j.
 
-    Returns ``out`` (M, E): a_ie = sum_j exp(-|x_i-y_j|^2/sigma^2) b_je, or
-    L_ie = log sum_j exp(-|x_i-y_j|^2/sigma^2 + b_je)."""
+    Returns ``out`` (M, E): a_ie = sum_j k_ij b_je, L_ie = log sum_j exp(-|x_i-y_j|^2/sigma^2
+    + b_je), or max_j / min_j k_ij b_je.  ``kernel``: "gaussian" (default), "laplace",
+    "cauchy" or "imq" (Sum, Max and Min)."""
     torch = _torch()
-    red = {"sum": KR_SUM, "lse": KR_LSE}.get(reduction)
+    red = {"sum": KR_SUM, "lse": KR_LSE, "max": KR_MAX, "min": KR_MIN}.get(reduction)
     if red is None:
-        raise ValueError(f"reduction must be 'sum' or 'lse', got {reduction!r}")
+        raise ValueError(f"reduction must be 'sum', 'lse', 'max' or 'min', got {reduction!r}")
     x = _mat(x, None, "x")
     M, D = x.shape
     y = _mat(y, None, "y", D)
@@ -210,9 +229,40 @@ def kernel_reduce(x, y, b, sigma: float, reduction: str = "sum", out=None, split
     out2 = _mat(out, M, "out", E)
     _same_device(x, out2)
     st = load_library().kernel_reduce_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(out2), M, N, D, E, float(sigma), red,
-                                         _stream(dev), _options(split, path))
+                                         _stream(dev), _options(split, path, kernel))
     _check(st, "kernel_reduce")
     return out
+
+
+def kernel_reduce_arg(x, y, b, sigma: float, reduction: str = "max", idx=None, out=None, want_values: bool = True,
+                      split: int = 0, kernel="gaussian"):
+    """ArgMax / ArgMin of k_ij b_je over j (lowest index on ties) with the extreme value.
+
+    Returns (idx int32 (M, E), values float32 (M, E) or None)."""
+    torch = _torch()
+    red = {"max": KR_MAX, "min": KR_MIN}.get(reduction)
+    if red is None:
+        raise ValueError(f"reduction must be 'max' or 'min', got {reduction!r}")
+    x = _mat(x, None, "x")
+    M, D = x.shape
+    y = _mat(y, None, "y", D)
+    N = y.shape[0]
+    b = _mat(b, N, "b")
+    E = b.shape[1]
+    dev = _same_device(x, y, b)
+    if idx is None:
+        idx = torch.empty((M, E), dtype=torch.int32, device=dev)
+    if out is None and want_values:
+        out = torch.empty((M, E), dtype=torch.float32, device=dev)
+    if idx.dtype != torch.int32 or tuple(idx.shape) != (M, E) or not idx.is_contiguous():
+        raise ValueError("idx must be a contiguous int32 tensor of shape (M, E)")
+    if out is not None:
+        out = _mat(out, M, "out", E)
+    _same_device(x, idx, out)
+    st = load_library().kernel_reduce_arg_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(out), _ptr(idx), M, N, D, E,
+                                             float(sigma), red, _stream(dev), _options(split, 0, kernel))
+    _check(st, "kernel_reduce_arg")
+    return idx, out
 
 
 def kernel_reduce_noalloc(x, y, b, sigma: float, reduction: str, out):
@@ -281,7 +331,7 @@ def kernel_reduce_grad_y(x, y, b, g, sigma: float, out=None, split: int = 0):
     return out
 
 
-def kernel_reduce_grad_b(x, y, g, sigma: float, out=None, split: int = 0, path: int = 0):
+def kernel_reduce_grad_b(x, y, g, sigma: float, out=None, split: int = 0, path: int = 0, kernel="gaussian"):
     """Gradient wrt b of sum_ie g_ie a_ie: gb_je = sum_i k_ij g_ie; returns (N, E)."""
     torch = _torch()
     x = _mat(x, None, "x")
@@ -296,7 +346,7 @@ def kernel_reduce_grad_b(x, y, g, sigma: float, out=None, split: int = 0, path: 
     out2 = _mat(out, N, "out", E)
     _same_device(x, out2)
     st = load_library().kernel_reduce_grad_b_ex(_ptr(x), _ptr(y), _ptr(g), _ptr(out2), M, N, D, E, float(sigma),
-                                                _stream(dev), _options(split, path))
+                                                _stream(dev), _options(split, path, kernel))
     _check(st, "kernel_reduce_grad_b")
     return out
 

@@ -23,7 +23,8 @@ PROBE_LIB = os.path.join(HERE, "libkrprobe.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["kr_api.cpp", "kr_fwd_sum.cu", "kr_fwd_lse.cu", "kr_grad.cu", "kr_knn.cu", "kr_combine.cu",
-           "kr_noalloc.cu", "kr_tc.cu"]
+           "kr_noalloc.cu", "kr_tc.cu", "kr_radial_gauss.cu", "kr_radial_laplace.cu", "kr_radial_cauchy.cu",
+           "kr_radial_imq.cu"]
 PROBE_SOURCES = ["kr_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC", "-I", INCLUDE]

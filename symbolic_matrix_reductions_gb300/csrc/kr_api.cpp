@@ -58,6 +58,7 @@ static int64_t workspace_bytes(int op, const Instance &in, int64_t M, int D, int
         case OP_LSE: return 2 * (int64_t)S * M * EK * (int64_t)sizeof(float);
         case OP_GRAD: return 2 * (int64_t)S * M * D * (int64_t)sizeof(float);
         case OP_KNN: return (int64_t)S * M * in.ek_pad * (int64_t)(sizeof(float) + sizeof(int32_t));
+        case OP_MAX: return (int64_t)S * M * EK * (int64_t)(sizeof(float) + sizeof(int32_t));
     }
     return 0;
 }
@@ -113,8 +114,8 @@ static void plan_tc(int64_t M, int64_t N, int num_sms, int blocks_per_sm, int fo
     p->workspace_bytes = 256 + operands + (S > 1 ? 2 * (int64_t)S * M * (int64_t)sizeof(float) : 0);
 }
 
-static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, int path) {
-    if (op != OP_SUM || path == KR_PATH_CUDA_CORES || !tc_dims(D, EK)) return false;
+static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, int path, int kind) {
+    if (op != OP_SUM || kind != KR_KERNEL_GAUSSIAN || path == KR_PATH_CUDA_CORES || !tc_dims(D, EK)) return false;
     return (round_up(std::max<int64_t>(M, 1), kTcRows) + round_up(std::max<int64_t>(N, 1), kTcCols)) * 256 <=
            kMaxTcOperands;
 }
@@ -187,7 +188,8 @@ static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int bl
 namespace {
 struct DeviceCache {
     int num_sms = 0;
-    int occ[4][10][33] = {};  // resident blocks per (op, d_pad index, ek_pad); 0 = not queried
+    int occ[kNumOps][kNumKernels][10][33] = {};  // resident blocks per (op, kernel kind, d_pad index,
+                                                 // ek_pad); 0 = not queried
     int tc_occ = 0;           // resident tensor-core Sum blocks; 0 = not queried
 };
 std::mutex g_cache_mutex;
@@ -205,7 +207,19 @@ int d_index(int d_pad) {
     }
 }
 
-int query_occupancy(int op, const Instance &in) {
+int occupancy_radial(int kind, int red, const Instance &in) {
+    switch (kind) {
+        case KR_KERNEL_GAUSSIAN: return occupancy_radial_gauss(red, in);
+        case KR_KERNEL_LAPLACE: return occupancy_radial_laplace(red, in);
+        case KR_KERNEL_CAUCHY: return occupancy_radial_cauchy(red, in);
+        case KR_KERNEL_INVERSE_MULTIQUADRIC: return occupancy_radial_imq(red, in);
+    }
+    return 0;
+}
+
+int query_occupancy(int op, int kind, const Instance &in) {
+    if (op == OP_MAX) return occupancy_radial(kind, 1, in);
+    if (op == OP_SUM && kind != KR_KERNEL_GAUSSIAN) return occupancy_radial(kind, 0, in);
     switch (op) {
         case OP_SUM: return occupancy_sum(in);
         case OP_LSE: return occupancy_lse(in);
@@ -215,7 +229,7 @@ int query_occupancy(int op, const Instance &in) {
     return 0;
 }
 
-int device_info(int dev, int op, const Instance &in, int *num_sms, int *occ) {
+int device_info(int dev, int op, int kind, const Instance &in, int *num_sms, int *occ) {
     if (dev < 0 || dev >= 64) return -1;
     std::lock_guard<std::mutex> lock(g_cache_mutex);
     DeviceCache &c = g_cache[dev];
@@ -225,8 +239,8 @@ int device_info(int dev, int op, const Instance &in, int *num_sms, int *occ) {
         c.num_sms = n;
     }
     *num_sms = c.num_sms;
-    int &slot = c.occ[op][d_index(in.d_pad)][in.ek_pad];
-    if (slot == 0) slot = query_occupancy(op, in);
+    int &slot = c.occ[op][kind][d_index(in.d_pad)][in.ek_pad];
+    if (slot == 0) slot = query_occupancy(op, kind, in);
     *occ = slot;
     return 0;
 }
@@ -264,8 +278,11 @@ static int validate(int op, const Buf *bufs, int nbuf, int64_t M, int64_t N, int
     if (opt) {
         if (opt->split < 0) return KR_ERR_INVALID;
         if (opt->path < KR_PATH_AUTO || opt->path > KR_PATH_TENSOR_CORES) return KR_ERR_INVALID;
-        for (int k = 0; k < 6; ++k)
+        if (opt->kernel < 0 || opt->kernel >= kNumKernels) return KR_ERR_INVALID;
+        for (int k = 0; k < 5; ++k)
             if (opt->reserved[k] != 0) return KR_ERR_INVALID;
+        // the other kernels serve the Sum (and the b-gradient) and Max / Min
+        if (opt->kernel != KR_KERNEL_GAUSSIAN && op != OP_SUM && op != OP_MAX) return KR_ERR_UNSUPPORTED;
     }
     if (D > kMaxD) return KR_ERR_UNSUPPORTED;
     if (op == OP_KNN ? EK > kMaxK : EK > kMaxE) return KR_ERR_UNSUPPORTED;
@@ -307,6 +324,28 @@ static int is_device_ptr(const void *p, bool *dev) {
     }
     *dev = (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged);
     return 0;
+}
+
+// ---- radial-kernel family: one launcher per kernel kind ------------------------------
+static cudaError_t launch_radial(int kind, int red, const Instance &in, const Args &a, dim3 grid,
+                                 cudaStream_t s) {
+    switch (kind) {
+        case KR_KERNEL_GAUSSIAN: return launch_radial_gauss(red, in, a, grid, s);
+        case KR_KERNEL_LAPLACE: return launch_radial_laplace(red, in, a, grid, s);
+        case KR_KERNEL_CAUCHY: return launch_radial_cauchy(red, in, a, grid, s);
+        case KR_KERNEL_INVERSE_MULTIQUADRIC: return launch_radial_imq(red, in, a, grid, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// Coordinate prescale c of each kernel kind: the kernels evaluate k from |c x - c y|.
+static double kernel_prescale(int kind, float sigma) {
+    switch (kind) {
+        case KR_KERNEL_LAPLACE: return 1.4426950408889634 / (double)sigma;     // 2^(-|x'-y'|)
+        case KR_KERNEL_CAUCHY:
+        case KR_KERNEL_INVERSE_MULTIQUADRIC: return 1.0 / (double)sigma;       // 1 + |x'-y'|^2
+        default: return std::sqrt(1.4426950408889634) / (double)sigma;         // 2^(-|x'-y'|^2)
+    }
 }
 
 // ---- tensor-core Sum: operand prepass, tensor kernel, CUDA-core stand-in, combine -------
@@ -372,10 +411,11 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
     if (ce != cudaSuccess) return cuda_fail(ce);
 
     const Instance in = choose_instance(op, a.D, EK);
+    const int kind = opt ? opt->kernel : KR_KERNEL_GAUSSIAN;
     int num_sms = 0, occ = 0;
-    if (device_info(dev, op, in, &num_sms, &occ) != 0) return cuda_fail(cudaGetLastError());
+    if (device_info(dev, op, kind, in, &num_sms, &occ) != 0) return cuda_fail(cudaGetLastError());
     kr_plan_t p;
-    const bool tc = tc_eligible(op, a.M, a.N, a.D, EK, opt ? opt->path : 0) && tc_available();
+    const bool tc = tc_eligible(op, a.M, a.N, a.D, EK, opt ? opt->path : 0, kind) && tc_available();
     if (tc)
         plan_tc(a.M, a.N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, &p);
     else
@@ -417,12 +457,16 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
     char *ws = mem ? mem + stage_bytes : nullptr;
 
     if (status == KR_OK) {
-        // Buffer order: x, y, b, [g,] out | x, y, idx, dist
+        // Buffer order: x, y, b, [g,] out | x, y, idx, dist | x, y, b, out, idx (Max)
         a.x = (const float *)dptr[0];
         a.y = (const float *)dptr[1];
         if (op == OP_KNN) {
             a.idx = (int32_t *)dptr[2];
             a.out = (float *)dptr[3];
+        } else if (op == OP_MAX) {
+            a.b = (const float *)dptr[2];
+            a.out = (float *)dptr[3];
+            a.idx = (int32_t *)dptr[4];
         } else {
             a.b = (const float *)dptr[2];
             if (op == OP_GRAD) {
@@ -441,13 +485,19 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
                 a.ws0 = (float *)ws;
                 if (op == OP_KNN) {
                     a.wsi = (int32_t *)(ws + (int64_t)p.split * a.M * p.ek_pad * (int64_t)sizeof(float));
+                } else if (op == OP_MAX) {
+                    a.wsi = (int32_t *)(ws + (int64_t)p.split * a.M * EK * (int64_t)sizeof(float));
                 } else {
                     a.ws1 = (float *)(ws + p.workspace_bytes / 2);
                 }
             }
             const dim3 grid((unsigned)p.row_blocks, (unsigned)p.split);
             switch (op) {
-                case OP_SUM: ce = launch_sum(in, a, grid, stream); break;
+                case OP_SUM:
+                    ce = kind == KR_KERNEL_GAUSSIAN ? launch_sum(in, a, grid, stream)
+                                                    : launch_radial(kind, 0, in, a, grid, stream);
+                    break;
+                case OP_MAX: ce = launch_radial(kind, 1, in, a, grid, stream); break;
                 case OP_LSE: ce = launch_lse(in, a, grid, stream); break;
                 case OP_GRAD: ce = launch_grad(in, a, grid, stream); break;
                 default: ce = launch_knn(in, a, grid, stream); break;
@@ -484,8 +534,31 @@ using namespace kr;
 
 extern "C" {
 
+// Max / Min with their Arg: out (nullable when idx is given) and idx (nullable).
+static int reduce_maxmin(const float *x, const float *y, const float *b, float *out, int32_t *idx, int64_t M,
+                         int64_t N, int D, int E, float sigma, int reduction, kr_stream_t stream,
+                         const kr_options *opt) {
+    if (M < 0 || N < 0 || D < 1 || E < 1) return KR_ERR_INVALID;
+    if (!out && !idx && M > 0) return KR_ERR_INVALID;
+    const int64_t f = (int64_t)sizeof(float);
+    Buf bufs[5] = {{x, M * D * f, false}, {y, N * D * f, false}, {b, N * E * f, false},
+                   {out, out ? M * E * f : 0, true}, {idx, idx ? M * E * (int64_t)sizeof(int32_t) : 0, true}};
+    Args a{};
+    a.M = M;
+    a.N = N;
+    a.D = D;
+    a.E = E;
+    a.c = (float)kernel_prescale(opt ? opt->kernel : 0, sigma);
+    a.vsign = reduction == KR_MAX ? 1.f : -1.f;
+    return run(OP_MAX, bufs, 5, a, E, sigma, (cudaStream_t)stream, opt);
+}
+
 int kernel_reduce_ex(const float *x, const float *y, const float *b, float *out, int64_t M, int64_t N,
                      int D, int E, float sigma, int reduction, kr_stream_t stream, const kr_options *opt) {
+    if (reduction == KR_MAX || reduction == KR_MIN) {
+        if (!out && M > 0) return KR_ERR_INVALID;
+        return reduce_maxmin(x, y, b, out, nullptr, M, N, D, E, sigma, reduction, stream, opt);
+    }
     if (reduction != KR_SUM && reduction != KR_LSE) return KR_ERR_INVALID;
     const int op = reduction == KR_SUM ? OP_SUM : OP_LSE;
     if (M < 0 || N < 0 || D < 1 || E < 1) return KR_ERR_INVALID;
@@ -497,8 +570,21 @@ int kernel_reduce_ex(const float *x, const float *y, const float *b, float *out,
     a.D = D;
     a.E = E;
     a.K = 0;
-    a.c = (float)(std::sqrt(1.4426950408889634) / (double)sigma);
+    a.c = (float)kernel_prescale(op == OP_SUM && opt ? opt->kernel : 0, sigma);
     return run(op, bufs, 4, a, E, sigma, (cudaStream_t)stream, opt);
+}
+
+int kernel_reduce_arg_ex(const float *x, const float *y, const float *b, float *out, int32_t *idx, int64_t M,
+                         int64_t N, int D, int E, float sigma, int reduction, kr_stream_t stream,
+                         const kr_options *opt) {
+    if (reduction != KR_MAX && reduction != KR_MIN) return KR_ERR_INVALID;
+    if (!idx && M > 0) return KR_ERR_INVALID;
+    return reduce_maxmin(x, y, b, out, idx, M, N, D, E, sigma, reduction, stream, opt);
+}
+
+int kernel_reduce_arg(const float *x, const float *y, const float *b, float *out, int32_t *idx, int64_t M,
+                      int64_t N, int D, int E, float sigma, int reduction, kr_stream_t stream) {
+    return kernel_reduce_arg_ex(x, y, b, out, idx, M, N, D, E, sigma, reduction, stream, nullptr);
 }
 
 int kernel_reduce(const float *x, const float *y, const float *b, float *out, int64_t M, int64_t N, int D,
@@ -603,10 +689,10 @@ int kr_last_cuda_error(void) { return g_last_cuda_error; }
 
 int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm, const kr_options *opt,
             kr_plan_t *out) {
-    if (!out || op < 0 || op > 3) return KR_ERR_INVALID;
+    if (!out || op < 0 || op >= kNumOps) return KR_ERR_INVALID;
     const int st = validate(op, nullptr, 0, M, N, D, EK, 1.f, opt);
     if (st != KR_OK) return st;
-    if (tc_eligible(op, M, N, D, EK, opt ? opt->path : 0)) {
+    if (tc_eligible(op, M, N, D, EK, opt ? opt->path : 0, opt ? opt->kernel : 0)) {
         plan_tc(M, N, num_sms, blocks_per_sm, opt ? opt->split : 0, out);
         return KR_OK;
     }
@@ -614,15 +700,17 @@ int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks
 }
 
 int kr_plan_device(int op, int64_t M, int64_t N, int D, int EK, const kr_options *opt, kr_plan_t *out) {
-    if (!out || op < 0 || op > 3) return KR_ERR_INVALID;
+    if (!out || op < 0 || op >= kNumOps) return KR_ERR_INVALID;
     const int st = validate(op, nullptr, 0, M, N, D, EK, 1.f, opt);
     if (st != KR_OK) return st;
     int dev = 0;
     cudaError_t ce = cudaGetDevice(&dev);
     if (ce != cudaSuccess) return cuda_fail(ce);
     int num_sms = 0, occ = 0;
-    if (device_info(dev, op, choose_instance(op, D, EK), &num_sms, &occ) != 0) return cuda_fail(cudaGetLastError());
-    if (tc_eligible(op, M, N, D, EK, opt ? opt->path : 0) && tc_available()) {
+    const int kind = opt ? opt->kernel : KR_KERNEL_GAUSSIAN;
+    if (device_info(dev, op, kind, choose_instance(op, D, EK), &num_sms, &occ) != 0)
+        return cuda_fail(cudaGetLastError());
+    if (tc_eligible(op, M, N, D, EK, opt ? opt->path : 0, kind) && tc_available()) {
         plan_tc(M, N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, out);
         return KR_OK;
     }

@@ -62,6 +62,23 @@ __global__ void combine_knn_kernel(const Args a, int KP) {
     }
 }
 
+__global__ void combine_max_kernel(const Args a) {
+    const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t total = a.M * a.E;
+    if (o >= total) return;
+    float best = -f_inf();
+    int bj = -1;
+    for (int s = 0; s < a.S; ++s) {
+        const float v = a.ws0[s * total + o];
+        if (v > best) {  // strictly larger: an earlier split (lower j) keeps a tie
+            best = v;
+            bj = a.wsi[s * total + o];
+        }
+    }
+    if (a.out) a.out[o] = a.vsign * best;
+    if (a.idx) a.idx[o] = bj;
+}
+
 cudaError_t launch_combine(int op, const Instance &inst, const Args &a, cudaStream_t s) {
     const int threads = 256;
     int64_t n = 0;
@@ -77,6 +94,10 @@ cudaError_t launch_combine(int op, const Instance &inst, const Args &a, cudaStre
         case OP_LSE:
             n = a.M * a.E;
             combine_lse_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(a);
+            break;
+        case OP_MAX:
+            n = a.M * a.E;
+            combine_max_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(a);
             break;
         case OP_KNN:
             n = a.M;

@@ -8,7 +8,9 @@
 
 namespace kr {
 
-enum Op { OP_SUM = 0, OP_LSE = 1, OP_GRAD = 2, OP_KNN = 3 };
+enum Op { OP_SUM = 0, OP_LSE = 1, OP_GRAD = 2, OP_KNN = 3, OP_MAX = 4 };
+constexpr int kNumOps = 5;
+constexpr int kNumKernels = 4;  // radial kernel kinds (KR_KERNEL_*)
 
 constexpr int kThreads = 128;   // threads per block for every main kernel
 constexpr int kMaxD = 128;
@@ -35,6 +37,7 @@ struct Args {
     int S;
     const unsigned *tc_guard;  // Sum only: non-null when the tensor-core kernel ran first;
                                // the CUDA-core kernel then works only if the norms failed it
+    float vsign;         // Max/Min: +1 (Max) or -1 (Min, computed as -Max of k (-b))
 };
 
 // Compile-time shape of one kernel instance, chosen by the planner.
@@ -52,6 +55,16 @@ cudaError_t launch_lse(const Instance &inst, const Args &a, dim3 grid, cudaStrea
 cudaError_t launch_grad(const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
 cudaError_t launch_knn(const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
 cudaError_t launch_combine(int op, const Instance &inst, const Args &a, cudaStream_t s);
+// Radial-kernel family (kr_radial.cuh): red 0 = Sum (Laplace, Cauchy, inverse
+// multiquadric), 1 = Max/Min (every kind); one launcher per kernel kind.
+cudaError_t launch_radial_gauss(int red, const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
+cudaError_t launch_radial_laplace(int red, const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
+cudaError_t launch_radial_cauchy(int red, const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
+cudaError_t launch_radial_imq(int red, const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
+int occupancy_radial_gauss(int red, const Instance &inst);
+int occupancy_radial_laplace(int red, const Instance &inst);
+int occupancy_radial_cauchy(int red, const Instance &inst);
+int occupancy_radial_imq(int red, const Instance &inst);
 
 // Resident blocks per SM of an instance (cudaOccupancyMaxActiveBlocksPerMultiprocessor);
 // 0 if unknown.

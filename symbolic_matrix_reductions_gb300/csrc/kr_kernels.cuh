@@ -558,5 +558,7 @@ __global__ void combine_sum_kernel(const Args a, int W);
 __global__ void combine_lse_kernel(const Args a);
 // K-min: S sorted lists of KP pairs merged by (d, j); empty slots rank last.
 __global__ void combine_knn_kernel(const Args a, int KP);
+// Max/Min: the largest (value, lowest index) over the splits, times the value sign.
+__global__ void combine_max_kernel(const Args a);
 
 }  // namespace kr

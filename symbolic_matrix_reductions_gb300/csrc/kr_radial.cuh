@@ -1,0 +1,269 @@
+// kr_radial.cuh -- Sum and Max/Min reductions of k(x_i, y_j) b_je for the radial
+// kernels other than the tuned Gaussian Sum:
+//   Gaussian   exp(-|x-y|^2/sigma^2) = 2^(-|x'-y'|^2),  x' = x sqrt(log2 e)/sigma
+//   Laplace    exp(-|x-y|/sigma)     = 2^(-|x'-y'|),    x' = x log2 e/sigma
+//   Cauchy     1/(1 + |x-y|^2/sigma^2) = 1/(1 + |x'-y'|^2),       x' = x/sigma
+//   inverse multiquadric 1/sqrt(1 + |x-y|^2/sigma^2) = rsqrt(1 + |x'-y'|^2)
+// ("Kernel Operations on the GPU...", §2: reductions of generic formulas, sum /
+// max / min / argmin; KeOps README: a wide range of formulas; Sum, Min, Max,
+// ArgMin, ArgMax reductions).
+//
+// Same tiling as the Gaussian kernels: a thread keeps R rows of x' in registers,
+// the block stages tiles of y' (negated, so x' - y' is one add) and b in shared
+// memory, and every thread reads each record with broadcast 16-byte loads.  One
+// body serves two lane widths: L = 2 evaluates two points per instruction on
+// f32x2 register pairs (coordinate counts up to 64), L = 1 is the scalar form
+// (128 coordinates, whose register pairs would not fit).
+//
+// Sum: per-tile fp32 partials folded into a compensated (TwoSum) running pair.
+// Max: per (row, column) the best value and its index.  The values of a group of
+// points are compared with the best once (their maximum); only when that test
+// passes are the points walked in increasing j, replacing the best on a strictly
+// larger value, so equal values keep the lowest index.  Min is Max of k (-b):
+// the block stages -b and the result is negated on output.  Padding points carry
+// b = NaN: k NaN is NaN, which neither wins a comparison nor survives fmaxf.
+#pragma once
+
+#include "kr_kernels_packed.cuh"
+
+namespace kr {
+
+enum RadialKind { KT_GAUSS = 0, KT_LAPLACE = 1, KT_CAUCHY = 2, KT_IMQ = 3 };
+enum RadialRed { RR_SUM = 0, RR_MAX = 1 };
+
+__device__ __forceinline__ float sqrt_approx(float v) {
+    float r;
+    asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float rcp_approx(float v) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float rsqrt_approx(float v) {
+    float r;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// k as a function of the prescaled squared distance (plus 1 for Cauchy and the
+// inverse multiquadric, folded into the start of the distance sum).
+template <int KT>
+__device__ __forceinline__ float radial_value(float q) {
+    if (KT == KT_GAUSS) return ex2_approx(-q);
+    if (KT == KT_LAPLACE) return ex2_approx(-sqrt_approx(q));
+    if (KT == KT_CAUCHY) return rcp_approx(q);
+    return rsqrt_approx(q);
+}
+template <int KT>
+KR_HD constexpr float radial_q0() { return (KT == KT_CAUCHY || KT == KT_IMQ) ? 1.f : 0.f; }
+
+// ---- lane-width abstraction: float (L = 1) or float2 (L = 2) ------------------------
+template <int L> struct Lanes;
+template <> struct Lanes<1> {
+    typedef float T;
+    static __device__ __forceinline__ T splat(float v) { return v; }
+    static __device__ __forceinline__ T add(T a, T b) { return a + b; }
+    static __device__ __forceinline__ T mul(T a, T b) { return a * b; }
+    static __device__ __forceinline__ T fma(T a, T b, T c) { return fmaf(a, b, c); }
+    static __device__ __forceinline__ float lane(T v, int) { return v; }
+    static __device__ __forceinline__ float hmax(T v) { return v; }
+    static __device__ __forceinline__ float hsum(T v) { return v; }
+    template <int KT>
+    static __device__ __forceinline__ T kval(T q) { return radial_value<KT>(q); }
+};
+template <> struct Lanes<2> {
+    typedef float2 T;
+    static __device__ __forceinline__ T splat(float v) { return make_float2(v, v); }
+    static __device__ __forceinline__ T add(T a, T b) { return __fadd2_rn(a, b); }
+    static __device__ __forceinline__ T mul(T a, T b) { return __fmul2_rn(a, b); }
+    static __device__ __forceinline__ T fma(T a, T b, T c) { return __ffma2_rn(a, b, c); }
+    static __device__ __forceinline__ float lane(T v, int l) { return l ? v.y : v.x; }
+    static __device__ __forceinline__ float hmax(T v) { return fmaxf(v.x, v.y); }
+    static __device__ __forceinline__ float hsum(T v) { return v.x + v.y; }
+    template <int KT>
+    static __device__ __forceinline__ T kval(T q) { return make_float2(radial_value<KT>(q.x), radial_value<KT>(q.y)); }
+};
+
+// Lane width, record floats and tile geometry of an instance.
+KR_HD constexpr int radial_lanes(int DP) { return packed(DP) ? 2 : 1; }
+KR_HD constexpr int radial_stride(int DP, int EP) { return packed(DP) ? pair_stride(DP, EP) : pack_stride(DP, EP); }
+// Points per unrolled step (a multiple of the lane width).
+KR_HD constexpr int radial_step(int DP) { return packed(DP) ? 2 * unroll_pairs(DP) : unroll_points(DP); }
+
+// Field f (coordinate d, or DP + e for a value) of tile point p.
+template <int L, int PS>
+__device__ __forceinline__ float *radial_slot(float *tile, int p, int f) {
+    if (L == 2) return pair_slot<PS>(tile, p, f);
+    return tile + p * PS + f;
+}
+
+template <int L, int PS>
+__device__ __forceinline__ void radial_load(const float *rec, typename Lanes<L>::T (&pv)[PS / L]) {
+    if constexpr (L == 2)
+        load_pair_record<PS>(rec, pv);
+    else
+        load_record<PS>(rec, pv);
+}
+
+template <int DP, int EP, int R, int BN, int KT, int RED>
+__global__ void __launch_bounds__(kThreads) radial_kernel(const Args a) {
+    constexpr int L = radial_lanes(DP);
+    typedef Lanes<L> V;
+    typedef typename V::T T;
+    constexpr int PS = radial_stride(DP, EP);
+    constexpr int UPT = radial_step(DP);      // points per step
+    constexpr int UR = UPT / L;                // records per step
+    static_assert(BN % UPT == 0, "tile must be a multiple of the step");
+    __shared__ __align__(16) float tile[(BN / L) * PS];
+
+    const int t = threadIdx.x;
+    const int64_t row0 = (int64_t)blockIdx.x * (kThreads * R);
+    const int64_t j_begin = (int64_t)blockIdx.y * a.chunk;
+    const int64_t j_end = min(a.N, j_begin + a.chunk);
+    const float nan = __int_as_float(0x7fc00000);
+
+    // zero the padded coordinates D..DP-1 of every tile point once
+    if (a.D < DP) {
+        for (int f = t; f < BN * DP; f += kThreads) {
+            const int p = f / DP, d = f % DP;
+            if (d >= a.D) *radial_slot<L, PS>(tile, p, d) = 0.f;
+        }
+    }
+    T xr[R][DP];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t i = row0 + (int64_t)r * kThreads + t;
+#pragma unroll
+        for (int d = 0; d < DP; ++d) xr[r][d] = V::splat((i < a.M && d < a.D) ? a.c * __ldg(a.x + i * a.D + d) : 0.f);
+    }
+
+    T part[R][EP];
+    float hi[R][EP], lo[R][EP];  // Sum: compensated running pair; Max: best value, unused
+    int bj[R][EP];               // Max: index of the best value
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+            part[r][e] = V::splat(0.f);
+            hi[r][e] = RED == RR_MAX ? -f_inf() : 0.f;
+            lo[r][e] = 0.f;
+            bj[r][e] = -1;
+        }
+
+    for (int64_t jt = j_begin; jt < j_end; jt += BN) {
+        const int nv = (int)min((int64_t)BN, j_end - jt);
+        const int nvp = (nv + UPT - 1) / UPT * UPT;
+        __syncthreads();  // every thread is done with the previous tile
+        for (int p = t; p < nvp; p += kThreads) {
+            if (p < nv) {
+                const float *src = a.y + (jt + p) * a.D;
+#pragma unroll
+                for (int d = 0; d < DP; ++d)
+                    if (d < a.D) *radial_slot<L, PS>(tile, p, d) = -a.c * __ldg(src + d);
+#pragma unroll
+                for (int e = 0; e < EP; ++e) {
+                    float v = RED == RR_MAX ? nan : 0.f;
+                    if (e < a.E) {
+                        v = __ldg(a.b + (jt + p) * a.E + e);
+                        if (RED == RR_MAX) v *= a.vsign;
+                    }
+                    *radial_slot<L, PS>(tile, p, DP + e) = v;
+                }
+            } else {
+#pragma unroll
+                for (int d = 0; d < DP; ++d)
+                    if (d < a.D) *radial_slot<L, PS>(tile, p, d) = 0.f;
+#pragma unroll
+                for (int e = 0; e < EP; ++e) *radial_slot<L, PS>(tile, p, DP + e) = RED == RR_MAX ? nan : 0.f;
+            }
+        }
+        __syncthreads();  // tile staged
+
+        for (int jj = 0; jj < nvp; jj += UPT) {
+            T kv[UR][R][EP];
+#pragma unroll
+            for (int u = 0; u < UR; ++u) {
+                T pv[PS / L];
+                radial_load<L, PS>(tile + (jj / L + u) * PS, pv);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    T q = V::splat(radial_q0<KT>());
+#pragma unroll
+                    for (int d = 0; d < DP; ++d) {
+                        const T df = V::add(xr[r][d], pv[d]);
+                        q = (d == 0 && radial_q0<KT>() == 0.f) ? V::mul(df, df) : V::fma(df, df, q);
+                    }
+                    const T k = V::template kval<KT>(q);
+#pragma unroll
+                    for (int e = 0; e < EP; ++e) {
+                        if (RED == RR_SUM)
+                            part[r][e] = V::fma(k, pv[DP + e], part[r][e]);
+                        else
+                            kv[u][r][e] = V::mul(k, pv[DP + e]);
+                    }
+                }
+            }
+            if (RED == RR_MAX) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int e = 0; e < EP; ++e) {
+                        float m = V::hmax(kv[0][r][e]);
+#pragma unroll
+                        for (int u = 1; u < UR; ++u) m = fmaxf(m, V::hmax(kv[u][r][e]));
+                        if (m > hi[r][e]) {  // rare: walk the step's points in increasing j
+#pragma unroll
+                            for (int u = 0; u < UR; ++u)
+#pragma unroll
+                                for (int l = 0; l < L; ++l) {
+                                    const float f = V::lane(kv[u][r][e], l);
+                                    if (f > hi[r][e]) {
+                                        hi[r][e] = f;
+                                        bj[r][e] = (int)(jt + jj + u * L + l);
+                                    }
+                                }
+                        }
+                    }
+            }
+        }
+        if (RED == RR_SUM) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int e = 0; e < EP; ++e) {
+                    two_sum_add(hi[r][e], lo[r][e], V::hsum(part[r][e]));
+                    part[r][e] = V::splat(0.f);
+                }
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t i = row0 + (int64_t)r * kThreads + t;
+        if (i >= a.M) continue;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+            if (e >= a.E) continue;
+            const int64_t o = i * a.E + e;
+            if (a.S == 1) {
+                if (RED == RR_SUM) {
+                    a.out[o] = hi[r][e] + lo[r][e];
+                } else {
+                    if (a.out) a.out[o] = a.vsign * hi[r][e];
+                    if (a.idx) a.idx[o] = bj[r][e];
+                }
+            } else {
+                const int64_t w = (int64_t)blockIdx.y * a.M * a.E + o;
+                a.ws0[w] = hi[r][e];
+                if (RED == RR_SUM)
+                    a.ws1[w] = lo[r][e];
+                else
+                    a.wsi[w] = bj[r][e];
+            }
+        }
+    }
+}
+
+}  // namespace kr

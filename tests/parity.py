@@ -98,3 +98,53 @@ def check_knn(idx_gpu, dist_gpu, x, y, idx_ref, d_ref, next_ref, what=""):
         assert (err <= 2e-5 * np.abs(d_ref[fin]) + 1e-7).all(), \
             f"K-min {what}: distance error {np.max(err) if err.size else 0}"
     return int(ties.sum())
+
+
+# ---------------------------------------------------------------------------
+# Max / Min with Arg
+# ---------------------------------------------------------------------------
+MAX_RTOL = 1e-4
+FLUSH = 2.0 ** -126   # ex2 / rcp / rsqrt flush results below this to zero (ftz)
+
+# k as a function of the squared distance, used only to validate the index the GPU
+# returns at a near-tie (its value must be within tolerance of the oracle's extreme).
+_KFN = {
+    "gaussian": lambda q, s: np.exp(-q / s ** 2),
+    "laplace": lambda q, s: np.exp(-np.sqrt(q) / s),
+    "cauchy": lambda q, s: 1.0 / (1.0 + q / s ** 2),
+    "imq": lambda q, s: 1.0 / np.sqrt(1.0 + q / s ** 2),
+}
+
+
+def check_maxmin(val_gpu, idx_gpu, x, y, b, sigma, kernel, val_ref, idx_ref, second_ref, what=""):
+    """Value: |v_gpu - v| <= 1e-4 |v| + 2^-126 max_j |b_je| (the flush-to-zero floor).
+    Index: exact where the oracle's extreme and runner-up differ by more than 1e-5
+    relative (plus the floor); at near-ties the GPU's index must be a valid point whose
+    fp64 value is within the value tolerance of the extreme.  Returns the near-tie count."""
+    b = np.asarray(b, dtype=np.float64)
+    floor = FLUSH * (np.max(np.abs(b), axis=0)[None, :] if b.size else 0.0)
+    if val_gpu is not None:
+        v = np.asarray(val_gpu, dtype=np.float64)
+        same_inf = np.isinf(v) & np.isinf(val_ref) & (np.sign(v) == np.sign(val_ref))
+        with np.errstate(invalid="ignore"):
+            err = np.where(same_inf, 0.0, np.abs(v - val_ref))
+        ok = err <= MAX_RTOL * np.where(np.isfinite(val_ref), np.abs(val_ref), 0.0) + floor
+        assert ok.all(), f"Max/Min value {what}: {int((~ok).sum())} bad, worst {np.max(err):.3e}"
+    idx_gpu = np.asarray(idx_gpu).astype(np.int64)
+    with np.errstate(invalid="ignore"):
+        sep = np.abs(val_ref - second_ref) > TIE_RTOL * np.abs(val_ref) + floor
+    sep |= idx_ref < 0
+    bad = sep & (idx_gpu != idx_ref)
+    assert not bad.any(), (f"Arg parity {what}: {int(bad.sum())} separated entries differ; "
+                           f"first at {np.argwhere(bad)[0].tolist()}")
+    x = np.asarray(x, dtype=np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    kf = _KFN[kernel]
+    ties = np.argwhere(~sep)
+    for (i, e) in ties:
+        j = idx_gpu[i, e]
+        assert 0 <= j < y.shape[0], f"Arg {what}: row {i} column {e} index {j} out of range"
+        f = kf(float(np.sum((x[i] - y[j]) ** 2)), sigma) * b[j, e]
+        assert abs(f - val_ref[i, e]) <= MAX_RTOL * abs(val_ref[i, e]) + floor[0, e], \
+            f"Arg {what}: near-tie row {i} column {e}: index {j} gives {f} vs {val_ref[i, e]}"
+    return len(ties)

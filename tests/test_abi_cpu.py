@@ -61,7 +61,8 @@ def _reduce(lib, x=FAKE[0], y=FAKE[1], b=FAKE[2], out=FAKE[3], M=10, N=10, D=3, 
     (dict(sigma=-1.0), kr.KR_ERR_INVALID),
     (dict(sigma=float("nan")), kr.KR_ERR_INVALID),
     (dict(sigma=float("inf")), kr.KR_ERR_INVALID),
-    (dict(red=2), kr.KR_ERR_INVALID),
+    (dict(red=4), kr.KR_ERR_INVALID),
+    (dict(red=-1), kr.KR_ERR_INVALID),
     (dict(x=None), kr.KR_ERR_INVALID),
     (dict(y=None), kr.KR_ERR_INVALID),
     (dict(b=None), kr.KR_ERR_INVALID),
@@ -101,6 +102,58 @@ def test_grad_and_knn_validation(lib):
     # idx and dist may not overlap
     assert k(FAKE[0], FAKE[1], FAKE[2], P(0x30000 + 4), 10, 10, 3, 4, None, None) == kr.KR_ERR_INVALID
     assert k(None, None, None, None, 0, 0, 3, 4, None, None) == kr.KR_OK
+
+
+def test_kernel_option_validation(lib):
+    o = kr.KrOptions()
+    for kern in range(4):
+        o.kernel = kern
+        # valid kinds pass validation for the Sum and Max/Min (then fail on the fake pointers
+        # only when a device is used: here the request is rejected earlier for a bad width)
+        assert _reduce(lib, sigma=0.0, opt=ctypes.byref(o)) == kr.KR_ERR_INVALID
+        assert _reduce(lib, red=kr.KR_MAX, D=200, opt=ctypes.byref(o)) == kr.KR_ERR_UNSUPPORTED
+    for bad in (-1, 4):
+        o.kernel = bad
+        assert _reduce(lib, opt=ctypes.byref(o)) == kr.KR_ERR_INVALID
+    o.kernel = kr.KERNELS["laplace"]
+    # the LogSumExp, gradients and K-min are Gaussian / distance only
+    assert _reduce(lib, red=kr.KR_LSE, opt=ctypes.byref(o)) == kr.KR_ERR_UNSUPPORTED
+    g = lib.kernel_reduce_grad_x_ex
+    assert g(*FAKE[:5], 10, 10, 3, 1, 1.0, None, ctypes.byref(o)) == kr.KR_ERR_UNSUPPORTED
+    assert lib.kernel_reduce_grad_y_ex(*FAKE[:5], 10, 10, 3, 1, 1.0, None, ctypes.byref(o)) == kr.KR_ERR_UNSUPPORTED
+    assert lib.kernel_knn_ex(*FAKE[:4], 10, 10, 3, 4, None, ctypes.byref(o)) == kr.KR_ERR_UNSUPPORTED
+    o.kernel = 0
+    o.reserved[4] = 7
+    assert _reduce(lib, opt=ctypes.byref(o)) == kr.KR_ERR_INVALID
+
+
+def test_arg_validation(lib):
+    f = lib.kernel_reduce_arg_ex
+    # x, y, b, out (nullable), idx
+    assert f(*FAKE[:3], None, None, 10, 10, 3, 1, 1.0, kr.KR_MAX, None, None) == kr.KR_ERR_INVALID   # idx missing
+    assert f(*FAKE[:5], 10, 10, 3, 1, 1.0, kr.KR_SUM, None, None) == kr.KR_ERR_INVALID             # not Max/Min
+    assert f(*FAKE[:5], 10, 10, 3, 1, 1.0, kr.KR_LSE, None, None) == kr.KR_ERR_INVALID
+    assert f(*FAKE[:5], 10, 10, 3, 1, -1.0, kr.KR_MIN, None, None) == kr.KR_ERR_INVALID
+    assert f(*FAKE[:5], 10, 10, 3, 17, 1.0, kr.KR_MIN, None, None) == kr.KR_ERR_UNSUPPORTED
+    # idx (10 x 1 int32) overlapping out
+    assert f(*FAKE[:4], P(0x40000 + 8), 10, 10, 3, 1, 1.0, kr.KR_MAX, None, None) == kr.KR_ERR_INVALID
+    assert f(None, FAKE[1], FAKE[2], None, None, 0, 10, 3, 1, 1.0, kr.KR_MAX, None, None) == kr.KR_OK
+    # kernel_reduce with Max needs out
+    assert _reduce(lib, out=None, red=kr.KR_MAX) == kr.KR_ERR_INVALID
+
+
+def test_maxmin_plan(lib):
+    """Max/Min plans like the Sum (same rows and tiles), never on the tensor cores, and
+    keeps (value, index) partials per split."""
+    for D in (3, 50):
+        ps = kr.plan(kr.OP_SUM, 100_000, 10_000_000, D, 1, num_sms=152, blocks_per_sm=4, path=kr.KR_PATH_CUDA_CORES)
+        pm = kr.plan(kr.OP_MAX, 100_000, 10_000_000, D, 1, num_sms=152, blocks_per_sm=4)
+        assert pm.path == kr.KR_PATH_CUDA_CORES
+        assert (pm.rows_per_thread, pm.tile_points, pm.d_pad) == (ps.rows_per_thread, ps.tile_points, ps.d_pad)
+        assert pm.split > 1 and pm.workspace_bytes == pm.split * 100_000 * 8
+    # other kernels never take the tensor-core path
+    assert kr.plan(kr.OP_SUM, 1000, 1000, 50, 1, kernel="laplace").path == kr.KR_PATH_CUDA_CORES
+    assert kr.plan(kr.OP_SUM, 1000, 1000, 50, 1, kernel="gaussian").path == kr.KR_PATH_TENSOR_CORES
 
 
 def test_grad_y_and_grad_b_validation(lib):
@@ -218,6 +271,10 @@ def test_python_marshalling_errors():
     with pytest.raises(ValueError):
         kr.kernel_reduce(x, torch.zeros(4, 2), torch.zeros(4), 1.0)
     with pytest.raises(ValueError):
-        kr.kernel_reduce(x, x, torch.zeros(4), 1.0, reduction="max")
+        kr.kernel_reduce(x, x, torch.zeros(4), 1.0, reduction="median")
+    with pytest.raises(ValueError):
+        kr.kernel_reduce(x, x, torch.zeros(4), 1.0, kernel="matern")
+    with pytest.raises(ValueError):
+        kr.kernel_reduce_arg(x, x, torch.zeros(4), 1.0, reduction="sum")
     with pytest.raises(ValueError):
         kr.kernel_reduce(x.t(), x, torch.zeros(3), 1.0)
