@@ -15,8 +15,10 @@ before every timed step, outside the events.  Also reported:
     the pipe probe in this run) and the maximum SM clock;
   * e2e: the same step with HOST buffers through the same C ABI calls (the
     library stages inputs and results), timed on the host clock;
-  * secondary lines for the other workloads (D=3 at 1M points, the D=50 tall
-    product, the D=16 K-min), one timed run set each, each with its roofline;
+  * secondary lines, one timed run set each with its roofline: the other kernels
+    (Laplace, Cauchy, inverse multiquadric) and the Max/Min reductions on the
+    gauss_d3 batch, the y- and b-gradients on it, and the other workloads (D=3 at
+    1M points, the D=50 tall product, the D=16 K-min);
   * cpu_baseline: the fp64 oracle on this host's cores on a bounded row sample.
 ``--impl reference`` times the oracle as the reference arm instead.
 Under torchrun (N > 1) every rank runs its own replica (no data exchange); the
@@ -49,9 +51,18 @@ K_NN = 10
 # offset W - w'_j starts the distance's fma chain, so no per-pair max is needed);
 # grad: D sub + D fma
 # (distance) + 1 mul (k*b) + D fma;  K-min: D sub + D fma + 1 compare.
-def ops_per_pair(op: str, D: int, E: int = 1):
+# Other kernels (Sum, Max/Min): Laplace adds a square root on the XU pipe before
+# the ex2; Cauchy and the inverse multiquadric start the distance sum at 1 and take
+# one rcp / rsqrt instead of the ex2.  Max/Min: k*b is one multiply per column and
+# the running comparison one ALU op per pair.
+XU_PER_KERNEL = {"gaussian": 1, "laplace": 2, "cauchy": 1, "imq": 1}
+
+
+def ops_per_pair(op: str, D: int, E: int = 1, kernel: str = "gaussian"):
     if op == "sum":
-        return {"fp32": 2 * D + E, "xu": 1, "alu": 0}
+        return {"fp32": 2 * D + E, "xu": XU_PER_KERNEL[kernel], "alu": 0}
+    if op in ("max", "min"):
+        return {"fp32": 2 * D + E, "xu": XU_PER_KERNEL[kernel], "alu": E}
     if op == "lse":
         return {"fp32": 2 * D + E, "xu": E, "alu": 0}
     if op == "grad":
@@ -189,8 +200,9 @@ def roofline_tensor(seconds_per_launch, pairs, kernel, fp32_line):
             "vs_fp32_direct_roofline": {"peak_pairs_per_s": fp32_line["peak"], "frac": fp32_line["frac"]}}
 
 
-def roofline(op, D, E, seconds_per_launch, pairs, nsm, clk_mhz, xu_lanes, kernel, live_mhz=None):
-    n = ops_per_pair(op, D, E)
+def roofline(op, D, E, seconds_per_launch, pairs, nsm, clk_mhz, xu_lanes, kernel, live_mhz=None,
+             kind="gaussian"):
+    n = ops_per_pair(op, D, E, kind)
 
     def peak_at(mhz):
         f = mhz * 1e6
@@ -382,6 +394,24 @@ def _time_op(torch, fn, reps):
 def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
     """One timed set (1 warm-up + 2 runs) per other workload, with its roofline."""
     out = []
+    # other kernels and the Max/Min reductions on the gauss_d3 batch
+    inp = W.generate("gauss_d3")
+    x, y, bb = (torch.from_numpy(inp[k]).to(dev) for k in ("x", "y", "b"))
+    M, D = x.shape
+    N, E = y.shape[0], bb.shape[1]
+    s = inp["sigma"]
+    for op, kind in (("sum", "laplace"), ("sum", "cauchy"), ("sum", "imq"), ("max", "gaussian"),
+                     ("min", "gaussian"), ("max", "cauchy")):
+        fn = (lambda op=op, kind=kind: kr.kernel_reduce(x, y, bb, s, op, kernel=kind))
+        p = kr.plan_device(kr.OP_SUM if op == "sum" else kr.OP_MAX, M, N, D, E, kernel=kind)
+        ms = _time_op(torch, fn, 5)
+        kname = f"radial_kernel<{kind},{'Sum' if op == 'sum' else 'Max'}>[D={D},E={E}]"
+        rl = roofline(op, D, E, ms / 1e3, M * N, nsm, max_mhz, xu_lanes, kname, kind=kind)
+        out.append({"workload": f"gauss_d3: {W.WORKLOADS['gauss_d3'].note}", "op": f"{op} ({kind})", "ms": ms,
+                    "value": M * N / (ms / 1e3), "unit": UNIT, "split": p.split, "path": "cuda cores",
+                    "roofline": rl})
+    del x, y, bb
+
     plan = [("gauss_d3", [("grad_y", None), ("grad_b", None)]),
             ("gauss_d3_unit", [("sum", "b"), ("lse", "w_log")]), ("falkon_d50", [("sum", "b")]),
             ("knn_d16", [("knn", None)])]
