@@ -99,7 +99,13 @@ typedef struct {
     int kernel;      /* KR_KERNEL_*: the radial kernel (0 = Gaussian).  Other kernels serve
                         the Sum, Max and Min (and the b-gradient); the LogSumExp, the x- and
                         y-gradients and the K-min give KR_ERR_UNSUPPORTED for them. */
-    int reserved[5]; /* must be zero */
+    int batch;       /* B >= 2: B independent problems of the given sizes in one call (batch
+                        dimension; "Kernel Operations on the GPU...", §2: LazyTensors support
+                        batch dimensions).  Every array then holds its B problems one after
+                        the other (x: B x M x D, ..., out: B x M x E), each row-major; the
+                        sizes M, N, D, E, K are per problem.  0 or 1: one problem.  At most
+                        65535; batched Sums run on the CUDA cores. */
+    int reserved[4]; /* must be zero */
 } kr_options;
 
 typedef enum {

@@ -61,7 +61,7 @@ class KrError(RuntimeError):
 
 class KrOptions(ctypes.Structure):
     _fields_ = [("split", ctypes.c_int), ("path", ctypes.c_int), ("kernel", ctypes.c_int),
-                ("reserved", ctypes.c_int * 5)]
+                ("batch", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
 
 
 KR_PATH_AUTO, KR_PATH_CUDA_CORES, KR_PATH_TENSOR_CORES = 0, 1, 2
@@ -137,14 +137,15 @@ def _kernel_code(kernel) -> int:
     return int(kernel)
 
 
-def _options(split: int, path: int = 0, kernel=0):
+def _options(split: int, path: int = 0, kernel=0, batch: int = 0):
     kernel = _kernel_code(kernel)
-    if not split and not path and not kernel:
+    if not split and not path and not kernel and batch <= 1:
         return None
     o = KrOptions()
     o.split = int(split)
     o.path = int(path)
     o.kernel = kernel
+    o.batch = int(batch) if batch > 1 else 0
     return ctypes.byref(o)
 
 
@@ -173,19 +174,40 @@ def _torch():
     return torch
 
 
-def _mat(t, rows, name, cols=None):
+def _mat(t, rows, name, cols=None, B=0):
+    """t as a contiguous float32 (rows, cols) matrix, or (B, rows, cols) when B > 0; a
+    missing last dimension (a vector per problem) is taken as one column."""
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != torch.float32:
         raise TypeError(f"{name} must be float32, got {t.dtype}")
-    if t.dim() == 1:
-        t = t.view(-1, 1)
-    if t.dim() != 2 or (rows is not None and t.shape[0] != rows) or (cols is not None and t.shape[1] != cols):
+    lead = (B,) if B else ()
+    if t.dim() == len(lead) + 1:
+        t = t.view(*t.shape, 1)
+    if (t.dim() != len(lead) + 2 or tuple(t.shape[:len(lead)]) != lead
+            or (rows is not None and t.shape[-2] != rows) or (cols is not None and t.shape[-1] != cols)):
         raise ValueError(f"{name}: bad shape {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t
+
+
+def _batch_of(x):
+    """B for a batched call (x of shape (B, M, D)), 0 for a single problem (x (M, D))."""
+    torch = _torch()
+    if not isinstance(x, torch.Tensor):
+        raise TypeError("x must be a torch.Tensor")
+    if x.dim() == 3:
+        if x.shape[0] < 1:
+            raise ValueError("x: empty batch dimension")
+        return int(x.shape[0])
+    return 0
+
+
+def _empty(B, rows, cols, dtype, dev):
+    torch = _torch()
+    return torch.empty(((B,) if B else ()) + (rows, cols), dtype=dtype, device=dev)
 
 
 def _same_device(*ts):
@@ -206,30 +228,36 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else None
 
 
+def _clouds(x, y):
+    """(B, x, y, M, N, D) for a single problem (B = 0) or a batch of B problems."""
+    B = _batch_of(x)
+    x = _mat(x, None, "x", B=B)
+    M, D = x.shape[-2:]
+    y = _mat(y, None, "y", D, B=B)
+    return B, x, y, M, y.shape[-2], D
+
+
 def kernel_reduce(x, y, b, sigma: float, reduction: str = "sum", out=None, split: int = 0, path: int = 0,
                   kernel="gaussian"):
     """Sum (``"sum"``), LogSumExp (``"lse"``; b holds log-weights), Max or Min over j.
 
     Returns ``out`` (M, E): a_ie = sum_j k_ij b_je, L_ie = log sum_j exp(-|x_i-y_j|^2/sigma^2
     + b_je), or max_j / min_j k_ij b_je.  ``kernel``: "gaussian" (default), "laplace",
-    "cauchy" or "imq" (Sum, Max and Min)."""
-    torch = _torch()
+    "cauchy" or "imq" (Sum, Max and Min).  With x (B, M, D), y (B, N, D), b (B, N, E) the
+    call reduces B independent problems and returns (B, M, E)."""
     red = {"sum": KR_SUM, "lse": KR_LSE, "max": KR_MAX, "min": KR_MIN}.get(reduction)
     if red is None:
         raise ValueError(f"reduction must be 'sum', 'lse', 'max' or 'min', got {reduction!r}")
-    x = _mat(x, None, "x")
-    M, D = x.shape
-    y = _mat(y, None, "y", D)
-    N = y.shape[0]
-    b = _mat(b, N, "b")
-    E = b.shape[1]
+    B, x, y, M, N, D = _clouds(x, y)
+    b = _mat(b, N, "b", B=B)
+    E = b.shape[-1]
     dev = _same_device(x, y, b)
     if out is None:
-        out = torch.empty((M, E), dtype=torch.float32, device=dev)
-    out2 = _mat(out, M, "out", E)
+        out = _empty(B, M, E, x.dtype, dev)
+    out2 = _mat(out, M, "out", E, B=B)
     _same_device(x, out2)
     st = load_library().kernel_reduce_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(out2), M, N, D, E, float(sigma), red,
-                                         _stream(dev), _options(split, path, kernel))
+                                         _stream(dev), _options(split, path, kernel, B))
     _check(st, "kernel_reduce")
     return out
 
@@ -238,29 +266,27 @@ def kernel_reduce_arg(x, y, b, sigma: float, reduction: str = "max", idx=None, o
                       split: int = 0, kernel="gaussian"):
     """ArgMax / ArgMin of k_ij b_je over j (lowest index on ties) with the extreme value.
 
-    Returns (idx int32 (M, E), values float32 (M, E) or None)."""
+    Returns (idx int32 (M, E), values float32 (M, E) or None); (B, M, E) for a batch."""
     torch = _torch()
     red = {"max": KR_MAX, "min": KR_MIN}.get(reduction)
     if red is None:
         raise ValueError(f"reduction must be 'max' or 'min', got {reduction!r}")
-    x = _mat(x, None, "x")
-    M, D = x.shape
-    y = _mat(y, None, "y", D)
-    N = y.shape[0]
-    b = _mat(b, N, "b")
-    E = b.shape[1]
+    B, x, y, M, N, D = _clouds(x, y)
+    b = _mat(b, N, "b", B=B)
+    E = b.shape[-1]
     dev = _same_device(x, y, b)
     if idx is None:
-        idx = torch.empty((M, E), dtype=torch.int32, device=dev)
+        idx = _empty(B, M, E, torch.int32, dev)
     if out is None and want_values:
-        out = torch.empty((M, E), dtype=torch.float32, device=dev)
-    if idx.dtype != torch.int32 or tuple(idx.shape) != (M, E) or not idx.is_contiguous():
-        raise ValueError("idx must be a contiguous int32 tensor of shape (M, E)")
+        out = _empty(B, M, E, torch.float32, dev)
+    want = ((B,) if B else ()) + (M, E)
+    if idx.dtype != torch.int32 or tuple(idx.shape) != want or not idx.is_contiguous():
+        raise ValueError(f"idx must be a contiguous int32 tensor of shape {want}")
     if out is not None:
-        out = _mat(out, M, "out", E)
+        out = _mat(out, M, "out", E, B=B)
     _same_device(x, idx, out)
     st = load_library().kernel_reduce_arg_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(out), _ptr(idx), M, N, D, E,
-                                             float(sigma), red, _stream(dev), _options(split, 0, kernel))
+                                             float(sigma), red, _stream(dev), _options(split, 0, kernel, B))
     _check(st, "kernel_reduce_arg")
     return idx, out
 
@@ -290,63 +316,51 @@ def kernel_reduce_noalloc(x, y, b, sigma: float, reduction: str, out):
 
 
 def kernel_reduce_grad_x(x, y, b, g, sigma: float, out=None, split: int = 0):
-    """Gradient wrt x of sum_ie g_ie a_ie (a the Sum reduction); returns (M, D)."""
-    torch = _torch()
-    x = _mat(x, None, "x")
-    M, D = x.shape
-    y = _mat(y, None, "y", D)
-    N = y.shape[0]
-    b = _mat(b, N, "b")
-    E = b.shape[1]
-    g = _mat(g, M, "g", E)
+    """Gradient wrt x of sum_ie g_ie a_ie (a the Sum reduction); returns (M, D) or (B, M, D)."""
+    B, x, y, M, N, D = _clouds(x, y)
+    b = _mat(b, N, "b", B=B)
+    E = b.shape[-1]
+    g = _mat(g, M, "g", E, B=B)
     dev = _same_device(x, y, b, g)
     if out is None:
-        out = torch.empty((M, D), dtype=torch.float32, device=dev)
-    out = _mat(out, M, "out", D)
+        out = _empty(B, M, D, x.dtype, dev)
+    out = _mat(out, M, "out", D, B=B)
     _same_device(x, out)
     st = load_library().kernel_reduce_grad_x_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(g), _ptr(out), M, N, D, E,
-                                                float(sigma), _stream(dev), _options(split))
+                                                float(sigma), _stream(dev), _options(split, batch=B))
     _check(st, "kernel_reduce_grad_x")
     return out
 
 
 def kernel_reduce_grad_y(x, y, b, g, sigma: float, out=None, split: int = 0):
-    """Gradient wrt y of sum_ie g_ie a_ie (a the Sum reduction); returns (N, D)."""
-    torch = _torch()
-    x = _mat(x, None, "x")
-    M, D = x.shape
-    y = _mat(y, None, "y", D)
-    N = y.shape[0]
-    b = _mat(b, N, "b")
-    E = b.shape[1]
-    g = _mat(g, M, "g", E)
+    """Gradient wrt y of sum_ie g_ie a_ie (a the Sum reduction); returns (N, D) or (B, N, D)."""
+    B, x, y, M, N, D = _clouds(x, y)
+    b = _mat(b, N, "b", B=B)
+    E = b.shape[-1]
+    g = _mat(g, M, "g", E, B=B)
     dev = _same_device(x, y, b, g)
     if out is None:
-        out = torch.empty((N, D), dtype=torch.float32, device=dev)
-    out = _mat(out, N, "out", D)
+        out = _empty(B, N, D, x.dtype, dev)
+    out = _mat(out, N, "out", D, B=B)
     _same_device(x, out)
     st = load_library().kernel_reduce_grad_y_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(g), _ptr(out), M, N, D, E,
-                                                float(sigma), _stream(dev), _options(split))
+                                                float(sigma), _stream(dev), _options(split, batch=B))
     _check(st, "kernel_reduce_grad_y")
     return out
 
 
 def kernel_reduce_grad_b(x, y, g, sigma: float, out=None, split: int = 0, path: int = 0, kernel="gaussian"):
-    """Gradient wrt b of sum_ie g_ie a_ie: gb_je = sum_i k_ij g_ie; returns (N, E)."""
-    torch = _torch()
-    x = _mat(x, None, "x")
-    M, D = x.shape
-    y = _mat(y, None, "y", D)
-    N = y.shape[0]
-    g = _mat(g, M, "g")
-    E = g.shape[1]
+    """Gradient wrt b of sum_ie g_ie a_ie: gb_je = sum_i k_ij g_ie; returns (N, E) or (B, N, E)."""
+    B, x, y, M, N, D = _clouds(x, y)
+    g = _mat(g, M, "g", B=B)
+    E = g.shape[-1]
     dev = _same_device(x, y, g)
     if out is None:
-        out = torch.empty((N, E), dtype=torch.float32, device=dev)
-    out2 = _mat(out, N, "out", E)
+        out = _empty(B, N, E, x.dtype, dev)
+    out2 = _mat(out, N, "out", E, B=B)
     _same_device(x, out2)
     st = load_library().kernel_reduce_grad_b_ex(_ptr(x), _ptr(y), _ptr(g), _ptr(out2), M, N, D, E, float(sigma),
-                                                _stream(dev), _options(split, path, kernel))
+                                                _stream(dev), _options(split, path, kernel, B))
     _check(st, "kernel_reduce_grad_b")
     return out
 
@@ -354,25 +368,23 @@ def kernel_reduce_grad_b(x, y, g, sigma: float, out=None, split: int = 0, path: 
 def kernel_knn(x, y, K: int, idx=None, dist=None, want_dist: bool = True, split: int = 0):
     """K smallest (|x_i-y_j|^2, j) per row, ascending, lowest index on ties.
 
-    Returns (idx int32 (M, K), dist float32 (M, K) or None)."""
+    Returns (idx int32 (M, K), dist float32 (M, K) or None); (B, M, K) for a batch."""
     torch = _torch()
-    x = _mat(x, None, "x")
-    M, D = x.shape
-    y = _mat(y, None, "y", D)
-    N = y.shape[0]
+    B, x, y, M, N, D = _clouds(x, y)
     dev = _same_device(x, y)
     K = int(K)
     if idx is None:
-        idx = torch.empty((M, K), dtype=torch.int32, device=dev)
+        idx = _empty(B, M, K, torch.int32, dev)
     if dist is None and want_dist:
-        dist = torch.empty((M, K), dtype=torch.float32, device=dev)
-    if idx.dtype != torch.int32 or tuple(idx.shape) != (M, K) or not idx.is_contiguous():
-        raise ValueError("idx must be a contiguous int32 tensor of shape (M, K)")
+        dist = _empty(B, M, K, torch.float32, dev)
+    want = ((B,) if B else ()) + (M, K)
+    if idx.dtype != torch.int32 or tuple(idx.shape) != want or not idx.is_contiguous():
+        raise ValueError(f"idx must be a contiguous int32 tensor of shape {want}")
     if dist is not None:
-        dist = _mat(dist, M, "dist", K)
+        dist = _mat(dist, M, "dist", K, B=B)
     _same_device(x, idx, dist)
     st = load_library().kernel_knn_ex(_ptr(x), _ptr(y), _ptr(idx), _ptr(dist), M, N, D, K, _stream(dev),
-                                      _options(split))
+                                      _options(split, batch=B))
     _check(st, "kernel_knn")
     return idx, dist
 
@@ -384,7 +396,8 @@ def _make_gaussian_sum():
         """a = sum_j exp(-|x_i-y_j|^2/sigma^2) b_j, differentiable wrt x, y and b.
 
         The backward pass runs the library's x-gradient, y-gradient and transposed
-        product (b-gradient) kernels for the inputs that need a gradient."""
+        product (b-gradient) kernels for the inputs that need a gradient.  Batched
+        inputs (x (B, M, D), ...) are differentiated problem by problem."""
 
         @staticmethod
         def forward(ctx, x, y, b, sigma):
@@ -396,8 +409,8 @@ def _make_gaussian_sum():
         @staticmethod
         def backward(ctx, grad_out):
             x, y, b = ctx.saved_tensors
-            xd, yd, bd = x.detach(), y.detach(), b.detach().contiguous().view(y.shape[0], -1)
-            g = grad_out.contiguous().view(x.shape[0], -1)
+            xd, yd, bd = x.detach(), y.detach(), b.detach().contiguous()
+            g = grad_out.contiguous()
             gx = gy = gb = None
             if ctx.needs_input_grad[0]:
                 gx = kernel_reduce_grad_x(xd, yd, bd, g, ctx.sigma)

@@ -114,15 +114,19 @@ static void plan_tc(int64_t M, int64_t N, int num_sms, int blocks_per_sm, int fo
     p->workspace_bytes = 256 + operands + (S > 1 ? 2 * (int64_t)S * M * (int64_t)sizeof(float) : 0);
 }
 
-static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, int path, int kind) {
+static int64_t batch_of(const kr_options *opt) { return opt && opt->batch > 1 ? opt->batch : 1; }
+
+static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, const kr_options *opt) {
+    const int path = opt ? opt->path : 0, kind = opt ? opt->kernel : KR_KERNEL_GAUSSIAN;
     if (op != OP_SUM || kind != KR_KERNEL_GAUSSIAN || path == KR_PATH_CUDA_CORES || !tc_dims(D, EK)) return false;
+    if (batch_of(opt) > 1) return false;  // the tensor-core prepass and tiles serve one problem
     return (round_up(std::max<int64_t>(M, 1), kTcRows) + round_up(std::max<int64_t>(N, 1), kTcCols)) * 256 <=
            kMaxTcOperands;
 }
 
 // Pure planner (no CUDA call).  blocks_per_sm <= 0: assume 4 resident blocks.
 static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm,
-                int forced_split, kr_plan_t *p) {
+                int forced_split, int64_t batch, kr_plan_t *p) {
     const Instance in = choose_instance(op, D, EK);
     p->path = KR_PATH_CUDA_CORES;
     p->d_pad = in.d_pad;
@@ -152,7 +156,7 @@ static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int bl
         const double lanes_k = 32.0 * in.ek_pad;
         double best = 0.0;
         for (int64_t s = 1; s <= s_max; ++s) {
-            if (workspace_bytes(op, in, M, D, EK, (int)s) > kMaxWorkspace) break;
+            if (batch * workspace_bytes(op, in, M, D, EK, (int)s) > kMaxWorkspace) break;
             const int64_t chunk = (N + s - 1) / s;
             const int64_t tiles = (chunk + in.tile - 1) / in.tile;
             double work = (double)chunk + 32.0 * (double)tiles;   // per block, in points
@@ -161,7 +165,7 @@ static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int bl
                 const double events = groups <= lanes_k ? groups : lanes_k * (1.0 + std::log(groups / lanes_k));
                 work += events * ins_points;
             }
-            const int64_t per_sm = (p->row_blocks * s + num_sms - 1) / num_sms;
+            const int64_t per_sm = (p->row_blocks * s * batch + num_sms - 1) / num_sms;
             const int64_t conc = std::min<int64_t>(per_sm, blocks_per_sm);
             const double eff = std::min(1.0, (double)(conc * (kThreads / 32)) / 16.0);
             // each split also costs a little in partial traffic and the combine
@@ -180,7 +184,7 @@ static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int bl
         S = (int)((N + p->chunk - 1) / p->chunk);
         p->split = S;
     }
-    p->workspace_bytes = workspace_bytes(op, in, M, D, EK, S);
+    p->workspace_bytes = batch * workspace_bytes(op, in, M, D, EK, S);
     return KR_OK;
 }
 
@@ -279,7 +283,9 @@ static int validate(int op, const Buf *bufs, int nbuf, int64_t M, int64_t N, int
         if (opt->split < 0) return KR_ERR_INVALID;
         if (opt->path < KR_PATH_AUTO || opt->path > KR_PATH_TENSOR_CORES) return KR_ERR_INVALID;
         if (opt->kernel < 0 || opt->kernel >= kNumKernels) return KR_ERR_INVALID;
-        for (int k = 0; k < 5; ++k)
+        if (opt->batch < 0) return KR_ERR_INVALID;
+        if (opt->batch > kMaxBatch) return KR_ERR_UNSUPPORTED;
+        for (int k = 0; k < 4; ++k)
             if (opt->reserved[k] != 0) return KR_ERR_INVALID;
         // the other kernels serve the Sum (and the b-gradient) and Max / Min
         if (opt->kernel != KR_KERNEL_GAUSSIAN && op != OP_SUM && op != OP_MAX) return KR_ERR_UNSUPPORTED;
@@ -415,11 +421,25 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
     int num_sms = 0, occ = 0;
     if (device_info(dev, op, kind, in, &num_sms, &occ) != 0) return cuda_fail(cudaGetLastError());
     kr_plan_t p;
-    const bool tc = tc_eligible(op, a.M, a.N, a.D, EK, opt ? opt->path : 0, kind) && tc_available();
+    const bool tc = tc_eligible(op, a.M, a.N, a.D, EK, opt) && tc_available();
+    const int64_t B = batch_of(opt);
     if (tc)
         plan_tc(a.M, a.N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, &p);
     else
-        plan(op, a.M, a.N, a.D, EK, num_sms, occ, opt ? opt->split : 0, &p);
+        plan(op, a.M, a.N, a.D, EK, num_sms, occ, opt ? opt->split : 0, B, &p);
+    // With a batch dimension every array holds B problems one after the other.
+    for (int k = 0; k < nbuf; ++k) bufs[k].bytes *= B;
+    if (B > 1) {
+        const int64_t w_out = op == OP_GRAD ? a.D : op == OP_KNN ? a.K : a.E;
+        a.batch = (int)B;
+        a.bs_x = a.M * a.D;
+        a.bs_y = a.N * a.D;
+        a.bs_b = a.N * a.E;
+        a.bs_g = a.M * a.E;
+        a.bs_out = a.M * w_out;
+        a.bs_idx = a.M * (op == OP_KNN ? a.K : a.E);
+        a.bs_ws = (int64_t)p.split * a.M * (op == OP_GRAD ? a.D : op == OP_KNN ? p.ek_pad : a.E);
+    }
 
     // Host arrays: stage through one device allocation.
     bool host[8] = {};
@@ -484,14 +504,14 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
             if (p.split > 1) {
                 a.ws0 = (float *)ws;
                 if (op == OP_KNN) {
-                    a.wsi = (int32_t *)(ws + (int64_t)p.split * a.M * p.ek_pad * (int64_t)sizeof(float));
+                    a.wsi = (int32_t *)(ws + B * p.split * a.M * p.ek_pad * (int64_t)sizeof(float));
                 } else if (op == OP_MAX) {
-                    a.wsi = (int32_t *)(ws + (int64_t)p.split * a.M * EK * (int64_t)sizeof(float));
+                    a.wsi = (int32_t *)(ws + B * p.split * a.M * EK * (int64_t)sizeof(float));
                 } else {
                     a.ws1 = (float *)(ws + p.workspace_bytes / 2);
                 }
             }
-            const dim3 grid((unsigned)p.row_blocks, (unsigned)p.split);
+            const dim3 grid((unsigned)p.row_blocks, (unsigned)p.split, (unsigned)B);
             switch (op) {
                 case OP_SUM:
                     ce = kind == KR_KERNEL_GAUSSIAN ? launch_sum(in, a, grid, stream)
@@ -692,11 +712,11 @@ int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks
     if (!out || op < 0 || op >= kNumOps) return KR_ERR_INVALID;
     const int st = validate(op, nullptr, 0, M, N, D, EK, 1.f, opt);
     if (st != KR_OK) return st;
-    if (tc_eligible(op, M, N, D, EK, opt ? opt->path : 0, opt ? opt->kernel : 0)) {
+    if (tc_eligible(op, M, N, D, EK, opt)) {
         plan_tc(M, N, num_sms, blocks_per_sm, opt ? opt->split : 0, out);
         return KR_OK;
     }
-    return plan(op, M, N, D, EK, num_sms, blocks_per_sm, opt ? opt->split : 0, out);
+    return plan(op, M, N, D, EK, num_sms, blocks_per_sm, opt ? opt->split : 0, batch_of(opt), out);
 }
 
 int kr_plan_device(int op, int64_t M, int64_t N, int D, int EK, const kr_options *opt, kr_plan_t *out) {
@@ -710,11 +730,11 @@ int kr_plan_device(int op, int64_t M, int64_t N, int D, int EK, const kr_options
     const int kind = opt ? opt->kernel : KR_KERNEL_GAUSSIAN;
     if (device_info(dev, op, kind, choose_instance(op, D, EK), &num_sms, &occ) != 0)
         return cuda_fail(cudaGetLastError());
-    if (tc_eligible(op, M, N, D, EK, opt ? opt->path : 0, kind) && tc_available()) {
+    if (tc_eligible(op, M, N, D, EK, opt) && tc_available()) {
         plan_tc(M, N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, out);
         return KR_OK;
     }
-    return plan(op, M, N, D, EK, num_sms, occ, opt ? opt->split : 0, out);
+    return plan(op, M, N, D, EK, num_sms, occ, opt ? opt->split : 0, batch_of(opt), out);
 }
 
 }  // extern "C"

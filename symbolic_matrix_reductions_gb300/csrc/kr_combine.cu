@@ -3,7 +3,8 @@
 
 namespace kr {
 
-__global__ void combine_sum_kernel(const Args a, int W) {
+__global__ void combine_sum_kernel(const Args a_, int W) {
+    const Args a = batch_view(a_);
     const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = a.M * W;
     if (o >= total) return;
@@ -12,7 +13,8 @@ __global__ void combine_sum_kernel(const Args a, int W) {
     a.out[o] = (float)acc;
 }
 
-__global__ void combine_lse_kernel(const Args a) {
+__global__ void combine_lse_kernel(const Args a_) {
+    const Args a = batch_view(a_);
     const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = a.M * a.E;
     if (o >= total) return;
@@ -30,7 +32,8 @@ __global__ void combine_lse_kernel(const Args a) {
     a.out[o] = (float)(0.6931471805599453 * ((double)mmax + log2(acc)));
 }
 
-__global__ void combine_knn_kernel(const Args a, int KP) {
+__global__ void combine_knn_kernel(const Args a_, int KP) {
+    const Args a = batch_view(a_);
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= a.M) return;
     int head[kMaxSplit];
@@ -62,7 +65,8 @@ __global__ void combine_knn_kernel(const Args a, int KP) {
     }
 }
 
-__global__ void combine_max_kernel(const Args a) {
+__global__ void combine_max_kernel(const Args a_) {
+    const Args a = batch_view(a_);
     const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = a.M * a.E;
     if (o >= total) return;
@@ -85,23 +89,23 @@ cudaError_t launch_combine(int op, const Instance &inst, const Args &a, cudaStre
     switch (op) {
         case OP_SUM:
             n = a.M * a.E;
-            combine_sum_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(a, a.E);
+            combine_sum_kernel<<<dim3((unsigned)((n + threads - 1) / threads), 1, (unsigned)(a.batch > 1 ? a.batch : 1)), threads, 0, s>>>(a, a.E);
             break;
         case OP_GRAD:
             n = a.M * a.D;
-            combine_sum_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(a, a.D);
+            combine_sum_kernel<<<dim3((unsigned)((n + threads - 1) / threads), 1, (unsigned)(a.batch > 1 ? a.batch : 1)), threads, 0, s>>>(a, a.D);
             break;
         case OP_LSE:
             n = a.M * a.E;
-            combine_lse_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(a);
+            combine_lse_kernel<<<dim3((unsigned)((n + threads - 1) / threads), 1, (unsigned)(a.batch > 1 ? a.batch : 1)), threads, 0, s>>>(a);
             break;
         case OP_MAX:
             n = a.M * a.E;
-            combine_max_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(a);
+            combine_max_kernel<<<dim3((unsigned)((n + threads - 1) / threads), 1, (unsigned)(a.batch > 1 ? a.batch : 1)), threads, 0, s>>>(a);
             break;
         case OP_KNN:
             n = a.M;
-            combine_knn_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(a, inst.ek_pad);
+            combine_knn_kernel<<<dim3((unsigned)((n + threads - 1) / threads), 1, (unsigned)(a.batch > 1 ? a.batch : 1)), threads, 0, s>>>(a, inst.ek_pad);
             break;
         default:
             return cudaErrorInvalidValue;

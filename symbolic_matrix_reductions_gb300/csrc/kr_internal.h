@@ -17,6 +17,7 @@ constexpr int kMaxD = 128;
 constexpr int kMaxE = 16;
 constexpr int kMaxK = 32;
 constexpr int kMaxSplit = 64;   // most j-ranges a call is split into
+constexpr int kMaxBatch = 65535;  // most problems in one batched call (grid z)
 
 // Everything a main kernel needs; passed by value as the kernel parameter.
 struct Args {
@@ -38,6 +39,10 @@ struct Args {
     const unsigned *tc_guard;  // Sum only: non-null when the tensor-core kernel ran first;
                                // the CUDA-core kernel then works only if the norms failed it
     float vsign;         // Max/Min: +1 (Max) or -1 (Min, computed as -Max of k (-b))
+    // Batch dimension: blockIdx.z selects one of `batch` independent problems whose
+    // arrays follow each other in memory; the strides are in elements (0 when batch == 1).
+    int batch;
+    int64_t bs_x, bs_y, bs_b, bs_g, bs_out, bs_idx, bs_ws;
 };
 
 // Compile-time shape of one kernel instance, chosen by the planner.

@@ -40,6 +40,24 @@ __device__ __forceinline__ float lg2_approx(float v) {
 
 __device__ __forceinline__ float f_inf() { return __int_as_float(0x7f800000); }
 
+// The arguments of this block's problem: with a batch dimension (grid z), every
+// array pointer moves to problem blockIdx.z.  Uniform across the block.
+__device__ __forceinline__ Args batch_view(const Args &a) {
+    if (a.batch <= 1) return a;
+    Args v = a;
+    const int64_t z = blockIdx.z;
+    v.x += z * a.bs_x;
+    v.y += z * a.bs_y;
+    if (v.b) v.b += z * a.bs_b;
+    if (v.g) v.g += z * a.bs_g;
+    if (v.out) v.out += z * a.bs_out;
+    if (v.idx) v.idx += z * a.bs_idx;
+    if (v.ws0) v.ws0 += z * a.bs_ws;
+    if (v.ws1) v.ws1 += z * a.bs_ws;
+    if (v.wsi) v.wsi += z * a.bs_ws;
+    return v;
+}
+
 // Knuth's TwoSum: (hi, lo) += v with the rounding error of hi + v kept in lo.
 __device__ __forceinline__ void two_sum_add(float &hi, float &lo, float v) {
     const float s = __fadd_rn(hi, v);
@@ -123,7 +141,8 @@ __device__ __forceinline__ void zero_pad_coords(const Args &a, float *tile) {
 //   with the row's own tile maximum as the frame (the "careful" path).
 // ---------------------------------------------------------------------------
 template <int DP, int EP, int R, int BN, bool LSE>
-__global__ void __launch_bounds__(kThreads) fwd_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads) fwd_kernel(const Args a_) {
+    const Args a = batch_view(a_);
     if (!LSE && a.tc_guard &&
         __uint_as_float(a.tc_guard[0]) + __uint_as_float(a.tc_guard[1]) <= kTcNormLimit)
         return;  // the tensor-core kernel computed this call
@@ -355,7 +374,8 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const Args a) {
 // For E = 1, g_i is factored out of the sum and applied at the end.
 // ---------------------------------------------------------------------------
 template <int DP, int EP, int R, int BN>
-__global__ void __launch_bounds__(kThreads) grad_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads) grad_kernel(const Args a_) {
+    const Args a = batch_view(a_);
     constexpr int PS = pack_stride(DP, EP);
     constexpr int U = unroll_points(DP);
     __shared__ __align__(16) float tile[BN * PS];
@@ -476,7 +496,8 @@ __device__ __forceinline__ void knn_insert(float (&dk)[KP], int (&ik)[KP], float
 }
 
 template <int DP, int KP, int R, int BN>
-__global__ void __launch_bounds__(kThreads) knn_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads) knn_kernel(const Args a_) {
+    const Args a = batch_view(a_);
     constexpr int PS = pack_stride(DP, 0);
     constexpr int U = unroll_points(DP);
     __shared__ __align__(16) float tile[BN * PS];

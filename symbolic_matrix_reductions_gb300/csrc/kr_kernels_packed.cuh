@@ -95,7 +95,8 @@ __device__ __forceinline__ float2 sq_dist_pair(const float2 (&x2)[DP], const flo
 // fwd_kernel; the LSE tile frame and careful path are the same.
 // ---------------------------------------------------------------------------
 template <int DP, int EP, int R, int BN, bool LSE>
-__global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
+    const Args a = batch_view(a_);
     if (!LSE && a.tc_guard &&
         __uint_as_float(a.tc_guard[0]) + __uint_as_float(a.tc_guard[1]) <= kTcNormLimit)
         return;  // the tensor-core kernel computed this call
@@ -325,7 +326,8 @@ __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a) {
 // x-gradient (packed): the same sum as grad_kernel, two points per instruction.
 // ---------------------------------------------------------------------------
 template <int DP, int EP, int R, int BN>
-__global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a_) {
+    const Args a = batch_view(a_);
     constexpr int PS2 = pair_stride(DP, EP);
     constexpr int UP = unroll_pairs(DP);
     constexpr int UPT = 2 * UP;
@@ -464,7 +466,8 @@ __device__ __forceinline__ void knn_drain_warp(float (&dk)[R][KP], int (&ik)[R][
 }
 
 template <int DP, int KP, int R, int BN>
-__global__ void __launch_bounds__(kThreads, knn_buffer(DP, KP) > 0 ? 4 : 1) knn2_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads, knn_buffer(DP, KP) > 0 ? 4 : 1) knn2_kernel(const Args a_) {
+    const Args a = batch_view(a_);
     constexpr int PS2 = pair_stride(DP, 0);
     constexpr int UP = unroll_pairs(DP);
     constexpr int UPT = 2 * UP;

@@ -108,7 +108,8 @@ __device__ __forceinline__ void radial_load(const float *rec, typename Lanes<L>:
 }
 
 template <int DP, int EP, int R, int BN, int KT, int RED>
-__global__ void __launch_bounds__(kThreads) radial_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
+    const Args a = batch_view(a_);
     constexpr int L = radial_lanes(DP);
     typedef Lanes<L> V;
     typedef typename V::T T;

@@ -123,8 +123,27 @@ def test_kernel_option_validation(lib):
     assert lib.kernel_reduce_grad_y_ex(*FAKE[:5], 10, 10, 3, 1, 1.0, None, ctypes.byref(o)) == kr.KR_ERR_UNSUPPORTED
     assert lib.kernel_knn_ex(*FAKE[:4], 10, 10, 3, 4, None, ctypes.byref(o)) == kr.KR_ERR_UNSUPPORTED
     o.kernel = 0
-    o.reserved[4] = 7
+    o.reserved[3] = 7
     assert _reduce(lib, opt=ctypes.byref(o)) == kr.KR_ERR_INVALID
+
+
+def test_batch_option(lib):
+    o = kr.KrOptions()
+    o.batch = -1
+    assert _reduce(lib, opt=ctypes.byref(o)) == kr.KR_ERR_INVALID
+    o.batch = 65536
+    assert _reduce(lib, opt=ctypes.byref(o)) == kr.KR_ERR_UNSUPPORTED
+    # a batch of problems needs fewer splits to fill the GPU, and its workspace is B times larger
+    one = kr.plan(kr.OP_SUM, 2000, 100_000, 3, 1, num_sms=152, blocks_per_sm=8)
+    o.batch = 64
+    many = kr.KrPlan()
+    assert lib.kr_plan(kr.OP_SUM, 2000, 100_000, 3, 1, 152, 8, ctypes.byref(o), ctypes.byref(many)) == kr.KR_OK
+    assert many.split < one.split
+    assert many.workspace_bytes == 64 * (2 * many.split * 2000 * 4 if many.split > 1 else 0)
+    # batched tensor-core-sized Sums plan on the CUDA cores
+    tc = kr.KrPlan()
+    assert lib.kr_plan(kr.OP_SUM, 2000, 100_000, 50, 1, 152, 1, ctypes.byref(o), ctypes.byref(tc)) == kr.KR_OK
+    assert tc.path == kr.KR_PATH_CUDA_CORES
 
 
 def test_arg_validation(lib):
