@@ -16,6 +16,8 @@ Functions (each follows the passage cited in ``oracle.c``):
   inverse-multiquadric kernel
 * ``kernel_maxmin(x, y, b, sigma, kernel, "max"|"min")`` -> (val, idx, second)  Max / Min of
   k b over j with the lowest attaining index and the runner-up value
+* ``kernel_ranges(x, y, b, sigma, kernel, "sum"|"max"|"min", ranges_i, slices_i, redranges_j)``
+  block-sparse Sum / Max / Min over per-cluster column ranges
 * ``knn(x, y, K)``                -> (idx, dist, next)  K-min by (distance, index)
 
 Inputs may be float32 or float64 arrays; they are converted to float64 (exact for
@@ -83,6 +85,9 @@ class Oracle:
         lib.oracle_kernel_maxmin.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, _dp,
                                              _i64p, _dp]
+        lib.oracle_kernel_ranges.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int64, _i64p, _i64p, _i64p, _dp, _dp, _i64p, _dp]
         lib.oracle_knn.argtypes = [_dp, _dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                    ctypes.c_int, _i64p, _dp, _dp]
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -195,6 +200,33 @@ class Oracle:
         second = np.empty((M, E))
         self._lib.oracle_kernel_maxmin(_ptr(x), _ptr(y), _ptr(b), M, N, D, E, float(sigma), KERNELS[kernel],
                                        sense, _ptr(val), idx.ctypes.data_as(_i64p), _ptr(second))
+        return val, idx, second
+
+    def kernel_ranges(self, x, y, b, sigma, kernel, reduction, ranges_i, slices_i, redranges_j):
+        """Block-sparse Sum / Max / Min.  ranges_i (nc, 2) row clusters [start, end),
+        slices_i (nc,) cumulative ends into redranges_j (nr, 2) column ranges [start, end).
+        Returns (a, S) for "sum", (val, idx, second) for "max" / "min"."""
+        x, y = self._points(x, y)
+        M, D = x.shape
+        N = y.shape[0]
+        b = _as2d(b, N, "b")
+        E = b.shape[1]
+        ri = np.ascontiguousarray(np.asarray(ranges_i, dtype=np.int64).reshape(-1, 2))
+        si = np.ascontiguousarray(np.asarray(slices_i, dtype=np.int64).reshape(-1))
+        rj = np.ascontiguousarray(np.asarray(redranges_j, dtype=np.int64).reshape(-1, 2))
+        if si.shape[0] != ri.shape[0]:
+            raise ValueError("slices_i needs one entry per row cluster")
+        red = {"sum": 0, "max": 1, "min": -1}[reduction]
+        val = np.empty((M, E))
+        scale = np.empty((M, E))
+        idx = np.empty((M, E), dtype=np.int64)
+        second = np.empty((M, E))
+        p64 = lambda a: a.ctypes.data_as(_i64p)
+        self._lib.oracle_kernel_ranges(_ptr(x), _ptr(y), _ptr(b), M, N, D, E, float(sigma), KERNELS[kernel], red,
+                                       ri.shape[0], p64(ri), p64(si), p64(rj), _ptr(val), _ptr(scale), p64(idx),
+                                       _ptr(second))
+        if red == 0:
+            return val, scale
         return val, idx, second
 
     def knn(self, x, y, K):

@@ -319,6 +319,73 @@ void oracle_kernel_maxmin(const double *x, const double *y, const double *b,
     }
 }
 
+/*
+ * Block-sparse (cluster-wise truncated) Sum, Max and Min ("Kernel Operations on the
+ * GPU...", §3 "Applications": cluster-wise block-sparsity for large kernel systems;
+ * §4: the block-sparse truncation rule; KeOps README: an interface for block-sparse
+ * strategies).  The rows are grouped in clusters c = 0..nc-1, cluster c owning rows
+ * [ranges_i[2c], ranges_i[2c+1]); cluster c reduces over the j-ranges
+ * redranges_j[2r] <= j < redranges_j[2r+1] for r from slices_i[c-1] (0 for c = 0) to
+ * slices_i[c] - 1.  A point listed in two ranges of a cluster counts twice in the Sum.
+ *   red = 0: a_ie = sum over the cluster's ranges of k(x_i, y_j) b_je (+ scale S_ie)
+ *   red = +1 / -1: the Max / Min of k(x_i, y_j) b_je over those j with the lowest j
+ *   attaining it (val, idx, runner-up in second).
+ * Rows in no cluster reduce over nothing: Sum 0, Max -inf, Min +inf, index -1.
+ */
+void oracle_kernel_ranges(const double *x, const double *y, const double *b,
+                          int64_t M, int64_t N, int D, int E, double sigma, int kind, int red,
+                          int64_t nc, const int64_t *ranges_i, const int64_t *slices_i,
+                          const int64_t *redranges_j,
+                          double *val, double *scale, int64_t *idx, double *second)
+{
+    (void)N;
+    for (int64_t i = 0; i < M * E; ++i) {
+        val[i] = red == 0 ? 0.0 : (red > 0 ? -INFINITY : INFINITY);
+        if (scale) scale[i] = 0.0;
+        if (idx) idx[i] = -1;
+        if (second) second[i] = val[i];
+    }
+    for (int64_t c = 0; c < nc; ++c) {
+        int64_t r0 = c == 0 ? 0 : slices_i[c - 1], r1 = slices_i[c];
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t i = ranges_i[2 * c]; i < ranges_i[2 * c + 1]; ++i) {
+            for (int e = 0; e < E; ++e) {
+                double s = 0.0, cs = 0.0, sa = 0.0, ca = 0.0;
+                double best = red > 0 ? -INFINITY : INFINITY, runner = best;
+                int64_t bj = -1;
+                for (int64_t r = r0; r < r1; ++r) {
+                    for (int64_t j = redranges_j[2 * r]; j < redranges_j[2 * r + 1]; ++j) {
+                        double f = radial_kernel(kind, sq_dist(x + i * D, y + j * D, D), sigma) * b[j * E + e];
+                        if (red == 0) {
+                            neumaier_add(&s, &cs, f);
+                            neumaier_add(&sa, &ca, fabs(f));
+                            continue;
+                        }
+                        int better = red > 0 ? f > best : f < best;
+                        int same_lower = f == best && bj >= 0 && j < bj;
+                        if (better || same_lower) {
+                            runner = best;  /* the displaced value (equal to f on a tie) */
+                            best = f;
+                            bj = j;
+                        } else {
+                            int beats_runner = red > 0 ? f > runner : f < runner;
+                            if (beats_runner || (f == best && j != bj)) runner = f;
+                        }
+                    }
+                }
+                if (red == 0) {
+                    val[i * E + e] = s + cs;
+                    if (scale) scale[i * E + e] = sa + ca;
+                } else {
+                    val[i * E + e] = best;
+                    if (idx) idx[i * E + e] = bj;
+                    if (second) second[i * E + e] = runner;
+                }
+            }
+        }
+    }
+}
+
 /* (d1, j1) < (d2, j2) in lexicographic order: smaller distance first, then the
  * lower index. */
 static int lex_less(double d1, int64_t j1, double d2, int64_t j2)

@@ -553,6 +553,94 @@ def pin_min_is_negated_max(orc):
 
 
 # ---------------------------------------------------------------------------
+# block-sparse (cluster ranges) Sum / Max / Min
+# ---------------------------------------------------------------------------
+def _random_ranges(r, M, N, nc, max_ranges, overlap=True):
+    """Row clusters covering a random subset of [0, M) and random column ranges."""
+    cuts = np.sort(r.choice(np.arange(1, M), size=2 * nc - 1, replace=False))
+    edges = np.concatenate([[0], cuts, [M]])
+    ranges_i = np.stack([edges[0:-1:2], edges[1::2]], 1)[:nc]   # every other segment is a cluster
+    slices, red = [], []
+    for _ in range(nc):
+        for _ in range(r.integers(0, max_ranges + 1)):
+            a = int(r.integers(0, N))
+            c = int(r.integers(a, N + 1)) if overlap else min(N, a + int(r.integers(0, 6)))
+            red.append([a, c])
+        slices.append(len(red))
+    return ranges_i, np.array(slices), np.array(red, dtype=np.int64).reshape(-1, 2)
+
+
+def _mask(M, N, ranges_i, slices_i, redranges_j):
+    W = np.zeros((M, N))
+    for c, (i0, i1) in enumerate(ranges_i):
+        for rr in range(slices_i[c - 1] if c else 0, slices_i[c]):
+            W[i0:i1, redranges_j[rr][0]:redranges_j[rr][1]] += 1
+    covered = np.zeros(M, bool)
+    for (i0, i1) in ranges_i:
+        covered[i0:i1] = True
+    return W, covered
+
+
+def pin_ranges_golden(orc):
+    for case in _golden()["ranges"]:
+        args = (case["ranges_i"], case["slices_i"], case["redranges_j"])
+        a, _ = orc.kernel_ranges(case["x"], case["y"], case["b"], case["sigma"], case["kernel"], "sum", *args)
+        _close(a[:, 0], [_val(v) for v in case["sum"]], 1e-15, 0, case["name"])
+        for red in ("max", "min"):
+            v, i, _ = orc.kernel_ranges(case["x"], case["y"], case["b"], case["sigma"], case["kernel"], red, *args)
+            _close(v[:2, 0], [_val(t) for t in case[red]["val"]], 1e-15, 0, f"{case['name']} {red}")
+            assert i[:2, 0].tolist() == case[red]["idx"], (red, i)
+            assert i[2, 0] == -1 and np.isinf(v[2, 0]) and (v[2, 0] > 0) == (red == "min")
+
+
+def pin_ranges_mask_bruteforce(orc):
+    """Against a dense masked product: W_ij = how many ranges of i's cluster contain j;
+    a = (K o W) b, and Max / Min over the j with W_ij > 0 (NumPy, first occurrence)."""
+    from scipy.spatial.distance import cdist
+    r = _rng(30)
+    for kern, fn in KERNEL_FNS.items():
+        M, N = 40, 60
+        x = np.round(r.standard_normal((M, 2)) * 2) / 2
+        y = np.round(r.standard_normal((N, 2)) * 2) / 2
+        b = np.round(r.standard_normal((N, 2)) * 2) / 2
+        ri, si, rj = _random_ranges(r, M, N, 5, 3)
+        W, covered = _mask(M, N, ri, si, rj)
+        Kd = fn(cdist(x, y, "sqeuclidean"), 0.9)
+        a, S = orc.kernel_ranges(x, y, b, 0.9, kern, "sum", ri, si, rj)
+        _close(a, (Kd * W) @ b, 1e-12, 1e-14, f"{kern} masked sum")
+        _close(S, (Kd * W) @ np.abs(b), 1e-12, 1e-14, f"{kern} masked scale")
+        for red, big in (("max", -np.inf), ("min", np.inf)):
+            v, i, _ = orc.kernel_ranges(x, y, b, 0.9, kern, red, ri, si, rj)
+            for e in range(2):
+                F = np.where(W > 0, Kd * b[:, e][None, :], big)
+                pick = (np.argmax if red == "max" else np.argmin)(F, axis=1)
+                has = (W > 0).any(1)
+                assert np.array_equal(i[:, e], np.where(has, pick, -1)), (kern, red)
+                want = np.where(has, F[np.arange(M), pick], big)
+                _close(v[:, e], want, 1e-14, 1e-300, f"{kern} {red} masked")
+
+
+def pin_ranges_split_invariance(orc):
+    """Cutting a column range in two, or a row cluster in two with the same ranges, leaves
+    the Sum (to rounding) and the Max and its index (exactly) unchanged; one cluster over
+    all rows with one range over all columns is the dense reduction."""
+    r = _rng(31)
+    x, y, b = r.standard_normal((20, 3)), r.standard_normal((50, 3)), r.standard_normal((50, 1))
+    base = ([[0, 20]], [2], [[5, 40], [30, 50]])
+    cut_j = ([[0, 20]], [3], [[5, 17], [17, 40], [30, 50]])
+    cut_i = ([[0, 8], [8, 20]], [2, 4], [[5, 40], [30, 50], [5, 40], [30, 50]])
+    a0, _ = orc.kernel_ranges(x, y, b, 1.2, "laplace", "sum", *base)
+    v0, i0, _ = orc.kernel_ranges(x, y, b, 1.2, "laplace", "max", *base)
+    for alt in (cut_j, cut_i):
+        a1, _ = orc.kernel_ranges(x, y, b, 1.2, "laplace", "sum", *alt)
+        _close(a1, a0, 1e-13, 1e-15, "split invariance")
+        v1, i1, _ = orc.kernel_ranges(x, y, b, 1.2, "laplace", "max", *alt)
+        assert np.array_equal(v1, v0) and np.array_equal(i1, i0)
+    a, _ = orc.kernel_ranges(x, y, b, 1.2, "gaussian", "sum", [[0, 20]], [1], [[0, 50]])
+    _close(a, orc.gauss_sum(x, y, b, 1.2)[0], 1e-15, 0, "dense cover")
+
+
+# ---------------------------------------------------------------------------
 # K-min / ArgMin
 # ---------------------------------------------------------------------------
 def pin_knn_golden(orc):

@@ -68,6 +68,12 @@ MUTANTS = [
     ("maxmin_drops_signal",
      "double f = radial_kernel(kind, sq_dist(x + i * D, y + j * D, D), sigma) * b[j * E + e];",
      "double f = radial_kernel(kind, sq_dist(x + i * D, y + j * D, D), sigma);", 0),
+    ("ranges_end_inclusive", "j < redranges_j[2 * r + 1]; ++j)", "j <= redranges_j[2 * r + 1] && j < N; ++j)", 0),
+    ("ranges_slice_start_off_by_one", "int64_t r0 = c == 0 ? 0 : slices_i[c - 1], r1 = slices_i[c];",
+     "int64_t r0 = slices_i[c] - 1, r1 = slices_i[c];", 0),
+    ("ranges_ties_keep_scan_order", "int same_lower = f == best && bj >= 0 && j < bj;", "int same_lower = 0;", 0),
+    ("ranges_uncovered_max_zero", "val[i] = red == 0 ? 0.0 : (red > 0 ? -INFINITY : INFINITY);",
+     "val[i] = 0.0;", 0),
     ("knn_tie_highest_index", "(d1 == d2 && j1 < j2)", "(d1 == d2 && j1 > j2)", 0),
     ("knn_largest_first", "return d1 < d2 ||", "return d1 > d2 ||", 0),
     ("knn_next_is_kth", "next[i] = (K < n) ? bd[K] : INFINITY;",
