@@ -159,6 +159,34 @@ int kernel_reduce_arg_ex(const float *x, const float *y, const float *b, float *
                          kr_stream_t stream, const kr_options *opt);
 
 /*
+ * Block-sparse (cluster-wise truncated) Sum, Max or Min ("Kernel Operations on the
+ * GPU...", §3 "Applications": cluster-wise block-sparsity for large kernel systems;
+ * §4: the block-sparse truncation rule; KeOps README: an interface for block-sparse
+ * strategies).  The rows of x are grouped in clusters; cluster c owns rows
+ * ranges_i[2c] <= i < ranges_i[2c+1] and reduces only over the column ranges
+ * redranges_j[2r] <= j < redranges_j[2r+1] for slices_i[c-1] <= r < slices_i[c]
+ * (slices_i[-1] = 0).  A point in two ranges of one cluster counts twice in the Sum.
+ * Rows in no cluster reduce over nothing (Sum 0, Max -inf, Min +inf, index -1).
+ *   reduction: KR_SUM (out required, idx must be NULL), KR_MAX or KR_MIN (out and/or
+ *              idx; idx = the lowest j attaining the extreme, whatever the order of
+ *              the ranges).
+ *   ranges_i [nclusters x 2], slices_i [nclusters], redranges_j [nranges x 2]: int64
+ *              HOST arrays, read during the call (the library copies the tables it
+ *              builds from them); clusters must not overlap, slices must not
+ *              decrease and end at most at nranges, ranges must lie in [0, N).
+ *              Anything else gives KR_ERR_INVALID.
+ *   opt: kernel kind as for kernel_reduce; split and batch are not available in this
+ *        mode (KR_ERR_UNSUPPORTED).  Other arrays as for kernel_reduce_arg.
+ * One thread block serves at most 128 R consecutive rows of one cluster (R the rows
+ * per thread of the instance) and walks all of that cluster's ranges.
+ */
+int kernel_reduce_ranges(const float *x, const float *y, const float *b, float *out, int32_t *idx,
+                         int64_t M, int64_t N, int D, int E, float sigma, int reduction,
+                         int64_t nclusters, const int64_t *ranges_i, const int64_t *slices_i,
+                         int64_t nranges, const int64_t *redranges_j, kr_stream_t stream,
+                         const kr_options *opt);
+
+/*
  * kernel_reduce without any device allocation.  The pages have no counterpart to
  * this entry point; it exists for callers that cannot allocate device memory when
  * they call -- a process whose own memory arena already holds (almost) all of the

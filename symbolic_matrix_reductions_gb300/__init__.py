@@ -11,6 +11,7 @@ Functions, named after the C entry points (see ``include/kreduce.h``):
 * ``kernel_reduce(x, y, b, sigma, reduction="sum"|"lse"|"max"|"min", out=None, split=0,
   kernel="gaussian"|"laplace"|"cauchy"|"imq")``
 * ``kernel_reduce_arg(x, y, b, sigma, reduction="max"|"min", idx=None, out=None, split=0, kernel=...)``
+* ``kernel_reduce_ranges(x, y, b, sigma, "sum"|"max"|"min", ranges_i, slices_i, redranges_j, ...)``
 * ``kernel_reduce_grad_x(x, y, b, g, sigma, out=None, split=0)``
 * ``kernel_reduce_grad_y(x, y, b, g, sigma, out=None, split=0)``
 * ``kernel_reduce_grad_b(x, y, g, sigma, out=None, split=0)``
@@ -40,7 +41,7 @@ OP_SUM, OP_LSE, OP_GRAD, OP_KNN, OP_MAX = 0, 1, 2, 3, 4
 
 # Names exported by libkreduce.so, in the order include/kreduce.h declares them.
 EXPORTS = ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_arg", "kernel_reduce_arg_ex",
-           "kernel_reduce_noalloc", "kernel_reduce_grad_x",
+           "kernel_reduce_ranges", "kernel_reduce_noalloc", "kernel_reduce_grad_x",
            "kernel_reduce_grad_x_ex", "kernel_reduce_grad_y", "kernel_reduce_grad_y_ex",
            "kernel_reduce_grad_b", "kernel_reduce_grad_b_ex",
            "kernel_knn", "kernel_knn_ex", "kr_status_string", "kr_last_cuda_error", "kr_plan",
@@ -95,6 +96,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kernel_reduce_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp, opt]
         lib.kernel_reduce_arg.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
         lib.kernel_reduce_arg_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp, opt]
+        lib.kernel_reduce_ranges.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, i64, vp, vp, i64, vp,
+                                             vp, opt]
         lib.kernel_reduce_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
         lib.kernel_reduce_grad_x.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
         lib.kernel_reduce_grad_x_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
@@ -289,6 +292,50 @@ def kernel_reduce_arg(x, y, b, sigma: float, reduction: str = "max", idx=None, o
                                              float(sigma), red, _stream(dev), _options(split, 0, kernel, B))
     _check(st, "kernel_reduce_arg")
     return idx, out
+
+
+def kernel_reduce_ranges(x, y, b, sigma: float, reduction: str, ranges_i, slices_i, redranges_j, out=None,
+                         idx=None, want_index: bool = False, kernel="gaussian"):
+    """Block-sparse Sum / Max / Min: the rows of cluster c (ranges_i[c] = [start, end))
+    reduce only over the column ranges redranges_j[slices_i[c-1]:slices_i[c]].
+
+    ranges_i (nc, 2), slices_i (nc,), redranges_j (nr, 2): integer arrays on the host
+    (NumPy or CPU tensors).  Returns ``out`` for "sum"; (idx, out) for "max" / "min" when
+    ``want_index`` (else ``out``)."""
+    import numpy as np
+    torch = _torch()
+    red = {"sum": KR_SUM, "max": KR_MAX, "min": KR_MIN}.get(reduction)
+    if red is None:
+        raise ValueError(f"reduction must be 'sum', 'max' or 'min', got {reduction!r}")
+    B, x, y, M, N, D = _clouds(x, y)
+    if B:
+        raise ValueError("the block-sparse mode takes one problem (2-D x and y)")
+    b = _mat(b, N, "b")
+    E = b.shape[-1]
+    dev = _same_device(x, y, b)
+    tabs = []
+    for name, arr, cols in (("ranges_i", ranges_i, 2), ("slices_i", slices_i, 1), ("redranges_j", redranges_j, 2)):
+        if isinstance(arr, torch.Tensor):
+            arr = arr.detach().cpu().numpy()
+        a = np.ascontiguousarray(np.asarray(arr, dtype=np.int64))
+        if (cols == 2 and a.size and (a.ndim != 2 or a.shape[1] != 2)) or (cols == 1 and a.ndim > 1):
+            raise ValueError(f"{name}: bad shape {a.shape}")
+        tabs.append(a.reshape(-1, cols) if cols == 2 else a.reshape(-1))
+    ri, si, rj = tabs
+    if out is None:
+        out = _empty(0, M, E, torch.float32, dev)
+    out = _mat(out, M, "out", E)
+    if red != KR_SUM and want_index and idx is None:
+        idx = _empty(0, M, E, torch.int32, dev)
+    if idx is not None and (idx.dtype != torch.int32 or tuple(idx.shape) != (M, E) or not idx.is_contiguous()):
+        raise ValueError("idx must be a contiguous int32 tensor of shape (M, E)")
+    _same_device(x, out, idx)
+    p64 = lambda a: ctypes.c_void_p(a.ctypes.data) if a.size else None
+    st = load_library().kernel_reduce_ranges(_ptr(x), _ptr(y), _ptr(b), _ptr(out), _ptr(idx), M, N, D, E,
+                                             float(sigma), red, ri.shape[0], p64(ri), p64(si), rj.shape[0], p64(rj),
+                                             _stream(dev), _options(0, 0, kernel))
+    _check(st, "kernel_reduce_ranges")
+    return (idx, out) if (red != KR_SUM and want_index) else out
 
 
 def kernel_reduce_noalloc(x, y, b, sigma: float, reduction: str, out):

@@ -20,6 +20,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "kr_config.h"
 #include "kr_internal.h"
@@ -406,8 +407,18 @@ static cudaError_t run_tc(Args a, const kr_plan_t &p, const Instance &in, char *
 }
 
 // ---- the common driver --------------------------------------------------------------
+// Block-sparse mode: the per-block work table and the column ranges, built on the host.
+struct RangeTables {
+    std::vector<int4> blocks;  // {first row, end row, first range, end range} per block
+    std::vector<int2> ranges;  // column ranges [start, end)
+    int64_t bytes() const { return (int64_t)(blocks.size() * sizeof(int4) + ranges.size() * sizeof(int2)); }
+};
+
 static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStream_t stream,
-               const kr_options *opt) {
+               const kr_options *opt, const RangeTables *rt = nullptr) {
+    const int64_t B = batch_of(opt);
+    // With a batch dimension every array holds B problems one after the other.
+    for (int k = 0; k < nbuf; ++k) bufs[k].bytes *= B;
     int st = validate(op, bufs, nbuf, a.M, a.N, a.D, EK, sigma, opt);
     if (st != KR_OK) return st;
     if (a.M == 0) return KR_OK;
@@ -421,14 +432,18 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
     int num_sms = 0, occ = 0;
     if (device_info(dev, op, kind, in, &num_sms, &occ) != 0) return cuda_fail(cudaGetLastError());
     kr_plan_t p;
-    const bool tc = tc_eligible(op, a.M, a.N, a.D, EK, opt) && tc_available();
-    const int64_t B = batch_of(opt);
-    if (tc)
+    const bool tc = !rt && tc_eligible(op, a.M, a.N, a.D, EK, opt) && tc_available();
+    if (tc) {
         plan_tc(a.M, a.N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, &p);
-    else
+    } else {
         plan(op, a.M, a.N, a.D, EK, num_sms, occ, opt ? opt->split : 0, B, &p);
-    // With a batch dimension every array holds B problems one after the other.
-    for (int k = 0; k < nbuf; ++k) bufs[k].bytes *= B;
+        if (rt) {  // one block per table entry, no split; the tables are the workspace
+            p.row_blocks = (int64_t)rt->blocks.size();
+            p.split = 1;
+            p.chunk = std::max<int64_t>(a.N, 1);
+            p.workspace_bytes = rt->bytes();
+        }
+    }
     if (B > 1) {
         const int64_t w_out = op == OP_GRAD ? a.D : op == OP_KNN ? a.K : a.E;
         a.batch = (int)B;
@@ -498,7 +513,17 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
         }
         a.S = p.split;
         a.chunk = p.chunk;
-        if (tc) {
+        if (rt) {
+            const size_t nb = rt->blocks.size() * sizeof(int4);
+            ce = cudaMemcpyAsync(ws, rt->blocks.data(), nb, cudaMemcpyHostToDevice, stream);
+            if (ce == cudaSuccess && !rt->ranges.empty())
+                ce = cudaMemcpyAsync(ws + nb, rt->ranges.data(), rt->ranges.size() * sizeof(int2),
+                                     cudaMemcpyHostToDevice, stream);
+            a.blk = (const int4 *)ws;
+            a.rng = (const int2 *)(ws + nb);
+            if (ce == cudaSuccess)
+                ce = launch_radial(kind, op == OP_MAX ? 1 : 0, in, a, dim3((unsigned)p.row_blocks, 1, 1), stream);
+        } else if (tc) {
             ce = run_tc(a, p, in, ws, stream);
         } else {
             if (p.split > 1) {
@@ -605,6 +630,62 @@ int kernel_reduce_arg_ex(const float *x, const float *y, const float *b, float *
 int kernel_reduce_arg(const float *x, const float *y, const float *b, float *out, int32_t *idx, int64_t M,
                       int64_t N, int D, int E, float sigma, int reduction, kr_stream_t stream) {
     return kernel_reduce_arg_ex(x, y, b, out, idx, M, N, D, E, sigma, reduction, stream, nullptr);
+}
+
+int kernel_reduce_ranges(const float *x, const float *y, const float *b, float *out, int32_t *idx, int64_t M,
+                         int64_t N, int D, int E, float sigma, int reduction, int64_t nclusters,
+                         const int64_t *ranges_i, const int64_t *slices_i, int64_t nranges,
+                         const int64_t *redranges_j, kr_stream_t stream, const kr_options *opt) {
+    if (reduction != KR_SUM && reduction != KR_MAX && reduction != KR_MIN) return KR_ERR_INVALID;
+    if (M < 0 || N < 0 || D < 1 || E < 1 || nclusters < 0 || nranges < 0) return KR_ERR_INVALID;
+    if ((nclusters > 0 && (!ranges_i || !slices_i)) || (nranges > 0 && !redranges_j)) return KR_ERR_INVALID;
+    if (reduction == KR_SUM ? (!out || idx) : (!out && !idx)) {
+        if (M > 0) return KR_ERR_INVALID;
+    }
+    if (opt && (opt->split > 1 || opt->batch > 1)) return KR_ERR_UNSUPPORTED;
+    // the tables: clusters disjoint and inside [0, M), slices non-decreasing, ranges inside [0, N)
+    std::vector<int64_t> order((size_t)nclusters);
+    for (int64_t c = 0; c < nclusters; ++c) {
+        const int64_t i0 = ranges_i[2 * c], i1 = ranges_i[2 * c + 1];
+        if (i0 < 0 || i1 < i0 || i1 > M) return KR_ERR_INVALID;
+        if (slices_i[c] < (c ? slices_i[c - 1] : 0) || slices_i[c] > nranges) return KR_ERR_INVALID;
+        order[(size_t)c] = c;
+    }
+    std::sort(order.begin(), order.end(), [&](int64_t p, int64_t q) { return ranges_i[2 * p] < ranges_i[2 * q]; });
+    for (size_t k = 1; k < order.size(); ++k)
+        if (ranges_i[2 * order[k]] < ranges_i[2 * order[k - 1] + 1]) return KR_ERR_INVALID;  // overlapping clusters
+    RangeTables rt;
+    rt.ranges.resize((size_t)nranges);
+    for (int64_t r = 0; r < nranges; ++r) {
+        const int64_t j0 = redranges_j[2 * r], j1 = redranges_j[2 * r + 1];
+        if (j0 < 0 || j1 < j0 || j1 > N) return KR_ERR_INVALID;
+        rt.ranges[(size_t)r] = make_int2((int)j0, (int)j1);
+    }
+    const int op = reduction == KR_SUM ? OP_SUM : OP_MAX;
+    const int64_t bm = (int64_t)kThreads * choose_instance(op, D, E).rows;
+    auto add_rows = [&](int64_t i0, int64_t i1, int r0, int r1) {
+        for (int64_t i = i0; i < i1; i += bm)
+            rt.blocks.push_back(make_int4((int)i, (int)std::min(i1, i + bm), r0, r1));
+    };
+    int64_t cursor = 0;
+    for (int64_t c : order) {
+        add_rows(cursor, ranges_i[2 * c], 0, 0);  // rows in no cluster: the empty reduction
+        add_rows(ranges_i[2 * c], ranges_i[2 * c + 1], (int)(c ? slices_i[c - 1] : 0), (int)slices_i[c]);
+        cursor = ranges_i[2 * c + 1];
+    }
+    add_rows(cursor, M, 0, 0);
+
+    const int64_t f = (int64_t)sizeof(float);
+    Buf bufs[5] = {{x, M * D * f, false}, {y, N * D * f, false}, {b, N * E * f, false},
+                   {out, out ? M * E * f : 0, true}, {idx, idx ? M * E * (int64_t)sizeof(int32_t) : 0, true}};
+    Args a{};
+    a.M = M;
+    a.N = N;
+    a.D = D;
+    a.E = E;
+    a.c = (float)kernel_prescale(opt ? opt->kernel : 0, sigma);
+    a.vsign = reduction == KR_MIN ? -1.f : 1.f;
+    return run(op, bufs, 5, a, E, sigma, (cudaStream_t)stream, opt, &rt);
 }
 
 int kernel_reduce(const float *x, const float *y, const float *b, float *out, int64_t M, int64_t N, int D,

@@ -43,6 +43,10 @@ struct Args {
     // arrays follow each other in memory; the strides are in elements (0 when batch == 1).
     int batch;
     int64_t bs_x, bs_y, bs_b, bs_g, bs_out, bs_idx, bs_ws;
+    // Block-sparse mode (radial kernels): block b owns rows blk[b].x..blk[b].y-1 and
+    // reduces over the column ranges rng[blk[b].z .. blk[b].w-1]; null otherwise.
+    const int4 *blk;
+    const int2 *rng;
 };
 
 // Compile-time shape of one kernel instance, chosen by the planner.

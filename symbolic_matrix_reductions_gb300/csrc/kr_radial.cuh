@@ -120,7 +120,19 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
     __shared__ __align__(16) float tile[(BN / L) * PS];
 
     const int t = threadIdx.x;
-    const int64_t row0 = (int64_t)blockIdx.x * (kThreads * R);
+    // Dense mode: row block blockIdx.x, split blockIdx.y's column chunk.  Block-sparse
+    // mode: the work table gives the block's rows and its list of column ranges, which
+    // need not be in increasing j, so Max/Min then breaks ties on the index itself.
+    const bool ranged = a.blk != nullptr;
+    int64_t row0 = (int64_t)blockIdx.x * (kThreads * R), row_end = a.M;
+    int r_lo = 0, r_hi = 1;
+    if (ranged) {
+        const int4 w = a.blk[blockIdx.x];
+        row0 = w.x;
+        row_end = w.y;
+        r_lo = w.z;
+        r_hi = w.w;
+    }
     const int64_t j_begin = (int64_t)blockIdx.y * a.chunk;
     const int64_t j_end = min(a.N, j_begin + a.chunk);
     const float nan = __int_as_float(0x7fc00000);
@@ -137,7 +149,7 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
     for (int r = 0; r < R; ++r) {
         const int64_t i = row0 + (int64_t)r * kThreads + t;
 #pragma unroll
-        for (int d = 0; d < DP; ++d) xr[r][d] = V::splat((i < a.M && d < a.D) ? a.c * __ldg(a.x + i * a.D + d) : 0.f);
+        for (int d = 0; d < DP; ++d) xr[r][d] = V::splat((i < row_end && d < a.D) ? a.c * __ldg(a.x + i * a.D + d) : 0.f);
     }
 
     T part[R][EP];
@@ -153,8 +165,11 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
             bj[r][e] = -1;
         }
 
-    for (int64_t jt = j_begin; jt < j_end; jt += BN) {
-        const int nv = (int)min((int64_t)BN, j_end - jt);
+    for (int rr = r_lo; rr < r_hi; ++rr) {
+    const int64_t js = ranged ? (int64_t)a.rng[rr].x : j_begin;
+    const int64_t je = ranged ? (int64_t)a.rng[rr].y : j_end;
+    for (int64_t jt = js; jt < je; jt += BN) {
+        const int nv = (int)min((int64_t)BN, je - jt);
         const int nvp = (nv + UPT - 1) / UPT * UPT;
         __syncthreads();  // every thread is done with the previous tile
         for (int p = t; p < nvp; p += kThreads) {
@@ -214,15 +229,16 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
                         float m = V::hmax(kv[0][r][e]);
 #pragma unroll
                         for (int u = 1; u < UR; ++u) m = fmaxf(m, V::hmax(kv[u][r][e]));
-                        if (m > hi[r][e]) {  // rare: walk the step's points in increasing j
+                        if (m > hi[r][e] || (ranged && m == hi[r][e])) {  // rare: walk the step's points
 #pragma unroll
                             for (int u = 0; u < UR; ++u)
 #pragma unroll
                                 for (int l = 0; l < L; ++l) {
                                     const float f = V::lane(kv[u][r][e], l);
-                                    if (f > hi[r][e]) {
+                                    const int j = (int)(jt + jj + u * L + l);
+                                    if (f > hi[r][e] || (ranged && f == hi[r][e] && j < bj[r][e])) {
                                         hi[r][e] = f;
-                                        bj[r][e] = (int)(jt + jj + u * L + l);
+                                        bj[r][e] = j;
                                     }
                                 }
                         }
@@ -239,11 +255,12 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
                 }
         }
     }
+    }
 
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int64_t i = row0 + (int64_t)r * kThreads + t;
-        if (i >= a.M) continue;
+        if (i >= row_end) continue;
 #pragma unroll
         for (int e = 0; e < EP; ++e) {
             if (e >= a.E) continue;

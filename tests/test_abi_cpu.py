@@ -146,6 +146,37 @@ def test_batch_option(lib):
     assert tc.path == kr.KR_PATH_CUDA_CORES
 
 
+def test_ranges_validation(lib):
+    I64 = ctypes.c_int64 * 64
+    f = lib.kernel_reduce_ranges
+
+    def call(red=kr.KR_SUM, out=FAKE[3], idx=None, M=10, N=20, ri=(0, 5, 5, 10), si=(1, 2), rj=(0, 10, 10, 20),
+             opt=None, nc=None, nr=None):
+        a_ri, a_si, a_rj = I64(*ri), I64(*si), I64(*rj)
+        return f(FAKE[0], FAKE[1], FAKE[2], out, idx, M, N, 3, 1, 1.0, red,
+                 len(si) if nc is None else nc, a_ri, a_si, len(rj) // 2 if nr is None else nr, a_rj, None, opt)
+
+    assert call(red=kr.KR_LSE) == kr.KR_ERR_INVALID
+    assert call(ri=(0, 6, 5, 10)) == kr.KR_ERR_INVALID          # overlapping clusters
+    assert call(ri=(5, 10, 0, 6)) == kr.KR_ERR_INVALID          # ... in any order
+    assert call(ri=(0, 5, 5, 11)) == kr.KR_ERR_INVALID          # past M
+    assert call(ri=(3, 2, 5, 10)) == kr.KR_ERR_INVALID          # end before start
+    assert call(si=(2, 1)) == kr.KR_ERR_INVALID                 # decreasing slices
+    assert call(si=(1, 3)) == kr.KR_ERR_INVALID                 # past the last range
+    assert call(rj=(0, 10, 10, 21)) == kr.KR_ERR_INVALID        # past N
+    assert call(rj=(-1, 10, 10, 20)) == kr.KR_ERR_INVALID
+    assert call(idx=FAKE[4]) == kr.KR_ERR_INVALID               # the Sum has no index
+    assert call(red=kr.KR_MAX, out=None, idx=None) == kr.KR_ERR_INVALID
+    assert f(FAKE[0], FAKE[1], FAKE[2], FAKE[3], None, 10, 20, 3, 1, 1.0, kr.KR_SUM, 2, None, None, 0, None,
+             None, None) == kr.KR_ERR_INVALID                   # missing tables
+    o = kr.KrOptions()
+    o.split = 2
+    assert call(opt=ctypes.byref(o)) == kr.KR_ERR_UNSUPPORTED
+    o.split, o.batch = 0, 2
+    assert call(opt=ctypes.byref(o)) == kr.KR_ERR_UNSUPPORTED
+    assert call(M=0, ri=(0, 0), si=(0,), rj=(), out=None) == kr.KR_OK
+
+
 def test_arg_validation(lib):
     f = lib.kernel_reduce_arg_ex
     # x, y, b, out (nullable), idx

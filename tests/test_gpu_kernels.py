@@ -86,22 +86,21 @@ def test_maxmin(orc, kernel, M, N, D, E, sigma, split):
 
 
 def test_maxmin_ties_lowest_index(orc):
-    """Integer grid points and b = 1: equal values come only from equal distances, which
-    fp32 computes exactly, so every split count must return the lowest attaining index
-    for the nearest (Max) and the farthest (Min) point.  sigma = 3 keeps every kernel
-    value far above the flush-to-zero range."""
+    """Every point of y is one of 60 distinct points, repeated: duplicates have bitwise
+    equal kernel values, so each extreme is attained by a group of indices and every
+    split count must return the lowest of them.  With b = 1 Max is the nearest point."""
     r = np.random.Generator(np.random.PCG64(31))
-    y = r.integers(-3, 4, size=(3000, 3)).astype(np.float32)
-    x = r.integers(-3, 4, size=(400, 3)).astype(np.float32)
+    x = r.standard_normal((400, 3)).astype(np.float32)
+    y = r.standard_normal((60, 3)).astype(np.float32)[r.integers(0, 60, size=3000)]
     b = np.ones((3000, 1), np.float32)
     i1, _, _ = orc.knn(x, y, 1)
     for kernel in KINDS:
         for red in ("max", "min"):
-            v_ref, i_ref, s_ref = orc.kernel_maxmin(x, y, b, 3.0, kernel, red)
+            v_ref, i_ref, s_ref = orc.kernel_maxmin(x, y, b, 0.8, kernel, red)
             if red == "max":
                 assert np.array_equal(i_ref[:, 0], i1[:, 0])
             for split in (0, 1, 7):
-                idx, val = kr.kernel_reduce_arg(*_dev(x, y, b), 3.0, red, split=split, kernel=kernel)
+                idx, val = kr.kernel_reduce_arg(*_dev(x, y, b), 0.8, red, split=split, kernel=kernel)
                 assert np.array_equal(_np(idx), i_ref), (kernel, red, split)
 
 
