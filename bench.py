@@ -17,8 +17,10 @@ before every timed step, outside the events.  Also reported:
     library stages inputs and results), timed on the host clock;
   * secondary lines, one timed run set each with its roofline: the other kernels
     (Laplace, Cauchy, inverse multiquadric) and the Max/Min reductions on the
-    gauss_d3 batch, the y- and b-gradients on it, and the other workloads (D=3 at
-    1M points, the D=50 tall product, the D=16 K-min);
+    gauss_d3 batch, a batch of 256 small problems, a block-sparse (truncated) Sum
+    on the 1M-point clouds sorted into slabs (its value counts the pairs
+    evaluated), the y- and b-gradients, and the other workloads (D=3 at 1M
+    points, the D=50 tall product, the D=16 K-min);
   * cpu_baseline: the fp64 oracle on this host's cores on a bounded row sample.
 ``--impl reference`` times the oracle as the reference arm instead.
 Under torchrun (N > 1) every rank runs its own replica (no data exchange); the
@@ -411,6 +413,43 @@ def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
                     "value": M * N / (ms / 1e3), "unit": UNIT, "split": p.split, "path": "cuda cores",
                     "roofline": rl})
     del x, y, bb
+
+    # batch dimension: 256 independent gauss_d3-distributed problems of 2000 x 2000 points
+    r = np.random.Generator(np.random.PCG64(2024))
+    Bb, Mb = 256, 2000
+    xb = torch.from_numpy(r.standard_normal((Bb, Mb, 3)).astype(np.float32)).to(dev)
+    yb = torch.from_numpy(r.standard_normal((Bb, Mb, 3)).astype(np.float32)).to(dev)
+    bb3 = torch.from_numpy(r.standard_normal((Bb, Mb, 1)).astype(np.float32)).to(dev)
+    ms = _time_op(torch, lambda: kr.kernel_reduce(xb, yb, bb3, 0.5, "sum"), 5)
+    pairs = Bb * Mb * Mb
+    out.append({"workload": f"batch of {Bb} problems, M=N={Mb}, D=3, x,y,b ~ N(0,1), sigma=0.5", "op": "sum (batched)",
+                "ms": ms, "value": pairs / (ms / 1e3), "unit": UNIT, "split": None, "path": "cuda cores",
+                "roofline": roofline("sum", 3, 1, ms / 1e3, pairs, nsm, max_mhz, xu_lanes,
+                                     f"fwd_kernel<Sum>[D=3,E=1] x {Bb} (grid z)")})
+    del xb, yb, bb3
+
+    # block-sparse: the gauss_d3_unit clouds (1e6 points each) sorted into 250 slabs along the
+    # first coordinate; cluster c of x reduces over slabs c-1..c+1 of y (a truncated kernel
+    # product; the value counts the pairs evaluated)
+    inp = W.generate("gauss_d3_unit")
+    xs = inp["x"][np.argsort(inp["x"][:, 0], kind="stable")]
+    order = np.argsort(inp["y"][:, 0], kind="stable")
+    ys, bs = inp["y"][order], inp["b"][order]
+    M, N, C = xs.shape[0], ys.shape[0], 250
+    ex, ey = np.linspace(0, M, C + 1).astype(np.int64), np.linspace(0, N, C + 1).astype(np.int64)
+    ri = np.stack([ex[:-1], ex[1:]], 1)
+    rj = np.array([[ey[max(c - 1, 0)], ey[min(c + 2, C)]] for c in range(C)])
+    si = np.arange(1, C + 1)
+    pairs = int(sum((ri[c, 1] - ri[c, 0]) * (rj[c, 1] - rj[c, 0]) for c in range(C)))
+    xt, yt, bt = (torch.from_numpy(a).to(dev) for a in (xs, ys, bs))
+    ms = _time_op(torch, lambda: kr.kernel_reduce_ranges(xt, yt, bt, inp["sigma"], "sum", ri, si, rj), 5)
+    out.append({"workload": f"gauss_d3_unit clouds (1e6 points) sorted into {C} slabs along x_0; each cluster reduces "
+                            f"over its 3 neighbouring slabs ({pairs} of {M * N} pairs evaluated)",
+                "op": "sum (block-sparse)", "ms": ms, "value": pairs / (ms / 1e3), "unit": UNIT, "split": None,
+                "path": "cuda cores",
+                "roofline": roofline("sum", 3, 1, ms / 1e3, pairs, nsm, max_mhz, xu_lanes,
+                                     "radial_kernel<gaussian,Sum>[D=3,E=1] (ranges)")})
+    del xt, yt, bt
 
     plan = [("gauss_d3", [("grad_y", None), ("grad_b", None)]),
             ("gauss_d3_unit", [("sum", "b"), ("lse", "w_log")]), ("falkon_d50", [("sum", "b")]),

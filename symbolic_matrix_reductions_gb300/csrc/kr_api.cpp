@@ -414,6 +414,23 @@ struct RangeTables {
     int64_t bytes() const { return (int64_t)(blocks.size() * sizeof(int4) + ranges.size() * sizeof(int2)); }
 };
 
+// Splits of the block-sparse mode: enough blocks for about two rounds of resident
+// blocks on every SM, but every split keeps at least two tiles of the average block's
+// ranges, and the partials stay within the workspace bound.
+static int ranges_split(const RangeTables &rt, int tile, int num_sms, int occ, int64_t M, int EK) {
+    if (rt.blocks.empty()) return 1;
+    int64_t tiles = 0;
+    for (const int4 &b : rt.blocks)
+        for (int r = b.z; r < b.w; ++r) tiles += (rt.ranges[(size_t)r].y - rt.ranges[(size_t)r].x + tile - 1) / tile;
+    const int64_t nb = (int64_t)rt.blocks.size();
+    const int64_t target = 2 * (int64_t)std::max(num_sms, 1) * std::max(occ, 1);
+    int64_t S = (target + nb - 1) / nb;
+    S = std::min<int64_t>(S, std::max<int64_t>(1, tiles / (2 * nb)));
+    S = std::min<int64_t>(S, kMaxSplit);
+    while (S > 1 && 2 * S * M * EK * (int64_t)sizeof(float) > kMaxWorkspace) --S;
+    return (int)std::max<int64_t>(S, 1);
+}
+
 static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStream_t stream,
                const kr_options *opt, const RangeTables *rt = nullptr) {
     const int64_t B = batch_of(opt);
@@ -437,11 +454,12 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
         plan_tc(a.M, a.N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, &p);
     } else {
         plan(op, a.M, a.N, a.D, EK, num_sms, occ, opt ? opt->split : 0, B, &p);
-        if (rt) {  // one block per table entry, no split; the tables are the workspace
+        if (rt) {  // one block per table entry and split; the tables lead the workspace
             p.row_blocks = (int64_t)rt->blocks.size();
-            p.split = 1;
+            p.split = ranges_split(*rt, in.tile, num_sms, occ, a.M, EK);
             p.chunk = std::max<int64_t>(a.N, 1);
-            p.workspace_bytes = rt->bytes();
+            p.workspace_bytes = (rt->bytes() + 255) / 256 * 256 +
+                                (p.split > 1 ? workspace_bytes(op, in, a.M, a.D, EK, p.split) : 0);
         }
     }
     if (B > 1) {
@@ -521,8 +539,18 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
                                      cudaMemcpyHostToDevice, stream);
             a.blk = (const int4 *)ws;
             a.rng = (const int2 *)(ws + nb);
+            if (p.split > 1) {  // split partials after the tables, laid out as in dense split-j
+                char *part = ws + (rt->bytes() + 255) / 256 * 256;
+                a.ws0 = (float *)part;
+                if (op == OP_MAX)
+                    a.wsi = (int32_t *)(part + (int64_t)p.split * a.M * EK * (int64_t)sizeof(float));
+                else
+                    a.ws1 = a.ws0 + (int64_t)p.split * a.M * EK;
+            }
             if (ce == cudaSuccess)
-                ce = launch_radial(kind, op == OP_MAX ? 1 : 0, in, a, dim3((unsigned)p.row_blocks, 1, 1), stream);
+                ce = launch_radial(kind, op == OP_MAX ? 1 : 0, in, a,
+                                   dim3((unsigned)p.row_blocks, (unsigned)p.split, 1), stream);
+            if (ce == cudaSuccess && p.split > 1) ce = launch_combine(op, in, a, stream);
         } else if (tc) {
             ce = run_tc(a, p, in, ws, stream);
         } else {

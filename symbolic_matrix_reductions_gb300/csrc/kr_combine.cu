@@ -74,9 +74,12 @@ __global__ void combine_max_kernel(const Args a_) {
     int bj = -1;
     for (int s = 0; s < a.S; ++s) {
         const float v = a.ws0[s * total + o];
-        if (v > best) {  // strictly larger: an earlier split (lower j) keeps a tie
+        const int j = a.wsi[s * total + o];
+        // larger value, or the same value at a lower index (block-sparse splits need
+        // not hold increasing j; dense splits do, so there this keeps the earlier split)
+        if (v > best || (v == best && j >= 0 && (bj < 0 || j < bj))) {
             best = v;
-            bj = a.wsi[s * total + o];
+            bj = j;
         }
     }
     if (a.out) a.out[o] = a.vsign * best;

@@ -75,13 +75,13 @@ KR_HD constexpr int tile_points_packed(int PS2) {
     return (16384 / PS2) >= 512 ? 512 : (16384 / PS2) >= 256 ? 256 : (16384 / PS2) >= 128 ? 128
          : (16384 / PS2) >= 64 ? 64 : 32;
 }
-// Candidate buffer of the packed K-min: (d, j) slots per row in shared memory
-// (0: insert at once).  R x CB x 128 threads x 8 bytes sit beside the tile, and
-// the two must stay within 48 KB of static shared memory.  Buffered instances are
+// Queue of passing point groups of the packed K-min: slots per row in shared memory
+// (0: insert at once).  R x CB x 128 threads x 4 bytes sit beside the tile, and the
+// two must stay within 48 KB of static shared memory.  Queued instances are
 // compiled for 4 resident blocks per SM (at most 128 registers a thread).
-KR_HD constexpr int knn_buffer(int DP, int KP) { return DP <= 4 && KP <= 10 ? 8 : 0; }
+KR_HD constexpr int knn_buffer(int DP, int KP) { return DP <= 4 && KP <= 10 ? 16 : 0; }
 // Unrolled point groups between two warp-wide checks of the candidate buffers.
-KR_HD constexpr int knn_check_groups(int DP, int KP) { return 1; }
+KR_HD constexpr int knn_check_groups(int DP, int KP) { return 2; }
 // Pair records per unrolled step of the packed inner loop.
 KR_HD constexpr int unroll_pairs(int DP) { return DP <= 8 ? 2 : 1; }
 // Tile points of an instance (value columns VP = E, K-min: 0).

@@ -435,31 +435,56 @@ __global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a_) {
 // ---------------------------------------------------------------------------
 // K-min (packed distances).  The threshold test is taken once per row for a
 // group of UPT points (the minimum of their distances against the list's last
-// entry); the group's passing points are then walked in increasing j from a bit
-// mask.  Insertion is strictly-smaller and in increasing j, so equal distances
+// entry).  Insertion is strictly-smaller and in increasing j, so equal distances
 // keep the lower index.
 //
-// CB == 0: a passing point is inserted into the sorted register list at once.
-// Late in a scan passing points are rare and land in one lane at a time, so the
-// warp runs the whole insertion for a single row while 31 lanes wait.
-// CB > 0: a passing point is appended instead to its row's buffer of CB (d, j)
-// slots in shared memory (a few instructions).  Every G groups the warp checks
-// whether any lane could overflow a buffer in the next G groups; if so, all 32
-// lanes drain all their buffers together, one slot per step, so each insertion
-// step serves up to 32 rows.  Slots are drained in the order they were filled
-// (increasing j), and a slot that passed an older, looser threshold simply
-// leaves the list unchanged, so the result is the same list as with CB == 0.
+// CB == 0: the group's passing points are walked in increasing j from a bit mask
+// and inserted into the sorted register list at once.  Late in a scan passing
+// groups are rare and come one lane at a time, so the warp runs the whole
+// insertion for a single row while 31 lanes wait.
+// CB > 0: a passing group only appends its index to its row's queue of CB slots in
+// shared memory (one store).  Every G groups the warp checks whether any lane could
+// overflow a queue in the next G groups; if so, and always before the tile is
+// replaced, all 32 lanes drain their queues together, one slot per step: each slot's
+// four distances are recomputed from the tile (a few instructions at small D),
+// tested against the current threshold, and the passing points inserted in
+// increasing j.  Slots are drained in the order they were filled (increasing j), so
+// the result is the same list as with CB == 0.
 // ---------------------------------------------------------------------------
-template <int KP, int CB, int R>
-__device__ __forceinline__ void knn_drain_warp(float (&dk)[R][KP], int (&ik)[R][KP], int (&nc)[R],
-                                               const float2 *cbuf) {
+template <int DP, int KP, int R, int PS2, int UP>
+__device__ __forceinline__ void knn_drain_groups(const float2 (&x2)[R][DP], float (&dk)[R][KP], int (&ik)[R][KP],
+                                                 int (&nc)[R], const int *qbuf, const float *tile, int64_t jt,
+                                                 int CB) {
+    constexpr int UPT = 2 * UP;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int steps = __reduce_max_sync(0xffffffffu, nc[r]);
-        const float2 *slot = cbuf + r * CB * kThreads + threadIdx.x;
+        const int *slot = qbuf + r * CB * kThreads + threadIdx.x;
         for (int s = 0; s < steps; ++s) {
-            const float2 e = slot[s * kThreads];
-            knn_insert<KP>(dk[r], ik[r], s < nc[r] ? e.x : f_inf(), __float_as_int(e.y));
+            const int g = s < nc[r] ? slot[s * kThreads] : -1;
+            if (g < 0) continue;
+            float2 q[UP];
+#pragma unroll
+            for (int u = 0; u < UP; ++u) {
+                float2 pv[PS2 / 2];
+                load_pair_record<PS2>(tile + (g * UP + u) * PS2, pv);
+                q[u] = sq_dist_pair<DP, PS2>(x2[r], pv, make_float2(0.f, 0.f), false);
+            }
+            const float thr = dk[r][KP - 1];
+            unsigned mask = 0;
+#pragma unroll
+            for (int u = 0; u < UP; ++u) {
+                mask |= (q[u].x < thr ? 1u : 0u) << (2 * u);
+                mask |= (q[u].y < thr ? 1u : 0u) << (2 * u + 1);
+            }
+            while (mask) {  // usually one point; a stale value leaves the list as it is
+                const int c = __ffs(mask) - 1;
+                mask &= mask - 1;
+                float2 qq = q[0];
+#pragma unroll
+                for (int u = 1; u < UP; ++u) qq = ((c >> 1) == u) ? q[u] : qq;
+                knn_insert<KP>(dk[r], ik[r], (c & 1) ? qq.y : qq.x, (int)(jt + g * UPT + c));
+            }
         }
         nc[r] = 0;
     }
@@ -472,14 +497,13 @@ __global__ void __launch_bounds__(kThreads, knn_buffer(DP, KP) > 0 ? 4 : 1) knn2
     constexpr int UP = unroll_pairs(DP);
     constexpr int UPT = 2 * UP;
     constexpr int CB = knn_buffer(DP, KP);
-    constexpr int CBA = CB > 0 ? CB : 1;
-    constexpr int G = CB > 0 ? knn_check_groups(DP, KP) : 1;  // groups between buffer checks
-    constexpr int DRAIN_AT = CB - G * UPT;  // a lane above this many entries may overflow
-    static_assert(CB == 0 || DRAIN_AT >= 0, "buffer smaller than the points between checks");
+    constexpr int G = CB > 0 ? knn_check_groups(DP, KP) : 1;  // groups between queue checks
+    constexpr int DRAIN_AT = CB - G;  // a lane with more entries in one row may overflow it
+    static_assert(CB == 0 || DRAIN_AT >= 0, "queue shorter than the groups between checks");
     static_assert(BN % (G * UPT) == 0, "tile must be a multiple of the unroll");
     __shared__ __align__(16) float tile[(BN / 2) * PS2];
-    // per row r, slot s, thread t: cbuf[(r CB + s) kThreads + t] = (d, j bits)
-    __shared__ __align__(16) float2 cbuf[CB > 0 ? R * CB * kThreads : 2];
+    // per row r, slot s, thread t: qbuf[(r CB + s) kThreads + t] = a passing group of the tile
+    __shared__ int qbuf[CB > 0 ? R * CB * kThreads : 1];
 
     const int t = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.x * (kThreads * R);
@@ -492,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, knn_buffer(DP, KP) > 0 ? 4 : 1) knn2
     float dk[R][KP];
     int ik[R][KP];
     int nc[R];
-    int ntot = 0;  // entries over all of this thread's buffers (bounds each nc[r])
+    int nmax = 0;  // the largest of this thread's queue lengths (an upper bound)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
@@ -512,8 +536,8 @@ __global__ void __launch_bounds__(kThreads, knn_buffer(DP, KP) > 0 ? 4 : 1) knn2
 
         for (int jg = 0; jg < nvp; jg += G * UPT) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const int jj = jg + g * UPT;
+            for (int gg = 0; gg < G; ++gg) {
+                const int jj = jg + gg * UPT;
                 float2 q[UP][R];
 #pragma unroll
                 for (int u = 0; u < UP; ++u) {
@@ -529,39 +553,40 @@ __global__ void __launch_bounds__(kThreads, knn_buffer(DP, KP) > 0 ? 4 : 1) knn2
 #pragma unroll
                     for (int u = 1; u < UP; ++u) mn = fminf(mn, fminf(q[u][r].x, q[u][r].y));
                     if (mn < dk[r][KP - 1]) {
-                        const float thr = dk[r][KP - 1];
-                        unsigned mask = 0;
+                        if (CB == 0) {
+                            const float thr = dk[r][KP - 1];
+                            unsigned mask = 0;
 #pragma unroll
-                        for (int u = 0; u < UP; ++u) {
-                            mask |= (q[u][r].x < thr ? 1u : 0u) << (2 * u);
-                            mask |= (q[u][r].y < thr ? 1u : 0u) << (2 * u + 1);
-                        }
-                        const int j0 = (int)(jt + jj);
-                        while (mask) {
-                            const int c = __ffs(mask) - 1;
-                            mask &= mask - 1;
-                            float2 qq = q[0][r];
-#pragma unroll
-                            for (int u = 1; u < UP; ++u) qq = ((c >> 1) == u) ? q[u][r] : qq;
-                            const float v = (c & 1) ? qq.y : qq.x;
-                            if (CB == 0) {
-                                knn_insert<KP>(dk[r], ik[r], v, j0 + c);
-                            } else {
-                                cbuf[(r * CB + nc[r]) * kThreads + t] = make_float2(v, __int_as_float(j0 + c));
-                                ++nc[r];
-                                ++ntot;
+                            for (int u = 0; u < UP; ++u) {
+                                mask |= (q[u][r].x < thr ? 1u : 0u) << (2 * u);
+                                mask |= (q[u][r].y < thr ? 1u : 0u) << (2 * u + 1);
                             }
+                            const int j0 = (int)(jt + jj);
+                            while (mask) {
+                                const int c = __ffs(mask) - 1;
+                                mask &= mask - 1;
+                                float2 qq = q[0][r];
+#pragma unroll
+                                for (int u = 1; u < UP; ++u) qq = ((c >> 1) == u) ? q[u][r] : qq;
+                                knn_insert<KP>(dk[r], ik[r], (c & 1) ? qq.y : qq.x, j0 + c);
+                            }
+                        } else {
+                            qbuf[(r * CB + nc[r]) * kThreads + t] = jj / UPT;
+                            nmax = max(nmax, ++nc[r]);
                         }
                     }
                 }
             }
-            if (CB > 0 && __any_sync(0xffffffffu, ntot > DRAIN_AT)) {
-                knn_drain_warp<KP, CBA, R>(dk, ik, nc, cbuf);
-                ntot = 0;
+            if (CB > 0 && __any_sync(0xffffffffu, nmax > DRAIN_AT)) {
+                knn_drain_groups<DP, KP, R, PS2, UP>(x2, dk, ik, nc, qbuf, tile, jt, CB > 0 ? CB : 1);
+                nmax = 0;
             }
         }
+        if (CB > 0) {  // the queues name points of this tile: drain before it is replaced
+            knn_drain_groups<DP, KP, R, PS2, UP>(x2, dk, ik, nc, qbuf, tile, jt, CB > 0 ? CB : 1);
+            nmax = 0;
+        }
     }
-    if (CB > 0) knn_drain_warp<KP, CBA, R>(dk, ik, nc, cbuf);
 
 #pragma unroll
     for (int r = 0; r < R; ++r) {

@@ -122,7 +122,8 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
     const int t = threadIdx.x;
     // Dense mode: row block blockIdx.x, split blockIdx.y's column chunk.  Block-sparse
     // mode: the work table gives the block's rows and its list of column ranges, which
-    // need not be in increasing j, so Max/Min then breaks ties on the index itself.
+    // need not be in increasing j, so Max/Min then breaks ties on the index itself;
+    // with S splits, split blockIdx.y takes every S-th tile of the ranges.
     const bool ranged = a.blk != nullptr;
     int64_t row0 = (int64_t)blockIdx.x * (kThreads * R), row_end = a.M;
     int r_lo = 0, r_hi = 1;
@@ -165,10 +166,12 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
             bj[r][e] = -1;
         }
 
+    int tk = 0;  // block-sparse: tiles seen over the block's ranges; split y takes tk = y mod S
     for (int rr = r_lo; rr < r_hi; ++rr) {
     const int64_t js = ranged ? (int64_t)a.rng[rr].x : j_begin;
     const int64_t je = ranged ? (int64_t)a.rng[rr].y : j_end;
     for (int64_t jt = js; jt < je; jt += BN) {
+        if (ranged && (tk++ % a.S) != (int)blockIdx.y) continue;  // uniform across the block
         const int nv = (int)min((int64_t)BN, je - jt);
         const int nvp = (nv + UPT - 1) / UPT * UPT;
         __syncthreads();  // every thread is done with the previous tile
