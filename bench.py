@@ -55,22 +55,24 @@ K_NN = 10
 # (distance) + 1 mul (k*b) + D fma;  K-min: D sub + D fma + 1 compare.
 # Other kernels (Sum, Max/Min): Laplace adds a square root on the XU pipe before
 # the ex2; Cauchy and the inverse multiquadric start the distance sum at 1 and take
-# one rcp / rsqrt instead of the ex2.  Max/Min: k*b is one multiply per column and
-# the running comparison one ALU op per pair.
-XU_PER_KERNEL = {"gaussian": 1, "laplace": 2, "cauchy": 1, "imq": 1}
+# one rcp / rsqrt instead of the ex2.  Each XU operation has its own rate (measured
+# by the pipe probe), so XU counts are kept per operation.  Max/Min: k*b is one
+# multiply per column and the running comparison one ALU op per pair.
+XU_PER_KERNEL = {"gaussian": {"ex2": 1}, "laplace": {"sqrt": 1, "ex2": 1}, "cauchy": {"rcp": 1},
+                 "imq": {"rsqrt": 1}}
 
 
 def ops_per_pair(op: str, D: int, E: int = 1, kernel: str = "gaussian"):
     if op == "sum":
-        return {"fp32": 2 * D + E, "xu": XU_PER_KERNEL[kernel], "alu": 0}
+        return {"fp32": 2 * D + E, "xu": dict(XU_PER_KERNEL[kernel]), "alu": 0}
     if op in ("max", "min"):
-        return {"fp32": 2 * D + E, "xu": XU_PER_KERNEL[kernel], "alu": E}
+        return {"fp32": 2 * D + E, "xu": dict(XU_PER_KERNEL[kernel]), "alu": E}
     if op == "lse":
-        return {"fp32": 2 * D + E, "xu": E, "alu": 0}
+        return {"fp32": 2 * D + E, "xu": {"ex2": E}, "alu": 0}
     if op == "grad":
-        return {"fp32": 3 * D + 1 + (E if E > 1 else 0), "xu": 1, "alu": 0}
+        return {"fp32": 3 * D + 1 + (E if E > 1 else 0), "xu": {"ex2": 1}, "alu": 0}
     if op == "knn":
-        return {"fp32": 2 * D, "xu": 0, "alu": 1}
+        return {"fp32": 2 * D, "xu": {}, "alu": 1}
     raise ValueError(op)
 
 
@@ -160,7 +162,7 @@ def probe_pipes(torch, nsm):
     sink = torch.zeros(1, device="cuda")
     cyc = torch.zeros(blocks, dtype=torch.int64, device="cuda")
     ms = {}
-    for kind in (0, 2, 0, 2):
+    for kind in (0, 2, 3, 4, 5, 0, 2, 3, 4, 5):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
@@ -171,10 +173,14 @@ def probe_pipes(torch, nsm):
             raise RuntimeError(f"probe launch failed: {rc}")
         torch.cuda.synchronize()
         ms[kind] = e0.elapsed_time(e1)          # the second run of each kind is kept
-    ratio = ms[0] / ms[2]                       # same lane count in both probes
-    measured = FP32_LANES_PER_SM * ratio
-    return {"xu": float(2 ** round(np.log2(measured))), "xu_measured": measured, "ex2_to_ffma": ratio,
-            "ffma_lanes_per_s": nsm * bps * 256 * iters * 8 / (ms[0] / 1e3)}
+    lanes = {}
+    for name, kind in (("ex2", 2), ("rcp", 3), ("rsqrt", 4), ("sqrt", 5)):
+        measured = FP32_LANES_PER_SM * ms[0] / ms[kind]   # same lane count in both probes
+        lanes[name] = float(2 ** round(np.log2(measured)))
+        lanes[name + "_measured"] = measured
+    return {"xu": lanes["ex2"], "xu_lanes": {k: v for k, v in lanes.items() if not k.endswith("_measured")},
+            "xu_measured": {k[:-9]: v for k, v in lanes.items() if k.endswith("_measured")},
+            "ex2_to_ffma": ms[0] / ms[2], "ffma_lanes_per_s": nsm * bps * 256 * iters * 8 / (ms[0] / 1e3)}
 
 
 # Tensor-core Sum (E = 1, 32 <= D <= 62): per pair, three fp16 products (hi.hi, hi.lo,
@@ -204,23 +210,26 @@ def roofline_tensor(seconds_per_launch, pairs, kernel, fp32_line):
 
 def roofline(op, D, E, seconds_per_launch, pairs, nsm, clk_mhz, xu_lanes, kernel, live_mhz=None,
              kind="gaussian"):
+    """xu_lanes: {XU operation: lanes per clock per SM} from the pipe probe."""
     n = ops_per_pair(op, D, E, kind)
+    xu_clk = sum(cnt / xu_lanes[name] for name, cnt in n["xu"].items())   # XU clocks per pair per SM lane set
 
     def peak_at(mhz):
         f = mhz * 1e6
-        t = max(n["fp32"] / (nsm * FP32_LANES_PER_SM * f),
-                n["xu"] / (nsm * xu_lanes * f) if n["xu"] else 0.0,
+        t = max(n["fp32"] / (nsm * FP32_LANES_PER_SM * f), xu_clk / (nsm * f),
                 n["alu"] / (nsm * ALU_LANES_PER_SM * f) if n["alu"] else 0.0)
         return 1.0 / t
 
     peak = peak_at(clk_mhz)
     achieved = pairs / seconds_per_launch
-    pipe = "xu" if n["xu"] / xu_lanes > n["fp32"] / FP32_LANES_PER_SM else "fp32"
+    pipe = "xu" if xu_clk > n["fp32"] / FP32_LANES_PER_SM else "fp32"
     tr = TRAFFIC.get(kernel)
     traffic = tr["bytes_per_launch"] if tr and tr.get("source_hash") == _kernel_source_hash() else None
     out = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
            "traffic": traffic, "kernel": kernel, "limiting_pipe": pipe, "ops_per_pair": n,
-           "peak_basis": f"{nsm} SMs x (128 FP32, {xu_lanes:.0f} ex2, 64 ALU) lanes/clk x {clk_mhz:.0f} MHz max SM clock"}
+           "peak_basis": f"{nsm} SMs x (128 FP32, 64 ALU; XU per op " +
+                         ", ".join(f"{k} {v:.0f}" for k, v in xu_lanes.items()) +
+                         f") lanes/clk x {clk_mhz:.0f} MHz max SM clock"}
     if live_mhz:
         out["frac_at_live_clock"] = achieved / peak_at(live_mhz)
     return out
@@ -274,8 +283,9 @@ def run_ours(args, rank, world, local_rank):
         for _, fn in ops:
             fn()
     torch.cuda.synchronize(dev)
-    probe = probe_pipes(torch, nsm) if rank == 0 else {"xu": 32.0}
-    xu_lanes = probe["xu"]
+    probe = probe_pipes(torch, nsm) if rank == 0 else {"xu_lanes": {"ex2": 32.0, "rcp": 16.0, "rsqrt": 16.0,
+                                                                    "sqrt": 16.0}}
+    xu_lanes = probe["xu_lanes"]
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
     if world > 1:

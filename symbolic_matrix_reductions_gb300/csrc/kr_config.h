@@ -80,6 +80,8 @@ KR_HD constexpr int tile_points_packed(int PS2) {
 // two must stay within 48 KB of static shared memory.  Queued instances are
 // compiled for 4 resident blocks per SM (at most 128 registers a thread).
 KR_HD constexpr int knn_buffer(int DP, int KP) { return DP <= 4 && KP <= 10 ? 16 : 0; }
+// Resident blocks per SM the queued K-min instances are compiled for (registers cap).
+KR_HD constexpr int knn_min_blocks(int DP, int KP) { return knn_buffer(DP, KP) > 0 ? 4 : 1; }
 // Unrolled point groups between two warp-wide checks of the candidate buffers.
 KR_HD constexpr int knn_check_groups(int DP, int KP) { return 2; }
 // Pair records per unrolled step of the packed inner loop.

@@ -491,7 +491,7 @@ __device__ __forceinline__ void knn_drain_groups(const float2 (&x2)[R][DP], floa
 }
 
 template <int DP, int KP, int R, int BN>
-__global__ void __launch_bounds__(kThreads, knn_buffer(DP, KP) > 0 ? 4 : 1) knn2_kernel(const Args a_) {
+__global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knn2_kernel(const Args a_) {
     const Args a = batch_view(a_);
     constexpr int PS2 = pair_stride(DP, 0);
     constexpr int UP = unroll_pairs(DP);

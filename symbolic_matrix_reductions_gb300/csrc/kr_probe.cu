@@ -16,7 +16,24 @@ __device__ __forceinline__ float ex2_approx(float v) {
     return r;
 }
 
-// kind 0: scalar FFMA; 1: packed FFMA2 (f32x2); 2: MUFU ex2.approx.
+__device__ __forceinline__ float rcp_approx(float v) {
+    float r;
+    asm volatile("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float rsqrt_approx(float v) {
+    float r;
+    asm volatile("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float sqrt_approx(float v) {
+    float r;
+    asm volatile("sqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// kind 0: scalar FFMA; 1: packed FFMA2 (f32x2); 2: ex2.approx; 3: rcp.approx;
+// 4: rsqrt.approx; 5: sqrt.approx (the transcendental-unit operations of the kernels).
 template <int KIND>
 __global__ void __launch_bounds__(256) probe_kernel(int iters, float seed, float *sink, long long *cycles) {
     float v[kChains];
@@ -35,6 +52,9 @@ __global__ void __launch_bounds__(256) probe_kernel(int iters, float seed, float
             if (KIND == 0) v[c] = fmaf(v[c], 0.999f, 0.001f);
             if (KIND == 1) w[c] = __ffma2_rn(w[c], m2, a2);
             if (KIND == 2) v[c] = ex2_approx(-v[c]);
+            if (KIND == 3) v[c] = rcp_approx(v[c]);     // alternates between v and 1/v
+            if (KIND == 4) v[c] = rsqrt_approx(v[c]);   // tends to 1
+            if (KIND == 5) v[c] = sqrt_approx(v[c]);    // tends to 1
         }
     }
     __syncthreads();
@@ -59,6 +79,9 @@ int kr_probe_pipe(int kind, int blocks, int iters, float *sink_dev, long long *c
         case 0: probe_kernel<0><<<blocks, 256, 0, s>>>(iters, 0.5f, sink_dev, cycles_dev); break;
         case 1: probe_kernel<1><<<blocks, 256, 0, s>>>(iters, 0.5f, sink_dev, cycles_dev); break;
         case 2: probe_kernel<2><<<blocks, 256, 0, s>>>(iters, 0.5f, sink_dev, cycles_dev); break;
+        case 3: probe_kernel<3><<<blocks, 256, 0, s>>>(iters, 0.5f, sink_dev, cycles_dev); break;
+        case 4: probe_kernel<4><<<blocks, 256, 0, s>>>(iters, 0.5f, sink_dev, cycles_dev); break;
+        case 5: probe_kernel<5><<<blocks, 256, 0, s>>>(iters, 0.5f, sink_dev, cycles_dev); break;
         default: return (int)cudaErrorInvalidValue;
     }
     return (int)cudaGetLastError();
