@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(256) probe_kernel(int iters, float seed, float
             if (KIND == 0) v[c] = fmaf(v[c], 0.999f, 0.001f);
             if (KIND == 1) w[c] = __ffma2_rn(w[c], m2, a2);
             if (KIND == 2) v[c] = ex2_approx(-v[c]);
-            if (KIND == 3) v[c] = rcp_approx(v[c]);     // alternates between v and 1/v
+            if (KIND == 3) v[c] = rcp_approx(v[c] + 0.5f);  // the add keeps 1/(1/v) from folding
             if (KIND == 4) v[c] = rsqrt_approx(v[c]);   // tends to 1
             if (KIND == 5) v[c] = sqrt_approx(v[c]);    // tends to 1
         }
