@@ -36,8 +36,11 @@
  *           only, the call is asynchronous on `stream`.
  * Ownership. The caller owns every array, outputs included; the library never
  *           frees or keeps caller memory.  Workspace (split-j partials, staging)
- *           is taken stream-ordered (cudaMallocAsync / cudaFreeAsync on
- *           `stream`) and released before the work it serves is complete.
+ *           is taken stream-ordered on `stream` from a memory pool the library
+ *           creates on each device (cudaMemPoolCreate; cudaMallocFromPoolAsync /
+ *           cudaFreeAsync) and released in stream order after the work it serves.
+ *           The pool keeps up to 256 MiB of freed workspace across
+ *           synchronisations for the next call and returns the rest.
  * Aliasing. Outputs must not overlap inputs or each other.
  * Stream.   `stream` is a cudaStream_t (NULL = the legacy default stream).  The
  *           device is the current device of the calling thread.

@@ -160,7 +160,9 @@ static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int bl
             if (batch * workspace_bytes(op, in, M, D, EK, (int)s) > kMaxWorkspace) break;
             const int64_t chunk = (N + s - 1) / s;
             const int64_t tiles = (chunk + in.tile - 1) / in.tile;
-            double work = (double)chunk + 32.0 * (double)tiles;   // per block, in points
+            // per block, in points: its chunk, a per-tile cost (staging, barriers) and a fixed
+            // cost (loading its rows, writing its partials, its share of the combine)
+            double work = (double)chunk + 32.0 * (double)tiles + 128.0;
             if (op == OP_KNN) {
                 const double groups = (double)chunk / group;
                 const double events = groups <= lanes_k ? groups : lanes_k * (1.0 + std::log(groups / lanes_k));
@@ -169,8 +171,10 @@ static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int bl
             const int64_t per_sm = (p->row_blocks * s * batch + num_sms - 1) / num_sms;
             const int64_t conc = std::min<int64_t>(per_sm, blocks_per_sm);
             const double eff = std::min(1.0, (double)(conc * (kThreads / 32)) / 16.0);
-            // each split also costs a little in partial traffic and the combine
-            const double cost = (double)per_sm * work / eff * (1.0 + 0.002 * (double)s);
+            // each split also costs a little in partial traffic and the combine, and splitting
+            // at all costs a workspace allocation and a combine launch (worth ~4096 points of
+            // one block's work, about 60 us)
+            const double cost = (double)per_sm * work / eff * (1.0 + 0.002 * (double)s) + (s > 1 ? 4096.0 : 0.0);
             if (s == 1 || cost < best * 0.999) {
                 best = cost;
                 S = (int)s;
@@ -196,6 +200,8 @@ struct DeviceCache {
     int occ[kNumOps][kNumKernels][10][33] = {};  // resident blocks per (op, kernel kind, d_pad index,
                                                  // ek_pad); 0 = not queried
     int tc_occ = 0;           // resident tensor-core Sum blocks; 0 = not queried
+    cudaMemPool_t pool = nullptr;  // the library's workspace pool on this device
+    bool pool_tried = false;
 };
 std::mutex g_cache_mutex;
 DeviceCache g_cache[64];
@@ -248,6 +254,35 @@ int device_info(int dev, int op, int kind, const Instance &in, int *num_sms, int
     if (slot == 0) slot = query_occupancy(op, kind, in);
     *occ = slot;
     return 0;
+}
+
+// Workspace and staging memory come from a stream-ordered pool the library owns on
+// each device, so freed blocks are reused by the next call instead of going back to
+// the driver at every synchronisation (the default pool's behaviour).  The pool keeps
+// at most kPoolKeep bytes across synchronisations; larger peaks are returned.
+constexpr uint64_t kPoolKeep = (uint64_t)256 << 20;
+
+cudaMemPool_t device_pool(int dev) {
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_cache_mutex);
+    DeviceCache &c = g_cache[dev];
+    if (!c.pool_tried) {
+        c.pool_tried = true;
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) == cudaSuccess) {
+            uint64_t keep = kPoolKeep;
+            cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+            c.pool = pool;
+        } else {
+            cudaGetLastError();  // no pool: allocate from the device's default pool
+        }
+    }
+    return c.pool;
 }
 
 int device_tc_occupancy(int dev) {
@@ -310,7 +345,7 @@ static int validate(int op, const Buf *bufs, int nbuf, int64_t M, int64_t N, int
 }
 
 // ---- allocation (with an opt-in failure injection for tests) -----------------------
-static cudaError_t ws_alloc(void **p, size_t bytes, cudaStream_t s) {
+static cudaError_t ws_alloc(void **p, size_t bytes, cudaStream_t s, int dev) {
     // KREDUCE_FAIL_ALLOC=1 makes every workspace/staging allocation fail, so that
     // the KR_ERR_ALLOC path can be tested without exhausting device memory.
     const char *inj = std::getenv("KREDUCE_FAIL_ALLOC");
@@ -318,7 +353,8 @@ static cudaError_t ws_alloc(void **p, size_t bytes, cudaStream_t s) {
         *p = nullptr;
         return cudaErrorMemoryAllocation;
     }
-    return cudaMallocAsync(p, bytes, s);
+    cudaMemPool_t pool = device_pool(dev);
+    return pool ? cudaMallocFromPoolAsync(p, bytes, pool, s) : cudaMallocAsync(p, bytes, s);
 }
 
 // Is `p` directly usable by kernels?  Host memory (pageable or pinned) is staged.
@@ -488,7 +524,7 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
     const int64_t ws_bytes = (p.workspace_bytes + 255) / 256 * 256;
     char *mem = nullptr;
     if (stage_bytes + ws_bytes > 0) {
-        ce = ws_alloc((void **)&mem, (size_t)(stage_bytes + ws_bytes), stream);
+        ce = ws_alloc((void **)&mem, (size_t)(stage_bytes + ws_bytes), stream, dev);
         if (ce != cudaSuccess) {
             cudaGetLastError();
             return KR_ERR_ALLOC;
