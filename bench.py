@@ -462,7 +462,7 @@ def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
     del xt, yt, bt
 
     plan = [("gauss_d3", [("grad_y", None), ("grad_b", None)]),
-            ("gauss_d3_unit", [("sum", "b"), ("lse", "w_log")]), ("falkon_d50", [("sum", "b")]),
+            ("gauss_d3_unit", [("sum", "b"), ("lse", "w_log")]), ("falkon_d50", [("sum", "b"), ("lse", "b")]),
             ("knn_d16", [("knn", None)])]
     for wname, ops in plan:
         inp = W.generate(wname)
@@ -505,7 +505,7 @@ def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
             ms = _time_op(torch, fn, 2)
             rl = roofline(op, D, E, ms / 1e3, M * N, nsm, max_mhz, xu_lanes, kname)
             if getattr(p, "path", 1) == kr.KR_PATH_TENSOR_CORES:
-                rl = roofline_tensor(ms / 1e3, M * N, "tc_sum_kernel (tcgen05)", rl)
+                rl = roofline_tensor(ms / 1e3, M * N, f"tc_{op}_kernel (tcgen05)", rl)
             out.append({"workload": f"{wname}: {W.WORKLOADS[wname].note}", "op": op, "ms": ms,
                         "value": M * N / (ms / 1e3), "unit": UNIT, "split": p.split,
                         "path": "tensor cores" if getattr(p, "path", 1) == kr.KR_PATH_TENSOR_CORES else "cuda cores",

@@ -111,7 +111,9 @@ static void plan_tc(int64_t M, int64_t N, int num_sms, int blocks_per_sm, int fo
     S = (int)std::max<int64_t>(1, (N + p->chunk - 1) / p->chunk);  // every split nonempty
     p->split = S;
     const int64_t n_pad = round_up(std::max<int64_t>(N, 1), kTcCols);
-    const int64_t operands = (round_up(std::max<int64_t>(M, 1), kTcRows) + n_pad) * 256 + n_pad * 4;
+    // split fp16 operands (256 B a point), the padded signal / weights, the LSE tile frames
+    const int64_t operands = (round_up(std::max<int64_t>(M, 1), kTcRows) + n_pad) * 256 + n_pad * 4 +
+                             round_up(n_pad / kTcCols * 4, 256);
     p->workspace_bytes = 256 + operands + (S > 1 ? 2 * (int64_t)S * M * (int64_t)sizeof(float) : 0);
 }
 
@@ -119,7 +121,8 @@ static int64_t batch_of(const kr_options *opt) { return opt && opt->batch > 1 ? 
 
 static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, const kr_options *opt) {
     const int path = opt ? opt->path : 0, kind = opt ? opt->kernel : KR_KERNEL_GAUSSIAN;
-    if (op != OP_SUM || kind != KR_KERNEL_GAUSSIAN || path == KR_PATH_CUDA_CORES || !tc_dims(D, EK)) return false;
+    if ((op != OP_SUM && op != OP_LSE) || kind != KR_KERNEL_GAUSSIAN || path == KR_PATH_CUDA_CORES || !tc_dims(D, EK))
+        return false;
     if (batch_of(opt) > 1) return false;  // the tensor-core prepass and tiles serve one problem
     return (round_up(std::max<int64_t>(M, 1), kTcRows) + round_up(std::max<int64_t>(N, 1), kTcCols)) * 256 <=
            kMaxTcOperands;
@@ -395,7 +398,8 @@ static double kernel_prescale(int kind, float sigma) {
 // Workspace: [guard (2 x u32) + status | A_hi | A_lo | B_hi | B_lo | padded b | partials].  The
 // CUDA-core kernel is always launched after the tensor kernel with the same splits;
 // it returns at once unless the prepass found norms the expansion cannot serve.
-static cudaError_t run_tc(Args a, const kr_plan_t &p, const Instance &in, char *ws, cudaStream_t stream) {
+static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in, char *ws, cudaStream_t stream) {
+    const bool lse = op == OP_LSE;
     const int64_t m_pad = round_up(a.M, kTcRows), n_pad = round_up(std::max<int64_t>(a.N, 1), kTcCols);
     unsigned *guard = (unsigned *)ws;
     __half *a_hi = (__half *)(ws + 256);
@@ -403,12 +407,14 @@ static cudaError_t run_tc(Args a, const kr_plan_t &p, const Instance &in, char *
     __half *b_hi = a_lo + m_pad * 64;
     __half *b_lo = b_hi + n_pad * 64;
     float *bpad = (float *)(b_lo + n_pad * 64);
-    float *part = bpad + n_pad;
+    float *fpad = bpad + n_pad;
+    float *part = (float *)((char *)fpad + round_up(n_pad / kTcCols * 4, 256));
     cudaError_t ce = cudaMemsetAsync(guard, 0, 256, stream);
     if (ce == cudaSuccess)
-        ce = tc_launch_prep(a.x, a.M, m_pad, a.D, a.c, true, a_hi, a_lo, guard, nullptr, nullptr, stream);
+        ce = tc_launch_prep(a.x, a.M, m_pad, a.D, a.c, true, a_hi, a_lo, guard, nullptr, nullptr, nullptr, stream);
     if (ce == cudaSuccess)
-        ce = tc_launch_prep(a.y, a.N, n_pad, a.D, a.c, false, b_hi, b_lo, guard + 1, a.b, bpad, stream);
+        ce = tc_launch_prep(a.y, a.N, n_pad, a.D, a.c, false, b_hi, b_lo, guard + 1, a.b, bpad,
+                            lse ? fpad : nullptr, stream);
     if (p.split > 1) {
         a.ws0 = part;
         a.ws1 = part + (int64_t)p.split * a.M;
@@ -420,6 +426,8 @@ static cudaError_t run_tc(Args a, const kr_plan_t &p, const Instance &in, char *
         t.b_hi = b_hi;
         t.b_lo = b_lo;
         t.bpad = bpad;
+        t.fpad = fpad;
+        t.lse = lse;
         t.m_pad = m_pad;
         t.n_pad = n_pad;
         t.out = a.out;
@@ -433,12 +441,13 @@ static cudaError_t run_tc(Args a, const kr_plan_t &p, const Instance &in, char *
         t.S = p.split;
         ce = tc_launch_sum(t, dim3((unsigned)p.row_blocks, (unsigned)p.split), stream);
     }
-    if (ce == cudaSuccess) {
+    if (ce == cudaSuccess) {  // the CUDA-core stand-in: returns at once unless the guard failed
         a.tc_guard = guard;
         const int64_t bm = (int64_t)kThreads * in.rows;
-        ce = launch_sum(in, a, dim3((unsigned)((a.M + bm - 1) / bm), (unsigned)p.split), stream);
+        const dim3 grid((unsigned)((a.M + bm - 1) / bm), (unsigned)p.split);
+        ce = lse ? launch_lse(in, a, grid, stream) : launch_sum(in, a, grid, stream);
     }
-    if (ce == cudaSuccess && p.split > 1) ce = launch_combine(OP_SUM, in, a, stream);
+    if (ce == cudaSuccess && p.split > 1) ce = launch_combine(op, in, a, stream);
     return ce;
 }
 
@@ -588,7 +597,7 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
                                    dim3((unsigned)p.row_blocks, (unsigned)p.split, 1), stream);
             if (ce == cudaSuccess && p.split > 1) ce = launch_combine(op, in, a, stream);
         } else if (tc) {
-            ce = run_tc(a, p, in, ws, stream);
+            ce = run_tc(op, a, p, in, ws, stream);
         } else {
             if (p.split > 1) {
                 a.ws0 = (float *)ws;

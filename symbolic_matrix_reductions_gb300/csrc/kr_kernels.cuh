@@ -143,8 +143,7 @@ __device__ __forceinline__ void zero_pad_coords(const Args &a, float *tile) {
 template <int DP, int EP, int R, int BN, bool LSE>
 __global__ void __launch_bounds__(kThreads) fwd_kernel(const Args a_) {
     const Args a = batch_view(a_);
-    if (!LSE && a.tc_guard &&
-        __uint_as_float(a.tc_guard[0]) + __uint_as_float(a.tc_guard[1]) <= kTcNormLimit)
+    if (a.tc_guard && __uint_as_float(a.tc_guard[0]) + __uint_as_float(a.tc_guard[1]) <= kTcNormLimit)
         return;  // the tensor-core kernel computed this call
     constexpr int PS = pack_stride(DP, EP);
     constexpr int U = unroll_points(DP);

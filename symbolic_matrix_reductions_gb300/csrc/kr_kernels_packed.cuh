@@ -97,8 +97,7 @@ __device__ __forceinline__ float2 sq_dist_pair(const float2 (&x2)[DP], const flo
 template <int DP, int EP, int R, int BN, bool LSE>
 __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
     const Args a = batch_view(a_);
-    if (!LSE && a.tc_guard &&
-        __uint_as_float(a.tc_guard[0]) + __uint_as_float(a.tc_guard[1]) <= kTcNormLimit)
+    if (a.tc_guard && __uint_as_float(a.tc_guard[0]) + __uint_as_float(a.tc_guard[1]) <= kTcNormLimit)
         return;  // the tensor-core kernel computed this call
     constexpr int PS2 = pair_stride(DP, EP);
     constexpr int UP = unroll_pairs(DP);

@@ -14,6 +14,13 @@
 // kernel leaves the work to the CUDA-core kernel launched after it (which runs only
 // in that case), without a host round trip.
 //
+// The LogSumExp (tc_lse_kernel) shares everything up to the evaluation: the prepass
+// stores each B tile's weights relative to the tile's largest, w' - F (w' = w log2 e),
+// so every term 2^(t + w' - F) is at most 1 (t <= 0 is the exponent above), and the
+// evaluation warps fold each tile's partial into a running (frame, hi, lo) per row.
+// Within the norm guard t >= -32, so the tile's largest-weight term is at least
+// 2^-32 and the partial cannot vanish while a finite weight is present.
+//
 // Block = 10 warps, one block per SM, warp-specialised around mbarriers:
 //   warp 0, one thread: TMA producer.  Loads the block's A tiles (hi, lo) once, then
 //     streams B tiles of 256 points (hi, lo: 2 x 32 KB, landing in the
@@ -58,6 +65,7 @@ constexpr int kBTileBytes = kCols * 128;  // 256 rows x 64 fp16
 constexpr int kTmemCols = 2 * kCols;      // two fp32 accumulators
 constexpr long kWaitLimit = 1L << 26;     // mbarrier polls before giving up
 static_assert(kThreadsTc == 64 + 32 * kEvalWarps, "warp roles");
+static_assert(kCols == 256, "the prepass computes an LSE tile frame per block of 256 threads");
 static_assert(kTmemCols <= 512, "TMEM has 512 columns");
 
 // Dynamic shared memory: A hi, A lo, kStages x (B hi, B lo), plus 1 KB of alignment
@@ -159,12 +167,31 @@ __device__ __forceinline__ bool norms_ok(const unsigned *guard) {
 // zero.  guard receives the largest |.'|^2 (as float bits; non-negative floats
 // order like unsigned integers).  With b non-null, bpad[r] = b[r] (0 past `rows`).
 // ---------------------------------------------------------------------------
+// LogSumExp (fpad non-null): b holds the log-weights w; block k of 256 threads is
+// tile k of the B operands, and its frame F_k = max over the tile of w' = w log2 e
+// goes to fpad[k] while bpad[r] = w'_r - F_k <= 0 (-inf past `rows`), so every term
+// 2^(t + bpad) of the tile is at most 1 in the frame F_k.
 __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t rows, int64_t rows_pad, int D,
                                                       float c, int is_x, __half *hi, __half *lo, unsigned *guard,
-                                                      const float *b, float *bpad) {
+                                                      const float *b, float *bpad, float *fpad) {
+    __shared__ float wmax[8];
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (r >= rows_pad) return;
+    if (r >= rows_pad) return;  // with fpad, rows_pad is a multiple of 256: whole blocks leave together
     const bool live = r < rows;
+    if (fpad) {
+        const float wl = live ? 1.4426950408889634f * __ldg(b + r) : -__int_as_float(0x7f800000);
+        float m = wl;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+        __syncthreads();
+        float F = wmax[0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) F = fmaxf(F, wmax[k]);
+        if (F == -__int_as_float(0x7f800000)) F = 0.f;  // no weight in the tile: any frame
+        bpad[r] = wl - F;
+        if (threadIdx.x == 0) fpad[blockIdx.x] = F;
+    }
     const float *row = src + (live ? r : 0) * D;
     float n = 0.f;
     if (live) {
@@ -174,7 +201,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t 
         }
         atomicMax(guard, __float_as_uint(n));
     }
-    if (bpad) bpad[r] = live ? __ldg(b + r) : 0.f;
+    if (bpad && !fpad) bpad[r] = live ? __ldg(b + r) : 0.f;
     const float scale = is_x ? 2.f * c : c;
     const float v_d = is_x ? -n : 1.f, v_d1 = is_x ? -1.f : n;
     uint4 *ph = reinterpret_cast<uint4 *>(hi + r * 64);
@@ -200,7 +227,8 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t 
 // Main kernel: grid (ceil(M/128), S); block (row block, split) reduces its 128 rows
 // over the split's tiles of 256 points.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreadsTc, 1) tc_sum_kernel(const __grid_constant__ TcParams p) {
+template <bool LSE>
+__device__ __forceinline__ void tc_body(const TcParams &p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -247,6 +275,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_sum_kernel(const __grid_cons
     const uint32_t tmem = tmem_slot;
 
     float hi = 0.f, lo = 0.f;
+    float m = -__int_as_float(0x7f800000);  // LSE: the frame of (hi, lo), base 2
     if (w == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0 && T > 0) {
@@ -312,29 +341,49 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_sum_kernel(const __grid_cons
             asm volatile("tcgen05.fence::before_thread_sync;");
             __syncwarp();
             if (lane == 0) mbar_arrive(b_acce0 + 8 * k);  // the MMAs of tile i+2 may overwrite it
-            // b of the tile's points (zero past N), the same for all lanes: L1 broadcasts
+            // b of the tile's points (zero past N), or the LSE weights relative to the tile's
+            // frame (-inf past N); the same for all lanes: L1 broadcasts
             const float4 *bv = reinterpret_cast<const float4 *>(p.bpad + j_begin + (int64_t)i * kCols + c0);
             float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
             for (int q = 0; q < kEvalCols; q += 4) {
                 const float4 b4 = __ldg(bv + q / 4);
-                p0 = fmaf(ex2_approx(__uint_as_float(r[q + 0])), b4.x, p0);
-                p1 = fmaf(ex2_approx(__uint_as_float(r[q + 1])), b4.y, p1);
-                p2 = fmaf(ex2_approx(__uint_as_float(r[q + 2])), b4.z, p2);
-                p3 = fmaf(ex2_approx(__uint_as_float(r[q + 3])), b4.w, p3);
+                if (LSE) {
+                    p0 += ex2_approx(__uint_as_float(r[q + 0]) + b4.x);
+                    p1 += ex2_approx(__uint_as_float(r[q + 1]) + b4.y);
+                    p2 += ex2_approx(__uint_as_float(r[q + 2]) + b4.z);
+                    p3 += ex2_approx(__uint_as_float(r[q + 3]) + b4.w);
+                } else {
+                    p0 = fmaf(ex2_approx(__uint_as_float(r[q + 0])), b4.x, p0);
+                    p1 = fmaf(ex2_approx(__uint_as_float(r[q + 1])), b4.y, p1);
+                    p2 = fmaf(ex2_approx(__uint_as_float(r[q + 2])), b4.z, p2);
+                    p3 = fmaf(ex2_approx(__uint_as_float(r[q + 3])), b4.w, p3);
+                }
             }
-            two_sum_add(hi, lo, (p0 + p1) + (p2 + p3));
+            const float pt = (p0 + p1) + (p2 + p3);
+            if (!LSE) {
+                two_sum_add(hi, lo, pt);
+            } else if (pt > 0.f) {  // fold the tile (frame F) into the running (m, hi, lo)
+                const float F = __ldg(p.fpad + j_begin / kCols + i);
+                const float mn = fmaxf(m, F);
+                const float so = ex2_approx(m - mn), sn = ex2_approx(F - mn);
+                hi *= so;
+                lo *= so;
+                two_sum_add(hi, lo, pt * sn);
+                m = mn;
+            }
         }
     }
 
     __syncthreads();
     const bool ok = !*abort;
     if (!ok && t == 0) atomicExch(p.status, 1);
-    // warps 6..9 hand their row sums to warps 2..5 through the (now idle) A tile
+    // warps 6..9 hand their row sums (and LSE frames) to warps 2..5 through the idle A tile
     float *red = reinterpret_cast<float *>(smem);
     if (w >= 6) {
         red[32 * (w & 3) + lane] = hi;
         red[kRows + 32 * (w & 3) + lane] = lo;
+        red[2 * kRows + 32 * (w & 3) + lane] = m;
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
@@ -342,20 +391,50 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_sum_kernel(const __grid_cons
 
     if (w >= 2 && w < 6) {
         const int rl = 32 * (w & 3) + lane;
-        two_sum_add(hi, lo, red[rl]);
-        lo += red[kRows + rl];
+        float h2 = red[rl], l2 = red[kRows + rl];
+        if (LSE) {  // bring both halves to the larger frame
+            const float m2 = red[2 * kRows + rl], mn = fmaxf(m, m2);
+            const float s1 = mn == -__int_as_float(0x7f800000) ? 0.f : ex2_approx(m - mn);
+            const float s2 = mn == -__int_as_float(0x7f800000) ? 0.f : ex2_approx(m2 - mn);
+            hi *= s1;
+            lo *= s1;
+            h2 *= s2;
+            l2 *= s2;
+            m = mn;
+        }
+        two_sum_add(hi, lo, h2);
+        lo += l2;
         const int64_t i = row0 + rl;
         if (i < p.M) {
             const float nan = __int_as_float(0x7fc00000);
-            if (p.S == 1) {
-                p.out[i] = ok ? hi + lo : nan;
+            const int64_t o = (int64_t)blockIdx.y * p.M + i;
+            if (!LSE) {
+                if (p.S == 1) {
+                    p.out[i] = ok ? hi + lo : nan;
+                } else {
+                    p.ws0[o] = ok ? hi : nan;
+                    p.ws1[o] = ok ? lo : 0.f;
+                }
             } else {
-                const int64_t o = (int64_t)blockIdx.y * p.M + i;
-                p.ws0[o] = ok ? hi : nan;
-                p.ws1[o] = ok ? lo : 0.f;
+                // the CUDA-core LogSumExp's output and partials: L = ln 2 (m + log2 tot); (m, tot)
+                const float tot = hi + lo;
+                const float ninf = -__int_as_float(0x7f800000);
+                if (p.S == 1) {
+                    p.out[i] = !ok ? nan : tot > 0.f ? (float)(0.6931471805599453 * ((double)m + log2((double)tot))) : ninf;
+                } else {
+                    p.ws0[o] = !ok ? nan : tot > 0.f ? m : ninf;
+                    p.ws1[o] = ok ? tot : 0.f;
+                }
             }
         }
     }
+}
+
+__global__ void __launch_bounds__(kThreadsTc, 1) tc_sum_kernel(const __grid_constant__ TcParams p) {
+    tc_body<false>(p);
+}
+__global__ void __launch_bounds__(kThreadsTc, 1) tc_lse_kernel(const __grid_constant__ TcParams p) {
+    tc_body<true>(p);
 }
 
 // Host: cuTensorMapEncodeTiled through the runtime's driver entry point (no link
@@ -395,10 +474,28 @@ bool make_map(CUtensorMap *m, const __half *base, int64_t rows, int box_rows) {
 
 int tc_smem_bytes() { return kSmemBytes; }
 
+// Opt both tensor-core kernels in to kSmemBytes of dynamic shared memory, once per device.
+cudaError_t tc_set_attributes() {
+    static std::mutex mu;
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(tc_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tc_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    return e;
+}
+
 cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x, __half *hi,
-                           __half *lo, unsigned *guard, const float *b, float *bpad, cudaStream_t s) {
+                           __half *lo, unsigned *guard, const float *b, float *bpad, float *fpad, cudaStream_t s) {
+    // LSE frames: a prep block of 256 threads is one whole tile of kTcCols = 256 points
+    if (fpad && rows_pad % 256) return cudaErrorInvalidValue;
     const unsigned blocks = (unsigned)((rows_pad + 255) / 256);
-    tc_prep_kernel<<<blocks, 256, 0, s>>>(src, rows, rows_pad, D, c, is_x ? 1 : 0, hi, lo, guard, b, bpad);
+    tc_prep_kernel<<<blocks, 256, 0, s>>>(src, rows, rows_pad, D, c, is_x ? 1 : 0, hi, lo, guard, b, bpad, fpad);
     return cudaGetLastError();
 }
 
@@ -409,6 +506,7 @@ cudaError_t tc_launch_sum(const TcArgs &a, dim3 grid, cudaStream_t s) {
         !make_map(&p.tm_b_hi, a.b_hi, a.n_pad, kCols) || !make_map(&p.tm_b_lo, a.b_lo, a.n_pad, kCols))
         return cudaErrorInvalidValue;
     p.bpad = a.bpad;
+    p.fpad = a.fpad;
     p.out = a.out;
     p.ws0 = a.ws0;
     p.ws1 = a.ws1;
@@ -418,22 +516,18 @@ cudaError_t tc_launch_sum(const TcArgs &a, dim3 grid, cudaStream_t s) {
     p.N = a.N;
     p.chunk = a.chunk;
     p.S = a.S;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
-    tc_sum_kernel<<<grid, kThreadsTc, kSmemBytes, s>>>(p);
+    cudaError_t e = tc_set_attributes();
+    if (e != cudaSuccess) return e;
+    if (a.lse)
+        tc_lse_kernel<<<grid, kThreadsTc, kSmemBytes, s>>>(p);
+    else
+        tc_sum_kernel<<<grid, kThreadsTc, kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
 
 int tc_occupancy() {
     int n = 0;
-    if (cudaFuncSetAttribute(tc_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
-        return 0;
+    if (tc_set_attributes() != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_sum_kernel, kThreadsTc, kSmemBytes) != cudaSuccess)
         return 0;
     return n;

@@ -1,4 +1,4 @@
-// kr_tc.h -- the tensor-core path of the Gaussian Sum (see kr_tc.cu).
+// kr_tc.h -- the tensor-core path of the Gaussian Sum and LogSumExp (see kr_tc.cu).
 #pragma once
 
 #include <cuda.h>
@@ -14,7 +14,9 @@ namespace kr {
 struct TcArgs {
     const __half *a_hi, *a_lo;  // m_pad x 64 augmented x operands (split fp16), m_pad % kTcRows == 0
     const __half *b_hi, *b_lo;  // n_pad x 64 augmented y operands, n_pad % kTcCols == 0
-    const float *bpad;          // n_pad signal values (zero past N), 16-byte aligned
+    const float *bpad;          // Sum: n_pad signal values (zero past N); LSE: log2 e w - tile frame
+                                // (-inf past N); 16-byte aligned
+    const float *fpad;          // LSE: n_pad / kTcCols tile frames (base 2); Sum: unused
     float *out;                 // S == 1: M outputs
     float *ws0, *ws1;           // S > 1: S x M (hi, lo) partials, as the CUDA-core Sum writes them
     const unsigned *guard;      // [0] max |x'|^2, [1] max |y'|^2 (float bits), written by the prepass
@@ -22,12 +24,13 @@ struct TcArgs {
     int64_t M, N, m_pad, n_pad;
     int64_t chunk;              // points per split, a multiple of kTcCols
     int S;
+    bool lse;                   // LogSumExp (CUDA-core LSE partials) instead of the Sum
 };
 
 // Kernel parameters: TMA descriptors of the four operand arrays plus the rest.
 struct TcParams {
     CUtensorMap tm_a_hi, tm_a_lo, tm_b_hi, tm_b_lo;
-    const float *bpad;
+    const float *bpad, *fpad;
     float *out, *ws0, *ws1;
     const unsigned *guard;
     int *status;
@@ -38,8 +41,13 @@ struct TcParams {
 int tc_smem_bytes();
 int tc_occupancy();
 bool tc_available();  // the driver offers cuTensorMapEncodeTiled
+// Operand prepass.  fpad non-null (B operands of the LogSumExp): b holds the log-weights,
+// bpad receives them relative to each tile's frame and fpad the frames.
 cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x,
-                           __half *hi, __half *lo, unsigned *guard, const float *b, float *bpad, cudaStream_t s);
+                           __half *hi, __half *lo, unsigned *guard, const float *b, float *bpad, float *fpad,
+                           cudaStream_t s);
+// Opts the tensor-core kernels in to their dynamic shared memory on the current device.
+cudaError_t tc_set_attributes();
 cudaError_t tc_launch_sum(const TcArgs &a, dim3 grid, cudaStream_t s);
 
 }  // namespace kr

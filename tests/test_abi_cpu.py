@@ -238,7 +238,7 @@ def test_instance_choice(lib):
     assert (p.d_pad, p.ek_pad, p.threads) == (3, 1, 128)
     assert kr.plan(kr.OP_SUM, 10, 10, 5, 2).d_pad == 8 and kr.plan(kr.OP_SUM, 10, 10, 5, 2).ek_pad == 4
     assert kr.plan(kr.OP_SUM, 10, 10, 50, 1, path=kr.KR_PATH_CUDA_CORES).d_pad == 50
-    assert kr.plan(kr.OP_LSE, 10, 10, 50, 1).d_pad == 50
+    assert kr.plan(kr.OP_LSE, 10, 10, 50, 1, path=kr.KR_PATH_CUDA_CORES).d_pad == 50
     assert kr.plan(kr.OP_SUM, 10, 10, 51, 16).d_pad == 64
     assert kr.plan(kr.OP_KNN, 10, 10, 16, 10).ek_pad == 10
     assert kr.plan(kr.OP_KNN, 10, 10, 16, 11).ek_pad == 16
@@ -295,10 +295,15 @@ def test_tensor_core_plan(lib):
     assert p.chunk * 256 <= 48 << 20
     assert kr.plan(kr.OP_SUM, M, 1_000_000, 50, 1, num_sms=152, blocks_per_sm=1).chunk * 256 <= 48 << 20
     n_pad = (N + 255) // 256 * 256
-    ops = ((M + 127) // 128 * 128 + n_pad) * 256 + 4 * n_pad
+    frames = (n_pad // 256 * 4 + 255) // 256 * 256          # LSE tile frames
+    ops = ((M + 127) // 128 * 128 + n_pad) * 256 + 4 * n_pad + frames
     assert p.workspace_bytes == 256 + ops + (2 * p.split * M * 4 if p.split > 1 else 0)
+    # the LogSumExp takes the tensor cores under the same conditions, with the same plan
+    q = kr.plan(kr.OP_LSE, M, N, 50, 1, num_sms=152, blocks_per_sm=1)
+    assert q.path == kr.KR_PATH_TENSOR_CORES and (q.split, q.chunk, q.workspace_bytes) == (p.split, p.chunk,
+                                                                                            p.workspace_bytes)
     for shape in [(kr.OP_SUM, 10, 10, 31, 1), (kr.OP_SUM, 10, 10, 63, 1), (kr.OP_SUM, 10, 10, 50, 2),
-                  (kr.OP_LSE, 10, 10, 50, 1), (kr.OP_GRAD, 10, 10, 50, 1)]:
+                  (kr.OP_LSE, 10, 10, 50, 2), (kr.OP_GRAD, 10, 10, 50, 1), (kr.OP_MAX, 10, 10, 50, 1)]:
         assert kr.plan(*shape).path == kr.KR_PATH_CUDA_CORES, shape
     assert kr.plan(kr.OP_SUM, 10, 10, 50, 1, path=kr.KR_PATH_CUDA_CORES).path == kr.KR_PATH_CUDA_CORES
     assert kr.plan(kr.OP_SUM, 10, 2560, 50, 1, split=5).split == 5

@@ -255,6 +255,11 @@ def test_workload_falkon_d50(orc):
     rows = W.row_subset(inp["x"].shape[0], 1000, 9)
     a_ref, S_ref = orc.gauss_sum(inp["x"][rows], inp["y"], inp["b"], s)
     check_sum(a[rows], a_ref, S_ref, "falkon_d50")
+    # the LogSumExp of the same product (b as log-weights) on the tensor cores too
+    assert kr.plan_device(kr.OP_LSE, inp["x"].shape[0], inp["y"].shape[0], 50, 1).path == kr.KR_PATH_TENSOR_CORES
+    L = _np(kr.kernel_reduce(xt, yt, bt, s, "lse"))
+    rows = W.row_subset(inp["x"].shape[0], 256, 10)
+    check_lse(L[rows], orc.gauss_lse(inp["x"][rows], inp["y"], inp["b"], s), "falkon_d50 lse")
 
 
 def test_workload_knn_d16(orc):
@@ -289,6 +294,35 @@ def test_tensor_core_sum(orc, M, N, D, sigma, split):
     check_sum(_np(a), a_ref, S_ref, f"tc {M}x{N} D{D} S{split}")
 
 
+@pytest.mark.parametrize("M,N,D,sigma,split", TC_CASES)
+def test_tensor_core_lse(orc, M, N, D, sigma, split):
+    """The LogSumExp on the tensor cores (tile frames from the weights' maximum), with
+    weights spread over many orders of magnitude and some -inf (weight 0)."""
+    r = _rng(M + 3 * N + D)
+    x = (r.standard_normal((M, D)) / np.sqrt(D)).astype(np.float32)
+    y = (r.standard_normal((N, D)) / np.sqrt(D)).astype(np.float32)
+    w = (4.0 * r.standard_normal((N, 1))).astype(np.float32)
+    w[r.random((N, 1)) < 0.05] = -np.inf
+    assert kr.plan_device(kr.OP_LSE, M, N, D, 1).path == kr.KR_PATH_TENSOR_CORES
+    L = kr.kernel_reduce(*_dev(x, y, w), sigma, "lse", split=split, path=kr.KR_PATH_TENSOR_CORES)
+    check_lse(_np(L), orc.gauss_lse(x, y, w, sigma), f"tc lse {M}x{N} D{D} S{split}")
+
+
+def test_tensor_core_lse_empty_weights_and_guard(orc):
+    """All weights -inf gives -inf; large norms stand the tensor kernel down."""
+    r = _rng(78)
+    x = (r.standard_normal((300, 40)) / 6).astype(np.float32)
+    y = (r.standard_normal((900, 40)) / 6).astype(np.float32)
+    w = np.full((900, 1), -np.inf, np.float32)
+    L = _np(kr.kernel_reduce(*_dev(x, y, w), 1.0, "lse", path=kr.KR_PATH_TENSOR_CORES))
+    assert np.isneginf(L).all()
+    x = (3.0 * r.standard_normal((200, 50))).astype(np.float32)
+    y = (x[r.integers(0, 200, 700)] + 0.3 * r.standard_normal((700, 50))).astype(np.float32)
+    w = r.standard_normal((700, 1)).astype(np.float32)
+    L = kr.kernel_reduce(*_dev(x, y, w), 2.0, "lse", path=kr.KR_PATH_TENSOR_CORES)
+    check_lse(_np(L), orc.gauss_lse(x, y, w, 2.0), "lse norm guard")
+
+
 def test_tensor_core_norm_guard_falls_back(orc):
     """Points far from the origin in units of sigma: the expansion would lose the
     tolerance, so the tensor kernel stands down and the CUDA-core kernel answers."""
@@ -309,3 +343,7 @@ def test_tensor_and_cuda_core_paths_agree():
     S = _np(kr.kernel_reduce(xt, yt, bt.abs(), 1.0, "sum", path=kr.KR_PATH_CUDA_CORES))
     assert (np.abs(a_tc - a_cc) <= 1e-4 * S).all()
     assert np.array_equal(a_tc, _np(kr.kernel_reduce(xt, yt, bt, 1.0, "sum", path=kr.KR_PATH_TENSOR_CORES)))
+    L_tc = _np(kr.kernel_reduce(xt, yt, bt, 1.0, "lse", path=kr.KR_PATH_TENSOR_CORES))
+    L_cc = _np(kr.kernel_reduce(xt, yt, bt, 1.0, "lse", path=kr.KR_PATH_CUDA_CORES))
+    assert (np.abs(L_tc - L_cc) <= 2e-4).all()
+    assert np.array_equal(L_tc, _np(kr.kernel_reduce(xt, yt, bt, 1.0, "lse", path=kr.KR_PATH_TENSOR_CORES)))
