@@ -183,7 +183,7 @@ def probe_pipes(torch, nsm):
             "ex2_to_ffma": ms[0] / ms[2], "ffma_lanes_per_s": nsm * bps * 256 * iters * 8 / (ms[0] / 1e3)}
 
 
-# Tensor-core Sum (E = 1, 32 <= D <= 62): per pair, three fp16 products (hi.hi, hi.lo,
+# Tensor-core Sum and LSE (E = 1, 32 <= D <= 62): per pair, three fp16 products (hi.hi, hi.lo,
 # lo.hi) of the K = 64 augmented vectors, 2 FLOP per multiply-add.
 TC_FLOP_PER_PAIR = 3 * 2 * 64
 
