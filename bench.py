@@ -236,6 +236,25 @@ def roofline(op, D, E, seconds_per_launch, pairs, nsm, clk_mhz, xu_lanes, kernel
 
 
 # ---------------------------------------------------------------------------
+# replicas: every rank runs its own problem; the job is as slow as its slowest rank
+# ---------------------------------------------------------------------------
+def slowest_rank(ms: float, world: int) -> float:
+    """The largest of the ranks' times (all-reduce MAX over the process group)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(pairs_per_step: float, ms_per_step: float, world: int) -> float:
+    """Whole-job pair-evaluations per second: every rank does a step's pairs."""
+    return world * pairs_per_step / (ms_per_step / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 def run_ours(args, rank, world, local_rank):
@@ -306,14 +325,9 @@ def run_ours(args, rank, world, local_rank):
     step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(args.steps)]
     op_ms = {name: float(np.mean([ev[k][o].elapsed_time(ev[k][o + 1]) for k in range(args.steps)]))
              for o, (name, _) in enumerate(ops)}
-    total_ms = float(np.sum(step_ms))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank(float(np.sum(step_ms)), world)
     ms_per_step = total_ms / args.steps
-    value = world * pairs_per_step / (ms_per_step / 1e3)
+    value = job_value(pairs_per_step, ms_per_step, world)
     clocks = clk.summary()
 
     e2e_line = e2e(torch, kr, inp, s, args, world)
@@ -379,11 +393,7 @@ def e2e(torch, kr, inp, s, args, world):
     t0 = time.perf_counter()
     for _ in range(steps):
         step()
-    t = (time.perf_counter() - t0) / steps
-    if world > 1:
-        tt = torch.tensor([t], dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t = float(tt.item())
+    t = slowest_rank((time.perf_counter() - t0) / steps, world)
     return {"value": world * 4 * M * N / t, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": t * 1e3, "steps": steps, "timer": "host perf_counter; each call blocks on host outputs"}
 
@@ -558,7 +568,8 @@ def run_reference(args, rank, world):
     inp = W.generate(args.workload, M=args.size[0], N=args.size[1]) if args.size else W.generate(args.workload)
     s = inp["sigma"]
     N = inp["y"].shape[0]
-    per_step = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    # each step samples about a fifth of --cpu-seconds (3 s by default), fewer when many steps
+    per_step = max(0.05, min(args.cpu_seconds / 5.0, 150.0 / max(1, args.steps + args.warmup)))
     r = _oracle_rows_for(orc, inp, s, per_step)
     rows = np.arange(r)
     for _ in range(args.warmup):
