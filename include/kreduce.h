@@ -275,6 +275,19 @@ const char *kr_status_string(int status);
 int kr_last_cuda_error(void);
 
 /*
+ * Sticky device status of the calling thread's current device (no counterpart on the
+ * pages; failure detection of this build).  Every wait of the tensor-core kernels on
+ * their mbarriers is bounded (2 s of global time by default); a block whose wait gives
+ * up writes NaN for its rows and sets bit 0 of this status.  Reads the status into
+ * *status (0 = nothing happened since the last clear) and clears it when `clear` is
+ * nonzero.  Synchronous: waits for the device's work.  Test hooks read at each call:
+ * KREDUCE_TC_WAIT_MS overrides the wait bound; KREDUCE_TC_STARVE=1 makes the
+ * tensor-core kernel withhold its B tiles, so its waits run out (the context stays
+ * usable, the next call works normally).
+ */
+int kr_device_status(unsigned *status, int clear);
+
+/*
  * Launch plan, exposed so that the host logic can be inspected without a GPU.
  * op: 0 = Sum, 1 = LogSumExp, 2 = grad-x, 3 = K-min, 4 = Max / Min; EK = E (ops 0-2, 4)
  * or K (op 3).  opt->kernel selects the radial kernel of ops 0 and 4.

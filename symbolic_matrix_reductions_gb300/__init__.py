@@ -44,8 +44,8 @@ EXPORTS = ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_arg", "kernel_red
            "kernel_reduce_ranges", "kernel_reduce_noalloc", "kernel_reduce_grad_x",
            "kernel_reduce_grad_x_ex", "kernel_reduce_grad_y", "kernel_reduce_grad_y_ex",
            "kernel_reduce_grad_b", "kernel_reduce_grad_b_ex",
-           "kernel_knn", "kernel_knn_ex", "kr_status_string", "kr_last_cuda_error", "kr_plan",
-           "kr_plan_device")
+           "kernel_knn", "kernel_knn_ex", "kr_status_string", "kr_last_cuda_error", "kr_device_status",
+           "kr_plan", "kr_plan_device")
 
 
 class KrError(RuntimeError):
@@ -110,6 +110,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kr_status_string.argtypes = [i32]
         lib.kr_status_string.restype = ctypes.c_char_p
         lib.kr_last_cuda_error.argtypes = []
+        lib.kr_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         lib.kr_plan.argtypes = [i32, i64, i64, i32, i32, i32, i32, opt, ctypes.POINTER(KrPlan)]
         lib.kr_plan_device.argtypes = [i32, i64, i64, i32, i32, opt, ctypes.POINTER(KrPlan)]
         for name in EXPORTS:
@@ -130,6 +131,14 @@ def _check(status: int, what: str) -> None:
     if status != KR_OK:
         cuda_err = load_library().kr_last_cuda_error() if status == KR_ERR_CUDA else 0
         raise KrError(status, what, cuda_err)
+
+
+def device_status(clear: bool = False) -> int:
+    """The sticky device status of the current device (bit 0: a tensor-core wait gave
+    up and its rows came out NaN); waits for the device's work."""
+    v = ctypes.c_uint(0)
+    _check(load_library().kr_device_status(ctypes.byref(v), 1 if clear else 0), "kr_device_status")
+    return int(v.value)
 
 
 def _kernel_code(kernel) -> int:

@@ -434,7 +434,14 @@ static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in
         t.ws0 = a.ws0;
         t.ws1 = a.ws1;
         t.guard = guard;
-        t.status = (int *)(guard + 2);
+        // Every mbarrier wait of the tensor kernel gives up after this long (2 s unless
+        // KREDUCE_TC_WAIT_MS says otherwise).  KREDUCE_TC_STARVE=1 withholds the B tiles so
+        // that a test can watch the waits run out and the status report it.
+        const char *wms = std::getenv("KREDUCE_TC_WAIT_MS");
+        const long ms = wms ? std::strtol(wms, nullptr, 10) : 2000;
+        t.wait_ns = (uint64_t)(ms > 0 ? ms : 2000) * 1000000ull;
+        const char *starve = std::getenv("KREDUCE_TC_STARVE");
+        t.starve = starve && starve[0] == '1';
         t.M = a.M;
         t.N = a.N;
         t.chunk = p.chunk;
@@ -860,6 +867,14 @@ const char *kr_status_string(int status) {
 }
 
 int kr_last_cuda_error(void) { return g_last_cuda_error; }
+
+int kr_device_status(unsigned *status, int clear) {
+    if (!status) return KR_ERR_INVALID;
+    *status = 0;
+    if (!tc_available()) return KR_OK;  // no tensor-core kernel can have run
+    const cudaError_t e = tc_read_status(clear != 0, status);
+    return e == cudaSuccess ? KR_OK : cuda_fail(e);
+}
 
 int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm, const kr_options *opt,
             kr_plan_t *out) {

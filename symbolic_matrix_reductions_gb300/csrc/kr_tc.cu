@@ -36,10 +36,11 @@
 //     half in one TMEM load, releases the accumulator (the MMAs of tile i+2 may then
 //     overwrite it), computes 2^t and accumulates b_j 2^t, with b_j read through
 //     the L1 cache.
-// Every mbarrier wait is bounded; a role that gives up raises a block-wide abort
-// flag, records an error, and every role then leaves its loop; the producer and the
-// MMA issuer then wait (bounded) for their copies and MMAs in flight, and the
-// block's rows come out as NaN.
+// Every mbarrier wait is bounded (by global time, default 2 s, and a poll count); a
+// role that gives up raises a block-wide abort flag, and every role then leaves its
+// loop; the producer and the MMA issuer then wait (bounded) for their copies and MMAs
+// in flight, the block's rows come out as NaN, and bit 0 of a sticky device status
+// word is set, which kr_device_status() reads and clears.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -108,19 +109,36 @@ __device__ __forceinline__ void commit(uint32_t mbar) {
                  : "memory");
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Bounded wait for the completion of the phase with the given parity.  Gives up
-// after kWaitLimit polls, or early when another role raised `abort`.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volatile int *abort) {
+// (raising `abort`) after `limit_ns` of global time or kWaitLimit polls, whichever
+// comes first, or early when another role raised `abort`.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volatile int *abort, uint64_t limit_ns) {
+    uint64_t t0 = 0;
     for (long it = 0; it < kWaitLimit; ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(done)
-            : "r"(mbar), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((it & 255) == 255 && *abort) return false;
+        if (mbar_try(mbar, parity)) return true;
+        if ((it & 255) == 255) {
+            if (*abort) return false;
+            const uint64_t now = global_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > limit_ns) break;
+        }
     }
     *abort = 1;
     return false;
@@ -128,19 +146,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volati
 
 // Bounded wait that ignores `abort`: used after an abort, to let this block's own
 // copies and MMAs in flight land before the block releases its memory.
-__device__ __forceinline__ bool mbar_drain(uint32_t mbar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_drain(uint32_t mbar, uint32_t parity, uint64_t limit_ns) {
+    uint64_t t0 = 0;
     for (long it = 0; it < kWaitLimit; ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(done)
-            : "r"(mbar), "r"(parity)
-            : "memory");
-        if (done) return true;
+        if (mbar_try(mbar, parity)) return true;
+        if ((it & 255) == 255) {
+            const uint64_t now = global_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > limit_ns) break;
+        }
     }
     return false;
 }
+
+// Sticky device-side status of the tensor-core kernels: bit 0 = a bounded wait gave up
+// (the rows of that block came out NaN).  Read and cleared by tc_read_status().
+__device__ unsigned int g_tc_status;
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t mbar) {
     asm volatile(
@@ -285,28 +306,29 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
             int issued = 0;
             for (int i = 0; i < T; ++i) {
                 const int s = i % kStages;
-                if (i >= kStages && !mbar_wait(b_empty0 + 8 * s, ((i / kStages) - 1) & 1, abort)) break;
+                if (i >= kStages && !mbar_wait(b_empty0 + 8 * s, ((i / kStages) - 1) & 1, abort, p.wait_ns)) break;
                 const int j0 = (int)(j_begin + (int64_t)i * kCols);
                 const uint32_t st = s_stage0 + s * kStageBytes, full = b_full0 + 8 * s;
+                if (p.starve) continue;  // test hook: no B tile ever arrives, so the MMA issuer's wait runs out
                 mbar_expect_tx(full, kStageBytes);
                 tma_2d(st, &p.tm_b_hi, 0, j0, full);
                 tma_2d(st + kBTileBytes, &p.tm_b_lo, 0, j0, full);
                 issued = i + 1;
             }
             if (*abort) {  // let the copies in flight land before shared memory is released
-                mbar_drain(b_a_full, 0);
+                mbar_drain(b_a_full, 0, p.wait_ns);
                 for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-                    mbar_drain(b_full0 + 8 * (i % kStages), (i / kStages) & 1);
+                    mbar_drain(b_full0 + 8 * (i % kStages), (i / kStages) & 1, p.wait_ns);
             }
         }
     } else if (w == 1) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0 && T > 0 && mbar_wait(b_a_full, 0, abort)) {
+        if (lane == 0 && T > 0 && mbar_wait(b_a_full, 0, abort, p.wait_ns)) {
             bool issued = false;
             for (int i = 0; i < T; ++i) {
                 const int s = i % kStages, k = i & 1;
-                if (!mbar_wait(b_full0 + 8 * s, (i / kStages) & 1, abort)) break;
-                if (i >= 2 && !mbar_wait(b_acce0 + 8 * k, ((i >> 1) - 1) & 1, abort)) break;
+                if (!mbar_wait(b_full0 + 8 * s, (i / kStages) & 1, abort, p.wait_ns)) break;
+                if (i >= 2 && !mbar_wait(b_acce0 + 8 * k, ((i >> 1) - 1) & 1, abort, p.wait_ns)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;");
                 const uint32_t acc = tmem + (uint32_t)(k * kCols);
                 const uint32_t bh = s_stage0 + s * kStageBytes, bl = bh + kBTileBytes;
@@ -324,7 +346,7 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
             }
             if (*abort && issued) {  // let the MMAs in flight finish before TMEM is released
                 commit(b_drain);
-                mbar_drain(b_drain, 0);
+                mbar_drain(b_drain, 0, p.wait_ns);
             }
         }
     } else {
@@ -333,7 +355,7 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
         const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
         for (int i = 0; i < T; ++i) {
             const int k = i & 1;
-            if (!mbar_wait(b_accf0 + 8 * k, (i >> 1) & 1, abort)) break;
+            if (!mbar_wait(b_accf0 + 8 * k, (i >> 1) & 1, abort, p.wait_ns)) break;
             asm volatile("tcgen05.fence::after_thread_sync;");
             uint32_t r[kEvalCols];
             tmem_ld128(tmem + lanes + (uint32_t)(k * kCols + c0), r);  // one load, one wait
@@ -377,7 +399,7 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
 
     __syncthreads();
     const bool ok = !*abort;
-    if (!ok && t == 0) atomicExch(p.status, 1);
+    if (!ok && t == 0) atomicOr(&g_tc_status, 1u);
     // warps 6..9 hand their row sums (and LSE frames) to warps 2..5 through the idle A tile
     float *red = reinterpret_cast<float *>(smem);
     if (w >= 6) {
@@ -511,7 +533,8 @@ cudaError_t tc_launch_sum(const TcArgs &a, dim3 grid, cudaStream_t s) {
     p.ws0 = a.ws0;
     p.ws1 = a.ws1;
     p.guard = a.guard;
-    p.status = a.status;
+    p.wait_ns = a.wait_ns;
+    p.starve = a.starve ? 1 : 0;
     p.M = a.M;
     p.N = a.N;
     p.chunk = a.chunk;
@@ -534,5 +557,14 @@ int tc_occupancy() {
 }
 
 bool tc_available() { return encode_fn() != nullptr; }
+
+cudaError_t tc_read_status(bool clear, unsigned *status) {
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_tc_status, sizeof(unsigned));
+    if (e == cudaSuccess && clear) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(unsigned));
+    }
+    return e;
+}
 
 }  // namespace kr

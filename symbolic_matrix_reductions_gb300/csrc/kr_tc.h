@@ -20,7 +20,8 @@ struct TcArgs {
     float *out;                 // S == 1: M outputs
     float *ws0, *ws1;           // S > 1: S x M (hi, lo) partials, as the CUDA-core Sum writes them
     const unsigned *guard;      // [0] max |x'|^2, [1] max |y'|^2 (float bits), written by the prepass
-    int *status;                // set to 1 when a bounded wait gave up
+    uint64_t wait_ns;           // bound of every mbarrier wait (global time)
+    bool starve;                // test hook: issue no B tile, so the waits run out
     int64_t M, N, m_pad, n_pad;
     int64_t chunk;              // points per split, a multiple of kTcCols
     int S;
@@ -33,7 +34,8 @@ struct TcParams {
     const float *bpad, *fpad;
     float *out, *ws0, *ws1;
     const unsigned *guard;
-    int *status;
+    uint64_t wait_ns;
+    int starve;
     int64_t M, N, chunk;
     int S;
 };
@@ -49,5 +51,8 @@ cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int
 // Opts the tensor-core kernels in to their dynamic shared memory on the current device.
 cudaError_t tc_set_attributes();
 cudaError_t tc_launch_sum(const TcArgs &a, dim3 grid, cudaStream_t s);
+// Reads (and optionally clears) the sticky device status of the tensor-core kernels on the
+// current device: bit 0 = a bounded wait gave up.  Synchronous.
+cudaError_t tc_read_status(bool clear, unsigned *status);
 
 }  // namespace kr

@@ -37,6 +37,17 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_device_status_without_a_device(lib):
+    v = ctypes.c_uint(7)
+    assert lib.kr_device_status(None, 0) == kr.KR_ERR_INVALID
+    if not lib.kernel_reduce:  # pragma: no cover
+        return
+    import torch
+    if not torch.cuda.is_available():
+        # no driver entry point here: no tensor-core kernel can have run
+        assert lib.kr_device_status(ctypes.byref(v), 1) == kr.KR_OK and v.value == 0
+
+
 def test_status_strings(lib):
     texts = {lib.kr_status_string(s).decode() for s in range(5)}
     assert len(texts) == 5

@@ -323,6 +323,31 @@ def test_tensor_core_lse_empty_weights_and_guard(orc):
     check_lse(_np(L), orc.gauss_lse(x, y, w, 2.0), "lse norm guard")
 
 
+def test_tensor_core_wait_bound_reports_status(orc):
+    """Failure detection without a fault: with the B tiles withheld (test hook) every
+    bounded mbarrier wait of the tensor kernel runs out after 50 ms; the rows come out
+    NaN, the sticky device status says so, and the context stays usable."""
+    r = _rng(79)
+    x = (r.standard_normal((300, 50)) / np.sqrt(50)).astype(np.float32)
+    y = (r.standard_normal((1000, 50)) / np.sqrt(50)).astype(np.float32)
+    b = r.standard_normal((1000, 1)).astype(np.float32)
+    xt, yt, bt = _dev(x, y, b)
+    kr.device_status(clear=True)
+    os.environ["KREDUCE_TC_STARVE"] = "1"
+    os.environ["KREDUCE_TC_WAIT_MS"] = "50"
+    try:
+        a = _np(kr.kernel_reduce(xt, yt, bt, 1.0, "sum", path=kr.KR_PATH_TENSOR_CORES))
+    finally:
+        del os.environ["KREDUCE_TC_STARVE"], os.environ["KREDUCE_TC_WAIT_MS"]
+    assert np.isnan(a).all()
+    assert kr.device_status(clear=True) & 1
+    assert kr.device_status() == 0
+    a = kr.kernel_reduce(xt, yt, bt, 1.0, "sum", path=kr.KR_PATH_TENSOR_CORES)
+    a_ref, S_ref = orc.gauss_sum(x, y, b, 1.0)
+    check_sum(_np(a), a_ref, S_ref, "after a run-out wait")
+    assert kr.device_status() == 0
+
+
 def test_tensor_core_norm_guard_falls_back(orc):
     """Points far from the origin in units of sigma: the expansion would lose the
     tolerance, so the tensor kernel stands down and the CUDA-core kernel answers."""
