@@ -59,6 +59,10 @@ constexpr int kTcThreads = 320;
 // Coordinate range of the tensor-core Sum (the augmented vector must fit K = 64).
 KR_HD constexpr bool tc_dims(int D, int E) { return E == 1 && D >= 32 && D <= 62; }
 
+// Independent partial sums of a squared distance: at large D one fma chain over the
+// coordinates is a long dependency chain (4 cycles a link) with few rows per thread to
+// hide it, so the sum is split into this many interleaved chains, added at the end.
+KR_HD constexpr int dist_chains(int DP) { return DP >= 32 ? 4 : DP >= 16 ? 2 : 1; }
 // Inner-loop unroll over tile points (tiles are padded to a multiple of it).
 KR_HD constexpr int unroll_points(int DP) { return DP <= 8 ? 4 : DP <= 32 ? 2 : 1; }
 

@@ -226,12 +226,18 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const Args a_) {
                 load_record<PS>(tile + (jj + u) * PS, pv);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    float q = (LSE && EP == 1) ? pv[DP] : 0.f;
+                    constexpr int NC = dist_chains(DP);
+                    float qc[NC];
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) qc[c] = (c == 0 && LSE && EP == 1) ? pv[DP] : 0.f;
 #pragma unroll
                     for (int d = 0; d < DP; ++d) {
                         const float df = xr[r][d] - pv[d];
-                        q = fmaf(df, df, q);
+                        qc[d % NC] = fmaf(df, df, qc[d % NC]);
                     }
+                    float q = qc[0];
+#pragma unroll
+                    for (int c = 1; c < NC; ++c) q += qc[c];
                     if (!LSE) {
                         const float k = ex2_approx(-q);
 #pragma unroll
@@ -419,13 +425,19 @@ __global__ void __launch_bounds__(kThreads) grad_kernel(const Args a_) {
                 load_record<PS>(tile + (jj + u) * PS, pv);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
+                    constexpr int NC = dist_chains(DP);
                     float df[DP];
-                    float q = 0.f;
+                    float qc[NC];
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) qc[c] = 0.f;
 #pragma unroll
                     for (int d = 0; d < DP; ++d) {
                         df[d] = xr[r][d] - pv[d];
-                        q = fmaf(df[d], df[d], q);
+                        qc[d % NC] = fmaf(df[d], df[d], qc[d % NC]);
                     }
+                    float q = qc[0];
+#pragma unroll
+                    for (int c = 1; c < NC; ++c) q += qc[c];
                     float beta;
                     if (EP == 1) {
                         beta = pv[DP];
@@ -534,12 +546,18 @@ __global__ void __launch_bounds__(kThreads) knn_kernel(const Args a_) {
                 const int j = (int)(jt + jj + u);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    float q = 0.f;
+                    constexpr int NC = dist_chains(DP);  // interleaved partial sums
+                    float qc[NC];
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) qc[c] = 0.f;
 #pragma unroll
                     for (int d = 0; d < DP; ++d) {
                         const float df = xr[r][d] - pv[d];
-                        q = fmaf(df, df, q);
+                        qc[d % NC] = fmaf(df, df, qc[d % NC]);
                     }
+                    float q = qc[0];
+#pragma unroll
+                    for (int c = 1; c < NC; ++c) q += qc[c];
                     if (q < dk[r][KP - 1]) knn_insert<KP>(dk[r], ik[r], q, j);
                 }
             }

@@ -81,12 +81,20 @@ __device__ __forceinline__ void zero_pad_coords_pairs(const Args &a, float *tile
 template <int DP, int PS2>
 __device__ __forceinline__ float2 sq_dist_pair(const float2 (&x2)[DP], const float2 (&pv)[PS2 / 2], float2 q0,
                                                bool start_from_q0) {
-    float2 q = q0;
+    constexpr int NC = dist_chains(DP);  // interleaved partial sums (see kr_config.h)
+    float2 qc[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) qc[c] = q0;
 #pragma unroll
     for (int d = 0; d < DP; ++d) {
         const float2 df = __fadd2_rn(x2[d], pv[d]);
-        q = (d == 0 && !start_from_q0) ? __fmul2_rn(df, df) : __ffma2_rn(df, df, q);
+        const int c = d % NC;
+        const bool first = d < NC && !(c == 0 && start_from_q0);
+        qc[c] = first ? __fmul2_rn(df, df) : __ffma2_rn(df, df, qc[c]);
     }
+    float2 q = qc[0];
+#pragma unroll
+    for (int c = 1; c < NC; ++c) q = __fadd2_rn(q, qc[c]);
     return q;
 }
 

@@ -208,12 +208,20 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
                 radial_load<L, PS>(tile + (jj / L + u) * PS, pv);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    T q = V::splat(radial_q0<KT>());
+                    constexpr int NC = dist_chains(DP);  // interleaved partial sums
+                    T qc[NC];
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) qc[c] = V::splat(c == 0 ? radial_q0<KT>() : 0.f);
 #pragma unroll
                     for (int d = 0; d < DP; ++d) {
                         const T df = V::add(xr[r][d], pv[d]);
-                        q = (d == 0 && radial_q0<KT>() == 0.f) ? V::mul(df, df) : V::fma(df, df, q);
+                        const int c = d % NC;
+                        const bool first = d < NC && !(c == 0 && radial_q0<KT>() != 0.f);
+                        qc[c] = first ? V::mul(df, df) : V::fma(df, df, qc[c]);
                     }
+                    T q = qc[0];
+#pragma unroll
+                    for (int c = 1; c < NC; ++c) q = V::add(q, qc[c]);
                     const T k = V::template kval<KT>(q);
 #pragma unroll
                     for (int e = 0; e < EP; ++e) {
