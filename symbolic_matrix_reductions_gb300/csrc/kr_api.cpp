@@ -44,9 +44,11 @@ Instance choose_instance(int op, int D, int EK) {
         in.tile = instance_tile(in.d_pad, 0);
     } else {
         in.ek_pad = pad_e(EK);
-        in.rows = (op == OP_GRAD) ? rows_grad(in.d_pad, in.ek_pad) : rows_fwd(in.d_pad, in.ek_pad);
-        in.tile = (op == OP_GRAD && !packed_grad(in.d_pad)) ? tile_points(pack_stride(in.d_pad, in.ek_pad))
-                                                            : instance_tile(in.d_pad, in.ek_pad);
+        in.rows = (op == OP_GRAD) ? (wide_grad(in.d_pad) ? 1 : rows_grad(in.d_pad, in.ek_pad))
+                                  : rows_fwd(in.d_pad, in.ek_pad);
+        in.tile = (op == OP_GRAD && wide_grad(in.d_pad))    ? kWideGradTile
+                  : (op == OP_GRAD && !packed_grad(in.d_pad)) ? tile_points(pack_stride(in.d_pad, in.ek_pad))
+                                                              : instance_tile(in.d_pad, in.ek_pad);
     }
     return in;
 }

@@ -71,6 +71,13 @@ KR_HD constexpr int unroll_points(int DP) { return DP <= 8 ? 4 : DP <= 32 ? 2 : 
 KR_HD constexpr bool packed(int DP) { return DP <= 64; }
 // The packed gradient also keeps 2 R D partial sums in registers: up to D = 16.
 KR_HD constexpr bool packed_grad(int DP) { return DP <= 16; }
+// Wide gradient (32 <= D <= 64): one row per thread with x, the differences and the
+// tile's partial sums in registers (3 D floats) and the compensated running sums in
+// shared memory, so the block needs no more than ~170 registers a thread.
+KR_HD constexpr bool wide_grad(int DP) { return DP >= 32 && DP <= 64; }
+// Points per tile of the wide gradient (the tile and the running sums share the
+// block's dynamic shared memory).
+constexpr int kWideGradTile = 64;
 // Pair record: points 2m and 2m+1 of a tile interleaved field by field, so one
 // 16-byte load yields two float2 operands; rounded up to whole float4s.
 KR_HD constexpr int pair_stride(int DP, int VP) { return (2 * (DP + VP) + 3) / 4 * 4; }

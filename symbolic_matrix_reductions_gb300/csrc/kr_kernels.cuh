@@ -587,6 +587,118 @@ __global__ void __launch_bounds__(kThreads) knn_kernel(const Args a_) {
 }
 
 // ---------------------------------------------------------------------------
+// x-gradient for wide points (32 <= D <= 64).  The same sums as grad_kernel, one row
+// per thread, but the compensated running sums (hi, lo) of the D coordinates live in
+// dynamic shared memory, laid out [coordinate][hi|lo][thread] so every access of a
+// warp is to consecutive words; each thread folds its tile partials into its own
+// slots, so no barrier is needed for them.  Registers hold x (D), the differences of
+// the current pair (D) and the tile partials (D).  Dynamic shared memory:
+// BN * PS + 2 * DP * kThreads floats.
+// ---------------------------------------------------------------------------
+template <int DP, int EP, int BN>
+__global__ void __launch_bounds__(kThreads) gradw_kernel(const Args a_) {
+    const Args a = batch_view(a_);
+    constexpr int PS = pack_stride(DP, EP);
+    extern __shared__ __align__(16) float wsm[];
+    float *tile = wsm;
+    float *acc = wsm + BN * PS;  // acc[(2 d + 0|1) kThreads + t] = hi | lo of coordinate d
+
+    const int t = threadIdx.x;
+    const int64_t i = (int64_t)blockIdx.x * kThreads + t;
+    const int64_t j_begin = (int64_t)blockIdx.y * a.chunk;
+    const int64_t j_end = min(a.N, j_begin + a.chunk);
+
+    zero_pad_coords<DP, PS, BN>(a, tile);
+    float xr[DP];
+#pragma unroll
+    for (int d = 0; d < DP; ++d) xr[d] = (i < a.M && d < a.D) ? a.c * __ldg(a.x + i * a.D + d) : 0.f;
+    float gr[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) gr[e] = (i < a.M && e < a.E) ? __ldg(a.g + i * a.E + e) : 0.f;
+    float part[DP];
+#pragma unroll
+    for (int d = 0; d < DP; ++d) {
+        part[d] = 0.f;
+        acc[(2 * d) * kThreads + t] = 0.f;
+        acc[(2 * d + 1) * kThreads + t] = 0.f;
+    }
+
+    for (int64_t jt = j_begin; jt < j_end; jt += BN) {
+        const int nv = (int)min((int64_t)BN, j_end - jt);
+        __syncthreads();
+        stage_coords<DP, PS>(a, tile, jt, nv, nv, a.c, 0.f);
+        for (int p = t; p < nv; p += kThreads) {
+#pragma unroll
+            for (int e = 0; e < EP; ++e) tile[p * PS + DP + e] = e < a.E ? __ldg(a.b + (jt + p) * a.E + e) : 0.f;
+        }
+        __syncthreads();
+
+        for (int jj = 0; jj < nv; ++jj) {
+            const float4 *rec = reinterpret_cast<const float4 *>(tile + jj * PS);
+            constexpr int NC = dist_chains(DP);
+            float df[DP];
+            float qc[NC];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) qc[c] = 0.f;
+#pragma unroll
+            for (int k = 0; k < DP / 4; ++k) {  // the record in 16-byte pieces, used at once
+                const float4 v = rec[k];
+                const float yv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int d = 4 * k + u;
+                    df[d] = xr[d] - yv[u];
+                    qc[d % NC] = fmaf(df[d], df[d], qc[d % NC]);
+                }
+            }
+#pragma unroll
+            for (int d = DP / 4 * 4; d < DP; ++d) {  // the coordinates past the last whole piece
+                df[d] = xr[d] - tile[jj * PS + d];
+                qc[d % NC] = fmaf(df[d], df[d], qc[d % NC]);
+            }
+            float q = qc[0];
+#pragma unroll
+            for (int c = 1; c < NC; ++c) q += qc[c];
+            float beta;
+            if (EP == 1) {
+                beta = tile[jj * PS + DP];
+            } else {
+                beta = 0.f;
+#pragma unroll
+                for (int e = 0; e < EP; ++e) beta = fmaf(gr[e], tile[jj * PS + DP + e], beta);
+            }
+            const float kb = ex2_approx(-q) * beta;
+#pragma unroll
+            for (int d = 0; d < DP; ++d) part[d] = fmaf(kb, df[d], part[d]);
+        }
+#pragma unroll
+        for (int d = 0; d < DP; ++d) {  // fold the tile into this thread's own slots
+            float h = acc[(2 * d) * kThreads + t], l = acc[(2 * d + 1) * kThreads + t];
+            two_sum_add(h, l, part[d]);
+            acc[(2 * d) * kThreads + t] = h;
+            acc[(2 * d + 1) * kThreads + t] = l;
+            part[d] = 0.f;
+        }
+    }
+
+    if (i >= a.M) return;
+    const float sc = (EP == 1) ? a.gscale * gr[0] : a.gscale;
+#pragma unroll
+    for (int d = 0; d < DP; ++d) {
+        if (d >= a.D) continue;
+        const float h = acc[(2 * d) * kThreads + t], l = acc[(2 * d + 1) * kThreads + t];
+        const int64_t o = i * a.D + d;
+        if (a.S == 1) {
+            a.out[o] = (h + l) * sc;
+        } else {
+            const int64_t w = (int64_t)blockIdx.y * a.M * a.D + o;
+            a.ws0[w] = h * sc;
+            a.ws1[w] = l * sc;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Split-j combines: one thread per output element, partials visited in
 // increasing split order, so the result does not depend on scheduling.
 // ---------------------------------------------------------------------------
