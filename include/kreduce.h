@@ -288,6 +288,16 @@ int kr_last_cuda_error(void);
 int kr_device_status(unsigned *status, int clear);
 
 /*
+ * 1 for a debug build of the library (compiled with -DKR_DEBUG, libkreduce_debug.so),
+ * else 0.  In a debug build every global-memory access of the CUDA-core kernels checks
+ * its element index against the array's extent; a violation skips the access and sets a
+ * bit (x 1, y 2, b 4, g 8, out 16, idx 32, split partials 64, shared memory 128) that
+ * kr_device_status reports shifted left by 8.  (Test infrastructure for index arithmetic;
+ * no counterpart on the pages.)
+ */
+int kr_debug_build(void);
+
+/*
  * Launch plan, exposed so that the host logic can be inspected without a GPU.
  * op: 0 = Sum, 1 = LogSumExp, 2 = grad-x, 3 = K-min, 4 = Max / Min; EK = E (ops 0-2, 4)
  * or K (op 3).  opt->kernel selects the radial kernel of ops 0 and 4.

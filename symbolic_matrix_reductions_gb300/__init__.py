@@ -45,7 +45,7 @@ EXPORTS = ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_arg", "kernel_red
            "kernel_reduce_grad_x_ex", "kernel_reduce_grad_y", "kernel_reduce_grad_y_ex",
            "kernel_reduce_grad_b", "kernel_reduce_grad_b_ex",
            "kernel_knn", "kernel_knn_ex", "kr_status_string", "kr_last_cuda_error", "kr_device_status",
-           "kr_plan", "kr_plan_device")
+           "kr_debug_build", "kr_plan", "kr_plan_device")
 
 
 class KrError(RuntimeError):
@@ -89,35 +89,48 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             raise RuntimeError(
                 f"libkreduce.so not found at {path}; build it with "
                 "`python -m symbolic_matrix_reductions_gb300.build` (there is no CPU fallback)")
-        lib = ctypes.CDLL(path)
-        vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
-        opt = ctypes.POINTER(KrOptions)
-        lib.kernel_reduce.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
-        lib.kernel_reduce_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp, opt]
-        lib.kernel_reduce_arg.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
-        lib.kernel_reduce_arg_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp, opt]
-        lib.kernel_reduce_ranges.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, i64, vp, vp, i64, vp,
-                                             vp, opt]
-        lib.kernel_reduce_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
-        lib.kernel_reduce_grad_x.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
-        lib.kernel_reduce_grad_x_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
-        lib.kernel_reduce_grad_y.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
-        lib.kernel_reduce_grad_y_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
-        lib.kernel_reduce_grad_b.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
-        lib.kernel_reduce_grad_b_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
-        lib.kernel_knn.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp]
-        lib.kernel_knn_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp, opt]
-        lib.kr_status_string.argtypes = [i32]
-        lib.kr_status_string.restype = ctypes.c_char_p
-        lib.kr_last_cuda_error.argtypes = []
-        lib.kr_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
-        lib.kr_plan.argtypes = [i32, i64, i64, i32, i32, i32, i32, opt, ctypes.POINTER(KrPlan)]
-        lib.kr_plan_device.argtypes = [i32, i64, i64, i32, i32, opt, ctypes.POINTER(KrPlan)]
-        for name in EXPORTS:
-            if name != "kr_status_string":
-                getattr(lib, name).restype = ctypes.c_int
-        _lib = lib
-        return lib
+        _lib = _configure(ctypes.CDLL(path))
+        return _lib
+
+
+def load_debug_library() -> ctypes.CDLL:
+    """Builds (if needed) and loads libkreduce_debug.so, the variant whose kernels check
+    every global element index (test infrastructure; see kr_debug_build in the header).
+    It is a separate handle: the module's functions keep using the release library."""
+    from . import build
+    return _configure(ctypes.CDLL(build.build_debug()))
+
+
+def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declares the C signatures on a loaded library."""
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    opt = ctypes.POINTER(KrOptions)
+    lib.kernel_reduce.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
+    lib.kernel_reduce_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp, opt]
+    lib.kernel_reduce_arg.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
+    lib.kernel_reduce_arg_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp, opt]
+    lib.kernel_reduce_ranges.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, i64, vp, vp, i64, vp,
+                                         vp, opt]
+    lib.kernel_reduce_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp]
+    lib.kernel_reduce_grad_x.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
+    lib.kernel_reduce_grad_x_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
+    lib.kernel_reduce_grad_y.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
+    lib.kernel_reduce_grad_y_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
+    lib.kernel_reduce_grad_b.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, vp]
+    lib.kernel_reduce_grad_b_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, f32, vp, opt]
+    lib.kernel_knn.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp]
+    lib.kernel_knn_ex.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp, opt]
+    lib.kr_status_string.argtypes = [i32]
+    lib.kr_status_string.restype = ctypes.c_char_p
+    lib.kr_last_cuda_error.argtypes = []
+    lib.kr_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+    lib.kr_debug_build.argtypes = []
+    lib.kr_plan.argtypes = [i32, i64, i64, i32, i32, i32, i32, opt, ctypes.POINTER(KrPlan)]
+    lib.kr_plan_device.argtypes = [i32, i64, i64, i32, i32, opt, ctypes.POINTER(KrPlan)]
+    for name in EXPORTS:
+        if name != "kr_status_string":
+            getattr(lib, name).restype = ctypes.c_int
+    return lib
 
 
 def _status_text(status: int) -> str:

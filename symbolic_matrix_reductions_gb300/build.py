@@ -19,6 +19,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkreduce.so")
+# Debug variant (-DKR_DEBUG): the kernels check every global element index against its
+# array's extent and report violations through kr_device_status; built only on request.
+OBJ_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libkreduce_debug.so")
 PROBE_LIB = os.path.join(HERE, "libkrprobe.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
@@ -49,6 +53,32 @@ def up_to_date() -> bool:
         return False
     t = min(os.path.getmtime(LIB), os.path.getmtime(PROBE_LIB))
     return all(os.path.getmtime(f) <= t for f in _deps())
+
+
+def build_debug(force: bool = False) -> str:
+    """Compile and link the debug variant libkreduce_debug.so; returns its path."""
+    if not force and os.path.exists(LIB_DEBUG) and all(os.path.getmtime(f) <= os.path.getmtime(LIB_DEBUG)
+                                                       for f in _deps()):
+        return LIB_DEBUG
+    nvcc = _nvcc()
+    os.makedirs(OBJ_DEBUG, exist_ok=True)
+
+    def compile_one(src):
+        obj = os.path.join(OBJ_DEBUG, os.path.splitext(src)[0] + ".o")
+        cmd = [nvcc, *NVCC_FLAGS, "-DKR_DEBUG", "-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src} (debug):\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = LIB_DEBUG + ".tmp"
+    r = subprocess.run([nvcc, "-shared", *ARCH, "-cudart", "static", "-o", tmp, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed (debug):\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB_DEBUG)
+    return LIB_DEBUG
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:

@@ -207,6 +207,7 @@ struct DeviceCache {
     int tc_occ = 0;           // resident tensor-core Sum blocks; 0 = not queried
     cudaMemPool_t pool = nullptr;  // the library's workspace pool on this device
     bool pool_tried = false;
+    unsigned *dbg = nullptr;       // debug builds: the index-check status word
 };
 std::mutex g_cache_mutex;
 DeviceCache g_cache[64];
@@ -288,6 +289,22 @@ cudaMemPool_t device_pool(int dev) {
         }
     }
     return c.pool;
+}
+
+// Debug builds (-DKR_DEBUG): the device word the kernels' index checks write to, one
+// per device for the life of the process.  Release builds never allocate it.
+unsigned *debug_word(int dev) {
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_cache_mutex);
+    DeviceCache &c = g_cache[dev];
+    if (!c.dbg) {
+        unsigned *p = nullptr;
+        if (cudaMalloc((void **)&p, sizeof(unsigned)) == cudaSuccess && cudaMemset(p, 0, sizeof(unsigned)) == cudaSuccess)
+            c.dbg = p;
+        else
+            cudaGetLastError();
+    }
+    return c.dbg;
 }
 
 int device_tc_occupancy(int dev) {
@@ -515,6 +532,15 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
             p.workspace_bytes = (rt->bytes() + 255) / 256 * 256 +
                                 (p.split > 1 ? workspace_bytes(op, in, a.M, a.D, EK, p.split) : 0);
         }
+    }
+    {  // element counts of one problem's outputs and partials (index checks of debug builds)
+        const int64_t w_out = op == OP_GRAD ? a.D : op == OP_KNN ? a.K : a.E;
+        a.out_n = a.M * w_out;
+        a.idx_n = a.M * (op == OP_KNN ? a.K : a.E);
+        a.ws_n = (int64_t)p.split * a.M * (op == OP_GRAD ? a.D : op == OP_KNN ? p.ek_pad : a.E);
+#ifdef KR_DEBUG
+        a.dbg = debug_word(dev);
+#endif
     }
     if (B > 1) {
         const int64_t w_out = op == OP_GRAD ? a.D : op == OP_KNN ? a.K : a.E;
@@ -873,9 +899,28 @@ int kr_last_cuda_error(void) { return g_last_cuda_error; }
 int kr_device_status(unsigned *status, int clear) {
     if (!status) return KR_ERR_INVALID;
     *status = 0;
-    if (!tc_available()) return KR_OK;  // no tensor-core kernel can have run
-    const cudaError_t e = tc_read_status(clear != 0, status);
+    if (!tc_available()) return KR_OK;  // no device work can have run
+    cudaError_t e = tc_read_status(clear != 0, status);
+#ifdef KR_DEBUG
+    int dev = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    unsigned *w = e == cudaSuccess ? debug_word(dev) : nullptr;
+    if (w) {
+        unsigned v = 0;
+        e = cudaMemcpy(&v, w, sizeof(unsigned), cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess && clear) e = cudaMemset(w, 0, sizeof(unsigned));
+        *status |= v << 8;
+    }
+#endif
     return e == cudaSuccess ? KR_OK : cuda_fail(e);
+}
+
+int kr_debug_build(void) {
+#ifdef KR_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm, const kr_options *opt,

@@ -9,8 +9,8 @@ __global__ void combine_sum_kernel(const Args a_, int W) {
     const int64_t total = a.M * W;
     if (o >= total) return;
     double acc = 0.0;
-    for (int s = 0; s < a.S; ++s) acc += (double)a.ws0[s * total + o] + (double)a.ws1[s * total + o];
-    a.out[o] = (float)acc;
+    for (int s = 0; s < a.S; ++s) acc += (double)ldg_chk(a, a.ws0, s * total + o, a.ws_n, KRD_WS) + (double)ldg_chk(a, a.ws1, s * total + o, a.ws_n, KRD_WS);
+    st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)acc);
 }
 
 __global__ void combine_lse_kernel(const Args a_) {
@@ -19,17 +19,17 @@ __global__ void combine_lse_kernel(const Args a_) {
     const int64_t total = a.M * a.E;
     if (o >= total) return;
     float mmax = -f_inf();
-    for (int s = 0; s < a.S; ++s) mmax = fmaxf(mmax, a.ws0[s * total + o]);
+    for (int s = 0; s < a.S; ++s) mmax = fmaxf(mmax, ldg_chk(a, a.ws0, s * total + o, a.ws_n, KRD_WS));
     if (mmax == -f_inf()) {
-        a.out[o] = -f_inf();
+        st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)(-f_inf()));
         return;
     }
     double acc = 0.0;
     for (int s = 0; s < a.S; ++s) {
-        const float acc_s = a.ws1[s * total + o];
-        if (acc_s > 0.f) acc += (double)acc_s * exp2((double)a.ws0[s * total + o] - (double)mmax);
+        const float acc_s = ldg_chk(a, a.ws1, s * total + o, a.ws_n, KRD_WS);
+        if (acc_s > 0.f) acc += (double)acc_s * exp2((double)ldg_chk(a, a.ws0, s * total + o, a.ws_n, KRD_WS) - (double)mmax);
     }
-    a.out[o] = (float)(0.6931471805599453 * ((double)mmax + log2(acc)));
+    st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)(0.6931471805599453 * ((double)mmax + log2(acc))));
 }
 
 __global__ void combine_knn_kernel(const Args a_, int KP) {
@@ -45,9 +45,9 @@ __global__ void combine_knn_kernel(const Args a_, int KP) {
         for (int s = 0; s < a.S; ++s) {
             if (head[s] >= KP) continue;
             const int64_t w = ((int64_t)s * a.M + i) * KP + head[s];
-            const int j = a.wsi[w];
+            const int j = ldg_chk(a, (const int32_t *)a.wsi, w, a.ws_n, KRD_WS);
             if (j < 0) continue;  // empty slot: ranks after every real pair
-            const float d = a.ws0[w];
+            const float d = ldg_chk(a, a.ws0, w, a.ws_n, KRD_WS);
             if (best < 0 || d < bd || (d == bd && j < bj)) {
                 best = s;
                 bd = d;
@@ -55,11 +55,11 @@ __global__ void combine_knn_kernel(const Args a_, int KP) {
             }
         }
         if (best < 0) {
-            a.idx[i * a.K + k] = -1;
-            if (a.out) a.out[i * a.K + k] = f_inf();
+            st_chk(a, a.idx, i * a.K + k, a.idx_n, KRD_IDX, (int32_t)(-1));
+            if (a.out) st_chk(a, a.out, i * a.K + k, a.out_n, KRD_OUT, (float)(f_inf()));
         } else {
-            a.idx[i * a.K + k] = bj;
-            if (a.out) a.out[i * a.K + k] = bd;
+            st_chk(a, a.idx, i * a.K + k, a.idx_n, KRD_IDX, (int32_t)(bj));
+            if (a.out) st_chk(a, a.out, i * a.K + k, a.out_n, KRD_OUT, (float)(bd));
             ++head[best];
         }
     }
@@ -73,8 +73,8 @@ __global__ void combine_max_kernel(const Args a_) {
     float best = -f_inf();
     int bj = -1;
     for (int s = 0; s < a.S; ++s) {
-        const float v = a.ws0[s * total + o];
-        const int j = a.wsi[s * total + o];
+        const float v = ldg_chk(a, a.ws0, s * total + o, a.ws_n, KRD_WS);
+        const int j = ldg_chk(a, (const int32_t *)a.wsi, s * total + o, a.ws_n, KRD_WS);
         // larger value, or the same value at a lower index (block-sparse splits need
         // not hold increasing j; dense splits do, so there this keeps the earlier split)
         if (v > best || (v == best && j >= 0 && (bj < 0 || j < bj))) {
@@ -82,8 +82,8 @@ __global__ void combine_max_kernel(const Args a_) {
             bj = j;
         }
     }
-    if (a.out) a.out[o] = a.vsign * best;
-    if (a.idx) a.idx[o] = bj;
+    if (a.out) st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)(a.vsign * best));
+    if (a.idx) st_chk(a, a.idx, o, a.idx_n, KRD_IDX, (int32_t)(bj));
 }
 
 cudaError_t launch_combine(int op, const Instance &inst, const Args &a, cudaStream_t s) {

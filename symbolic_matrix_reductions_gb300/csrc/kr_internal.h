@@ -47,6 +47,15 @@ struct Args {
     // reduces over the column ranges rng[blk[b].z .. blk[b].w-1]; null otherwise.
     const int4 *blk;
     const int2 *rng;
+    // Element counts of the outputs and split partials of one problem, for the index
+    // checks of debug builds (-DKR_DEBUG), which record a violated bound in *dbg.
+    int64_t out_n, idx_n, ws_n;
+    unsigned *dbg;
+};
+
+// Bits of the debug status word (debug builds; kr_device_status reports them << 8).
+enum DebugBits : unsigned {
+    KRD_X = 1u, KRD_Y = 2u, KRD_B = 4u, KRD_G = 8u, KRD_OUT = 16u, KRD_IDX = 32u, KRD_WS = 64u, KRD_SMEM = 128u
 };
 
 // Compile-time shape of one kernel instance, chosen by the planner.

@@ -40,6 +40,42 @@ __device__ __forceinline__ float lg2_approx(float v) {
 
 __device__ __forceinline__ float f_inf() { return __int_as_float(0x7f800000); }
 
+// Checked global accesses.  Release builds compile them to the plain access; debug
+// builds (-DKR_DEBUG) first check the element index against the array's extent and, on
+// a violation, set the array's bit in the status word a.dbg and skip the access (a load
+// then returns 0), so a wrong index shows up as a status instead of a fault.
+template <typename T>
+__device__ __forceinline__ T ldg_chk(const Args &a, const T *p, int64_t k, int64_t n, unsigned bit) {
+#ifdef KR_DEBUG
+    if (k < 0 || k >= n) {
+        if (a.dbg) atomicOr(a.dbg, bit);
+        return T(0);
+    }
+#endif
+    return __ldg(p + k);
+}
+template <typename T>
+__device__ __forceinline__ void st_chk(const Args &a, T *p, int64_t k, int64_t n, unsigned bit, T v) {
+#ifdef KR_DEBUG
+    if (k < 0 || k >= n) {
+        if (a.dbg) atomicOr(a.dbg, bit);
+        return;
+    }
+#endif
+    p[k] = v;
+}
+// Shared-memory index check (debug builds): false, and KRD_SMEM recorded, when k is
+// outside [0, n).
+__device__ __forceinline__ bool smem_ok(const Args &a, int64_t k, int64_t n) {
+#ifdef KR_DEBUG
+    if (k < 0 || k >= n) {
+        if (a.dbg) atomicOr(a.dbg, (unsigned)KRD_SMEM);
+        return false;
+    }
+#endif
+    return true;
+}
+
 // The arguments of this block's problem: with a batch dimension (grid z), every
 // array pointer moves to problem blockIdx.z.  Uniform across the block.
 __device__ __forceinline__ Args batch_view(const Args &a) {
@@ -91,7 +127,7 @@ __device__ __forceinline__ void load_rows(const Args &a, int64_t row0, float (&x
         const int64_t i = row0 + (int64_t)r * kThreads + threadIdx.x;
 #pragma unroll
         for (int d = 0; d < DP; ++d)
-            xr[r][d] = (i < a.M && d < a.D) ? scale * __ldg(a.x + i * a.D + d) : 0.f;
+            xr[r][d] = (i < a.M && d < a.D) ? scale * ldg_chk(a, a.x, i * a.D + d, a.M * a.D, KRD_X) : 0.f;
     }
 }
 
@@ -107,7 +143,7 @@ __device__ __forceinline__ void stage_coords(const Args &a, float *tile, int64_t
             const float *src = a.y + (jt + p) * a.D;
 #pragma unroll
             for (int d = 0; d < DP; ++d)
-                if (d < a.D) dst[d] = scale * __ldg(src + d);
+                if (d < a.D) dst[d] = scale * ldg_chk(a, a.y, (jt + p) * a.D + d, a.N * a.D, KRD_Y);
         } else {
 #pragma unroll
             for (int d = 0; d < DP; ++d)
@@ -181,7 +217,7 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const Args a_) {
             for (int p = t; p < nvp; p += kThreads) {
 #pragma unroll
                 for (int e = 0; e < EP; ++e)
-                    tile[p * PS + DP + e] = (p < nv && e < a.E) ? __ldg(a.b + (jt + p) * a.E + e) : 0.f;
+                    tile[p * PS + DP + e] = (p < nv && e < a.E) ? ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : 0.f;
             }
         } else {
             float lmax[EP];
@@ -190,7 +226,7 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const Args a_) {
             for (int p = t; p < nvp; p += kThreads) {
 #pragma unroll
                 for (int e = 0; e < EP; ++e) {
-                    const float v = (p < nv && e < a.E) ? kLog2e * __ldg(a.b + (jt + p) * a.E + e) : -f_inf();
+                    const float v = (p < nv && e < a.E) ? kLog2e * ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : -f_inf();
                     tile[p * PS + DP + e] = v;
                     lmax[e] = fmaxf(lmax[e], v);
                 }
@@ -350,21 +386,21 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const Args a_) {
             const int64_t o = i * a.E + e;
             if (!LSE) {
                 if (a.S == 1) {
-                    a.out[o] = hi[r][e] + lo[r][e];
+                    st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)(hi[r][e] + lo[r][e]));
                 } else {
                     const int64_t w = (int64_t)blockIdx.y * a.M * a.E + o;
-                    a.ws0[w] = hi[r][e];
-                    a.ws1[w] = lo[r][e];
+                    st_chk(a, a.ws0, w, a.ws_n, KRD_WS, (float)(hi[r][e]));
+                    st_chk(a, a.ws1, w, a.ws_n, KRD_WS, (float)(lo[r][e]));
                 }
             } else {
                 const float tot = hi[r][e] + lo[r][e];
                 if (a.S == 1) {
-                    a.out[o] = tot > 0.f ? (float)(0.6931471805599453 * ((double)m[r][e] + log2((double)tot)))
-                                         : -f_inf();
+                    st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)(tot > 0.f ? (float)(0.6931471805599453 * ((double)m[r][e] + log2((double)tot)))
+                                         : -f_inf()));
                 } else {
                     const int64_t w = (int64_t)blockIdx.y * a.M * a.E + o;
-                    a.ws0[w] = tot > 0.f ? m[r][e] : -f_inf();
-                    a.ws1[w] = tot;
+                    st_chk(a, a.ws0, w, a.ws_n, KRD_WS, (float)(tot > 0.f ? m[r][e] : -f_inf()));
+                    st_chk(a, a.ws1, w, a.ws_n, KRD_WS, (float)(tot));
                 }
             }
         }
@@ -398,7 +434,7 @@ __global__ void __launch_bounds__(kThreads) grad_kernel(const Args a_) {
     for (int r = 0; r < R; ++r) {
         const int64_t i = row0 + (int64_t)r * kThreads + t;
 #pragma unroll
-        for (int e = 0; e < EP; ++e) gr[r][e] = (i < a.M && e < a.E) ? __ldg(a.g + i * a.E + e) : 0.f;
+        for (int e = 0; e < EP; ++e) gr[r][e] = (i < a.M && e < a.E) ? ldg_chk(a, a.g, i * a.E + e, a.M * a.E, KRD_G) : 0.f;
     }
     float part[R][DP], hi[R][DP], lo[R][DP];
 #pragma unroll
@@ -414,7 +450,7 @@ __global__ void __launch_bounds__(kThreads) grad_kernel(const Args a_) {
         for (int p = t; p < nvp; p += kThreads) {
 #pragma unroll
             for (int e = 0; e < EP; ++e)
-                tile[p * PS + DP + e] = (p < nv && e < a.E) ? __ldg(a.b + (jt + p) * a.E + e) : 0.f;
+                tile[p * PS + DP + e] = (p < nv && e < a.E) ? ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : 0.f;
         }
         __syncthreads();
 
@@ -471,11 +507,11 @@ __global__ void __launch_bounds__(kThreads) grad_kernel(const Args a_) {
             if (d >= a.D) continue;
             const int64_t o = i * a.D + d;
             if (a.S == 1) {
-                a.out[o] = (hi[r][d] + lo[r][d]) * sc;
+                st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)((hi[r][d] + lo[r][d]) * sc));
             } else {
                 const int64_t w = (int64_t)blockIdx.y * a.M * a.D + o;
-                a.ws0[w] = hi[r][d] * sc;
-                a.ws1[w] = lo[r][d] * sc;
+                st_chk(a, a.ws0, w, a.ws_n, KRD_WS, (float)(hi[r][d] * sc));
+                st_chk(a, a.ws1, w, a.ws_n, KRD_WS, (float)(lo[r][d] * sc));
             }
         }
     }
@@ -572,15 +608,15 @@ __global__ void __launch_bounds__(kThreads) knn_kernel(const Args a_) {
 #pragma unroll
             for (int k = 0; k < KP; ++k) {
                 if (k >= a.K) continue;
-                a.idx[i * a.K + k] = ik[r][k];
-                if (a.out) a.out[i * a.K + k] = dk[r][k];
+                st_chk(a, a.idx, i * a.K + k, a.idx_n, KRD_IDX, (int32_t)(ik[r][k]));
+                if (a.out) st_chk(a, a.out, i * a.K + k, a.out_n, KRD_OUT, (float)(dk[r][k]));
             }
         } else {
             const int64_t w = ((int64_t)blockIdx.y * a.M + i) * KP;
 #pragma unroll
             for (int k = 0; k < KP; ++k) {
-                a.ws0[w + k] = dk[r][k];
-                a.wsi[w + k] = ik[r][k];
+                st_chk(a, a.ws0, w + k, a.ws_n, KRD_WS, (float)(dk[r][k]));
+                st_chk(a, a.wsi, w + k, a.ws_n, KRD_WS, (int32_t)(ik[r][k]));
             }
         }
     }
@@ -611,10 +647,10 @@ __global__ void __launch_bounds__(kThreads) gradw_kernel(const Args a_) {
     zero_pad_coords<DP, PS, BN>(a, tile);
     float xr[DP];
 #pragma unroll
-    for (int d = 0; d < DP; ++d) xr[d] = (i < a.M && d < a.D) ? a.c * __ldg(a.x + i * a.D + d) : 0.f;
+    for (int d = 0; d < DP; ++d) xr[d] = (i < a.M && d < a.D) ? a.c * ldg_chk(a, a.x, i * a.D + d, a.M * a.D, KRD_X) : 0.f;
     float gr[EP];
 #pragma unroll
-    for (int e = 0; e < EP; ++e) gr[e] = (i < a.M && e < a.E) ? __ldg(a.g + i * a.E + e) : 0.f;
+    for (int e = 0; e < EP; ++e) gr[e] = (i < a.M && e < a.E) ? ldg_chk(a, a.g, i * a.E + e, a.M * a.E, KRD_G) : 0.f;
     float part[DP];
 #pragma unroll
     for (int d = 0; d < DP; ++d) {
@@ -629,7 +665,7 @@ __global__ void __launch_bounds__(kThreads) gradw_kernel(const Args a_) {
         stage_coords<DP, PS>(a, tile, jt, nv, nv, a.c, 0.f);
         for (int p = t; p < nv; p += kThreads) {
 #pragma unroll
-            for (int e = 0; e < EP; ++e) tile[p * PS + DP + e] = e < a.E ? __ldg(a.b + (jt + p) * a.E + e) : 0.f;
+            for (int e = 0; e < EP; ++e) tile[p * PS + DP + e] = e < a.E ? ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : 0.f;
         }
         __syncthreads();
 
@@ -689,11 +725,11 @@ __global__ void __launch_bounds__(kThreads) gradw_kernel(const Args a_) {
         const float h = acc[(2 * d) * kThreads + t], l = acc[(2 * d + 1) * kThreads + t];
         const int64_t o = i * a.D + d;
         if (a.S == 1) {
-            a.out[o] = (h + l) * sc;
+            st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)((h + l) * sc));
         } else {
             const int64_t w = (int64_t)blockIdx.y * a.M * a.D + o;
-            a.ws0[w] = h * sc;
-            a.ws1[w] = l * sc;
+            st_chk(a, a.ws0, w, a.ws_n, KRD_WS, (float)(h * sc));
+            st_chk(a, a.ws1, w, a.ws_n, KRD_WS, (float)(l * sc));
         }
     }
 }

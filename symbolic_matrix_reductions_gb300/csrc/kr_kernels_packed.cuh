@@ -36,7 +36,7 @@ __device__ __forceinline__ void load_rows_pairs(const Args &a, int64_t row0, flo
         const int64_t i = row0 + (int64_t)r * kThreads + threadIdx.x;
 #pragma unroll
         for (int d = 0; d < DP; ++d) {
-            const float v = (i < a.M && d < a.D) ? scale * __ldg(a.x + i * a.D + d) : 0.f;
+            const float v = (i < a.M && d < a.D) ? scale * ldg_chk(a, a.x, i * a.D + d, a.M * a.D, KRD_X) : 0.f;
             x2[r][d] = make_float2(v, v);
         }
     }
@@ -58,7 +58,7 @@ __device__ __forceinline__ void stage_coords_pairs(const Args &a, float *tile, i
             const float *src = a.y + (jt + p) * a.D;
 #pragma unroll
             for (int d = 0; d < DP; ++d)
-                if (d < a.D) *pair_slot<PS2>(tile, p, d) = scale * __ldg(src + d);
+                if (d < a.D) *pair_slot<PS2>(tile, p, d) = scale * ldg_chk(a, a.y, (jt + p) * a.D + d, a.N * a.D, KRD_Y);
         } else {
 #pragma unroll
             for (int d = 0; d < DP; ++d)
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
             for (int p = t; p < nvp; p += kThreads) {
 #pragma unroll
                 for (int e = 0; e < EP; ++e)
-                    *pair_slot<PS2>(tile, p, DP + e) = (p < nv && e < a.E) ? __ldg(a.b + (jt + p) * a.E + e) : 0.f;
+                    *pair_slot<PS2>(tile, p, DP + e) = (p < nv && e < a.E) ? ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : 0.f;
             }
         } else {
             float lmax[EP];
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
             for (int p = t; p < nvp; p += kThreads) {
 #pragma unroll
                 for (int e = 0; e < EP; ++e) {
-                    const float v = (p < nv && e < a.E) ? kLog2e * __ldg(a.b + (jt + p) * a.E + e) : -f_inf();
+                    const float v = (p < nv && e < a.E) ? kLog2e * ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : -f_inf();
                     *pair_slot<PS2>(tile, p, DP + e) = v;
                     lmax[e] = fmaxf(lmax[e], v);
                 }
@@ -308,21 +308,21 @@ __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
             const int64_t o = i * a.E + e;
             if (!LSE) {
                 if (a.S == 1) {
-                    a.out[o] = hi[r][e] + lo[r][e];
+                    st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)(hi[r][e] + lo[r][e]));
                 } else {
                     const int64_t w = (int64_t)blockIdx.y * a.M * a.E + o;
-                    a.ws0[w] = hi[r][e];
-                    a.ws1[w] = lo[r][e];
+                    st_chk(a, a.ws0, w, a.ws_n, KRD_WS, (float)(hi[r][e]));
+                    st_chk(a, a.ws1, w, a.ws_n, KRD_WS, (float)(lo[r][e]));
                 }
             } else {
                 const float tot = hi[r][e] + lo[r][e];
                 if (a.S == 1) {
-                    a.out[o] = tot > 0.f ? (float)(0.6931471805599453 * ((double)m[r][e] + log2((double)tot)))
-                                         : -f_inf();
+                    st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)(tot > 0.f ? (float)(0.6931471805599453 * ((double)m[r][e] + log2((double)tot)))
+                                         : -f_inf()));
                 } else {
                     const int64_t w = (int64_t)blockIdx.y * a.M * a.E + o;
-                    a.ws0[w] = tot > 0.f ? m[r][e] : -f_inf();
-                    a.ws1[w] = tot;
+                    st_chk(a, a.ws0, w, a.ws_n, KRD_WS, (float)(tot > 0.f ? m[r][e] : -f_inf()));
+                    st_chk(a, a.ws1, w, a.ws_n, KRD_WS, (float)(tot));
                 }
             }
         }
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a_) {
         const int64_t i = row0 + (int64_t)r * kThreads + t;
 #pragma unroll
         for (int e = 0; e < EP; ++e) {
-            gr[r][e] = (i < a.M && e < a.E) ? __ldg(a.g + i * a.E + e) : 0.f;
+            gr[r][e] = (i < a.M && e < a.E) ? ldg_chk(a, a.g, i * a.E + e, a.M * a.E, KRD_G) : 0.f;
             g2[r][e] = make_float2(gr[r][e], gr[r][e]);
         }
     }
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a_) {
         for (int p = t; p < nvp; p += kThreads) {
 #pragma unroll
             for (int e = 0; e < EP; ++e)
-                *pair_slot<PS2>(tile, p, DP + e) = (p < nv && e < a.E) ? __ldg(a.b + (jt + p) * a.E + e) : 0.f;
+                *pair_slot<PS2>(tile, p, DP + e) = (p < nv && e < a.E) ? ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : 0.f;
         }
         __syncthreads();
 
@@ -429,11 +429,11 @@ __global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a_) {
             if (d >= a.D) continue;
             const int64_t o = i * a.D + d;
             if (a.S == 1) {
-                a.out[o] = (hi[r][d] + lo[r][d]) * sc;
+                st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)((hi[r][d] + lo[r][d]) * sc));
             } else {
                 const int64_t w = (int64_t)blockIdx.y * a.M * a.D + o;
-                a.ws0[w] = hi[r][d] * sc;
-                a.ws1[w] = lo[r][d] * sc;
+                st_chk(a, a.ws0, w, a.ws_n, KRD_WS, (float)(hi[r][d] * sc));
+                st_chk(a, a.ws1, w, a.ws_n, KRD_WS, (float)(lo[r][d] * sc));
             }
         }
     }
@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knn2_kernel(
                                 knn_insert<KP>(dk[r], ik[r], (c & 1) ? qq.y : qq.x, j0 + c);
                             }
                         } else {
-                            qbuf[(r * CB + nc[r]) * kThreads + t] = jj / UPT;
+                            if (smem_ok(a, nc[r], CB)) qbuf[(r * CB + nc[r]) * kThreads + t] = jj / UPT;
                             nmax = max(nmax, ++nc[r]);
                         }
                     }
@@ -603,15 +603,15 @@ __global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knn2_kernel(
 #pragma unroll
             for (int k = 0; k < KP; ++k) {
                 if (k >= a.K) continue;
-                a.idx[i * a.K + k] = ik[r][k];
-                if (a.out) a.out[i * a.K + k] = dk[r][k];
+                st_chk(a, a.idx, i * a.K + k, a.idx_n, KRD_IDX, (int32_t)(ik[r][k]));
+                if (a.out) st_chk(a, a.out, i * a.K + k, a.out_n, KRD_OUT, (float)(dk[r][k]));
             }
         } else {
             const int64_t w = ((int64_t)blockIdx.y * a.M + i) * KP;
 #pragma unroll
             for (int k = 0; k < KP; ++k) {
-                a.ws0[w + k] = dk[r][k];
-                a.wsi[w + k] = ik[r][k];
+                st_chk(a, a.ws0, w + k, a.ws_n, KRD_WS, (float)(dk[r][k]));
+                st_chk(a, a.wsi, w + k, a.ws_n, KRD_WS, (int32_t)(ik[r][k]));
             }
         }
     }

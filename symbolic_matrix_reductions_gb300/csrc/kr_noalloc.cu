@@ -120,6 +120,8 @@ extern "C" int kernel_reduce_noalloc(const float *x, const float *y, const float
     a.c = (float)(std::sqrt(1.4426950408889634) / (double)sigma);
     a.S = p.split;
     a.chunk = p.chunk;
+    a.out_n = M * E;
+    a.ws_n = (int64_t)p.split * M * E;
     if (p.split > 1) {
         a.ws0 = scratch;
         a.ws1 = scratch + (int64_t)p.split * M * E;

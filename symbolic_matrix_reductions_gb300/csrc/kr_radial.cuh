@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
     for (int r = 0; r < R; ++r) {
         const int64_t i = row0 + (int64_t)r * kThreads + t;
 #pragma unroll
-        for (int d = 0; d < DP; ++d) xr[r][d] = V::splat((i < row_end && d < a.D) ? a.c * __ldg(a.x + i * a.D + d) : 0.f);
+        for (int d = 0; d < DP; ++d) xr[r][d] = V::splat((i < row_end && d < a.D) ? a.c * ldg_chk(a, a.x, i * a.D + d, a.M * a.D, KRD_X) : 0.f);
     }
 
     T part[R][EP];
@@ -180,12 +180,12 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
                 const float *src = a.y + (jt + p) * a.D;
 #pragma unroll
                 for (int d = 0; d < DP; ++d)
-                    if (d < a.D) *radial_slot<L, PS>(tile, p, d) = -a.c * __ldg(src + d);
+                    if (d < a.D) *radial_slot<L, PS>(tile, p, d) = -a.c * ldg_chk(a, a.y, (jt + p) * a.D + d, a.N * a.D, KRD_Y);
 #pragma unroll
                 for (int e = 0; e < EP; ++e) {
                     float v = RED == RR_MAX ? nan : 0.f;
                     if (e < a.E) {
-                        v = __ldg(a.b + (jt + p) * a.E + e);
+                        v = ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B);
                         if (RED == RR_MAX) v *= a.vsign;
                     }
                     *radial_slot<L, PS>(tile, p, DP + e) = v;
@@ -278,18 +278,18 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
             const int64_t o = i * a.E + e;
             if (a.S == 1) {
                 if (RED == RR_SUM) {
-                    a.out[o] = hi[r][e] + lo[r][e];
+                    st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)(hi[r][e] + lo[r][e]));
                 } else {
-                    if (a.out) a.out[o] = a.vsign * hi[r][e];
-                    if (a.idx) a.idx[o] = bj[r][e];
+                    if (a.out) st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)(a.vsign * hi[r][e]));
+                    if (a.idx) st_chk(a, a.idx, o, a.idx_n, KRD_IDX, (int32_t)(bj[r][e]));
                 }
             } else {
                 const int64_t w = (int64_t)blockIdx.y * a.M * a.E + o;
-                a.ws0[w] = hi[r][e];
+                st_chk(a, a.ws0, w, a.ws_n, KRD_WS, (float)(hi[r][e]));
                 if (RED == RR_SUM)
-                    a.ws1[w] = lo[r][e];
+                    st_chk(a, a.ws1, w, a.ws_n, KRD_WS, (float)(lo[r][e]));
                 else
-                    a.wsi[w] = bj[r][e];
+                    st_chk(a, a.wsi, w, a.ws_n, KRD_WS, (int32_t)(bj[r][e]));
             }
         }
     }
