@@ -41,7 +41,7 @@ Instance choose_instance(int op, int D, int EK) {
     if (op == OP_KNN) {
         in.ek_pad = pad_k(EK);
         in.rows = rows_knn(in.d_pad, in.ek_pad);
-        in.tile = instance_tile(in.d_pad, 0);
+        in.tile = knn_instance_tile(in.d_pad);
     } else {
         in.ek_pad = pad_e(EK);
         in.rows = (op == OP_GRAD) ? (wide_grad(in.d_pad) ? 1 : rows_grad(in.d_pad, in.ek_pad))

@@ -102,4 +102,23 @@ KR_HD constexpr int instance_tile(int DP, int VP) {
     return packed(DP) ? tile_points_packed(pair_stride(DP, VP)) : tile_points(pack_stride(DP, VP));
 }
 
+// K-min with the expansion filter: |y~|^2 - 2 x~.y~ (D FMAs a pair) screens groups of
+// points and only the groups that may hold a candidate get the direct distance.  Used
+// up to D = 16, where a tile record is shared by 2-4 rows of a thread and its
+// shared-memory loads stay well below the FMA work; at larger D one row per thread
+// would make the loop load-bound.
+KR_HD constexpr bool knn_expand(int DP) { return DP <= 16; }
+// Margin of the filter per unit of |x~|^2 + |y~|^2 + threshold: (8 DP + 12) u with
+// u = 2^-24, twice the first-order bound on the rounding the filter can hide.
+KR_HD constexpr float knn_kappa(int DP) { return (float)(8 * DP + 12) * 5.9604644775390625e-8f; }
+// Tile points of the filtered K-min: its two record arrays (filter: -y~ and h; exact:
+// -y) together within 36 KB of static shared memory.
+KR_HD constexpr int knn_tile_bytes(int DP, int BN) { return (BN / 2) * (pair_stride(DP, 1) + pair_stride(DP, 0)) * 4; }
+KR_HD constexpr int knn_tile(int DP) {
+    return knn_tile_bytes(DP, 512) <= 36864 ? 512 : knn_tile_bytes(DP, 256) <= 36864 ? 256
+         : knn_tile_bytes(DP, 128) <= 36864 ? 128 : 64;
+}
+// Tile points of the K-min instance for DP.
+KR_HD constexpr int knn_instance_tile(int DP) { return knn_expand(DP) ? knn_tile(DP) : instance_tile(DP, 0); }
+
 }  // namespace kr

@@ -140,7 +140,6 @@ __device__ __forceinline__ void stage_coords(const Args &a, float *tile, int64_t
     for (int p = threadIdx.x; p < nvp; p += kThreads) {
         float *dst = tile + p * PS;
         if (p < nv) {
-            const float *src = a.y + (jt + p) * a.D;
 #pragma unroll
             for (int d = 0; d < DP; ++d)
                 if (d < a.D) dst[d] = scale * ldg_chk(a, a.y, (jt + p) * a.D + d, a.N * a.D, KRD_Y);

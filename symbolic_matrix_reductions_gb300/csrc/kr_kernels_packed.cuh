@@ -55,7 +55,6 @@ __device__ __forceinline__ void stage_coords_pairs(const Args &a, float *tile, i
                                                    float scale, float pad0) {
     for (int p = threadIdx.x; p < nvp; p += kThreads) {
         if (p < nv) {
-            const float *src = a.y + (jt + p) * a.D;
 #pragma unroll
             for (int d = 0; d < DP; ++d)
                 if (d < a.D) *pair_slot<PS2>(tile, p, d) = scale * ldg_chk(a, a.y, (jt + p) * a.D + d, a.N * a.D, KRD_Y);
@@ -591,6 +590,324 @@ __global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knn2_kernel(
         }
         if (CB > 0) {  // the queues name points of this tile: drain before it is replaced
             knn_drain_groups<DP, KP, R, PS2, UP>(x2, dk, ik, nc, qbuf, tile, jt, CB > 0 ? CB : 1);
+            nmax = 0;
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t i = row0 + (int64_t)r * kThreads + t;
+        if (i >= a.M) continue;
+        if (a.S == 1) {
+#pragma unroll
+            for (int k = 0; k < KP; ++k) {
+                if (k >= a.K) continue;
+                st_chk(a, a.idx, i * a.K + k, a.idx_n, KRD_IDX, (int32_t)(ik[r][k]));
+                if (a.out) st_chk(a, a.out, i * a.K + k, a.out_n, KRD_OUT, (float)(dk[r][k]));
+            }
+        } else {
+            const int64_t w = ((int64_t)blockIdx.y * a.M + i) * KP;
+#pragma unroll
+            for (int k = 0; k < KP; ++k) {
+                st_chk(a, a.ws0, w + k, a.ws_n, KRD_WS, (float)(dk[r][k]));
+                st_chk(a, a.wsi, w + k, a.ws_n, KRD_WS, (int32_t)(ik[r][k]));
+            }
+        }
+    }
+}
+
+
+// ---------------------------------------------------------------------------
+// K-min with an expansion filter (D <= 16).
+//
+// Which y_j rank first for a row x only depends on |y_j|^2 - 2 x.y_j (|x|^2 is the
+// same for every j): D FMAs a pair, against D subtractions and D FMAs for |x - y|^2.
+// In fp32 that value cancels when |x| and |y| are large against the distance, so here
+// it only screens: a group of points whose filter values all lie above a bound T is
+// skipped, T being placed so that a skipped point's direct fp32 distance cannot lie
+// below the current K-th distance thr, i.e. it could not have been inserted.  Every
+// other group gets the direct fp32 distance (the arithmetic of the unfiltered
+// kernels, from the exact coordinates) and is inserted by that value, so the list is
+// the one the unfiltered scan produces.
+//
+// The block subtracts c, the mean of its rows of x, from x and y before the filter
+// (x~ = fl(x - c), y~ = fl(y - c)), so an offset common to the data does not loosen
+// the bound.  For point j and row i:
+//   f_ij = h_j + sum_d x~_id (-y~_jd),   h_j = fl(|y~_j|^2) (1 - kappa) / 2,
+//   T_i  = ((thr_i + 2^-100 + kappa (|x~_i|^2 + thr_i)) - |x~_i|^2) / 2.
+// f_ij > T_i means |x~ - y~|^2 > thr + 2^-100 + kappa Q (Q = |x~|^2 + |y~|^2 + thr) up
+// to the rounding of f, h, T, of the centring and of the direct distance, which in
+// all stays below (3D + 7) u Q (u = 2^-24) plus a few 2^-126 (flushed subnormals);
+// kappa = (8D + 12) u is more than twice that and 2^-100 covers the absolute part,
+// so the direct distance is >= thr.  A point with |y~|^2 not below 2^100 (or NaN)
+// gets h = -inf and a row with |x~|^2 not below 2^100 gets T = +inf: they always
+// pass, and the direct distance decides.  (Non-finite coordinates give a non-finite
+// or NaN direct distance, which is never inserted, so their filter values need no
+// bound.)
+// ---------------------------------------------------------------------------
+template <int DP>
+__device__ __forceinline__ float knn_filter_bound(float thr, float xx) {
+    constexpr float kappa = knn_kappa(DP);
+    if (!(xx < 0x1p100f)) return f_inf();
+    return 0.5f * (fmaf(kappa, xx + thr, thr + 0x1p-100f) - xx);
+}
+
+// |x~|^2 of a row held as duplicated register pairs (fp32 fma chain).
+template <int DP>
+__device__ __forceinline__ float sq_norm_pairs(const float2 (&x2)[DP]) {
+    float s = x2[0].x * x2[0].x;
+#pragma unroll
+    for (int d = 1; d < DP; ++d) s = fmaf(x2[d].x, x2[d].x, s);
+    return s;
+}
+
+// Filter values of the two points of a filter record (fields -y~_d, then h).
+template <int DP, int PSF>
+__device__ __forceinline__ float2 filter_pair(const float2 (&x2)[DP], const float2 (&pv)[PSF / 2]) {
+    constexpr int NC = dist_chains(DP);
+    float2 acc[NC];
+    acc[0] = __ffma2_rn(x2[0], pv[0], pv[DP]);
+#pragma unroll
+    for (int c = 1; c < NC; ++c) acc[c] = __fmul2_rn(x2[c], pv[c]);
+#pragma unroll
+    for (int d = NC; d < DP; ++d) acc[d % NC] = __ffma2_rn(x2[d], pv[d], acc[d % NC]);
+    float2 f = acc[0];
+#pragma unroll
+    for (int c = 1; c < NC; ++c) f = __fadd2_rn(f, acc[c]);
+    return f;
+}
+
+// Exact coordinates of row i as duplicated register pairs (zero beyond M and D).
+template <int DP>
+__device__ __forceinline__ void load_row_exact(const Args &a, int64_t i, float2 (&xe)[DP]) {
+#pragma unroll
+    for (int d = 0; d < DP; ++d) {
+        const float v = (i < a.M && d < a.D) ? ldg_chk(a, a.x, i * a.D + d, a.M * a.D, KRD_X) : 0.f;
+        xe[d] = make_float2(v, v);
+    }
+}
+
+// Direct fp32 distances of the UP exact records from rec0 on, and their insertion (in
+// increasing j) into the row's list.
+template <int DP, int KP, int PSE, int UP>
+__device__ __forceinline__ void knnx_insert_group(const float2 (&xe)[DP], float (&dk)[KP], int (&ik)[KP],
+                                                  const float *tileE, int rec0, int64_t j0) {
+    float2 q[UP];
+#pragma unroll
+    for (int u = 0; u < UP; ++u) {
+        float2 pv[PSE / 2];
+        load_pair_record<PSE>(tileE + (rec0 + u) * PSE, pv);
+        q[u] = sq_dist_pair<DP, PSE>(xe, pv, make_float2(0.f, 0.f), false);
+    }
+    const float thr = dk[KP - 1];
+    unsigned mask = 0;
+#pragma unroll
+    for (int u = 0; u < UP; ++u) {
+        mask |= (q[u].x < thr ? 1u : 0u) << (2 * u);
+        mask |= (q[u].y < thr ? 1u : 0u) << (2 * u + 1);
+    }
+    while (mask) {  // usually one point
+        const int c = __ffs(mask) - 1;
+        mask &= mask - 1;
+        float2 qq = q[0];
+#pragma unroll
+        for (int u = 1; u < UP; ++u) qq = ((c >> 1) == u) ? q[u] : qq;
+        knn_insert<KP>(dk, ik, (c & 1) ? qq.y : qq.x, (int)(j0 + c));
+    }
+}
+
+// Tile of the filtered K-min: exact records -y (padding: -inf in coordinate 0, so the
+// direct distance is +inf) and filter records -y~ and h (padding: zeros and h = +inf,
+// so f = +inf).  Coordinates d >= D are zero in both.
+template <int DP, int PSF, int PSE>
+__device__ __forceinline__ void stage_knn_filter(const Args &a, float *tileF, float *tileE, const float *cen,
+                                                 int64_t jt, int nv, int nvp) {
+    constexpr float kH = 0.5f * (1.0f - knn_kappa(DP));
+    for (int p = threadIdx.x; p < nvp; p += kThreads) {
+        if (p < nv) {
+            float yy = 0.f;
+#pragma unroll
+            for (int d = 0; d < DP; ++d) {
+                const float v = d < a.D ? ldg_chk(a, a.y, (jt + p) * a.D + d, a.N * a.D, KRD_Y) : 0.f;
+                const float w = v - cen[d];
+                *pair_slot<PSE>(tileE, p, d) = -v;
+                *pair_slot<PSF>(tileF, p, d) = -w;
+                yy = (d == 0) ? w * w : fmaf(w, w, yy);
+            }
+            *pair_slot<PSF>(tileF, p, DP) = (yy < 0x1p100f) ? kH * yy : -f_inf();
+        } else {
+#pragma unroll
+            for (int d = 0; d < DP; ++d) {
+                *pair_slot<PSE>(tileE, p, d) = (d == 0) ? -f_inf() : 0.f;
+                *pair_slot<PSF>(tileF, p, d) = 0.f;
+            }
+            *pair_slot<PSF>(tileF, p, DP) = f_inf();
+        }
+    }
+}
+
+// Drains the queues of passing groups (one byte per entry: the group's index in the
+// tile), all 32 lanes together, one slot per step, in the order they were filled.
+template <int DP, int KP, int R, int PSE, int UP>
+__device__ __forceinline__ void knnx_drain(const Args &a, int64_t row0, const float2 (&x2)[R][DP], float (&T)[R],
+                                           float (&dk)[R][KP], int (&ik)[R][KP], int (&nc)[R],
+                                           const uint8_t *qbuf, const float *tileE, int64_t jt, int CB) {
+    constexpr int UPT = 2 * UP;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int steps = __reduce_max_sync(0xffffffffu, nc[r]);
+        if (steps == 0) continue;
+        float2 xe[DP];
+        load_row_exact<DP>(a, row0 + (int64_t)r * kThreads + threadIdx.x, xe);
+        const uint8_t *slot = qbuf + r * CB * kThreads + threadIdx.x;
+        for (int s = 0; s < steps; ++s) {
+            if (s >= nc[r]) continue;
+            const int g = slot[s * kThreads];
+            knnx_insert_group<DP, KP, PSE, UP>(xe, dk[r], ik[r], tileE, g * UP, jt + g * UPT);
+        }
+        nc[r] = 0;
+        T[r] = knn_filter_bound<DP>(dk[r][KP - 1], sq_norm_pairs<DP>(x2[r]));
+    }
+}
+
+template <int DP, int KP, int R, int BN>
+__global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knnx_kernel(const Args a_) {
+    const Args a = batch_view(a_);
+    constexpr int PSF = pair_stride(DP, 1);
+    constexpr int PSE = pair_stride(DP, 0);
+    constexpr int UP = unroll_pairs(DP);
+    constexpr int UPT = 2 * UP;
+    constexpr int CB = knn_buffer(DP, KP);
+    constexpr int G = CB > 0 ? knn_check_groups(DP, KP) : 1;
+    constexpr int DRAIN_AT = CB - G;
+    static_assert(CB == 0 || DRAIN_AT >= 0, "queue shorter than the groups between checks");
+    static_assert(BN % (G * UPT) == 0, "tile must be a multiple of the unroll");
+    static_assert(BN / UPT <= 256, "queue entries are bytes");
+    static_assert(knn_tile_bytes(DP, BN) + (CB > 0 ? R * CB * kThreads : 0) <= 45056, "shared memory");
+    __shared__ __align__(16) float tileF[(BN / 2) * PSF];
+    __shared__ __align__(16) float tileE[(BN / 2) * PSE];
+    // per row r, slot s, thread t: qbuf[(r CB + s) kThreads + t] = a passing group of the tile
+    __shared__ uint8_t qbuf[CB > 0 ? R * CB * kThreads : 1];
+    __shared__ float cpart[kThreads / 32][2 * DP];
+    __shared__ float cen[DP];
+
+    const int t = threadIdx.x;
+    const int64_t row0 = (int64_t)blockIdx.x * (kThreads * R);
+    const int64_t j_begin = (int64_t)blockIdx.y * a.chunk;
+    const int64_t j_end = min(a.N, j_begin + a.chunk);
+
+    // Centre: mean of the block's rows of x, per coordinate over its finite values,
+    // summed in a fixed order (lane 0 of each warp, then the warps in turn).
+    float2 x2[R][DP];
+    load_rows_pairs<DP, R>(a, row0, x2, 1.f);
+    {
+        float s[DP], n[DP];
+#pragma unroll
+        for (int d = 0; d < DP; ++d) {
+            s[d] = 0.f;
+            n[d] = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float v = x2[r][d].x;
+                if (row0 + (int64_t)r * kThreads + t < a.M && isfinite(v)) {
+                    s[d] += v;
+                    n[d] += 1.f;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                s[d] += __shfl_xor_sync(0xffffffffu, s[d], o);
+                n[d] += __shfl_xor_sync(0xffffffffu, n[d], o);
+            }
+        }
+        if ((t & 31) == 0) {
+#pragma unroll
+            for (int d = 0; d < DP; ++d) {
+                cpart[t >> 5][d] = s[d];
+                cpart[t >> 5][DP + d] = n[d];
+            }
+        }
+        __syncthreads();
+        if (t < DP) {
+            float S = 0.f, Nn = 0.f;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) {
+                S += cpart[w][t];
+                Nn += cpart[w][DP + t];
+            }
+            cen[t] = Nn > 0.f ? S / Nn : 0.f;
+        }
+        __syncthreads();
+    }
+    float T[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int d = 0; d < DP; ++d) {
+            const float w = x2[r][d].x - cen[d];
+            x2[r][d] = make_float2(w, w);
+        }
+        T[r] = f_inf();
+    }
+
+    float dk[R][KP];
+    int ik[R][KP];
+    int nc[R];
+    int nmax = 0;  // the largest of this thread's queue lengths (an upper bound)
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int k = 0; k < KP; ++k) {
+            dk[r][k] = f_inf();
+            ik[r][k] = -1;
+        }
+        nc[r] = 0;
+    }
+
+    for (int64_t jt = j_begin; jt < j_end; jt += BN) {
+        const int nv = (int)min((int64_t)BN, j_end - jt);
+        const int nvp = (nv + G * UPT - 1) / (G * UPT) * (G * UPT);
+        __syncthreads();
+        stage_knn_filter<DP, PSF, PSE>(a, tileF, tileE, cen, jt, nv, nvp);
+        __syncthreads();
+
+        for (int jg = 0; jg < nvp; jg += G * UPT) {
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                const int jj = jg + gg * UPT;
+                float2 f[UP][R];
+#pragma unroll
+                for (int u = 0; u < UP; ++u) {
+                    float2 pv[PSF / 2];
+                    load_pair_record<PSF>(tileF + ((jj >> 1) + u) * PSF, pv);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) f[u][r] = filter_pair<DP, PSF>(x2[r], pv);
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float mn = fminf(f[0][r].x, f[0][r].y);
+#pragma unroll
+                    for (int u = 1; u < UP; ++u) mn = fminf(mn, fminf(f[u][r].x, f[u][r].y));
+                    if (!(mn > T[r])) {
+                        if (CB == 0) {
+                            float2 xe[DP];
+                            load_row_exact<DP>(a, row0 + (int64_t)r * kThreads + t, xe);
+                            knnx_insert_group<DP, KP, PSE, UP>(xe, dk[r], ik[r], tileE, jj >> 1, jt + jj);
+                            T[r] = knn_filter_bound<DP>(dk[r][KP - 1], sq_norm_pairs<DP>(x2[r]));
+                        } else {
+                            if (smem_ok(a, nc[r], CB)) qbuf[(r * CB + nc[r]) * kThreads + t] = (uint8_t)(jj / UPT);
+                            nmax = max(nmax, ++nc[r]);
+                        }
+                    }
+                }
+            }
+            if (CB > 0 && __any_sync(0xffffffffu, nmax > DRAIN_AT)) {
+                knnx_drain<DP, KP, R, PSE, UP>(a, row0, x2, T, dk, ik, nc, qbuf, tileE, jt, CB > 0 ? CB : 1);
+                nmax = 0;
+            }
+        }
+        if (CB > 0) {  // the queues name points of this tile: drain before it is replaced
+            knnx_drain<DP, KP, R, PSE, UP>(a, row0, x2, T, dk, ik, nc, qbuf, tileE, jt, CB > 0 ? CB : 1);
             nmax = 0;
         }
     }

@@ -8,10 +8,12 @@ typedef void (*KernelFn)(const Args);
 
 template <int DP, int KP>
 KernelFn knn_instance() {
-    if constexpr (packed(DP))
-        return knn2_kernel<DP, KP, rows_knn(DP, KP), instance_tile(DP, 0)>;
+    if constexpr (knn_expand(DP))
+        return knnx_kernel<DP, KP, rows_knn(DP, KP), knn_instance_tile(DP)>;
+    else if constexpr (packed(DP))
+        return knn2_kernel<DP, KP, rows_knn(DP, KP), knn_instance_tile(DP)>;
     else
-        return knn_kernel<DP, KP, rows_knn(DP, KP), instance_tile(DP, 0)>;
+        return knn_kernel<DP, KP, rows_knn(DP, KP), knn_instance_tile(DP)>;
 }
 
 template <int KP>

@@ -177,7 +177,6 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
         __syncthreads();  // every thread is done with the previous tile
         for (int p = t; p < nvp; p += kThreads) {
             if (p < nv) {
-                const float *src = a.y + (jt + p) * a.D;
 #pragma unroll
                 for (int d = 0; d < DP; ++d)
                     if (d < a.D) *radial_slot<L, PS>(tile, p, d) = -a.c * ldg_chk(a, a.y, (jt + p) * a.D + d, a.N * a.D, KRD_Y);
