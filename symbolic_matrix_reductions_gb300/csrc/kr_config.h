@@ -86,15 +86,15 @@ KR_HD constexpr int tile_points_packed(int PS2) {
     return (16384 / PS2) >= 512 ? 512 : (16384 / PS2) >= 256 ? 256 : (16384 / PS2) >= 128 ? 128
          : (16384 / PS2) >= 64 ? 64 : 32;
 }
-// Queue of passing point groups of the packed K-min: slots per row in shared memory
-// (0: insert at once).  R x CB x 128 threads x 4 bytes sit beside the tile, and the
-// two must stay within 48 KB of static shared memory.  Queued instances are
-// compiled for 4 resident blocks per SM (at most 128 registers a thread).
-KR_HD constexpr int knn_buffer(int DP, int KP) { return DP <= 4 && KP <= 10 ? 16 : 0; }
-// Resident blocks per SM the queued K-min instances are compiled for (registers cap).
-KR_HD constexpr int knn_min_blocks(int DP, int KP) { return knn_buffer(DP, KP) > 0 ? 4 : 1; }
-// Unrolled point groups between two warp-wide checks of the candidate buffers.
-KR_HD constexpr int knn_check_groups(int DP, int KP) { return 2; }
+// Filtered K-min (D <= 4, K <= 10): the pass bits of this many consecutive point groups
+// are gathered in one word per row and queued as one entry (block index, bit mask),
+// so the scan loop itself carries no branch.
+KR_HD constexpr int knnx_mask_groups(int DP, int KP) { return 8; }
+// Entries per row of the filtered K-min's queue (0: immediate insertion).
+KR_HD constexpr int knnx_queue(int DP, int KP) { return DP <= 4 && KP <= 10 ? 8 : 0; }
+// Resident blocks per SM the K-min instances are compiled for (registers cap): the
+// queued filtered instances keep at most 128 registers a thread.
+KR_HD constexpr int knn_min_blocks(int DP, int KP) { return knnx_queue(DP, KP) > 0 ? 4 : 1; }
 // Pair records per unrolled step of the packed inner loop.
 KR_HD constexpr int unroll_pairs(int DP) { return DP <= 8 ? 2 : 1; }
 // Tile points of an instance (value columns VP = E, K-min: 0).
@@ -112,11 +112,13 @@ KR_HD constexpr bool knn_expand(int DP) { return DP <= 16; }
 // u = 2^-24, twice the first-order bound on the rounding the filter can hide.
 KR_HD constexpr float knn_kappa(int DP) { return (float)(8 * DP + 12) * 5.9604644775390625e-8f; }
 // Tile points of the filtered K-min: its two record arrays (filter: -y~ and h; exact:
-// -y) together within 36 KB of static shared memory.
+// -y) together within 36 KB of static shared memory.  Up to 1024 points: the queues
+// are drained at least once a tile, and a longer tile gives each lane more entries
+// per drain, so the warp-wide drain steps are better filled.
 KR_HD constexpr int knn_tile_bytes(int DP, int BN) { return (BN / 2) * (pair_stride(DP, 1) + pair_stride(DP, 0)) * 4; }
 KR_HD constexpr int knn_tile(int DP) {
-    return knn_tile_bytes(DP, 512) <= 36864 ? 512 : knn_tile_bytes(DP, 256) <= 36864 ? 256
-         : knn_tile_bytes(DP, 128) <= 36864 ? 128 : 64;
+    return knn_tile_bytes(DP, 1024) <= 36864 ? 1024 : knn_tile_bytes(DP, 512) <= 36864 ? 512
+         : knn_tile_bytes(DP, 256) <= 36864 ? 256 : knn_tile_bytes(DP, 128) <= 36864 ? 128 : 64;
 }
 // Tile points of the K-min instance for DP.
 KR_HD constexpr int knn_instance_tile(int DP) { return knn_expand(DP) ? knn_tile(DP) : instance_tile(DP, 0); }

@@ -439,77 +439,21 @@ __global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a_) {
 }
 
 // ---------------------------------------------------------------------------
-// K-min (packed distances).  The threshold test is taken once per row for a
-// group of UPT points (the minimum of their distances against the list's last
-// entry).  Insertion is strictly-smaller and in increasing j, so equal distances
-// keep the lower index.
-//
-// CB == 0: the group's passing points are walked in increasing j from a bit mask
-// and inserted into the sorted register list at once.  Late in a scan passing
-// groups are rare and come one lane at a time, so the warp runs the whole
-// insertion for a single row while 31 lanes wait.
-// CB > 0: a passing group only appends its index to its row's queue of CB slots in
-// shared memory (one store).  Every G groups the warp checks whether any lane could
-// overflow a queue in the next G groups; if so, and always before the tile is
-// replaced, all 32 lanes drain their queues together, one slot per step: each slot's
-// four distances are recomputed from the tile (a few instructions at small D),
-// tested against the current threshold, and the passing points inserted in
-// increasing j.  Slots are drained in the order they were filled (increasing j), so
-// the result is the same list as with CB == 0.
+// K-min (packed direct distances, 32 <= D <= 64; smaller D take the filtered kernel
+// below).  The threshold test is taken once per row for a group of UPT points (the
+// minimum of their distances against the list's last entry); a passing group's
+// points are walked in increasing j from a bit mask and inserted into the sorted
+// register list.  Insertion is strictly-smaller and in increasing j, so equal
+// distances keep the lower index.
 // ---------------------------------------------------------------------------
-template <int DP, int KP, int R, int PS2, int UP>
-__device__ __forceinline__ void knn_drain_groups(const float2 (&x2)[R][DP], float (&dk)[R][KP], int (&ik)[R][KP],
-                                                 int (&nc)[R], const int *qbuf, const float *tile, int64_t jt,
-                                                 int CB) {
-    constexpr int UPT = 2 * UP;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int steps = __reduce_max_sync(0xffffffffu, nc[r]);
-        const int *slot = qbuf + r * CB * kThreads + threadIdx.x;
-        for (int s = 0; s < steps; ++s) {
-            const int g = s < nc[r] ? slot[s * kThreads] : -1;
-            if (g < 0) continue;
-            float2 q[UP];
-#pragma unroll
-            for (int u = 0; u < UP; ++u) {
-                float2 pv[PS2 / 2];
-                load_pair_record<PS2>(tile + (g * UP + u) * PS2, pv);
-                q[u] = sq_dist_pair<DP, PS2>(x2[r], pv, make_float2(0.f, 0.f), false);
-            }
-            const float thr = dk[r][KP - 1];
-            unsigned mask = 0;
-#pragma unroll
-            for (int u = 0; u < UP; ++u) {
-                mask |= (q[u].x < thr ? 1u : 0u) << (2 * u);
-                mask |= (q[u].y < thr ? 1u : 0u) << (2 * u + 1);
-            }
-            while (mask) {  // usually one point; a stale value leaves the list as it is
-                const int c = __ffs(mask) - 1;
-                mask &= mask - 1;
-                float2 qq = q[0];
-#pragma unroll
-                for (int u = 1; u < UP; ++u) qq = ((c >> 1) == u) ? q[u] : qq;
-                knn_insert<KP>(dk[r], ik[r], (c & 1) ? qq.y : qq.x, (int)(jt + g * UPT + c));
-            }
-        }
-        nc[r] = 0;
-    }
-}
-
 template <int DP, int KP, int R, int BN>
-__global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knn2_kernel(const Args a_) {
+__global__ void __launch_bounds__(kThreads) knn2_kernel(const Args a_) {
     const Args a = batch_view(a_);
     constexpr int PS2 = pair_stride(DP, 0);
     constexpr int UP = unroll_pairs(DP);
     constexpr int UPT = 2 * UP;
-    constexpr int CB = knn_buffer(DP, KP);
-    constexpr int G = CB > 0 ? knn_check_groups(DP, KP) : 1;  // groups between queue checks
-    constexpr int DRAIN_AT = CB - G;  // a lane with more entries in one row may overflow it
-    static_assert(CB == 0 || DRAIN_AT >= 0, "queue shorter than the groups between checks");
-    static_assert(BN % (G * UPT) == 0, "tile must be a multiple of the unroll");
+    static_assert(BN % UPT == 0, "tile must be a multiple of the unroll");
     __shared__ __align__(16) float tile[(BN / 2) * PS2];
-    // per row r, slot s, thread t: qbuf[(r CB + s) kThreads + t] = a passing group of the tile
-    __shared__ int qbuf[CB > 0 ? R * CB * kThreads : 1];
 
     const int t = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.x * (kThreads * R);
@@ -521,8 +465,6 @@ __global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knn2_kernel(
     load_rows_pairs<DP, R>(a, row0, x2, 1.f);
     float dk[R][KP];
     int ik[R][KP];
-    int nc[R];
-    int nmax = 0;  // the largest of this thread's queue lengths (an upper bound)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
@@ -530,67 +472,49 @@ __global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knn2_kernel(
             dk[r][k] = f_inf();
             ik[r][k] = -1;
         }
-        nc[r] = 0;
     }
 
     for (int64_t jt = j_begin; jt < j_end; jt += BN) {
         const int nv = (int)min((int64_t)BN, j_end - jt);
-        const int nvp = (nv + G * UPT - 1) / (G * UPT) * (G * UPT);
+        const int nvp = (nv + UPT - 1) / UPT * UPT;
         __syncthreads();
         stage_coords_pairs<DP, PS2>(a, tile, jt, nv, nvp, -1.f, -f_inf());
         __syncthreads();
 
-        for (int jg = 0; jg < nvp; jg += G * UPT) {
+        for (int jj = 0; jj < nvp; jj += UPT) {
+            float2 q[UP][R];
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg) {
-                const int jj = jg + gg * UPT;
-                float2 q[UP][R];
+            for (int u = 0; u < UP; ++u) {
+                float2 pv[PS2 / 2];
+                load_pair_record<PS2>(tile + ((jj >> 1) + u) * PS2, pv);
 #pragma unroll
-                for (int u = 0; u < UP; ++u) {
-                    float2 pv[PS2 / 2];
-                    load_pair_record<PS2>(tile + ((jj >> 1) + u) * PS2, pv);
+                for (int r = 0; r < R; ++r)
+                    q[u][r] = sq_dist_pair<DP, PS2>(x2[r], pv, make_float2(0.f, 0.f), false);
+            }
 #pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        q[u][r] = sq_dist_pair<DP, PS2>(x2[r], pv, make_float2(0.f, 0.f), false);
-                }
+            for (int r = 0; r < R; ++r) {
+                float mn = fminf(q[0][r].x, q[0][r].y);
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    float mn = fminf(q[0][r].x, q[0][r].y);
+                for (int u = 1; u < UP; ++u) mn = fminf(mn, fminf(q[u][r].x, q[u][r].y));
+                if (mn < dk[r][KP - 1]) {
+                    const float thr = dk[r][KP - 1];
+                    unsigned mask = 0;
 #pragma unroll
-                    for (int u = 1; u < UP; ++u) mn = fminf(mn, fminf(q[u][r].x, q[u][r].y));
-                    if (mn < dk[r][KP - 1]) {
-                        if (CB == 0) {
-                            const float thr = dk[r][KP - 1];
-                            unsigned mask = 0;
+                    for (int u = 0; u < UP; ++u) {
+                        mask |= (q[u][r].x < thr ? 1u : 0u) << (2 * u);
+                        mask |= (q[u][r].y < thr ? 1u : 0u) << (2 * u + 1);
+                    }
+                    const int j0 = (int)(jt + jj);
+                    while (mask) {
+                        const int c = __ffs(mask) - 1;
+                        mask &= mask - 1;
+                        float2 qq = q[0][r];
 #pragma unroll
-                            for (int u = 0; u < UP; ++u) {
-                                mask |= (q[u][r].x < thr ? 1u : 0u) << (2 * u);
-                                mask |= (q[u][r].y < thr ? 1u : 0u) << (2 * u + 1);
-                            }
-                            const int j0 = (int)(jt + jj);
-                            while (mask) {
-                                const int c = __ffs(mask) - 1;
-                                mask &= mask - 1;
-                                float2 qq = q[0][r];
-#pragma unroll
-                                for (int u = 1; u < UP; ++u) qq = ((c >> 1) == u) ? q[u][r] : qq;
-                                knn_insert<KP>(dk[r], ik[r], (c & 1) ? qq.y : qq.x, j0 + c);
-                            }
-                        } else {
-                            if (smem_ok(a, nc[r], CB)) qbuf[(r * CB + nc[r]) * kThreads + t] = jj / UPT;
-                            nmax = max(nmax, ++nc[r]);
-                        }
+                        for (int u = 1; u < UP; ++u) qq = ((c >> 1) == u) ? q[u][r] : qq;
+                        knn_insert<KP>(dk[r], ik[r], (c & 1) ? qq.y : qq.x, j0 + c);
                     }
                 }
             }
-            if (CB > 0 && __any_sync(0xffffffffu, nmax > DRAIN_AT)) {
-                knn_drain_groups<DP, KP, R, PS2, UP>(x2, dk, ik, nc, qbuf, tile, jt, CB > 0 ? CB : 1);
-                nmax = 0;
-            }
-        }
-        if (CB > 0) {  // the queues name points of this tile: drain before it is replaced
-            knn_drain_groups<DP, KP, R, PS2, UP>(x2, dk, ik, nc, qbuf, tile, jt, CB > 0 ? CB : 1);
-            nmax = 0;
         }
     }
 
@@ -615,7 +539,6 @@ __global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knn2_kernel(
         }
     }
 }
-
 
 // ---------------------------------------------------------------------------
 // K-min with an expansion filter (D <= 16).
@@ -687,18 +610,22 @@ __device__ __forceinline__ void load_row_exact(const Args &a, int64_t i, float2 
     }
 }
 
-// Direct fp32 distances of the UP exact records from rec0 on, and their insertion (in
-// increasing j) into the row's list.
-template <int DP, int KP, int PSE, int UP>
-__device__ __forceinline__ void knnx_insert_group(const float2 (&xe)[DP], float (&dk)[KP], int (&ik)[KP],
-                                                  const float *tileE, int rec0, int64_t j0) {
-    float2 q[UP];
+// Direct fp32 distances of the UP exact records from rec0 on.
+template <int DP, int PSE, int UP>
+__device__ __forceinline__ void knnx_exact_group(const float2 (&xe)[DP], const float *tileE, int rec0,
+                                                 float2 (&q)[UP]) {
 #pragma unroll
     for (int u = 0; u < UP; ++u) {
         float2 pv[PSE / 2];
         load_pair_record<PSE>(tileE + (rec0 + u) * PSE, pv);
         q[u] = sq_dist_pair<DP, PSE>(xe, pv, make_float2(0.f, 0.f), false);
     }
+}
+
+// Inserts the points of a group (distances q, first index j0) that beat the row's
+// current K-th distance, in increasing j.
+template <int KP, int UP>
+__device__ __forceinline__ void knnx_insert_group(const float2 (&q)[UP], float (&dk)[KP], int (&ik)[KP], int64_t j0) {
     const float thr = dk[KP - 1];
     unsigned mask = 0;
 #pragma unroll
@@ -746,12 +673,15 @@ __device__ __forceinline__ void stage_knn_filter(const Args &a, float *tileF, fl
     }
 }
 
-// Drains the queues of passing groups (one byte per entry: the group's index in the
-// tile), all 32 lanes together, one slot per step, in the order they were filled.
-template <int DP, int KP, int R, int PSE, int UP>
+// Drains the queues of one thread's rows, all 32 lanes together, in the order the
+// entries were made.  An entry is (block << 8) | mask: bit g of mask marks group
+// block * IB + g of the tile.  The groups of an entry are taken two at a time, both
+// groups' distances computed before the first insertion (the second's test then sees
+// the threshold the first left).
+template <int DP, int KP, int R, int PSE, int UP, int IB>
 __device__ __forceinline__ void knnx_drain(const Args &a, int64_t row0, const float2 (&x2)[R][DP], float (&T)[R],
                                            float (&dk)[R][KP], int (&ik)[R][KP], int (&nc)[R],
-                                           const uint8_t *qbuf, const float *tileE, int64_t jt, int CB) {
+                                           const uint16_t *qbuf, const float *tileE, int64_t jt, int CB) {
     constexpr int UPT = 2 * UP;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -759,11 +689,23 @@ __device__ __forceinline__ void knnx_drain(const Args &a, int64_t row0, const fl
         if (steps == 0) continue;
         float2 xe[DP];
         load_row_exact<DP>(a, row0 + (int64_t)r * kThreads + threadIdx.x, xe);
-        const uint8_t *slot = qbuf + r * CB * kThreads + threadIdx.x;
+        const uint16_t *slot = qbuf + r * CB * kThreads + threadIdx.x;
         for (int s = 0; s < steps; ++s) {
-            if (s >= nc[r]) continue;
-            const int g = slot[s * kThreads];
-            knnx_insert_group<DP, KP, PSE, UP>(xe, dk[r], ik[r], tileE, g * UP, jt + g * UPT);
+            const unsigned e = s < nc[r] ? (unsigned)slot[s * kThreads] : 0u;
+            unsigned mask = e & 0xffu;
+            const int g_base = (int)(e >> 8) * IB;
+            while (mask) {
+                const int g0 = g_base + __ffs(mask) - 1;
+                mask &= mask - 1;
+                const bool two = mask != 0;
+                const int g1 = two ? g_base + __ffs(mask) - 1 : g0;
+                mask &= mask - 1;
+                float2 q0[UP], q1[UP];
+                knnx_exact_group<DP, PSE, UP>(xe, tileE, g0 * UP, q0);
+                knnx_exact_group<DP, PSE, UP>(xe, tileE, g1 * UP, q1);
+                knnx_insert_group<KP, UP>(q0, dk[r], ik[r], jt + g0 * UPT);
+                if (two) knnx_insert_group<KP, UP>(q1, dk[r], ik[r], jt + g1 * UPT);
+            }
         }
         nc[r] = 0;
         T[r] = knn_filter_bound<DP>(dk[r][KP - 1], sq_norm_pairs<DP>(x2[r]));
@@ -777,17 +719,17 @@ __global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knnx_kernel(
     constexpr int PSE = pair_stride(DP, 0);
     constexpr int UP = unroll_pairs(DP);
     constexpr int UPT = 2 * UP;
-    constexpr int CB = knn_buffer(DP, KP);
-    constexpr int G = CB > 0 ? knn_check_groups(DP, KP) : 1;
-    constexpr int DRAIN_AT = CB - G;
-    static_assert(CB == 0 || DRAIN_AT >= 0, "queue shorter than the groups between checks");
-    static_assert(BN % (G * UPT) == 0, "tile must be a multiple of the unroll");
-    static_assert(BN / UPT <= 256, "queue entries are bytes");
-    static_assert(knn_tile_bytes(DP, BN) + (CB > 0 ? R * CB * kThreads : 0) <= 45056, "shared memory");
+    constexpr int CB = knnx_queue(DP, KP);
+    constexpr int IB = CB > 0 ? knnx_mask_groups(DP, KP) : 1;  // groups per block
+    constexpr int BP = IB * UPT;                                 // points per block
+    static_assert(IB <= 8, "a block's mask is one byte of the entry");
+    static_assert(BN % BP == 0, "tile must be a multiple of the block");
+    static_assert(BN / BP <= 256, "block index is one byte of the entry");
+    static_assert(knn_tile_bytes(DP, BN) + (CB > 0 ? R * CB * kThreads * 2 : 0) <= 45056, "shared memory");
     __shared__ __align__(16) float tileF[(BN / 2) * PSF];
     __shared__ __align__(16) float tileE[(BN / 2) * PSE];
-    // per row r, slot s, thread t: qbuf[(r CB + s) kThreads + t] = a passing group of the tile
-    __shared__ uint8_t qbuf[CB > 0 ? R * CB * kThreads : 1];
+    // per row r, slot s, thread t: qbuf[(r CB + s) kThreads + t] = (block << 8) | pass mask
+    __shared__ uint16_t qbuf[CB > 0 ? R * CB * kThreads : 1];
     __shared__ float cpart[kThreads / 32][2 * DP];
     __shared__ float cen[DP];
 
@@ -853,7 +795,6 @@ __global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knnx_kernel(
     float dk[R][KP];
     int ik[R][KP];
     int nc[R];
-    int nmax = 0;  // the largest of this thread's queue lengths (an upper bound)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
@@ -866,15 +807,18 @@ __global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knnx_kernel(
 
     for (int64_t jt = j_begin; jt < j_end; jt += BN) {
         const int nv = (int)min((int64_t)BN, j_end - jt);
-        const int nvp = (nv + G * UPT - 1) / (G * UPT) * (G * UPT);
+        const int nvp = (nv + BP - 1) / BP * BP;
         __syncthreads();
         stage_knn_filter<DP, PSF, PSE>(a, tileF, tileE, cen, jt, nv, nvp);
         __syncthreads();
 
-        for (int jg = 0; jg < nvp; jg += G * UPT) {
+        for (int jb = 0; jb < nvp; jb += BP) {
+            unsigned m[R];
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg) {
-                const int jj = jg + gg * UPT;
+            for (int r = 0; r < R; ++r) m[r] = 0u;
+#pragma unroll
+            for (int gg = 0; gg < IB; ++gg) {
+                const int jj = jb + gg * UPT;
                 float2 f[UP][R];
 #pragma unroll
                 for (int u = 0; u < UP; ++u) {
@@ -883,33 +827,45 @@ __global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knnx_kernel(
 #pragma unroll
                     for (int r = 0; r < R; ++r) f[u][r] = filter_pair<DP, PSF>(x2[r], pv);
                 }
+                bool any = false;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     float mn = fminf(f[0][r].x, f[0][r].y);
 #pragma unroll
                     for (int u = 1; u < UP; ++u) mn = fminf(mn, fminf(f[u][r].x, f[u][r].y));
-                    if (!(mn > T[r])) {
-                        if (CB == 0) {
-                            float2 xe[DP];
-                            load_row_exact<DP>(a, row0 + (int64_t)r * kThreads + t, xe);
-                            knnx_insert_group<DP, KP, PSE, UP>(xe, dk[r], ik[r], tileE, jj >> 1, jt + jj);
-                            T[r] = knn_filter_bound<DP>(dk[r][KP - 1], sq_norm_pairs<DP>(x2[r]));
-                        } else {
-                            if (smem_ok(a, nc[r], CB)) qbuf[(r * CB + nc[r]) * kThreads + t] = (uint8_t)(jj / UPT);
-                            nmax = max(nmax, ++nc[r]);
-                        }
+                    const bool pass = !(mn > T[r]);
+                    m[r] |= pass ? (1u << gg) : 0u;
+                    any |= pass;
+                }
+                if (CB == 0 && any) {
+                    // insert at once: one branch for all rows, rarely taken late in a scan
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        if (m[r] == 0u) continue;
+                        float2 xe[DP], q[UP];
+                        load_row_exact<DP>(a, row0 + (int64_t)r * kThreads + t, xe);
+                        knnx_exact_group<DP, PSE, UP>(xe, tileE, jj >> 1, q);
+                        knnx_insert_group<KP, UP>(q, dk[r], ik[r], jt + jj);
+                        T[r] = knn_filter_bound<DP>(dk[r][KP - 1], sq_norm_pairs<DP>(x2[r]));
                     }
                 }
             }
-            if (CB > 0 && __any_sync(0xffffffffu, nmax > DRAIN_AT)) {
-                knnx_drain<DP, KP, R, PSE, UP>(a, row0, x2, T, dk, ik, nc, qbuf, tileE, jt, CB > 0 ? CB : 1);
-                nmax = 0;
+            if (CB > 0) {
+                // one entry per row and block, kept (the count advanced) only if a bit is set
+                int nm = 0;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (smem_ok(a, nc[r], CB))
+                        qbuf[(r * CB + nc[r]) * kThreads + t] = (uint16_t)(((jb / BP) << 8) | m[r]);
+                    nc[r] += m[r] != 0u ? 1 : 0;
+                    nm = max(nm, nc[r]);
+                }
+                if (__any_sync(0xffffffffu, nm >= CB))  // a full queue is drained before the next block
+                    knnx_drain<DP, KP, R, PSE, UP, IB>(a, row0, x2, T, dk, ik, nc, qbuf, tileE, jt, CB > 0 ? CB : 1);
             }
         }
-        if (CB > 0) {  // the queues name points of this tile: drain before it is replaced
-            knnx_drain<DP, KP, R, PSE, UP>(a, row0, x2, T, dk, ik, nc, qbuf, tileE, jt, CB > 0 ? CB : 1);
-            nmax = 0;
-        }
+        if (CB > 0)  // the entries name points of this tile: drain before it is replaced
+            knnx_drain<DP, KP, R, PSE, UP, IB>(a, row0, x2, T, dk, ik, nc, qbuf, tileE, jt, CB > 0 ? CB : 1);
     }
 
 #pragma unroll
