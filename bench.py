@@ -232,6 +232,13 @@ def roofline(op, D, E, seconds_per_launch, pairs, nsm, clk_mhz, xu_lanes, kernel
                          f") lanes/clk x {clk_mhz:.0f} MHz max SM clock"}
     if live_mhz:
         out["frac_at_live_clock"] = achieved / peak_at(live_mhz)
+    if op == "knn" and D <= 16:
+        # The K-min kernel at D <= 16 screens pairs with |y~|^2 - 2 x~.y~ (D FMAs) and computes the
+        # direct distance only for passing groups; frac above is against the method's direct count.
+        f = clk_mhz * 1e6
+        screen_peak = 1.0 / max(D / (nsm * FP32_LANES_PER_SM * f), 1.0 / (nsm * ALU_LANES_PER_SM * f))
+        out["screen"] = {"ops_per_pair": {"fp32": D, "xu": {}, "alu": 1}, "peak": screen_peak,
+                         "frac": achieved / screen_peak}
     return out
 
 
