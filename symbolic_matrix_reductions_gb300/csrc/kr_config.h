@@ -86,15 +86,17 @@ KR_HD constexpr int tile_points_packed(int PS2) {
     return (16384 / PS2) >= 512 ? 512 : (16384 / PS2) >= 256 ? 256 : (16384 / PS2) >= 128 ? 128
          : (16384 / PS2) >= 64 ? 64 : 32;
 }
-// Filtered K-min (D <= 4, K <= 10): the pass bits of this many consecutive point groups
-// are gathered in one word per row and queued as one entry (block index, bit mask),
-// so the scan loop itself carries no branch.
+// Filtered K-min (K <= 10): the pass bits of this many consecutive point groups are
+// gathered in one word per row and queued as one entry (block index, bit mask), so the
+// scan loop itself carries no branch.
 KR_HD constexpr int knnx_mask_groups(int DP, int KP) { return 8; }
 // Entries per row of the filtered K-min's queue (0: immediate insertion).
-KR_HD constexpr int knnx_queue(int DP, int KP) { return DP <= 4 && KP <= 10 ? 8 : 0; }
+KR_HD constexpr int knnx_queue(int DP, int KP) { return DP <= 16 && KP <= 10 ? 8 : 0; }
 // Resident blocks per SM the K-min instances are compiled for (registers cap): the
-// queued filtered instances keep at most 128 registers a thread.
-KR_HD constexpr int knn_min_blocks(int DP, int KP) { return knnx_queue(DP, KP) > 0 ? 4 : 1; }
+// queued filtered instances keep at most 128 (D <= 4), 170 (D = 8) or 255 registers.
+KR_HD constexpr int knn_min_blocks(int DP, int KP) {
+    return knnx_queue(DP, KP) > 0 ? (DP <= 4 ? 4 : DP <= 8 ? 3 : 2) : 1;
+}
 // Pair records per unrolled step of the packed inner loop.
 KR_HD constexpr int unroll_pairs(int DP) { return DP <= 8 ? 2 : 1; }
 // Tile points of an instance (value columns VP = E, K-min: 0).
