@@ -114,8 +114,9 @@ typedef struct {
 typedef enum {
     KR_PATH_AUTO = 0,         /* tensor cores where eligible, else CUDA cores */
     KR_PATH_CUDA_CORES = 1,   /* FP32 pipe: direct differences, every shape */
-    KR_PATH_TENSOR_CORES = 2  /* tcgen05 split-fp16 expansion: Gaussian Sum and LogSumExp with
-                                 E = 1, 32 <= D <= 62, no batch; ignored elsewhere.  At run
+    KR_PATH_TENSOR_CORES = 2  /* tcgen05 split-fp16 expansion: Gaussian Sum (E = 1,
+                                 32 <= D <= 62) and LogSumExp (E = 1, 32 <= D <= 61), no
+                                 batch; ignored elsewhere.  At run
                                  time it stands down to the CUDA cores when max |x'|^2 +
                                  max |y'|^2 exceeds 16 (x' = x sqrt(log2 e)/sigma), where the
                                  expansion's rounding would exceed the tolerance. */

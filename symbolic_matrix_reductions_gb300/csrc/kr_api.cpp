@@ -125,6 +125,7 @@ static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, const kr_op
     const int path = opt ? opt->path : 0, kind = opt ? opt->kernel : KR_KERNEL_GAUSSIAN;
     if ((op != OP_SUM && op != OP_LSE) || kind != KR_KERNEL_GAUSSIAN || path == KR_PATH_CUDA_CORES || !tc_dims(D, EK))
         return false;
+    if (op == OP_LSE && D > kTcLseMaxD) return false;  // the weight takes one more operand slot
     if (batch_of(opt) > 1) return false;  // the tensor-core prepass and tiles serve one problem
     return (round_up(std::max<int64_t>(M, 1), kTcRows) + round_up(std::max<int64_t>(N, 1), kTcCols)) * 256 <=
            kMaxTcOperands;
@@ -430,9 +431,10 @@ static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in
     float *part = (float *)((char *)fpad + round_up(n_pad / kTcCols * 4, 256));
     cudaError_t ce = cudaMemsetAsync(guard, 0, 256, stream);
     if (ce == cudaSuccess)
-        ce = tc_launch_prep(a.x, a.M, m_pad, a.D, a.c, true, a_hi, a_lo, guard, nullptr, nullptr, nullptr, stream);
+        ce = tc_launch_prep(a.x, a.M, m_pad, a.D, a.c, true, lse, a_hi, a_lo, guard, nullptr, nullptr, nullptr,
+                            stream);
     if (ce == cudaSuccess)
-        ce = tc_launch_prep(a.y, a.N, n_pad, a.D, a.c, false, b_hi, b_lo, guard + 1, a.b, bpad,
+        ce = tc_launch_prep(a.y, a.N, n_pad, a.D, a.c, false, lse, b_hi, b_lo, guard + 1, a.b, lse ? nullptr : bpad,
                             lse ? fpad : nullptr, stream);
     if (p.split > 1) {
         a.ws0 = part;

@@ -58,6 +58,8 @@ constexpr int kTcCols = 256;
 constexpr int kTcThreads = 320;
 // Coordinate range of the tensor-core Sum (the augmented vector must fit K = 64).
 KR_HD constexpr bool tc_dims(int D, int E) { return E == 1 && D >= 32 && D <= 62; }
+// The tensor-core LogSumExp adds the tile-relative log-weight as one more slot.
+constexpr int kTcLseMaxD = 61;
 
 // Independent partial sums of a squared distance: at large D one fma chain over the
 // coordinates is a long dependency chain (4 cycles a link) with few rows per thread to

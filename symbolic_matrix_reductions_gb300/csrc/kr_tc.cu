@@ -14,12 +14,15 @@
 // kernel leaves the work to the CUDA-core kernel launched after it (which runs only
 // in that case), without a host round trip.
 //
-// The LogSumExp (tc_lse_kernel) shares everything up to the evaluation: the prepass
-// stores each B tile's weights relative to the tile's largest, w' - F (w' = w log2 e),
-// so every term 2^(t + w' - F) is at most 1 (t <= 0 is the exponent above), and the
-// evaluation warps fold each tile's partial into a running (frame, hi, lo) per row.
-// Within the norm guard t >= -32, so the tile's largest-weight term is at least
-// 2^-32 and the partial cannot vanish while a finite weight is present.
+// The LogSumExp (tc_lse_kernel) adds the weight to the product itself: the prepass
+// gives A one more slot of 1 and B the point's log-weight relative to its tile's
+// largest, w' - F (w' = w log2 e, at least -1024, so an empty weight is a term of 0),
+// so the accumulator already holds t + w' - F <= 0 (t <= 0 is the exponent above) and
+// the evaluation reads nothing but TMEM; the warps fold each tile's partial into a
+// running (frame, hi, lo) per row.  Within the norm guard t >= -32, so the tile's
+// largest-weight term is at least 2^-32 and the partial cannot vanish while a finite
+// weight is present.  The split fp16 pair carries w' - F to 2^-21 of its size, and
+// a term whose w' - F is large is negligible beside the tile's largest.
 //
 // Block = 10 warps, one block per SM, warp-specialised around mbarriers:
 //   warp 0, one thread: TMA producer.  Loads the block's A tiles (hi, lo) once, then
@@ -188,17 +191,19 @@ __device__ __forceinline__ bool norms_ok(const unsigned *guard) {
 // zero.  guard receives the largest |.'|^2 (as float bits; non-negative floats
 // order like unsigned integers).  With b non-null, bpad[r] = b[r] (0 past `rows`).
 // ---------------------------------------------------------------------------
-// LogSumExp (fpad non-null): b holds the log-weights w; block k of 256 threads is
-// tile k of the B operands, and its frame F_k = max over the tile of w' = w log2 e
-// goes to fpad[k] while bpad[r] = w'_r - F_k <= 0 (-inf past `rows`), so every term
-// 2^(t + bpad) of the tile is at most 1 in the frame F_k.
+// LogSumExp (lse): slot D + 2 is the weight slot, 1 in A; in B (fpad non-null, b the
+// log-weights w) block k of 256 threads is tile k of the B operands, its frame
+// F_k = max over the tile of w' = w log2 e goes to fpad[k] and the slot holds
+// max(w'_r - F_k, -1024) <= 0 (-1024 past `rows`), so every term 2^(t + slot) of the
+// tile is at most 1 in the frame F_k.
 __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t rows, int64_t rows_pad, int D,
-                                                      float c, int is_x, __half *hi, __half *lo, unsigned *guard,
-                                                      const float *b, float *bpad, float *fpad) {
+                                                      float c, int is_x, int lse, __half *hi, __half *lo,
+                                                      unsigned *guard, const float *b, float *bpad, float *fpad) {
     __shared__ float wmax[8];
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= rows_pad) return;  // with fpad, rows_pad is a multiple of 256: whole blocks leave together
     const bool live = r < rows;
+    float wslot = is_x ? 1.f : 0.f;
     if (fpad) {
         const float wl = live ? 1.4426950408889634f * __ldg(b + r) : -__int_as_float(0x7f800000);
         float m = wl;
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t 
 #pragma unroll
         for (int k = 1; k < 8; ++k) F = fmaxf(F, wmax[k]);
         if (F == -__int_as_float(0x7f800000)) F = 0.f;  // no weight in the tile: any frame
-        bpad[r] = wl - F;
+        wslot = (wl - F < -1024.f) ? -1024.f : wl - F;    // a NaN weight stays NaN
         if (threadIdx.x == 0) fpad[blockIdx.x] = F;
     }
     const float *row = src + (live ? r : 0) * D;
@@ -236,6 +241,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t 
             const int k = 8 * q + e;
             float v = 0.f;
             if (live) v = k < D ? scale * __ldg(row + k) : (k == D ? v_d : (k == D + 1 ? v_d1 : 0.f));
+            if (lse && k == D + 2) v = wslot;  // dead B rows too: -1024, a term of 0
             h[e] = __float2half_rn(v);
             l[e] = __float2half_rn(v - __half2float(h[e]));
         }
@@ -355,6 +361,8 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
         const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
         for (int i = 0; i < T; ++i) {
             const int k = i & 1;
+            // LSE: the tile's frame, loaded before the wait so its latency is hidden
+            const float F = LSE ? __ldg(p.fpad + j_begin / kCols + i) : 0.f;
             if (!mbar_wait(b_accf0 + 8 * k, (i >> 1) & 1, abort, p.wait_ns)) break;
             asm volatile("tcgen05.fence::after_thread_sync;");
             uint32_t r[kEvalCols];
@@ -363,19 +371,21 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
             asm volatile("tcgen05.fence::before_thread_sync;");
             __syncwarp();
             if (lane == 0) mbar_arrive(b_acce0 + 8 * k);  // the MMAs of tile i+2 may overwrite it
-            // b of the tile's points (zero past N), or the LSE weights relative to the tile's
-            // frame (-inf past N); the same for all lanes: L1 broadcasts
-            const float4 *bv = reinterpret_cast<const float4 *>(p.bpad + j_begin + (int64_t)i * kCols + c0);
             float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+            if (LSE) {  // the accumulator holds t + w' - F: nothing else to read
 #pragma unroll
-            for (int q = 0; q < kEvalCols; q += 4) {
-                const float4 b4 = __ldg(bv + q / 4);
-                if (LSE) {
-                    p0 += ex2_approx(__uint_as_float(r[q + 0]) + b4.x);
-                    p1 += ex2_approx(__uint_as_float(r[q + 1]) + b4.y);
-                    p2 += ex2_approx(__uint_as_float(r[q + 2]) + b4.z);
-                    p3 += ex2_approx(__uint_as_float(r[q + 3]) + b4.w);
-                } else {
+                for (int q = 0; q < kEvalCols; q += 4) {
+                    p0 += ex2_approx(__uint_as_float(r[q + 0]));
+                    p1 += ex2_approx(__uint_as_float(r[q + 1]));
+                    p2 += ex2_approx(__uint_as_float(r[q + 2]));
+                    p3 += ex2_approx(__uint_as_float(r[q + 3]));
+                }
+            } else {
+                // b of the tile's points (zero past N), the same for all lanes: L1 broadcasts
+                const float4 *bv = reinterpret_cast<const float4 *>(p.bpad + j_begin + (int64_t)i * kCols + c0);
+#pragma unroll
+                for (int q = 0; q < kEvalCols; q += 4) {
+                    const float4 b4 = __ldg(bv + q / 4);
                     p0 = fmaf(ex2_approx(__uint_as_float(r[q + 0])), b4.x, p0);
                     p1 = fmaf(ex2_approx(__uint_as_float(r[q + 1])), b4.y, p1);
                     p2 = fmaf(ex2_approx(__uint_as_float(r[q + 2])), b4.z, p2);
@@ -385,8 +395,7 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
             const float pt = (p0 + p1) + (p2 + p3);
             if (!LSE) {
                 two_sum_add(hi, lo, pt);
-            } else if (pt > 0.f) {  // fold the tile (frame F) into the running (m, hi, lo)
-                const float F = __ldg(p.fpad + j_begin / kCols + i);
+            } else if (!(pt == 0.f)) {  // fold the tile (frame F) into the running (m, hi, lo)
                 const float mn = fmaxf(m, F);
                 const float so = ex2_approx(m - mn), sn = ex2_approx(F - mn);
                 hi *= so;
@@ -512,12 +521,15 @@ cudaError_t tc_set_attributes() {
     return e;
 }
 
-cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x, __half *hi,
-                           __half *lo, unsigned *guard, const float *b, float *bpad, float *fpad, cudaStream_t s) {
+cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x, bool lse,
+                           __half *hi, __half *lo, unsigned *guard, const float *b, float *bpad, float *fpad,
+                           cudaStream_t s) {
     // LSE frames: a prep block of 256 threads is one whole tile of kTcCols = 256 points
     if (fpad && rows_pad % 256) return cudaErrorInvalidValue;
+    if (lse && (D + 2 >= 64 || (!is_x && !fpad))) return cudaErrorInvalidValue;
     const unsigned blocks = (unsigned)((rows_pad + 255) / 256);
-    tc_prep_kernel<<<blocks, 256, 0, s>>>(src, rows, rows_pad, D, c, is_x ? 1 : 0, hi, lo, guard, b, bpad, fpad);
+    tc_prep_kernel<<<blocks, 256, 0, s>>>(src, rows, rows_pad, D, c, is_x ? 1 : 0, lse ? 1 : 0, hi, lo, guard, b,
+                                          bpad, fpad);
     return cudaGetLastError();
 }
 

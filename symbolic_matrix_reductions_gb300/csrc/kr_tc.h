@@ -43,9 +43,10 @@ struct TcParams {
 int tc_smem_bytes();
 int tc_occupancy();
 bool tc_available();  // the driver offers cuTensorMapEncodeTiled
-// Operand prepass.  fpad non-null (B operands of the LogSumExp): b holds the log-weights,
-// bpad receives them relative to each tile's frame and fpad the frames.
-cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x,
+// Operand prepass.  lse: the operands carry the weight slot of the LogSumExp (A: 1; B: the
+// log-weight relative to its tile's frame, which fpad receives; b holds the log-weights).
+// Otherwise bpad receives b padded with zeros.
+cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x, bool lse,
                            __half *hi, __half *lo, unsigned *guard, const float *b, float *bpad, float *fpad,
                            cudaStream_t s);
 // Opts the tensor-core kernels in to their dynamic shared memory on the current device.

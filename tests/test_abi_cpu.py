@@ -314,8 +314,11 @@ def test_tensor_core_plan(lib):
     assert q.path == kr.KR_PATH_TENSOR_CORES and (q.split, q.chunk, q.workspace_bytes) == (p.split, p.chunk,
                                                                                             p.workspace_bytes)
     for shape in [(kr.OP_SUM, 10, 10, 31, 1), (kr.OP_SUM, 10, 10, 63, 1), (kr.OP_SUM, 10, 10, 50, 2),
-                  (kr.OP_LSE, 10, 10, 50, 2), (kr.OP_GRAD, 10, 10, 50, 1), (kr.OP_MAX, 10, 10, 50, 1)]:
+                  (kr.OP_LSE, 10, 10, 50, 2), (kr.OP_GRAD, 10, 10, 50, 1), (kr.OP_MAX, 10, 10, 50, 1),
+                  (kr.OP_LSE, 10, 10, 62, 1)]:     # the LogSumExp's weight slot leaves D <= 61
         assert kr.plan(*shape).path == kr.KR_PATH_CUDA_CORES, shape
+    assert kr.plan(kr.OP_SUM, 10, 10, 62, 1).path == kr.KR_PATH_TENSOR_CORES
+    assert kr.plan(kr.OP_LSE, 10, 10, 61, 1).path == kr.KR_PATH_TENSOR_CORES
     assert kr.plan(kr.OP_SUM, 10, 10, 50, 1, path=kr.KR_PATH_CUDA_CORES).path == kr.KR_PATH_CUDA_CORES
     assert kr.plan(kr.OP_SUM, 10, 2560, 50, 1, split=5).split == 5
     assert kr.plan(kr.OP_SUM, 10, 2000, 50, 1, split=5).split == 4   # 512-point chunks

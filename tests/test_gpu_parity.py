@@ -294,16 +294,20 @@ def test_tensor_core_sum(orc, M, N, D, sigma, split):
     check_sum(_np(a), a_ref, S_ref, f"tc {M}x{N} D{D} S{split}")
 
 
-@pytest.mark.parametrize("M,N,D,sigma,split", TC_CASES)
+@pytest.mark.parametrize("M,N,D,sigma,split", TC_CASES + [(200, 3000, 61, 1.2, 2)])
 def test_tensor_core_lse(orc, M, N, D, sigma, split):
-    """The LogSumExp on the tensor cores (tile frames from the weights' maximum), with
-    weights spread over many orders of magnitude and some -inf (weight 0)."""
+    """The LogSumExp on the tensor cores (the weight relative to its tile's frame is one more
+    operand slot, so D <= 61; D = 62 takes the CUDA cores), with weights spread over many
+    orders of magnitude, some -inf (weight 0) and some so small that they leave the
+    operand's range (clamped to 2^-1024 of the tile's largest)."""
     r = _rng(M + 3 * N + D)
     x = (r.standard_normal((M, D)) / np.sqrt(D)).astype(np.float32)
     y = (r.standard_normal((N, D)) / np.sqrt(D)).astype(np.float32)
     w = (4.0 * r.standard_normal((N, 1))).astype(np.float32)
     w[r.random((N, 1)) < 0.05] = -np.inf
-    assert kr.plan_device(kr.OP_LSE, M, N, D, 1).path == kr.KR_PATH_TENSOR_CORES
+    w[r.random((N, 1)) < 0.02] = -3000.0
+    tc = D <= 61
+    assert (kr.plan_device(kr.OP_LSE, M, N, D, 1).path == kr.KR_PATH_TENSOR_CORES) == tc
     L = kr.kernel_reduce(*_dev(x, y, w), sigma, "lse", split=split, path=kr.KR_PATH_TENSOR_CORES)
     check_lse(_np(L), orc.gauss_lse(x, y, w, sigma), f"tc lse {M}x{N} D{D} S{split}")
 
