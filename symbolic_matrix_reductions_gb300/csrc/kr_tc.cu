@@ -36,9 +36,12 @@
 //     as wide as TMEM allows: 12 MMAs per handshake.
 //   warps 2-9: evaluation.  Warp w reads TMEM lanes 32 (w mod 4)..+31 (its rows);
 //     warps w and w+4 take the two 128-column halves of the tile.  Each loads its
-//     half in one TMEM load, releases the accumulator (the MMAs of tile i+2 may then
-//     overwrite it), computes 2^t and accumulates b_j 2^t, with b_j read through
-//     the L1 cache.
+//     half, releases the accumulator (the MMAs of tile i+2 may then overwrite it),
+//     computes 2^t and accumulates b_j 2^t.  The Sum loads in the 16x256b shape (a
+//     thread holds 4 rows x 32 columns), so a thread reads b at 32 columns only (the
+//     prepass stores them contiguously; L1 broadcasts) and adds column pairs with
+//     f32x2 FMAs; the four lanes that share rows are combined at the end.  The
+//     LogSumExp loads one row per lane (32x32b) and reads nothing else.
 // Every mbarrier wait is bounded (by global time, default 2 s, and a poll count); a
 // role that gives up raises a block-wide abort flag, and every role then leaves its
 // loop; the producer and the MMA issuer then wait (bounded) for their copies and MMAs
@@ -174,6 +177,15 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
         : "memory");
 }
 
+// One warp reads 128 consecutive fp32 columns of 16 TMEM lanes (from lane base B) in
+// the 16x256b shape: register 4k + 2h + e of thread t holds lane B + t/4 + 8h, column
+// 8k + 2(t%4) + e (k < 16; h, e < 2).
+__device__ __forceinline__ void tmem_ld16x256_x16(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+                 : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31]),"=r"(r[32]),"=r"(r[33]),"=r"(r[34]),"=r"(r[35]),"=r"(r[36]),"=r"(r[37]),"=r"(r[38]),"=r"(r[39]),"=r"(r[40]),"=r"(r[41]),"=r"(r[42]),"=r"(r[43]),"=r"(r[44]),"=r"(r[45]),"=r"(r[46]),"=r"(r[47]),"=r"(r[48]),"=r"(r[49]),"=r"(r[50]),"=r"(r[51]),"=r"(r[52]),"=r"(r[53]),"=r"(r[54]),"=r"(r[55]),"=r"(r[56]),"=r"(r[57]),"=r"(r[58]),"=r"(r[59]),"=r"(r[60]),"=r"(r[61]),"=r"(r[62]),"=r"(r[63])
+                 : "r"(taddr));
+}
+
 // One warp reads 128 consecutive fp32 columns of its 32 TMEM lanes (one row per lane).
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];"
@@ -227,7 +239,15 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t 
         }
         atomicMax(guard, __float_as_uint(n));
     }
-    if (bpad && !fpad) bpad[r] = live ? __ldg(b + r) : 0.f;
+    if (bpad && !fpad) {
+        // Sum: b in the order the evaluation threads read it.  Column c of a 256-point tile
+        // is c0 + 8 kk + 2 q + e (c0 = 0 or 128, kk < 16, q < 4, e < 2) and thread q of each
+        // quad of lanes takes columns c0 + 8 kk + 2 q + e, so it goes to c0 + 32 q + 2 kk + e:
+        // one thread's 32 values are contiguous.
+        const int64_t c = r % kCols, hv = c / 128, cc = c % 128;
+        const int64_t dst = (r - c) + 128 * hv + 32 * ((cc % 8) / 2) + 2 * (cc / 8) + (cc % 2);
+        bpad[dst] = live ? __ldg(b + r) : 0.f;
+    }
     const float scale = is_x ? 2.f * c : c;
     const float v_d = is_x ? -n : 1.f, v_d1 = is_x ? -1.f : n;
     uint4 *ph = reinterpret_cast<uint4 *>(hi + r * 64);
@@ -301,8 +321,9 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
     asm volatile("tcgen05.fence::after_thread_sync;");
     const uint32_t tmem = tmem_slot;
 
-    float hi = 0.f, lo = 0.f;
-    float m = -__int_as_float(0x7f800000);  // LSE: the frame of (hi, lo), base 2
+    // running compensated sums: Sum, four rows a thread (hs[h], ls[h]); LSE, one row (hs[0], ls[0])
+    float hs[4] = {0.f, 0.f, 0.f, 0.f}, ls[4] = {0.f, 0.f, 0.f, 0.f};
+    float m = -__int_as_float(0x7f800000);  // LSE: the frame of (hs[0], ls[0]), base 2
     if (w == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0 && T > 0) {
@@ -365,14 +386,15 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
             const float F = LSE ? __ldg(p.fpad + j_begin / kCols + i) : 0.f;
             if (!mbar_wait(b_accf0 + 8 * k, (i >> 1) & 1, abort, p.wait_ns)) break;
             asm volatile("tcgen05.fence::after_thread_sync;");
-            uint32_t r[kEvalCols];
-            tmem_ld128(tmem + lanes + (uint32_t)(k * kCols + c0), r);  // one load, one wait
-            asm volatile("tcgen05.wait::ld.sync.aligned;");
-            asm volatile("tcgen05.fence::before_thread_sync;");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_acce0 + 8 * k);  // the MMAs of tile i+2 may overwrite it
-            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-            if (LSE) {  // the accumulator holds t + w' - F: nothing else to read
+            if (LSE) {
+                // one row per lane (32x32b), the accumulator holds t + w' - F: nothing else to read
+                uint32_t r[kEvalCols];
+                tmem_ld128(tmem + lanes + (uint32_t)(k * kCols + c0), r);  // one load, one wait
+                asm volatile("tcgen05.wait::ld.sync.aligned;");
+                asm volatile("tcgen05.fence::before_thread_sync;");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_acce0 + 8 * k);  // the MMAs of tile i+2 may overwrite it
+                float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
                 for (int q = 0; q < kEvalCols; q += 4) {
                     p0 += ex2_approx(__uint_as_float(r[q + 0]));
@@ -380,28 +402,49 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
                     p2 += ex2_approx(__uint_as_float(r[q + 2]));
                     p3 += ex2_approx(__uint_as_float(r[q + 3]));
                 }
-            } else {
-                // b of the tile's points (zero past N), the same for all lanes: L1 broadcasts
-                const float4 *bv = reinterpret_cast<const float4 *>(p.bpad + j_begin + (int64_t)i * kCols + c0);
-#pragma unroll
-                for (int q = 0; q < kEvalCols; q += 4) {
-                    const float4 b4 = __ldg(bv + q / 4);
-                    p0 = fmaf(ex2_approx(__uint_as_float(r[q + 0])), b4.x, p0);
-                    p1 = fmaf(ex2_approx(__uint_as_float(r[q + 1])), b4.y, p1);
-                    p2 = fmaf(ex2_approx(__uint_as_float(r[q + 2])), b4.z, p2);
-                    p3 = fmaf(ex2_approx(__uint_as_float(r[q + 3])), b4.w, p3);
+                const float pt = (p0 + p1) + (p2 + p3);
+                if (!(pt == 0.f)) {  // fold the tile (frame F) into the running (m, hi, lo)
+                    const float mn = fmaxf(m, F);
+                    const float so = ex2_approx(m - mn), sn = ex2_approx(F - mn);
+                    hs[0] *= so;
+                    ls[0] *= so;
+                    two_sum_add(hs[0], ls[0], pt * sn);
+                    m = mn;
                 }
-            }
-            const float pt = (p0 + p1) + (p2 + p3);
-            if (!LSE) {
-                two_sum_add(hi, lo, pt);
-            } else if (!(pt == 0.f)) {  // fold the tile (frame F) into the running (m, hi, lo)
-                const float mn = fmaxf(m, F);
-                const float so = ex2_approx(m - mn), sn = ex2_approx(F - mn);
-                hi *= so;
-                lo *= so;
-                two_sum_add(hi, lo, pt * sn);
-                m = mn;
+            } else {
+                // four rows per thread (two 16x256b loads): rows 32 quarter + t/4 + 8 h (+16 for
+                // the second load), columns c0 + 8 kk + 2 (t%4) + e; so a thread needs b at only
+                // its 32 columns
+                uint32_t r0[64], r1[64];
+                tmem_ld16x256_x16(tmem + lanes + (uint32_t)(k * kCols + c0), r0);
+                tmem_ld16x256_x16(tmem + lanes + (16u << 16) + (uint32_t)(k * kCols + c0), r1);
+                asm volatile("tcgen05.wait::ld.sync.aligned;");
+                asm volatile("tcgen05.fence::before_thread_sync;");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_acce0 + 8 * k);  // the MMAs of tile i+2 may overwrite it
+                // b of this thread's 32 columns, stored contiguously by the prepass
+                const float4 *bv =
+                    reinterpret_cast<const float4 *>(p.bpad + j_begin + (int64_t)i * kCols + c0 + 32 * (lane & 3));
+                float2 acc[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) acc[h] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    float4 b4;
+                    if ((kk & 1) == 0) b4 = __ldg(bv + kk / 2);
+                    const float2 b2 = (kk & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float2 e0 = make_float2(ex2_approx(__uint_as_float(r0[4 * kk + 2 * h])),
+                                                      ex2_approx(__uint_as_float(r0[4 * kk + 2 * h + 1])));
+                        const float2 e1 = make_float2(ex2_approx(__uint_as_float(r1[4 * kk + 2 * h])),
+                                                      ex2_approx(__uint_as_float(r1[4 * kk + 2 * h + 1])));
+                        acc[h] = __ffma2_rn(e0, b2, acc[h]);
+                        acc[2 + h] = __ffma2_rn(e1, b2, acc[2 + h]);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 4; ++h) two_sum_add(hs[h], ls[h], acc[h].x + acc[h].y);
             }
         }
     }
@@ -409,21 +452,43 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
     __syncthreads();
     const bool ok = !*abort;
     if (!ok && t == 0) atomicOr(&g_tc_status, 1u);
-    // warps 6..9 hand their row sums (and LSE frames) to warps 2..5 through the idle A tile
     float *red = reinterpret_cast<float *>(smem);
+    if (!LSE && w >= 2) {
+        // the four lanes t^1, t^2, t^3 hold the same rows: combine them in a fixed order
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1)
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float h2 = __shfl_xor_sync(0xffffffffu, hs[h], o), l2 = __shfl_xor_sync(0xffffffffu, ls[h], o);
+                two_sum_add(hs[h], ls[h], h2);
+                ls[h] += l2;
+            }
+    }
+    // warps 6..9 hand their row sums (and LSE frames) to warps 2..5 through the idle A tile
     if (w >= 6) {
-        red[32 * (w & 3) + lane] = hi;
-        red[kRows + 32 * (w & 3) + lane] = lo;
-        red[2 * kRows + 32 * (w & 3) + lane] = m;
+        if (LSE) {
+            red[32 * (w & 3) + lane] = hs[0];
+            red[kRows + 32 * (w & 3) + lane] = ls[0];
+            red[2 * kRows + 32 * (w & 3) + lane] = m;
+        } else if ((lane & 3) == 0) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int rl = 32 * (w & 3) + (lane >> 2) + 8 * h;
+                red[rl] = hs[h];
+                red[kRows + rl] = ls[h];
+            }
+        }
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
     if (w == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 
-    if (w >= 2 && w < 6) {
+    const float nan = __int_as_float(0x7fc00000);
+    if (LSE && w >= 2 && w < 6) {
         const int rl = 32 * (w & 3) + lane;
+        float hi = hs[0], lo = ls[0];
         float h2 = red[rl], l2 = red[kRows + rl];
-        if (LSE) {  // bring both halves to the larger frame
+        {  // bring both halves to the larger frame
             const float m2 = red[2 * kRows + rl], mn = fmaxf(m, m2);
             const float s1 = mn == -__int_as_float(0x7f800000) ? 0.f : ex2_approx(m - mn);
             const float s2 = mn == -__int_as_float(0x7f800000) ? 0.f : ex2_approx(m2 - mn);
@@ -437,24 +502,33 @@ __device__ __forceinline__ void tc_body(const TcParams &p) {
         lo += l2;
         const int64_t i = row0 + rl;
         if (i < p.M) {
-            const float nan = __int_as_float(0x7fc00000);
             const int64_t o = (int64_t)blockIdx.y * p.M + i;
-            if (!LSE) {
+            // the CUDA-core LogSumExp's output and partials: L = ln 2 (m + log2 tot); (m, tot)
+            const float tot = hi + lo;
+            const float ninf = -__int_as_float(0x7f800000);
+            if (p.S == 1) {
+                p.out[i] = !ok ? nan : tot > 0.f ? (float)(0.6931471805599453 * ((double)m + log2((double)tot))) : ninf;
+            } else {
+                p.ws0[o] = !ok ? nan : tot > 0.f ? m : ninf;
+                p.ws1[o] = ok ? tot : 0.f;
+            }
+        }
+    }
+    if (!LSE && w >= 2 && w < 6 && (lane & 3) == 0) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int rl = 32 * (w & 3) + (lane >> 2) + 8 * h;
+            float hi = hs[h], lo = ls[h];
+            two_sum_add(hi, lo, red[rl]);
+            lo += red[kRows + rl];
+            const int64_t i = row0 + rl;
+            if (i < p.M) {
+                const int64_t o = (int64_t)blockIdx.y * p.M + i;
                 if (p.S == 1) {
                     p.out[i] = ok ? hi + lo : nan;
                 } else {
                     p.ws0[o] = ok ? hi : nan;
                     p.ws1[o] = ok ? lo : 0.f;
-                }
-            } else {
-                // the CUDA-core LogSumExp's output and partials: L = ln 2 (m + log2 tot); (m, tot)
-                const float tot = hi + lo;
-                const float ninf = -__int_as_float(0x7f800000);
-                if (p.S == 1) {
-                    p.out[i] = !ok ? nan : tot > 0.f ? (float)(0.6931471805599453 * ((double)m + log2((double)tot))) : ninf;
-                } else {
-                    p.ws0[o] = !ok ? nan : tot > 0.f ? m : ninf;
-                    p.ws1[o] = ok ? tot : 0.f;
                 }
             }
         }
