@@ -366,7 +366,7 @@ def run_ours(args, rank, world, local_rank):
         "wall_s_timed": t_wall,
     }
     line["e2e"] = e2e_line
-    if world == 1:
+    if world == 1 and not args.no_secondary:
         line["secondary"] = secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev)
         line["cpu_baseline"] = cpu_baseline(inp, s, target_s=args.cpu_seconds)
     return line
@@ -606,6 +606,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the CPU baseline sample")
     ap.add_argument("--size", type=lambda v: tuple(int(t) for t in v.split(",")), default=None,
                     help="M,N: the workload's distributions at another size (e.g. a smaller case to profile)")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="only the step (no secondary lines, no CPU baseline): a short command to profile")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3   # at least three warm-up steps
