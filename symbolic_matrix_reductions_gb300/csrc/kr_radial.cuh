@@ -24,6 +24,8 @@
 // b = NaN: k NaN is NaN, which neither wins a comparison nor survives fmaxf.
 #pragma once
 
+#include <type_traits>
+
 #include "kr_kernels_packed.cuh"
 
 namespace kr {
@@ -64,9 +66,10 @@ template <int L> struct Lanes;
 template <> struct Lanes<1> {
     typedef float T;
     static __device__ __forceinline__ T splat(float v) { return v; }
-    static __device__ __forceinline__ T add(T a, T b) { return a + b; }
-    static __device__ __forceinline__ T mul(T a, T b) { return a * b; }
-    static __device__ __forceinline__ T fma(T a, T b, T c) { return fmaf(a, b, c); }
+    // explicitly rounded, so no context contracts them differently (Max recomputes values)
+    static __device__ __forceinline__ T add(T a, T b) { return __fadd_rn(a, b); }
+    static __device__ __forceinline__ T mul(T a, T b) { return __fmul_rn(a, b); }
+    static __device__ __forceinline__ T fma(T a, T b, T c) { return __fmaf_rn(a, b, c); }
     static __device__ __forceinline__ float lane(T v, int) { return v; }
     static __device__ __forceinline__ float hmax(T v) { return v; }
     static __device__ __forceinline__ float hsum(T v) { return v; }
@@ -107,6 +110,36 @@ __device__ __forceinline__ void radial_load(const float *rec, typename Lanes<L>:
         load_record<PS>(rec, pv);
 }
 
+// Max, dense mode, E = 1: steps per block of the running-maximum test.  A larger block
+// tests less often but recomputes more points when a lane's maximum rose (and some lane
+// of a warp usually does in each tile).
+KR_HD constexpr int radial_max_block(int KT) { return 2; }
+
+// k of a row (coordinates xr, prescaled) against the L points of a record: the distance
+// summed in dist_chains(DP) interleaved chains, then the kernel.  Max recomputes values
+// with it, so the scan and the recomputation give the same bits.
+template <int DP, int L, int PS, int KT>
+__device__ __forceinline__ typename Lanes<L>::T radial_k(const typename Lanes<L>::T (&xr)[DP],
+                                                         const typename Lanes<L>::T (&pv)[PS / L]) {
+    typedef Lanes<L> V;
+    typedef typename V::T T;
+    constexpr int NC = dist_chains(DP);  // interleaved partial sums
+    T qc[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) qc[c] = V::splat(c == 0 ? radial_q0<KT>() : 0.f);
+#pragma unroll
+    for (int d = 0; d < DP; ++d) {
+        const T df = V::add(xr[d], pv[d]);
+        const int c = d % NC;
+        const bool first = d < NC && !(c == 0 && radial_q0<KT>() != 0.f);
+        qc[c] = first ? V::mul(df, df) : V::fma(df, df, qc[c]);
+    }
+    T q = qc[0];
+#pragma unroll
+    for (int c = 1; c < NC; ++c) q = V::add(q, qc[c]);
+    return V::template kval<KT>(q);
+}
+
 template <int DP, int EP, int R, int BN, int KT, int RED>
 __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
     const Args a = batch_view(a_);
@@ -116,7 +149,11 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
     constexpr int PS = radial_stride(DP, EP);
     constexpr int UPT = radial_step(DP);      // points per step
     constexpr int UR = UPT / L;                // records per step
-    static_assert(BN % UPT == 0, "tile must be a multiple of the step");
+    // Max, dense mode, E = 1: the running maximum is tested once per block of IB steps
+    // (wider signals keep the per-step walk: the block state would not fit in registers)
+    constexpr bool kBlockMax = RED == RR_MAX && EP == 1;
+    constexpr int IB = radial_max_block(KT);
+    static_assert(BN % (IB * UPT) == 0, "tile must be a multiple of the step and of the block");
     __shared__ __align__(16) float tile[(BN / L) * PS];
 
     const int t = threadIdx.x;
@@ -125,6 +162,9 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
     // need not be in increasing j, so Max/Min then breaks ties on the index itself;
     // with S splits, split blockIdx.y takes every S-th tile of the ranges.
     const bool ranged = a.blk != nullptr;
+    // tiles are padded to whole steps, and for the dense Max to whole blocks of IB steps
+    // (padding points carry b = NaN there, which never wins)
+    const int BPT = (kBlockMax && !ranged) ? IB * UPT : UPT;
     int64_t row0 = (int64_t)blockIdx.x * (kThreads * R), row_end = a.M;
     int r_lo = 0, r_hi = 1;
     if (ranged) {
@@ -156,6 +196,7 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
     T part[R][EP];
     float hi[R][EP], lo[R][EP];  // Sum: compensated running pair; Max: best value, unused
     int bj[R][EP];               // Max: index of the best value
+    int last[R][EP];             // Max, dense mode: the tile step that last raised it (-1: none)
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -164,6 +205,7 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
             hi[r][e] = RED == RR_MAX ? -f_inf() : 0.f;
             lo[r][e] = 0.f;
             bj[r][e] = -1;
+            last[r][e] = -1;
         }
 
     int tk = 0;  // block-sparse: tiles seen over the block's ranges; split y takes tk = y mod S
@@ -173,7 +215,7 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
     for (int64_t jt = js; jt < je; jt += BN) {
         if (ranged && (tk++ % a.S) != (int)blockIdx.y) continue;  // uniform across the block
         const int nv = (int)min((int64_t)BN, je - jt);
-        const int nvp = (nv + UPT - 1) / UPT * UPT;
+        const int nvp = (nv + BPT - 1) / BPT * BPT;
         __syncthreads();  // every thread is done with the previous tile
         for (int p = t; p < nvp; p += kThreads) {
             if (p < nv) {
@@ -199,29 +241,20 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
         }
         __syncthreads();  // tile staged
 
-        for (int jj = 0; jj < nvp; jj += UPT) {
-            T kv[UR][R][EP];
+        // One pass over the tile.  Max, dense mode, E = 1: no branch in the pass; the
+        // running maximum and the last block of IB steps that raised it are kept (one test
+        // per block), and that block is recomputed after the pass to find the index
+        // (strictly greater raises it, so ties keep the lowest j).  Otherwise (block-sparse
+        // mode, whose ranges come in any order, or E > 1) a raising or tying step walks its
+        // points at once and ties break on the index.
+        auto eval_step = [&](int jj, T (&kv)[UR][R][EP]) {
 #pragma unroll
             for (int u = 0; u < UR; ++u) {
                 T pv[PS / L];
                 radial_load<L, PS>(tile + (jj / L + u) * PS, pv);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    constexpr int NC = dist_chains(DP);  // interleaved partial sums
-                    T qc[NC];
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) qc[c] = V::splat(c == 0 ? radial_q0<KT>() : 0.f);
-#pragma unroll
-                    for (int d = 0; d < DP; ++d) {
-                        const T df = V::add(xr[r][d], pv[d]);
-                        const int c = d % NC;
-                        const bool first = d < NC && !(c == 0 && radial_q0<KT>() != 0.f);
-                        qc[c] = first ? V::mul(df, df) : V::fma(df, df, qc[c]);
-                    }
-                    T q = qc[0];
-#pragma unroll
-                    for (int c = 1; c < NC; ++c) q = V::add(q, qc[c]);
-                    const T k = V::template kval<KT>(q);
+                    const T k = radial_k<DP, L, PS, KT>(xr[r], pv);
 #pragma unroll
                     for (int e = 0; e < EP; ++e) {
                         if (RED == RR_SUM)
@@ -231,7 +264,14 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
                     }
                 }
             }
-            if (RED == RR_MAX) {
+        };
+        if constexpr (RED == RR_SUM) {
+            T kv[UR][R][EP];
+            for (int jj = 0; jj < nvp; jj += UPT) eval_step(jj, kv);
+        } else if (!kBlockMax || ranged) {
+            for (int jj = 0; jj < nvp; jj += UPT) {
+                T kv[UR][R][EP];
+                eval_step(jj, kv);
 #pragma unroll
                 for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -239,14 +279,14 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
                         float m = V::hmax(kv[0][r][e]);
 #pragma unroll
                         for (int u = 1; u < UR; ++u) m = fmaxf(m, V::hmax(kv[u][r][e]));
-                        if (m > hi[r][e] || (ranged && m == hi[r][e])) {  // rare: walk the step's points
+                        if (m >= hi[r][e]) {  // rare: walk the step's points
 #pragma unroll
                             for (int u = 0; u < UR; ++u)
 #pragma unroll
                                 for (int l = 0; l < L; ++l) {
                                     const float f = V::lane(kv[u][r][e], l);
                                     const int j = (int)(jt + jj + u * L + l);
-                                    if (f > hi[r][e] || (ranged && f == hi[r][e] && j < bj[r][e])) {
+                                    if (f > hi[r][e] || (f == hi[r][e] && j < bj[r][e])) {
                                         hi[r][e] = f;
                                         bj[r][e] = j;
                                     }
@@ -254,6 +294,55 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
                         }
                     }
             }
+        } else if constexpr (kBlockMax) {
+            for (int jb = 0; jb < nvp; jb += IB * UPT) {
+                float bm[R][EP];
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int e = 0; e < EP; ++e) bm[r][e] = -f_inf();
+#pragma unroll
+                for (int g = 0; g < IB; ++g) {
+                    T kv[UR][R][EP];
+                    eval_step(jb + g * UPT, kv);
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+#pragma unroll
+                        for (int e = 0; e < EP; ++e)
+#pragma unroll
+                            for (int u = 0; u < UR; ++u) bm[r][e] = fmaxf(bm[r][e], V::hmax(kv[u][r][e]));
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int e = 0; e < EP; ++e) {
+                        last[r][e] = bm[r][e] > hi[r][e] ? jb : last[r][e];
+                        hi[r][e] = fmaxf(hi[r][e], bm[r][e]);
+                    }
+            }
+            // the index of each raised maximum: the first point of its last raising block
+            // whose recomputed value equals it
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int e = 0; e < EP; ++e) {
+                    const int jb = last[r][e];
+                    if (jb < 0) continue;
+                    last[r][e] = -1;
+                    bool found = false;
+                    for (int u = 0; u < IB * UR; ++u) {
+                        T pv[PS / L];
+                        radial_load<L, PS>(tile + (jb / L + u) * PS, pv);
+                        const T f = V::mul(radial_k<DP, L, PS, KT>(xr[r], pv), pv[DP + e]);
+#pragma unroll
+                        for (int l = 0; l < L; ++l) {
+                            if (!found && V::lane(f, l) == hi[r][e]) {
+                                bj[r][e] = (int)(jt + jb + u * L + l);
+                                found = true;
+                            }
+                        }
+                    }
+                }
         }
         if (RED == RR_SUM) {
 #pragma unroll
