@@ -24,8 +24,6 @@
 // b = NaN: k NaN is NaN, which neither wins a comparison nor survives fmaxf.
 #pragma once
 
-#include <type_traits>
-
 #include "kr_kernels_packed.cuh"
 
 namespace kr {
