@@ -43,7 +43,7 @@ KR_HD constexpr int rows_grad(int DP, int EP) {
     return DP <= 4 ? (EP == 1 ? 4 : EP == 4 ? 2 : 1) : DP <= 8 ? (EP == 1 ? 2 : 1) : 1;
 }
 KR_HD constexpr int rows_knn(int DP, int KP) {
-    return DP <= 4 ? (KP <= 10 ? 4 : KP == 16 ? 2 : 1) : DP <= 16 ? (KP <= 10 ? 2 : 1) : 1;
+    return DP <= 4 ? (KP <= 10 ? 4 : 2) : DP <= 16 ? 2 : 1;
 }
 
 // Tensor-core Sum: largest |x'|^2 + |y'|^2 (prescaled, base-2 exponent units) for
@@ -88,16 +88,17 @@ KR_HD constexpr int tile_points_packed(int PS2) {
     return (16384 / PS2) >= 512 ? 512 : (16384 / PS2) >= 256 ? 256 : (16384 / PS2) >= 128 ? 128
          : (16384 / PS2) >= 64 ? 64 : 32;
 }
-// Filtered K-min (K <= 10): the pass bits of this many consecutive point groups are
-// gathered in one word per row and queued as one entry (block index, bit mask), so the
-// scan loop itself carries no branch.
+// Filtered K-min: the pass bits of this many consecutive point groups are gathered in one
+// word per row and queued as one entry (block index, bit mask), so the scan loop itself
+// carries no branch.
 KR_HD constexpr int knnx_mask_groups(int DP, int KP) { return 8; }
 // Entries per row of the filtered K-min's queue (0: immediate insertion).
-KR_HD constexpr int knnx_queue(int DP, int KP) { return DP <= 16 && KP <= 10 ? 8 : 0; }
+KR_HD constexpr int knnx_queue(int DP, int KP) { return DP <= 16 ? 8 : 0; }
 // Resident blocks per SM the K-min instances are compiled for (registers cap): the
-// queued filtered instances keep at most 128 (D <= 4), 170 (D = 8) or 255 registers.
+// queued filtered instances keep at most 128 (D <= 4, K <= 16), 170 (D = 8, K <= 16) or
+// 255 registers (D = 16, or two rows of 32-entry lists).
 KR_HD constexpr int knn_min_blocks(int DP, int KP) {
-    return knnx_queue(DP, KP) > 0 ? (DP <= 4 ? 4 : DP <= 8 ? 3 : 2) : 1;
+    return knnx_queue(DP, KP) > 0 ? (DP <= 4 ? (KP <= 16 ? 4 : 2) : DP <= 8 ? (KP <= 16 ? 3 : 2) : 2) : 1;
 }
 // Pair records per unrolled step of the packed inner loop.
 KR_HD constexpr int unroll_pairs(int DP) { return DP <= 8 ? 2 : 1; }

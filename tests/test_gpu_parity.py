@@ -89,7 +89,9 @@ def test_grad_small(orc, M, N, D, E, sigma, split):
 KNN_SMALL = [
     (1, 1, 3, 1, 0), (33, 7, 3, 10, 0), (513, 1537, 3, 10, 0), (513, 1537, 3, 10, 6), (300, 2000, 16, 10, 0),
     (300, 2000, 16, 10, 3), (200, 900, 1, 4, 0), (100, 700, 5, 3, 0), (90, 1000, 50, 16, 2), (70, 300, 128, 32, 0),
-    (64, 100, 8, 1, 0), (64, 100, 8, 1, 4), (50, 20, 2, 32, 0),   # last: K > N
+    (64, 100, 8, 1, 0), (64, 100, 8, 1, 4), (50, 20, 2, 32, 0),   # K > N
+    (300, 2000, 16, 32, 0), (200, 1500, 8, 32, 3), (300, 2000, 16, 16, 2), (250, 1800, 3, 32, 2),
+    (260, 1700, 4, 16, 0),   # two rows a thread with 16- and 32-entry lists
 ]
 
 
