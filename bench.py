@@ -81,12 +81,15 @@ ALU_LANES_PER_SM = 64     # integer/compare pipe: 4 partitions x 16 lanes
 
 # DRAM traffic per launch from ncu captures (profiles/), keyed by kernel and the
 # hash of the kernel source it was taken on; stale entries report null.
-TRAFFIC = {}
+TRAFFIC = {
+    # profiles/grad2_kernel_d3_gauss_d3.md: dram__bytes_read.sum + dram__bytes_write.sum
+    "grad_kernel[D=3,E=1]": {"bytes_per_launch": 3221504, "source_hash": "52c0ebcb93d10c42"},
+}
 
 
 def _kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("kr_kernels.cuh", "kr_config.h"):
+    for f in ("kr_kernels.cuh", "kr_kernels_packed.cuh", "kr_config.h"):
         with open(os.path.join(ROOT, "symbolic_matrix_reductions_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
