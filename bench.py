@@ -29,6 +29,7 @@ job value is N times the per-step pairs over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+from concurrent.futures import ThreadPoolExecutor
 import ctypes
 import hashlib
 import json
@@ -414,11 +415,24 @@ def e2e(torch, kr, inp, s, args, world):
     idx = torch.empty((M, K_NN), dtype=torch.int32).pin_memory()
     dist_ = torch.empty((M, K_NN)).pin_memory()
 
+    # As in the device-timed step, the four independent calls run at once: one host thread and
+    # one stream each (the calls release the GIL and return when their outputs are in host memory).
+    calls = [lambda: kr.kernel_knn(xc, yc, K_NN, idx=idx, dist=dist_),
+             lambda: kr.kernel_reduce_grad_x(xc, yc, bc, gc, s, out=gx),
+             lambda: kr.kernel_reduce(xc, yc, bc, s, "sum", out=a),
+             lambda: kr.kernel_reduce(xc, yc, bc, s, "lse", out=L)]
+    dev = torch.cuda.current_device()
+    streams = [torch.cuda.Stream(dev) for _ in calls]
+
+    def on_stream(k):
+        with torch.cuda.stream(streams[k]):
+            calls[k]()
+
+    pool = ThreadPoolExecutor(max_workers=len(calls))
+
     def step():
-        kr.kernel_reduce(xc, yc, bc, s, "sum", out=a)
-        kr.kernel_reduce(xc, yc, bc, s, "lse", out=L)
-        kr.kernel_reduce_grad_x(xc, yc, bc, gc, s, out=gx)
-        kr.kernel_knn(xc, yc, K_NN, idx=idx, dist=dist_)
+        for f in [pool.submit(on_stream, k) for k in range(len(calls))]:
+            f.result()
 
     nb = lambda t: t.numel() * t.element_size()
     h2d = 4 * (nb(xc) + nb(yc)) + 3 * nb(bc) + nb(gc)
@@ -432,8 +446,11 @@ def e2e(torch, kr, inp, s, args, world):
     for _ in range(steps):
         step()
     t = slowest_rank((time.perf_counter() - t0) / steps, world)
+    pool.shutdown()
     return {"value": world * 4 * M * N / t, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": t * 1e3, "steps": steps, "timer": "host perf_counter; each call blocks on host outputs"}
+            "ms_per_step": t * 1e3, "steps": steps,
+            "timer": "host perf_counter; the four calls on four host threads and streams, each blocking on "
+                     "its host outputs"}
 
 
 def _time_op(torch, fn, reps):
