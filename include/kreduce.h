@@ -276,8 +276,8 @@ const char *kr_status_string(int status);
 int kr_last_cuda_error(void);
 
 /*
- * Sticky device status of the calling thread's current device (no counterpart on the
- * pages; failure detection of this build).  Every wait of the tensor-core kernels on
+ * Sticky device status of the calling thread's current device (failure detection; no
+ * counterpart on the pages).  Every wait of the tensor-core kernels on
  * their mbarriers is bounded (2 s of global time by default); a block whose wait gives
  * up writes NaN for its rows and sets bit 0 of this status.  Reads the status into
  * *status (0 = nothing happened since the last clear) and clears it when `clear` is
