@@ -400,7 +400,9 @@ def run_ours(args, rank, world, local_rank):
     line["e2e"] = e2e_line
     if world == 1 and not args.no_secondary:
         line["secondary"] = secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev)
-        line["cpu_baseline"] = cpu_baseline(inp, s, target_s=args.cpu_seconds)
+        line["cpu_baseline"], ref = cpu_baseline(inp, s, target_s=args.cpu_seconds)
+        # the step's outputs (last pass) on the oracle's rows
+        line["parity"] = parity_stats(ref, *(t.cpu().numpy() for t in (a, L, gx, idx, dist_)))
     return line
 
 
@@ -585,10 +587,38 @@ def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
 # ---------------------------------------------------------------------------
 def _oracle_step(orc, inp, s, rows):
     x = inp["x"][rows]
-    orc.gauss_sum(x, inp["y"], inp["b"], s)
-    orc.gauss_lse(x, inp["y"], inp["b"], s)
-    orc.gauss_grad_x(x, inp["y"], inp["b"], inp["g"][rows], s)
-    orc.knn(x, inp["y"], K_NN)
+    return {"sum": orc.gauss_sum(x, inp["y"], inp["b"], s),
+            "lse": orc.gauss_lse(x, inp["y"], inp["b"], s),
+            "grad": orc.gauss_grad_x(x, inp["y"], inp["b"], inp["g"][rows], s),
+            "knn": orc.knn(x, inp["y"], K_NN)}
+
+
+def parity_stats(ref, a, L, gx, idx, dist):
+    """The step's GPU outputs on the oracle's sample rows against the oracle, with the library's
+    tolerances: Sum |err| <= 1e-4 S (S = sum_j |k b|), LSE |err| <= 1e-4 + 2^-20 |L|, grad-x
+    |err| <= 1e-4 G (G = its sum of magnitudes), K-min indices equal wherever the oracle's
+    distance at that position is separated (1e-5 relative) from its neighbours; the other
+    positions are near-ties, counted."""
+    a_ref, S_ref = ref["sum"]
+    L_ref = ref["lse"]
+    g_ref, G_ref = ref["grad"]
+    i_ref, d_ref, n_ref = ref["knn"]
+    r = a_ref.shape[0]
+    sum_err = float(np.max(np.abs(a[:r] - a_ref) / np.maximum(S_ref, 1e-300)))
+    lse_err = np.abs(L[:r] - L_ref)
+    lse_ok = bool(np.all(lse_err <= 1e-4 + 2.0 ** -20 * np.abs(L_ref)))
+    grad_err = float(np.max(np.abs(gx[:r] - g_ref) / np.maximum(G_ref, 1e-300)))
+    ext = np.concatenate([np.full((r, 1), -np.inf), d_ref, n_ref[:, None]], axis=1)
+    cur = ext[:, 1:-1]
+    with np.errstate(invalid="ignore"):
+        sep = ((cur - ext[:, :-2]) > 1e-5 * np.abs(cur)) & ((ext[:, 2:] - cur) > 1e-5 * np.abs(cur))
+    mism = int(np.sum(sep & (idx[:r].astype(np.int64) != i_ref)))
+    dist_err = float(np.max(np.abs(dist[:r] - d_ref) / np.maximum(np.abs(d_ref), 1e-30)))
+    ok = sum_err <= 1e-4 and lse_ok and grad_err <= 1e-4 and mism == 0
+    return {"rows": r, "ok": ok, "sum_err_over_S": sum_err, "lse_abs_err": float(np.max(lse_err)),
+            "grad_err_over_G": grad_err, "knn_separated_mismatches": mism,
+            "knn_near_ties": int(np.sum(~sep)), "knn_dist_rel_err": dist_err,
+            "tolerances": "Sum 1e-4 S; LSE 1e-4 + 2^-20 |L|; grad 1e-4 G; K-min indices exact where separated"}
 
 
 def _oracle_rows_for(orc, inp, s, target_s):
@@ -606,12 +636,12 @@ def cpu_baseline(inp, s, target_s=15.0):
     r = _oracle_rows_for(orc, inp, s, target_s)
     rows = np.arange(r)
     t0 = time.perf_counter()
-    _oracle_step(orc, inp, s, rows)
+    ref = _oracle_step(orc, inp, s, rows)
     t = time.perf_counter() - t0
     N = inp["y"].shape[0]
     return {"value": 4 * r * N / t, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
             "sample": f"first {r} rows of the step's batch, full N={N}: Sum + LSE + grad-x + K-min "
-                      f"(K={K_NN}) in fp64, {t:.1f} s"}
+                      f"(K={K_NN}) in fp64, {t:.1f} s"}, ref
 
 
 def run_reference(args, rank, world):
