@@ -43,7 +43,7 @@ KR_HD constexpr int rows_grad(int DP, int EP) {
     return DP <= 4 ? (EP == 1 ? 4 : EP == 4 ? 2 : 1) : DP <= 8 ? (EP == 1 ? 2 : 1) : 1;
 }
 KR_HD constexpr int rows_knn(int DP, int KP) {
-    return DP <= 4 ? (KP <= 10 ? 4 : 2) : DP <= 16 ? 2 : 1;
+    return DP <= 16 ? (KP <= 10 ? 4 : 2) : 1;
 }
 
 // Tensor-core Sum: largest |x'|^2 + |y'|^2 (prescaled, base-2 exponent units) for
@@ -95,10 +95,12 @@ KR_HD constexpr int knnx_mask_groups(int DP, int KP) { return 8; }
 // Entries per row of the filtered K-min's queue (0: immediate insertion).
 KR_HD constexpr int knnx_queue(int DP, int KP) { return DP <= 16 ? 8 : 0; }
 // Resident blocks per SM the K-min instances are compiled for (registers cap): the
-// queued filtered instances keep at most 128 (D <= 4, K <= 16), 170 (D = 8, K <= 16) or
-// 255 registers (D = 16, or two rows of 32-entry lists).
+// queued filtered instances keep at most 128 (D <= 4, K <= 16), 170 (D = 8, K = 16) or
+// 255 registers (four rows at D = 8 or 16, or two rows of 32-entry lists).  At D = 8
+// and 16 the screen's records are wide (20 and 36 floats a point pair), so four rows
+// per record read are worth the lower occupancy: the loop is bound by shared memory.
 KR_HD constexpr int knn_min_blocks(int DP, int KP) {
-    return knnx_queue(DP, KP) > 0 ? (DP <= 4 ? (KP <= 16 ? 4 : 2) : DP <= 8 ? (KP <= 16 ? 3 : 2) : 2) : 1;
+    return knnx_queue(DP, KP) > 0 ? (DP <= 4 ? (KP <= 16 ? 4 : 2) : DP <= 8 ? (KP == 16 ? 3 : 2) : 2) : 1;
 }
 // Pair records per unrolled step of the packed inner loop.
 KR_HD constexpr int unroll_pairs(int DP) { return DP <= 8 ? 2 : 1; }
