@@ -184,6 +184,9 @@ __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
         __syncthreads();
 
         // ---- fast pass ------------------------------------------------------------
+        // the Sum's loop is unrolled four steps deep (4 % faster at D = 3); the LogSumExp's is
+        // not (slower so)
+#pragma unroll(LSE ? 1 : 4)
         for (int jj = 0; jj < nvp; jj += UPT) {
 #pragma unroll
             for (int u = 0; u < UP; ++u) {
