@@ -256,6 +256,19 @@ def test_instance_choice(lib):
     assert kr.plan(kr.OP_KNN, 10, 10, 16, 1).ek_pad == 1
 
 
+@pytest.mark.parametrize("D,K,rows,tile", [
+    (3, 10, 4, 1024), (3, 1, 4, 1024), (4, 10, 4, 512), (3, 16, 2, 1024), (3, 32, 2, 1024),
+    (8, 10, 4, 512), (8, 16, 2, 512), (16, 10, 4, 256), (16, 32, 2, 256), (50, 10, 1, 128), (128, 10, 1, 64),
+])
+def test_knn_instances(lib, D, K, rows, tile):
+    """K-min instances: the screened kernel (D <= 16) keeps both record arrays of a tile within
+    36 KB (1024 points at D <= 3, 512 at D = 4, 8, 256 at D = 16) and four rows a thread for K <= 10
+    (two for longer lists); the direct kernels above D = 16 one row."""
+    p = kr.plan(kr.OP_KNN, 100_000, 100_000, D, K)
+    assert (p.rows_per_thread, p.tile_points) == (rows, tile)
+    assert p.row_blocks == (100_000 + 128 * rows - 1) // (128 * rows)
+
+
 @pytest.mark.parametrize("op,M,N,D,EK", [
     (kr.OP_SUM, 100_000, 100_000, 3, 1),
     (kr.OP_LSE, 1_000_000, 1_000_000, 3, 1),
