@@ -32,6 +32,22 @@ def test_header_declares_the_boundary():
     assert tuple(names) == kr.EXPORTS
 
 
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++17")])
+def test_header_compiles_alone(tmp_path, lang, std):
+    """The public header is self-contained C99 and C++17: it compiles with no other include
+    and no warning under -Wall -Wextra -pedantic."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("t.c" if lang == "c" else "t.cpp")
+    src.write_text('#include "kreduce.h"\nint main(void) { return (int)sizeof(kr_options) == 0; }\n')
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-I", os.path.dirname(HEADER), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
