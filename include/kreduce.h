@@ -50,8 +50,10 @@
  *           errors during execution surface at the caller's next synchronisation.
  * Threads.  Calls from several host threads on different streams are safe; the
  *           library's only global state is per-device cached attributes.
- * Limits.   1 <= D <= 128, 1 <= E <= 16, 1 <= K <= 32; M, N >= 0; M*D, N*D,
- *           M*E, N*E and M*K below 2^31 elements.  sigma finite and > 0.
+ * Limits.   1 <= D <= 128, 1 <= E <= 16, 1 <= K <= 32; M >= 0; 0 <= N < 2^31 - 1
+ *           (indices are int32); M*D, N*D, M*E, N*E and M*K at most 2^60 elements
+ *           (every element index is 64-bit: y may exceed 2^31 floats, e.g.
+ *           N = 10^9 points in D = 50).  sigma finite and > 0.
  *           M = 0 is a no-op; N = 0 gives Sum 0, LogSumExp -inf, grad 0,
  *           K-min indices -1 and distances +inf.
  * Numerics. fp32 inputs and outputs; exp is computed as ex2.approx on arguments

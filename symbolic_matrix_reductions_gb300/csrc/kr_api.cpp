@@ -323,8 +323,10 @@ static bool overlaps(const void *a, int64_t abytes, const void *b, int64_t bbyte
     return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
 }
 
-static bool fits_int31(int64_t rows, int64_t cols) {
-    return rows >= 0 && cols >= 0 && (cols == 0 || rows <= (((int64_t)1 << 31) - 1) / cols);
+// Element counts up to 2^60, so that byte sizes (x 4 or 8) and every 64-bit element index
+// stay far from overflow.
+static bool fits_elements(int64_t rows, int64_t cols) {
+    return rows >= 0 && cols >= 0 && (cols == 0 || rows <= ((int64_t)1 << 60) / cols);
 }
 
 struct Buf {
@@ -352,7 +354,7 @@ static int validate(int op, const Buf *bufs, int nbuf, int64_t M, int64_t N, int
     if (D > kMaxD) return KR_ERR_UNSUPPORTED;
     if (op == OP_KNN ? EK > kMaxK : EK > kMaxE) return KR_ERR_UNSUPPORTED;
     const int64_t Mx = std::max<int64_t>(M, 1), Nx = std::max<int64_t>(N, 1);
-    if (!fits_int31(Mx, D) || !fits_int31(Nx, D) || !fits_int31(Mx, EK) || !fits_int31(Nx, EK))
+    if (!fits_elements(Mx, D) || !fits_elements(Nx, D) || !fits_elements(Mx, EK) || !fits_elements(Nx, EK))
         return KR_ERR_UNSUPPORTED;
     if (N > INT32_MAX - 1) return KR_ERR_UNSUPPORTED;
     for (int k = 0; k < nbuf; ++k)

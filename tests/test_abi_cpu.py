@@ -96,7 +96,8 @@ def _reduce(lib, x=FAKE[0], y=FAKE[1], b=FAKE[2], out=FAKE[3], M=10, N=10, D=3, 
     (dict(out=None), kr.KR_ERR_INVALID),
     (dict(D=129), kr.KR_ERR_UNSUPPORTED),
     (dict(E=17), kr.KR_ERR_UNSUPPORTED),
-    (dict(M=1 << 30, D=3), kr.KR_ERR_UNSUPPORTED),      # M*D >= 2^31
+    (dict(M=1 << 59, D=3), kr.KR_ERR_UNSUPPORTED),      # M*D > 2^60 elements
+    (dict(N=1 << 31, D=3), kr.KR_ERR_UNSUPPORTED),      # indices are int32
     (dict(out=P(0x10000 + 8)), kr.KR_ERR_INVALID),      # output overlaps x
     (dict(M=0, out=None, x=None), kr.KR_OK),            # M = 0 is a no-op, no device needed
 ])

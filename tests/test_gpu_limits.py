@@ -3,6 +3,9 @@
 * N = 2^28 + 12345 points (D = 1): indices far above 2^24 must come out exact, the
   split-j partial layout must not overflow, and ties between a low and a very high
   index must keep the low one.
+* N*D above 2^31 elements (N = 1.4e8 points in D = 16, y = 9 GB): rows planted as exact
+  copies of points beyond element 2^31 must find them (K-min, ArgMax) and their Sum must
+  see them.
 * Every kernel family run twice on the same inputs gives bitwise-equal results (split-j
   partials are combined in a fixed order; nothing depends on scheduling)."""
 import numpy as np
@@ -37,6 +40,29 @@ def orc():
 def _np(t):
     torch.cuda.synchronize()
     return t.cpu().numpy()
+
+
+def test_elements_beyond_2_31():
+    M, D, N = 64, 16, 140_000_000                       # N*D = 2.24e9 > 2^31
+    g = torch.Generator(device=DEV).manual_seed(2031)
+    y = torch.randn((N, D), device=DEV, generator=g)
+    first = (1 << 31) // D + 1                          # first point whose elements lie past 2^31
+    jh = np.linspace(first, N - 1, M).round().astype(np.int64)   # fp64 and integer: in range
+    assert jh.min() >= first and jh.max() <= N - 1
+    j = torch.from_numpy(jh).to(DEV)
+    x = y[j].clone()                                    # row k is an exact copy of point j_k
+    b = torch.zeros((N, 1), device=DEV)
+    b[j] = 1.0
+    idx, dist = kr.kernel_knn(x, y, 2)
+    assert np.array_equal(_np(idx)[:, 0], jh) and (_np(dist)[:, 0] == 0).all()
+    am, vm = kr.kernel_reduce_arg(x, y, b, 0.5, "max")
+    assert np.array_equal(_np(am)[:, 0], jh) and (_np(vm)[:, 0] == 1.0).all()
+    # Sum: only the planted points carry weight; the exact value from those points alone
+    a = _np(kr.kernel_reduce(x, y, b, 0.5, "sum"))[:, 0]
+    xp = x.double().cpu().numpy()
+    ref = np.exp(-((xp[:, None, :] - xp[None, :, :]) ** 2).sum(-1) / 0.25).sum(1)
+    assert np.all(np.abs(a - ref) <= 1e-4 * ref)
+    del y, b
 
 
 def test_large_n_index_range(orc):
