@@ -71,8 +71,9 @@ extern "C" int kernel_reduce_noalloc(const float *x, const float *y, const float
     if (!x || !out || (N > 0 && (!y || !b))) return KR_ERR_INVALID;
     // Two splits of (hi, lo) or (m, acc) per output element must fit the scratch.
     if (M * (int64_t)E > kScratchFloats / 4) return KR_ERR_UNSUPPORTED;
-    if (M * (int64_t)D > INT32_MAX || N * (int64_t)D > INT32_MAX || N * (int64_t)E > INT32_MAX)
-        return KR_ERR_UNSUPPORTED;
+    // the limits of kernel_reduce: int32 indices, element counts up to 2^60
+    const int64_t kMaxElems = (int64_t)1 << 60;
+    if (N > INT32_MAX - 1 || M > kMaxElems / D || N > kMaxElems / D || N > kMaxElems / E) return KR_ERR_UNSUPPORTED;
     // Host arrays would need staging memory: device (or managed) pointers only.
     if (!on_device(x) || !on_device(out) || (N > 0 && (!on_device(y) || !on_device(b)))) return KR_ERR_INVALID;
     const uintptr_t o0 = (uintptr_t)out, o1 = o0 + (uintptr_t)(M * E * (int64_t)sizeof(float));
