@@ -43,3 +43,25 @@ def test_each_gate_fails_past_its_tolerance(orc):
     out[3] = i
     p = bench.parity_stats(ref, *out)
     assert not p["ok"] and p["knn_separated_mismatches"] >= 1
+
+
+def test_roofline_peaks():
+    """The pipe-count peaks the bench reports (152 SMs, 2070 MHz; FP32 128, ALU 64 lanes per
+    clock and SM; ex2 32, sqrt/rcp/rsqrt 16): Sum at D = 3 is FP32-bound at 7 operations a pair,
+    the K-min's direct count is 6 FP32 + 1 ALU (its screen's 3 + 1), the Laplace Sum is bound by
+    its two XU operations (sqrt at 16 lanes, ex2 at 32)."""
+    xu = {"ex2": 32.0, "rcp": 16.0, "rsqrt": 16.0, "sqrt": 16.0}
+    clk = 152 * 2070e6
+    s = bench.roofline("sum", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "k")
+    assert abs(s["peak"] - clk * 128 / 7) < 1 and s["limiting_pipe"] == "fp32"
+    assert abs(s["frac"] - 1e12 / s["peak"]) < 1e-12
+    k = bench.roofline("knn", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "k")
+    assert abs(k["peak"] - clk * 128 / 6) < 1 and abs(k["screen"]["peak"] - clk * 128 / 3) < 1
+    lp = bench.roofline("sum", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "k", kind="laplace")
+    assert abs(lp["peak"] - clk / (1 / 16 + 1 / 32)) < 1 and lp["limiting_pipe"] == "xu"
+    # traffic only for a captured kernel, and only while its sources are the captured ones
+    name = "grad_kernel[D=3,E=1]"
+    fresh = bench.TRAFFIC[name]["source_hash"] == bench._kernel_source_hash()
+    t = bench.roofline("grad", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, name)["traffic"]
+    assert t == (bench.TRAFFIC[name]["bytes_per_launch"] if fresh else None)
+    assert bench.roofline("grad", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "other")["traffic"] is None
