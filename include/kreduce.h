@@ -283,12 +283,22 @@ int kr_last_cuda_error(void);
  * their mbarriers is bounded (2 s of global time by default); a block whose wait gives
  * up writes NaN for its rows and sets bit 0 of this status.  Reads the status into
  * *status (0 = nothing happened since the last clear) and clears it when `clear` is
- * nonzero.  Synchronous: waits for the device's work.  Test hooks read at each call:
- * KREDUCE_TC_WAIT_MS overrides the wait bound; KREDUCE_TC_STARVE=1 makes the
- * tensor-core kernel withhold its B tiles, so its waits run out (the context stays
- * usable, the next call works normally).
+ * nonzero.  Synchronous: waits for the device's work.  The environment variable
+ * KREDUCE_TC_WAIT_MS (read once per process) sets another wait bound in ms.
  */
 int kr_device_status(unsigned *status, int clear);
+
+/*
+ * Test hook of the failure detection above (no counterpart on the pages).  Sets the
+ * tensor-core wait bound to wait_ms (0: back to 2000) for the whole process, and with
+ * starve = 1 makes the tensor-core kernels withhold their B tiles, so that every wait
+ * runs out (rows NaN, status bit 0; the context stays usable and the next call with
+ * starve = 0 works normally).  Starvation exists only in the debug build
+ * (kr_debug_build() == 1): the release library returns KR_ERR_UNSUPPORTED for
+ * starve = 1 and carries no such path.  KR_ERR_INVALID for wait_ms < 0 or starve not
+ * 0 or 1.  Not thread-safe against calls in flight on other threads.
+ */
+int kr_set_tc_test_hooks(int wait_ms, int starve);
 
 /*
  * 1 for a debug build of the library (compiled with -DKR_DEBUG, libkreduce_debug.so),

@@ -45,7 +45,7 @@ EXPORTS = ("kernel_reduce", "kernel_reduce_ex", "kernel_reduce_arg", "kernel_red
            "kernel_reduce_grad_x_ex", "kernel_reduce_grad_y", "kernel_reduce_grad_y_ex",
            "kernel_reduce_grad_b", "kernel_reduce_grad_b_ex",
            "kernel_knn", "kernel_knn_ex", "kr_status_string", "kr_last_cuda_error", "kr_device_status",
-           "kr_debug_build", "kr_plan", "kr_plan_device")
+           "kr_set_tc_test_hooks", "kr_debug_build", "kr_plan", "kr_plan_device")
 
 
 class KrError(RuntimeError):
@@ -124,6 +124,7 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.kr_status_string.restype = ctypes.c_char_p
     lib.kr_last_cuda_error.argtypes = []
     lib.kr_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+    lib.kr_set_tc_test_hooks.argtypes = [i32, i32]
     lib.kr_debug_build.argtypes = []
     lib.kr_plan.argtypes = [i32, i64, i64, i32, i32, i32, i32, opt, ctypes.POINTER(KrPlan)]
     lib.kr_plan_device.argtypes = [i32, i64, i64, i32, i32, opt, ctypes.POINTER(KrPlan)]

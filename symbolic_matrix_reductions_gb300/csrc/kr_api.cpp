@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -292,6 +293,14 @@ cudaMemPool_t device_pool(int dev) {
     return c.pool;
 }
 
+int device_tc_occupancy(int dev) {
+    if (dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(g_cache_mutex);
+    if (g_cache[dev].tc_occ == 0) g_cache[dev].tc_occ = tc_occupancy();
+    return g_cache[dev].tc_occ;
+}
+}  // namespace
+
 // Debug builds (-DKR_DEBUG): the device word the kernels' index checks write to, one
 // per device for the life of the process.  Release builds never allocate it.
 unsigned *debug_word(int dev) {
@@ -308,13 +317,21 @@ unsigned *debug_word(int dev) {
     return c.dbg;
 }
 
-int device_tc_occupancy(int dev) {
-    if (dev < 0 || dev >= 64) return 0;
-    std::lock_guard<std::mutex> lock(g_cache_mutex);
-    if (g_cache[dev].tc_occ == 0) g_cache[dev].tc_occ = tc_occupancy();
-    return g_cache[dev].tc_occ;
+// Bound of every mbarrier wait of the tensor-core kernels, in ms: KREDUCE_TC_WAIT_MS read
+// once per process (2000 if unset or not positive), or what kr_set_tc_test_hooks set.
+// Starvation of the B tiles (the failure-detection test) exists only in debug builds.
+static std::once_flag g_tc_wait_once;
+static std::atomic<long> g_tc_wait_ms{2000};
+static std::atomic<int> g_tc_starve{0};
+
+static uint64_t tc_wait_ns() {
+    std::call_once(g_tc_wait_once, [] {
+        const char *wms = std::getenv("KREDUCE_TC_WAIT_MS");
+        const long ms = wms ? std::strtol(wms, nullptr, 10) : 0;
+        if (ms > 0) g_tc_wait_ms.store(ms);
+    });
+    return (uint64_t)g_tc_wait_ms.load() * 1000000ull;
 }
-}  // namespace
 
 // ---- validation ---------------------------------------------------------------------
 static bool overlaps(const void *a, int64_t abytes, const void *b, int64_t bbytes) {
@@ -457,14 +474,14 @@ static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in
         t.ws0 = a.ws0;
         t.ws1 = a.ws1;
         t.guard = guard;
-        // Every mbarrier wait of the tensor kernel gives up after this long (2 s unless
-        // KREDUCE_TC_WAIT_MS says otherwise).  KREDUCE_TC_STARVE=1 withholds the B tiles so
-        // that a test can watch the waits run out and the status report it.
-        const char *wms = std::getenv("KREDUCE_TC_WAIT_MS");
-        const long ms = wms ? std::strtol(wms, nullptr, 10) : 2000;
-        t.wait_ns = (uint64_t)(ms > 0 ? ms : 2000) * 1000000ull;
-        const char *starve = std::getenv("KREDUCE_TC_STARVE");
-        t.starve = starve && starve[0] == '1';
+        // Every mbarrier wait of the tensor kernel gives up after this long.  In debug builds
+        // a test can withhold the B tiles (kr_set_tc_test_hooks) to watch the waits run out.
+        t.wait_ns = tc_wait_ns();
+#ifdef KR_DEBUG
+        t.starve = g_tc_starve.load() != 0;
+#else
+        t.starve = false;
+#endif
         t.M = a.M;
         t.N = a.N;
         t.chunk = p.chunk;
@@ -917,6 +934,17 @@ int kr_device_status(unsigned *status, int clear) {
     }
 #endif
     return e == cudaSuccess ? KR_OK : cuda_fail(e);
+}
+
+int kr_set_tc_test_hooks(int wait_ms, int starve) {
+    if (wait_ms < 0 || (starve != 0 && starve != 1)) return KR_ERR_INVALID;
+#ifndef KR_DEBUG
+    if (starve) return KR_ERR_UNSUPPORTED;  // release builds carry no fault path
+#endif
+    tc_wait_ns();  // the environment's default is read first, so it cannot override this call
+    g_tc_wait_ms.store(wait_ms > 0 ? (long)wait_ms : 2000);
+    g_tc_starve.store(starve);
+    return KR_OK;
 }
 
 int kr_debug_build(void) {

@@ -18,8 +18,19 @@ __global__ void combine_lse_kernel(const Args a_) {
     const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = a.M * a.E;
     if (o >= total) return;
+    // A split that could not finish (a tensor-core wait that ran out) leaves NaN in its
+    // frame; fmaxf would drop it, so NaN is looked for first and passed on to the output.
     float mmax = -f_inf();
-    for (int s = 0; s < a.S; ++s) mmax = fmaxf(mmax, ldg_chk(a, a.ws0, s * total + o, a.ws_n, KRD_WS));
+    bool nan = false;
+    for (int s = 0; s < a.S; ++s) {
+        const float m = ldg_chk(a, a.ws0, s * total + o, a.ws_n, KRD_WS);
+        nan |= m != m;
+        mmax = fmaxf(mmax, m);
+    }
+    if (nan) {
+        st_chk(a, a.out, o, a.out_n, KRD_OUT, __int_as_float(0x7fc00000));
+        return;
+    }
     if (mmax == -f_inf()) {
         st_chk(a, a.out, o, a.out_n, KRD_OUT, (float)(-f_inf()));
         return;

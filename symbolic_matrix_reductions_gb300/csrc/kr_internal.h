@@ -63,6 +63,11 @@ struct Instance {
     int d_pad, ek_pad, rows, tile;
 };
 
+// Debug builds (-DKR_DEBUG): the device word of `dev` that the kernels' index checks
+// write to (allocated once per device, kept for the life of the process); null when it
+// could not be allocated.  Release builds never call it.
+unsigned *debug_word(int dev);
+
 // Instance selection (pure host logic).
 Instance choose_instance(int op, int D, int EK);
 

@@ -123,6 +123,9 @@ extern "C" int kernel_reduce_noalloc(const float *x, const float *y, const float
     a.chunk = p.chunk;
     a.out_n = M * E;
     a.ws_n = (int64_t)p.split * M * E;
+#ifdef KR_DEBUG
+    a.dbg = debug_word(dev);  // the index checks report where kr_device_status reads
+#endif
     if (p.split > 1) {
         a.ws0 = scratch;
         a.ws1 = scratch + (int64_t)p.split * M * E;

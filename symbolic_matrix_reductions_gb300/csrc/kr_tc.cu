@@ -81,7 +81,8 @@ constexpr int kStageBytes = 2 * kBTileBytes;
 constexpr int kSmemBytes = 2 * kATileBytes + kStages * kStageBytes + 1024;
 static_assert(kSmemBytes + 256 <= 227 * 1024, "shared memory per block");
 
-// tcgen05 instruction descriptor: D = f32, A = B = f16, both K-major, M = 128, N = 128.
+// tcgen05 instruction descriptor: D = f32, A = B = f16, both K-major, M = kRows (128),
+// N = kCols (256).
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kCols >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }

@@ -64,6 +64,17 @@ def test_device_status_without_a_device(lib):
         assert lib.kr_device_status(ctypes.byref(v), 1) == kr.KR_OK and v.value == 0
 
 
+def test_tc_test_hooks_release_has_no_fault_path(lib):
+    """The release library refuses the starvation hook (only the debug build carries it);
+    the wait bound itself may be set and reset.  No CUDA call is made."""
+    assert lib.kr_debug_build() == 0
+    assert lib.kr_set_tc_test_hooks(50, 1) == kr.KR_ERR_UNSUPPORTED
+    assert lib.kr_set_tc_test_hooks(-1, 0) == kr.KR_ERR_INVALID
+    assert lib.kr_set_tc_test_hooks(50, 2) == kr.KR_ERR_INVALID
+    assert lib.kr_set_tc_test_hooks(50, 0) == kr.KR_OK
+    assert lib.kr_set_tc_test_hooks(0, 0) == kr.KR_OK
+
+
 def test_status_strings(lib):
     texts = {lib.kr_status_string(s).decode() for s in range(5)}
     assert len(texts) == 5

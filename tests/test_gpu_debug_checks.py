@@ -68,6 +68,8 @@ def test_debug_build_finds_no_bad_index(libs, M, N, D, E):
         "ranges min": lambda: list(kr.kernel_reduce_ranges(x, y, b, 0.9, "min", ri, si, rj, want_index=True)),
         "batched": lambda: [kr.kernel_reduce(torch.stack([x, x.flip(0)]), torch.stack([y, y]), torch.stack([b, b]),
                                              0.9, "sum", path=kr.KR_PATH_CUDA_CORES)],
+        "noalloc sum": lambda: [kr.kernel_reduce_noalloc(x, y, b, 0.9, "sum", out=torch.empty((M, E), device=DEV))],
+        "noalloc lse": lambda: [kr.kernel_reduce_noalloc(x, y, b, 0.9, "lse", out=torch.empty((M, E), device=DEV))],
     }
     kr.device_status(clear=True)
     for name, fn in calls.items():

@@ -233,18 +233,39 @@ def test_workload_gauss_d3(orc):
     check_grad(gx[rows], gx_ref, G_ref, "gauss_d3")
 
 
+def test_workload_gauss_d3_grad_of_sum_of_squares(orc):
+    """The gradient the README differentiates, at the full M = N = 1e5: a = Sum, then the
+    x-gradient of sum_i a_i^2, i.e. the upstream g = 2a (computed by the GPU for every
+    row).  The oracle checks a and the gradient on 4096 seeded rows with the full N; its
+    gradient takes the same upstream values the GPU used, so the gate is the kernel's."""
+    inp = W.generate("gauss_d3")
+    s = inp["sigma"]
+    xt, yt, bt = _dev(inp["x"], inp["y"], inp["b"])
+    a = kr.kernel_reduce(xt, yt, bt, s, "sum")
+    gx = _np(kr.kernel_reduce_grad_x(xt, yt, bt, 2.0 * a, s))
+    a = _np(a)
+    rows = W.row_subset(inp["x"].shape[0], 4096, 11)
+    a_ref, S_ref = orc.gauss_sum(inp["x"][rows], inp["y"], inp["b"], s)
+    worst_sum = check_sum(a[rows], a_ref, S_ref, "gauss_d3 a")
+    gx_ref, G_ref = orc.gauss_grad_x(inp["x"][rows], inp["y"], inp["b"], 2.0 * a[rows], s)
+    worst_grad = check_grad(gx[rows], gx_ref, G_ref, "gauss_d3 grad of sum(a^2)")
+    print(f"gauss_d3 grad of sum(a^2), {rows.size} rows: a err/S {worst_sum:.2e}, grad err/G {worst_grad:.2e}")
+
+
 def test_workload_gauss_d3_unit(orc):
     inp = W.generate("gauss_d3_unit")
     s = inp["sigma"]
     xt, yt, bt, wt = _dev(inp["x"], inp["y"], inp["b"], inp["w_log"])
     a = _np(kr.kernel_reduce(xt, yt, bt, s, "sum"))
     L = _np(kr.kernel_reduce(xt, yt, wt, s, "lse"))
-    rows = W.row_subset(inp["x"].shape[0], 512, 8)
+    # a seeded subset of 4096 rows with the full N = 1e6 (rows are independent)
+    rows = W.row_subset(inp["x"].shape[0], 4096, 8)
     a_ref, S_ref = orc.gauss_sum(inp["x"][rows], inp["y"], inp["b"], s)
-    check_sum(a[rows], a_ref, S_ref, "gauss_d3_unit")
-    check_lse(L[rows], orc.gauss_lse(inp["x"][rows], inp["y"], inp["w_log"], s), "gauss_d3_unit")
+    worst_sum = check_sum(a[rows], a_ref, S_ref, "gauss_d3_unit")
+    worst_lse = check_lse(L[rows], orc.gauss_lse(inp["x"][rows], inp["y"], inp["w_log"], s), "gauss_d3_unit")
     # LogSumExp of log b equals log of the Sum of b (b > 0)
     assert np.max(np.abs(L[rows] - np.log(a_ref))) < 1e-4
+    print(f"gauss_d3_unit, {rows.size} rows: Sum err/S {worst_sum:.2e}, LSE abs err {worst_lse:.2e}")
 
 
 def test_workload_falkon_d50(orc):
@@ -268,10 +289,11 @@ def test_workload_knn_d16(orc):
     inp = W.generate("knn_d16")
     xt, yt = _dev(inp["x"], inp["y"])
     idx, dist = kr.kernel_knn(xt, yt, inp["K"])
-    rows = W.row_subset(inp["x"].shape[0], 1024, 10)
+    # a seeded subset of 4096 rows with the full N = 1e6 (rows are independent)
+    rows = W.row_subset(inp["x"].shape[0], 4096, 10)
     i_ref, d_ref, n_ref = orc.knn(inp["x"][rows], inp["y"], inp["K"])
     ties = check_knn(_np(idx)[rows], _np(dist)[rows], inp["x"][rows], inp["y"], i_ref, d_ref, n_ref, "knn_d16")
-    print(f"knn_d16: {ties} near-tie positions of {i_ref.size}")
+    print(f"knn_d16, {rows.size} rows: {ties} near-tie positions of {i_ref.size}")
 
 
 # ---------------------------------------------------------------------------
@@ -329,29 +351,41 @@ def test_tensor_core_lse_empty_weights_and_guard(orc):
     check_lse(_np(L), orc.gauss_lse(x, y, w, 2.0), "lse norm guard")
 
 
-def test_tensor_core_wait_bound_reports_status(orc):
-    """Failure detection without a fault: with the B tiles withheld (test hook) every
-    bounded mbarrier wait of the tensor kernel runs out after 50 ms; the rows come out
-    NaN, the sticky device status says so, and the context stays usable."""
+@pytest.mark.parametrize("op,split", [("sum", 0), ("sum", 2), ("lse", 0), ("lse", 3)])
+def test_tensor_core_wait_bound_reports_status(orc, op, split):
+    """Failure detection without a fault: with the B tiles withheld (a test hook that only
+    the debug build honours) every bounded mbarrier wait of the tensor kernel runs out
+    after 50 ms; the rows come out NaN (through the split-j combine too), the sticky device
+    status says so, and the context stays usable."""
     r = _rng(79)
     x = (r.standard_normal((300, 50)) / np.sqrt(50)).astype(np.float32)
     y = (r.standard_normal((1000, 50)) / np.sqrt(50)).astype(np.float32)
     b = r.standard_normal((1000, 1)).astype(np.float32)
     xt, yt, bt = _dev(x, y, b)
-    kr.device_status(clear=True)
-    os.environ["KREDUCE_TC_STARVE"] = "1"
-    os.environ["KREDUCE_TC_WAIT_MS"] = "50"
+    release = kr.load_library()
+    assert release.kr_set_tc_test_hooks(50, 1) == kr.KR_ERR_UNSUPPORTED
+    debug = kr.load_debug_library()
+    saved = kr._lib
+    kr._lib = debug
     try:
-        a = _np(kr.kernel_reduce(xt, yt, bt, 1.0, "sum", path=kr.KR_PATH_TENSOR_CORES))
+        kr.device_status(clear=True)
+        assert debug.kr_set_tc_test_hooks(50, 1) == kr.KR_OK
+        try:
+            a = _np(kr.kernel_reduce(xt, yt, bt, 1.0, op, split=split, path=kr.KR_PATH_TENSOR_CORES))
+        finally:
+            assert debug.kr_set_tc_test_hooks(0, 0) == kr.KR_OK
+        assert np.isnan(a).all()
+        assert kr.device_status(clear=True) & 1
+        assert kr.device_status() == 0
+        a = _np(kr.kernel_reduce(xt, yt, bt, 1.0, op, split=split, path=kr.KR_PATH_TENSOR_CORES))
+        assert kr.device_status() == 0
     finally:
-        del os.environ["KREDUCE_TC_STARVE"], os.environ["KREDUCE_TC_WAIT_MS"]
-    assert np.isnan(a).all()
-    assert kr.device_status(clear=True) & 1
-    assert kr.device_status() == 0
-    a = kr.kernel_reduce(xt, yt, bt, 1.0, "sum", path=kr.KR_PATH_TENSOR_CORES)
-    a_ref, S_ref = orc.gauss_sum(x, y, b, 1.0)
-    check_sum(_np(a), a_ref, S_ref, "after a run-out wait")
-    assert kr.device_status() == 0
+        kr._lib = saved
+    if op == "sum":
+        a_ref, S_ref = orc.gauss_sum(x, y, b, 1.0)
+        check_sum(a, a_ref, S_ref, "after a run-out wait")
+    else:
+        check_lse(a, orc.gauss_lse(x, y, b, 1.0), "after a run-out wait")
 
 
 def test_tensor_core_norm_guard_falls_back(orc):
