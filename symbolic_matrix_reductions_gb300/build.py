@@ -26,7 +26,7 @@ LIB_DEBUG = os.path.join(HERE, "libkreduce_debug.so")
 PROBE_LIB = os.path.join(HERE, "libkrprobe.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["kr_api.cpp", "kr_fwd_sum.cu", "kr_fwd_lse.cu", "kr_grad.cu", "kr_knn.cu", "kr_combine.cu",
+SOURCES = ["kr_api.cpp", "kr_fwd_sum.cu", "kr_fwd_lse.cu", "kr_grad.cu", "kr_knn.cu", "kr_combine.cu", "kr_records.cu",
            "kr_noalloc.cu", "kr_tc.cu", "kr_radial_gauss.cu", "kr_radial_laplace.cu", "kr_radial_cauchy.cu",
            "kr_radial_imq.cu"]
 PROBE_SOURCES = ["kr_probe.cu"]

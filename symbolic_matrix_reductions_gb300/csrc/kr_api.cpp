@@ -36,7 +36,7 @@ static int cuda_fail(cudaError_t e) {
     return KR_ERR_CUDA;
 }
 
-Instance choose_instance(int op, int D, int EK) {
+Instance choose_instance(int op, int D, int EK, int kind) {
     Instance in{};
     in.d_pad = pad_d(D);
     if (op == OP_KNN) {
@@ -50,8 +50,18 @@ Instance choose_instance(int op, int D, int EK) {
         in.tile = (op == OP_GRAD && wide_grad(in.d_pad))    ? kWideGradTile
                   : (op == OP_GRAD && !packed_grad(in.d_pad)) ? tile_points(pack_stride(in.d_pad, in.ek_pad))
                                                               : instance_tile(in.d_pad, in.ek_pad);
+        in.rec = streamed(in.d_pad) && (op == OP_LSE || op == OP_GRAD || (op == OP_SUM && kind == KR_KERNEL_GAUSSIAN));
     }
     return in;
+}
+
+static int64_t round256(int64_t v) { return (v + 255) / 256 * 256; }
+
+// Bytes of the streamed records (and LogSumExp tile frames) of a call with N points.
+static int64_t record_bytes(int op, const Instance &in, int64_t N, int64_t batch) {
+    if (!in.rec) return 0;
+    return batch * (round256(record_elems(in, N) * (int64_t)sizeof(float)) +
+                    round256(wtile_elems(op, in, N) * (int64_t)sizeof(float)));
 }
 
 // Bytes of split-j workspace for S splits.
@@ -132,10 +142,13 @@ static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, const kr_op
            kMaxTcOperands;
 }
 
-// Pure planner (no CUDA call).  blocks_per_sm <= 0: assume 4 resident blocks.
+// Pure planner (no CUDA call).  blocks_per_sm <= 0: assume 4 resident blocks.  Streamed
+// instances split on tile boundaries (every split's range is whole prepass tiles) and add
+// their records to the workspace.
 static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm,
-                int forced_split, int64_t batch, kr_plan_t *p) {
-    const Instance in = choose_instance(op, D, EK);
+                int forced_split, int64_t batch, int kind, kr_plan_t *p) {
+    const Instance in = choose_instance(op, D, EK, kind);
+    const int64_t align = in.rec ? in.tile : 1;
     p->path = KR_PATH_CUDA_CORES;
     p->d_pad = in.d_pad;
     p->ek_pad = in.ek_pad;
@@ -165,7 +178,8 @@ static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int bl
         double best = 0.0;
         for (int64_t s = 1; s <= s_max; ++s) {
             if (batch * workspace_bytes(op, in, M, D, EK, (int)s) > kMaxWorkspace) break;
-            const int64_t chunk = (N + s - 1) / s;
+            const int64_t chunk = round_up((N + s - 1) / s, align);
+            if (s > 1 && (s - 1) * chunk >= N) continue;  // an empty split: the same as fewer splits
             const int64_t tiles = (chunk + in.tile - 1) / in.tile;
             // per block, in points: its chunk, a per-tile cost (staging, barriers) and a fixed
             // cost (loading its rows, writing its partials, its share of the combine)
@@ -189,14 +203,15 @@ static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int bl
         }
     }
     p->split = S;
-    p->chunk = (N + S - 1) / S;
+    p->chunk = round_up((N + S - 1) / S, align);
     if (p->chunk < 1) p->chunk = 1;
     // Every split must own a nonempty range, except when N == 0.
     if (N > 0 && (int64_t)(S - 1) * p->chunk >= N) {
         S = (int)((N + p->chunk - 1) / p->chunk);
         p->split = S;
     }
-    p->workspace_bytes = batch * workspace_bytes(op, in, M, D, EK, S);
+    const int64_t parts = batch * workspace_bytes(op, in, M, D, EK, S);
+    p->workspace_bytes = in.rec ? round256(parts) + record_bytes(op, in, N, batch) : parts;
     return KR_OK;
 }
 
@@ -536,16 +551,17 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
     cudaError_t ce = cudaGetDevice(&dev);
     if (ce != cudaSuccess) return cuda_fail(ce);
 
-    const Instance in = choose_instance(op, a.D, EK);
     const int kind = opt ? opt->kernel : KR_KERNEL_GAUSSIAN;
+    Instance in = choose_instance(op, a.D, EK, kind);
     int num_sms = 0, occ = 0;
     if (device_info(dev, op, kind, in, &num_sms, &occ) != 0) return cuda_fail(cudaGetLastError());
     kr_plan_t p;
     const bool tc = !rt && tc_eligible(op, a.M, a.N, a.D, EK, opt) && tc_available();
+    if (tc || rt) in.rec = false;  // the tensor-core stand-in and the block-sparse kernels stage their own tiles
     if (tc) {
         plan_tc(a.M, a.N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, &p);
     } else {
-        plan(op, a.M, a.N, a.D, EK, num_sms, occ, opt ? opt->split : 0, B, &p);
+        plan(op, a.M, a.N, a.D, EK, num_sms, occ, opt ? opt->split : 0, B, kind, &p);
         if (rt) {  // one block per table entry and split; the tables lead the workspace
             p.row_blocks = (int64_t)rt->blocks.size();
             p.split = ranges_split(*rt, in.tile, num_sms, occ, a.M, EK);
@@ -655,6 +671,7 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
         } else if (tc) {
             ce = run_tc(op, a, p, in, ws, stream);
         } else {
+            const int64_t part_bytes = B * workspace_bytes(op, in, a.M, a.D, EK, p.split);
             if (p.split > 1) {
                 a.ws0 = (float *)ws;
                 if (op == OP_KNN) {
@@ -662,11 +679,23 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
                 } else if (op == OP_MAX) {
                     a.wsi = (int32_t *)(ws + B * p.split * a.M * EK * (int64_t)sizeof(float));
                 } else {
-                    a.ws1 = (float *)(ws + p.workspace_bytes / 2);
+                    a.ws1 = (float *)(ws + part_bytes / 2);
                 }
             }
             const dim3 grid((unsigned)p.row_blocks, (unsigned)p.split, (unsigned)B);
-            switch (op) {
+            if (in.rec && a.N > 0) {
+                // the streamed instances: the prepass packs this call's tiles after the partials
+                a.rec_n = record_elems(in, a.N);
+                a.wtile_n = wtile_elems(op, in, a.N);
+                a.bs_rec = round256(a.rec_n * (int64_t)sizeof(float)) / (int64_t)sizeof(float);
+                a.bs_wtile = round256(a.wtile_n * (int64_t)sizeof(float)) / (int64_t)sizeof(float);
+                a.rec = (float *)(ws + round256(part_bytes));
+                a.wtile = op == OP_LSE ? a.rec + B * a.bs_rec : nullptr;
+                ce = launch_pack(op, in, a, (a.N + in.tile - 1) / in.tile, stream);
+            } else {
+                in.rec = false;  // nothing to stream (N = 0): the kernel's own staging writes the empty result
+            }
+            if (ce == cudaSuccess) switch (op) {
                 case OP_SUM:
                     ce = kind == KR_KERNEL_GAUSSIAN ? launch_sum(in, a, grid, stream)
                                                     : launch_radial(kind, 0, in, a, grid, stream);
@@ -964,7 +993,8 @@ int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks
         plan_tc(M, N, num_sms, blocks_per_sm, opt ? opt->split : 0, out);
         return KR_OK;
     }
-    return plan(op, M, N, D, EK, num_sms, blocks_per_sm, opt ? opt->split : 0, batch_of(opt), out);
+    return plan(op, M, N, D, EK, num_sms, blocks_per_sm, opt ? opt->split : 0, batch_of(opt),
+                opt ? opt->kernel : KR_KERNEL_GAUSSIAN, out);
 }
 
 int kr_plan_device(int op, int64_t M, int64_t N, int D, int EK, const kr_options *opt, kr_plan_t *out) {
@@ -976,13 +1006,13 @@ int kr_plan_device(int op, int64_t M, int64_t N, int D, int EK, const kr_options
     if (ce != cudaSuccess) return cuda_fail(ce);
     int num_sms = 0, occ = 0;
     const int kind = opt ? opt->kernel : KR_KERNEL_GAUSSIAN;
-    if (device_info(dev, op, kind, choose_instance(op, D, EK), &num_sms, &occ) != 0)
+    if (device_info(dev, op, kind, choose_instance(op, D, EK, kind), &num_sms, &occ) != 0)
         return cuda_fail(cudaGetLastError());
     if (tc_eligible(op, M, N, D, EK, opt) && tc_available()) {
         plan_tc(M, N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, out);
         return KR_OK;
     }
-    return plan(op, M, N, D, EK, num_sms, occ, opt ? opt->split : 0, batch_of(opt), out);
+    return plan(op, M, N, D, EK, num_sms, occ, opt ? opt->split : 0, batch_of(opt), kind, out);
 }
 
 }  // extern "C"

@@ -88,6 +88,14 @@ KR_HD constexpr int tile_points_packed(int PS2) {
     return (16384 / PS2) >= 512 ? 512 : (16384 / PS2) >= 256 ? 256 : (16384 / PS2) >= 128 ? 128
          : (16384 / PS2) >= 64 ? 64 : 32;
 }
+// Streamed records (Gaussian Sum, LogSumExp and x-gradient up to D = 16): a prepass packs
+// the call's y (prescaled and negated) and its signal (or the LogSumExp's tile-relative
+// log-weight) once into tile-aligned pair records in device memory, and the reduction
+// kernel copies each tile into shared memory with 16-byte cp.async, double-buffered, so
+// the next tile's copy overlaps the current tile's scan and a tile costs one barrier.
+KR_HD constexpr bool streamed(int DP) { return DP <= 16; }
+// Floats of one tile of pair records (BN points).
+KR_HD constexpr int record_tile_floats(int DP, int EP, int BN) { return (BN / 2) * pair_stride(DP, EP); }
 // Filtered K-min: the pass bits of this many consecutive point groups are gathered in one
 // word per row and queued as one entry (block index, bit mask), so the scan loop itself
 // carries no branch.

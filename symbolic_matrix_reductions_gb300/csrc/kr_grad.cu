@@ -1,8 +1,4 @@
 // x-gradient instances and launcher.
-#include <mutex>
-#include <utility>
-#include <vector>
-
 #include "kr_kernels_packed.cuh"
 
 namespace kr {
@@ -10,61 +6,54 @@ namespace kr {
 namespace {
 typedef void (*KernelFn)(const Args);
 
+// rec: the streamed variant of the packed kernel (records from the prepass).
 template <int DP, int EP>
-KernelFn grad_instance() {
-    if constexpr (packed_grad(DP))
-        return grad2_kernel<DP, EP, rows_grad(DP, EP), tile_points_packed(pair_stride(DP, EP))>;
-    else if constexpr (wide_grad(DP))
-        return gradw_kernel<DP, EP, kWideGradTile>;
-    else
-        return grad_kernel<DP, EP, rows_grad(DP, EP), tile_points(pack_stride(DP, EP))>;
+KernelFn grad_instance(bool rec) {
+    if constexpr (packed_grad(DP)) {
+        static_assert(!packed_grad(DP) || streamed(DP), "every packed gradient instance has a streamed variant");
+        return rec ? grad2_kernel<DP, EP, rows_grad(DP, EP), tile_points_packed(pair_stride(DP, EP)), true>
+                   : grad2_kernel<DP, EP, rows_grad(DP, EP), tile_points_packed(pair_stride(DP, EP)), false>;
+    } else if constexpr (wide_grad(DP)) {
+        return rec ? nullptr : gradw_kernel<DP, EP, kWideGradTile>;
+    } else {
+        return rec ? nullptr : grad_kernel<DP, EP, rows_grad(DP, EP), tile_points(pack_stride(DP, EP))>;
+    }
 }
 
-// Dynamic shared memory of an instance (the wide kernel's tile and running sums).
+// Dynamic shared memory of an instance (the wide kernel's tile and running sums; the
+// streamed kernel's two record tiles).
 size_t grad_smem(const Instance &inst) {
+    if (inst.rec) return 2 * (size_t)record_tile_floats(inst.d_pad, inst.ek_pad, inst.tile) * sizeof(float);
     if (!wide_grad(inst.d_pad)) return 0;
     return ((size_t)kWideGradTile * pack_stride(inst.d_pad, inst.ek_pad) + 2 * (size_t)inst.d_pad * kThreads) *
            sizeof(float);
 }
 
-// Opts a wide instance in to its dynamic shared memory (above the 48 KB default), once.
-cudaError_t grad_prepare(KernelFn k, size_t smem) {
-    if (smem <= 48 * 1024) return cudaSuccess;
-    static std::mutex mu;
-    static std::vector<std::pair<int, KernelFn>> done;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(mu);
-    for (const auto &dk : done)
-        if (dk.first == dev && dk.second == k) return cudaSuccess;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) done.emplace_back(dev, k);
-    return e;
-}
+// Opts an instance in to its dynamic shared memory (above the 48 KB default), once.
+cudaError_t grad_prepare(KernelFn k, size_t smem) { return set_dyn_smem((const void *)k, smem); }
 
 template <int EP>
-KernelFn grad_by_d(int dp) {
+KernelFn grad_by_d(int dp, bool rec) {
     switch (dp) {
-        case 1: return grad_instance<1, EP>();
-        case 2: return grad_instance<2, EP>();
-        case 3: return grad_instance<3, EP>();
-        case 4: return grad_instance<4, EP>();
-        case 8: return grad_instance<8, EP>();
-        case 16: return grad_instance<16, EP>();
-        case 32: return grad_instance<32, EP>();
-        case 50: return grad_instance<50, EP>();
-        case 64: return grad_instance<64, EP>();
-        case 128: return grad_instance<128, EP>();
+        case 1: return grad_instance<1, EP>(rec);
+        case 2: return grad_instance<2, EP>(rec);
+        case 3: return grad_instance<3, EP>(rec);
+        case 4: return grad_instance<4, EP>(rec);
+        case 8: return grad_instance<8, EP>(rec);
+        case 16: return grad_instance<16, EP>(rec);
+        case 32: return grad_instance<32, EP>(rec);
+        case 50: return grad_instance<50, EP>(rec);
+        case 64: return grad_instance<64, EP>(rec);
+        case 128: return grad_instance<128, EP>(rec);
         default: return nullptr;
     }
 }
 
 KernelFn grad_kernel_for(const Instance &inst) {
     switch (inst.ek_pad) {
-        case 1: return grad_by_d<1>(inst.d_pad);
-        case 4: return grad_by_d<4>(inst.d_pad);
-        case 16: return grad_by_d<16>(inst.d_pad);
+        case 1: return grad_by_d<1>(inst.d_pad, inst.rec);
+        case 4: return grad_by_d<4>(inst.d_pad, inst.rec);
+        case 16: return grad_by_d<16>(inst.d_pad, inst.rec);
         default: return nullptr;
     }
 }

@@ -51,6 +51,13 @@ struct Args {
     // checks of debug builds (-DKR_DEBUG), which record a violated bound in *dbg.
     int64_t out_n, idx_n, ws_n;
     unsigned *dbg;
+    // Streamed records (instances with Instance::rec): tile-major pair records of y (and the
+    // signal or tile-relative log-weight), written by the prepass, read by cp.async; the
+    // LogSumExp's tile frames (EP floats a tile, base 2).  Element counts of one problem
+    // (rec_n, wtile_n) and batch strides (bs_rec, bs_wtile).
+    float *rec;
+    float *wtile;
+    int64_t rec_n, wtile_n, bs_rec, bs_wtile;
 };
 
 // Bits of the debug status word (debug builds; kr_device_status reports them << 8).
@@ -61,6 +68,7 @@ enum DebugBits : unsigned {
 // Compile-time shape of one kernel instance, chosen by the planner.
 struct Instance {
     int d_pad, ek_pad, rows, tile;
+    bool rec;  // y tiles streamed from prepass records (see streamed() in kr_config.h)
 };
 
 // Debug builds (-DKR_DEBUG): the device word of `dev` that the kernels' index checks
@@ -68,8 +76,9 @@ struct Instance {
 // could not be allocated.  Release builds never call it.
 unsigned *debug_word(int dev);
 
-// Instance selection (pure host logic).
-Instance choose_instance(int op, int D, int EK);
+// Instance selection (pure host logic).  kind: the kernel kind (KR_KERNEL_*) of a Sum; the
+// streamed variant (rec) serves the Gaussian Sum, LogSumExp and x-gradient up to D = 16.
+Instance choose_instance(int op, int D, int EK, int kind = 0);
 
 // Launchers, one per kernel family; they dispatch on the instance and return the
 // launch's cudaError_t.  grid = (row_blocks, S).
@@ -78,6 +87,16 @@ cudaError_t launch_lse(const Instance &inst, const Args &a, dim3 grid, cudaStrea
 cudaError_t launch_grad(const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
 cudaError_t launch_knn(const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);
 cudaError_t launch_combine(int op, const Instance &inst, const Args &a, cudaStream_t s);
+// Prepass of the streamed instances: packs y and b of op (Sum / grad: the signal; LSE: the
+// tile-relative log-weight and the tile frames) into a.rec (and a.wtile); grid = (tiles, 1,
+// batch).
+cudaError_t launch_pack(int op, const Instance &inst, const Args &a, int64_t tiles, cudaStream_t s);
+// Elements of the records and tile frames of one problem with N points.
+int64_t record_elems(const Instance &inst, int64_t N);
+int64_t wtile_elems(int op, const Instance &inst, int64_t N);
+// Opts kernel `fn` in to `smem` bytes of dynamic shared memory on the current device when
+// that is above the 48 KB default (once per device and kernel).
+cudaError_t set_dyn_smem(const void *fn, size_t smem);
 // Radial-kernel family (kr_radial.cuh): red 0 = Sum (Laplace, Cauchy, inverse
 // multiquadric), 1 = Max/Min (every kind); one launcher per kernel kind.
 cudaError_t launch_radial_gauss(int red, const Instance &inst, const Args &a, dim3 grid, cudaStream_t s);

@@ -91,8 +91,45 @@ __device__ __forceinline__ Args batch_view(const Args &a) {
     if (v.ws0) v.ws0 += z * a.bs_ws;
     if (v.ws1) v.ws1 += z * a.bs_ws;
     if (v.wsi) v.wsi += z * a.bs_ws;
+    if (v.rec) v.rec += z * a.bs_rec;
+    if (v.wtile) v.wtile += z * a.bs_wtile;
     return v;
 }
+
+// ---------------------------------------------------------------------------
+// Asynchronous tile copies (streamed records): 16-byte cp.async from global to shared
+// memory through L2 only (.cg), grouped per tile; cp.async.wait_all plus the block
+// barrier that follows make a tile visible to every thread.  These are hardware waits on
+// the thread's own copies, not spin loops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Starts the copy of record tile `t` (TF floats, TF % 4 == 0) into `dst`: every thread
+// copies 16-byte pieces t0 + threadIdx.x + k kThreads, coalesced.  Debug builds check the
+// pieces against the records' extent (a.rec_n) and skip those outside.
+template <int TF>
+__device__ __forceinline__ void issue_record_tile(const Args &a, float *dst, int64_t t) {
+    static_assert(TF % 4 == 0, "tiles are whole 16-byte pieces");
+    const float *src = a.rec + t * TF;
+    for (int c = threadIdx.x; c < TF / 4; c += kThreads) {
+#ifdef KR_DEBUG
+        if (t < 0 || t * TF + 4 * (int64_t)c + 3 >= a.rec_n) {
+            if (a.dbg) atomicOr(a.dbg, (unsigned)KRD_WS);
+            continue;
+        }
+#endif
+        cp_async16(dst + 4 * c, src + 4 * c);
+    }
+    cp_async_commit();
+}
+
+// Dynamic shared memory of the streamed kernels (two record tiles).
+extern __shared__ float4 kr_dyn_smem[];
 
 // Knuth's TwoSum: (hi, lo) += v with the rounding error of hi + v kept in lo.
 __device__ __forceinline__ void two_sum_add(float &hi, float &lo, float v) {

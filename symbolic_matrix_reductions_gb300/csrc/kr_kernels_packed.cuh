@@ -101,7 +101,14 @@ __device__ __forceinline__ float2 sq_dist_pair(const float2 (&x2)[DP], const flo
 // Sum / LogSumExp (packed).  Value fields: b_je (Sum) or W_e - w'_je (LSE), as in
 // fwd_kernel; the LSE tile frame and careful path are the same.
 // ---------------------------------------------------------------------------
-template <int DP, int EP, int R, int BN, bool LSE>
+//
+// REC (streamed records, D <= 16): the tiles come ready-made from the prepass (pack
+// kernel below): pair records of -y' and b (Sum) or of -y' and W - w' (LSE), with the
+// tile frame W in a.wtile.  They are copied into two shared-memory buffers with cp.async:
+// while the block scans tile k, the copy of tile k + 1 is in flight, and one barrier per
+// tile separates them.  a.chunk is then a multiple of BN, so every block's tiles are the
+// prepass's tiles.
+template <int DP, int EP, int R, int BN, bool LSE, bool REC>
 __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
     const Args a = batch_view(a_);
     if (a.tc_guard && __uint_as_float(a.tc_guard[0]) + __uint_as_float(a.tc_guard[1]) <= kTcNormLimit)
@@ -109,17 +116,23 @@ __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
     constexpr int PS2 = pair_stride(DP, EP);
     constexpr int UP = unroll_pairs(DP);
     constexpr int UPT = 2 * UP;
+    constexpr int TF = record_tile_floats(DP, EP, BN);
     constexpr float kLog2e = 1.4426950408889634f;
     static_assert(BN % UPT == 0, "tile must be a multiple of the unroll");
-    __shared__ __align__(16) float tile[(BN / 2) * PS2];
+    __shared__ __align__(16) float stile[REC ? 4 : TF];
     __shared__ float wmax[kThreads / 32][EP];
+    float *const tbuf = REC ? reinterpret_cast<float *>(kr_dyn_smem) : stile;
 
     const int t = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.x * (kThreads * R);
     const int64_t j_begin = (int64_t)blockIdx.y * a.chunk;
     const int64_t j_end = min(a.N, j_begin + a.chunk);
 
-    zero_pad_coords_pairs<DP, PS2, BN>(a, tile);
+    if constexpr (REC) {
+        if (j_begin < j_end) issue_record_tile<TF>(a, tbuf, j_begin / BN);
+    } else {
+        zero_pad_coords_pairs<DP, PS2, BN>(a, tbuf);
+    }
     float2 x2[R][DP];
     load_rows_pairs<DP, R>(a, row0, x2, a.c);
 
@@ -134,18 +147,33 @@ __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
             m[r][e] = est[r][e] = -f_inf();
         }
 
-    for (int64_t jt = j_begin; jt < j_end; jt += BN) {
+    int kt = 0;
+    for (int64_t jt = j_begin; jt < j_end; jt += BN, ++kt) {
         const int nv = (int)min((int64_t)BN, j_end - jt);
         const int nvp = (nv + UPT - 1) / UPT * UPT;
-        __syncthreads();
-        stage_coords_pairs<DP, PS2>(a, tile, jt, nv, nvp, -a.c, 0.f);
-
         float W[EP];
-        if (!LSE) {
+        const float *tile;
+        if constexpr (REC) {
+            tile = tbuf + (kt & 1) * TF;
+            if (LSE) {
+#pragma unroll
+                for (int e = 0; e < EP; ++e) W[e] = ldg_chk(a, (const float *)a.wtile, (jt / BN) * EP + e, a.wtile_n, KRD_WS);
+            }
+            cp_async_wait_all();
+            __syncthreads();  // tile kt landed; every thread is done with the other buffer
+            if (jt + BN < j_end) issue_record_tile<TF>(a, tbuf + ((kt + 1) & 1) * TF, jt / BN + 1);
+        } else {
+            tile = tbuf;
+            __syncthreads();
+            stage_coords_pairs<DP, PS2>(a, tbuf, jt, nv, nvp, -a.c, 0.f);
+        }
+
+        if (REC) {
+        } else if (!LSE) {
             for (int p = t; p < nvp; p += kThreads) {
 #pragma unroll
                 for (int e = 0; e < EP; ++e)
-                    *pair_slot<PS2>(tile, p, DP + e) = (p < nv && e < a.E) ? ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : 0.f;
+                    *pair_slot<PS2>(tbuf, p, DP + e) = (p < nv && e < a.E) ? ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : 0.f;
             }
         } else {
             float lmax[EP];
@@ -155,7 +183,7 @@ __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
 #pragma unroll
                 for (int e = 0; e < EP; ++e) {
                     const float v = (p < nv && e < a.E) ? kLog2e * ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : -f_inf();
-                    *pair_slot<PS2>(tile, p, DP + e) = v;
+                    *pair_slot<PS2>(tbuf, p, DP + e) = v;
                     lmax[e] = fmaxf(lmax[e], v);
                 }
             }
@@ -175,13 +203,13 @@ __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
             for (int p = t; p < nvp; p += kThreads) {
 #pragma unroll
                 for (int e = 0; e < EP; ++e) {
-                    float *slot = pair_slot<PS2>(tile, p, DP + e);
+                    float *slot = pair_slot<PS2>(tbuf, p, DP + e);
                     const float v = *slot;
                     *slot = (v == -f_inf()) ? f_inf() : W[e] - v;
                 }
             }
         }
-        __syncthreads();
+        if (!REC) __syncthreads();
 
         // ---- fast pass ------------------------------------------------------------
         // the Sum's loop is unrolled four steps deep (4 % faster at D = 3); the LogSumExp's is
@@ -334,21 +362,29 @@ __global__ void __launch_bounds__(kThreads) fwd2_kernel(const Args a_) {
 // ---------------------------------------------------------------------------
 // x-gradient (packed): the same sum as grad_kernel, two points per instruction.
 // ---------------------------------------------------------------------------
-template <int DP, int EP, int R, int BN>
+// REC: the tiles are streamed from the prepass records (-y', b), double-buffered, as in
+// fwd2_kernel.
+template <int DP, int EP, int R, int BN, bool REC>
 __global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a_) {
     const Args a = batch_view(a_);
     constexpr int PS2 = pair_stride(DP, EP);
     constexpr int UP = unroll_pairs(DP);
     constexpr int UPT = 2 * UP;
+    constexpr int TF = record_tile_floats(DP, EP, BN);
     static_assert(BN % UPT == 0, "tile must be a multiple of the unroll");
-    __shared__ __align__(16) float tile[(BN / 2) * PS2];
+    __shared__ __align__(16) float stile[REC ? 4 : TF];
+    float *const tbuf = REC ? reinterpret_cast<float *>(kr_dyn_smem) : stile;
 
     const int t = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.x * (kThreads * R);
     const int64_t j_begin = (int64_t)blockIdx.y * a.chunk;
     const int64_t j_end = min(a.N, j_begin + a.chunk);
 
-    zero_pad_coords_pairs<DP, PS2, BN>(a, tile);
+    if constexpr (REC) {
+        if (j_begin < j_end) issue_record_tile<TF>(a, tbuf, j_begin / BN);
+    } else {
+        zero_pad_coords_pairs<DP, PS2, BN>(a, tbuf);
+    }
     float2 x2[R][DP];
     load_rows_pairs<DP, R>(a, row0, x2, a.c);
     float gr[R][EP];
@@ -372,17 +408,27 @@ __global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a_) {
             hi[r][d] = lo[r][d] = 0.f;
         }
 
-    for (int64_t jt = j_begin; jt < j_end; jt += BN) {
+    int kt = 0;
+    for (int64_t jt = j_begin; jt < j_end; jt += BN, ++kt) {
         const int nv = (int)min((int64_t)BN, j_end - jt);
         const int nvp = (nv + UPT - 1) / UPT * UPT;
-        __syncthreads();
-        stage_coords_pairs<DP, PS2>(a, tile, jt, nv, nvp, -a.c, 0.f);
-        for (int p = t; p < nvp; p += kThreads) {
+        const float *tile;
+        if constexpr (REC) {
+            tile = tbuf + (kt & 1) * TF;
+            cp_async_wait_all();
+            __syncthreads();  // tile kt landed; every thread is done with the other buffer
+            if (jt + BN < j_end) issue_record_tile<TF>(a, tbuf + ((kt + 1) & 1) * TF, jt / BN + 1);
+        } else {
+            tile = tbuf;
+            __syncthreads();
+            stage_coords_pairs<DP, PS2>(a, tbuf, jt, nv, nvp, -a.c, 0.f);
+            for (int p = t; p < nvp; p += kThreads) {
 #pragma unroll
-            for (int e = 0; e < EP; ++e)
-                *pair_slot<PS2>(tile, p, DP + e) = (p < nv && e < a.E) ? ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : 0.f;
+                for (int e = 0; e < EP; ++e)
+                    *pair_slot<PS2>(tbuf, p, DP + e) = (p < nv && e < a.E) ? ldg_chk(a, a.b, (jt + p) * a.E + e, a.N * a.E, KRD_B) : 0.f;
+            }
+            __syncthreads();
         }
-        __syncthreads();
 
         for (int jj = 0; jj < nvp; jj += UPT) {
 #pragma unroll

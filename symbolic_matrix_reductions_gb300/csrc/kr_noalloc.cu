@@ -92,7 +92,8 @@ extern "C" int kernel_reduce_noalloc(const float *x, const float *y, const float
     if (ce != cudaSuccess) return KR_ERR_CUDA;
     int num_sms = 0;
     if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KR_ERR_CUDA;
-    const Instance in = choose_instance(op, D, E);
+    Instance in = choose_instance(op, D, E);
+    in.rec = false;  // the kernels stage their own tiles: no records, which would need memory
     const int occ = op == OP_SUM ? occupancy_sum(in) : occupancy_lse(in);
 
     // The planner's split for the CUDA-core kernel, at least 2, at most what the

@@ -178,7 +178,8 @@ def test_batch_option(lib):
     many = kr.KrPlan()
     assert lib.kr_plan(kr.OP_SUM, 2000, 100_000, 3, 1, 152, 8, ctypes.byref(o), ctypes.byref(many)) == kr.KR_OK
     assert many.split < one.split
-    assert many.workspace_bytes == 64 * (2 * many.split * 2000 * 4 if many.split > 1 else 0)
+    parts = 64 * (2 * many.split * 2000 * 4 if many.split > 1 else 0)
+    assert many.workspace_bytes == _r256(parts) + 64 * _record_bytes(kr.OP_SUM, 3, 1, 100_000)
     # batched tensor-core-sized Sums plan on the CUDA cores
     tc = kr.KrPlan()
     assert lib.kr_plan(kr.OP_SUM, 2000, 100_000, 50, 1, 152, 1, ctypes.byref(o), ctypes.byref(tc)) == kr.KR_OK
@@ -315,7 +316,8 @@ def test_split_covers_all_columns(lib, op, M, N, D, EK):
     bm = 128 if p.path == kr.KR_PATH_TENSOR_CORES else p.threads * p.rows_per_thread
     assert p.row_blocks == (M + bm - 1) // bm
     if p.split == 1:
-        assert p.workspace_bytes == 0
+        streamed = p.path == kr.KR_PATH_CUDA_CORES and op != kr.OP_KNN and D <= 16
+        assert p.workspace_bytes == (_record_bytes(op, D, EK, N) if streamed else 0)
 
 
 def test_split_fills_the_gpu_for_tall_products(lib):
@@ -370,7 +372,49 @@ def test_forced_split(lib):
     p = kr.plan(kr.OP_KNN, 1000, 5000, 16, 10, split=7)
     assert p.split == 7 and p.chunk == 715
     assert p.workspace_bytes == 7 * 1000 * 10 * 8
-    assert kr.plan(kr.OP_SUM, 10, 3, 3, 1, split=9).split == 3   # never more splits than columns
+    assert kr.plan(kr.OP_KNN, 10, 3, 3, 1, split=9).split == 3   # never more splits than columns
+    # streamed instances split on whole tiles: 3 columns are one 512-point tile
+    assert kr.plan(kr.OP_SUM, 10, 3, 3, 1, split=9).split == 1
+    assert kr.plan(kr.OP_SUM, 10, 3, 3, 1, split=9, kernel="laplace").split == 3
+
+
+def _r256(v):
+    return (v + 255) // 256 * 256
+
+
+def _record_bytes(op, D, E, N):
+    """Workspace of the streamed records of a Sum / LSE / gradient call at D <= 16: whole
+    tiles of pair records (points 2m, 2m+1 interleaved field by field, padded to 16 bytes),
+    and for the LogSumExp one frame per tile and column."""
+    dp = D if D <= 4 else 8 if D <= 8 else 16
+    ep = 1 if E <= 1 else 4 if E <= 4 else 16
+    ps2 = (2 * (dp + ep) + 3) // 4 * 4
+    bn = next(t for t in (512, 256, 128, 64, 32) if 16384 // ps2 >= t)
+    tiles = (N + bn - 1) // bn
+    return _r256(tiles * (bn // 2) * ps2 * 4) + (_r256(tiles * ep * 4) if op == kr.OP_LSE else 0)
+
+
+@pytest.mark.parametrize("op,D,E,N,split", [
+    (kr.OP_SUM, 3, 1, 100_000, 0), (kr.OP_LSE, 3, 1, 1_000_000, 0), (kr.OP_GRAD, 3, 1, 100_000, 7),
+    (kr.OP_SUM, 16, 4, 30_000, 5), (kr.OP_LSE, 8, 16, 9_999, 3), (kr.OP_GRAD, 16, 1, 70_001, 0),
+    (kr.OP_SUM, 1, 1, 513, 9),
+])
+def test_streamed_plan(lib, op, D, E, N, split):
+    """Gaussian Sum / LSE / gradient up to D = 16 stream prepass records: every split is whole
+    tiles (so each block's tiles are the prepass's), every split nonempty, and the workspace is
+    the split partials followed by the records (and the LogSumExp's tile frames)."""
+    M = 5000
+    p = kr.plan(op, M, N, D, E, num_sms=152, blocks_per_sm=4, split=split)
+    assert p.chunk % p.tile_points == 0
+    assert p.split * p.chunk >= N and (p.split - 1) * p.chunk < N
+    w = D if op == kr.OP_GRAD else E
+    parts = 2 * p.split * M * w * 4 if p.split > 1 else 0
+    assert p.workspace_bytes == _r256(parts) + _record_bytes(op, D, E, N)
+    # the other kernels, the K-min and D > 16 stream nothing
+    c = kr.plan(kr.OP_SUM, M, N, D, E, kernel="cauchy")
+    assert c.workspace_bytes == (2 * c.split * M * E * 4 if c.split > 1 else 0)
+    q = kr.plan(kr.OP_SUM, M, N, 32, E, path=kr.KR_PATH_CUDA_CORES, split=split)
+    assert q.workspace_bytes == (2 * q.split * M * E * 4 if q.split > 1 else 0)
 
 
 def test_python_marshalling_errors():
