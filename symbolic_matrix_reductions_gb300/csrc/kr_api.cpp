@@ -6,7 +6,8 @@
 // results a second kernel combines in a fixed order (split-j).  S is chosen to
 // minimise a model of the busiest SM's time: it runs ceil(blocks / SMs) blocks of
 // (chunk + per-tile overhead [+ K-min insertions]) work each, at full rate when it
-// holds at least 16 resident warps and proportionally slower below that.  So
+// holds at least 16 resident warps and proportionally slower below that, and (except
+// K-min) a little slower the fewer waves of blocks there are.  So
 // small-M / huge-N problems (the tall products of the GitHub issue "Transparent
 // interface for billion-scale matrices") still fill every SM, the last wave of a
 // large problem is not left mostly empty, and K-min, whose register list restarts
@@ -147,8 +148,12 @@ static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, const kr_op
 // their records to the workspace.
 static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm,
                 int forced_split, int64_t batch, int kind, kr_plan_t *p) {
-    const Instance in = choose_instance(op, D, EK, kind);
+    Instance in = choose_instance(op, D, EK, kind);
+    // Splits on whole tiles whether or not the call streams, so that the same split gives
+    // the same tiles (and the same bits) either way; batched problems are small, and there a
+    // prepass launch would cost more than streaming saves.
     const int64_t align = in.rec ? in.tile : 1;
+    if (batch > 1) in.rec = false;
     p->path = KR_PATH_CUDA_CORES;
     p->d_pad = in.d_pad;
     p->ek_pad = in.ek_pad;
@@ -192,10 +197,18 @@ static int plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int bl
             const int64_t per_sm = (p->row_blocks * s * batch + num_sms - 1) / num_sms;
             const int64_t conc = std::min<int64_t>(per_sm, blocks_per_sm);
             const double eff = std::min(1.0, (double)(conc * (kThreads / 32)) / 16.0);
+            // Load balance: with few waves of large blocks the slowest SM sets the end; with
+            // more, smaller blocks the faster SMs take more of them.  Fitted on forced-split
+            // timings of the D = 3 x-gradient at M = N = 1e5 (3 splits, 0.97 waves, 7 % slower
+            // than 10 splits, 3.2 waves).  K-min keeps its own insertion term instead (its
+            // lists restart in every split).
+            const double waves = (double)(p->row_blocks * s * batch) / ((double)num_sms * blocks_per_sm);
+            const double balance = op == OP_KNN ? 1.0 : 1.0 + 0.136 / waves;
             // each split also costs a little in partial traffic and the combine, and splitting
             // at all costs a workspace allocation and a combine launch (worth ~4096 points of
             // one block's work, about 60 us)
-            const double cost = (double)per_sm * work / eff * (1.0 + 0.002 * (double)s) + (s > 1 ? 4096.0 : 0.0);
+            const double cost =
+                (double)per_sm * work / eff * balance * (1.0 + 0.002 * (double)s) + (s > 1 ? 4096.0 : 0.0);
             if (s == 1 || cost < best * 0.999) {
                 best = cost;
                 S = (int)s;
@@ -557,7 +570,9 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
     if (device_info(dev, op, kind, in, &num_sms, &occ) != 0) return cuda_fail(cudaGetLastError());
     kr_plan_t p;
     const bool tc = !rt && tc_eligible(op, a.M, a.N, a.D, EK, opt) && tc_available();
-    if (tc || rt) in.rec = false;  // the tensor-core stand-in and the block-sparse kernels stage their own tiles
+    // the tensor-core stand-in and the block-sparse kernels stage their own tiles, and so do
+    // batched calls (small problems, where a prepass launch would cost more than it saves)
+    if (tc || rt || B > 1) in.rec = false;
     if (tc) {
         plan_tc(a.M, a.N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, &p);
     } else {

@@ -93,6 +93,7 @@ KR_HD constexpr int tile_points_packed(int PS2) {
 // log-weight) once into tile-aligned pair records in device memory, and the reduction
 // kernel copies each tile into shared memory with 16-byte cp.async, double-buffered, so
 // the next tile's copy overlaps the current tile's scan and a tile costs one barrier.
+// Batched calls (many small problems) keep the kernels' own staging.
 KR_HD constexpr bool streamed(int DP) { return DP <= 16; }
 // Floats of one tile of pair records (BN points).
 KR_HD constexpr int record_tile_floats(int DP, int EP, int BN) { return (BN / 2) * pair_stride(DP, EP); }

@@ -40,6 +40,19 @@ __device__ __forceinline__ float lg2_approx(float v) {
 
 __device__ __forceinline__ float f_inf() { return __int_as_float(0x7f800000); }
 
+// max(a, b, c) and min(a, b, c) in one instruction each (the three-input max.f32 /
+// min.f32 of sm_100 and later); a NaN input is passed over as fmaxf / fminf pass it over.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Checked global accesses.  Release builds compile them to the plain access; debug
 // builds (-DKR_DEBUG) first check the element index against the array's extent and, on
 // a violation, set the array's bit in the status word a.dbg and skip the access (a load

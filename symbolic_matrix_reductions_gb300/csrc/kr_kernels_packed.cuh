@@ -881,7 +881,7 @@ __global__ void __launch_bounds__(kThreads, knn_min_blocks(DP, KP)) knnx_kernel(
                 for (int r = 0; r < R; ++r) {
                     float mn = fminf(f[0][r].x, f[0][r].y);
 #pragma unroll
-                    for (int u = 1; u < UP; ++u) mn = fminf(mn, fminf(f[u][r].x, f[u][r].y));
+                    for (int u = 1; u < UP; ++u) mn = fmin3(mn, f[u][r].x, f[u][r].y);
                     const bool pass = !(mn > T[r]);
                     m[r] |= pass ? (1u << gg) : 0u;
                     any |= pass;

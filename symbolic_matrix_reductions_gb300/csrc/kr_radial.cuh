@@ -70,6 +70,7 @@ template <> struct Lanes<1> {
     static __device__ __forceinline__ T fma(T a, T b, T c) { return __fmaf_rn(a, b, c); }
     static __device__ __forceinline__ float lane(T v, int) { return v; }
     static __device__ __forceinline__ float hmax(T v) { return v; }
+    static __device__ __forceinline__ float max_into(float m, T v) { return fmaxf(m, v); }
     static __device__ __forceinline__ float hsum(T v) { return v; }
     template <int KT>
     static __device__ __forceinline__ T kval(T q) { return radial_value<KT>(q); }
@@ -82,6 +83,7 @@ template <> struct Lanes<2> {
     static __device__ __forceinline__ T fma(T a, T b, T c) { return __ffma2_rn(a, b, c); }
     static __device__ __forceinline__ float lane(T v, int l) { return l ? v.y : v.x; }
     static __device__ __forceinline__ float hmax(T v) { return fmaxf(v.x, v.y); }
+    static __device__ __forceinline__ float max_into(float m, T v) { return fmax3(m, v.x, v.y); }
     static __device__ __forceinline__ float hsum(T v) { return v.x + v.y; }
     template <int KT>
     static __device__ __forceinline__ T kval(T q) { return make_float2(radial_value<KT>(q.x), radial_value<KT>(q.y)); }
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
 #pragma unroll
                         for (int e = 0; e < EP; ++e)
 #pragma unroll
-                            for (int u = 0; u < UR; ++u) bm[r][e] = fmaxf(bm[r][e], V::hmax(kv[u][r][e]));
+                            for (int u = 0; u < UR; ++u) bm[r][e] = V::max_into(bm[r][e], kv[u][r][e]);
                 }
 #pragma unroll
                 for (int r = 0; r < R; ++r)
