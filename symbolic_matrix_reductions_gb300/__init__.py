@@ -385,8 +385,9 @@ def kernel_reduce_noalloc(x, y, b, sigma: float, reduction: str, out):
     return out
 
 
-def kernel_reduce_grad_x(x, y, b, g, sigma: float, out=None, split: int = 0):
-    """Gradient wrt x of sum_ie g_ie a_ie (a the Sum reduction); returns (M, D) or (B, M, D)."""
+def kernel_reduce_grad_x(x, y, b, g, sigma: float, out=None, split: int = 0, path: int = 0):
+    """Gradient wrt x of sum_ie g_ie a_ie (a the Sum reduction); returns (M, D) or (B, M, D).
+    path: KR_PATH_AUTO (tensor cores for 32 <= D <= 62, E = 1) or KR_PATH_CUDA_CORES."""
     B, x, y, M, N, D = _clouds(x, y)
     b = _mat(b, N, "b", B=B)
     E = b.shape[-1]
@@ -397,7 +398,7 @@ def kernel_reduce_grad_x(x, y, b, g, sigma: float, out=None, split: int = 0):
     out = _mat(out, M, "out", D, B=B)
     _same_device(x, out)
     st = load_library().kernel_reduce_grad_x_ex(_ptr(x), _ptr(y), _ptr(b), _ptr(g), _ptr(out), M, N, D, E,
-                                                float(sigma), _stream(dev), _options(split, batch=B))
+                                                float(sigma), _stream(dev), _options(split, path, batch=B))
     _check(st, "kernel_reduce_grad_x")
     return out
 

@@ -85,19 +85,23 @@ static const int64_t kTcChunkMax = (int64_t)3 << 16;     // points per tensor-pa
 
 static int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
-// Tensor-core Sum plan: kTcRows rows per block (one TMEM lane each), tiles of
-// kTcCols points, splits on tile boundaries, one block per SM.
-static void plan_tc(int64_t M, int64_t N, int num_sms, int blocks_per_sm, int forced_split, kr_plan_t *p) {
+// Tensor-core plan: kTcRows rows per block (one TMEM lane each), tiles of kTcCols points
+// (the x-gradient: kTcGradCols), splits on tile boundaries, one block per SM.  Split
+// partials: M values (Sum, LSE) or M x D (the gradient) per split.
+static void plan_tc(int op, int64_t M, int64_t N, int D, int num_sms, int blocks_per_sm, int forced_split,
+                    kr_plan_t *p) {
+    const int tile = op == OP_GRAD ? kTcGradCols : kTcCols;
+    const int64_t width = op == OP_GRAD ? D : 1;
     p->d_pad = 64;
     p->ek_pad = 1;
     p->rows_per_thread = 1;
     p->threads = kTcThreads;
-    p->tile_points = kTcCols;
+    p->tile_points = tile;
     p->row_blocks = (M + kTcRows - 1) / kTcRows;
     p->path = KR_PATH_TENSOR_CORES;
     if (num_sms < 1) num_sms = 1;
     if (blocks_per_sm < 1) blocks_per_sm = 1;
-    const int64_t tiles_total = std::max<int64_t>(1, (N + kTcCols - 1) / kTcCols);
+    const int64_t tiles_total = std::max<int64_t>(1, (N + tile - 1) / tile);
     int S = 1;
     if (forced_split >= 1) {
         S = (int)std::min<int64_t>(std::min<int64_t>(forced_split, tiles_total), kMaxSplit);
@@ -106,13 +110,17 @@ static void plan_tc(int64_t M, int64_t N, int num_sms, int blocks_per_sm, int fo
         // at slightly different paces; while a split's operands (256 B per point) fit
         // in L2 every block after the first reads them from there.  Longer splits
         // fall out of L2 and the copy latency of the misses stalls the MMAs.
-        const int64_t min_split = std::min<int64_t>((N + kTcChunkMax - 1) / kTcChunkMax, kMaxSplit);
+        // The partials cap the splits too (the gradient's are D times larger): when L2 residency
+        // asks for more splits than the cap allows, take as many as it allows.
+        const int64_t s_cap = std::max<int64_t>(
+            1, std::min<int64_t>(std::min<int64_t>(kMaxSplit, tiles_total),
+                                 kMaxWorkspace / std::max<int64_t>(1, 2 * M * width * (int64_t)sizeof(float))));
+        const int64_t min_split = std::min<int64_t>((N + kTcChunkMax - 1) / kTcChunkMax, s_cap);
         // per block: its tiles plus a fixed start-up cost of about 1/8 tile
         double best = 0.0;
-        for (int64_t s = std::max<int64_t>(1, min_split); s <= std::min<int64_t>(kMaxSplit, tiles_total); ++s) {
-            if (2 * s * M * (int64_t)sizeof(float) > kMaxWorkspace) break;
-            const int64_t chunk = round_up((N + s - 1) / s, kTcCols);
-            const double work = (double)(chunk / kTcCols) + 0.125;
+        for (int64_t s = std::max<int64_t>(1, min_split); s <= s_cap; ++s) {
+            const int64_t chunk = round_up((N + s - 1) / s, tile);
+            const double work = (double)(chunk / tile) + 0.125;
             const int64_t per_sm = (p->row_blocks * s + num_sms - 1) / num_sms;
             const double cost = (double)per_sm * work * (1.0 + 0.002 * (double)s);
             if (best == 0.0 || cost < best * 0.999) {
@@ -121,21 +129,23 @@ static void plan_tc(int64_t M, int64_t N, int num_sms, int blocks_per_sm, int fo
             }
         }
     }
-    p->chunk = round_up((std::max<int64_t>(N, 1) + S - 1) / S, kTcCols);
+    p->chunk = round_up((std::max<int64_t>(N, 1) + S - 1) / S, tile);
     S = (int)std::max<int64_t>(1, (N + p->chunk - 1) / p->chunk);  // every split nonempty
     p->split = S;
     const int64_t n_pad = round_up(std::max<int64_t>(N, 1), kTcCols);
     // split fp16 operands (256 B a point), the padded signal / weights, the LSE tile frames
     const int64_t operands = (round_up(std::max<int64_t>(M, 1), kTcRows) + n_pad) * 256 + n_pad * 4 +
                              round_up(n_pad / kTcCols * 4, 256);
-    p->workspace_bytes = 256 + operands + (S > 1 ? 2 * (int64_t)S * M * (int64_t)sizeof(float) : 0);
+    p->workspace_bytes = 256 + operands + (S > 1 ? 2 * (int64_t)S * M * width * (int64_t)sizeof(float) : 0) +
+                         (op == OP_GRAD ? round_up((int64_t)S * M, 256) : 0);  // the gradient's weak-row flags
 }
 
 static int64_t batch_of(const kr_options *opt) { return opt && opt->batch > 1 ? opt->batch : 1; }
 
 static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, const kr_options *opt) {
     const int path = opt ? opt->path : 0, kind = opt ? opt->kernel : KR_KERNEL_GAUSSIAN;
-    if ((op != OP_SUM && op != OP_LSE) || kind != KR_KERNEL_GAUSSIAN || path == KR_PATH_CUDA_CORES || !tc_dims(D, EK))
+    if ((op != OP_SUM && op != OP_LSE && op != OP_GRAD) || kind != KR_KERNEL_GAUSSIAN || path == KR_PATH_CUDA_CORES ||
+        !tc_dims(D, EK))
         return false;
     if (op == OP_LSE && D > kTcLseMaxD) return false;  // the weight takes one more operand slot
     if (batch_of(opt) > 1) return false;  // the tensor-core prepass and tiles serve one problem
@@ -466,7 +476,8 @@ static double kernel_prescale(int kind, float sigma) {
 // CUDA-core kernel is always launched after the tensor kernel with the same splits;
 // it returns at once unless the prepass found norms the expansion cannot serve.
 static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in, char *ws, cudaStream_t stream) {
-    const bool lse = op == OP_LSE;
+    const bool lse = op == OP_LSE, grad = op == OP_GRAD;
+    const int64_t width = grad ? a.D : 1;  // split partials per row
     const int64_t m_pad = round_up(a.M, kTcRows), n_pad = round_up(std::max<int64_t>(a.N, 1), kTcCols);
     unsigned *guard = (unsigned *)ws;
     __half *a_hi = (__half *)(ws + 256);
@@ -476,16 +487,19 @@ static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in
     float *bpad = (float *)(b_lo + n_pad * 64);
     float *fpad = bpad + n_pad;
     float *part = (float *)((char *)fpad + round_up(n_pad / kTcCols * 4, 256));
+    // the x-gradient's flags (S x M bytes) follow the split partials
+    uint8_t *flags = (uint8_t *)(part + (p.split > 1 ? 2 * (int64_t)p.split * a.M * width : 0));
     cudaError_t ce = cudaMemsetAsync(guard, 0, 256, stream);
     if (ce == cudaSuccess)
         ce = tc_launch_prep(a.x, a.M, m_pad, a.D, a.c, true, lse, a_hi, a_lo, guard, nullptr, nullptr, nullptr,
                             stream);
+    if (ce == cudaSuccess && grad) ce = tc_launch_bmax(a.b, a.N, guard, stream);
     if (ce == cudaSuccess)
         ce = tc_launch_prep(a.y, a.N, n_pad, a.D, a.c, false, lse, b_hi, b_lo, guard + 1, a.b, lse ? nullptr : bpad,
-                            lse ? fpad : nullptr, stream);
+                            lse ? fpad : nullptr, stream, grad);
     if (p.split > 1) {
         a.ws0 = part;
-        a.ws1 = part + (int64_t)p.split * a.M;
+        a.ws1 = part + (int64_t)p.split * a.M * width;
     }
     if (ce == cudaSuccess) {
         TcArgs t{};
@@ -514,13 +528,21 @@ static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in
         t.N = a.N;
         t.chunk = p.chunk;
         t.S = p.split;
-        ce = tc_launch_sum(t, dim3((unsigned)p.row_blocks, (unsigned)p.split), stream);
+        t.x = a.x;
+        t.g = a.g;
+        t.D = a.D;
+        t.c = a.c;
+        t.gscale = a.gscale;
+        t.flags = flags;
+        const dim3 tgrid((unsigned)p.row_blocks, (unsigned)p.split);
+        ce = grad ? tc_launch_grad(t, tgrid, stream) : tc_launch_sum(t, tgrid, stream);
     }
     if (ce == cudaSuccess) {  // the CUDA-core stand-in: returns at once unless the guard failed
         a.tc_guard = guard;
+        a.tc_flags = grad ? flags : nullptr;  // (or, for the gradient, on the rows flagged weak)
         const int64_t bm = (int64_t)kThreads * in.rows;
         const dim3 grid((unsigned)((a.M + bm - 1) / bm), (unsigned)p.split);
-        ce = lse ? launch_lse(in, a, grid, stream) : launch_sum(in, a, grid, stream);
+        ce = grad ? launch_grad(in, a, grid, stream) : lse ? launch_lse(in, a, grid, stream) : launch_sum(in, a, grid, stream);
     }
     if (ce == cudaSuccess && p.split > 1) ce = launch_combine(op, in, a, stream);
     return ce;
@@ -574,7 +596,7 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
     // batched calls (small problems, where a prepass launch would cost more than it saves)
     if (tc || rt || B > 1) in.rec = false;
     if (tc) {
-        plan_tc(a.M, a.N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, &p);
+        plan_tc(op, a.M, a.N, a.D, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, &p);
     } else {
         plan(op, a.M, a.N, a.D, EK, num_sms, occ, opt ? opt->split : 0, B, kind, &p);
         if (rt) {  // one block per table entry and split; the tables lead the workspace
@@ -1005,7 +1027,7 @@ int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks
     const int st = validate(op, nullptr, 0, M, N, D, EK, 1.f, opt);
     if (st != KR_OK) return st;
     if (tc_eligible(op, M, N, D, EK, opt)) {
-        plan_tc(M, N, num_sms, blocks_per_sm, opt ? opt->split : 0, out);
+        plan_tc(op, M, N, D, num_sms, blocks_per_sm, opt ? opt->split : 0, out);
         return KR_OK;
     }
     return plan(op, M, N, D, EK, num_sms, blocks_per_sm, opt ? opt->split : 0, batch_of(opt),
@@ -1024,7 +1046,7 @@ int kr_plan_device(int op, int64_t M, int64_t N, int D, int EK, const kr_options
     if (device_info(dev, op, kind, choose_instance(op, D, EK, kind), &num_sms, &occ) != 0)
         return cuda_fail(cudaGetLastError());
     if (tc_eligible(op, M, N, D, EK, opt) && tc_available()) {
-        plan_tc(M, N, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, out);
+        plan_tc(op, M, N, D, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, out);
         return KR_OK;
     }
     return plan(op, M, N, D, EK, num_sms, occ, opt ? opt->split : 0, batch_of(opt), kind, out);

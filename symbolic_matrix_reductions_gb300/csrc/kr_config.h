@@ -60,6 +60,10 @@ constexpr int kTcThreads = 320;
 KR_HD constexpr bool tc_dims(int D, int E) { return E == 1 && D >= 32 && D <= 62; }
 // The tensor-core LogSumExp adds the tile-relative log-weight as one more slot.
 constexpr int kTcLseMaxD = 61;
+// Tensor-core x-gradient: points per tile (the N of its first product and the K of its
+// second, P . [y' | 1]); same coordinate range as the Sum (the second product reads the
+// augmented B tile, whose slot D holds 1).
+constexpr int kTcGradCols = 128;
 
 // Independent partial sums of a squared distance: at large D one fma chain over the
 // coordinates is a long dependency chain (4 cycles a link) with few rows per thread to

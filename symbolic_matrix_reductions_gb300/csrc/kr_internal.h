@@ -36,8 +36,9 @@ struct Args {
     float gscale;        // grad: -2 / (sigma^2 c)
     int64_t chunk;       // columns per split
     int S;
-    const unsigned *tc_guard;  // Sum only: non-null when the tensor-core kernel ran first;
-                               // the CUDA-core kernel then works only if the norms failed it
+    const unsigned *tc_guard;  // non-null when the tensor-core kernel ran first; the CUDA-core
+                               // kernel then works only if the guard failed it ...
+    const uint8_t *tc_flags;   // ... or (x-gradient) on the rows this flag array (S x M) marks
     float vsign;         // Max/Min: +1 (Max) or -1 (Min, computed as -Max of k (-b))
     // Batch dimension: blockIdx.z selects one of `batch` independent problems whose
     // arrays follow each other in memory; the strides are in elements (0 when batch == 1).

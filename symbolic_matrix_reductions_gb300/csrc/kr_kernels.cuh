@@ -690,6 +690,14 @@ __global__ void __launch_bounds__(kThreads) gradw_kernel(const Args a_) {
 
     const int t = threadIdx.x;
     const int64_t i = (int64_t)blockIdx.x * kThreads + t;
+    // After the tensor-core gradient: nothing to do if its guard held (norms, a finite signal),
+    // except the rows of this split it flagged as too weak for its fp16 P tile.
+    bool mine = true;
+    if (a.tc_guard && __uint_as_float(a.tc_guard[0]) + __uint_as_float(a.tc_guard[1]) <= kTcNormLimit &&
+        __uint_as_float(a.tc_guard[2]) <= 3.0e38f) {
+        mine = a.tc_flags && i < a.M && a.tc_flags[(int64_t)blockIdx.y * a.M + i] != 0;
+        if (!__syncthreads_or(mine)) return;
+    }
     const int64_t j_begin = (int64_t)blockIdx.y * a.chunk;
     const int64_t j_end = min(a.N, j_begin + a.chunk);
 
@@ -766,7 +774,7 @@ __global__ void __launch_bounds__(kThreads) gradw_kernel(const Args a_) {
         }
     }
 
-    if (i >= a.M) return;
+    if (i >= a.M || !mine) return;
     const float sc = (EP == 1) ? a.gscale * gr[0] : a.gscale;
 #pragma unroll
     for (int d = 0; d < DP; ++d) {

@@ -1,4 +1,5 @@
-// kr_tc.cu -- tensor-core (tcgen05) path of the Gaussian Sum for 32 <= D <= 62, E = 1.
+// kr_tc.cu -- tensor-core (tcgen05) path of the Gaussian Sum, LogSumExp and x-gradient
+// for 32 <= D <= 62, E = 1 (the x-gradient's two products are described at its kernel).
 //
 // The exponent of the prescaled Gaussian is a dot product of augmented vectors:
 //   -|x' - y'|^2 = 2 x'.y' - |x'|^2 - |y'|^2 = A_i . B_j,
@@ -94,12 +95,23 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// D[tmem] (+)= A[smem] . B[smem]^T, fp16 operands, fp32 accumulation.
-__device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t accumulate) {
+// The same tile read MN-major (the gradient's second product reads the B tile's point
+// rows as its K dimension): N = 64 fp16 is one 128-byte swizzle row, so only the stride
+// between 8-row groups along K matters (1024 B); the other byte offset is given the same
+// value, so it is right whichever of the two fields the layout takes it from.
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)(1024 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T, fp16 operands, fp32 accumulation (instruction
+// descriptor idesc: shapes and operand majors).
+__device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t accumulate,
+                                        uint32_t idesc = kIdesc) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
-        "l"(ad), "l"(bd), "r"(kIdesc), "r"(accumulate));
+        "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
@@ -194,8 +206,38 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
                  : "r"(taddr));
 }
 
+// One warp reads n consecutive fp32 columns of its 32 TMEM lanes (one row per lane).
+__device__ __forceinline__ void tmem_ld32x32b_x64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+                 : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31]),"=r"(r[32]),"=r"(r[33]),"=r"(r[34]),"=r"(r[35]),"=r"(r[36]),"=r"(r[37]),"=r"(r[38]),"=r"(r[39]),"=r"(r[40]),"=r"(r[41]),"=r"(r[42]),"=r"(r[43]),"=r"(r[44]),"=r"(r[45]),"=r"(r[46]),"=r"(r[47]),"=r"(r[48]),"=r"(r[49]),"=r"(r[50]),"=r"(r[51]),"=r"(r[52]),"=r"(r[53]),"=r"(r[54]),"=r"(r[55]),"=r"(r[56]),"=r"(r[57]),"=r"(r[58]),"=r"(r[59]),"=r"(r[60]),"=r"(r[61]),"=r"(r[62]),"=r"(r[63])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31])
+                 : "r"(taddr));
+}
+
 __device__ __forceinline__ bool norms_ok(const unsigned *guard) {
     return __uint_as_float(guard[0]) + __uint_as_float(guard[1]) <= kTcNormLimit;
+}
+
+// The power of two 2^e >= m (m >= 0 finite; 1 for m = 0): the x-gradient scales its signal
+// by 2^-e into [-1, 1], which keeps the fp16 P tile from overflowing, and scales back.
+__device__ __forceinline__ float pow2_above(float m) {
+    if (!(m > 0.f)) return 1.f;
+    int e;
+    frexpf(m, &e);  // m = f 2^e, 0.5 <= f < 1
+    return ldexpf(1.f, e);
+}
+
+// x-gradient signal bound: guard[2] = the largest |b| (float bits), written by tc_bmax_kernel.
+__global__ void __launch_bounds__(256) tc_bmax_kernel(const float *b, int64_t n, unsigned *gmax) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    float m = r < n ? fabsf(__ldg(b + r)) : 0.f;  // a NaN becomes NaN bits, above +inf: the guard fails
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = __uint_as_float(max(__float_as_uint(m), __float_as_uint(__shfl_xor_sync(0xffffffffu, m, o))));
+    if ((threadIdx.x & 31) == 0) atomicMax(gmax, __float_as_uint(m));
 }
 
 // ---------------------------------------------------------------------------
@@ -209,9 +251,12 @@ __device__ __forceinline__ bool norms_ok(const unsigned *guard) {
 // F_k = max over the tile of w' = w log2 e goes to fpad[k] and the slot holds
 // max(w'_r - F_k, -1024) <= 0 (-1024 past `rows`), so every term 2^(t + slot) of the
 // tile is at most 1 in the frame F_k.
+// bmax non-null (the x-gradient): bpad[r] = b[r] / 2^e in point order (the gradient's
+// evaluation reads it so), 2^e = pow2_above(largest |b|), instead of the Sum's per-thread order.
 __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t rows, int64_t rows_pad, int D,
                                                       float c, int is_x, int lse, __half *hi, __half *lo,
-                                                      unsigned *guard, const float *b, float *bpad, float *fpad) {
+                                                      unsigned *guard, const float *b, float *bpad, float *fpad,
+                                                      const unsigned *bmax) {
     __shared__ float wmax[8];
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= rows_pad) return;  // with fpad, rows_pad is a multiple of 256: whole blocks leave together
@@ -240,7 +285,11 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t 
         }
         atomicMax(guard, __float_as_uint(n));
     }
-    if (bpad && !fpad) {
+    if (bpad && !fpad && bmax) {
+        const float m = __uint_as_float(*bmax);
+        const float inv = (m <= 3.0e38f) ? 1.f / pow2_above(m) : 0.f;  // an exact power of two
+        bpad[r] = live ? __ldg(b + r) * inv : 0.f;
+    } else if (bpad && !fpad) {
         // Sum: b in the order the evaluation threads read it.  Column c of a 256-point tile
         // is c0 + 8 kk + 2 q + e (c0 = 0 or 128, kk < 16, q < 4, e < 2) and thread q of each
         // quad of lanes takes columns c0 + 8 kk + 2 q + e, so it goes to c0 + 32 q + 2 kk + e:
@@ -543,6 +592,342 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_lse_kernel(const __grid_cons
     tc_body<true>(p);
 }
 
+// One warp writes n consecutive fp32 columns of its 32 TMEM lanes (one row per lane).
+__device__ __forceinline__ void tmem_st32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr), "r"(r[0]),"r"(r[1]),"r"(r[2]),"r"(r[3]),"r"(r[4]),"r"(r[5]),"r"(r[6]),"r"(r[7]),"r"(r[8]),"r"(r[9]),"r"(r[10]),"r"(r[11]),"r"(r[12]),"r"(r[13]),"r"(r[14]),"r"(r[15]),"r"(r[16]),"r"(r[17]),"r"(r[18]),"r"(r[19]),"r"(r[20]),"r"(r[21]),"r"(r[22]),"r"(r[23]),"r"(r[24]),"r"(r[25]),"r"(r[26]),"r"(r[27]),"r"(r[28]),"r"(r[29]),"r"(r[30]),"r"(r[31])
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// x-gradient (tc_grad_kernel), 32 <= D <= 62, E = 1:
+//   gx_id = gscale g_i sum_j k_ij b_j (x'_id - y'_jd) = gscale g_i (x'_id s0_i - s_id),
+//   s0_i = sum_j P_ij,  s_id = sum_j P_ij y'_jd,  P_ij = k_ij b_j = 2^(S_ij) b_j.
+// Both contractions run on the tensor cores.  Per tile of kGCols = 128 points:
+//   MMA 1: S = A . B^T as for the Sum (N = 128), into one of two TMEM accumulators;
+//   evaluation warps: P = 2^S b in fp32, split P = hi + lo (fp16 each) and written into
+//     the shared-memory P tile (K-major over the tile's points, 128-byte swizzle);
+//   MMA 2: D2 += P . [y' | 1 | ...], where the right operand is the same B tile read
+//     MN-major (its point rows are now the K dimension): column d < D of D2 is s_id and
+//     column D (B's slot of 1) is s0_i; products Phi.Bhi + Phi.Blo + Plo.Bhi, fp32, in one
+//     of two further TMEM accumulators, each summing kGGroup tiles;
+//   evaluation warps fold each group's D2 into compensated (TwoSum) running sums, kept in
+//     TMEM too, so that a warp's registers hold only the tile in flight.
+// s0 and s come from the same rounded P, so the cancellation in x' s0 - s leaves only the
+// operands' own rounding (about 2^-22 of them) against sum_j |P_ij| |x'_id - y'_jd|, the
+// tolerance's scale.  The MMA issuer runs the first products two tiles ahead of the
+// second, so the next S is computed while the warps turn the last one into P.
+// Block = 10 warps (TMA producer, MMA issuer, 8 evaluation warps); TMEM columns [0, 256):
+// two S accumulators of 128; [256, 384): two D2 accumulators of 64; [384, 512): the
+// running sums (hi at 384 + c, lo at 448 + c for D2 column c).  Evaluation warp w reads
+// TMEM lanes 32 (w mod 4).. (its rows) and takes S columns 64 h.. and D2 columns 32 h..
+// (h = (w - 2) / 4).
+// ---------------------------------------------------------------------------
+constexpr int kGCols = kTcGradCols;
+constexpr int kGStages = 3;
+constexpr int kGGroup = 4;                      // tiles summed in one D2 accumulator
+constexpr int kGBTileBytes = kGCols * 128;      // 128 points x 64 fp16
+constexpr int kGStageBytes = 2 * kGBTileBytes;  // hi, lo
+constexpr int kGPHalfBytes = kRows * 128;       // 128 rows x 64 points fp16: one K half of P
+constexpr int kGPBytes = 4 * kGPHalfBytes;      // hi (two K halves), lo (two K halves)
+constexpr int kGSmemBytes = 2 * kATileBytes + kGStages * kGStageBytes + kGPBytes + 1024;
+static_assert(kGSmemBytes + 512 <= 227 * 1024, "shared memory per block");
+static_assert(kGPBytes >= kRows * 64 * 2 * 4, "the P tile holds the final (hi, lo) sums");
+// MMA 1: M = 128, N = 128, both K-major.  MMA 2: M = 128, N = 64, A K-major, B MN-major.
+constexpr uint32_t kIdescG1 = (1u << 4) | ((uint32_t)(kGCols >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+constexpr uint32_t kIdescG2 = (1u << 4) | (1u << 16) | ((uint32_t)(64 >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+constexpr int kGTmemS = 0, kGTmemD2 = 2 * kGCols, kGTmemRun = kGTmemD2 + 128;
+
+__global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    // a_full, full[3], empty[3], s_full[2], s_empty[2], d2_full[2], d2_empty[2], p_full, p_empty, drain
+    __shared__ __align__(8) uint64_t bars[1 + 2 * kGStages + 8 + 3];
+    __shared__ float pmx[2][kRows];  // largest |P| of each row's two column halves
+    if (!norms_ok(p.guard) || !(__uint_as_float(p.guard[2]) <= 3.0e38f))
+        return;  // the CUDA-core kernel does this call's work
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t s_a_hi = smem_addr(smem), s_a_lo = s_a_hi + kATileBytes;
+    const uint32_t s_stage0 = s_a_hi + 2 * kATileBytes;
+    uint8_t *const pbuf = smem + 2 * kATileBytes + kGStages * kGStageBytes;
+    const uint32_t s_p = smem_addr(pbuf);  // P hi: K halves at +0, +kGPHalfBytes; P lo after them
+    const uint32_t b_a_full = smem_addr(&bars[0]);
+    const uint32_t b_full0 = b_a_full + 8, b_empty0 = b_full0 + 8 * kGStages;
+    const uint32_t b_sf0 = b_empty0 + 8 * kGStages, b_se0 = b_sf0 + 16;
+    const uint32_t b_df0 = b_se0 + 16, b_de0 = b_df0 + 16;
+    const uint32_t b_pfull = b_de0 + 16, b_pempty = b_pfull + 8, b_drain = b_pempty + 8;
+    volatile int *abort = &abort_flag;
+
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    const int64_t row0 = (int64_t)blockIdx.x * kRows;
+    const int64_t j_begin = (int64_t)blockIdx.y * p.chunk;
+    const int64_t j_end = min(p.N, j_begin + p.chunk);
+    const int T = j_end > j_begin ? (int)((j_end - j_begin + kGCols - 1) / kGCols) : 0;
+
+    if (w == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_slot)),
+                     "r"(512));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (t == 0) {
+        abort_flag = 0;
+        mbar_init(b_a_full, 1);
+        for (int s = 0; s < kGStages; ++s) {
+            mbar_init(b_full0 + 8 * s, 1);   // the producer's expect_tx arrival
+            mbar_init(b_empty0 + 8 * s, 1);  // the second product's commit
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(b_sf0 + 8 * k, 1);           // first product's commit
+            mbar_init(b_se0 + 8 * k, kEvalWarps);  // S read by the evaluation warps
+            mbar_init(b_df0 + 8 * k, 1);           // a group's last second product
+            mbar_init(b_de0 + 8 * k, kEvalWarps);  // D2 read by the evaluation warps
+        }
+        mbar_init(b_pfull, kEvalWarps);            // P tile written
+        mbar_init(b_pempty, 1);                    // P tile read by the second product
+        mbar_init(b_drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const uint32_t tmem = tmem_slot;
+    const int quarter = w & 3, hcol = (w - 2) >> 2, row_l = 32 * quarter + lane;
+    const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
+    const uint32_t t_hi = tmem + lanes + (uint32_t)(kGTmemRun + 32 * hcol);  // this warp's running sums
+    const uint32_t t_lo = t_hi + 64;
+
+    if (w == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0 && T > 0) {
+            mbar_expect_tx(b_a_full, 2 * kATileBytes);
+            tma_2d(s_a_hi, &p.tm_a_hi, 0, (int)row0, b_a_full);
+            tma_2d(s_a_lo, &p.tm_a_lo, 0, (int)row0, b_a_full);
+            int issued = 0;
+            for (int i = 0; i < T; ++i) {
+                const int s = i % kGStages;
+                if (i >= kGStages && !mbar_wait(b_empty0 + 8 * s, ((i / kGStages) - 1) & 1, abort, p.wait_ns)) break;
+                const int j0 = (int)(j_begin + (int64_t)i * kGCols);
+                const uint32_t st = s_stage0 + s * kGStageBytes, full = b_full0 + 8 * s;
+                if (p.starve) continue;  // test hook: no B tile ever arrives, so the MMA issuer's wait runs out
+                mbar_expect_tx(full, kGStageBytes);
+                tma_2d(st, &p.tm_b_hi, 0, j0, full);
+                tma_2d(st + kGBTileBytes, &p.tm_b_lo, 0, j0, full);
+                issued = i + 1;
+            }
+            if (*abort) {  // let the copies in flight land before shared memory is released
+                mbar_drain(b_a_full, 0, p.wait_ns);
+                for (int i = issued > kGStages ? issued - kGStages : 0; i < issued; ++i)
+                    mbar_drain(b_full0 + 8 * (i % kGStages), (i / kGStages) & 1, p.wait_ns);
+            }
+        }
+    } else if (w == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0 && T > 0 && mbar_wait(b_a_full, 0, abort, p.wait_ns)) {
+            bool issued = false;
+            // second product of tile j: D2[group] += P(j) . B(j) (B read MN-major); then the P
+            // tile and B(j)'s stage are free, and after a group's last tile its D2 is complete
+            auto mma2 = [&](int j) -> bool {
+                const int s = j % kGStages, g = j / kGGroup, kk = g & 1;
+                const bool first = j % kGGroup == 0, last = j % kGGroup == kGGroup - 1 || j == T - 1;
+                if (!mbar_wait(b_pfull, j & 1, abort, p.wait_ns)) return false;
+                if (first && g >= 2 && !mbar_wait(b_de0 + 8 * kk, ((g >> 1) - 1) & 1, abort, p.wait_ns)) return false;
+                asm volatile("tcgen05.fence::after_thread_sync;");
+                const uint32_t acc = tmem + (uint32_t)(kGTmemD2 + kk * 64);
+                const uint32_t bh = s_stage0 + s * kGStageBytes, bl = bh + kGBTileBytes;
+                const uint32_t ph = s_p, pl = s_p + 2 * kGPHalfBytes;
+#pragma unroll
+                for (int q = 0; q < kGCols / 16; ++q) {  // K = 16 points per product
+                    const uint32_t pa = (uint32_t)((q >> 2) * kGPHalfBytes + 32 * (q & 3));
+                    const uint32_t bb = (uint32_t)(16 * 128 * q);
+                    mma_f16(acc, desc_sw128(ph + pa), desc_sw128_mn(bh + bb), (first && q == 0) ? 0u : 1u, kIdescG2);
+                    mma_f16(acc, desc_sw128(ph + pa), desc_sw128_mn(bl + bb), 1, kIdescG2);
+                    mma_f16(acc, desc_sw128(pl + pa), desc_sw128_mn(bh + bb), 1, kIdescG2);
+                }
+                commit(b_pempty);
+                commit(b_empty0 + 8 * s);
+                if (last) commit(b_df0 + 8 * kk);
+                return true;
+            };
+            bool ok = true;
+            for (int i = 0; i < T && ok; ++i) {
+                const int s = i % kGStages, k = i & 1;
+                if (!mbar_wait(b_full0 + 8 * s, (i / kGStages) & 1, abort, p.wait_ns)) break;
+                if (i >= 2 && !mbar_wait(b_se0 + 8 * k, ((i >> 1) - 1) & 1, abort, p.wait_ns)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;");
+                const uint32_t acc = tmem + (uint32_t)(kGTmemS + k * kGCols);
+                const uint32_t bh = s_stage0 + s * kGStageBytes, bl = bh + kGBTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(acc, desc_sw128(s_a_hi + 32 * kk), desc_sw128(bh + 32 * kk), kk > 0, kIdescG1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(acc, desc_sw128(s_a_hi + 32 * kk), desc_sw128(bl + 32 * kk), 1, kIdescG1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(acc, desc_sw128(s_a_lo + 32 * kk), desc_sw128(bh + 32 * kk), 1, kIdescG1);
+                commit(b_sf0 + 8 * k);
+                issued = true;
+                if (i >= 2) ok = mma2(i - 2);  // the second products run two tiles behind
+            }
+            for (int j = T >= 2 ? T - 2 : 0; j < T && ok && !*abort; ++j) ok = mma2(j);
+            if (*abort && issued) {  // let the products in flight finish before TMEM is released
+                commit(b_drain);
+                mbar_drain(b_drain, 0, p.wait_ns);
+            }
+        }
+    } else {
+        // ---------------- evaluation warps 2..9 ----------------
+        uint8_t *const hb = pbuf + hcol * kGPHalfBytes + row_l * 128;        // this row's P hi, this K half
+        uint8_t *const lb = pbuf + (2 + hcol) * kGPHalfBytes + row_l * 128;  // and P lo
+        const int sw = row_l & 7;                                            // 128-byte swizzle of the row
+        {  // the running sums start at zero
+            uint32_t z[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) z[c] = 0u;
+            tmem_st32x32b_x32(t_hi, z);
+            tmem_st32x32b_x32(t_lo, z);
+            asm volatile("tcgen05.wait::st.sync.aligned;");
+        }
+        // group g's D2 (complete once its last second product is): fold into the running sums
+        auto fold = [&](int g) -> bool {
+            const int kk = g & 1;
+            if (!mbar_wait(b_df0 + 8 * kk, (g >> 1) & 1, abort, p.wait_ns)) return false;
+            asm volatile("tcgen05.fence::after_thread_sync;");
+            uint32_t d[32], h[32], l[32];
+            tmem_ld32x32b_x32(tmem + lanes + (uint32_t)(kGTmemD2 + kk * 64 + 32 * hcol), d);
+            tmem_ld32x32b_x32(t_hi, h);
+            tmem_ld32x32b_x32(t_lo, l);
+            asm volatile("tcgen05.wait::ld.sync.aligned;");
+            asm volatile("tcgen05.fence::before_thread_sync;");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_de0 + 8 * kk);  // the second products of group g+2 may overwrite it
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                float hv = __uint_as_float(h[c]), lv = __uint_as_float(l[c]);
+                two_sum_add(hv, lv, __uint_as_float(d[c]));
+                h[c] = __float_as_uint(hv);
+                l[c] = __float_as_uint(lv);
+            }
+            tmem_st32x32b_x32(t_hi, h);
+            tmem_st32x32b_x32(t_lo, l);
+            asm volatile("tcgen05.wait::st.sync.aligned;");
+            return true;
+        };
+        bool ok = true;
+        float pm = 0.f;  // largest |P| of this row's columns in this split
+        for (int i = 0; i < T && ok; ++i) {
+            const int k = i & 1;
+            const float4 *bv = reinterpret_cast<const float4 *>(p.bpad + j_begin + (int64_t)i * kGCols + 64 * hcol);
+            if (!mbar_wait(b_sf0 + 8 * k, (i >> 1) & 1, abort, p.wait_ns)) break;
+            asm volatile("tcgen05.fence::after_thread_sync;");
+            // P = 2^S b for this warp's 64 points, split into fp16 hi + lo, packed two points a
+            // register: all of it before waiting for the P tile, which the second product of the
+            // previous tile may still be reading
+            uint32_t ph[32], pl[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[32];
+                tmem_ld32x32b_x32(tmem + lanes + (uint32_t)(kGTmemS + k * kGCols + 64 * hcol + 32 * half), r);
+                asm volatile("tcgen05.wait::ld.sync.aligned;");
+                if (half == 1) {
+                    asm volatile("tcgen05.fence::before_thread_sync;");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_se0 + 8 * k);  // the first product of tile i+2 may overwrite it
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 b4 = __ldg(bv + 8 * half + q);
+                    const float p0 = ex2_approx(__uint_as_float(r[4 * q + 0])) * b4.x;
+                    const float p1 = ex2_approx(__uint_as_float(r[4 * q + 1])) * b4.y;
+                    const float p2 = ex2_approx(__uint_as_float(r[4 * q + 2])) * b4.z;
+                    const float p3 = ex2_approx(__uint_as_float(r[4 * q + 3])) * b4.w;
+                    pm = fmax3(pm, fabsf(p0), fabsf(p1));
+                    pm = fmax3(pm, fabsf(p2), fabsf(p3));
+                    const __half2 h01 = __floats2half2_rn(p0, p1), h23 = __floats2half2_rn(p2, p3);
+                    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                    const __half2 l01 = __floats2half2_rn(p0 - f01.x, p1 - f01.y);
+                    const __half2 l23 = __floats2half2_rn(p2 - f23.x, p3 - f23.y);
+                    ph[16 * half + 2 * q] = *reinterpret_cast<const uint32_t *>(&h01);
+                    ph[16 * half + 2 * q + 1] = *reinterpret_cast<const uint32_t *>(&h23);
+                    pl[16 * half + 2 * q] = *reinterpret_cast<const uint32_t *>(&l01);
+                    pl[16 * half + 2 * q + 1] = *reinterpret_cast<const uint32_t *>(&l23);
+                }
+            }
+            if (i >= 1 && !mbar_wait(b_pempty, (i - 1) & 1, abort, p.wait_ns)) {
+                ok = false;
+                break;
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // 16-byte chunk c = points 8c..8c+7 of this K half, swizzled
+                *reinterpret_cast<uint4 *>(hb + ((c ^ sw) << 4)) = make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
+                *reinterpret_cast<uint4 *>(lb + ((c ^ sw) << 4)) = make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_pfull);
+            if (i >= 1 && (i - 1) % kGGroup == kGGroup - 1) ok = fold((i - 1) / kGGroup);
+        }
+        if (ok && !*abort && T > 0) fold((T - 1) / kGGroup);
+        pmx[hcol][row_l] = pm;
+    }
+
+    __syncthreads();
+    const bool ok = !*abort;
+    if (!ok && t == 0) atomicOr(&g_tc_status, 1u);
+    // every row's 64 running sums (hi, lo) through the idle P tile, so both halves see s0 (column D)
+    float *red = reinterpret_cast<float *>(pbuf);
+    float ah[32], al[32];
+    if (w >= 2) {
+        uint32_t h[32], l[32];
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        tmem_ld32x32b_x32(t_hi, h);
+        tmem_ld32x32b_x32(t_lo, l);
+        asm volatile("tcgen05.wait::ld.sync.aligned;");
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            ah[c] = __uint_as_float(h[c]);
+            al[c] = __uint_as_float(l[c]);
+            red[row_l * 64 + 32 * hcol + c] = ah[c];
+            red[kRows * 64 + row_l * 64 + 32 * hcol + c] = al[c];
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    if (w == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+    if (w >= 2) {
+        const int64_t i = row0 + row_l;
+        // A row whose largest |P| in this split is below 2^-8 (every point far from it, or a small
+        // signal there) keeps too few bits in the fp16 P tile: the CUDA-core kernel launched
+        // after this one redoes this split's part of it (the flag says so), exactly.
+        const bool weak = ok && T > 0 && fmaxf(pmx[0][row_l], pmx[1][row_l]) < 0x1p-8f;
+        if (i < p.M && hcol == 0) p.flags[(int64_t)blockIdx.y * p.M + i] = weak ? 1 : 0;
+        if (i < p.M && !weak) {
+            const double s0 = (double)red[row_l * 64 + p.D] + (double)red[kRows * 64 + row_l * 64 + p.D];
+            // the signal went in as b / 2^e (pow2_above of its largest magnitude): scale back
+            const double sc =
+                (double)p.gscale * (double)__ldg(p.g + i) * (double)pow2_above(__uint_as_float(p.guard[2]));
+            const float nan = __int_as_float(0x7fc00000);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const int d = 32 * hcol + c;
+                if (d >= p.D) continue;
+                const double xd = (double)(p.c * __ldg(p.x + i * p.D + d));
+                const double v = (xd * s0 - ((double)ah[c] + (double)al[c])) * sc;
+                const int64_t o = i * p.D + d;
+                if (p.S == 1) {
+                    p.out[o] = ok ? (float)v : nan;
+                } else {
+                    const int64_t wo = (int64_t)blockIdx.y * p.M * p.D + o;
+                    const float hi = (float)v;
+                    p.ws0[wo] = ok ? hi : nan;
+                    p.ws1[wo] = ok ? (float)(v - (double)hi) : 0.f;
+                }
+            }
+        }
+    }
+}
+
 // Host: cuTensorMapEncodeTiled through the runtime's driver entry point (no link
 // against the driver library).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -592,19 +977,28 @@ cudaError_t tc_set_attributes() {
     e = cudaFuncSetAttribute(tc_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tc_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tc_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemBytes);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return e;
 }
 
+cudaError_t tc_launch_bmax(const float *b, int64_t n, unsigned *guard, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    tc_bmax_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(b, n, guard + 2);
+    return cudaGetLastError();
+}
+
 cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x, bool lse,
                            __half *hi, __half *lo, unsigned *guard, const float *b, float *bpad, float *fpad,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool natural_b) {
     // LSE frames: a prep block of 256 threads is one whole tile of kTcCols = 256 points
     if (fpad && rows_pad % 256) return cudaErrorInvalidValue;
     if (lse && (D + 2 >= 64 || (!is_x && !fpad))) return cudaErrorInvalidValue;
     const unsigned blocks = (unsigned)((rows_pad + 255) / 256);
+    // the y side's guard slot is guard[1] of the call's guard words; the largest |b| is guard[2]
     tc_prep_kernel<<<blocks, 256, 0, s>>>(src, rows, rows_pad, D, c, is_x ? 1 : 0, lse ? 1 : 0, hi, lo, guard, b,
-                                          bpad, fpad);
+                                          bpad, fpad, natural_b ? guard + 1 : nullptr);
     return cudaGetLastError();
 }
 
@@ -633,6 +1027,44 @@ cudaError_t tc_launch_sum(const TcArgs &a, dim3 grid, cudaStream_t s) {
     else
         tc_sum_kernel<<<grid, kThreadsTc, kSmemBytes, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t tc_launch_grad(const TcArgs &a, dim3 grid, cudaStream_t s) {
+    TcParams p;
+    if (a.m_pad % kRows || a.n_pad % kGCols || a.chunk % kGCols || a.D < 32 || a.D > 62) return cudaErrorInvalidValue;
+    if (!make_map(&p.tm_a_hi, a.a_hi, a.m_pad, kRows) || !make_map(&p.tm_a_lo, a.a_lo, a.m_pad, kRows) ||
+        !make_map(&p.tm_b_hi, a.b_hi, a.n_pad, kGCols) || !make_map(&p.tm_b_lo, a.b_lo, a.n_pad, kGCols))
+        return cudaErrorInvalidValue;
+    p.bpad = a.bpad;
+    p.fpad = nullptr;
+    p.out = a.out;
+    p.ws0 = a.ws0;
+    p.ws1 = a.ws1;
+    p.guard = a.guard;
+    p.wait_ns = a.wait_ns;
+    p.starve = a.starve ? 1 : 0;
+    p.M = a.M;
+    p.N = a.N;
+    p.chunk = a.chunk;
+    p.S = a.S;
+    p.x = a.x;
+    p.g = a.g;
+    p.D = a.D;
+    p.c = a.c;
+    p.gscale = a.gscale;
+    p.flags = a.flags;
+    cudaError_t e = tc_set_attributes();
+    if (e != cudaSuccess) return e;
+    tc_grad_kernel<<<grid, kThreadsTc, kGSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+int tc_grad_occupancy() {
+    int n = 0;
+    if (tc_set_attributes() != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_grad_kernel, kThreadsTc, kGSmemBytes) != cudaSuccess)
+        return 0;
+    return n;
 }
 
 int tc_occupancy() {

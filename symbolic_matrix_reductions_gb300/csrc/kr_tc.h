@@ -23,9 +23,15 @@ struct TcArgs {
     uint64_t wait_ns;           // bound of every mbarrier wait (global time)
     bool starve;                // test hook: issue no B tile, so the waits run out
     int64_t M, N, m_pad, n_pad;
-    int64_t chunk;              // points per split, a multiple of kTcCols
+    int64_t chunk;              // points per split, a multiple of kTcCols (gradient: kTcGradCols)
     int S;
     bool lse;                   // LogSumExp (CUDA-core LSE partials) instead of the Sum
+    // x-gradient (tc_launch_grad): x (M x D fp32), upstream g (M), prescale c, the factor
+    // -2 / (sigma^2 c); out / ws0 / ws1 are then M x D (S x M x D partials).
+    const float *x, *g;
+    int D;
+    float c, gscale;
+    uint8_t *flags;  // x-gradient: S x M, 1 where the CUDA-core kernel must redo (split, row)
 };
 
 // Kernel parameters: TMA descriptors of the four operand arrays plus the rest.
@@ -38,6 +44,10 @@ struct TcParams {
     int starve;
     int64_t M, N, chunk;
     int S;
+    const float *x, *g;  // x-gradient only
+    int D;
+    float c, gscale;
+    uint8_t *flags;
 };
 
 int tc_smem_bytes();
@@ -46,12 +56,19 @@ bool tc_available();  // the driver offers cuTensorMapEncodeTiled
 // Operand prepass.  lse: the operands carry the weight slot of the LogSumExp (A: 1; B: the
 // log-weight relative to its tile's frame, which fpad receives; b holds the log-weights).
 // Otherwise bpad receives b padded with zeros.
+// natural_b: bpad in point order (the x-gradient) rather than the Sum's evaluation order.
 cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x, bool lse,
                            __half *hi, __half *lo, unsigned *guard, const float *b, float *bpad, float *fpad,
-                           cudaStream_t s);
+                           cudaStream_t s, bool natural_b = false);
+// x-gradient: guard[2] receives the largest |b| (float bits), from which the prepass of the
+// y side scales bpad by a power of two into [-1, 1] (run before that prepass).
+cudaError_t tc_launch_bmax(const float *b, int64_t n, unsigned *guard, cudaStream_t s);
 // Opts the tensor-core kernels in to their dynamic shared memory on the current device.
 cudaError_t tc_set_attributes();
 cudaError_t tc_launch_sum(const TcArgs &a, dim3 grid, cudaStream_t s);
+// The x-gradient on the tensor cores (32 <= D <= 62, E = 1): grid (ceil(M / 128), S).
+cudaError_t tc_launch_grad(const TcArgs &a, dim3 grid, cudaStream_t s);
+int tc_grad_occupancy();
 // Reads (and optionally clears) the sticky device status of the tensor-core kernels on the
 // current device: bit 0 = a bounded wait gave up.  Synchronous.
 cudaError_t tc_read_status(bool clear, unsigned *status);

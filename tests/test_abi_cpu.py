@@ -358,11 +358,22 @@ def test_tensor_core_plan(lib):
     assert q.path == kr.KR_PATH_TENSOR_CORES and (q.split, q.chunk, q.workspace_bytes) == (p.split, p.chunk,
                                                                                             p.workspace_bytes)
     for shape in [(kr.OP_SUM, 10, 10, 31, 1), (kr.OP_SUM, 10, 10, 63, 1), (kr.OP_SUM, 10, 10, 50, 2),
-                  (kr.OP_LSE, 10, 10, 50, 2), (kr.OP_GRAD, 10, 10, 50, 1), (kr.OP_MAX, 10, 10, 50, 1),
+                  (kr.OP_LSE, 10, 10, 50, 2), (kr.OP_GRAD, 10, 10, 50, 2), (kr.OP_GRAD, 10, 10, 63, 1),
+                  (kr.OP_MAX, 10, 10, 50, 1),
                   (kr.OP_LSE, 10, 10, 62, 1)]:     # the LogSumExp's weight slot leaves D <= 61
         assert kr.plan(*shape).path == kr.KR_PATH_CUDA_CORES, shape
     assert kr.plan(kr.OP_SUM, 10, 10, 62, 1).path == kr.KR_PATH_TENSOR_CORES
     assert kr.plan(kr.OP_LSE, 10, 10, 61, 1).path == kr.KR_PATH_TENSOR_CORES
+    # the x-gradient: 128-point tiles, D x M partials per split
+    g = kr.plan(kr.OP_GRAD, 100_000, 1_000_000, 50, 1, num_sms=152, blocks_per_sm=1)
+    assert g.path == kr.KR_PATH_TENSOR_CORES and g.tile_points == 128 and g.chunk % 128 == 0
+    assert g.split * g.chunk >= 1_000_000 and (g.split - 1) * g.chunk < 1_000_000
+    n_pad = (1_000_000 + 255) // 256 * 256
+    ops_g = ((100_000 + 127) // 128 * 128 + n_pad) * 256 + n_pad * 4 + (n_pad // 256 * 4 + 255) // 256 * 256
+    flags = (g.split * 100_000 + 255) // 256 * 256
+    assert g.workspace_bytes == 256 + ops_g + (2 * g.split * 100_000 * 50 * 4 if g.split > 1 else 0) + flags
+    assert kr.plan(kr.OP_GRAD, 10, 10, 32, 1).path == kr.KR_PATH_TENSOR_CORES
+    assert kr.plan(kr.OP_GRAD, 10, 10, 50, 1, path=kr.KR_PATH_CUDA_CORES).path == kr.KR_PATH_CUDA_CORES
     assert kr.plan(kr.OP_SUM, 10, 10, 50, 1, path=kr.KR_PATH_CUDA_CORES).path == kr.KR_PATH_CUDA_CORES
     assert kr.plan(kr.OP_SUM, 10, 2560, 50, 1, split=5).split == 5
     assert kr.plan(kr.OP_SUM, 10, 2000, 50, 1, split=5).split == 4   # 512-point chunks

@@ -283,6 +283,14 @@ def test_workload_falkon_d50(orc):
     L = _np(kr.kernel_reduce(xt, yt, bt, s, "lse"))
     rows = W.row_subset(inp["x"].shape[0], 256, 10)
     check_lse(L[rows], orc.gauss_lse(inp["x"][rows], inp["y"], inp["b"], s), "falkon_d50 lse")
+    # the x-gradient of the same product (g ~ N(0,1)) on the tensor cores
+    assert kr.plan_device(kr.OP_GRAD, inp["x"].shape[0], inp["y"].shape[0], 50, 1).path == kr.KR_PATH_TENSOR_CORES
+    gt = _dev(inp["g"])[0]
+    gx = _np(kr.kernel_reduce_grad_x(xt, yt, bt, gt, s))
+    rows = W.row_subset(inp["x"].shape[0], 256, 12)
+    gx_ref, G_ref = orc.gauss_grad_x(inp["x"][rows], inp["y"], inp["b"], inp["g"][rows], s)
+    worst = check_grad(gx[rows], gx_ref, G_ref, "falkon_d50 grad")
+    print(f"falkon_d50 grad, {rows.size} rows: err/G {worst:.2e}")
 
 
 def test_workload_knn_d16(orc):
@@ -351,7 +359,7 @@ def test_tensor_core_lse_empty_weights_and_guard(orc):
     check_lse(_np(L), orc.gauss_lse(x, y, w, 2.0), "lse norm guard")
 
 
-@pytest.mark.parametrize("op,split", [("sum", 0), ("sum", 2), ("lse", 0), ("lse", 3)])
+@pytest.mark.parametrize("op,split", [("sum", 0), ("sum", 2), ("lse", 0), ("lse", 3), ("grad", 0), ("grad", 2)])
 def test_tensor_core_wait_bound_reports_status(orc, op, split):
     """Failure detection without a fault: with the B tiles withheld (a test hook that only
     the debug build honours) every bounded mbarrier wait of the tensor kernel runs out
@@ -361,7 +369,14 @@ def test_tensor_core_wait_bound_reports_status(orc, op, split):
     x = (r.standard_normal((300, 50)) / np.sqrt(50)).astype(np.float32)
     y = (r.standard_normal((1000, 50)) / np.sqrt(50)).astype(np.float32)
     b = r.standard_normal((1000, 1)).astype(np.float32)
-    xt, yt, bt = _dev(x, y, b)
+    g = r.standard_normal((300, 1)).astype(np.float32)
+    xt, yt, bt, gt = _dev(x, y, b, g)
+
+    def call():
+        if op == "grad":
+            return kr.kernel_reduce_grad_x(xt, yt, bt, gt, 1.0, split=split)
+        return kr.kernel_reduce(xt, yt, bt, 1.0, op, split=split, path=kr.KR_PATH_TENSOR_CORES)
+
     release = kr.load_library()
     assert release.kr_set_tc_test_hooks(50, 1) == kr.KR_ERR_UNSUPPORTED
     debug = kr.load_debug_library()
@@ -371,21 +386,90 @@ def test_tensor_core_wait_bound_reports_status(orc, op, split):
         kr.device_status(clear=True)
         assert debug.kr_set_tc_test_hooks(50, 1) == kr.KR_OK
         try:
-            a = _np(kr.kernel_reduce(xt, yt, bt, 1.0, op, split=split, path=kr.KR_PATH_TENSOR_CORES))
+            a = _np(call())
         finally:
             assert debug.kr_set_tc_test_hooks(0, 0) == kr.KR_OK
         assert np.isnan(a).all()
         assert kr.device_status(clear=True) & 1
         assert kr.device_status() == 0
-        a = _np(kr.kernel_reduce(xt, yt, bt, 1.0, op, split=split, path=kr.KR_PATH_TENSOR_CORES))
+        a = _np(call())
         assert kr.device_status() == 0
     finally:
         kr._lib = saved
     if op == "sum":
         a_ref, S_ref = orc.gauss_sum(x, y, b, 1.0)
         check_sum(a, a_ref, S_ref, "after a run-out wait")
-    else:
+    elif op == "lse":
         check_lse(a, orc.gauss_lse(x, y, b, 1.0), "after a run-out wait")
+    else:
+        gx_ref, G_ref = orc.gauss_grad_x(x, y, b, g, 1.0)
+        check_grad(a, gx_ref, G_ref, "after a run-out wait")
+
+
+@pytest.mark.parametrize("M,N,D,sigma,split", TC_CASES + [(200, 3000, 61, 1.2, 2), (129, 257, 33, 0.7, 0)])
+def test_tensor_core_grad(orc, M, N, D, sigma, split):
+    """The x-gradient with both contractions on the tensor cores (S = A.B^T, then
+    P.[y' | 1] with P = 2^S b split into fp16 hi + lo), against the oracle's gradient and
+    its scale G; ragged row blocks and tiles, forced splits, D from 32 to 62."""
+    r = _rng(M + 5 * N + D)
+    x = (r.standard_normal((M, D)) / np.sqrt(D)).astype(np.float32)
+    y = (r.standard_normal((N, D)) / np.sqrt(D)).astype(np.float32)
+    b = r.standard_normal((N, 1)).astype(np.float32)
+    g = r.standard_normal((M, 1)).astype(np.float32)
+    assert kr.plan_device(kr.OP_GRAD, M, N, D, 1).path == kr.KR_PATH_TENSOR_CORES
+    gx = kr.kernel_reduce_grad_x(*_dev(x, y, b, g), sigma, split=split)
+    gx_ref, G_ref = orc.gauss_grad_x(x, y, b, g, sigma)
+    check_grad(_np(gx), gx_ref, G_ref, f"tc grad {M}x{N} D{D} S{split}")
+
+
+def test_tensor_core_grad_guard_and_agreement(orc):
+    """Large norms (|x'|^2 + |y'|^2 > 16) stand the tensor kernel down and the CUDA-core
+    gradient answers; on normal clouds the two paths agree within the tolerance and reruns
+    give the same bits.  (The clouds here are independent, so no coordinate of x_i nearly
+    equals that of all its neighbours: there fp32 coordinates, prescaled or expanded, lose
+    the relative precision of the difference; that limit is described with the
+    gradient's tolerance.)"""
+    r = _rng(83)
+    x = (3.0 * r.standard_normal((200, 50))).astype(np.float32)
+    y = (3.0 * r.standard_normal((700, 50))).astype(np.float32)
+    b = r.standard_normal((700, 1)).astype(np.float32)
+    g = r.standard_normal((200, 1)).astype(np.float32)
+    gx = kr.kernel_reduce_grad_x(*_dev(x, y, b, g), 8.0)
+    gx_ref, G_ref = orc.gauss_grad_x(x, y, b, g, 8.0)
+    check_grad(_np(gx), gx_ref, G_ref, "tc grad norm guard")
+    inp = W.generate("falkon_d50", M=2000, N=50_000)
+    gg = _rng(84).standard_normal((2000, 1)).astype(np.float32)
+    xt, yt, bt, gt = _dev(inp["x"], inp["y"], inp["b"], gg)
+    g_tc = _np(kr.kernel_reduce_grad_x(xt, yt, bt, gt, 1.0))
+    g_cc = _np(kr.kernel_reduce_grad_x(xt, yt, bt, gt, 1.0, path=kr.KR_PATH_CUDA_CORES))
+    rows = W.row_subset(2000, 200, 85)
+    gx_ref, G_ref = orc.gauss_grad_x(inp["x"][rows], inp["y"], inp["b"], gg[rows], 1.0)
+    check_grad(g_tc[rows], gx_ref, G_ref, "falkon-shaped tc grad")
+    check_grad(g_cc[rows], gx_ref, G_ref, "falkon-shaped cuda-core grad")
+    assert np.array_equal(g_tc, _np(kr.kernel_reduce_grad_x(xt, yt, bt, gt, 1.0)))
+
+
+@pytest.mark.parametrize("bscale,split", [(1.0, 0), (1e6, 3), (1e-8, 0), (3e4, 5)])
+def test_tensor_core_grad_far_rows_and_signal_scale(orc, bscale, split):
+    """The tensor-core gradient's P tile is fp16: the signal is scaled by a power of two into
+    [-1, 1] (signals of 1e6 would overflow it, 1e-8 would vanish), and rows whose largest |P|
+    in a split is below 2^-8 (here rows 2.2-3.0 units from a tight cloud, within the norm
+    guard) are redone for that split by the CUDA-core kernel.  Every row must meet the
+    oracle's tolerance."""
+    r = _rng(91 + split)
+    M, N, D = 300, 3000, 40
+    y = (0.5 * r.standard_normal((N, D)) / np.sqrt(D)).astype(np.float32)
+    x = (0.5 * r.standard_normal((M, D)) / np.sqrt(D)).astype(np.float32)
+    u = r.standard_normal((M, D))
+    u /= np.linalg.norm(u, axis=1, keepdims=True)
+    far = np.arange(M) % 3 == 0
+    x[far] = (u[far] * np.linspace(2.2, 3.0, far.sum())[:, None]).astype(np.float32)
+    b = (bscale * r.standard_normal((N, 1))).astype(np.float32)
+    g = r.standard_normal((M, 1)).astype(np.float32)
+    assert kr.plan_device(kr.OP_GRAD, M, N, D, 1).path == kr.KR_PATH_TENSOR_CORES
+    gx = kr.kernel_reduce_grad_x(*_dev(x, y, b, g), 1.0, split=split)
+    gx_ref, G_ref = orc.gauss_grad_x(x, y, b, g, 1.0)
+    check_grad(_np(gx), gx_ref, G_ref, f"tc grad far rows, b x {bscale}, S{split}")
 
 
 def test_tensor_core_norm_guard_falls_back(orc):
