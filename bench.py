@@ -195,8 +195,10 @@ def probe_pipes(torch, nsm):
 
 
 # Tensor-core Sum and LSE (E = 1, 32 <= D <= 62): per pair, three fp16 products (hi.hi, hi.lo,
-# lo.hi) of the K = 64 augmented vectors, 2 FLOP per multiply-add.
+# lo.hi) of the K = 64 augmented vectors, 2 FLOP per multiply-add.  The x-gradient adds a second
+# product P.[y' | 1] of the same width (three split products, N = 64): twice the FLOP.
 TC_FLOP_PER_PAIR = 3 * 2 * 64
+TC_GRAD_FLOP_PER_PAIR = 2 * TC_FLOP_PER_PAIR
 
 
 def tensor_peak_tflops():
@@ -210,11 +212,11 @@ def tensor_peak_tflops():
     return 1900.0, "fallback 1.9 PFLOP/s bf16 (fp16 nominal ratio 1)"
 
 
-def roofline_tensor(seconds_per_launch, pairs, kernel, fp32_line):
+def roofline_tensor(seconds_per_launch, pairs, kernel, fp32_line, flop_per_pair=TC_FLOP_PER_PAIR):
     peak, basis = tensor_peak_tflops()
-    achieved = pairs * TC_FLOP_PER_PAIR / seconds_per_launch / 1e12
+    achieved = pairs * flop_per_pair / seconds_per_launch / 1e12
     return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": None, "kernel": kernel, "flop_per_pair": TC_FLOP_PER_PAIR, "peak_basis": basis,
+            "traffic": None, "kernel": kernel, "flop_per_pair": flop_per_pair, "peak_basis": basis,
             "pairs_per_s": pairs / seconds_per_launch,
             "vs_fp32_direct_roofline": {"peak_pairs_per_s": fp32_line["peak"], "frac": fp32_line["frac"]}}
 
@@ -305,11 +307,14 @@ def _median_ms(torch, fn, warm=WARM_SECONDARY, runs=RUNS_SECONDARY):
                                   "min_ms": float(np.min(ts)), "max_ms": float(np.max(ts))}
 
 
-def launches_of(kr, p) -> int:
+def launches_of(kr, p, op="sum", batch=1) -> int:
     """Kernels of this library one call with plan p launches."""
     if p.path == kr.KR_PATH_TENSOR_CORES:
-        return 4 + (p.split > 1)   # two operand prepasses, the tensor kernel, its stand-in [, combine]
-    return 1 + (p.split > 1)
+        # two operand prepasses (and for the gradient the signal bound), the tensor kernel, its
+        # CUDA-core stand-in [, combine]
+        return 4 + (op == "grad") + (p.split > 1)
+    streamed = op in ("sum", "lse", "grad") and p.d_pad <= 16 and batch <= 1
+    return 1 + streamed + (p.split > 1)   # [record prepass,] the kernel [, combine]
 
 
 # ---------------------------------------------------------------------------
@@ -359,7 +364,7 @@ def run_ours(args, rank, world, local_rank):
            ("knn", lambda: kr.kernel_knn(x, y, K_NN, idx=idx, dist=dist_))]
     op_code = {"sum": kr.OP_SUM, "lse": kr.OP_LSE, "grad": kr.OP_GRAD, "knn": kr.OP_KNN}
     plans = {name: kr.plan_device(op_code[name], max(m, 1), N, D, K_NN if name == "knn" else E) for name, _ in ops}
-    launches_per_step = sum(launches_of(kr, plans[n]) for n, _ in ops) if m > 0 else 0
+    launches_per_step = sum(launches_of(kr, plans[n], n) for n, _ in ops) if m > 0 else 0
     pairs_per_step = 4 * M * N   # the whole problem (every rank's slice)
 
     # The four reductions are independent calls on the same inputs: a step issues each on its
@@ -526,24 +531,31 @@ def measure_d50(torch, kr, W, nsm, max_mhz, xu_lanes, dev, args):
     M, D = inp["x"].shape
     N = inp["y"].shape[0]
     s = inp["sigma"]
-    x, y, b = (torch.from_numpy(inp[k]).to(dev) for k in ("x", "y", "b"))
+    x, y, b, g = (torch.from_numpy(inp[k]).to(dev) for k in ("x", "y", "b", "g"))
     a = torch.empty((M, 1), device=dev)
     L = torch.empty((M, 1), device=dev)
+    gx = torch.empty((M, D), device=dev)
     out = {"workload": f"{D50}: {W.WORKLOADS[D50].note}", "M": M, "N": N, "D": D, "E": 1, "sigma": s,
-           "metric": METRIC, "unit": UNIT}
-    for op, o in (("sum", a), ("lse", L)):
-        p = kr.plan_device(kr.OP_SUM if op == "sum" else kr.OP_LSE, M, N, D, 1)
-        ms, how = _median_ms(torch, lambda op=op, o=o: kr.kernel_reduce(x, y, b, s, op, out=o))
-        rl = roofline(op, D, 1, ms / 1e3, M * N, nsm, max_mhz, xu_lanes, f"fwd_kernel<{op}>[D={D},E=1]")
+           "metric": METRIC, "unit": UNIT,
+           "note": "value = the tall kernel-vector product (the Sum); the LogSumExp (b as log-weights) and the "
+                   "x-gradient (g ~ N(0,1)) of the same clouds beside it"}
+    calls = {"sum": (kr.OP_SUM, lambda: kr.kernel_reduce(x, y, b, s, "sum", out=a)),
+             "lse": (kr.OP_LSE, lambda: kr.kernel_reduce(x, y, b, s, "lse", out=L)),
+             "grad": (kr.OP_GRAD, lambda: kr.kernel_reduce_grad_x(x, y, b, g, s, out=gx))}
+    for op, (code, fn) in calls.items():
+        p = kr.plan_device(code, M, N, D, 1)
+        ms, how = _median_ms(torch, fn, warm=3, runs=10 if op != "grad" else 5)
+        rl = roofline(op, D, 1, ms / 1e3, M * N, nsm, max_mhz, xu_lanes, f"{op}[D={D},E=1] (CUDA-core count)")
         if p.path == kr.KR_PATH_TENSOR_CORES:
-            rl = roofline_tensor(ms / 1e3, M * N, f"tc_{op}_kernel (tcgen05)", rl)
+            rl = roofline_tensor(ms / 1e3, M * N, f"tc_{op}_kernel (tcgen05)", rl,
+                                 TC_GRAD_FLOP_PER_PAIR if op == "grad" else TC_FLOP_PER_PAIR)
         out[op] = {"value": M * N / (ms / 1e3), "ms": ms, "timing": how, "split": p.split,
                    "path": "tensor cores" if p.path == kr.KR_PATH_TENSOR_CORES else "cuda cores",
-                   "gpu_launches_per_call": launches_of(kr, p), "roofline": rl}
+                   "gpu_launches_per_call": launches_of(kr, p, op), "roofline": rl}
     out["value"] = out["sum"]["value"]
     out["roofline"] = out["sum"]["roofline"]
-    a_dev, L_dev = a.cpu().numpy(), L.cpu().numpy()
-    del x, y
+    a_dev, L_dev, gx_dev = a.cpu().numpy(), L.cpu().numpy(), gx.cpu().numpy()
+    del x, y, g, gx
     torch.cuda.empty_cache()
     # e2e: the product through the C ABI with pinned host buffers (inputs up, result down)
     xc, yc, bc = (torch.from_numpy(inp[k]).pin_memory() for k in ("x", "y", "b"))
@@ -575,11 +587,15 @@ def measure_d50(torch, kr, W, nsm, max_mhz, xu_lanes, dev, args):
     out["cpu_baseline"] = {"value": r * N / t, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
                            "sample": f"seeded subset of {r} rows of {D50}, full N={N}: the Sum in fp64, {t:.1f} s"}
     L_ref = orc.gauss_lse(inp["x"][rows[:64]], inp["y"], inp["b"], s)
+    g_ref, G_ref = orc.gauss_grad_x(inp["x"][rows[:32]], inp["y"], inp["b"], inp["g"][rows[:32]], s)
     sum_err = float(np.max(np.abs(a_dev[rows] - a_ref) / np.maximum(S_ref, 1e-300)))
     lse_err = np.abs(L_dev[rows[:64]] - L_ref)
+    grad_err = float(np.max(np.abs(gx_dev[rows[:32]] - g_ref) / np.maximum(G_ref, 1e-300)))
     out["parity"] = {"rows": r, "sum_err_over_S": sum_err, "lse_rows": 64, "lse_abs_err": float(np.max(lse_err)),
-                     "ok": bool(sum_err <= 1e-4 and np.all(lse_err <= 1e-4 + 2.0 ** -20 * np.abs(L_ref))),
-                     "tolerances": "Sum 1e-4 S; LSE 1e-4 + 2^-20 |L|"}
+                     "grad_rows": 32, "grad_err_over_G": grad_err,
+                     "ok": bool(sum_err <= 1e-4 and np.all(lse_err <= 1e-4 + 2.0 ** -20 * np.abs(L_ref))
+                                and grad_err <= 1e-4),
+                     "tolerances": "Sum 1e-4 S; LSE 1e-4 + 2^-20 |L|; grad 1e-4 G"}
     return out
 
 

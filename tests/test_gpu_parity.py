@@ -287,7 +287,7 @@ def test_workload_falkon_d50(orc):
     assert kr.plan_device(kr.OP_GRAD, inp["x"].shape[0], inp["y"].shape[0], 50, 1).path == kr.KR_PATH_TENSOR_CORES
     gt = _dev(inp["g"])[0]
     gx = _np(kr.kernel_reduce_grad_x(xt, yt, bt, gt, s))
-    rows = W.row_subset(inp["x"].shape[0], 256, 12)
+    rows = W.row_subset(inp["x"].shape[0], 32, 12)   # the fp64 gradient costs ~1 s a row at N = 1e7
     gx_ref, G_ref = orc.gauss_grad_x(inp["x"][rows], inp["y"], inp["b"], inp["g"][rows], s)
     worst = check_grad(gx[rows], gx_ref, G_ref, "falkon_d50 grad")
     print(f"falkon_d50 grad, {rows.size} rows: err/G {worst:.2e}")
