@@ -89,9 +89,10 @@ ALU_LANES_PER_SM = 64     # integer/compare pipe: 4 partitions x 16 lanes
 # DRAM traffic per launch from ncu captures (profiles/), keyed by kernel and the
 # hash of the kernel sources it was taken on; stale entries report null.
 TRAFFIC = {
-    # profiles/grad2_kernel_d3_gauss_d3.md: dram__bytes_read.sum + dram__bytes_write.sum (the hash is of
-    # the kernel sources at a commit where grad2_kernel's code is the captured one)
-    "grad_kernel[D=3,E=1]": {"bytes_per_launch": 3221504, "source_hash": "24ce0b589a53db11"},
+    # profiles/grad2_kernel_d3_gauss_d3_unit.md: dram__bytes_read.sum + dram__bytes_write.sum of one
+    # full-size launch of the step's x-gradient (1e6 x 1e6, 7 splits; a one-pass capture), with the hash
+    # of the kernel sources it ran
+    "grad_kernel[D=3,E=1]": {"bytes_per_launch": 42504960 + 117179648, "source_hash": "832c7144ec0e4b2b"},
 }
 
 
