@@ -95,7 +95,7 @@ static void plan_tc(int op, int64_t M, int64_t N, int D, int num_sms, int blocks
     p->d_pad = 64;
     p->ek_pad = 1;
     p->rows_per_thread = 1;
-    p->threads = kTcThreads;
+    p->threads = op == OP_GRAD ? kTcGradThreads : kTcThreads;
     p->tile_points = tile;
     p->row_blocks = (M + kTcRows - 1) / kTcRows;
     p->path = KR_PATH_TENSOR_CORES;

@@ -104,6 +104,14 @@ __device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// The descriptor of base + off from the base's: the start address (16-byte units, bits
+// 0-13) is the low field of the low word, and a block's shared memory stays below 256 KB,
+// so off / 16 adds to the low word without carrying out of the field.  One integer add an
+// operand, for issue loops that place many products in the same tiles.
+__device__ __forceinline__ uint64_t desc_add(uint64_t base, uint32_t off) {
+    return (base & 0xFFFFFFFF00000000ull) | (uint64_t)((uint32_t)base + (off >> 4));
+}
+
 // D[tmem] (+)= A[smem] . B[smem]^T, fp16 operands, fp32 accumulation (instruction
 // descriptor idesc: shapes and operand majors).
 __device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t accumulate,
@@ -598,6 +606,27 @@ __device__ __forceinline__ void tmem_st32x32b_x32(uint32_t taddr, const uint32_t
                  : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr), "r"(r[0]),"r"(r[1]),"r"(r[2]),"r"(r[3]),"r"(r[4]),"r"(r[5]),"r"(r[6]),"r"(r[7]),"r"(r[8]),"r"(r[9]),"r"(r[10]),"r"(r[11]),"r"(r[12]),"r"(r[13]),"r"(r[14]),"r"(r[15])
+                 : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // x-gradient (tc_grad_kernel), 32 <= D <= 62, E = 1:
 //   gx_id = gscale g_i sum_j k_ij b_j (x'_id - y'_jd) = gscale g_i (x'_id s0_i - s_id),
@@ -615,35 +644,41 @@ __device__ __forceinline__ void tmem_st32x32b_x32(uint32_t taddr, const uint32_t
 // s0 and s come from the same rounded P, so the cancellation in x' s0 - s leaves only the
 // operands' own rounding (about 2^-22 of them) against sum_j |P_ij| |x'_id - y'_jd|, the
 // tolerance's scale.  The MMA issuer runs the first products two tiles ahead of the
-// second, so the next S is computed while the warps turn the last one into P.
-// Block = 10 warps (TMA producer, MMA issuer, 8 evaluation warps); TMEM columns [0, 256):
+// second, so the next S is computed while the warps turn the last one into P.  A tile's B
+// stage is released only by its second product, two tiles after its first: of the four
+// stages, the one beyond those three is the TMA's lookahead.
+// Block = 18 warps (TMA producer, MMA issuer, 16 evaluation warps: the evaluation is
+// latency-bound, so four warps a scheduler, at 96 registers each); TMEM columns [0, 256):
 // two S accumulators of 128; [256, 384): two D2 accumulators of 64; [384, 512): the
 // running sums (hi at 384 + c, lo at 448 + c for D2 column c).  Evaluation warp w reads
-// TMEM lanes 32 (w mod 4).. (its rows) and takes S columns 64 h.. and D2 columns 32 h..
-// (h = (w - 2) / 4).
+// TMEM lanes 32 (w mod 4).. (its rows) and takes S columns 32 q.. and D2 columns 16 q..
+// (q = (w - 2) / 4).
 // ---------------------------------------------------------------------------
 constexpr int kGCols = kTcGradCols;
-constexpr int kGStages = 3;
+constexpr int kGStages = 4;  // the second product holds a tile's B stage two tiles longer
+constexpr int kGEvalWarps = 16;                 // four per TMEM lane quarter: 32 S columns each
+constexpr int kGThreads = kTcGradThreads;
+static_assert(kGThreads == 64 + 32 * kGEvalWarps, "warp roles");
 constexpr int kGGroup = 4;                      // tiles summed in one D2 accumulator
 constexpr int kGBTileBytes = kGCols * 128;      // 128 points x 64 fp16
 constexpr int kGStageBytes = 2 * kGBTileBytes;  // hi, lo
 constexpr int kGPHalfBytes = kRows * 128;       // 128 rows x 64 points fp16: one K half of P
 constexpr int kGPBytes = 4 * kGPHalfBytes;      // hi (two K halves), lo (two K halves)
 constexpr int kGSmemBytes = 2 * kATileBytes + kGStages * kGStageBytes + kGPBytes + 1024;
-static_assert(kGSmemBytes + 512 <= 227 * 1024, "shared memory per block");
+static_assert(kGSmemBytes + 1024 <= 227 * 1024, "shared memory per block (the static part is under 1 KB)");
 static_assert(kGPBytes >= kRows * 64 * 2 * 4, "the P tile holds the final (hi, lo) sums");
 // MMA 1: M = 128, N = 128, both K-major.  MMA 2: M = 128, N = 64, A K-major, B MN-major.
 constexpr uint32_t kIdescG1 = (1u << 4) | ((uint32_t)(kGCols >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 constexpr uint32_t kIdescG2 = (1u << 4) | (1u << 16) | ((uint32_t)(64 >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 constexpr int kGTmemS = 0, kGTmemD2 = 2 * kGCols, kGTmemRun = kGTmemD2 + 128;
 
-__global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kGThreads, 1) tc_grad_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
-    // a_full, full[3], empty[3], s_full[2], s_empty[2], d2_full[2], d2_empty[2], p_full, p_empty, drain
+    // a_full, full[4], empty[4], s_full[2], s_empty[2], d2_full[2], d2_empty[2], p_full, p_empty, drain
     __shared__ __align__(8) uint64_t bars[1 + 2 * kGStages + 8 + 3];
-    __shared__ float pmx[2][kRows];  // largest |P| of each row's two column halves
+    __shared__ unsigned pmx[kRows];  // largest |P| of each row (float bits: non-negative, so ordered as integers)
     if (!norms_ok(p.guard) || !(__uint_as_float(p.guard[2]) <= 3.0e38f))
         return;  // the CUDA-core kernel does this call's work
 
@@ -670,6 +705,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
                      "r"(512));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    if (t < kRows) pmx[t] = 0u;
     if (t == 0) {
         abort_flag = 0;
         mbar_init(b_a_full, 1);
@@ -679,11 +715,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(b_sf0 + 8 * k, 1);           // first product's commit
-            mbar_init(b_se0 + 8 * k, kEvalWarps);  // S read by the evaluation warps
+            mbar_init(b_se0 + 8 * k, kGEvalWarps);  // S read by the evaluation warps
             mbar_init(b_df0 + 8 * k, 1);           // a group's last second product
-            mbar_init(b_de0 + 8 * k, kEvalWarps);  // D2 read by the evaluation warps
+            mbar_init(b_de0 + 8 * k, kGEvalWarps);  // D2 read by the evaluation warps
         }
-        mbar_init(b_pfull, kEvalWarps);            // P tile written
+        mbar_init(b_pfull, kGEvalWarps);           // P tile written
         mbar_init(b_pempty, 1);                    // P tile read by the second product
         mbar_init(b_drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;");
@@ -692,9 +728,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;");
     const uint32_t tmem = tmem_slot;
-    const int quarter = w & 3, hcol = (w - 2) >> 2, row_l = 32 * quarter + lane;
+    // evaluation warp w: TMEM lanes 32 (w mod 4).. (its rows), column part (w - 2) / 4: S columns
+    // 32 part.., D2 columns 16 part..
+    const int quarter = w & 3, part = (w - 2) >> 2, row_l = 32 * quarter + lane;
     const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
-    const uint32_t t_hi = tmem + lanes + (uint32_t)(kGTmemRun + 32 * hcol);  // this warp's running sums
+    const uint32_t t_hi = tmem + lanes + (uint32_t)(kGTmemRun + 16 * part);  // this warp's running sums
     const uint32_t t_lo = t_hi + 64;
 
     if (w == 0) {
@@ -725,6 +763,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
         // ---------------- MMA issuer ----------------
         if (lane == 0 && T > 0 && mbar_wait(b_a_full, 0, abort, p.wait_ns)) {
             bool issued = false;
+            // base descriptors: A (hi, lo after it), the B stages K-major and MN-major, P
+            const uint64_t d_a = desc_sw128(s_a_hi), d_b = desc_sw128(s_stage0), d_bmn = desc_sw128_mn(s_stage0);
+            const uint64_t d_p = desc_sw128(s_p);
             // second product of tile j: D2[group] += P(j) . B(j) (B read MN-major); then the P
             // tile and B(j)'s stage are free, and after a group's last tile its D2 is complete
             auto mma2 = [&](int j) -> bool {
@@ -734,15 +775,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
                 if (first && g >= 2 && !mbar_wait(b_de0 + 8 * kk, ((g >> 1) - 1) & 1, abort, p.wait_ns)) return false;
                 asm volatile("tcgen05.fence::after_thread_sync;");
                 const uint32_t acc = tmem + (uint32_t)(kGTmemD2 + kk * 64);
-                const uint32_t bh = s_stage0 + s * kGStageBytes, bl = bh + kGBTileBytes;
-                const uint32_t ph = s_p, pl = s_p + 2 * kGPHalfBytes;
+                const uint32_t so = (uint32_t)(s * kGStageBytes);
 #pragma unroll
                 for (int q = 0; q < kGCols / 16; ++q) {  // K = 16 points per product
                     const uint32_t pa = (uint32_t)((q >> 2) * kGPHalfBytes + 32 * (q & 3));
-                    const uint32_t bb = (uint32_t)(16 * 128 * q);
-                    mma_f16(acc, desc_sw128(ph + pa), desc_sw128_mn(bh + bb), (first && q == 0) ? 0u : 1u, kIdescG2);
-                    mma_f16(acc, desc_sw128(ph + pa), desc_sw128_mn(bl + bb), 1, kIdescG2);
-                    mma_f16(acc, desc_sw128(pl + pa), desc_sw128_mn(bh + bb), 1, kIdescG2);
+                    const uint32_t bb = so + (uint32_t)(16 * 128 * q);
+                    const uint64_t dph = desc_add(d_p, pa), dpl = desc_add(d_p, pa + 2 * kGPHalfBytes);
+                    const uint64_t dbh = desc_add(d_bmn, bb), dbl = desc_add(d_bmn, bb + kGBTileBytes);
+                    mma_f16(acc, dph, dbh, (first && q == 0) ? 0u : 1u, kIdescG2);
+                    mma_f16(acc, dph, dbl, 1, kIdescG2);
+                    mma_f16(acc, dpl, dbh, 1, kIdescG2);
                 }
                 commit(b_pempty);
                 commit(b_empty0 + 8 * s);
@@ -756,16 +798,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
                 if (i >= 2 && !mbar_wait(b_se0 + 8 * k, ((i >> 1) - 1) & 1, abort, p.wait_ns)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;");
                 const uint32_t acc = tmem + (uint32_t)(kGTmemS + k * kGCols);
-                const uint32_t bh = s_stage0 + s * kGStageBytes, bl = bh + kGBTileBytes;
+                const uint32_t so = (uint32_t)(s * kGStageBytes);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_f16(acc, desc_sw128(s_a_hi + 32 * kk), desc_sw128(bh + 32 * kk), kk > 0, kIdescG1);
+                    mma_f16(acc, desc_add(d_a, 32 * kk), desc_add(d_b, so + 32 * kk), kk > 0, kIdescG1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_f16(acc, desc_sw128(s_a_hi + 32 * kk), desc_sw128(bl + 32 * kk), 1, kIdescG1);
+                    mma_f16(acc, desc_add(d_a, 32 * kk), desc_add(d_b, so + kGBTileBytes + 32 * kk), 1, kIdescG1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_f16(acc, desc_sw128(s_a_lo + 32 * kk), desc_sw128(bh + 32 * kk), 1, kIdescG1);
+                    mma_f16(acc, desc_add(d_a, kATileBytes + 32 * kk), desc_add(d_b, so + 32 * kk), 1, kIdescG1);
                 commit(b_sf0 + 8 * k);
                 issued = true;
                 if (i >= 2) ok = mma2(i - 2);  // the second products run two tiles behind
@@ -777,16 +819,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
             }
         }
     } else {
-        // ---------------- evaluation warps 2..9 ----------------
-        uint8_t *const hb = pbuf + hcol * kGPHalfBytes + row_l * 128;        // this row's P hi, this K half
-        uint8_t *const lb = pbuf + (2 + hcol) * kGPHalfBytes + row_l * 128;  // and P lo
-        const int sw = row_l & 7;                                            // 128-byte swizzle of the row
+        // ---------------- evaluation warps 2..17 ----------------
+        // this row's P hi and lo in K half part / 2, 16-byte chunks 4 (part mod 2).. of the row
+        uint8_t *const hb = pbuf + (part >> 1) * kGPHalfBytes + row_l * 128;
+        uint8_t *const lb = pbuf + (2 + (part >> 1)) * kGPHalfBytes + row_l * 128;
+        const int c0 = 4 * (part & 1), sw = row_l & 7;  // first chunk; 128-byte swizzle of the row
         {  // the running sums start at zero
-            uint32_t z[32];
+            uint32_t z[16];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) z[c] = 0u;
-            tmem_st32x32b_x32(t_hi, z);
-            tmem_st32x32b_x32(t_lo, z);
+            for (int c = 0; c < 16; ++c) z[c] = 0u;
+            tmem_st32x32b_x16(t_hi, z);
+            tmem_st32x32b_x16(t_lo, z);
             asm volatile("tcgen05.wait::st.sync.aligned;");
         }
         // group g's D2 (complete once its last second product is): fold into the running sums
@@ -794,50 +837,59 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
             const int kk = g & 1;
             if (!mbar_wait(b_df0 + 8 * kk, (g >> 1) & 1, abort, p.wait_ns)) return false;
             asm volatile("tcgen05.fence::after_thread_sync;");
-            uint32_t d[32], h[32], l[32];
-            tmem_ld32x32b_x32(tmem + lanes + (uint32_t)(kGTmemD2 + kk * 64 + 32 * hcol), d);
-            tmem_ld32x32b_x32(t_hi, h);
-            tmem_ld32x32b_x32(t_lo, l);
-            asm volatile("tcgen05.wait::ld.sync.aligned;");
-            asm volatile("tcgen05.fence::before_thread_sync;");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_de0 + 8 * kk);  // the second products of group g+2 may overwrite it
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                float hv = __uint_as_float(h[c]), lv = __uint_as_float(l[c]);
-                two_sum_add(hv, lv, __uint_as_float(d[c]));
-                h[c] = __float_as_uint(hv);
-                l[c] = __float_as_uint(lv);
+            for (int half = 0; half < 2; ++half) {  // 8 columns at a time (registers)
+                uint32_t d[8], h[8], l[8];
+                tmem_ld32x32b_x8(tmem + lanes + (uint32_t)(kGTmemD2 + kk * 64 + 16 * part + 8 * half), d);
+                tmem_ld32x32b_x8(t_hi + 8 * half, h);
+                tmem_ld32x32b_x8(t_lo + 8 * half, l);
+                asm volatile("tcgen05.wait::ld.sync.aligned;");
+                if (half == 1) {
+                    asm volatile("tcgen05.fence::before_thread_sync;");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_de0 + 8 * kk);  // the second products of group g+2 may overwrite it
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float hv = __uint_as_float(h[c]), lv = __uint_as_float(l[c]);
+                    two_sum_add(hv, lv, __uint_as_float(d[c]));
+                    h[c] = __float_as_uint(hv);
+                    l[c] = __float_as_uint(lv);
+                }
+                tmem_st32x32b_x8(t_hi + 8 * half, h);
+                tmem_st32x32b_x8(t_lo + 8 * half, l);
             }
-            tmem_st32x32b_x32(t_hi, h);
-            tmem_st32x32b_x32(t_lo, l);
             asm volatile("tcgen05.wait::st.sync.aligned;");
             return true;
         };
         bool ok = true;
         float pm = 0.f;  // largest |P| of this row's columns in this split
+        // this warp's 32 signal values of the next tile, loaded a tile ahead (their latency
+        // overlaps the P stores, the fold and the wait for S instead of following S)
+        float4 bn[8];
+        {
+            const float4 *bv = reinterpret_cast<const float4 *>(p.bpad + j_begin + 32 * part);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) bn[q] = T > 0 ? __ldg(bv + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         for (int i = 0; i < T && ok; ++i) {
             const int k = i & 1;
-            const float4 *bv = reinterpret_cast<const float4 *>(p.bpad + j_begin + (int64_t)i * kGCols + 64 * hcol);
             if (!mbar_wait(b_sf0 + 8 * k, (i >> 1) & 1, abort, p.wait_ns)) break;
             asm volatile("tcgen05.fence::after_thread_sync;");
-            // P = 2^S b for this warp's 64 points, split into fp16 hi + lo, packed two points a
+            // P = 2^S b for this warp's 32 points, split into fp16 hi + lo, packed two points a
             // register: all of it before waiting for the P tile, which the second product of the
             // previous tile may still be reading
-            uint32_t ph[32], pl[32];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
+            uint32_t ph[16], pl[16];
+            {
                 uint32_t r[32];
-                tmem_ld32x32b_x32(tmem + lanes + (uint32_t)(kGTmemS + k * kGCols + 64 * hcol + 32 * half), r);
+                tmem_ld32x32b_x32(tmem + lanes + (uint32_t)(kGTmemS + k * kGCols + 32 * part), r);
                 asm volatile("tcgen05.wait::ld.sync.aligned;");
-                if (half == 1) {
-                    asm volatile("tcgen05.fence::before_thread_sync;");
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(b_se0 + 8 * k);  // the first product of tile i+2 may overwrite it
-                }
+                asm volatile("tcgen05.fence::before_thread_sync;");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_se0 + 8 * k);  // the first product of tile i+2 may overwrite it
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const float4 b4 = __ldg(bv + 8 * half + q);
+                    const float4 b4 = bn[q];
                     const float p0 = ex2_approx(__uint_as_float(r[4 * q + 0])) * b4.x;
                     const float p1 = ex2_approx(__uint_as_float(r[4 * q + 1])) * b4.y;
                     const float p2 = ex2_approx(__uint_as_float(r[4 * q + 2])) * b4.z;
@@ -848,20 +900,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
                     const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
                     const __half2 l01 = __floats2half2_rn(p0 - f01.x, p1 - f01.y);
                     const __half2 l23 = __floats2half2_rn(p2 - f23.x, p3 - f23.y);
-                    ph[16 * half + 2 * q] = *reinterpret_cast<const uint32_t *>(&h01);
-                    ph[16 * half + 2 * q + 1] = *reinterpret_cast<const uint32_t *>(&h23);
-                    pl[16 * half + 2 * q] = *reinterpret_cast<const uint32_t *>(&l01);
-                    pl[16 * half + 2 * q + 1] = *reinterpret_cast<const uint32_t *>(&l23);
+                    ph[2 * q] = *reinterpret_cast<const uint32_t *>(&h01);
+                    ph[2 * q + 1] = *reinterpret_cast<const uint32_t *>(&h23);
+                    pl[2 * q] = *reinterpret_cast<const uint32_t *>(&l01);
+                    pl[2 * q + 1] = *reinterpret_cast<const uint32_t *>(&l23);
                 }
+            }
+            if (i + 1 < T) {
+                const float4 *bv = reinterpret_cast<const float4 *>(p.bpad + j_begin + (int64_t)(i + 1) * kGCols + 32 * part);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) bn[q] = __ldg(bv + q);
             }
             if (i >= 1 && !mbar_wait(b_pempty, (i - 1) & 1, abort, p.wait_ns)) {
                 ok = false;
                 break;
             }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // 16-byte chunk c = points 8c..8c+7 of this K half, swizzled
-                *reinterpret_cast<uint4 *>(hb + ((c ^ sw) << 4)) = make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
-                *reinterpret_cast<uint4 *>(lb + ((c ^ sw) << 4)) = make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
+            for (int cc = 0; cc < 4; ++cc) {  // chunk c0 + cc = points 8 (c0 + cc).. of the K half, swizzled
+                const int c = c0 + cc;
+                *reinterpret_cast<uint4 *>(hb + ((c ^ sw) << 4)) = make_uint4(ph[4 * cc], ph[4 * cc + 1], ph[4 * cc + 2], ph[4 * cc + 3]);
+                *reinterpret_cast<uint4 *>(lb + ((c ^ sw) << 4)) = make_uint4(pl[4 * cc], pl[4 * cc + 1], pl[4 * cc + 2], pl[4 * cc + 3]);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
             __syncwarp();
@@ -869,27 +927,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
             if (i >= 1 && (i - 1) % kGGroup == kGGroup - 1) ok = fold((i - 1) / kGGroup);
         }
         if (ok && !*abort && T > 0) fold((T - 1) / kGGroup);
-        pmx[hcol][row_l] = pm;
+        atomicMax(&pmx[row_l], __float_as_uint(pm));
     }
 
     __syncthreads();
     const bool ok = !*abort;
     if (!ok && t == 0) atomicOr(&g_tc_status, 1u);
-    // every row's 64 running sums (hi, lo) through the idle P tile, so both halves see s0 (column D)
+    // every row's 64 running sums (hi, lo) through the idle P tile, so every part sees s0 (column D)
     float *red = reinterpret_cast<float *>(pbuf);
-    float ah[32], al[32];
+    float ah[16], al[16];
     if (w >= 2) {
-        uint32_t h[32], l[32];
+        uint32_t h[16], l[16];
         asm volatile("tcgen05.fence::after_thread_sync;");
-        tmem_ld32x32b_x32(t_hi, h);
-        tmem_ld32x32b_x32(t_lo, l);
+        tmem_ld32x32b_x16(t_hi, h);
+        tmem_ld32x32b_x16(t_lo, l);
         asm volatile("tcgen05.wait::ld.sync.aligned;");
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < 16; ++c) {
             ah[c] = __uint_as_float(h[c]);
             al[c] = __uint_as_float(l[c]);
-            red[row_l * 64 + 32 * hcol + c] = ah[c];
-            red[kRows * 64 + row_l * 64 + 32 * hcol + c] = al[c];
+            red[row_l * 64 + 16 * part + c] = ah[c];
+            red[kRows * 64 + row_l * 64 + 16 * part + c] = al[c];
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
@@ -900,8 +958,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
         // A row whose largest |P| in this split is below 2^-8 (every point far from it, or a small
         // signal there) keeps too few bits in the fp16 P tile: the CUDA-core kernel launched
         // after this one redoes this split's part of it (the flag says so), exactly.
-        const bool weak = ok && T > 0 && fmaxf(pmx[0][row_l], pmx[1][row_l]) < 0x1p-8f;
-        if (i < p.M && hcol == 0) p.flags[(int64_t)blockIdx.y * p.M + i] = weak ? 1 : 0;
+        const bool weak = ok && T > 0 &&
+                          __uint_as_float(pmx[row_l]) < 0x1p-8f;
+        if (i < p.M && part == 0) p.flags[(int64_t)blockIdx.y * p.M + i] = weak ? 1 : 0;
         if (i < p.M && !weak) {
             const double s0 = (double)red[row_l * 64 + p.D] + (double)red[kRows * 64 + row_l * 64 + p.D];
             // the signal went in as b / 2^e (pow2_above of its largest magnitude): scale back
@@ -909,8 +968,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_grad_kernel(const __grid_con
                 (double)p.gscale * (double)__ldg(p.g + i) * (double)pow2_above(__uint_as_float(p.guard[2]));
             const float nan = __int_as_float(0x7fc00000);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const int d = 32 * hcol + c;
+            for (int c = 0; c < 16; ++c) {
+                const int d = 16 * part + c;
                 if (d >= p.D) continue;
                 const double xd = (double)(p.c * __ldg(p.x + i * p.D + d));
                 const double v = (xd * s0 - ((double)ah[c] + (double)al[c])) * sc;
@@ -1055,14 +1114,14 @@ cudaError_t tc_launch_grad(const TcArgs &a, dim3 grid, cudaStream_t s) {
     p.flags = a.flags;
     cudaError_t e = tc_set_attributes();
     if (e != cudaSuccess) return e;
-    tc_grad_kernel<<<grid, kThreadsTc, kGSmemBytes, s>>>(p);
+    tc_grad_kernel<<<grid, kGThreads, kGSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
 
 int tc_grad_occupancy() {
     int n = 0;
     if (tc_set_attributes() != cudaSuccess) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_grad_kernel, kThreadsTc, kGSmemBytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_grad_kernel, kGThreads, kGSmemBytes) != cudaSuccess)
         return 0;
     return n;
 }

@@ -10,6 +10,10 @@
 
 namespace kr {
 
+// Threads of the tensor-core x-gradient's block: a TMA warp, an MMA warp and 16 evaluation
+// warps (four per TMEM lane quarter, each with 32 of a tile's 128 points).
+constexpr int kTcGradThreads = 64 + 32 * 16;
+
 // Host-side description of one tensor-core Sum launch.
 struct TcArgs {
     const __half *a_hi, *a_lo;  // m_pad x 64 augmented x operands (split fp16), m_pad % kTcRows == 0
