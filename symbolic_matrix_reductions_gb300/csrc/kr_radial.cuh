@@ -24,6 +24,8 @@
 // b = NaN: k NaN is NaN, which neither wins a comparison nor survives fmaxf.
 #pragma once
 
+#include <type_traits>
+
 #include "kr_kernels_packed.cuh"
 
 namespace kr {
@@ -114,6 +116,8 @@ __device__ __forceinline__ void radial_load(const float *rec, typename Lanes<L>:
 // tests less often but recomputes more points when a lane's maximum rose (and some lane
 // of a warp usually does in each tile).
 KR_HD constexpr int radial_max_block(int KT) { return 2; }
+// The same for the Gaussian's log-domain scan (one compare a pair, no ex2 to hide it behind).
+KR_HD constexpr int log_max_block() { return 2; }
 
 // k of a row (coordinates xr, prescaled) against the L points of a record: the distance
 // summed in dist_chains(DP) interleaved chains, then the kernel.  Max recomputes values
@@ -138,6 +142,28 @@ __device__ __forceinline__ typename Lanes<L>::T radial_k(const typename Lanes<L>
 #pragma unroll
     for (int c = 1; c < NC; ++c) q = V::add(q, qc[c]);
     return V::template kval<KT>(q);
+}
+
+// Gaussian Max / Min in the log domain: the key t = |x'-y'|^2 - log2|b| of a row against
+// the L points of a record whose value slot holds -log2|b| (the first chain starts there),
+// so that k b = sign(b) 2^-t.  Used by the scan and by the index recomputation alike.
+template <int DP, int L, int PS>
+__device__ __forceinline__ typename Lanes<L>::T log_key(const typename Lanes<L>::T (&xr)[DP],
+                                                        const typename Lanes<L>::T (&pv)[PS / L]) {
+    typedef Lanes<L> V;
+    typedef typename V::T T;
+    constexpr int NC = dist_chains(DP);
+    T qc[NC];
+#pragma unroll
+    for (int d = 0; d < DP; ++d) {
+        const T df = V::add(xr[d], pv[d]);
+        const int c = d % NC;
+        qc[c] = d < NC ? (c == 0 ? V::fma(df, df, pv[DP]) : V::mul(df, df)) : V::fma(df, df, qc[c]);
+    }
+    T q = qc[0];
+#pragma unroll
+    for (int c = 1; c < NC; ++c) q = V::add(q, qc[c]);
+    return q;
 }
 
 template <int DP, int EP, int R, int BN, int KT, int RED>
@@ -208,8 +234,126 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
             last[r][e] = -1;
         }
 
+    // Gaussian Max / Min, dense mode, E = 1: the log domain.  With v_j = vsign b_j, the signs
+    // of v over the block's column chunk fix where the extreme can come from, the same for all
+    // its rows: some v_j > 0: the largest k v is 2^-t at the smallest key t = |x'-y'|^2 -
+    // log2 v_j over those points (mode 1); all v_j < 0 (none zero): it is -2^-t at the largest
+    // key over them (mode 2); otherwise (zeros without positives, only NaN, none) the value
+    // scan below (mode 0).  The scan then needs no ex2 and no product per pair, and the order
+    // of the keys is that of the values up to the rounding of t.  A row that finds no finite
+    // key (infinite or NaN coordinates) sends its block back to the value scan.
+    constexpr bool kLogMax = KT == KT_GAUSS && RED == RR_MAX && EP == 1 && L == 2;
+    constexpr int LB = log_max_block();
+    static_assert(!kLogMax || BN % (LB * UPT) == 0, "tile must be a multiple of the log-domain block");
+    int mode = 0;
+    if constexpr (kLogMax) {
+        if (!ranged) {
+            int f = 0;
+            for (int64_t j = j_begin + t; j < j_end; j += kThreads) {
+                const float v = a.vsign * ldg_chk(a, a.b, j, a.N, KRD_B);
+                f |= v > 0.f ? 1 : v < 0.f ? 2 : v == 0.f ? 4 : 0;
+            }
+            const bool any_pos = __syncthreads_or(f & 1), any_neg = __syncthreads_or(f & 2);
+            const bool any_zero = __syncthreads_or(f & 4);
+            mode = any_pos ? 1 : (any_neg && !any_zero) ? 2 : 0;
+        }
+    }
+    if constexpr (kLogMax) {
+        if (mode != 0) {
+            const bool neg = mode == 2;
+            const float none = neg ? -f_inf() : f_inf();  // the key of a point that cannot win
+            float tb[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) tb[r] = none;
+            // one tile: blocks of IB steps tested once against the best key; the last block that
+            // improved it is recomputed at the end of the tile for the first point attaining it
+            auto log_tile = [&](auto negc, int64_t jt, int nvp) {
+                constexpr bool NEG = decltype(negc)::value;
+                int lastb[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) lastb[r] = -1;
+                for (int jb = 0; jb < nvp; jb += LB * UPT) {
+                    float bm[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) bm[r] = NEG ? -f_inf() : f_inf();
+#pragma unroll
+                    for (int g = 0; g < LB; ++g)
+#pragma unroll
+                        for (int u = 0; u < UR; ++u) {
+                            T pv[PS / L];
+                            radial_load<L, PS>(tile + ((jb + g * UPT) / L + u) * PS, pv);
+#pragma unroll
+                            for (int r = 0; r < R; ++r) {
+                                const T k = log_key<DP, L, PS>(xr[r], pv);
+                                bm[r] = NEG ? fmax3(bm[r], k.x, k.y) : fmin3(bm[r], k.x, k.y);
+                            }
+                        }
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        lastb[r] = (NEG ? bm[r] > tb[r] : bm[r] < tb[r]) ? jb : lastb[r];
+                        tb[r] = NEG ? fmaxf(tb[r], bm[r]) : fminf(tb[r], bm[r]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int jb = lastb[r];
+                    if (jb < 0) continue;
+                    bool found = false;
+                    for (int u = 0; u < LB * UR; ++u) {
+                        T pv[PS / L];
+                        radial_load<L, PS>(tile + (jb / L + u) * PS, pv);
+                        const T k = log_key<DP, L, PS>(xr[r], pv);
+#pragma unroll
+                        for (int l = 0; l < L; ++l) {
+                            if (!found && V::lane(k, l) == tb[r]) {
+                                bj[r][0] = (int)(jt + jb + u * L + l);
+                                found = true;
+                            }
+                        }
+                    }
+                }
+            };
+            for (int64_t jt = j_begin; jt < j_end; jt += BN) {
+                const int nv = (int)min((int64_t)BN, j_end - jt);
+                const int nvp = (nv + LB * UPT - 1) / (LB * UPT) * (LB * UPT);
+                __syncthreads();  // every thread is done with the previous tile
+                for (int p = t; p < nvp; p += kThreads) {
+                    float key = none;
+                    if (p < nv) {
+#pragma unroll
+                        for (int d = 0; d < DP; ++d)
+                            if (d < a.D) *radial_slot<L, PS>(tile, p, d) = -a.c * ldg_chk(a, a.y, (jt + p) * a.D + d, a.N * a.D, KRD_Y);
+                        const float v = a.vsign * ldg_chk(a, a.b, jt + p, a.N, KRD_B);
+                        if (neg ? v < 0.f : v > 0.f) key = -log2f(fabsf(v));
+                    } else {
+#pragma unroll
+                        for (int d = 0; d < DP; ++d)
+                            if (d < a.D) *radial_slot<L, PS>(tile, p, d) = 0.f;
+                    }
+                    *radial_slot<L, PS>(tile, p, DP) = key;
+                }
+                __syncthreads();  // tile staged
+                if (neg)
+                    log_tile(std::true_type(), jt, nvp);
+                else
+                    log_tile(std::false_type(), jt, nvp);
+            }
+            bool open = false;
+#pragma unroll
+            for (int r = 0; r < R; ++r) open |= row0 + (int64_t)r * kThreads + t < row_end && bj[r][0] < 0;
+            if (__syncthreads_or(open)) {
+                mode = 0;  // the value scan redoes this block's chunk
+#pragma unroll
+                for (int r = 0; r < R; ++r) bj[r][0] = -1;
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r) hi[r][0] = neg ? -exp2f(-tb[r]) : exp2f(-tb[r]);
+            }
+        }
+    }
+
     int tk = 0;  // block-sparse: tiles seen over the block's ranges; split y takes tk = y mod S
-    for (int rr = r_lo; rr < r_hi; ++rr) {
+    for (int rr = r_lo; rr < r_hi && mode == 0; ++rr) {
     const int64_t js = ranged ? (int64_t)a.rng[rr].x : j_begin;
     const int64_t je = ranged ? (int64_t)a.rng[rr].y : j_end;
     for (int64_t jt = js; jt < je; jt += BN) {

@@ -104,6 +104,39 @@ def test_maxmin_ties_lowest_index(orc):
                 assert np.array_equal(_np(idx), i_ref), (kernel, red, split)
 
 
+def test_gaussian_maxmin_log_domain_modes(orc):
+    """Gaussian Max / Min with one signal column scan the keys |x'-y'|^2 - log2|v| (v = b
+    for Max, -b for Min) in a mode fixed by the signs of v over a block's column chunk:
+    some positive (the smallest key over them), all negative (the largest key), or zeros
+    without positives (the value scan).  Each case against the oracle, unsplit and with
+    splits whose chunks take different modes; with rows of infinite or NaN coordinates
+    (their blocks go back to the value scan) and without."""
+    r = np.random.Generator(np.random.PCG64(77))
+    M, N, D = 1500, 2600, 3
+    x = r.standard_normal((M, D)).astype(np.float32)
+    y = r.standard_normal((N, D)).astype(np.float32)
+    x_bad = x.copy()
+    x_bad[5, 0] = np.inf     # every distance infinite: value 0 at the first index
+    x_bad[1300, 1] = np.nan  # every value NaN: -inf (Max) / +inf (Min), index -1
+    pos = (np.abs(r.standard_normal((N, 1))) + 0.05).astype(np.float32)
+    j = np.arange(N)[:, None]
+    cases = {
+        "positive": pos,
+        "negative": -pos,
+        "zeros and negatives": np.where(j % 7 == 0, 0.0, -pos).astype(np.float32),
+        "positive then negative": np.where(j < N // 2, pos, -pos).astype(np.float32),
+        "mixed": r.standard_normal((N, 1)).astype(np.float32),
+    }
+    for xs, xname in ((x, "finite rows"), (x_bad, "inf and NaN rows")):
+        for name, b in cases.items():
+            for red in ("max", "min"):
+                v_ref, i_ref, s_ref = orc.kernel_maxmin(xs, y, b, 0.9, "gaussian", red)
+                for split in (0, 1, 2, 5):
+                    idx, val = kr.kernel_reduce_arg(*_dev(xs, y, b), 0.9, red, split=split)
+                    check_maxmin(_np(val), _np(idx), xs, y, b, 0.9, "gaussian", v_ref, i_ref, s_ref,
+                                 f"{xname}, {name}, {red}, split {split}")
+
+
 def test_maxmin_empty_and_degenerate(orc):
     x, y, b = _case(3, 50, 0, 3, 2)
     xt, yt, bt = _dev(x, np.zeros((0, 3), np.float32), np.zeros((0, 2), np.float32))
