@@ -889,17 +889,22 @@ __global__ void __launch_bounds__(kGThreads, 1) tc_grad_kernel(const __grid_cons
                 if (lane == 0) mbar_arrive(b_se0 + 8 * k);  // the first product of tile i+2 may overwrite it
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
+                    // two points an instruction (f32x2) for the products and the residuals
                     const float4 b4 = bn[q];
-                    const float p0 = ex2_approx(__uint_as_float(r[4 * q + 0])) * b4.x;
-                    const float p1 = ex2_approx(__uint_as_float(r[4 * q + 1])) * b4.y;
-                    const float p2 = ex2_approx(__uint_as_float(r[4 * q + 2])) * b4.z;
-                    const float p3 = ex2_approx(__uint_as_float(r[4 * q + 3])) * b4.w;
-                    pm = fmax3(pm, fabsf(p0), fabsf(p1));
-                    pm = fmax3(pm, fabsf(p2), fabsf(p3));
-                    const __half2 h01 = __floats2half2_rn(p0, p1), h23 = __floats2half2_rn(p2, p3);
-                    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                    const __half2 l01 = __floats2half2_rn(p0 - f01.x, p1 - f01.y);
-                    const __half2 l23 = __floats2half2_rn(p2 - f23.x, p3 - f23.y);
+                    const float2 p01 = __fmul2_rn(make_float2(ex2_approx(__uint_as_float(r[4 * q + 0])),
+                                                              ex2_approx(__uint_as_float(r[4 * q + 1]))),
+                                                  make_float2(b4.x, b4.y));
+                    const float2 p23 = __fmul2_rn(make_float2(ex2_approx(__uint_as_float(r[4 * q + 2])),
+                                                              ex2_approx(__uint_as_float(r[4 * q + 3]))),
+                                                  make_float2(b4.z, b4.w));
+                    pm = fmax3(pm, fabsf(p01.x), fabsf(p01.y));
+                    pm = fmax3(pm, fabsf(p23.x), fabsf(p23.y));
+                    const __half2 h01 = __floats2half2_rn(p01.x, p01.y), h23 = __floats2half2_rn(p23.x, p23.y);
+                    const float2 m1 = make_float2(-1.f, -1.f);
+                    const float2 d01 = __ffma2_rn(__half22float2(h01), m1, p01);  // p - hi, exact
+                    const float2 d23 = __ffma2_rn(__half22float2(h23), m1, p23);
+                    const __half2 l01 = __floats2half2_rn(d01.x, d01.y);
+                    const __half2 l23 = __floats2half2_rn(d23.x, d23.y);
                     ph[2 * q] = *reinterpret_cast<const uint32_t *>(&h01);
                     ph[2 * q + 1] = *reinterpret_cast<const uint32_t *>(&h23);
                     pl[2 * q] = *reinterpret_cast<const uint32_t *>(&l01);

@@ -310,7 +310,7 @@ def test_workload_knn_d16(orc):
 TC_CASES = [
     (1, 1, 32, 0.9, 0), (127, 129, 50, 1.0, 0), (300, 1000, 50, 1.0, 0), (300, 1000, 50, 1.0, 3),
     (513, 2000, 62, 1.3, 0), (256, 4096, 32, 0.8, 5), (1000, 300, 40, 1.1, 0),
-    (130, 20001, 50, 1.0, 1),   # one split: 79 tiles per block, the stage and accumulator rings wrap many times
+    (130, 20001, 50, 1.0, 1),   # one split: 79 tiles per block (the gradient: 157), the rings wrap many times
 ]
 
 
@@ -406,7 +406,11 @@ def test_tensor_core_wait_bound_reports_status(orc, op, split):
         check_grad(a, gx_ref, G_ref, "after a run-out wait")
 
 
-@pytest.mark.parametrize("M,N,D,sigma,split", TC_CASES + [(200, 3000, 61, 1.2, 2), (129, 257, 33, 0.7, 0)])
+@pytest.mark.parametrize("M,N,D,sigma,split", TC_CASES + [
+    (200, 3000, 61, 1.2, 2), (129, 257, 33, 0.7, 0),
+    # one split of 5, 8 and 9 tiles of 128 points: the D2 groups of 4 tiles folded inside the
+    # loop and after it in every combination
+    (100, 513, 50, 1.0, 1), (100, 1024, 50, 1.0, 1), (100, 1025, 40, 1.0, 1)])
 def test_tensor_core_grad(orc, M, N, D, sigma, split):
     """The x-gradient with both contractions on the tensor cores (S = A.B^T, then
     P.[y' | 1] with P = 2^S b split into fp16 hi + lo), against the oracle's gradient and
