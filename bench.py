@@ -371,6 +371,11 @@ def run_ours(args, rank, world, local_rank):
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     max_mhz = float(json.load(open(peaks_path)).get("sm_max_mhz", 2070.0)) if os.path.exists(peaks_path) else 2070.0
 
+    if args.lines:  # only the named secondary lines (a short command to profile one kernel)
+        probe = probe_pipes(torch, nsm)
+        names = [n.strip() for n in args.lines.split(",") if n.strip()]
+        return {"lines": names, "secondary": secondary(torch, kr, W, nsm, max_mhz, probe["xu_lanes"], dev, names)}
+
     inp = W.generate(args.workload, M=args.size[0], N=args.size[1]) if args.size else W.generate(args.workload)
     M, D = inp["x"].shape
     N, E = inp["y"].shape[0], inp["b"].shape[1]
@@ -630,9 +635,14 @@ def measure_d50(torch, kr, W, nsm, max_mhz, xu_lanes, dev, args):
     return out
 
 
-def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
-    """Other workloads and reductions, 3 warm-up + 10 timed runs each (median), with rooflines."""
+def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev, only=None):
+    """Other workloads and reductions, 3 warm-up + 10 timed runs each (median), with rooflines.
+    only: names of the lines to run (an op name as the lines print it, e.g. "max (gaussian)",
+    "sum (batched)"); None: all."""
     out = []
+
+    def want(name):
+        return only is None or name in only
     inp = W.generate("gauss_d3")
     x, y, bb, gg = (torch.from_numpy(inp[k]).to(dev) for k in ("x", "y", "b", "g"))
     M, D = x.shape
@@ -645,6 +655,8 @@ def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
                 ("grad", lambda: kr.kernel_reduce_grad_x(x, y, bb, gg, s), kr.OP_GRAD, E),
                 ("knn", lambda: kr.kernel_knn(x, y, K_NN), kr.OP_KNN, K_NN))
     for op, fn, code, ek in step_ops:
+        if not want(op):
+            continue
         p = kr.plan_device(code, M, N, D, ek)
         ms, how = _median_ms(torch, fn)
         out.append({"workload": wl, "op": op, "ms": ms, "value": M * N / (ms / 1e3), "unit": UNIT,
@@ -652,6 +664,8 @@ def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
                     "roofline": roofline(op, D, E, ms / 1e3, M * N, nsm, max_mhz, xu_lanes, f"{op}[D={D}]")})
     for op, kind in (("sum", "laplace"), ("sum", "cauchy"), ("sum", "imq"), ("max", "gaussian"),
                      ("min", "gaussian"), ("max", "cauchy")):
+        if not want(f"{op} ({kind})"):
+            continue
         fn = (lambda op=op, kind=kind: kr.kernel_reduce(x, y, bb, s, op, kernel=kind))
         p = kr.plan_device(kr.OP_SUM if op == "sum" else kr.OP_MAX, M, N, D, E, kernel=kind)
         ms, how = _median_ms(torch, fn)
@@ -661,6 +675,8 @@ def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
                     "split": p.split, "path": "cuda cores", "timing": how, "roofline": rl})
     # the transposed problem: N output rows, reduction over the M points of x
     for op in ("grad_y", "grad_b"):
+        if not want(op):
+            continue
         if op == "grad_y":
             fn = (lambda: kr.kernel_reduce_grad_y(x, y, bb, gg, s))
             p = kr.plan_device(kr.OP_GRAD, N, M, D, E)
@@ -675,59 +691,62 @@ def secondary(torch, kr, W, nsm, max_mhz, xu_lanes, dev):
                     "split": p.split, "path": "cuda cores", "timing": how, "roofline": rl})
     del x, y, bb, gg
 
-    # batch dimension: 256 independent gauss_d3-distributed problems of 2000 x 2000 points
-    r = np.random.Generator(np.random.PCG64(2024))
-    Bb, Mb = 256, 2000
-    xb = torch.from_numpy(r.standard_normal((Bb, Mb, 3)).astype(np.float32)).to(dev)
-    yb = torch.from_numpy(r.standard_normal((Bb, Mb, 3)).astype(np.float32)).to(dev)
-    bb3 = torch.from_numpy(r.standard_normal((Bb, Mb, 1)).astype(np.float32)).to(dev)
-    batch_fn = (lambda: kr.kernel_reduce(xb, yb, bb3, 0.5, "sum"))
-    ms, how = _steady_ms(torch, batch_fn)
-    ms1, how1 = _median_ms(torch, batch_fn)
-    pairs = Bb * Mb * Mb
-    how["single_call"] = dict(how1, ms=ms1, value=pairs / (ms1 / 1e3))
-    out.append({"workload": f"batch of {Bb} problems, M=N={Mb}, D=3, x,y,b ~ N(0,1), sigma=0.5", "op": "sum (batched)",
-                "ms": ms, "value": pairs / (ms / 1e3), "unit": UNIT, "split": None, "path": "cuda cores",
-                "timing": how, "roofline": roofline("sum", 3, 1, ms / 1e3, pairs, nsm, max_mhz, xu_lanes,
-                                                    f"fwd_kernel<Sum>[D=3,E=1] x {Bb} (grid z)")})
-    del xb, yb, bb3
+    if want('sum (batched)'):
+        # batch dimension: 256 independent gauss_d3-distributed problems of 2000 x 2000 points
+        r = np.random.Generator(np.random.PCG64(2024))
+        Bb, Mb = 256, 2000
+        xb = torch.from_numpy(r.standard_normal((Bb, Mb, 3)).astype(np.float32)).to(dev)
+        yb = torch.from_numpy(r.standard_normal((Bb, Mb, 3)).astype(np.float32)).to(dev)
+        bb3 = torch.from_numpy(r.standard_normal((Bb, Mb, 1)).astype(np.float32)).to(dev)
+        batch_fn = (lambda: kr.kernel_reduce(xb, yb, bb3, 0.5, "sum"))
+        ms, how = _steady_ms(torch, batch_fn)
+        ms1, how1 = _median_ms(torch, batch_fn)
+        pairs = Bb * Mb * Mb
+        how["single_call"] = dict(how1, ms=ms1, value=pairs / (ms1 / 1e3))
+        out.append({"workload": f"batch of {Bb} problems, M=N={Mb}, D=3, x,y,b ~ N(0,1), sigma=0.5", "op": "sum (batched)",
+                    "ms": ms, "value": pairs / (ms / 1e3), "unit": UNIT, "split": None, "path": "cuda cores",
+                    "timing": how, "roofline": roofline("sum", 3, 1, ms / 1e3, pairs, nsm, max_mhz, xu_lanes,
+                                                        f"fwd_kernel<Sum>[D=3,E=1] x {Bb} (grid z)")})
+        del xb, yb, bb3
 
-    # block-sparse: the gauss_d3_unit clouds (1e6 points each) sorted into 250 slabs along the
-    # first coordinate; cluster c of x reduces over slabs c-1..c+1 of y (a truncated kernel
-    # product; the value counts the pairs evaluated)
-    inp = W.generate("gauss_d3_unit")
-    xs = inp["x"][np.argsort(inp["x"][:, 0], kind="stable")]
-    order = np.argsort(inp["y"][:, 0], kind="stable")
-    ys, bs = inp["y"][order], inp["b"][order]
-    M, N, C = xs.shape[0], ys.shape[0], 250
-    ex, ey = np.linspace(0, M, C + 1).astype(np.int64), np.linspace(0, N, C + 1).astype(np.int64)
-    ri = np.stack([ex[:-1], ex[1:]], 1)
-    rj = np.array([[ey[max(c - 1, 0)], ey[min(c + 2, C)]] for c in range(C)])
-    si = np.arange(1, C + 1)
-    pairs = int(sum((ri[c, 1] - ri[c, 0]) * (rj[c, 1] - rj[c, 0]) for c in range(C)))
-    xt, yt, bt = (torch.from_numpy(a_).to(dev) for a_ in (xs, ys, bs))
-    ms, how = _median_ms(torch, lambda: kr.kernel_reduce_ranges(xt, yt, bt, inp["sigma"], "sum", ri, si, rj))
-    out.append({"workload": f"gauss_d3_unit clouds (1e6 points) sorted into {C} slabs along x_0; each cluster reduces "
-                            f"over its 3 neighbouring slabs ({pairs} of {M * N} pairs evaluated)",
-                "op": "sum (block-sparse)", "ms": ms, "value": pairs / (ms / 1e3), "unit": UNIT, "split": None,
-                "path": "cuda cores", "timing": how,
-                "roofline": roofline("sum", 3, 1, ms / 1e3, pairs, nsm, max_mhz, xu_lanes,
-                                     "radial_kernel<gaussian,Sum>[D=3,E=1] (ranges)")})
-    del xt, yt, bt
+    if want('sum (block-sparse)'):
+        # block-sparse: the gauss_d3_unit clouds (1e6 points each) sorted into 250 slabs along the
+        # first coordinate; cluster c of x reduces over slabs c-1..c+1 of y (a truncated kernel
+        # product; the value counts the pairs evaluated)
+        inp = W.generate("gauss_d3_unit")
+        xs = inp["x"][np.argsort(inp["x"][:, 0], kind="stable")]
+        order = np.argsort(inp["y"][:, 0], kind="stable")
+        ys, bs = inp["y"][order], inp["b"][order]
+        M, N, C = xs.shape[0], ys.shape[0], 250
+        ex, ey = np.linspace(0, M, C + 1).astype(np.int64), np.linspace(0, N, C + 1).astype(np.int64)
+        ri = np.stack([ex[:-1], ex[1:]], 1)
+        rj = np.array([[ey[max(c - 1, 0)], ey[min(c + 2, C)]] for c in range(C)])
+        si = np.arange(1, C + 1)
+        pairs = int(sum((ri[c, 1] - ri[c, 0]) * (rj[c, 1] - rj[c, 0]) for c in range(C)))
+        xt, yt, bt = (torch.from_numpy(a_).to(dev) for a_ in (xs, ys, bs))
+        ms, how = _median_ms(torch, lambda: kr.kernel_reduce_ranges(xt, yt, bt, inp["sigma"], "sum", ri, si, rj))
+        out.append({"workload": f"gauss_d3_unit clouds (1e6 points) sorted into {C} slabs along x_0; each cluster reduces "
+                                f"over its 3 neighbouring slabs ({pairs} of {M * N} pairs evaluated)",
+                    "op": "sum (block-sparse)", "ms": ms, "value": pairs / (ms / 1e3), "unit": UNIT, "split": None,
+                    "path": "cuda cores", "timing": how,
+                    "roofline": roofline("sum", 3, 1, ms / 1e3, pairs, nsm, max_mhz, xu_lanes,
+                                         "radial_kernel<gaussian,Sum>[D=3,E=1] (ranges)")})
+        del xt, yt, bt
 
-    # the D = 16 K-min
-    inp = W.generate("knn_d16")
-    x, y = (torch.from_numpy(inp[k]).to(dev) for k in ("x", "y"))
-    M, D = x.shape
-    N = y.shape[0]
-    K = inp["K"]
-    p = kr.plan_device(kr.OP_KNN, M, N, D, K)
-    ms, how = _median_ms(torch, lambda: kr.kernel_knn(x, y, K), warm=3, runs=5)
-    out.append({"workload": f"knn_d16: {W.WORKLOADS['knn_d16'].note}", "op": "knn", "ms": ms,
-                "value": M * N / (ms / 1e3), "unit": UNIT, "split": p.split, "path": "cuda cores", "timing": how,
-                "roofline": roofline("knn", D, 1, ms / 1e3, M * N, nsm, max_mhz, xu_lanes,
-                                     f"knn_kernel[D={D},K={K}]")})
-    del x, y
+    if want('knn'):
+        # the D = 16 K-min
+        inp = W.generate("knn_d16")
+        x, y = (torch.from_numpy(inp[k]).to(dev) for k in ("x", "y"))
+        M, D = x.shape
+        N = y.shape[0]
+        K = inp["K"]
+        p = kr.plan_device(kr.OP_KNN, M, N, D, K)
+        ms, how = _median_ms(torch, lambda: kr.kernel_knn(x, y, K), warm=3, runs=5)
+        out.append({"workload": f"knn_d16: {W.WORKLOADS['knn_d16'].note}", "op": "knn", "ms": ms,
+                    "value": M * N / (ms / 1e3), "unit": UNIT, "split": p.split, "path": "cuda cores", "timing": how,
+                    "roofline": roofline("knn", D, 1, ms / 1e3, M * N, nsm, max_mhz, xu_lanes,
+                                         f"knn_kernel[D={D},K={K}]")})
+        del x, y
     torch.cuda.empty_cache()
     return out
 
@@ -843,6 +862,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the CPU baseline sample")
     ap.add_argument("--size", type=lambda v: tuple(int(t) for t in v.split(",")), default=None,
                     help="M,N: the workload's distributions at another size (e.g. a smaller case to profile)")
+    ap.add_argument("--lines", default=None,
+                    help="run only these secondary lines (comma-separated op names as printed, e.g. "
+                         "'max (gaussian)'), nothing else: a short command to profile one kernel")
     ap.add_argument("--no-secondary", action="store_true",
                     help="only the step (no D = 50 line, no secondary lines, no CPU baseline): a short command "
                          "to profile")
