@@ -168,3 +168,20 @@ def test_far_subset_and_duplicates(orc):
     x = r.standard_normal((900, 3))
     for split in (0, 4):
         _run(orc, x, y, 10, split, f"far+dup S{split}", exact_rows=60)
+
+
+@pytest.mark.parametrize("D,split", [(3, 4), (16, 3), (8, 7)])
+def test_split_with_all_neighbours_in_one_split(orc, D, split):
+    """Split-j where every row's nearest points are in the first split's columns and the later
+    splits hold only far points (their lists fill with far candidates): the merged lists must
+    give the oracle's result."""
+    r = np.random.Generator(np.random.PCG64(404 + D + split))
+    M, N, K = 700, 9000, 10
+    x = r.standard_normal((M, D)).astype(np.float32)
+    near = (x[r.integers(0, M, size=2000)] + 0.01 * r.standard_normal((2000, D))).astype(np.float32)
+    far = (5.0 + r.standard_normal((N - 2000, D))).astype(np.float32)
+    y = np.concatenate([near, far])
+    idx, dist = kr.kernel_knn(*(torch.from_numpy(a).to(DEV) for a in (x, y)), K, split=split)
+    torch.cuda.synchronize()
+    i_ref, d_ref, n_ref = orc.knn(x, y, K)
+    check_knn(idx.cpu().numpy(), dist.cpu().numpy(), x, y, i_ref, d_ref, n_ref, f"one split near D{D} S{split}")
