@@ -65,3 +65,21 @@ def test_roofline_peaks():
     t = bench.roofline("grad", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, name)["traffic"]
     assert t == (bench.TRAFFIC[name]["bytes_per_launch"] if fresh else None)
     assert bench.roofline("grad", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "other")["traffic"] is None
+
+
+def test_gaussian_max_reports_both_bounds():
+    """The Gaussian Max / Min with one column is measured against the method's count (k b
+    formed per pair: 2D + 1 FP32, one ex2, one compare) and, beside it, against the
+    log-domain scan's own count (2D FP32 + 1 compare); other kernels and wider signals carry
+    only the method's."""
+    xu = {"ex2": 32.0, "rcp": 16.0, "rsqrt": 16.0, "sqrt": 16.0}
+    clk = 152 * 2070e6
+    m = bench.roofline("max", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "k")
+    assert m["ops_per_pair"] == {"fp32": 7, "xu": {"ex2": 1}, "cmp": 1}
+    assert abs(m["peak"] - clk * 128 / 7) < 1
+    assert m["own_bound"]["ops_per_pair"] == {"fp32": 6, "xu": {}, "cmp": 1}
+    assert abs(m["own_bound"]["peak"] - clk * 128 / 6) < 1
+    assert m["own_bound"]["frac"] < m["frac"]
+    assert "own_bound" in bench.roofline("min", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "k")
+    assert "own_bound" not in bench.roofline("max", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "k", kind="cauchy")
+    assert "own_bound" not in bench.roofline("max", 3, 4, 1e-3, 1e9, 152, 2070.0, xu, "k")
