@@ -64,10 +64,11 @@ WARM_SECONDARY, RUNS_SECONDARY = 3, 10
 # pipe before the ex2; Cauchy and the inverse multiquadric start the distance sum at 1
 # and take one rcp / rsqrt instead of the ex2.  Each XU operation has its own rate
 # (measured by the pipe probe), so XU counts are kept per operation.  Max/Min: k*b is
-# one multiply per column and the running comparison one compare per pair.  The Gaussian
-# with one column scans keys |x'-y'|^2 - log2|b| instead (the log2 starts the distance's
-# fma chain): D sub + D fma + 1 compare, no ex2 and no product; its line reports that
-# bound too ("own_bound"), beside the method's count.
+# one multiply per column and the running comparison one compare per pair.  With one column
+# the kernel scans a key instead (Gaussian q - log2|b|, the log2 starting the distance's fma
+# chain: D sub + D fma + 1 compare; Laplace sqrt(q) - log2|b|: one more add and the sqrt;
+# Cauchy (1 + q) / |b| and inverse multiquadric (1 + q) / b^2: one more multiply, no XU);
+# its line reports that bound too ("own_bound"), beside the method's count.
 XU_PER_KERNEL = {"gaussian": {"ex2": 1}, "laplace": {"sqrt": 1, "ex2": 1}, "cauchy": {"rcp": 1},
                  "imq": {"rsqrt": 1}}
 
@@ -252,12 +253,16 @@ def roofline(op, D, E, seconds_per_launch, pairs, nsm, clk_mhz, xu_lanes, kernel
                          f") lanes/clk x {clk_mhz:.0f} MHz max SM clock"}
     if live_mhz:
         out["frac_at_live_clock"] = achieved / peak_at(live_mhz)
-    if op in ("max", "min") and kind == "gaussian" and E == 1:
-        # the log-domain scan: D sub + D fma (the distance, started at -log2|b|) + 1 compare
+    if op in ("max", "min") and E == 1:
+        # the key scan: the distance, one more add / multiply except for the Gaussian, the
+        # Laplace's sqrt, and one compare a pair
         f = clk_mhz * 1e6
-        own_peak = 1.0 / max(2 * D / (nsm * FP32_LANES_PER_SM * f), 1.0 / (nsm * ALU_LANES_PER_SM * f))
-        out["own_bound"] = {"ops_per_pair": {"fp32": 2 * D, "xu": {}, "cmp": 1}, "peak": own_peak,
-                            "frac": achieved / own_peak}
+        own = {"fp32": 2 * D + (0 if kind == "gaussian" else 1),
+               "xu": {"sqrt": 1} if kind == "laplace" else {}, "cmp": 1}
+        own_xu = sum(cnt / xu_lanes[name] for name, cnt in own["xu"].items())
+        own_peak = 1.0 / max(own["fp32"] / (nsm * FP32_LANES_PER_SM * f), own_xu / (nsm * f),
+                             1.0 / (nsm * ALU_LANES_PER_SM * f))
+        out["own_bound"] = {"ops_per_pair": own, "peak": own_peak, "frac": achieved / own_peak}
     if op == "knn" and D <= 16:
         # The K-min kernel at D <= 16 screens pairs with |y~|^2 - 2 x~.y~ (D FMAs) and computes the
         # direct distance only for passing groups; frac above is against the method's direct count.

@@ -31,6 +31,9 @@
 namespace kr {
 
 enum RadialKind { KT_GAUSS = 0, KT_LAPLACE = 1, KT_CAUCHY = 2, KT_IMQ = 3 };
+
+// +inf as a constant expression
+KR_HD constexpr float f_inf_c() { return __builtin_huge_valf(); }
 enum RadialRed { RR_SUM = 0, RR_MAX = 1 };
 
 __device__ __forceinline__ float sqrt_approx(float v) {
@@ -144,25 +147,54 @@ __device__ __forceinline__ typename Lanes<L>::T radial_k(const typename Lanes<L>
     return V::template kval<KT>(q);
 }
 
-// Gaussian Max / Min in the log domain: the key t = |x'-y'|^2 - log2|b| of a row against
-// the L points of a record whose value slot holds -log2|b| (the first chain starts there),
-// so that k b = sign(b) 2^-t.  Used by the scan and by the index recomputation alike.
-template <int DP, int L, int PS>
+template <int L>
+__device__ __forceinline__ typename Lanes<L>::T make_lanes_sqrt(typename Lanes<L>::T q) {
+    if constexpr (L == 2) return make_float2(sqrt_approx(q.x), sqrt_approx(q.y));
+    else return sqrt_approx(q);
+}
+
+// Max / Min with one signal column without forming k b: a key t of the pair that falls as
+// |k b| rises, from the point's staged value slot s (two points a record, f32x2):
+//   Gaussian  t = q - log2|b|         (s = -log2|b| starts the distance's chain),  |k b| = 2^-t
+//   Laplace   t = sqrt(q) - log2|b|   (s = -log2|b|),                              |k b| = 2^-t
+//   Cauchy    t = (1 + q) / |b|       (s = 1 / |b|; the chain starts at 1),        |k b| = 1 / t
+//   inverse multiquadric  t = (1 + q) / b^2  (s = 1 / b^2),                         |k b| = 1 / sqrt(t)
+// with q = |x'-y'|^2.  A point that cannot hold the extreme carries s = +-inf (t = +-inf).
+// Used by the scan and by the index recomputation alike.
+template <int KT>
+__device__ __forceinline__ float log_slot(float v) {  // s of a signal value v != 0 (its magnitude)
+    const float m = fabsf(v);
+    if (KT == KT_GAUSS || KT == KT_LAPLACE) return -log2f(m);
+    if (KT == KT_CAUCHY) return 1.0f / m;
+    return 1.0f / (m * m);
+}
+template <int KT>
+__device__ __forceinline__ float log_value(float t) {  // |k b| at the key t
+    if (KT == KT_GAUSS || KT == KT_LAPLACE) return exp2f(-t);
+    if (KT == KT_CAUCHY) return 1.0f / t;
+    return 1.0f / sqrtf(t);
+}
+template <int DP, int L, int PS, int KT>
 __device__ __forceinline__ typename Lanes<L>::T log_key(const typename Lanes<L>::T (&xr)[DP],
                                                         const typename Lanes<L>::T (&pv)[PS / L]) {
     typedef Lanes<L> V;
     typedef typename V::T T;
     constexpr int NC = dist_chains(DP);
+    // the first chain starts at s (Gaussian), at 1 (Cauchy, inverse multiquadric) or at 0
+    const T q0 = KT == KT_GAUSS ? pv[DP] : V::splat(radial_q0<KT>());
+    const bool start = KT != KT_LAPLACE;
     T qc[NC];
 #pragma unroll
     for (int d = 0; d < DP; ++d) {
         const T df = V::add(xr[d], pv[d]);
         const int c = d % NC;
-        qc[c] = d < NC ? (c == 0 ? V::fma(df, df, pv[DP]) : V::mul(df, df)) : V::fma(df, df, qc[c]);
+        qc[c] = d < NC ? ((c == 0 && start) ? V::fma(df, df, q0) : V::mul(df, df)) : V::fma(df, df, qc[c]);
     }
     T q = qc[0];
 #pragma unroll
     for (int c = 1; c < NC; ++c) q = V::add(q, qc[c]);
+    if (KT == KT_LAPLACE) return V::add(make_lanes_sqrt<L>(q), pv[DP]);
+    if (KT == KT_CAUCHY || KT == KT_IMQ) return V::mul(q, pv[DP]);
     return q;
 }
 
@@ -234,28 +266,34 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
             last[r][e] = -1;
         }
 
-    // Gaussian Max / Min, dense mode, E = 1: the log domain.  With v_j = vsign b_j, the signs
-    // of v over the block's column chunk fix where the extreme can come from, the same for all
-    // its rows: some v_j > 0: the largest k v is 2^-t at the smallest key t = |x'-y'|^2 -
-    // log2 v_j over those points (mode 1); all v_j < 0 (none zero): it is -2^-t at the largest
-    // key over them (mode 2); otherwise (zeros without positives, only NaN, none) the value
-    // scan below (mode 0).  The scan then needs no ex2 and no product per pair, and the order
-    // of the keys is that of the values up to the rounding of t.  A row that finds no finite
-    // key (infinite or NaN coordinates) sends its block back to the value scan.
-    constexpr bool kLogMax = KT == KT_GAUSS && RED == RR_MAX && EP == 1 && L == 2;
+    // Max / Min, dense mode, E = 1: the key scan (log_key).  With v_j = vsign b_j, the signs of
+    // v over the block's column chunk fix where the extreme can come from, the same for all its
+    // rows: some v_j > 0: the largest k v is |k v| at the smallest key over those points (mode
+    // 1); all v_j < 0 (none zero): it is -|k v| at the largest key over them (mode 2);
+    // otherwise (zeros without positives, only NaN, none) the value scan below (mode 0).  The
+    // scan then needs no ex2 / rcp / rsqrt and no product per pair (the Laplace keeps its
+    // sqrt), and the order of the keys is that of the values up to the rounding of t.  A row
+    // that finds no finite key (infinite or NaN coordinates) sends its block back to the value
+    // scan.
+    constexpr bool kLogMax = RED == RR_MAX && EP == 1 && L == 2;
     constexpr int LB = log_max_block();
     static_assert(!kLogMax || BN % (LB * UPT) == 0, "tile must be a multiple of the log-domain block");
     int mode = 0;
     if constexpr (kLogMax) {
         if (!ranged) {
+            // the range where the staged 1 / |v| (Cauchy) or 1 / v^2 (inverse multiquadric) is
+            // exact and finite; outside it the chunk keeps the value scan
+            constexpr float kLo = KT == KT_CAUCHY ? 0x1p-126f : KT == KT_IMQ ? 0x1p-62f : 0.f;
+            constexpr float kHi = KT == KT_CAUCHY ? 0x1p126f : KT == KT_IMQ ? 0x1p62f : f_inf_c();
             int f = 0;
             for (int64_t j = j_begin + t; j < j_end; j += kThreads) {
                 const float v = a.vsign * ldg_chk(a, a.b, j, a.N, KRD_B);
                 f |= v > 0.f ? 1 : v < 0.f ? 2 : v == 0.f ? 4 : 0;
+                if (v != 0.f && !(fabsf(v) >= kLo && fabsf(v) <= kHi)) f |= 8;
             }
             const bool any_pos = __syncthreads_or(f & 1), any_neg = __syncthreads_or(f & 2);
-            const bool any_zero = __syncthreads_or(f & 4);
-            mode = any_pos ? 1 : (any_neg && !any_zero) ? 2 : 0;
+            const bool any_zero = __syncthreads_or(f & 4), out_of_range = __syncthreads_or(f & 8);
+            mode = out_of_range ? 0 : any_pos ? 1 : (any_neg && !any_zero) ? 2 : 0;
         }
     }
     if constexpr (kLogMax) {
@@ -284,7 +322,7 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
                             radial_load<L, PS>(tile + ((jb + g * UPT) / L + u) * PS, pv);
 #pragma unroll
                             for (int r = 0; r < R; ++r) {
-                                const T k = log_key<DP, L, PS>(xr[r], pv);
+                                const T k = log_key<DP, L, PS, KT>(xr[r], pv);
                                 bm[r] = NEG ? fmax3(bm[r], k.x, k.y) : fmin3(bm[r], k.x, k.y);
                             }
                         }
@@ -302,7 +340,7 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
                     for (int u = 0; u < LB * UR; ++u) {
                         T pv[PS / L];
                         radial_load<L, PS>(tile + (jb / L + u) * PS, pv);
-                        const T k = log_key<DP, L, PS>(xr[r], pv);
+                        const T k = log_key<DP, L, PS, KT>(xr[r], pv);
 #pragma unroll
                         for (int l = 0; l < L; ++l) {
                             if (!found && V::lane(k, l) == tb[r]) {
@@ -324,7 +362,7 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
                         for (int d = 0; d < DP; ++d)
                             if (d < a.D) *radial_slot<L, PS>(tile, p, d) = -a.c * ldg_chk(a, a.y, (jt + p) * a.D + d, a.N * a.D, KRD_Y);
                         const float v = a.vsign * ldg_chk(a, a.b, jt + p, a.N, KRD_B);
-                        if (neg ? v < 0.f : v > 0.f) key = -log2f(fabsf(v));
+                        if (neg ? v < 0.f : v > 0.f) key = log_slot<KT>(v);
                     } else {
 #pragma unroll
                         for (int d = 0; d < DP; ++d)
@@ -347,7 +385,7 @@ __global__ void __launch_bounds__(kThreads) radial_kernel(const Args a_) {
                 for (int r = 0; r < R; ++r) bj[r][0] = -1;
             } else {
 #pragma unroll
-                for (int r = 0; r < R; ++r) hi[r][0] = neg ? -exp2f(-tb[r]) : exp2f(-tb[r]);
+                for (int r = 0; r < R; ++r) hi[r][0] = neg ? -log_value<KT>(tb[r]) : log_value<KT>(tb[r]);
             }
         }
     }

@@ -67,11 +67,11 @@ def test_roofline_peaks():
     assert bench.roofline("grad", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "other")["traffic"] is None
 
 
-def test_gaussian_max_reports_both_bounds():
-    """The Gaussian Max / Min with one column is measured against the method's count (k b
-    formed per pair: 2D + 1 FP32, one ex2, one compare) and, beside it, against the
-    log-domain scan's own count (2D FP32 + 1 compare); other kernels and wider signals carry
-    only the method's."""
+def test_max_reports_both_bounds():
+    """Max / Min with one column are measured against the method's count (k b formed per pair:
+    2D + 1 FP32, the kernel's XU operation, one compare) and, beside it, against the key
+    scan's own count (Gaussian 2D FP32 + 1 compare; Cauchy 2D + 1 FP32 + 1 compare, no XU;
+    Laplace 2D + 1 FP32, one sqrt, 1 compare); wider signals carry only the method's."""
     xu = {"ex2": 32.0, "rcp": 16.0, "rsqrt": 16.0, "sqrt": 16.0}
     clk = 152 * 2070e6
     m = bench.roofline("max", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "k")
@@ -81,5 +81,11 @@ def test_gaussian_max_reports_both_bounds():
     assert abs(m["own_bound"]["peak"] - clk * 128 / 6) < 1
     assert m["own_bound"]["frac"] < m["frac"]
     assert "own_bound" in bench.roofline("min", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "k")
-    assert "own_bound" not in bench.roofline("max", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "k", kind="cauchy")
+    c = bench.roofline("max", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "k", kind="cauchy")
+    assert c["ops_per_pair"]["xu"] == {"rcp": 1} and abs(c["peak"] - clk * 16) < 1   # rcp-bound
+    assert c["own_bound"]["ops_per_pair"] == {"fp32": 7, "xu": {}, "cmp": 1}
+    assert abs(c["own_bound"]["peak"] - clk * 128 / 7) < 1
+    lp = bench.roofline("max", 3, 1, 1e-3, 1e9, 152, 2070.0, xu, "k", kind="laplace")
+    assert lp["own_bound"]["ops_per_pair"] == {"fp32": 7, "xu": {"sqrt": 1}, "cmp": 1}
+    assert abs(lp["own_bound"]["peak"] - clk * 16) < 1   # sqrt-bound
     assert "own_bound" not in bench.roofline("max", 3, 4, 1e-3, 1e9, 152, 2070.0, xu, "k")

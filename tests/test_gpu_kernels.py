@@ -104,13 +104,16 @@ def test_maxmin_ties_lowest_index(orc):
                 assert np.array_equal(_np(idx), i_ref), (kernel, red, split)
 
 
-def test_gaussian_maxmin_log_domain_modes(orc):
-    """Gaussian Max / Min with one signal column scan the keys |x'-y'|^2 - log2|v| (v = b
-    for Max, -b for Min) in a mode fixed by the signs of v over a block's column chunk:
-    some positive (the smallest key over them), all negative (the largest key), or zeros
-    without positives (the value scan).  Each case against the oracle, unsplit and with
-    splits whose chunks take different modes; with rows of infinite or NaN coordinates
-    (their blocks go back to the value scan) and without."""
+@pytest.mark.parametrize("kernel", KINDS)
+def test_maxmin_key_scan_modes(orc, kernel):
+    """Max / Min with one signal column scan a key that falls as |k v| rises (v = b for Max,
+    -b for Min; Gaussian q - log2|v|, Laplace sqrt(q) - log2|v|, Cauchy (1 + q) / |v|,
+    inverse multiquadric (1 + q) / v^2) in a mode fixed by the signs of v over a block's
+    column chunk: some positive (the smallest key over them), all negative (the largest), or
+    zeros without positives (the value scan).  Each case against the oracle, unsplit and
+    with splits whose chunks take different modes; with rows of infinite or NaN coordinates
+    (their blocks go back to the value scan) and without; and signals spanning 1e-30 to 1e30,
+    outside the range where the Cauchy and inverse-multiquadric keys are exact (value scan)."""
     r = np.random.Generator(np.random.PCG64(77))
     M, N, D = 1500, 2600, 3
     x = r.standard_normal((M, D)).astype(np.float32)
@@ -126,15 +129,16 @@ def test_gaussian_maxmin_log_domain_modes(orc):
         "zeros and negatives": np.where(j % 7 == 0, 0.0, -pos).astype(np.float32),
         "positive then negative": np.where(j < N // 2, pos, -pos).astype(np.float32),
         "mixed": r.standard_normal((N, 1)).astype(np.float32),
+        "wide range": (pos * 10.0 ** r.integers(-30, 31, size=(N, 1))).astype(np.float32),
     }
     for xs, xname in ((x, "finite rows"), (x_bad, "inf and NaN rows")):
         for name, b in cases.items():
             for red in ("max", "min"):
-                v_ref, i_ref, s_ref = orc.kernel_maxmin(xs, y, b, 0.9, "gaussian", red)
+                v_ref, i_ref, s_ref = orc.kernel_maxmin(xs, y, b, 0.9, kernel, red)
                 for split in (0, 1, 2, 5):
-                    idx, val = kr.kernel_reduce_arg(*_dev(xs, y, b), 0.9, red, split=split)
-                    check_maxmin(_np(val), _np(idx), xs, y, b, 0.9, "gaussian", v_ref, i_ref, s_ref,
-                                 f"{xname}, {name}, {red}, split {split}")
+                    idx, val = kr.kernel_reduce_arg(*_dev(xs, y, b), 0.9, red, split=split, kernel=kernel)
+                    check_maxmin(_np(val), _np(idx), xs, y, b, 0.9, kernel, v_ref, i_ref, s_ref,
+                                 f"{kernel}: {xname}, {name}, {red}, split {split}")
 
 
 def test_maxmin_empty_and_degenerate(orc):
