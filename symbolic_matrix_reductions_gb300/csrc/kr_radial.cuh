@@ -21,7 +21,11 @@
 // passes are the points walked in increasing j, replacing the best on a strictly
 // larger value, so equal values keep the lowest index.  Min is Max of k (-b):
 // the block stages -b and the result is negated on output.  Padding points carry
-// b = NaN: k NaN is NaN, which neither wins a comparison nor survives fmaxf.
+// b = NaN: k NaN is NaN, which neither wins a comparison nor survives fmaxf.  With
+// one signal column (and packed lanes) the scan compares a key that falls as |k b|
+// rises instead of the values (log_key), in a mode each block picks from the signs of
+// its chunk's signal, and forms the value once a row; the value scan remains for the
+// other cases.
 #pragma once
 
 #include <type_traits>
