@@ -121,7 +121,10 @@ typedef enum {
                                  batch; ignored elsewhere.  At run
                                  time it stands down to the CUDA cores when max |x'|^2 +
                                  max |y'|^2 exceeds 16 (x' = x sqrt(log2 e)/sigma), where the
-                                 expansion's rounding would exceed the tolerance. */
+                                 expansion's rounding would exceed the tolerance.  The
+                                 K-min (32 <= D <= 62, K <= 32, no batch) screens its pairs
+                                 with the same expansion and stands down when max |x|^2 +
+                                 max |y|^2 exceeds 4096. */
 } kr_path;
 
 /*
@@ -264,6 +267,12 @@ int kernel_reduce_grad_b_ex(const float *x, const float *y, const float *g, floa
  *   idx [M x K] (int32): the K indices j with the smallest (|x_i - y_j|^2, j),
  *                        ascending; ties keep the lowest j; -1 past N.
  *   dist [M x K] (nullable): the matching fp32 squared distances, +inf past N.
+ * The reported distance is always the direct fp32 sum over d of (x_id - y_jd)^2.  On the
+ * tensor-core path (kr_path above) the expansion |x|^2 + |y|^2 - 2 x.y only screens: a
+ * point whose screened distance is above the row's current K-th plus a bound on the
+ * expansion's rounding cannot enter the list and is skipped; every other point gets
+ * the direct distance, so the result is the CUDA-core path's up to the order of ties
+ * within fp32 rounding of the distance.
  */
 int kernel_knn(const float *x, const float *y, int32_t *idx, float *dist,
                int64_t M, int64_t N, int D, int K, kr_stream_t stream);

@@ -436,8 +436,10 @@ def kernel_reduce_grad_b(x, y, g, sigma: float, out=None, split: int = 0, path: 
     return out
 
 
-def kernel_knn(x, y, K: int, idx=None, dist=None, want_dist: bool = True, split: int = 0):
-    """K smallest (|x_i-y_j|^2, j) per row, ascending, lowest index on ties.
+def kernel_knn(x, y, K: int, idx=None, dist=None, want_dist: bool = True, split: int = 0, path: int = 0):
+    """K smallest (|x_i-y_j|^2, j) per row, ascending, lowest index on ties.  ``path``:
+    KR_PATH_AUTO (default; the tensor-core screen at 32 <= D <= 62, K <= 32) or
+    KR_PATH_CUDA_CORES.
 
     Returns (idx int32 (M, K), dist float32 (M, K) or None); (B, M, K) for a batch."""
     torch = _torch()
@@ -455,7 +457,7 @@ def kernel_knn(x, y, K: int, idx=None, dist=None, want_dist: bool = True, split:
         dist = _mat(dist, M, "dist", K, B=B)
     _same_device(x, idx, dist)
     st = load_library().kernel_knn_ex(_ptr(x), _ptr(y), _ptr(idx), _ptr(dist), M, N, D, K, _stream(dev),
-                                      _options(split, batch=B))
+                                      _options(split, path, batch=B))
     _check(st, "kernel_knn")
     return idx, dist
 

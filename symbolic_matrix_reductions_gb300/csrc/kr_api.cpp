@@ -88,12 +88,14 @@ static int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 // Tensor-core plan: kTcRows rows per block (one TMEM lane each), tiles of kTcCols points
 // (the x-gradient: kTcGradCols), splits on tile boundaries, one block per SM.  Split
 // partials: M values (Sum, LSE) or M x D (the gradient) per split.
-static void plan_tc(int op, int64_t M, int64_t N, int D, int num_sms, int blocks_per_sm, int forced_split,
+static void plan_tc(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm, int forced_split,
                     kr_plan_t *p) {
     const int tile = op == OP_GRAD ? kTcGradCols : kTcCols;
-    const int64_t width = op == OP_GRAD ? D : 1;
+    // split partials per row: (hi, lo) of the Sum / LSE; D of them for the gradient; a list of
+    // KP (distance, index) for the K-min (the same bytes: 2 x 4 a slot)
+    const int64_t width = op == OP_GRAD ? D : op == OP_KNN ? pad_k(EK) : 1;
     p->d_pad = 64;
-    p->ek_pad = 1;
+    p->ek_pad = op == OP_KNN ? pad_k(EK) : 1;
     p->rows_per_thread = 1;
     p->threads = op == OP_GRAD ? kTcGradThreads : kTcThreads;
     p->tile_points = tile;
@@ -137,16 +139,20 @@ static void plan_tc(int op, int64_t M, int64_t N, int D, int num_sms, int blocks
     const int64_t operands = (round_up(std::max<int64_t>(M, 1), kTcRows) + n_pad) * 256 + n_pad * 4 +
                              round_up(n_pad / kTcCols * 4, 256);
     p->workspace_bytes = 256 + operands + (S > 1 ? 2 * (int64_t)S * M * width * (int64_t)sizeof(float) : 0) +
-                         (op == OP_GRAD ? round_up((int64_t)S * M, 256) : 0);  // the gradient's weak-row flags
+                         (op == OP_GRAD ? round_up((int64_t)S * M, 256) : 0) +  // the gradient's weak-row flags
+                         (op == OP_KNN ? round_up(4 * M, 256) : 0);              // the K-min's shared K-th words
 }
 
 static int64_t batch_of(const kr_options *opt) { return opt && opt->batch > 1 ? opt->batch : 1; }
 
 static bool tc_eligible(int op, int64_t M, int64_t N, int D, int EK, const kr_options *opt) {
     const int path = opt ? opt->path : 0, kind = opt ? opt->kernel : KR_KERNEL_GAUSSIAN;
-    if ((op != OP_SUM && op != OP_LSE && op != OP_GRAD) || kind != KR_KERNEL_GAUSSIAN || path == KR_PATH_CUDA_CORES ||
-        !tc_dims(D, EK))
+    if (path == KR_PATH_CUDA_CORES) return false;
+    if (op == OP_KNN) {  // the screen: the Sum's coordinate range, lists of up to 32
+        if (!(D >= 32 && D <= 62 && EK >= 1 && EK <= 32) || batch_of(opt) > 1) return false;
+    } else if ((op != OP_SUM && op != OP_LSE && op != OP_GRAD) || kind != KR_KERNEL_GAUSSIAN || !tc_dims(D, EK)) {
         return false;
+    }
     if (op == OP_LSE && D > kTcLseMaxD) return false;  // the weight takes one more operand slot
     if (batch_of(opt) > 1) return false;  // the tensor-core prepass and tiles serve one problem
     return (round_up(std::max<int64_t>(M, 1), kTcRows) + round_up(std::max<int64_t>(N, 1), kTcCols)) * 256 <=
@@ -472,12 +478,13 @@ static double kernel_prescale(int kind, float sigma) {
 }
 
 // ---- tensor-core Sum: operand prepass, tensor kernel, CUDA-core stand-in, combine -------
-// Workspace: [guard (2 x u32) + status | A_hi | A_lo | B_hi | B_lo | padded b | partials].  The
-// CUDA-core kernel is always launched after the tensor kernel with the same splits;
-// it returns at once unless the prepass found norms the expansion cannot serve.
+// Workspace: [guard (2 x u32) + status | A_hi | A_lo | B_hi | B_lo | padded b | LSE frames |
+// partials | the gradient's flags or the K-min's K-th words].  The CUDA-core kernel is
+// always launched after the tensor kernel with the same splits; it returns at once unless
+// the prepass found norms the expansion cannot serve.
 static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in, char *ws, cudaStream_t stream) {
-    const bool lse = op == OP_LSE, grad = op == OP_GRAD;
-    const int64_t width = grad ? a.D : 1;  // split partials per row
+    const bool lse = op == OP_LSE, grad = op == OP_GRAD, knn = op == OP_KNN;
+    const int64_t width = grad ? a.D : knn ? p.ek_pad : 1;  // split partials per row
     const int64_t m_pad = round_up(a.M, kTcRows), n_pad = round_up(std::max<int64_t>(a.N, 1), kTcCols);
     unsigned *guard = (unsigned *)ws;
     __half *a_hi = (__half *)(ws + 256);
@@ -487,19 +494,24 @@ static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in
     float *bpad = (float *)(b_lo + n_pad * 64);
     float *fpad = bpad + n_pad;
     float *part = (float *)((char *)fpad + round_up(n_pad / kTcCols * 4, 256));
-    // the x-gradient's flags (S x M bytes) follow the split partials
+    // the x-gradient's flags (S x M bytes), or the K-min's K-th words (M), follow the split partials
     uint8_t *flags = (uint8_t *)(part + (p.split > 1 ? 2 * (int64_t)p.split * a.M * width : 0));
+    unsigned *kth = knn ? (unsigned *)flags : nullptr;
     cudaError_t ce = cudaMemsetAsync(guard, 0, 256, stream);
+    // (the K-min's screen reads the operands' high halves only)
     if (ce == cudaSuccess)
-        ce = tc_launch_prep(a.x, a.M, m_pad, a.D, a.c, true, lse, a_hi, a_lo, guard, nullptr, nullptr, nullptr,
-                            stream);
+        ce = tc_launch_prep(a.x, a.M, m_pad, a.D, a.c, true, lse, a_hi, knn ? nullptr : a_lo, guard, nullptr, nullptr,
+                            nullptr, stream, false, kth);
     if (ce == cudaSuccess && grad) ce = tc_launch_bmax(a.b, a.N, guard, stream);
     if (ce == cudaSuccess)
-        ce = tc_launch_prep(a.y, a.N, n_pad, a.D, a.c, false, lse, b_hi, b_lo, guard + 1, a.b, lse ? nullptr : bpad,
-                            lse ? fpad : nullptr, stream, grad);
+        ce = tc_launch_prep(a.y, a.N, n_pad, a.D, a.c, false, lse, b_hi, knn ? nullptr : b_lo, guard + 1,
+                            knn ? nullptr : a.b, (lse || knn) ? nullptr : bpad, lse ? fpad : nullptr, stream, grad);
     if (p.split > 1) {
         a.ws0 = part;
-        a.ws1 = part + (int64_t)p.split * a.M * width;
+        if (knn)  // the lists' distances, then their indices (as the CUDA-core K-min lays them out)
+            a.wsi = (int32_t *)(part + (int64_t)p.split * a.M * width);
+        else
+            a.ws1 = part + (int64_t)p.split * a.M * width;
     }
     if (ce == cudaSuccess) {
         TcArgs t{};
@@ -534,15 +546,24 @@ static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in
         t.c = a.c;
         t.gscale = a.gscale;
         t.flags = flags;
+        t.y = a.y;
+        t.idx = a.idx;
+        t.wsi = a.wsi;
+        t.K = a.K;
+        t.KP = p.ek_pad;
+        t.kth = kth;
         const dim3 tgrid((unsigned)p.row_blocks, (unsigned)p.split);
-        ce = grad ? tc_launch_grad(t, tgrid, stream) : tc_launch_sum(t, tgrid, stream);
+        ce = grad ? tc_launch_grad(t, tgrid, stream) : knn ? tc_launch_knn(t, tgrid, stream) : tc_launch_sum(t, tgrid, stream);
     }
     if (ce == cudaSuccess) {  // the CUDA-core stand-in: returns at once unless the guard failed
         a.tc_guard = guard;
         a.tc_flags = grad ? flags : nullptr;  // (or, for the gradient, on the rows flagged weak)
         const int64_t bm = (int64_t)kThreads * in.rows;
         const dim3 grid((unsigned)((a.M + bm - 1) / bm), (unsigned)p.split);
-        ce = grad ? launch_grad(in, a, grid, stream) : lse ? launch_lse(in, a, grid, stream) : launch_sum(in, a, grid, stream);
+        ce = grad  ? launch_grad(in, a, grid, stream)
+             : lse ? launch_lse(in, a, grid, stream)
+             : knn ? launch_knn(in, a, grid, stream)
+                   : launch_sum(in, a, grid, stream);
     }
     if (ce == cudaSuccess && p.split > 1) ce = launch_combine(op, in, a, stream);
     return ce;
@@ -596,7 +617,7 @@ static int run(int op, Buf *bufs, int nbuf, Args a, int EK, float sigma, cudaStr
     // batched calls (small problems, where a prepass launch would cost more than it saves)
     if (tc || rt || B > 1) in.rec = false;
     if (tc) {
-        plan_tc(op, a.M, a.N, a.D, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, &p);
+        plan_tc(op, a.M, a.N, a.D, EK, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, &p);
     } else {
         plan(op, a.M, a.N, a.D, EK, num_sms, occ, opt ? opt->split : 0, B, kind, &p);
         if (rt) {  // one block per table entry and split; the tables lead the workspace
@@ -1027,7 +1048,7 @@ int kr_plan(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks
     const int st = validate(op, nullptr, 0, M, N, D, EK, 1.f, opt);
     if (st != KR_OK) return st;
     if (tc_eligible(op, M, N, D, EK, opt)) {
-        plan_tc(op, M, N, D, num_sms, blocks_per_sm, opt ? opt->split : 0, out);
+        plan_tc(op, M, N, D, EK, num_sms, blocks_per_sm, opt ? opt->split : 0, out);
         return KR_OK;
     }
     return plan(op, M, N, D, EK, num_sms, blocks_per_sm, opt ? opt->split : 0, batch_of(opt),
@@ -1046,7 +1067,7 @@ int kr_plan_device(int op, int64_t M, int64_t N, int D, int EK, const kr_options
     if (device_info(dev, op, kind, choose_instance(op, D, EK, kind), &num_sms, &occ) != 0)
         return cuda_fail(cudaGetLastError());
     if (tc_eligible(op, M, N, D, EK, opt) && tc_available()) {
-        plan_tc(op, M, N, D, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, out);
+        plan_tc(op, M, N, D, EK, num_sms, device_tc_occupancy(dev), opt ? opt->split : 0, out);
         return KR_OK;
     }
     return plan(op, M, N, D, EK, num_sms, occ, opt ? opt->split : 0, batch_of(opt), kind, out);

@@ -8,6 +8,11 @@
 
 namespace kr {
 
+// K-min on the tensor cores: the largest |x|^2 + |y|^2 its screen takes (fp16 operands stay in
+// range and the screen's margin, 2^-14 of the norms, stays below the distances that matter);
+// above it the CUDA-core kernel does the call.
+constexpr float kTcKnnNormLimit = 4096.f;
+
 enum Op { OP_SUM = 0, OP_LSE = 1, OP_GRAD = 2, OP_KNN = 3, OP_MAX = 4 };
 constexpr int kNumOps = 5;
 constexpr int kNumKernels = 4;  // radial kernel kinds (KR_KERNEL_*)

@@ -40,6 +40,12 @@ __device__ __forceinline__ float lg2_approx(float v) {
 
 __device__ __forceinline__ float f_inf() { return __int_as_float(0x7f800000); }
 
+// The tensor-core K-min ran this call (its operand norms, written by its prepass, are within
+// its limit); a finite sum is required, so NaN inputs take the CUDA-core kernel.
+__device__ __forceinline__ bool tc_knn_ran(const unsigned *guard) {
+    return __uint_as_float(guard[0]) + __uint_as_float(guard[1]) <= kTcKnnNormLimit;
+}
+
 // max(a, b, c) and min(a, b, c) in one instruction each (the three-input max.f32 /
 // min.f32 of sm_100 and later); a NaN input is passed over as fmaxf / fminf pass it over.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

@@ -498,6 +498,7 @@ __global__ void __launch_bounds__(kThreads) grad2_kernel(const Args a_) {
 template <int DP, int KP, int R, int BN>
 __global__ void __launch_bounds__(kThreads) knn2_kernel(const Args a_) {
     const Args a = batch_view(a_);
+    if (a.tc_guard && tc_knn_ran(a.tc_guard)) return;  // the tensor-core K-min did this call
     constexpr int PS2 = pair_stride(DP, 0);
     constexpr int UP = unroll_pairs(DP);
     constexpr int UPT = 2 * UP;

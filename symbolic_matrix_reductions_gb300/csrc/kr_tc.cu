@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(256) tc_bmax_kernel(const float *b, int64_t n,
 __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t rows, int64_t rows_pad, int D,
                                                       float c, int is_x, int lse, __half *hi, __half *lo,
                                                       unsigned *guard, const float *b, float *bpad, float *fpad,
-                                                      const unsigned *bmax) {
+                                                      const unsigned *bmax, unsigned *kth) {
     __shared__ float wmax[8];
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= rows_pad) return;  // with fpad, rows_pad is a multiple of 256: whole blocks leave together
@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t 
             n = fmaf(s, s, n);
         }
         atomicMax(guard, __float_as_uint(n));
+        if (kth) kth[r] = 0x7f800000u;  // K-min: no K-th distance published for the row yet
     }
     if (bpad && !fpad && bmax) {
         const float m = __uint_as_float(*bmax);
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t 
     const float scale = is_x ? 2.f * c : c;
     const float v_d = is_x ? -n : 1.f, v_d1 = is_x ? -1.f : n;
     uint4 *ph = reinterpret_cast<uint4 *>(hi + r * 64);
-    uint4 *pl = reinterpret_cast<uint4 *>(lo + r * 64);
+    uint4 *pl = lo ? reinterpret_cast<uint4 *>(lo + r * 64) : nullptr;  // null: the high halves only
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         __align__(16) __half h[8];
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t 
             l[e] = __float2half_rn(v - __half2float(h[e]));
         }
         ph[q] = *reinterpret_cast<const uint4 *>(h);
-        pl[q] = *reinterpret_cast<const uint4 *>(l);
+        if (lo) pl[q] = *reinterpret_cast<const uint4 *>(l);
     }
 }
 
@@ -625,6 +626,321 @@ __device__ __forceinline__ void tmem_ld32x32b_x16(uint32_t taddr, uint32_t (&r)[
 __device__ __forceinline__ void tmem_st32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr), "r"(r[0]),"r"(r[1]),"r"(r[2]),"r"(r[3]),"r"(r[4]),"r"(r[5]),"r"(r[6]),"r"(r[7]),"r"(r[8]),"r"(r[9]),"r"(r[10]),"r"(r[11]),"r"(r[12]),"r"(r[13]),"r"(r[14]),"r"(r[15])
                  : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// K-min on the tensor cores (tc_knn_kernel), 32 <= D <= 62: a screen.  One product of the
+// operands' high fp16 halves, A_hi . B_hi^T with A = [2x, -|x|^2, -1] and B = [y, 1, |y|^2]
+// (prescale 1), gives S_ij = -|x_i - y_j|^2 up to
+//   2^-8 (|x_i|^2 + max_j |y_j|^2) + 2^-24 (D + 2).
+// The relative part: every operand is its fp16 half within 2^-11 of itself, so a product
+// within 2^-10 (and a little) of itself, and the products' magnitudes sum to at most
+// 2 (|x|^2 + |y|^2); the fp32 accumulation of 64 of them adds 2^-18 of that.  The absolute
+// part: an operand below fp16's normal range (under 2^-14; the tensor cores keep fp16
+// subnormals) is rounded to a multiple of 2^-24, within 2^-25, and meets the other
+// operand's entries (sum over d of |y_d| + 2 |x_d| + 2 <= 1.5 D + |x|^2 + |y|^2 + 2).
+// A point passes when -S_ij is at most T + margin, where T is the smallest K-th distance
+// found so far among all lists of row i: this list's own K-th, or one another list (the
+// other half of the tile's columns, another split) published in the per-row word kth[i].
+// The final K-th distance of the row is at most T, so no point of the row's final K fails
+// the screen.  Passing points get the direct fp32 distance (sum over d of (x_d - y_d)^2,
+// in order) and enter the row's sorted list when strictly below its K-th, in increasing j,
+// so equal distances keep the lower index; the lists are the CUDA-core kernel's up to the
+// rounding of the direct distance.  A list publishes its K-th (atomicMin on the word, as
+// float bits: non-negative floats order like unsigned integers) after a tile where it fell,
+// and reads the word once a tile: every list of a row whose split starts after another
+// split finished is screened by that split's K-th from its first tile on.  Evaluation warp
+// w owns rows 32 (w mod 4).. and the tile's columns 128 h.. (h = (w - 2) / 4): two lists a
+// row, merged at the end through shared memory.  A chunk of 64 columns holding no pass
+// costs one three-input max a column pair.  The B operand is only the high halves: a
+// stage is 32 KB and six of them are in flight.
+// ---------------------------------------------------------------------------
+constexpr int kKStages = 6;
+constexpr int kKChunk = 64;  // columns a TMEM load and a screen test
+static_assert(kATileBytes + kKStages * kBTileBytes + 1024 <= kSmemBytes, "K-min stages within the Sum's shared memory");
+static_assert(kEvalCols % kKChunk == 0, "whole chunks");
+
+__device__ __forceinline__ bool knn_norms_ok(const unsigned *guard) {
+    return __uint_as_float(guard[0]) + __uint_as_float(guard[1]) <= kTcKnnNormLimit;
+}
+
+// Inserts (q, j) into a list sorted by (d, j) when it ranks above its last entry (unfilled
+// slots are (+inf, -1)).
+template <int KP>
+__device__ __forceinline__ void knn_insert_dj(float (&dk)[KP], int (&ik)[KP], float q, int j) {
+    // (q, j) ranks before (d, i): a smaller distance, or an equal one with a lower index; an
+    // unfilled slot (+inf, -1) ranks after every real entry
+    auto before = [](float q, int j, float d, int i) { return q < d || (q == d && j >= 0 && (i < 0 || j < i)); };
+    // slot k takes the old slot k-1 when the new entry ranks before it, the new entry when it
+    // lands exactly at k, and keeps its value otherwise (as knn_insert, with the index tie-break)
+#pragma unroll
+    for (int k = KP - 1; k > 0; --k) {
+        const float da = dk[k - 1], db = dk[k];
+        const int ia = ik[k - 1], ib = ik[k];
+        const bool above = before(q, j, da, ia), here = before(q, j, db, ib);
+        dk[k] = above ? da : (here ? q : db);
+        ik[k] = above ? ia : (here ? j : ib);
+    }
+    if (before(q, j, dk[0], ik[0])) {
+        dk[0] = q;
+        ik[0] = j;
+    }
+}
+
+// dk[K - 1] with constant indices only, 1 <= K <= KP.  Each slot passes through an empty asm
+// so that the selects are not folded back into an indexed load, which would move the list
+// from registers to local memory.
+template <int KP>
+__device__ __forceinline__ float knn_kth(const float (&dk)[KP], int K) {
+    float v = dk[0];
+#pragma unroll
+    for (int k = 1; k < KP; ++k) {
+        float c = dk[k];
+        asm("" : "+f"(c));
+        v = k == K - 1 ? c : v;
+    }
+    return v;
+}
+
+// Direct fp32 squared distance between row i of x and point j of y (D coordinates each),
+// summed in coordinate order; eight loads at a time are in flight.
+__device__ __forceinline__ float tc_knn_dist(const float *xi, const float *yj, int D) {
+    float q = 0.f;
+    int d = 0;
+    for (; d + 8 <= D; d += 8) {
+        float a[8], b[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            a[e] = __ldg(xi + d + e);
+            b[e] = __ldg(yj + d + e);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q = fmaf(a[e] - b[e], a[e] - b[e], q);
+    }
+    for (; d < D; ++d) {
+        const float df = __ldg(xi + d) - __ldg(yj + d);
+        q = fmaf(df, df, q);
+    }
+    return q;
+}
+
+// The columns c of r whose screened distance -r[c] is at most thr, as two 32-bit masks.
+__device__ __forceinline__ void knn_pass_mask(const uint32_t (&r)[kKChunk], float thr, uint32_t &m0, uint32_t &m1) {
+    m0 = 0u;
+    m1 = 0u;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        m0 |= !(-__uint_as_float(r[c]) > thr) ? (1u << c) : 0u;
+        m1 |= !(-__uint_as_float(r[32 + c]) > thr) ? (1u << c) : 0u;
+    }
+}
+
+template <int KP>
+__global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    // barriers: a_full, full[kKStages], empty[kKStages], acc_full[2], acc_empty[2], drain
+    __shared__ __align__(8) uint64_t bars[1 + 2 * kKStages + 4 + 1];
+    if (!knn_norms_ok(p.guard)) return;  // the CUDA-core kernel does this call's work
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t s_a = smem_addr(smem), s_stage0 = s_a + kATileBytes;
+    const uint32_t b_a_full = smem_addr(&bars[0]);
+    const uint32_t b_full0 = b_a_full + 8, b_empty0 = b_full0 + 8 * kKStages;
+    const uint32_t b_accf0 = b_empty0 + 8 * kKStages, b_acce0 = b_accf0 + 16, b_drain = b_acce0 + 16;
+    volatile int *abort = &abort_flag;
+
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    const int64_t row0 = (int64_t)blockIdx.x * kRows;
+    const int64_t j_begin = (int64_t)blockIdx.y * p.chunk;
+    const int64_t j_end = min(p.N, j_begin + p.chunk);
+    const int T = j_end > j_begin ? (int)((j_end - j_begin + kCols - 1) / kCols) : 0;
+
+    if (w == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (t == 0) {
+        abort_flag = 0;
+        mbar_init(b_a_full, 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(b_full0 + 8 * s, 1);
+            mbar_init(b_empty0 + 8 * s, 1);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(b_accf0 + 8 * k, 1);
+            mbar_init(b_acce0 + 8 * k, kEvalWarps);
+        }
+        mbar_init(b_drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const uint32_t tmem = tmem_slot;
+
+    float dk[KP];
+    int ik[KP];
+#pragma unroll
+    for (int k = 0; k < KP; ++k) {
+        dk[k] = __int_as_float(0x7f800000);
+        ik[k] = -1;
+    }
+    if (w == 0) {
+        // ---------------- TMA producer: the high halves only ----------------
+        if (lane == 0 && T > 0) {
+            mbar_expect_tx(b_a_full, kATileBytes);
+            tma_2d(s_a, &p.tm_a_hi, 0, (int)row0, b_a_full);
+            int issued = 0;
+            for (int i = 0; i < T; ++i) {
+                const int s = i % kKStages;
+                if (i >= kKStages && !mbar_wait(b_empty0 + 8 * s, ((i / kKStages) - 1) & 1, abort, p.wait_ns)) break;
+                const int j0 = (int)(j_begin + (int64_t)i * kCols);
+                const uint32_t full = b_full0 + 8 * s;
+                if (p.starve) continue;  // test hook: no B tile ever arrives, so the MMA issuer's wait runs out
+                mbar_expect_tx(full, kBTileBytes);
+                tma_2d(s_stage0 + s * kBTileBytes, &p.tm_b_hi, 0, j0, full);
+                issued = i + 1;
+            }
+            if (*abort) {
+                mbar_drain(b_a_full, 0, p.wait_ns);
+                for (int i = issued > kKStages ? issued - kKStages : 0; i < issued; ++i)
+                    mbar_drain(b_full0 + 8 * (i % kKStages), (i / kKStages) & 1, p.wait_ns);
+            }
+        }
+    } else if (w == 1) {
+        // ---------------- MMA issuer: S = A_hi . B_hi^T, four K steps of 16 ----------------
+        if (lane == 0 && T > 0 && mbar_wait(b_a_full, 0, abort, p.wait_ns)) {
+            bool issued = false;
+            for (int i = 0; i < T; ++i) {
+                const int s = i % kKStages, k = i & 1;
+                if (!mbar_wait(b_full0 + 8 * s, (i / kKStages) & 1, abort, p.wait_ns)) break;
+                if (i >= 2 && !mbar_wait(b_acce0 + 8 * k, ((i >> 1) - 1) & 1, abort, p.wait_ns)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;");
+                const uint32_t acc = tmem + (uint32_t)(k * kCols);
+                const uint32_t bh = s_stage0 + s * kBTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) mma_f16(acc, desc_sw128(s_a + 32 * kk), desc_sw128(bh + 32 * kk), kk > 0);
+                commit(b_empty0 + 8 * s);
+                commit(b_accf0 + 8 * k);
+                issued = true;
+            }
+            if (*abort && issued) {
+                commit(b_drain);
+                mbar_drain(b_drain, 0, p.wait_ns);
+            }
+        }
+    } else {
+        // ---------------- evaluation warps 2..9 ----------------
+        const int quarter = w & 3, half = (w - 2) >> 2, c0 = kEvalCols * half;
+        const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
+        const int64_t i = row0 + 32 * quarter + lane;
+        const bool live = i < p.M;
+        const float *xi = p.x + (live ? i : 0) * p.D;
+        unsigned *const kw = p.kth + (live ? i : 0);  // the row's shared K-th word
+        // this row's |x|^2 (fp32) and the screen's margin
+        float nx = 0.f;
+        for (int d = 0; d < p.D; ++d) nx = fmaf(__ldg(xi + d), __ldg(xi + d), nx);
+        const float margin = 0x1p-8f * (nx + __uint_as_float(p.guard[1])) + 0x1p-24f * (float)(p.D + 2);
+        const float inf = __int_as_float(0x7f800000);
+        float kth = inf;  // this list's K-th distance
+        float pub = inf;  // the K-th it last published
+        float thr = inf;  // -S must be at most this to pass
+        for (int it = 0; it < T; ++it) {
+            const int k = it & 1;
+            // the row's smallest published K-th so far (read before the wait: it is in flight meanwhile)
+            const float gth = live ? __uint_as_float(__ldcg(kw)) : inf;
+            if (!mbar_wait(b_accf0 + 8 * k, (it >> 1) & 1, abort, p.wait_ns)) break;
+            asm volatile("tcgen05.fence::after_thread_sync;");
+            const int64_t jt = j_begin + (int64_t)it * kCols + c0;
+#pragma unroll 1
+            for (int ch = 0; ch < kEvalCols / kKChunk; ++ch) {
+                uint32_t r[kKChunk];
+                tmem_ld32x32b_x64(tmem + lanes + (uint32_t)(k * kCols + c0 + kKChunk * ch), r);
+                asm volatile("tcgen05.wait::ld.sync.aligned;");
+                // the chunk's largest S (nearest point): one test for 64 columns
+                float mx = __uint_as_float(r[0]);
+#pragma unroll
+                for (int c = 1; c < kKChunk - 1; c += 2) mx = fmax3(mx, __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+                mx = fmaxf(mx, __uint_as_float(r[kKChunk - 1]));
+                if (live && !(-mx > thr)) {
+                    // the passing columns, walked in increasing j; after an insertion the
+                    // threshold falls and the columns still to come are screened again
+                    uint32_t m0, m1;
+                    knn_pass_mask(r, thr, m0, m1);
+                    while (m0 | m1) {
+                        const int c = m0 ? __ffs(m0) - 1 : 32 + __ffs(m1) - 1;
+                        if (m0) m0 &= m0 - 1; else m1 &= m1 - 1;
+                        const int64_t j = jt + kKChunk * ch + c;
+                        if (j >= j_end) break;  // the rest of the chunk is past the split too
+                        const float q = tc_knn_dist(xi, p.y + j * p.D, p.D);
+                        if (q < kth) {
+                            knn_insert<KP>(dk, ik, q, (int)j);
+                            kth = knn_kth<KP>(dk, p.K);
+                            thr = fminf(kth, gth) + margin;
+                            uint32_t n0, n1;
+                            knn_pass_mask(r, thr, n0, n1);
+                            m0 &= n0;
+                            m1 &= n1;
+                        }
+                    }
+                }
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_acce0 + 8 * k);  // the MMAs of tile it+2 may overwrite it
+            if (kth < pub) {  // publish the list's new K-th to the row's other lists
+                atomicMin(kw, __float_as_uint(kth));
+                pub = kth;
+            }
+            thr = fminf(kth, gth) + margin;
+        }
+    }
+
+    __syncthreads();
+    const bool ok = !*abort;
+    if (!ok && t == 0) atomicOr(&g_tc_status, 1u);
+    // the second half's lists to the first through the idle operand tiles (128 rows x KP (d, j))
+    float *xd = reinterpret_cast<float *>(smem);
+    int *xj = reinterpret_cast<int *>(smem) + kRows * KP;
+    const int rl = 32 * (w & 3) + lane;
+    if (w >= 6) {
+#pragma unroll
+        for (int k = 0; k < KP; ++k) {
+            xd[rl * KP + k] = dk[k];
+            xj[rl * KP + k] = ik[k];
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    if (w == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    if (w >= 2 && w < 6) {
+        const int64_t i = row0 + rl;
+        if (i < p.M) {
+            // merge: the second list's entries into this one by (d, j), so the first KP of the
+            // union in that order (the two halves' indices interleave tile by tile)
+#pragma unroll 1
+            for (int k = 0; k < KP; ++k) knn_insert_dj<KP>(dk, ik, xd[rl * KP + k], xj[rl * KP + k]);
+            const float nan = __int_as_float(0x7fc00000);
+            if (p.S == 1) {
+#pragma unroll
+                for (int k = 0; k < KP; ++k) {
+                    if (k >= p.K) continue;
+                    p.idx[i * p.K + k] = ok ? ik[k] : -1;
+                    if (p.out) p.out[i * p.K + k] = ok ? dk[k] : nan;
+                }
+            } else {
+                const int64_t o = ((int64_t)blockIdx.y * p.M + i) * KP;
+#pragma unroll
+                for (int k = 0; k < KP; ++k) {
+                    p.ws0[o + k] = ok ? dk[k] : nan;
+                    p.wsi[o + k] = ok ? ik[k] : -1;
+                }
+            }
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1043,6 +1359,9 @@ cudaError_t tc_set_attributes() {
         e = cudaFuncSetAttribute(tc_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tc_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemBytes);
+    for (const void *f : {(const void *)tc_knn_kernel<1>, (const void *)tc_knn_kernel<4>, (const void *)tc_knn_kernel<10>,
+                          (const void *)tc_knn_kernel<16>, (const void *)tc_knn_kernel<32>})
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return e;
 }
@@ -1055,14 +1374,14 @@ cudaError_t tc_launch_bmax(const float *b, int64_t n, unsigned *guard, cudaStrea
 
 cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x, bool lse,
                            __half *hi, __half *lo, unsigned *guard, const float *b, float *bpad, float *fpad,
-                           cudaStream_t s, bool natural_b) {
+                           cudaStream_t s, bool natural_b, unsigned *kth) {
     // LSE frames: a prep block of 256 threads is one whole tile of kTcCols = 256 points
     if (fpad && rows_pad % 256) return cudaErrorInvalidValue;
     if (lse && (D + 2 >= 64 || (!is_x && !fpad))) return cudaErrorInvalidValue;
     const unsigned blocks = (unsigned)((rows_pad + 255) / 256);
     // the y side's guard slot is guard[1] of the call's guard words; the largest |b| is guard[2]
     tc_prep_kernel<<<blocks, 256, 0, s>>>(src, rows, rows_pad, D, c, is_x ? 1 : 0, lse ? 1 : 0, hi, lo, guard, b,
-                                          bpad, fpad, natural_b ? guard + 1 : nullptr);
+                                          bpad, fpad, natural_b ? guard + 1 : nullptr, kth);
     return cudaGetLastError();
 }
 
@@ -1120,6 +1439,50 @@ cudaError_t tc_launch_grad(const TcArgs &a, dim3 grid, cudaStream_t s) {
     cudaError_t e = tc_set_attributes();
     if (e != cudaSuccess) return e;
     tc_grad_kernel<<<grid, kGThreads, kGSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_launch_knn(const TcArgs &a, dim3 grid, cudaStream_t s) {
+    TcParams p;
+    if (a.m_pad % kRows || a.n_pad % kCols || a.chunk % kCols || a.D < 32 || a.D > 62 || a.K < 1 || a.K > a.KP ||
+        !a.kth)
+        return cudaErrorInvalidValue;
+    // the screen reads the high halves only
+    if (!make_map(&p.tm_a_hi, a.a_hi, a.m_pad, kRows) || !make_map(&p.tm_b_hi, a.b_hi, a.n_pad, kCols))
+        return cudaErrorInvalidValue;
+    p.bpad = nullptr;
+    p.fpad = nullptr;
+    p.out = a.out;  // the distances (or null)
+    p.ws0 = a.ws0;
+    p.ws1 = nullptr;
+    p.guard = a.guard;
+    p.wait_ns = a.wait_ns;
+    p.starve = a.starve ? 1 : 0;
+    p.M = a.M;
+    p.N = a.N;
+    p.chunk = a.chunk;
+    p.S = a.S;
+    p.x = a.x;
+    p.g = nullptr;
+    p.D = a.D;
+    p.c = 1.f;
+    p.gscale = 0.f;
+    p.flags = nullptr;
+    p.y = a.y;
+    p.idx = a.idx;
+    p.wsi = a.wsi;
+    p.K = a.K;
+    p.kth = a.kth;
+    cudaError_t e = tc_set_attributes();
+    if (e != cudaSuccess) return e;
+    switch (a.KP) {
+        case 1: tc_knn_kernel<1><<<grid, kThreadsTc, kSmemBytes, s>>>(p); break;
+        case 4: tc_knn_kernel<4><<<grid, kThreadsTc, kSmemBytes, s>>>(p); break;
+        case 10: tc_knn_kernel<10><<<grid, kThreadsTc, kSmemBytes, s>>>(p); break;
+        case 16: tc_knn_kernel<16><<<grid, kThreadsTc, kSmemBytes, s>>>(p); break;
+        case 32: tc_knn_kernel<32><<<grid, kThreadsTc, kSmemBytes, s>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

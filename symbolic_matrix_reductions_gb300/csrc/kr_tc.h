@@ -36,6 +36,14 @@ struct TcArgs {
     int D;
     float c, gscale;
     uint8_t *flags;  // x-gradient: S x M, 1 where the CUDA-core kernel must redo (split, row)
+    // K-min (tc_launch_knn): y (N x D fp32) for the direct distances, K, the index output
+    // (M x K; out: the distances, or null) and, with S > 1, the index partials (ws0: distances),
+    // S x M x KP each; kth: M words, the smallest K-th distance any list of the row has
+    // published (float bits; the x prepass sets them to +inf)
+    const float *y;
+    int32_t *idx, *wsi;
+    int K, KP;
+    unsigned *kth;
 };
 
 // Kernel parameters: TMA descriptors of the four operand arrays plus the rest.
@@ -48,10 +56,14 @@ struct TcParams {
     int starve;
     int64_t M, N, chunk;
     int S;
-    const float *x, *g;  // x-gradient only
+    const float *x, *g;  // x-gradient only (x: and K-min)
     int D;
     float c, gscale;
     uint8_t *flags;
+    const float *y;  // K-min only
+    int32_t *idx, *wsi;
+    int K;
+    unsigned *kth;
 };
 
 int tc_smem_bytes();
@@ -61,9 +73,10 @@ bool tc_available();  // the driver offers cuTensorMapEncodeTiled
 // log-weight relative to its tile's frame, which fpad receives; b holds the log-weights).
 // Otherwise bpad receives b padded with zeros.
 // natural_b: bpad in point order (the x-gradient) rather than the Sum's evaluation order.
+// lo null: only the high halves are written.  kth non-null: kth[r] = +inf bits for r < rows.
 cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x, bool lse,
                            __half *hi, __half *lo, unsigned *guard, const float *b, float *bpad, float *fpad,
-                           cudaStream_t s, bool natural_b = false);
+                           cudaStream_t s, bool natural_b = false, unsigned *kth = nullptr);
 // x-gradient: guard[2] receives the largest |b| (float bits), from which the prepass of the
 // y side scales bpad by a power of two into [-1, 1] (run before that prepass).
 cudaError_t tc_launch_bmax(const float *b, int64_t n, unsigned *guard, cudaStream_t s);
@@ -73,6 +86,9 @@ cudaError_t tc_launch_sum(const TcArgs &a, dim3 grid, cudaStream_t s);
 // The x-gradient on the tensor cores (32 <= D <= 62, E = 1): grid (ceil(M / 128), S).
 cudaError_t tc_launch_grad(const TcArgs &a, dim3 grid, cudaStream_t s);
 int tc_grad_occupancy();
+// K-min on the tensor cores (32 <= D <= 62, K <= 32): grid (ceil(M / 128), S); a screen by the
+// tensor product, direct fp32 distances for the points that pass.
+cudaError_t tc_launch_knn(const TcArgs &a, dim3 grid, cudaStream_t s);
 // Reads (and optionally clears) the sticky device status of the tensor-core kernels on the
 // current device: bit 0 = a bounded wait gave up.  Synchronous.
 cudaError_t tc_read_status(bool clear, unsigned *status);

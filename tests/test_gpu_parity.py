@@ -500,3 +500,74 @@ def test_tensor_and_cuda_core_paths_agree():
     L_cc = _np(kr.kernel_reduce(xt, yt, bt, 1.0, "lse", path=kr.KR_PATH_CUDA_CORES))
     assert (np.abs(L_tc - L_cc) <= 2e-4).all()
     assert np.array_equal(L_tc, _np(kr.kernel_reduce(xt, yt, bt, 1.0, "lse", path=kr.KR_PATH_TENSOR_CORES)))
+
+
+TC_KNN_CASES = [
+    (1, 1, 32, 1, 0), (127, 300, 50, 10, 0), (300, 3000, 50, 10, 3), (513, 2000, 62, 32, 0),
+    (256, 4096, 32, 4, 5), (1000, 257, 40, 16, 0),
+    (130, 20001, 50, 10, 1),   # one split: 79 tiles a block
+]
+
+
+@pytest.mark.parametrize("M,N,D,K,split", TC_KNN_CASES)
+def test_tensor_core_knn(orc, M, N, D, K, split):
+    """K-min at 32 <= D <= 62 on the tensor cores: the product screens the points, passing
+    ones get the direct fp32 distance; against the oracle (indices exact where separated),
+    ragged row blocks and tiles, forced splits, K from 1 to 32."""
+    r = _rng(M + 7 * N + D + K)
+    x = (r.standard_normal((M, D)) / np.sqrt(D)).astype(np.float32)
+    y = (r.standard_normal((N, D)) / np.sqrt(D)).astype(np.float32)
+    assert kr.plan_device(kr.OP_KNN, M, N, D, K).path == kr.KR_PATH_TENSOR_CORES
+    idx, dist = kr.kernel_knn(*_dev(x, y), K, split=split)
+    i_ref, d_ref, n_ref = orc.knn(x, y, K)
+    check_knn(_np(idx), _np(dist), x, y, i_ref, d_ref, n_ref, f"tc knn {M}x{N} D{D} K{K} S{split}")
+
+
+def test_tensor_core_knn_ties_guard_and_agreement(orc):
+    """Duplicated points (equal distances: the lowest index wins), clouds whose norms exceed
+    the screen's limit (the CUDA-core kernel answers), and agreement with the CUDA-core K-min:
+    the same indices wherever the distances are separated, distances within their rounding."""
+    r = _rng(2024)
+    x = (r.standard_normal((400, 50)) / 7).astype(np.float32)
+    base = (r.standard_normal((60, 50)) / 7).astype(np.float32)
+    y = base[r.integers(0, 60, size=3000)]
+    for split in (0, 1, 4):
+        idx, dist = kr.kernel_knn(*_dev(x, y), 10, split=split)
+        i_ref, d_ref, n_ref = orc.knn(x, y, 10)
+        check_knn(_np(idx), _np(dist), x, y, i_ref, d_ref, n_ref, f"tc knn ties S{split}")
+    # norms far above the limit: |x|^2 + |y|^2 ~ 2 x 50 x 100^2
+    xb, yb = (100.0 + r.standard_normal((300, 50))).astype(np.float32), (100.0 + r.standard_normal((2000, 50))).astype(np.float32)
+    idx, dist = kr.kernel_knn(*_dev(xb, yb), 8)
+    i_ref, d_ref, n_ref = orc.knn(xb, yb, 8)
+    check_knn(_np(idx), _np(dist), xb, yb, i_ref, d_ref, n_ref, "tc knn guard")
+    # tensor vs CUDA cores on the same clouds
+    xc = (r.standard_normal((700, 62)) / 8).astype(np.float32)
+    yc = (r.standard_normal((5000, 62)) / 8).astype(np.float32)
+    it, dt = (_np(v) for v in kr.kernel_knn(*_dev(xc, yc), 16))
+    ic, dc = (_np(v) for v in kr.kernel_knn(*_dev(xc, yc), 16, path=kr.KR_PATH_CUDA_CORES))
+    i_ref, d_ref, n_ref = orc.knn(xc, yc, 16)
+    check_knn(it, dt, xc, yc, i_ref, d_ref, n_ref, "tc knn vs oracle")
+    check_knn(ic, dc, xc, yc, i_ref, d_ref, n_ref, "cuda knn vs oracle")
+    assert np.allclose(dt, dc, rtol=1e-5, atol=0)
+
+
+@pytest.mark.parametrize("scale", [1e-5, 1e-3, 5.5, 0.0])
+def test_tensor_core_knn_scales(orc, scale):
+    """The screen's margin at the ends of its range: clouds so small that their fp16 operands
+    are subnormal (the margin's absolute part), clouds whose norms come near the limit of 4096
+    (max |x|^2 + max |y|^2 about 3700), and (scale 0) coordinates of random sign spread
+    log-uniformly over 1e-7 .. 1, every magnitude in between at once."""
+    r = _rng(int(1e6 * scale) + 11)
+    M, N, D, K = 300, 3000, 50, 8
+    if scale > 0:
+        x = (scale * r.standard_normal((M, D)) / 1.2).astype(np.float32)
+        y = (scale * r.standard_normal((N, D)) / 1.2).astype(np.float32)
+    else:
+        def wide(n):
+            return (np.sign(r.standard_normal((n, D))) * 10.0 ** r.uniform(-7, 0, (n, D))).astype(np.float32)
+        x, y = wide(M), wide(N)
+    assert kr.plan_device(kr.OP_KNN, M, N, D, K).path == kr.KR_PATH_TENSOR_CORES
+    for split in (0, 3):
+        idx, dist = kr.kernel_knn(*_dev(x, y), K, split=split)
+        i_ref, d_ref, n_ref = orc.knn(x, y, K)
+        check_knn(_np(idx), _np(dist), x, y, i_ref, d_ref, n_ref, f"tc knn scale {scale} S{split}")
