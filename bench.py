@@ -96,7 +96,7 @@ TRAFFIC = {
     # profiles/grad2_kernel_d3_gauss_d3_unit.md: dram__bytes_read.sum + dram__bytes_write.sum of one
     # full-size launch of the step's x-gradient (1e6 x 1e6, 7 splits; a one-pass capture), with the hash
     # of the kernel sources it ran
-    "grad_kernel[D=3,E=1]": {"bytes_per_launch": 42504960 + 117179648, "source_hash": "7061d987e614fbba"},
+    "grad_kernel[D=3,E=1]": {"bytes_per_launch": 42504960 + 117179648, "source_hash": "90173c85c31abf92"},
 }
 
 

@@ -86,11 +86,13 @@ static const int64_t kTcChunkMax = (int64_t)3 << 16;     // points per tensor-pa
 static int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
 // Tensor-core plan: kTcRows rows per block (one TMEM lane each), tiles of kTcCols points
-// (the x-gradient: kTcGradCols), splits on tile boundaries, one block per SM.  Split
-// partials: M values (Sum, LSE) or M x D (the gradient) per split.
+// (the x-gradient: kTcGradCols; the K-min: kTcKnnRows rows, tiles of kTcKnnCols), splits on
+// tile boundaries, one block per SM.  Split partials: M values (Sum, LSE), M x D (the
+// gradient) or M lists (the K-min) per split.
 static void plan_tc(int op, int64_t M, int64_t N, int D, int EK, int num_sms, int blocks_per_sm, int forced_split,
                     kr_plan_t *p) {
-    const int tile = op == OP_GRAD ? kTcGradCols : kTcCols;
+    const int tile = op == OP_GRAD ? kTcGradCols : op == OP_KNN ? kTcKnnCols : kTcCols;
+    const int rows = op == OP_KNN ? kTcKnnRows : kTcRows;  // rows a block
     // split partials per row: (hi, lo) of the Sum / LSE; D of them for the gradient; a list of
     // KP (distance, index) for the K-min (the same bytes: 2 x 4 a slot)
     const int64_t width = op == OP_GRAD ? D : op == OP_KNN ? pad_k(EK) : 1;
@@ -99,7 +101,7 @@ static void plan_tc(int op, int64_t M, int64_t N, int D, int EK, int num_sms, in
     p->rows_per_thread = 1;
     p->threads = op == OP_GRAD ? kTcGradThreads : kTcThreads;
     p->tile_points = tile;
-    p->row_blocks = (M + kTcRows - 1) / kTcRows;
+    p->row_blocks = (M + rows - 1) / rows;
     p->path = KR_PATH_TENSOR_CORES;
     if (num_sms < 1) num_sms = 1;
     if (blocks_per_sm < 1) blocks_per_sm = 1;
@@ -136,7 +138,7 @@ static void plan_tc(int op, int64_t M, int64_t N, int D, int EK, int num_sms, in
     p->split = S;
     const int64_t n_pad = round_up(std::max<int64_t>(N, 1), kTcCols);
     // split fp16 operands (256 B a point), the padded signal / weights, the LSE tile frames
-    const int64_t operands = (round_up(std::max<int64_t>(M, 1), kTcRows) + n_pad) * 256 + n_pad * 4 +
+    const int64_t operands = (round_up(std::max<int64_t>(M, 1), rows) + n_pad) * 256 + n_pad * 4 +
                              round_up(n_pad / kTcCols * 4, 256);
     p->workspace_bytes = 256 + operands + (S > 1 ? 2 * (int64_t)S * M * width * (int64_t)sizeof(float) : 0) +
                          (op == OP_GRAD ? round_up((int64_t)S * M, 256) : 0) +  // the gradient's weak-row flags
@@ -485,7 +487,7 @@ static double kernel_prescale(int kind, float sigma) {
 static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in, char *ws, cudaStream_t stream) {
     const bool lse = op == OP_LSE, grad = op == OP_GRAD, knn = op == OP_KNN;
     const int64_t width = grad ? a.D : knn ? p.ek_pad : 1;  // split partials per row
-    const int64_t m_pad = round_up(a.M, kTcRows), n_pad = round_up(std::max<int64_t>(a.N, 1), kTcCols);
+    const int64_t m_pad = round_up(a.M, knn ? kTcKnnRows : kTcRows), n_pad = round_up(std::max<int64_t>(a.N, 1), kTcCols);
     unsigned *guard = (unsigned *)ws;
     __half *a_hi = (__half *)(ws + 256);
     __half *a_lo = a_hi + m_pad * 64;

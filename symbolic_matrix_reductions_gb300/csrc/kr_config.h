@@ -64,6 +64,10 @@ constexpr int kTcLseMaxD = 61;
 // second, P . [y' | 1]); same coordinate range as the Sum (the second product reads the
 // augmented B tile, whose slot D holds 1).
 constexpr int kTcGradCols = 128;
+// Tensor-core K-min screen: rows per block (two A tiles of kTcRows, each its own MMA M) and
+// points per tile (MMA N), so that every B tile read from L2 serves 256 rows.
+constexpr int kTcKnnRows = 256;
+constexpr int kTcKnnCols = 128;
 
 // Independent partial sums of a squared distance: at large D one fma chain over the
 // coordinates is a long dependency chain (4 cycles a link) with few rows per thread to

@@ -649,16 +649,25 @@ __device__ __forceinline__ void tmem_st32x32b_x16(uint32_t taddr, const uint32_t
 // rounding of the direct distance.  A list publishes its K-th (atomicMin on the word, as
 // float bits: non-negative floats order like unsigned integers) after a tile where it fell,
 // and reads the word once a tile: every list of a row whose split starts after another
-// split finished is screened by that split's K-th from its first tile on.  Evaluation warp
-// w owns rows 32 (w mod 4).. and the tile's columns 128 h.. (h = (w - 2) / 4): two lists a
-// row, merged at the end through shared memory.  A chunk of 64 columns holding no pass
-// costs one three-input max a column pair.  The B operand is only the high halves: a
-// stage is 32 KB and six of them are in flight.
+// split finished is screened by that split's K-th from its first tile on.
+// Block: 256 rows (two A tiles of 128, one MMA each, so that every B tile read from L2
+// serves 256 rows) against tiles of 128 points; TMEM holds two tiles' products (two
+// buffers of two 128-column accumulators).  Evaluation warp w owns rows 128 h + 32 q..
+// (q = w mod 4, h = (w - 2) / 4): its TMEM lanes 32 q.. of accumulator h, one list a row.
+// A chunk of 64 columns holding no pass costs one three-input max a column pair.  The
+// operands are only the high halves: a B stage is 16 KB and ten of them are in flight.
 // ---------------------------------------------------------------------------
-constexpr int kKStages = 6;
+constexpr int kKRows = kTcKnnRows;  // 2 x kRows
+constexpr int kKCols = kTcKnnCols;
+constexpr int kKBTileBytes = kKCols * 128;  // 128 points x 64 fp16
+constexpr int kKStages = 10;
 constexpr int kKChunk = 64;  // columns a TMEM load and a screen test
-static_assert(kATileBytes + kKStages * kBTileBytes + 1024 <= kSmemBytes, "K-min stages within the Sum's shared memory");
-static_assert(kEvalCols % kKChunk == 0, "whole chunks");
+static_assert(kKRows == 2 * kRows, "two A tiles a block");
+static_assert(2 * kATileBytes + kKStages * kKBTileBytes + 1024 <= kSmemBytes, "K-min stages within the Sum's shared memory");
+static_assert(kKCols % kKChunk == 0 && 4 * kKCols <= kTmemCols, "whole chunks; two buffers of two accumulators");
+static_assert(kEvalWarps == 8, "two warps a TMEM lane quarter");
+// M = 128, N = kKCols, both K-major
+constexpr uint32_t kIdescK = (1u << 4) | ((uint32_t)(kKCols >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 
 __device__ __forceinline__ bool knn_norms_ok(const unsigned *guard) {
     return __uint_as_float(guard[0]) + __uint_as_float(guard[1]) <= kTcKnnNormLimit;
@@ -703,19 +712,20 @@ __device__ __forceinline__ float knn_kth(const float (&dk)[KP], int K) {
 }
 
 // Direct fp32 squared distance between row i of x and point j of y (D coordinates each),
-// summed in coordinate order; eight loads at a time are in flight.
+// summed in coordinate order; G coordinates of each at a time are in flight.
+template <int G>
 __device__ __forceinline__ float tc_knn_dist(const float *xi, const float *yj, int D) {
     float q = 0.f;
     int d = 0;
-    for (; d + 8 <= D; d += 8) {
-        float a[8], b[8];
+    for (; d + G <= D; d += G) {
+        float a[G], b[G];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < G; ++e) {
             a[e] = __ldg(xi + d + e);
             b[e] = __ldg(yj + d + e);
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q = fmaf(a[e] - b[e], a[e] - b[e], q);
+        for (int e = 0; e < G; ++e) q = fmaf(a[e] - b[e], a[e] - b[e], q);
     }
     for (; d < D; ++d) {
         const float df = __ldg(xi + d) - __ldg(yj + d);
@@ -745,17 +755,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_cons
     if (!knn_norms_ok(p.guard)) return;  // the CUDA-core kernel does this call's work
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const uint32_t s_a = smem_addr(smem), s_stage0 = s_a + kATileBytes;
+    const uint32_t s_a = smem_addr(smem), s_stage0 = s_a + 2 * kATileBytes;
     const uint32_t b_a_full = smem_addr(&bars[0]);
     const uint32_t b_full0 = b_a_full + 8, b_empty0 = b_full0 + 8 * kKStages;
     const uint32_t b_accf0 = b_empty0 + 8 * kKStages, b_acce0 = b_accf0 + 16, b_drain = b_acce0 + 16;
     volatile int *abort = &abort_flag;
 
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
-    const int64_t row0 = (int64_t)blockIdx.x * kRows;
+    const int64_t row0 = (int64_t)blockIdx.x * kKRows;
     const int64_t j_begin = (int64_t)blockIdx.y * p.chunk;
     const int64_t j_end = min(p.N, j_begin + p.chunk);
-    const int T = j_end > j_begin ? (int)((j_end - j_begin + kCols - 1) / kCols) : 0;
+    const int T = j_end > j_begin ? (int)((j_end - j_begin + kKCols - 1) / kKCols) : 0;
 
     if (w == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_slot)),
@@ -781,6 +791,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_cons
     asm volatile("tcgen05.fence::after_thread_sync;");
     const uint32_t tmem = tmem_slot;
 
+    // evaluation warps 2..9: row i (one a lane) and its list
+    const int quarter = w & 3, h = (w - 2) >> 2;
+    const int64_t i = row0 + kRows * h + 32 * quarter + lane;
+    const bool live = w >= 2 && i < p.M;
     float dk[KP];
     int ik[KP];
 #pragma unroll
@@ -791,38 +805,44 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_cons
     if (w == 0) {
         // ---------------- TMA producer: the high halves only ----------------
         if (lane == 0 && T > 0) {
-            mbar_expect_tx(b_a_full, kATileBytes);
+            mbar_expect_tx(b_a_full, 2 * kATileBytes);
             tma_2d(s_a, &p.tm_a_hi, 0, (int)row0, b_a_full);
+            tma_2d(s_a + kATileBytes, &p.tm_a_hi, 0, (int)(row0 + kRows), b_a_full);
             int issued = 0;
-            for (int i = 0; i < T; ++i) {
-                const int s = i % kKStages;
-                if (i >= kKStages && !mbar_wait(b_empty0 + 8 * s, ((i / kKStages) - 1) & 1, abort, p.wait_ns)) break;
-                const int j0 = (int)(j_begin + (int64_t)i * kCols);
+            for (int n = 0; n < T; ++n) {
+                const int s = n % kKStages;
+                if (n >= kKStages && !mbar_wait(b_empty0 + 8 * s, ((n / kKStages) - 1) & 1, abort, p.wait_ns)) break;
+                const int j0 = (int)(j_begin + (int64_t)n * kKCols);
                 const uint32_t full = b_full0 + 8 * s;
                 if (p.starve) continue;  // test hook: no B tile ever arrives, so the MMA issuer's wait runs out
-                mbar_expect_tx(full, kBTileBytes);
-                tma_2d(s_stage0 + s * kBTileBytes, &p.tm_b_hi, 0, j0, full);
-                issued = i + 1;
+                mbar_expect_tx(full, kKBTileBytes);
+                tma_2d(s_stage0 + s * kKBTileBytes, &p.tm_b_hi, 0, j0, full);
+                issued = n + 1;
             }
             if (*abort) {
                 mbar_drain(b_a_full, 0, p.wait_ns);
-                for (int i = issued > kKStages ? issued - kKStages : 0; i < issued; ++i)
-                    mbar_drain(b_full0 + 8 * (i % kKStages), (i / kKStages) & 1, p.wait_ns);
+                for (int n = issued > kKStages ? issued - kKStages : 0; n < issued; ++n)
+                    mbar_drain(b_full0 + 8 * (n % kKStages), (n / kKStages) & 1, p.wait_ns);
             }
         }
     } else if (w == 1) {
-        // ---------------- MMA issuer: S = A_hi . B_hi^T, four K steps of 16 ----------------
+        // ---------------- MMA issuer: S_h = A_h . B^T (h = 0, 1), four K steps of 16 each ----
         if (lane == 0 && T > 0 && mbar_wait(b_a_full, 0, abort, p.wait_ns)) {
             bool issued = false;
-            for (int i = 0; i < T; ++i) {
-                const int s = i % kKStages, k = i & 1;
-                if (!mbar_wait(b_full0 + 8 * s, (i / kKStages) & 1, abort, p.wait_ns)) break;
-                if (i >= 2 && !mbar_wait(b_acce0 + 8 * k, ((i >> 1) - 1) & 1, abort, p.wait_ns)) break;
+            for (int n = 0; n < T; ++n) {
+                const int s = n % kKStages, k = n & 1;
+                if (!mbar_wait(b_full0 + 8 * s, (n / kKStages) & 1, abort, p.wait_ns)) break;
+                if (n >= 2 && !mbar_wait(b_acce0 + 8 * k, ((n >> 1) - 1) & 1, abort, p.wait_ns)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;");
-                const uint32_t acc = tmem + (uint32_t)(k * kCols);
-                const uint32_t bh = s_stage0 + s * kBTileBytes;
+                const uint32_t bh = s_stage0 + s * kKBTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) mma_f16(acc, desc_sw128(s_a + 32 * kk), desc_sw128(bh + 32 * kk), kk > 0);
+                for (int a = 0; a < 2; ++a) {
+                    const uint32_t acc = tmem + (uint32_t)((2 * k + a) * kKCols);
+                    const uint32_t ah = s_a + (uint32_t)(a * kATileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16(acc, desc_sw128(ah + 32 * kk), desc_sw128(bh + 32 * kk), kk > 0, kIdescK);
+                }
                 commit(b_empty0 + 8 * s);
                 commit(b_accf0 + 8 * k);
                 issued = true;
@@ -833,11 +853,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_cons
             }
         }
     } else {
-        // ---------------- evaluation warps 2..9 ----------------
-        const int quarter = w & 3, half = (w - 2) >> 2, c0 = kEvalCols * half;
+        // ---------------- evaluation warps 2..9: one row a lane, one list a row ----------------
         const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
-        const int64_t i = row0 + 32 * quarter + lane;
-        const bool live = i < p.M;
         const float *xi = p.x + (live ? i : 0) * p.D;
         unsigned *const kw = p.kth + (live ? i : 0);  // the row's shared K-th word
         // this row's |x|^2 (fp32) and the screen's margin
@@ -854,11 +871,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_cons
             const float gth = live ? __uint_as_float(__ldcg(kw)) : inf;
             if (!mbar_wait(b_accf0 + 8 * k, (it >> 1) & 1, abort, p.wait_ns)) break;
             asm volatile("tcgen05.fence::after_thread_sync;");
-            const int64_t jt = j_begin + (int64_t)it * kCols + c0;
+            const int64_t jt = j_begin + (int64_t)it * kKCols;
 #pragma unroll 1
-            for (int ch = 0; ch < kEvalCols / kKChunk; ++ch) {
+            for (int ch = 0; ch < kKCols / kKChunk; ++ch) {
                 uint32_t r[kKChunk];
-                tmem_ld32x32b_x64(tmem + lanes + (uint32_t)(k * kCols + c0 + kKChunk * ch), r);
+                tmem_ld32x32b_x64(tmem + lanes + (uint32_t)((2 * k + h) * kKCols + kKChunk * ch), r);
                 asm volatile("tcgen05.wait::ld.sync.aligned;");
                 // the chunk's largest S (nearest point): one test for 64 columns
                 float mx = __uint_as_float(r[0]);
@@ -875,7 +892,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_cons
                         if (m0) m0 &= m0 - 1; else m1 &= m1 - 1;
                         const int64_t j = jt + kKChunk * ch + c;
                         if (j >= j_end) break;  // the rest of the chunk is past the split too
-                        const float q = tc_knn_dist(xi, p.y + j * p.D, p.D);
+                        // (longer lists leave fewer registers for the loads in flight)
+                        const float q = tc_knn_dist<KP <= 16 ? 16 : 8>(xi, p.y + j * p.D, p.D);
                         if (q < kth) {
                             knn_insert<KP>(dk, ik, q, (int)j);
                             kth = knn_kth<KP>(dk, p.K);
@@ -899,45 +917,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_cons
         }
     }
 
+    asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
     const bool ok = !*abort;
     if (!ok && t == 0) atomicOr(&g_tc_status, 1u);
-    // the second half's lists to the first through the idle operand tiles (128 rows x KP (d, j))
-    float *xd = reinterpret_cast<float *>(smem);
-    int *xj = reinterpret_cast<int *>(smem) + kRows * KP;
-    const int rl = 32 * (w & 3) + lane;
-    if (w >= 6) {
-#pragma unroll
-        for (int k = 0; k < KP; ++k) {
-            xd[rl * KP + k] = dk[k];
-            xj[rl * KP + k] = ik[k];
-        }
-    }
-    asm volatile("tcgen05.fence::before_thread_sync;");
-    __syncthreads();
     if (w == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
-    if (w >= 2 && w < 6) {
-        const int64_t i = row0 + rl;
-        if (i < p.M) {
-            // merge: the second list's entries into this one by (d, j), so the first KP of the
-            // union in that order (the two halves' indices interleave tile by tile)
-#pragma unroll 1
-            for (int k = 0; k < KP; ++k) knn_insert_dj<KP>(dk, ik, xd[rl * KP + k], xj[rl * KP + k]);
-            const float nan = __int_as_float(0x7fc00000);
-            if (p.S == 1) {
+    if (live) {
+        const float nan = __int_as_float(0x7fc00000);
+        if (p.S == 1) {
 #pragma unroll
-                for (int k = 0; k < KP; ++k) {
-                    if (k >= p.K) continue;
-                    p.idx[i * p.K + k] = ok ? ik[k] : -1;
-                    if (p.out) p.out[i * p.K + k] = ok ? dk[k] : nan;
-                }
-            } else {
-                const int64_t o = ((int64_t)blockIdx.y * p.M + i) * KP;
+            for (int k = 0; k < KP; ++k) {
+                if (k >= p.K) continue;
+                p.idx[i * p.K + k] = ok ? ik[k] : -1;
+                if (p.out) p.out[i * p.K + k] = ok ? dk[k] : nan;
+            }
+        } else {
+            const int64_t o = ((int64_t)blockIdx.y * p.M + i) * KP;
 #pragma unroll
-                for (int k = 0; k < KP; ++k) {
-                    p.ws0[o + k] = ok ? dk[k] : nan;
-                    p.wsi[o + k] = ok ? ik[k] : -1;
-                }
+            for (int k = 0; k < KP; ++k) {
+                p.ws0[o + k] = ok ? dk[k] : nan;
+                p.wsi[o + k] = ok ? ik[k] : -1;
             }
         }
     }
@@ -1444,11 +1443,11 @@ cudaError_t tc_launch_grad(const TcArgs &a, dim3 grid, cudaStream_t s) {
 
 cudaError_t tc_launch_knn(const TcArgs &a, dim3 grid, cudaStream_t s) {
     TcParams p;
-    if (a.m_pad % kRows || a.n_pad % kCols || a.chunk % kCols || a.D < 32 || a.D > 62 || a.K < 1 || a.K > a.KP ||
-        !a.kth)
+    if (a.m_pad % kKRows || a.n_pad % kKCols || a.chunk % kKCols || a.D < 32 || a.D > 62 || a.K < 1 ||
+        a.K > a.KP || !a.kth)
         return cudaErrorInvalidValue;
-    // the screen reads the high halves only
-    if (!make_map(&p.tm_a_hi, a.a_hi, a.m_pad, kRows) || !make_map(&p.tm_b_hi, a.b_hi, a.n_pad, kCols))
+    // the screen reads the high halves only: A tiles of 128 rows, B tiles of 128 points
+    if (!make_map(&p.tm_a_hi, a.a_hi, a.m_pad, kRows) || !make_map(&p.tm_b_hi, a.b_hi, a.n_pad, kKCols))
         return cudaErrorInvalidValue;
     p.bpad = nullptr;
     p.fpad = nullptr;
