@@ -142,7 +142,7 @@ static void plan_tc(int op, int64_t M, int64_t N, int D, int EK, int num_sms, in
                              round_up(n_pad / kTcCols * 4, 256);
     p->workspace_bytes = 256 + operands + (S > 1 ? 2 * (int64_t)S * M * width * (int64_t)sizeof(float) : 0) +
                          (op == OP_GRAD ? round_up((int64_t)S * M, 256) : 0) +  // the gradient's weak-row flags
-                         (op == OP_KNN ? round_up(4 * M, 256) : 0);              // the K-min's shared K-th words
+                         (op == OP_KNN ? round_up(4 * M * width, 256) : 0);      // the K-min's shared lists
 }
 
 static int64_t batch_of(const kr_options *opt) { return opt && opt->batch > 1 ? opt->batch : 1; }
@@ -481,7 +481,7 @@ static double kernel_prescale(int kind, float sigma) {
 
 // ---- tensor-core Sum: operand prepass, tensor kernel, CUDA-core stand-in, combine -------
 // Workspace: [guard (2 x u32) + status | A_hi | A_lo | B_hi | B_lo | padded b | LSE frames |
-// partials | the gradient's flags or the K-min's K-th words].  The CUDA-core kernel is
+// partials | the gradient's flags or the K-min's shared lists].  The CUDA-core kernel is
 // always launched after the tensor kernel with the same splits; it returns at once unless
 // the prepass found norms the expansion cannot serve.
 static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in, char *ws, cudaStream_t stream) {
@@ -496,14 +496,15 @@ static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in
     float *bpad = (float *)(b_lo + n_pad * 64);
     float *fpad = bpad + n_pad;
     float *part = (float *)((char *)fpad + round_up(n_pad / kTcCols * 4, 256));
-    // the x-gradient's flags (S x M bytes), or the K-min's K-th words (M), follow the split partials
+    // the x-gradient's flags (S x M bytes), or the K-min's shared lists (M x KP), follow the
+    // split partials
     uint8_t *flags = (uint8_t *)(part + (p.split > 1 ? 2 * (int64_t)p.split * a.M * width : 0));
-    unsigned *kth = knn ? (unsigned *)flags : nullptr;
+    float *carry = knn ? (float *)flags : nullptr;
     cudaError_t ce = cudaMemsetAsync(guard, 0, 256, stream);
     // (the K-min's screen reads the operands' high halves only)
     if (ce == cudaSuccess)
         ce = tc_launch_prep(a.x, a.M, m_pad, a.D, a.c, true, lse, a_hi, knn ? nullptr : a_lo, guard, nullptr, nullptr,
-                            nullptr, stream, false, kth);
+                            nullptr, stream, false, carry, knn ? (int)width : 0);
     if (ce == cudaSuccess && grad) ce = tc_launch_bmax(a.b, a.N, guard, stream);
     if (ce == cudaSuccess)
         ce = tc_launch_prep(a.y, a.N, n_pad, a.D, a.c, false, lse, b_hi, knn ? nullptr : b_lo, guard + 1,
@@ -553,7 +554,7 @@ static cudaError_t run_tc(int op, Args a, const kr_plan_t &p, const Instance &in
         t.wsi = a.wsi;
         t.K = a.K;
         t.KP = p.ek_pad;
-        t.kth = kth;
+        t.carry = carry;
         const dim3 tgrid((unsigned)p.row_blocks, (unsigned)p.split);
         ce = grad ? tc_launch_grad(t, tgrid, stream) : knn ? tc_launch_knn(t, tgrid, stream) : tc_launch_sum(t, tgrid, stream);
     }

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(256) tc_bmax_kernel(const float *b, int64_t n,
 __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t rows, int64_t rows_pad, int D,
                                                       float c, int is_x, int lse, __half *hi, __half *lo,
                                                       unsigned *guard, const float *b, float *bpad, float *fpad,
-                                                      const unsigned *bmax, unsigned *kth) {
+                                                      const unsigned *bmax, float *carry, int carry_w) {
     __shared__ float wmax[8];
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= rows_pad) return;  // with fpad, rows_pad is a multiple of 256: whole blocks leave together
@@ -292,7 +292,8 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float *src, int64_t 
             n = fmaf(s, s, n);
         }
         atomicMax(guard, __float_as_uint(n));
-        if (kth) kth[r] = 0x7f800000u;  // K-min: no K-th distance published for the row yet
+        if (carry)  // K-min: no list published for the row yet
+            for (int k = 0; k < carry_w; ++k) carry[r * carry_w + k] = __int_as_float(0x7f800000);
     }
     if (bpad && !fpad && bmax) {
         const float m = __uint_as_float(*bmax);
@@ -639,17 +640,24 @@ __device__ __forceinline__ void tmem_st32x32b_x16(uint32_t taddr, const uint32_t
 // part: an operand below fp16's normal range (under 2^-14; the tensor cores keep fp16
 // subnormals) is rounded to a multiple of 2^-24, within 2^-25, and meets the other
 // operand's entries (sum over d of |y_d| + 2 |x_d| + 2 <= 1.5 D + |x|^2 + |y|^2 + 2).
-// A point passes when -S_ij is at most T + margin, where T is the smallest K-th distance
-// found so far among all lists of row i: this list's own K-th, or one another list (the
-// other half of the tile's columns, another split) published in the per-row word kth[i].
-// The final K-th distance of the row is at most T, so no point of the row's final K fails
-// the screen.  Passing points get the direct fp32 distance (sum over d of (x_d - y_d)^2,
-// in order) and enter the row's sorted list when strictly below its K-th, in increasing j,
-// so equal distances keep the lower index; the lists are the CUDA-core kernel's up to the
-// rounding of the direct distance.  A list publishes its K-th (atomicMin on the word, as
-// float bits: non-negative floats order like unsigned integers) after a tile where it fell,
-// and reads the word once a tile: every list of a row whose split starts after another
-// split finished is screened by that split's K-th from its first tile on.
+// A point passes when -S_ij is at most T + margin, where T is the K-th distance of the row's
+// list: this block's own, which starts from the best list any block of the row has shared
+// (the row's shared list: distances only, in the workspace).  Its entries enter as stand-ins,
+// which rank after any point of equal distance and are never reported.  Why no point of
+// the row's final K fails the screen or is displaced: the shared lists hold distances of
+// real points of other blocks, sorted, so slot k of one (even one read while another block
+// rewrites it, slot by slot) is at least the k-th smallest distance of all the row's other
+// points; hence slot k of this list is at least the k-th smallest of all the row's points,
+// and a point of this split that the list turns away (or pushes past slot K - 1) has K
+// points of the row ranking before it.  A block reads the shared list whole only at its
+// start (so it never holds its own points), afterwards only its K-th slot as a bound, and
+// writes its own list there after a tile where it became better than the shared one.
+// Passing points get the direct fp32 distance (sum over d of (x_d - y_d)^2, in order) and
+// enter the list when they rank before its K-th entry, in increasing j, so equal distances
+// keep the lower index; the lists are the CUDA-core kernel's up to the rounding of the
+// direct distance.  Chained this way, the splits of a row together take about the
+// candidates of one list over all N points, K (1 + ln(N / K)), where lists that each started
+// empty would take K ln(N_split / K) apiece.
 // Block: 256 rows (two A tiles of 128, one MMA each, so that every B tile read from L2
 // serves 256 rows) against tiles of 128 points; TMEM holds two tiles' products (two
 // buffers of two 128-column accumulators).  Evaluation warp w owns rows 128 h + 32 q..
@@ -696,9 +704,9 @@ __device__ __forceinline__ void knn_insert_dj(float (&dk)[KP], int (&ik)[KP], fl
     }
 }
 
-// dk[K - 1] with constant indices only, 1 <= K <= KP.  Each slot passes through an empty asm
-// so that the selects are not folded back into an indexed load, which would move the list
-// from registers to local memory.
+// dk[K - 1] (ik[K - 1]) with constant indices only, 1 <= K <= KP.  Each slot passes through
+// an empty asm so that the selects are not folded back into an indexed load, which would move
+// the list from registers to local memory.
 template <int KP>
 __device__ __forceinline__ float knn_kth(const float (&dk)[KP], int K) {
     float v = dk[0];
@@ -710,6 +718,21 @@ __device__ __forceinline__ float knn_kth(const float (&dk)[KP], int K) {
     }
     return v;
 }
+template <int KP>
+__device__ __forceinline__ int knn_kth(const int (&ik)[KP], int K) {
+    int v = ik[0];
+#pragma unroll
+    for (int k = 1; k < KP; ++k) {
+        int c = ik[k];
+        asm("" : "+r"(c));
+        v = k == K - 1 ? c : v;
+    }
+    return v;
+}
+
+// Index of a stand-in entry: a distance taken from the row's shared list, which ranks after
+// every point of equal distance and is never reported.
+constexpr int kKnnStandIn = 0x7fffffff;
 
 // Direct fp32 squared distance between row i of x and point j of y (D coordinates each),
 // summed in coordinate order; G coordinates of each at a time are in flight.
@@ -856,20 +879,30 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_cons
         // ---------------- evaluation warps 2..9: one row a lane, one list a row ----------------
         const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
         const float *xi = p.x + (live ? i : 0) * p.D;
-        unsigned *const kw = p.kth + (live ? i : 0);  // the row's shared K-th word
+        float *const cl = p.carry + (live ? i : 0) * KP;  // the row's shared list
         // this row's |x|^2 (fp32) and the screen's margin
         float nx = 0.f;
         for (int d = 0; d < p.D; ++d) nx = fmaf(__ldg(xi + d), __ldg(xi + d), nx);
         const float margin = 0x1p-8f * (nx + __uint_as_float(p.guard[1])) + 0x1p-24f * (float)(p.D + 2);
         const float inf = __int_as_float(0x7f800000);
-        float kth = inf;  // this list's K-th distance
-        float pub = inf;  // the K-th it last published
-        float thr = inf;  // -S must be at most this to pass
+        // the list starts from the row's shared one: its distances enter as stand-ins (index
+        // kKnnStandIn), which rank after every point of equal distance and are never reported
+        if (live) {
+#pragma unroll
+            for (int k = 0; k < KP; ++k) {
+                const float v = __ldcg(cl + k);
+                if (v < inf) knn_insert_dj<KP>(dk, ik, v, kKnnStandIn);
+            }
+        }
+        float kth = knn_kth<KP>(dk, p.K);  // this list's K-th distance
+        float pub = kth;                    // the K-th it last published (or started from)
+        float thr = kth + margin;           // -S must be at most this to pass
         for (int it = 0; it < T; ++it) {
             const int k = it & 1;
-            // the row's smallest published K-th so far (read before the wait: it is in flight meanwhile)
-            const float gth = live ? __uint_as_float(__ldcg(kw)) : inf;
-            if (!mbar_wait(b_accf0 + 8 * k, (it >> 1) & 1, abort, p.wait_ns)) break;
+            // the row's shared K-th (read before the wait: it is in flight meanwhile)
+            const float gth = live ? __ldcg(cl + (p.K - 1)) : inf;
+            // (the warp leaves together)
+            if (!__all_sync(0xffffffffu, mbar_wait(b_accf0 + 8 * k, (it >> 1) & 1, abort, p.wait_ns))) break;
             asm volatile("tcgen05.fence::after_thread_sync;");
             const int64_t jt = j_begin + (int64_t)it * kKCols;
 #pragma unroll 1
@@ -894,8 +927,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_cons
                         if (j >= j_end) break;  // the rest of the chunk is past the split too
                         // (longer lists leave fewer registers for the loads in flight)
                         const float q = tc_knn_dist<KP <= 16 ? 16 : 8>(xi, p.y + j * p.D, p.D);
-                        if (q < kth) {
-                            knn_insert<KP>(dk, ik, q, (int)j);
+                        // (q, j) enters when it ranks before the K-th entry: a smaller distance,
+                        // or an equal one held by a stand-in (the list's own points have lower j)
+                        if (q < kth || (q == kth && knn_kth<KP>(ik, p.K) == kKnnStandIn)) {
+                            knn_insert_dj<KP>(dk, ik, q, (int)j);
                             kth = knn_kth<KP>(dk, p.K);
                             thr = fminf(kth, gth) + margin;
                             uint32_t n0, n1;
@@ -909,8 +944,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_cons
             asm volatile("tcgen05.fence::before_thread_sync;");
             __syncwarp();
             if (lane == 0) mbar_arrive(b_acce0 + 8 * k);  // the MMAs of tile it+2 may overwrite it
-            if (kth < pub) {  // publish the list's new K-th to the row's other lists
-                atomicMin(kw, __float_as_uint(kth));
+            if (live && kth < pub && kth < gth) {  // a better list than the row's: share it
+#pragma unroll
+                for (int e = 0; e < KP; ++e) __stcg(cl + e, dk[e]);
                 pub = kth;
             }
             thr = fminf(kth, gth) + margin;
@@ -923,21 +959,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_knn_kernel(const __grid_cons
     if (!ok && t == 0) atomicOr(&g_tc_status, 1u);
     if (w == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
     if (live) {
-        const float nan = __int_as_float(0x7fc00000);
-        if (p.S == 1) {
+        // the list's own points in order (the stand-ins left out), then empty slots
+        const float nan = __int_as_float(0x7fc00000), inf = __int_as_float(0x7f800000);
+        const int width = p.S == 1 ? p.K : KP;
+        const int64_t o = p.S == 1 ? i * p.K : ((int64_t)blockIdx.y * p.M + i) * KP;
+        int32_t *const oi = (p.S == 1 ? p.idx : p.wsi) + o;
+        float *const od = p.S == 1 ? (p.out ? p.out + o : nullptr) : p.ws0 + o;  // (the distances may be left out)
+        int n = 0;
 #pragma unroll
-            for (int k = 0; k < KP; ++k) {
-                if (k >= p.K) continue;
-                p.idx[i * p.K + k] = ok ? ik[k] : -1;
-                if (p.out) p.out[i * p.K + k] = ok ? dk[k] : nan;
-            }
-        } else {
-            const int64_t o = ((int64_t)blockIdx.y * p.M + i) * KP;
-#pragma unroll
-            for (int k = 0; k < KP; ++k) {
-                p.ws0[o + k] = ok ? dk[k] : nan;
-                p.wsi[o + k] = ok ? ik[k] : -1;
-            }
+        for (int k = 0; k < KP; ++k) {
+            if (k >= p.K || ik[k] < 0 || ik[k] == kKnnStandIn) continue;
+            oi[n] = ok ? ik[k] : -1;
+            if (od) od[n] = ok ? dk[k] : nan;
+            ++n;
+        }
+        for (; n < width; ++n) {
+            oi[n] = -1;
+            if (od) od[n] = ok ? inf : nan;
         }
     }
 }
@@ -1373,14 +1411,14 @@ cudaError_t tc_launch_bmax(const float *b, int64_t n, unsigned *guard, cudaStrea
 
 cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x, bool lse,
                            __half *hi, __half *lo, unsigned *guard, const float *b, float *bpad, float *fpad,
-                           cudaStream_t s, bool natural_b, unsigned *kth) {
+                           cudaStream_t s, bool natural_b, float *carry, int carry_w) {
     // LSE frames: a prep block of 256 threads is one whole tile of kTcCols = 256 points
     if (fpad && rows_pad % 256) return cudaErrorInvalidValue;
     if (lse && (D + 2 >= 64 || (!is_x && !fpad))) return cudaErrorInvalidValue;
     const unsigned blocks = (unsigned)((rows_pad + 255) / 256);
     // the y side's guard slot is guard[1] of the call's guard words; the largest |b| is guard[2]
     tc_prep_kernel<<<blocks, 256, 0, s>>>(src, rows, rows_pad, D, c, is_x ? 1 : 0, lse ? 1 : 0, hi, lo, guard, b,
-                                          bpad, fpad, natural_b ? guard + 1 : nullptr, kth);
+                                          bpad, fpad, natural_b ? guard + 1 : nullptr, carry, carry_w);
     return cudaGetLastError();
 }
 
@@ -1444,7 +1482,7 @@ cudaError_t tc_launch_grad(const TcArgs &a, dim3 grid, cudaStream_t s) {
 cudaError_t tc_launch_knn(const TcArgs &a, dim3 grid, cudaStream_t s) {
     TcParams p;
     if (a.m_pad % kKRows || a.n_pad % kKCols || a.chunk % kKCols || a.D < 32 || a.D > 62 || a.K < 1 ||
-        a.K > a.KP || !a.kth)
+        a.K > a.KP || !a.carry)
         return cudaErrorInvalidValue;
     // the screen reads the high halves only: A tiles of 128 rows, B tiles of 128 points
     if (!make_map(&p.tm_a_hi, a.a_hi, a.m_pad, kRows) || !make_map(&p.tm_b_hi, a.b_hi, a.n_pad, kKCols))
@@ -1471,7 +1509,7 @@ cudaError_t tc_launch_knn(const TcArgs &a, dim3 grid, cudaStream_t s) {
     p.idx = a.idx;
     p.wsi = a.wsi;
     p.K = a.K;
-    p.kth = a.kth;
+    p.carry = a.carry;
     cudaError_t e = tc_set_attributes();
     if (e != cudaSuccess) return e;
     switch (a.KP) {

@@ -38,12 +38,12 @@ struct TcArgs {
     uint8_t *flags;  // x-gradient: S x M, 1 where the CUDA-core kernel must redo (split, row)
     // K-min (tc_launch_knn): y (N x D fp32) for the direct distances, K, the index output
     // (M x K; out: the distances, or null) and, with S > 1, the index partials (ws0: distances),
-    // S x M x KP each; kth: M words, the smallest K-th distance any list of the row has
-    // published (float bits; the x prepass sets them to +inf)
+    // S x M x KP each; carry: M x KP, per row the distances of the best list any block of
+    // the row has published (the x prepass sets them to +inf)
     const float *y;
     int32_t *idx, *wsi;
     int K, KP;
-    unsigned *kth;
+    float *carry;
 };
 
 // Kernel parameters: TMA descriptors of the four operand arrays plus the rest.
@@ -63,7 +63,7 @@ struct TcParams {
     const float *y;  // K-min only
     int32_t *idx, *wsi;
     int K;
-    unsigned *kth;
+    float *carry;
 };
 
 int tc_smem_bytes();
@@ -73,10 +73,11 @@ bool tc_available();  // the driver offers cuTensorMapEncodeTiled
 // log-weight relative to its tile's frame, which fpad receives; b holds the log-weights).
 // Otherwise bpad receives b padded with zeros.
 // natural_b: bpad in point order (the x-gradient) rather than the Sum's evaluation order.
-// lo null: only the high halves are written.  kth non-null: kth[r] = +inf bits for r < rows.
+// lo null: only the high halves are written.  carry non-null: carry[r * carry_w + k] = +inf
+// for r < rows, k < carry_w.
 cudaError_t tc_launch_prep(const float *src, int64_t rows, int64_t rows_pad, int D, float c, bool is_x, bool lse,
                            __half *hi, __half *lo, unsigned *guard, const float *b, float *bpad, float *fpad,
-                           cudaStream_t s, bool natural_b = false, unsigned *kth = nullptr);
+                           cudaStream_t s, bool natural_b = false, float *carry = nullptr, int carry_w = 0);
 // x-gradient: guard[2] receives the largest |b| (float bits), from which the prepass of the
 // y side scales bpad by a power of two into [-1, 1] (run before that prepass).
 cudaError_t tc_launch_bmax(const float *b, int64_t n, unsigned *guard, cudaStream_t s);

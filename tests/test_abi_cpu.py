@@ -302,17 +302,17 @@ def test_knn_instances(lib, D, K, rows, tile):
 def test_knn_tensor_core_plan(lib):
     """K-min at 32 <= D <= 62 with K <= 32 plans the tensor-core screen: 256 rows a block,
     128-point tiles, the list padded as on the CUDA cores, split lists of KP (distance, index)
-    and the rows' shared K-th words in the workspace; other D, longer lists and batches stay
+    and the rows' shared lists in the workspace; other D, longer lists and batches stay
     on the CUDA cores."""
     p = kr.plan(kr.OP_KNN, 100_000, 1_000_000, 50, 10, num_sms=152, blocks_per_sm=1)
     assert p.path == kr.KR_PATH_TENSOR_CORES and (p.tile_points, p.threads, p.ek_pad) == (128, 320, 10)
     assert p.row_blocks == (100_000 + 255) // 256 and p.chunk % 128 == 0
     # operands as for the Sum (x padded to whole blocks of 256 rows), S x M lists of 10
-    # (distance, index), one K-th word a row
+    # (distance, index), one shared list of 10 distances a row
     n_pad = (1_000_000 + 255) // 256 * 256
     ops = ((100_000 + 255) // 256 * 256 + n_pad) * 256 + n_pad * 4 + (n_pad // 256 * 4 + 255) // 256 * 256
     lists = 2 * p.split * 100_000 * 10 * 4 if p.split > 1 else 0
-    assert p.workspace_bytes == 256 + ops + lists + (4 * 100_000 + 255) // 256 * 256
+    assert p.workspace_bytes == 256 + ops + lists + (4 * 100_000 * 10 + 255) // 256 * 256
     for D in (32, 62):
         assert kr.plan(kr.OP_KNN, 1000, 5000, D, 4).path == kr.KR_PATH_TENSOR_CORES
     assert kr.plan(kr.OP_KNN, 1000, 5000, 50, 32).ek_pad == 32

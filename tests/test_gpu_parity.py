@@ -571,3 +571,21 @@ def test_tensor_core_knn_scales(orc, scale):
         idx, dist = kr.kernel_knn(*_dev(x, y), K, split=split)
         i_ref, d_ref, n_ref = orc.knn(x, y, K)
         check_knn(_np(idx), _np(dist), x, y, i_ref, d_ref, n_ref, f"tc knn scale {scale} S{split}")
+
+
+@pytest.mark.parametrize("K,split", [(32, 8), (10, 0), (1, 5)])
+def test_tensor_core_knn_shared_lists_ties(orc, K, split):
+    """Every point duplicated hundreds of times across many splits: the splits' lists start
+    from the row's shared list (stand-ins of other splits' distances), so exact ties between
+    a stand-in and a point of the split decide which index is reported; the lowest must win."""
+    r = _rng(77 + K + split)
+    base = (r.standard_normal((50, 62)) / 8).astype(np.float32)
+    y = base[r.integers(0, 50, size=40_000)]
+    x = (base[r.integers(0, 50, size=600)] + 0.01 * r.standard_normal((600, 62))).astype(np.float32)
+    idx, dist = kr.kernel_knn(*_dev(x, y), K, split=split)
+    i_ref, d_ref, n_ref = orc.knn(x, y, K)
+    check_knn(_np(idx), _np(dist), x, y, i_ref, d_ref, n_ref, f"tc knn shared-list ties K{K} S{split}")
+    # the lowest index among the duplicates of the nearest centre, exactly
+    near = np.argmin(((x[:, None, :].astype(np.float64) - base[None].astype(np.float64)) ** 2).sum(-1), axis=1)
+    first = {c: int(np.flatnonzero((y == base[c]).all(1))[0]) for c in set(near.tolist())}
+    assert all(int(_np(idx)[i, 0]) == first[near[i]] for i in range(600))
