@@ -8,7 +8,8 @@ the LogSumExp (w = log b as log-weights), the x-gradient (upstream g ~ N(0,1)) a
 the K-min (K = 10), each through the C ABI; split-j runs whenever the planner picks
 it.  The metric is pair-evaluations per second, M*N per reduction, over the step.
 The D = 50 line (key "d50") is the tall kernel-vector product falkon_d50 (M = 10^5,
-N = 10^7, split-j, tensor cores), measured with the same protocol.
+N = 10^7, split-j, tensor cores), measured with the same protocol, with the LogSumExp,
+the x-gradient and the K-min of the same clouds beside it.
 
 Prints ONE JSON line (rank 0).  Timing: W warm-up steps, then K steps, each bracketed
 by CUDA events on the launching stream; L2 is flushed (a 256 MB write) before every
@@ -204,6 +205,7 @@ def probe_pipes(torch, nsm):
 # product P.[y' | 1] of the same width (three split products, N = 64): twice the FLOP.
 TC_FLOP_PER_PAIR = 3 * 2 * 64
 TC_GRAD_FLOP_PER_PAIR = 2 * TC_FLOP_PER_PAIR
+TC_KNN_FLOP_PER_PAIR = 2 * 64  # the K-min's screen: one fp16 product of the high halves
 
 
 def tensor_peak_tflops():
@@ -576,27 +578,32 @@ def measure_d50(torch, kr, W, nsm, max_mhz, xu_lanes, dev, args):
     a = torch.empty((M, 1), device=dev)
     L = torch.empty((M, 1), device=dev)
     gx = torch.empty((M, D), device=dev)
+    idx = torch.empty((M, K_NN), dtype=torch.int32, device=dev)
+    dist = torch.empty((M, K_NN), device=dev)
     out = {"workload": f"{D50}: {W.WORKLOADS[D50].note}", "M": M, "N": N, "D": D, "E": 1, "sigma": s,
            "metric": METRIC, "unit": UNIT,
-           "note": "value = the tall kernel-vector product (the Sum); the LogSumExp (b as log-weights) and the "
-                   "x-gradient (g ~ N(0,1)) of the same clouds beside it"}
+           "note": "value = the tall kernel-vector product (the Sum); the LogSumExp (b as log-weights), the "
+                   f"x-gradient (g ~ N(0,1)) and the K-min (K = {K_NN}) of the same clouds beside it"}
     calls = {"sum": (kr.OP_SUM, lambda: kr.kernel_reduce(x, y, b, s, "sum", out=a)),
              "lse": (kr.OP_LSE, lambda: kr.kernel_reduce(x, y, b, s, "lse", out=L)),
-             "grad": (kr.OP_GRAD, lambda: kr.kernel_reduce_grad_x(x, y, b, g, s, out=gx))}
+             "grad": (kr.OP_GRAD, lambda: kr.kernel_reduce_grad_x(x, y, b, g, s, out=gx)),
+             "knn": (kr.OP_KNN, lambda: kr.kernel_knn(x, y, K_NN, idx=idx, dist=dist))}
+    flop = {"sum": TC_FLOP_PER_PAIR, "lse": TC_FLOP_PER_PAIR, "grad": TC_GRAD_FLOP_PER_PAIR,
+            "knn": TC_KNN_FLOP_PER_PAIR}
     for op, (code, fn) in calls.items():
-        p = kr.plan_device(code, M, N, D, 1)
-        ms, how = _median_ms(torch, fn, warm=3, runs=10 if op != "grad" else 5)
+        p = kr.plan_device(code, M, N, D, K_NN if op == "knn" else 1)
+        ms, how = _median_ms(torch, fn, warm=3, runs=10 if op not in ("grad", "knn") else 5)
         rl = roofline(op, D, 1, ms / 1e3, M * N, nsm, max_mhz, xu_lanes, f"{op}[D={D},E=1] (CUDA-core count)")
         if p.path == kr.KR_PATH_TENSOR_CORES:
-            rl = roofline_tensor(ms / 1e3, M * N, f"tc_{op}_kernel (tcgen05)", rl,
-                                 TC_GRAD_FLOP_PER_PAIR if op == "grad" else TC_FLOP_PER_PAIR)
+            rl = roofline_tensor(ms / 1e3, M * N, f"tc_{op}_kernel (tcgen05)", rl, flop[op])
         out[op] = {"value": M * N / (ms / 1e3), "ms": ms, "timing": how, "split": p.split,
                    "path": "tensor cores" if p.path == kr.KR_PATH_TENSOR_CORES else "cuda cores",
                    "gpu_launches_per_call": launches_of(kr, p, op), "roofline": rl}
     out["value"] = out["sum"]["value"]
     out["roofline"] = out["sum"]["roofline"]
     a_dev, L_dev, gx_dev = a.cpu().numpy(), L.cpu().numpy(), gx.cpu().numpy()
-    del x, y, g, gx
+    idx_dev, dist_dev = idx.cpu().numpy(), dist.cpu().numpy()
+    del x, y, g, gx, idx, dist
     torch.cuda.empty_cache()
     # e2e: the product through the C ABI with pinned host buffers (inputs up, result down)
     xc, yc, bc = (torch.from_numpy(inp[k]).pin_memory() for k in ("x", "y", "b"))
@@ -629,14 +636,24 @@ def measure_d50(torch, kr, W, nsm, max_mhz, xu_lanes, dev, args):
                            "sample": f"seeded subset of {r} rows of {D50}, full N={N}: the Sum in fp64, {t:.1f} s"}
     L_ref = orc.gauss_lse(inp["x"][rows[:64]], inp["y"], inp["b"], s)
     g_ref, G_ref = orc.gauss_grad_x(inp["x"][rows[:32]], inp["y"], inp["b"], inp["g"][rows[:32]], s)
+    i_ref, d_ref, n_ref = orc.knn(inp["x"][rows[:32]], inp["y"], K_NN)
     sum_err = float(np.max(np.abs(a_dev[rows] - a_ref) / np.maximum(S_ref, 1e-300)))
     lse_err = np.abs(L_dev[rows[:64]] - L_ref)
     grad_err = float(np.max(np.abs(gx_dev[rows[:32]] - g_ref) / np.maximum(G_ref, 1e-300)))
+    ext = np.concatenate([np.full((32, 1), -np.inf), d_ref, n_ref[:, None]], axis=1)
+    cur = ext[:, 1:-1]
+    with np.errstate(invalid="ignore"):
+        sep = ((cur - ext[:, :-2]) > 1e-5 * np.abs(cur)) & ((ext[:, 2:] - cur) > 1e-5 * np.abs(cur))
+    mism = int(np.sum(sep & (idx_dev[rows[:32]].astype(np.int64) != i_ref)))
+    knn_dist_err = float(np.max(np.abs(dist_dev[rows[:32]] - d_ref) / np.maximum(np.abs(d_ref), 1e-30)))
     out["parity"] = {"rows": r, "sum_err_over_S": sum_err, "lse_rows": 64, "lse_abs_err": float(np.max(lse_err)),
                      "grad_rows": 32, "grad_err_over_G": grad_err,
+                     "knn_rows": 32, "knn_separated_mismatches": mism, "knn_near_ties": int(np.sum(~sep)),
+                     "knn_dist_rel_err": knn_dist_err,
                      "ok": bool(sum_err <= 1e-4 and np.all(lse_err <= 1e-4 + 2.0 ** -20 * np.abs(L_ref))
-                                and grad_err <= 1e-4),
-                     "tolerances": "Sum 1e-4 S; LSE 1e-4 + 2^-20 |L|; grad 1e-4 G"}
+                                and grad_err <= 1e-4 and mism == 0),
+                     "tolerances": "Sum 1e-4 S; LSE 1e-4 + 2^-20 |L|; grad 1e-4 G; "
+                                   "K-min indices exact where separated"}
     return out
 
 

@@ -291,6 +291,14 @@ def test_workload_falkon_d50(orc):
     gx_ref, G_ref = orc.gauss_grad_x(inp["x"][rows], inp["y"], inp["b"], inp["g"][rows], s)
     worst = check_grad(gx[rows], gx_ref, G_ref, "falkon_d50 grad")
     print(f"falkon_d50 grad, {rows.size} rows: err/G {worst:.2e}")
+    # the K-min (K = 10) of the same clouds: the tensor-core screen, its splits chained
+    # through the rows' shared lists
+    assert kr.plan_device(kr.OP_KNN, inp["x"].shape[0], inp["y"].shape[0], 50, 10).path == kr.KR_PATH_TENSOR_CORES
+    idx, dist = (_np(v) for v in kr.kernel_knn(xt, yt, 10))
+    rows = W.row_subset(inp["x"].shape[0], 64, 13)
+    i_ref, d_ref, n_ref = orc.knn(inp["x"][rows], inp["y"], 10)
+    ties = check_knn(idx[rows], dist[rows], inp["x"][rows], inp["y"], i_ref, d_ref, n_ref, "falkon_d50 knn")
+    print(f"falkon_d50 knn, {rows.size} rows: {ties} near-tie positions")
 
 
 def test_workload_knn_d16(orc):
