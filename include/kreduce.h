@@ -123,8 +123,8 @@ typedef enum {
                                  max |y'|^2 exceeds 16 (x' = x sqrt(log2 e)/sigma), where the
                                  expansion's rounding would exceed the tolerance.  The
                                  K-min (32 <= D <= 62, K <= 32, no batch) screens its pairs
-                                 with the same expansion and stands down when max |x|^2 +
-                                 max |y|^2 exceeds 4096. */
+                                 with one fp16 product of the expansion's high halves and
+                                 stands down when max |x|^2 + max |y|^2 exceeds 4096. */
 } kr_path;
 
 /*
