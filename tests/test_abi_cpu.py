@@ -313,6 +313,18 @@ def test_knn_tensor_core_plan(lib):
     ops = ((100_000 + 255) // 256 * 256 + n_pad) * 256 + n_pad * 4 + (n_pad // 256 * 4 + 255) // 256 * 256
     lists = 2 * p.split * 100_000 * 10 * 4 if p.split > 1 else 0
     assert p.workspace_bytes == 256 + ops + lists + (4 * 100_000 * 10 + 255) // 256 * 256
+    # any shape, automatic or forced splits: whole 128-point tiles, every split nonempty, the
+    # same workspace formula (the list width padded as on the CUDA cores: K 32 -> 32)
+    for M, N, D, K, forced in ((1, 1, 50, 1, 0), (300, 3000, 50, 10, 0), (300, 3000, 50, 10, 7),
+                               (513, 2000, 62, 32, 0), (100_000, 10_000_000, 50, 10, 0)):
+        q = kr.plan(kr.OP_KNN, M, N, D, K, num_sms=152, blocks_per_sm=1, split=forced)
+        assert q.path == kr.KR_PATH_TENSOR_CORES and q.chunk % 128 == 0
+        assert (q.split - 1) * q.chunk < N <= q.split * q.chunk
+        assert q.row_blocks == (M + 255) // 256
+        n_pad = (N + 255) // 256 * 256
+        ops = ((M + 255) // 256 * 256 + n_pad) * 256 + n_pad * 4 + (n_pad // 256 * 4 + 255) // 256 * 256
+        lists = 2 * q.split * M * q.ek_pad * 4 if q.split > 1 else 0
+        assert q.workspace_bytes == 256 + ops + lists + (4 * M * q.ek_pad + 255) // 256 * 256, (M, N, K)
     for D in (32, 62):
         assert kr.plan(kr.OP_KNN, 1000, 5000, D, 4).path == kr.KR_PATH_TENSOR_CORES
     assert kr.plan(kr.OP_KNN, 1000, 5000, 50, 32).ek_pad == 32
